@@ -1,0 +1,430 @@
+"""Benchmark of the shared paged KV decode step on GB300.
+
+Workload (the configuration the headline metric is quoted on): 8 agents x
+16384-token contexts, 32 query heads = 32 KV heads, head_dim 128, 16-token
+blocks, 60 % common prefix stored once (614 shared + 8 x 410 private blocks
+per layer), 32 layers, bf16 values ~N(0,1), one decode query per agent.
+
+One step = the whole hot path on that batch: GPU block fingerprints + dedup
+of the 8 token sequences (block tables, refcounts), then decode attention on
+all 32 layers through the deduplicated pool.  value = decode tokens/s =
+agents / step time.  KV of one step is 32.7 GB, far above L2, so no flush is
+needed between steps.
+
+Also reported: KV GB/s (unique bytes / step time), the attention kernel's
+roofline (algorithmic bytes per launch / average CUDA-event launch time vs
+the measured HBM peak), RoPE-reuse throughput (one layer of the all-gather
+round: 64 agents x 64 shared 128-token segments re-rotated into private
+blocks), the end-to-end rate through the public API with pinned host buffers,
+and the CPU oracle timed on a bounded sample of the same workload.
+
+Multi-GPU: the path partitions by agent with no exchange, so N ranks each run
+the full workload on their own agents (weak scaling, no collective).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+METRIC = "decode-attn tokens/s & KV GB/s vs GB300 HBM roofline; RoPE-reuse tokens/s"
+UNIT = "tokens/s"
+WORKLOAD = ("mha7b: 8 agents x 16384-token context, 60% shared prefix (614 shared + 8x410 private "
+            "16-token blocks), 32 q heads = 32 kv heads, head_dim 128, bf16, 32 layers, 1 decode token per agent")
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-rope", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--layers", type=int, default=32)
+    return ap.parse_args()
+
+
+# --------------------------------------------------------------- helpers ----
+def read_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def source_hash(files):
+    h = hashlib.sha256()
+    for f in files:
+        with open(os.path.join(ROOT, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+ATTN_SOURCES = ["shared_paged_kv_gb300/csrc/attn_tm.cu", "shared_paged_kv_gb300/csrc/common.cuh"]
+ATTN_KERNEL = "attn_tm_kernel<128,false,false>"
+
+
+def profiled_traffic(kernel_src_hash):
+    """DRAM bytes per launch of the attention kernel from the committed ncu
+    summary, if it was taken on the current kernel source (else None)."""
+    p = os.path.join(ROOT, "profiles", "attn_bf16_mha7b.md")
+    if not os.path.exists(p):
+        return None
+    vals = {}
+    with open(p) as f:
+        for line in f:
+            if line.startswith("- ") and ":" in line:
+                k, v = line[2:].split(":", 1)
+                vals[k.strip()] = v.strip().strip("`")
+    if vals.get("kernel_source_sha256_16") != kernel_src_hash:
+        return None
+    try:
+        return float(vals["dram_bytes_per_launch_full_size"])
+    except (KeyError, ValueError):
+        return None
+
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        self.out = ""
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                self.out, _ = self.proc.communicate()
+
+    def summary(self):
+        rows = [r.split(", ") for r in self.out.strip().splitlines() if r.count(",") >= 8]
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if "Active" in r[5 + i] and "Not" not in r[5 + i]})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+# ----------------------------------------------------------- CPU oracle -----
+CPU_PAIRS = [(a, h) for a in range(8) for h in (0, 9, 22, 31)]
+
+
+def cpu_sample_text(n_pairs):
+    return (f"oracle dedup of all 8 sequences + {n_pairs} (agent, head) pairs of one mha7b layer through the fp64 "
+            "oracle (dense materialise + attention), scaled to a full step of 8 agents x 32 heads x 32 layers")
+
+
+def cpu_oracle_step_seconds(layers: int, reps: int = 1, n_pairs: int = len(CPU_PAIRS)):
+    """Time the oracle as it stands on a bounded sample of the workload, reps
+    times; returns the extrapolated seconds of one full step for each rep.
+    Runs in a fresh interpreter with BLAS pinned to one thread, so it uses one
+    host core."""
+    code = f"""
+import sys, time, json
+sys.path.insert(0, {ROOT!r})
+import numpy as np
+from shared_paged_kv_gb300 import workloads as W
+from oracle import attention as OA, fingerprint as OF
+w = W.make_mha7b(n_layers=1)
+pairs = {CPU_PAIRS[:n_pairs]!r}
+rng = np.random.default_rng(0)
+out = []
+for rep in range({reps}):
+    t0 = time.perf_counter()
+    ref = OF.dedup(w.tokens, w.seq_off, w.tier, w.block_tokens, w.max_blocks)
+    t_dedup = time.perf_counter() - t0
+    cap = ref["n_phys"]
+    t_attn = 0.0
+    for a, h in pairs:
+        k = rng.standard_normal((cap, 1, 16, 128)).astype(np.float32)
+        v = rng.standard_normal((cap, 1, 16, 128)).astype(np.float32)
+        q = rng.standard_normal((1, 1, 128)).astype(np.float32)
+        t0 = time.perf_counter()
+        OA.decode_attention(q, k, v, ref["block_table"][a:a+1], w.seq_len[a:a+1], 16, w.scale)
+        t_attn += time.perf_counter() - t0
+    out.append(t_dedup + t_attn / len(pairs) * 8 * 32 * {layers})
+print(json.dumps(out))
+"""
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1")
+    r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, env=env, timeout=1800)
+    if r.returncode != 0:
+        raise RuntimeError(r.stderr[-2000:])
+    return json.loads(r.stdout.strip().splitlines()[-1])
+
+
+# ------------------------------------------------------------------ main ----
+def main():
+    args = parse()
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        # the CPU oracle as it stands; rank 0 only
+        if rank != 0:
+            return 0
+        n_pairs = 2
+        per_rep = cpu_oracle_step_seconds(args.layers, reps=args.warmup + args.steps, n_pairs=n_pairs)
+        timed = per_rep[args.warmup:]
+        step_s = sum(timed) / len(timed)
+        val = 8.0 / step_s
+        line = {"impl": "reference", "metric": METRIC, "value": val, "unit": UNIT, "n_gpus": args.gpus,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_s * 1e3,
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+                "data": "synthetic", "config": {"workload": WORKLOAD},
+                "cpu_baseline": {"kind": "oracle", "value": val, "unit": UNIT, "cores": 1,
+                                 "sample": cpu_sample_text(n_pairs) + " (per step)"},
+                "e2e": {"value": val, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+        print(json.dumps(line))
+        return 0
+
+    import torch
+    import torch.distributed as dist
+    import __graft_entry__ as G
+    G.build()
+    from shared_paged_kv_gb300 import kvs as K
+    from shared_paged_kv_gb300 import workloads as W
+
+    if world > 1:
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream()
+
+    # ---- workload, resident in HBM
+    L = args.layers
+    w = W.make_mha7b(n_layers=L)
+    B, D, H, N = w.block_tokens, w.head_dim, w.n_kv_heads, w.n_seq
+    cap = 614 + N * 410                       # physical blocks the dedup produces
+    gen = torch.Generator(device=dev).manual_seed(1000 + rank)
+    k_slabs = [torch.randn((cap, H, B, D), generator=gen, device=dev, dtype=torch.bfloat16) for _ in range(L)]
+    v_slabs = [torch.randn((cap, H, B, D), generator=gen, device=dev, dtype=torch.bfloat16) for _ in range(L)]
+    pool = K.kvs_pool_create(L, H, D, B, K.KVS_DTYPE_BF16, cap, N, [t.view(torch.int16) for t in k_slabs],
+                             [t.view(torch.int16) for t in v_slabs])
+    q = torch.randn((L, N, w.n_q_heads, D), generator=gen, device=dev, dtype=torch.bfloat16)
+    tokens = torch.from_numpy(w.tokens.view(np.int32)).to(dev)
+    seq_off = torch.from_numpy(w.seq_off).to(dev)
+    seq_len = torch.from_numpy(w.seq_len).to(dev)
+    fp = torch.zeros((N, w.max_blocks), dtype=torch.int64, device=dev)
+    table = torch.zeros((N, w.max_blocks), dtype=torch.int32, device=dev)
+    refc = torch.zeros(cap, dtype=torch.int32, device=dev)
+    nphys = torch.zeros(1, dtype=torch.int32, device=dev)
+    ws_d = torch.zeros(K.kvs_workspace_size(pool, K.KVS_OP_DEDUP, N, w.max_blocks), dtype=torch.uint8, device=dev)
+    ws_a = torch.zeros(K.kvs_workspace_size(pool, K.KVS_OP_DECODE_ATTN, N, w.max_blocks, w.n_q_heads),
+                       dtype=torch.uint8, device=dev)
+    out = torch.zeros((L, N, w.n_q_heads, D), dtype=torch.float32, device=dev)
+
+    ev_a = [[torch.cuda.Event(enable_timing=True) for _ in range(L)] for _ in range(args.steps)]
+    ev_b = [[torch.cuda.Event(enable_timing=True) for _ in range(L)] for _ in range(args.steps)]
+
+    def step(i=None):
+        K.kvs_fingerprint_dedup(pool, tokens, seq_off, N, None, None, None, fp, table, w.max_blocks, refc,
+                                nphys, ws_d)
+        for l in range(L):
+            if i is not None:
+                ev_a[i][l].record(stream)
+            K.kvs_decode_attn(pool, l, q[l], w.n_q_heads, table, w.max_blocks, seq_len, N, None, None, None,
+                              w.theta, w.scale, out[l], ws_a)
+            if i is not None:
+                ev_b[i][l].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    flags = K.kvs_pool_check(pool)
+    if flags:
+        raise RuntimeError(f"device status flags {flags:#x}")
+    assert int(nphys.item()) == cap, (int(nphys.item()), cap)
+
+    launches0 = K.kvs_launch_count()
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local_rank) as clk:
+        t0.record(stream)
+        for i in range(args.steps):
+            step(i)
+        t1.record(stream)
+        torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    launches = K.kvs_launch_count() - launches0
+    ms = t0.elapsed_time(t1)
+    if world > 1:
+        tt = torch.tensor([ms], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        ms = float(tt.item())
+    ms_step = ms / args.steps
+    attn_ms = [ev_a[i][l].elapsed_time(ev_b[i][l]) for i in range(args.steps) for l in range(L)]
+    attn_avg_ms = sum(attn_ms) / len(attn_ms)
+
+    # ---- algorithmic bytes of one attention launch (unique bytes leaving HBM)
+    kv_bytes = cap * H * B * D * 2 * 2
+    attn_bytes = kv_bytes + N * w.n_q_heads * D * 2 + N * w.max_blocks * 4 + N * 4 + N * w.n_q_heads * D * 4
+    peak, peak_kind = read_peaks()
+    achieved = attn_bytes / (attn_avg_ms * 1e-3) / 1e9
+    step_bytes = L * attn_bytes + w.tokens.nbytes + N * w.max_blocks * (8 + 4)
+    value = world * N / (ms_step * 1e-3)
+
+    # ---- end to end through the public API with pinned host buffers
+    e2e = None
+    if not args.no_e2e:
+        h_tok = torch.from_numpy(w.tokens.view(np.int32)).pin_memory()
+        h_off = torch.from_numpy(w.seq_off).pin_memory()
+        h_q = q.cpu().pin_memory()
+        h_out = torch.empty(out.shape, dtype=torch.float32).pin_memory()
+        d_tok, d_off, d_q = torch.empty_like(tokens), torch.empty_like(seq_off), torch.empty_like(q)
+
+        def e2e_step():
+            d_tok.copy_(h_tok, non_blocking=True)
+            d_off.copy_(h_off, non_blocking=True)
+            d_q.copy_(h_q, non_blocking=True)
+            K.kvs_fingerprint_dedup(pool, d_tok, d_off, N, None, None, None, fp, table, w.max_blocks, refc,
+                                    nphys, ws_d)
+            for l in range(L):
+                K.kvs_decode_attn(pool, l, d_q[l], w.n_q_heads, table, w.max_blocks, seq_len, N, None, None,
+                                  None, w.theta, w.scale, out[l], ws_a)
+            h_out.copy_(out, non_blocking=True)
+            torch.cuda.synchronize()
+
+        for _ in range(2):
+            e2e_step()
+        t_a = time.perf_counter()
+        for _ in range(args.steps):
+            e2e_step()
+        e2e_s = (time.perf_counter() - t_a) / args.steps
+        e2e = {"value": world * N / e2e_s, "unit": UNIT,
+               "h2d_bytes_per_step": int(h_tok.numel() * 4 + h_off.numel() * 8 + h_q.numel() * 2),
+               "d2h_bytes_per_step": int(h_out.numel() * 4)}
+
+    # ---- RoPE re-rotation on one layer of the all-gather round
+    rope = None
+    if not args.no_rope:
+        rope = bench_rope(torch, K, W, dev, stream, args, peak)
+
+    # ---- CPU oracle
+    cpu = None
+    if not args.no_cpu_baseline and rank == 0:
+        step_s = cpu_oracle_step_seconds(L)[0]
+        cpu = {"value": N / step_s, "unit": UNIT, "cores": 1, "kind": "oracle",
+               "sample": cpu_sample_text(len(CPU_PAIRS))}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "agents": N, "context": 16384, "layers": L,
+                       "l2": "inputs larger than L2 (32.7 GB of unique KV per step), no flush",
+                       "parallelism": f"replicas x{world} (agents partitioned, no collective)"},
+            "kv_gbs": world * step_bytes / (ms_step * 1e-3) / 1e9,
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                         "frac": achieved / peak, "traffic": profiled_traffic(source_hash(ATTN_SOURCES)),
+                         "kernel": ATTN_KERNEL, "peak_kind": peak_kind,
+                         "bytes_per_launch": attn_bytes, "avg_launch_ms": attn_avg_ms},
+            "cpu_baseline": cpu,
+            "e2e": e2e,
+            "gpu_launches": launches,
+            "clocks": clk.summary(),
+            "rope_reuse": rope,
+        }
+        print(json.dumps(line))
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+def bench_rope(torch, K, W, dev, stream, args, peak):
+    """All-gather round, one layer: 64 agents x 64 shared 128-token segments
+    re-rotated from the master copy into private blocks (524,288 rows)."""
+    w = W.make_allgather(n_layers=1)
+    # physical layout: masters = first occurrences; destinations after them
+    n_master = 64 * 8
+    rows = []
+    B = w.block_tokens
+    src_row = 0
+    r_off = w.rope_off
+    src_segs = w.rope_segs[r_off[0]:r_off[1]]
+    # source table: row 0 maps its segment blocks to master blocks 0..511
+    src_table = np.full((1, w.max_blocks), -1, np.int32)
+    by_src = {}
+    for j, (fb, nb, delta, _) in enumerate(src_segs):
+        src_table[0, fb:fb + nb] = np.arange(j * nb, (j + 1) * nb)
+        by_src[fb * B - delta] = fb * B
+    jobs = []
+    dst_table = np.full((w.n_seq, w.max_blocks), -1, np.int32)
+    nxt = n_master
+    for a in range(w.n_seq):
+        for (fb, nb, delta, _) in w.rope_segs[r_off[a]:r_off[a + 1]]:
+            dst_table[a, fb:fb + nb] = np.arange(nxt, nxt + nb)
+            nxt += nb
+            jobs.append((src_row, by_src[fb * B - delta], a, fb * B, nb * B, fb * B - delta, fb * B, 0))
+    jobs = np.array(jobs, np.int32)
+    cap = nxt
+    k = torch.randn((cap, w.n_kv_heads, B, w.head_dim), device=dev, dtype=torch.bfloat16)
+    v = torch.zeros(16, dtype=torch.int16, device=dev)
+    pool = K.kvs_pool_create(1, w.n_kv_heads, w.head_dim, B, K.KVS_DTYPE_BF16, cap, w.n_seq, [k.view(torch.int16)], [v])
+    jd = torch.from_numpy(jobs).to(dev)
+    st = torch.from_numpy(src_table).to(dev)
+    dt = torch.from_numpy(dst_table).to(dev)
+    n_rows = int(jobs[:, 4].sum())
+
+    def run():
+        K.kvs_rope_rerotate(pool, 0, jd, len(jobs), 128, w.theta, st, dt, w.max_blocks)
+
+    for _ in range(3):
+        run()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        run()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    flags = K.kvs_pool_check(pool)
+    t = e0.elapsed_time(e1) / args.steps * 1e-3
+    row_bytes = w.n_kv_heads * w.head_dim * 2
+    algo = n_master * w.n_kv_heads * B * w.head_dim * 2 + n_rows * row_bytes + jobs.nbytes
+    del k, pool
+    return {"rows_per_s": n_rows / t, "unit": "rows/s (one row = one token's K over all KV heads)",
+            "rows": n_rows, "ms": t * 1e3, "achieved_gbs": algo / t / 1e9, "frac": algo / t / 1e9 / peak,
+            "status_flags": flags}
+
+
+if __name__ == "__main__":
+    sys.exit(main())

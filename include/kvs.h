@@ -1,0 +1,264 @@
+/*
+ * kvs.h — C ABI of libkvs: decode-step attention over a pool of fixed-size KV
+ * blocks shared by many agents, for NVIDIA GB300 (sm_103a).
+ *
+ * The operations follow these pages:
+ *   [INMS]   "大模型多Agent系统显存优化：KV Cache共享机制解析" — a walkthrough of
+ *            "INMS: Memory Sharing for LLM based Agents": fixed-size blocks,
+ *            content fingerprints, refcounts, prefix sharing (§2.2, §3.2),
+ *            RoPE offset compensation (§3.2), tier folded into the
+ *            fingerprint (§5.1).
+ *   [TD]     "TokenDance: Scaling Multi-Agent LLM Serving via Collective KV
+ *            Cache Sharing" (news summary): segment hashing (section 1),
+ *            batched RoPE and critical-position selection (section 2, Fig. 6),
+ *            master/mirror block-sparse diffs with fused restore (section 3,
+ *            Fig. 7, Fig. 8).
+ *   [POOL]   "共享内存KV Cache池" — host shared-memory KV pool post: per-token KV
+ *            formula (§1.1), CalcHash (§3.2), longest-prefix match (§3.3).
+ *   [Q4]     "Agent Memory Below the Prompt: Persistent Q4 KV Cache for
+ *            Multi-Agent LLM Inference on Edge Devices" (summary): 256-token
+ *            4-bit blocks (§2.1), attention directly on Q4 (§2.2).
+ *   [MD]     "MemDecay: Region-Aware KV Cache Eviction" (§4.2: scores are
+ *            q.k / sqrt(head_dim)).
+ *
+ * Conventions for every call:
+ *   - Pointers named *_dev or documented "device" are device pointers in the
+ *     current CUDA device's memory; everything else is host memory.
+ *   - Every device buffer is owned by the caller.  The library allocates
+ *     device memory only in kvs_pool_create (a status word and the split-K
+ *     arrival counters, freed by kvs_pool_destroy).
+ *   - Calls that take a cudaStream_t only enqueue work on it and return
+ *     without synchronising, except kvs_pool_check and kvs_pool_stats.
+ *   - Calls on one pool must be ordered on one stream (the arrival counters
+ *     and the status word are per pool).
+ *   - Host-detectable argument errors return a status before anything is
+ *     enqueued.  Errors the device detects (a block id outside the pool, a
+ *     sequence longer than its block-table row, a capacity overflow, a
+ *     bounded wait that ran out) set bits in the pool's status word, skip the
+ *     offending access and never trap; read them with kvs_pool_check.
+ *   - kvs_last_error_string() describes the last failure on this host thread.
+ */
+#ifndef KVS_H
+#define KVS_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  KVS_OK = 0,
+  KVS_ERR_INVALID_ARG = 1,    /* a null/misaligned pointer or an out-of-range size */
+  KVS_ERR_CAPACITY = 2,       /* a pool, table or workspace is too small */
+  KVS_ERR_CUDA = 3,           /* a CUDA runtime call failed */
+  KVS_ERR_DEVICE_BOUNDS = 4,  /* the device saw an out-of-range index (kvs_pool_check) */
+  KVS_ERR_UNSUPPORTED = 5     /* a shape this build has no kernel for */
+} kvs_status;
+
+/* Device status-word bits reported by kvs_pool_check. */
+#define KVS_DEVERR_BLOCK_ID     0x1u  /* block id < 0 or >= capacity in a table */
+#define KVS_DEVERR_SEQ_LEN      0x2u  /* seq_len beyond max_blocks * block_tokens, or < 0 */
+#define KVS_DEVERR_CAPACITY     0x4u  /* dedup produced more physical blocks than capacity */
+#define KVS_DEVERR_DIFF_ID      0x8u  /* diff block id >= diff capacity */
+#define KVS_DEVERR_WAIT_TIMEOUT 0x10u /* a bounded wait on a TMA copy ran out */
+#define KVS_DEVERR_ROPE_RANGE   0x20u /* |position shift| >= 2^18 */
+#define KVS_DEVERR_JOB          0x40u /* a RoPE job addresses tokens outside its table row */
+
+typedef enum { KVS_DTYPE_BF16 = 0, KVS_DTYPE_Q4G64 = 1 } kvs_dtype;
+
+/* Pool geometry.  One K slab and one V slab per layer.
+ *   BF16:   slab[capacity_blocks][num_kv_heads][block_tokens][head_dim] bf16.
+ *   Q4G64:  codes[capacity_blocks][num_kv_heads][block_tokens][head_dim/2]
+ *           uint8 (element 2i in the low nibble of byte i) plus scale/bias
+ *           [capacity_blocks][num_kv_heads][block_tokens][head_dim/64][2] fp16
+ *           (index 0 = scale, 1 = bias; value = scale * code + bias) — [Q4]
+ *           §2.1 (ratio 0.281 fixes group 64 with fp16 scale and bias).
+ *   Mirror diffs (BF16 only): dk/dv slabs [diff_capacity_blocks][num_kv_heads]
+ *           [block_tokens][head_dim] bf16 holding K and V differences added to
+ *           a master block — [TD] section 3.
+ * Supported by this build: head_dim 64 or 128; BF16 block_tokens 16;
+ * Q4G64 block_tokens 256 with head_dim 128. */
+typedef struct {
+  int32_t num_layers;
+  int32_t num_kv_heads;
+  int32_t head_dim;
+  int32_t block_tokens;
+  int32_t dtype;                 /* kvs_dtype */
+  int32_t capacity_blocks;       /* physical blocks per layer slab */
+  int32_t diff_capacity_blocks;  /* 0 = no mirror diffs */
+  int32_t max_seqs;              /* largest n_seq any call will pass */
+} kvs_pool_desc;
+
+typedef struct kvs_pool kvs_pool;
+
+/* Create a pool over caller-owned per-layer slabs.  The pointer arrays are
+ * host arrays of num_layers device pointers (16-byte aligned); k_sb/v_sb are
+ * required for Q4G64 and must be NULL for BF16; dk/dv are required when
+ * diff_capacity_blocks > 0.  Builds one TMA tensor map per slab.  The pool
+ * never frees the slabs.  Errors: INVALID_ARG, UNSUPPORTED, CUDA. */
+kvs_status kvs_pool_create(const kvs_pool_desc* desc,
+                           void* const* k_layers, void* const* v_layers,
+                           void* const* k_sb_layers, void* const* v_sb_layers,
+                           void* const* dk_layers, void* const* dv_layers,
+                           kvs_pool** out);
+kvs_status kvs_pool_destroy(kvs_pool* pool);
+
+/* ---------------------------------------------------------------------------
+ * Block fingerprints + deduplication ([POOL] §3.2 CalcHash, §3.3; [INMS]
+ * §2.2, §3.2, §5.1; [TD] section 1 segment hashing).
+ *
+ * tokens_dev    uint32 token ids of all sequences, concatenated.
+ * seq_off_dev   int64 [n_seq+1] CSR offsets into tokens.
+ * tier_dev      uint32 [n_seq] memory tier per sequence, or NULL (= tier 0).
+ *               Tier 0xFFFFFFFF is PRIVATE: its blocks are never shared.
+ * seg_off_dev / seg_blocks_dev   optional CSR (int64 [n_seq+1] / int32) of
+ *               block indices where a hashed segment starts (block 0 always
+ *               does); NULL for plain prefix hashing.  Ascending per sequence.
+ * fp_out_dev    uint64 [n_seq][max_blocks]: CalcHash(block tokens, tier) of
+ *               every full block, 0 elsewhere.
+ * block_table_dev int32 [n_seq][max_blocks]: physical block id, -1 unused.
+ * refcount_dev  int32 [pool capacity]: references per physical block
+ *               (entries >= n_phys are zeroed).
+ * n_phys_dev    int32 [1]: physical blocks used.
+ * Rule: full blocks of equal tier (not PRIVATE), at the same index inside
+ * their segment, with identical token runs from the segment start through the
+ * block, share one physical block; tail and PRIVATE blocks get fresh ones; ids
+ * follow first occurrence scanning sequence-major.  The result is exact: a
+ * 64-bit hash collision is caught by a token compare and resolved.
+ * ws/ws_bytes   device scratch of kvs_workspace_size(KVS_OP_DEDUP) bytes.
+ * flags         0, or KVS_DEDUP_TEST_WEAK_KEYS (truncates the internal table
+ *               keys to 6 bits so that the collision path runs; results are
+ *               unchanged, only slower).
+ * Device errors: SEQ_LEN (a sequence needs more than max_blocks blocks),
+ * CAPACITY (more physical blocks than the pool holds). */
+#define KVS_DEDUP_TEST_WEAK_KEYS 0x1u
+kvs_status kvs_fingerprint_dedup(kvs_pool* pool,
+                                 const uint32_t* tokens_dev, const int64_t* seq_off_dev,
+                                 int32_t n_seq, const uint32_t* tier_dev,
+                                 const int64_t* seg_off_dev, const int32_t* seg_blocks_dev,
+                                 uint64_t* fp_out_dev, int32_t* block_table_dev,
+                                 int32_t max_blocks, int32_t* refcount_dev, int32_t* n_phys_dev,
+                                 uint32_t flags, void* ws, size_t ws_bytes, cudaStream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * Batched RoPE re-rotation of reused K ([INMS] §3.2; [TD] section 2, one
+ * batched RoPE call per layer).  Each job moves n_tok tokens of K:
+ *   K[dst] = R(dst_pos - src_pos) * K[src]
+ * with rotate-half pairing (i, i + d/2) and frequency theta^(-2i/d); V is not
+ * touched.  Source token t is token src_tok0+t of row src_row of
+ * src_table_dev; the destination is token dst_tok0+t of row dst_row of
+ * dst_table_dev; both tables are int32 [rows][max_blocks] into this layer's K
+ * slab, all KV heads.  Destinations must not overlap sources.
+ * jobs_dev      kvs_rope_job [n_jobs] (device).
+ * max_job_tokens  an upper bound of n_tok over the jobs (sizes the grid).
+ * |dst_pos - src_pos| must be < 2^18.  BF16 pools only. */
+typedef struct {
+  int32_t src_row, src_tok0, dst_row, dst_tok0, n_tok, src_pos, dst_pos, reserved;
+} kvs_rope_job;
+kvs_status kvs_rope_rerotate(kvs_pool* pool, int32_t layer, const kvs_rope_job* jobs_dev,
+                             int32_t n_jobs, int32_t max_job_tokens, float theta,
+                             const int32_t* src_table_dev, const int32_t* dst_table_dev,
+                             int32_t max_blocks, cudaStream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * Critical-position selection ([TD] section 2: one batched difference
+ * computation finds each request's positions whose cached and new K differ
+ * most).  For agent a with rows [row_off[a], row_off[a+1]) of k_cached and
+ * k_new (bf16 [rows][row_elems]):
+ *   score_t = || k_cached[t] - k_new[t] ||_2   (fp32 accumulation)
+ *   k_a = ceil(ratio * n_a)  (ratio as float32, product in fp64)
+ * keeps the k_a largest scores (ties toward the lower position) and writes
+ * their positions, relative to the agent's first row, ascending, to
+ * idx_out_dev[idx_off[a] ...]; idx_off_dev (int64 [n_agents+1]) is the
+ * exclusive prefix sum of k_a.  row_elems must be a multiple of 8.
+ * max_rows_per_agent bounds n_a (<= 65536).  ws: kvs_workspace_size(SELECT). */
+kvs_status kvs_select_critical(const void* k_cached_dev, const void* k_new_dev,
+                               const int64_t* row_off_dev, int32_t n_agents,
+                               int32_t max_rows_per_agent, int32_t row_elems, float ratio,
+                               int32_t* idx_out_dev, int64_t* idx_off_dev,
+                               void* ws, size_t ws_bytes, cudaStream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * Paged decode attention with the mirror-diff overlay and segment RoPE
+ * restore fused into the read ([TD] section 3, Fig. 8: blocks with a diff
+ * are corrected on chip before attention, nothing dense is materialised;
+ * [INMS] §3.2 rotation; [MD] §4.2 scaled dot product).  For every sequence a
+ * and query head h (kv head = h / (n_q_heads / num_kv_heads)):
+ *   out[a][h] = sum_t softmax_t(scale * <q[a][h], K~_a[t]>) V~_a[t]
+ *   K~ = R(delta_seg) (K_blk + DK_blk),  V~ = V_blk + DV_blk
+ * over t < seq_len[a]; DK/DV are the agent's diff block for that logical block
+ * (diff_table >= 0) and delta_seg the shift of the RoPE segment covering it.
+ * q_dev         bf16 [n_seq][n_q_heads][head_dim] (already position-encoded).
+ * block_table_dev int32 [n_seq][max_blocks]; seq_len_dev int32 [n_seq].
+ * diff_table_dev  int32 [n_seq][max_blocks] diff block id or -1; or NULL.
+ * rope_off_dev / rope_segs_dev  optional CSR: int32 [n_seq+1] offsets into
+ *               kvs_seg_rope entries {first_block, n_blocks, delta}; blocks
+ *               outside every entry are not rotated; |delta| < 2^18.
+ * out_dev       float32 [n_seq][n_q_heads][head_dim]; an empty context
+ *               (seq_len 0) yields zeros.
+ * ws            kvs_workspace_size(KVS_OP_DECODE_ATTN) bytes of device memory.
+ * Requires n_q_heads % num_kv_heads == 0 and a group of at most 16 query
+ * heads per KV head; BF16 pools. */
+typedef struct { int32_t first_block, n_blocks, delta, reserved; } kvs_seg_rope;
+kvs_status kvs_decode_attn(kvs_pool* pool, int32_t layer, const void* q_dev, int32_t n_q_heads,
+                           const int32_t* block_table_dev, int32_t max_blocks,
+                           const int32_t* seq_len_dev, int32_t n_seq,
+                           const int32_t* diff_table_dev,
+                           const int32_t* rope_off_dev, const kvs_seg_rope* rope_segs_dev,
+                           float theta, float scale, float* out_dev,
+                           void* ws, size_t ws_bytes, cudaStream_t stream);
+
+/* Decode attention reading a Q4G64 pool directly, dequantising in registers
+ * ([Q4] §2.2).  Same meaning as kvs_decode_attn without diffs or rotation. */
+kvs_status kvs_decode_attn_q4(kvs_pool* pool, int32_t layer, const void* q_dev, int32_t n_q_heads,
+                              const int32_t* block_table_dev, int32_t max_blocks,
+                              const int32_t* seq_len_dev, int32_t n_seq,
+                              float scale, float* out_dev,
+                              void* ws, size_t ws_bytes, cudaStream_t stream);
+
+/* Quantise bf16 K/V blocks into a Q4G64 pool ([Q4] §2.1).  k_src/v_src are
+ * bf16 [n_blocks][num_kv_heads][block_tokens][head_dim]; block i is written to
+ * physical block dst_blocks_dev[i] of `layer`.  Per 64-element group:
+ * scale = fp16((max-min)/15), bias = fp16(min) (float32 arithmetic),
+ * code = clamp(rint((x - bias)/scale), 0, 15), scale 0 -> code 0. */
+kvs_status kvs_quantize_q4(kvs_pool* pool, int32_t layer, const void* k_src_dev,
+                           const void* v_src_dev, const int32_t* dst_blocks_dev,
+                           int32_t n_blocks, cudaStream_t stream);
+
+/* Workspace bytes for an operation with the given call shape. */
+#define KVS_OP_DEDUP 0
+#define KVS_OP_DECODE_ATTN 1
+#define KVS_OP_DECODE_ATTN_Q4 2
+#define KVS_OP_SELECT 3
+kvs_status kvs_workspace_size(const kvs_pool* pool, int32_t op, int32_t n_seq,
+                              int32_t max_blocks, int32_t n_q_heads, size_t* bytes);
+
+/* Synchronise `stream`, read and clear the pool's device status word into
+ * *flags (KVS_DEVERR_* bits).  Returns KVS_ERR_DEVICE_BOUNDS when any bit was
+ * set, KVS_OK otherwise. */
+kvs_status kvs_pool_check(kvs_pool* pool, cudaStream_t stream, uint32_t* flags);
+
+/* Pool statistics from a dedup result: synchronises `stream`, copies the
+ * refcounts back and reports unique (n_phys), shared (refcount > 1) blocks,
+ * total references, and bytes a dense per-sequence layout would need versus
+ * the pool — [INMS] §1.2 independent vs shared footprint. */
+typedef struct {
+  int64_t unique_blocks, shared_blocks, total_refs;
+  int64_t pool_bytes, dense_bytes;
+} kvs_stats;
+kvs_status kvs_pool_stats(const kvs_pool* pool, const int32_t* refcount_dev,
+                          const int32_t* n_phys_dev, cudaStream_t stream, kvs_stats* out);
+
+/* Describes the last error raised on this host thread (never NULL). */
+const char* kvs_last_error_string(void);
+
+/* Number of kernels this library launched so far in this process. */
+uint64_t kvs_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* KVS_H */

@@ -1,0 +1,403 @@
+// Block fingerprints and exact deduplication into a shared physical pool.
+//
+// What is computed: shared-memory KV pool post §3.2 (CalcHash: FNV-1a-style
+// over whole 32-bit token ids with offset basis 1469598103934665603 and prime
+// 1099511628211, then the tag); INMS walkthrough §2.2 / §3.2 / §5.1 (blocks
+// are reused only with equal content, tier and position range, up to the
+// first divergence; the tier is part of the fingerprint); TokenDance summary
+// section 1 (with explicit segment boundaries the hashing is per segment).
+// Two full blocks share a physical block iff they have the same non-PRIVATE
+// tier, the same index inside their hashed segment and identical token runs
+// from the segment start through the block.  Ids follow first occurrence in
+// sequence-major order; refcount = references.
+//
+// How (GB300, all on device, no host round trip):
+//  1. prep: one warp per sequence computes CalcHash of each full block and a
+//     segment-local chain key with a warp-wide segmented scan of the affine
+//     map h -> h*M + fp (restarted at segment starts), finalised with
+//     SplitMix64's mixer and folded with the segment-local index.
+//  2. insert: every shareable block inserts its key into an open-addressing
+//     table; atomicMin keeps the lowest (sequence, block) slot per key.
+//  3. resolve: each block takes the table's owner as its representative and
+//     verifies it: same tier, same local index, equal block tokens, and the
+//     predecessor blocks resolve to the same representative (induction over
+//     the segment).  A failure (a key collision) raises a flag.
+//  4. fallback (only when flagged): exact brute-force representative search.
+//  5. scan: one CTA numbers first occurrences in slot order (deterministic).
+//  6. table: block_table and refcounts.
+#include <climits>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace kvs {
+
+constexpr uint64_t kFnvOffset = 1469598103934665603ull;
+constexpr uint64_t kFnvPrime = 1099511628211ull;
+constexpr uint32_t kPrivateTier = 0xFFFFFFFFu;
+constexpr uint64_t kChainMul = 0x9E3779B97F4A7C15ull;
+
+struct DedupParams {
+  const uint32_t* tokens;
+  const int64_t* seq_off;
+  const uint32_t* tier;
+  const int64_t* seg_off;
+  const int32_t* seg_blocks;
+  uint64_t* fp_out;
+  int32_t* block_table;
+  int32_t* refcount;
+  int32_t* n_phys;
+  uint32_t* status;
+  // workspace
+  unsigned long long* tkeys;
+  int32_t* tmin;
+  uint64_t* key;      // per slot, 0 = not shareable
+  int32_t* rep;       // per slot representative slot (or -1 unused)
+  int32_t* segstart;  // per slot
+  int32_t* pid;       // per slot physical id of first occurrences
+  uint32_t* flags;    // [0] collision
+  int n_seq, max_blocks, B, capacity, weak;
+  uint32_t tmask;
+};
+
+__device__ __forceinline__ uint64_t splitmix_mix(uint64_t z) {
+  z = (z ^ (z >> 30)) * 0xbf58476d1ce4e5b9ull;
+  z = (z ^ (z >> 27)) * 0x94d049bb133111ebull;
+  return z ^ (z >> 31);
+}
+
+__device__ __forceinline__ void seq_geom(const DedupParams& p, int s, int64_t& off, int& nblk, int& full) {
+  off = p.seq_off[s];
+  const int64_t len = p.seq_off[s + 1] - off;
+  int64_t nb = (len + p.B - 1) / p.B;
+  int64_t fu = len / p.B;
+  if (len < 0) nb = fu = 0;
+  if (nb > p.max_blocks) {
+    nb = p.max_blocks;
+    if (fu > nb) fu = nb;
+  }
+  nblk = static_cast<int>(nb);
+  full = static_cast<int>(fu);
+}
+
+// 1. one warp per sequence
+__global__ void dedup_prep(DedupParams p) {
+  const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (warp >= p.n_seq) return;
+  const int s = warp;
+  int64_t off;
+  int nblk, full;
+  seq_geom(p, s, off, nblk, full);
+  {
+    const int64_t len = p.seq_off[s + 1] - off;
+    if (lane == 0 && (len < 0 || (len + p.B - 1) / p.B > p.max_blocks)) set_err(p.status, KVS_DEVERR_SEQ_LEN);
+  }
+  const uint32_t tier = p.tier ? p.tier[s] : 0u;
+  const size_t row = (size_t)s * p.max_blocks;
+  // segment start of every block
+  for (int b = lane; b < p.max_blocks; b += 32) p.segstart[row + b] = 0;
+  __syncwarp();
+  if (p.seg_off) {
+    const int64_t e0 = p.seg_off[s], e1 = p.seg_off[s + 1];
+    int prev = 0;
+    for (int64_t e = e0; e < e1; ++e) {
+      const int st = p.seg_blocks[e];
+      if (st <= prev || st >= nblk) continue;   // ignore unsorted / out-of-range starts
+      int nxt = nblk;
+      for (int64_t e2 = e + 1; e2 < e1; ++e2) {
+        const int v = p.seg_blocks[e2];
+        if (v > st) { nxt = min(nxt, v); break; }
+      }
+      for (int b = st + lane; b < nxt; b += 32) p.segstart[row + b] = st;
+      prev = st;
+      __syncwarp();
+    }
+  }
+  __syncwarp();
+  uint64_t carryA = 1, carryC = 0;
+  for (int base = 0; base < p.max_blocks; base += 32) {
+    const int b = base + lane;
+    uint64_t fp = 0;
+    bool shareable = false;
+    int st = 0;
+    if (b < nblk) {
+      st = p.segstart[row + b];
+      if (b < full) {
+        const uint32_t* t = p.tokens + off + (int64_t)b * p.B;
+        uint64_t h = kFnvOffset;
+        for (int i = 0; i < p.B; ++i) {
+          h ^= (uint64_t)t[i];
+          h *= kFnvPrime;
+        }
+        h ^= (uint64_t)tier;
+        h *= kFnvPrime;
+        fp = h;
+        shareable = tier != kPrivateTier;
+      }
+    }
+    if (b < p.max_blocks) p.fp_out[row + b] = fp;
+    // segmented scan of x -> A x + C
+    uint64_t A = (b < nblk && b != st) ? kChainMul : (b < nblk ? 0ull : 1ull);
+    uint64_t Cc = (b < nblk) ? (b == st ? fp + kChainMul : fp) : 0ull;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint64_t A2 = __shfl_up_sync(0xffffffffu, A, o);
+      const uint64_t C2 = __shfl_up_sync(0xffffffffu, Cc, o);
+      if (lane >= o) {
+        Cc = A * C2 + Cc;
+        A = A * A2;
+      }
+    }
+    const uint64_t gC = A * carryC + Cc;
+    const uint64_t gA = A * carryA;
+    carryA = __shfl_sync(0xffffffffu, gA, 31);
+    carryC = __shfl_sync(0xffffffffu, gC, 31);
+    if (b < p.max_blocks) {
+      uint64_t k = 0;
+      if (shareable) {
+        k = splitmix_mix(gC ^ ((uint64_t)(b - st) * 0xD6E8FEB86659FD93ull) ^ ((uint64_t)tier << 32));
+        if (p.weak) k = (k & 63ull) + 1ull;
+        if (k == 0) k = 1;
+      }
+      p.key[row + b] = k;
+      p.rep[row + b] = b < nblk ? (int32_t)(row + b) : -1;
+    }
+  }
+}
+
+__device__ __forceinline__ uint32_t table_slot(uint64_t k, uint32_t mask) {
+  return static_cast<uint32_t>(splitmix_mix(k ^ 0x5851F42D4C957F2Dull)) & mask;
+}
+
+// 2. insert every shareable slot
+__global__ void dedup_insert(DedupParams p) {
+  const int slot = blockIdx.x * blockDim.x + threadIdx.x;
+  if (slot >= p.n_seq * p.max_blocks) return;
+  const uint64_t k = p.key[slot];
+  if (!k) return;
+  uint32_t i = table_slot(k, p.tmask);
+  for (uint32_t probe = 0; probe <= p.tmask; ++probe) {
+    const unsigned long long old = atomicCAS(p.tkeys + i, 0ull, (unsigned long long)k);
+    if (old == 0ull || old == k) {
+      atomicMin(p.tmin + i, slot);
+      return;
+    }
+    i = (i + 1) & p.tmask;
+  }
+}
+
+__device__ __forceinline__ int table_owner(const DedupParams& p, uint64_t k) {
+  uint32_t i = table_slot(k, p.tmask);
+  for (uint32_t probe = 0; probe <= p.tmask; ++probe) {
+    const unsigned long long v = p.tkeys[i];
+    if (v == k) return p.tmin[i];
+    if (v == 0ull) return -1;
+    i = (i + 1) & p.tmask;
+  }
+  return -1;
+}
+
+__device__ __forceinline__ bool same_block_tokens(const DedupParams& p, int s1, int b1, int s2, int b2) {
+  const uint32_t* t1 = p.tokens + p.seq_off[s1] + (int64_t)b1 * p.B;
+  const uint32_t* t2 = p.tokens + p.seq_off[s2] + (int64_t)b2 * p.B;
+  for (int i = 0; i < p.B; ++i)
+    if (t1[i] != t2[i]) return false;
+  return true;
+}
+
+// 3. resolve and verify representatives
+__global__ void dedup_resolve(DedupParams p) {
+  const int slot = blockIdx.x * blockDim.x + threadIdx.x;
+  if (slot >= p.n_seq * p.max_blocks) return;
+  const uint64_t k = p.key[slot];
+  if (!k) return;
+  const int r = table_owner(p, k);
+  bool ok = r >= 0;
+  if (ok && r != slot) {
+    const int s = slot / p.max_blocks, b = slot - s * p.max_blocks;
+    const int s2 = r / p.max_blocks, b2 = r - s2 * p.max_blocks;
+    const uint32_t t1 = p.tier ? p.tier[s] : 0u, t2 = p.tier ? p.tier[s2] : 0u;
+    const int st1 = p.segstart[slot], st2 = p.segstart[r];
+    ok = p.key[r] != 0 && t1 == t2 && (b - st1) == (b2 - st2) && same_block_tokens(p, s, b, s2, b2);
+    if (ok && b > st1) {
+      const int r1 = table_owner(p, p.key[slot - 1]);
+      const int r2 = table_owner(p, p.key[r - 1]);
+      ok = r1 >= 0 && r1 == r2;
+    }
+  }
+  if (ok) {
+    p.rep[slot] = r;
+  } else {
+    atomicOr(p.flags, 1u);
+  }
+}
+
+// 4. exact brute force, only after a collision was detected
+__global__ void dedup_fallback(DedupParams p) {
+  if (*(volatile uint32_t*)p.flags == 0u) return;
+  const int slot = blockIdx.x * blockDim.x + threadIdx.x;
+  if (slot >= p.n_seq * p.max_blocks) return;
+  if (!p.key[slot]) return;
+  const int s = slot / p.max_blocks, b = slot - s * p.max_blocks;
+  const uint32_t t1 = p.tier ? p.tier[s] : 0u;
+  const int st1 = p.segstart[slot];
+  const int local = b - st1;
+  for (int s2 = 0; s2 <= s; ++s2) {
+    if ((p.tier ? p.tier[s2] : 0u) != t1) continue;
+    int64_t off2;
+    int nblk2, full2;
+    seq_geom(p, s2, off2, nblk2, full2);
+    const int bend = (s2 == s) ? b : full2;
+    for (int b2 = 0; b2 < bend && b2 < full2; ++b2) {
+      const int o = s2 * p.max_blocks + b2;
+      if (!p.key[o]) continue;
+      const int st2 = p.segstart[o];
+      if (b2 - st2 != local) continue;
+      bool eq = true;
+      for (int j = 0; j <= local && eq; ++j) eq = same_block_tokens(p, s, st1 + j, s2, st2 + j);
+      if (eq) {
+        p.rep[slot] = o;
+        return;
+      }
+    }
+  }
+  p.rep[slot] = slot;
+}
+
+// 5. one CTA: number the first occurrences in slot order
+__global__ void __launch_bounds__(1024) dedup_scan(DedupParams p) {
+  __shared__ int warp_sums[32];
+  __shared__ int carry;
+  const int n = p.n_seq * p.max_blocks;
+  if (threadIdx.x == 0) carry = 0;
+  __syncthreads();
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  for (int base = 0; base < n; base += blockDim.x) {
+    const int slot = base + threadIdx.x;
+    int f = 0;
+    if (slot < n) {
+      const int r = p.rep[slot];
+      f = (r == slot) ? 1 : 0;
+    }
+    int x = f;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, x, o);
+      if (lane >= o) x += y;
+    }
+    if (lane == 31) warp_sums[warp] = x;
+    __syncthreads();
+    if (warp == 0) {
+      int w = warp_sums[lane];
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, w, o);
+        if (lane >= o) w += y;
+      }
+      warp_sums[lane] = w;
+    }
+    __syncthreads();
+    const int incl = x + (warp ? warp_sums[warp - 1] : 0) + carry;
+    if (slot < n && f) p.pid[slot] = incl - 1;
+    __syncthreads();
+    if (threadIdx.x == blockDim.x - 1) carry = incl;
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) {
+    *p.n_phys = carry;
+    if (carry > p.capacity) set_err(p.status, KVS_DEVERR_CAPACITY);
+  }
+}
+
+// 6. block table + refcounts
+__global__ void dedup_table(DedupParams p) {
+  const int slot = blockIdx.x * blockDim.x + threadIdx.x;
+  if (slot >= p.n_seq * p.max_blocks) return;
+  const int r = p.rep[slot];
+  if (r < 0) {
+    p.block_table[slot] = -1;
+    return;
+  }
+  const int id = p.pid[r];
+  p.block_table[slot] = id;
+  if (id < p.capacity) atomicAdd(p.refcount + id, 1);
+}
+
+}  // namespace kvs
+
+using namespace kvs;
+
+extern "C" kvs_status kvs_fingerprint_dedup(kvs_pool* pool, const uint32_t* tokens_dev, const int64_t* seq_off_dev,
+                                            int32_t n_seq, const uint32_t* tier_dev, const int64_t* seg_off_dev,
+                                            const int32_t* seg_blocks_dev, uint64_t* fp_out_dev,
+                                            int32_t* block_table_dev, int32_t max_blocks, int32_t* refcount_dev,
+                                            int32_t* n_phys_dev, uint32_t flags, void* ws, size_t ws_bytes,
+                                            cudaStream_t stream) {
+  if (!pool) return fail(KVS_ERR_INVALID_ARG, "fingerprint_dedup: null pool");
+  if (n_seq < 0 || max_blocks < 1) return fail(KVS_ERR_INVALID_ARG, "fingerprint_dedup: bad sizes");
+  if (!seq_off_dev || !fp_out_dev || !block_table_dev || !refcount_dev || !n_phys_dev || !ws)
+    return fail(KVS_ERR_INVALID_ARG, "fingerprint_dedup: null pointer");
+  if (n_seq > 0 && !tokens_dev) return fail(KVS_ERR_INVALID_ARG, "fingerprint_dedup: null tokens");
+  if ((seg_off_dev == nullptr) != (seg_blocks_dev == nullptr))
+    return fail(KVS_ERR_INVALID_ARG, "fingerprint_dedup: seg_off and seg_blocks go together");
+  if (!aligned16(ws)) return fail(KVS_ERR_INVALID_ARG, "fingerprint_dedup: ws must be 16-byte aligned");
+  if ((long long)n_seq * max_blocks > 0x3fffffffll) return fail(KVS_ERR_CAPACITY, "fingerprint_dedup: too many slots");
+  size_t need = 0;
+  kvs_workspace_size(pool, KVS_OP_DEDUP, n_seq, max_blocks, 0, &need);
+  if (ws_bytes < need) return fail(KVS_ERR_CAPACITY, "fingerprint_dedup: workspace too small");
+  const size_t slots = (size_t)n_seq * max_blocks;
+  size_t T = 1024;
+  while (T < 2 * slots) T <<= 1;
+
+  DedupParams p{};
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  auto take = [&](size_t bytes) {
+    uint8_t* r = w;
+    w += (bytes + 255) & ~size_t(255);
+    return r;
+  };
+  p.tkeys = reinterpret_cast<unsigned long long*>(take(T * 8));
+  p.tmin = reinterpret_cast<int32_t*>(take(T * 4));
+  p.key = reinterpret_cast<uint64_t*>(take(slots * 8));
+  p.rep = reinterpret_cast<int32_t*>(take(slots * 4));
+  p.segstart = reinterpret_cast<int32_t*>(take(slots * 4));
+  p.pid = reinterpret_cast<int32_t*>(take(slots * 4));
+  p.flags = reinterpret_cast<uint32_t*>(take(16));
+  p.tokens = tokens_dev;
+  p.seq_off = seq_off_dev;
+  p.tier = tier_dev;
+  p.seg_off = seg_off_dev;
+  p.seg_blocks = seg_blocks_dev;
+  p.fp_out = fp_out_dev;
+  p.block_table = block_table_dev;
+  p.refcount = refcount_dev;
+  p.n_phys = n_phys_dev;
+  p.status = pool->status;
+  p.n_seq = n_seq;
+  p.max_blocks = max_blocks;
+  p.B = pool->desc.block_tokens;
+  p.capacity = pool->desc.capacity_blocks;
+  p.weak = (flags & KVS_DEDUP_TEST_WEAK_KEYS) ? 1 : 0;
+  p.tmask = static_cast<uint32_t>(T - 1);
+
+  if (cudaMemsetAsync(p.tkeys, 0, T * 8, stream) != cudaSuccess ||
+      cudaMemsetAsync(p.tmin, 0x7f, T * 4, stream) != cudaSuccess ||
+      cudaMemsetAsync(p.flags, 0, 16, stream) != cudaSuccess ||
+      cudaMemsetAsync(refcount_dev, 0, (size_t)pool->desc.capacity_blocks * 4, stream) != cudaSuccess)
+    return fail(KVS_ERR_CUDA, "fingerprint_dedup: memset failed");
+  if (n_seq == 0) {
+    if (cudaMemsetAsync(n_phys_dev, 0, 4, stream) != cudaSuccess) return fail(KVS_ERR_CUDA, "fingerprint_dedup: memset failed");
+    return KVS_OK;
+  }
+  const int n = static_cast<int>(slots);
+  const int tb = 256;
+  dedup_prep<<<(n_seq * 32 + tb - 1) / tb, tb, 0, stream>>>(p);
+  dedup_insert<<<(n + tb - 1) / tb, tb, 0, stream>>>(p);
+  dedup_resolve<<<(n + tb - 1) / tb, tb, 0, stream>>>(p);
+  dedup_fallback<<<(n + tb - 1) / tb, tb, 0, stream>>>(p);
+  dedup_scan<<<1, 1024, 0, stream>>>(p);
+  dedup_table<<<(n + tb - 1) / tb, tb, 0, stream>>>(p);
+  count_launch(6);
+  return check_launch("fingerprint_dedup");
+}

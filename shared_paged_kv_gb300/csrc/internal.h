@@ -1,0 +1,52 @@
+// Host-side internals of libkvs shared by the translation units.
+#pragma once
+
+#include <cstdint>
+#include <string>
+#include <vector>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "kvs.h"
+
+struct kvs_pool {
+  kvs_pool_desc desc;
+  int device = 0;
+  int num_sms = 0;
+  std::vector<void*> k, v, ksb, vsb, dk, dv;    // per-layer device slabs (not owned)
+  std::vector<CUtensorMap> tk, tv, tdk, tdv;    // TMA maps per layer
+  uint32_t* status = nullptr;                   // device status word (owned)
+  int32_t* tickets = nullptr;                   // split-K arrival counters (owned)
+  size_t n_tickets = 0;
+  int32_t* sched = nullptr;                     // persistent-kernel work counters (owned, 2 ints)
+};
+
+namespace kvs {
+
+void set_error(const std::string& msg);
+kvs_status fail(kvs_status st, const std::string& msg);
+kvs_status check_launch(const char* what);
+void count_launch(uint64_t n = 1);
+bool aligned16(const void* p);
+
+// RoPE frequency split (see common.cuh): c[piece][i] for i < head_dim/2.
+void rope_split_host(float theta, int head_dim, float out[4][64]);
+
+// Split-K plan for decode attention: blocks per CTA chunk and chunk count.
+struct AttnPlan {
+  int bpc;        // logical blocks per CTA
+  int n_chunks;   // CTAs per (sequence, kv head)
+};
+AttnPlan attn_plan(const kvs_pool* pool, int n_seq, int max_blocks);   // bf16 path
+AttnPlan q4_plan(const kvs_pool* pool, int n_seq, int max_blocks);     // Q4 path
+constexpr int kAttnWarps = 4;
+
+// Token-major persistent decode attention (query group <= 8), attn_tm.cu.
+kvs_status decode_attn_token_major(kvs_pool* pool, int layer, const void* q, int n_q_heads, const int32_t* table,
+                                   int max_blocks, const int32_t* seq_len, int n_seq, const int32_t* diff,
+                                   const int32_t* rope_off, const kvs_seg_rope* rope_segs, float theta,
+                                   float scale, float* out, void* ws, cudaStream_t stream);
+size_t tm_workspace_bytes(const kvs_pool* pool, int n_seq, int max_blocks, int g);
+constexpr int kTmMaxGroup = 8;
+
+}  // namespace kvs

@@ -1,0 +1,490 @@
+// 4-bit group-quantised (Q4G64) KV: quantiser and decode attention that reads
+// the codes directly (Q4 edge paper summary §2.1: 256-token blocks stored
+// 4-bit, ratio 0.281 => group 64 with fp16 scale and bias; §2.2: attention on
+// the Q4 tensors without a dequantise-to-FP16 pass).
+//
+// Attention design (GB300): the codes are the *A* operand of mma.sync
+// m16n8k16 with tokens (QK^T) or head dims (PV) as the 16-row M dimension and
+// the <= 8 query heads of a KV head as the 8-column N dimension, so a GQA
+// group of 4 fills half of every MMA instead of a quarter.  Codes are turned
+// into fp16 in registers with the 1024-offset trick ((nibble | 0x6400) is the
+// fp16 value 1024 + nibble; subtracting 1024 is exact), and the affine
+// dequantisation is applied around the MMAs:
+//   q.k_hat   = sum_groups  s_g * (q_g . c_g) + b_g * sum(q_g)
+//   p.v_hat   = sum_t (p_t s_g[t]) c_t + sum_t p_t b_g[t]
+// The head-dim order inside each 16-wide k-step is permuted identically for q
+// and the codes (a dot product does not depend on the order), which lets a
+// thread fetch its codes with one 8-byte shared load per row and group.  The
+// P tile is transposed into the PV B operand with movmatrix.  K/V code tiles
+// arrive by 2-D TMA (64-byte swizzle); scale/bias rows by 1-D bulk copies; a
+// 2-stage ring shared by the CTA's 4 warps (each warp takes 64 of the 256
+// tokens of every block) with full/empty mbarriers.
+#include "common.cuh"
+#include "internal.h"
+#include "merge.cuh"
+
+namespace kvs {
+
+// ------------------------------------------------------------- quantiser ---
+__global__ void q4_quantize_kernel(const uint16_t* __restrict__ src_k, const uint16_t* __restrict__ src_v,
+                                   const int32_t* __restrict__ dst_blocks, int n_blocks, int hkv, int B, int capacity,
+                                   uint8_t* __restrict__ codes_k, uint8_t* __restrict__ codes_v,
+                                   __half* __restrict__ sb_k, __half* __restrict__ sb_v, uint32_t* status) {
+  constexpr int D = 128, G = 64;
+  const long long gid = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  const long long per_tensor = (long long)n_blocks * hkv * B * (D / G);
+  if (gid >= 2 * per_tensor) return;
+  const bool is_v = gid >= per_tensor;
+  long long r = is_v ? gid - per_tensor : gid;
+  const int grp = static_cast<int>(r % (D / G));
+  r /= (D / G);
+  const long long row = r;                   // (block i, head, token) row in src
+  const int i = static_cast<int>(row / ((long long)hkv * B));
+  const long long rin = row - (long long)i * hkv * B;
+  const int phys = dst_blocks[i];
+  if (phys < 0 || phys >= capacity) {
+    set_err(status, KVS_DEVERR_BLOCK_ID);
+    return;
+  }
+  const uint16_t* x = (is_v ? src_v : src_k) + row * D + grp * G;
+  float v[G];
+#pragma unroll
+  for (int j = 0; j < G / 8; ++j) {
+    const uint4 w = __ldg(reinterpret_cast<const uint4*>(x) + j);
+    const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      v[j * 8 + 2 * e] = bf16_lo(ws[e]);
+      v[j * 8 + 2 * e + 1] = bf16_hi(ws[e]);
+    }
+  }
+  float mn = v[0], mx = v[0];
+#pragma unroll
+  for (int j = 1; j < G; ++j) {
+    mn = fminf(mn, v[j]);
+    mx = fmaxf(mx, v[j]);
+  }
+  const __half s16 = __float2half_rn(__fdiv_rn(__fsub_rn(mx, mn), 15.0f));
+  const __half b16 = __float2half_rn(mn);
+  const float s = __half2float(s16), b = __half2float(b16);
+  uint32_t packed[G / 8];
+#pragma unroll
+  for (int j = 0; j < G / 8; ++j) {
+    uint32_t wv = 0;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      float cq = 0.f;
+      if (s != 0.f) cq = rintf(__fdiv_rn(__fsub_rn(v[j * 8 + e], b), s));
+      cq = fminf(fmaxf(cq, 0.f), 15.f);
+      wv |= (static_cast<uint32_t>(cq) & 15u) << (4 * e);
+    }
+    packed[j] = wv;
+  }
+  const long long drow = (long long)phys * hkv * B + rin;
+  uint8_t* cd = (is_v ? codes_v : codes_k) + drow * (D / 2) + grp * (G / 2);
+  reinterpret_cast<uint4*>(cd)[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+  reinterpret_cast<uint4*>(cd)[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
+  __half2 sbv = __halves2half2(s16, b16);
+  reinterpret_cast<__half2*>((is_v ? sb_v : sb_k) + (drow * (D / G) + grp) * 2)[0] = sbv;
+}
+
+// ------------------------------------------------------------- attention ---
+struct Q4Params {
+  const uint16_t* q;          // bf16 [n_seq][hq][128]
+  const int32_t* block_table; // [n_seq][max_blocks]
+  const int32_t* seq_len;
+  const uint8_t* ksb;         // fp16 scale/bias slab of this layer, 8 bytes per token-head
+  const uint8_t* vsb;
+  float* out;
+  float* part;
+  float* part_ml;
+  int32_t* tickets;
+  uint32_t* status;
+  int max_blocks, n_seq, hkv, g, hq, bpc, n_chunks, capacity;
+  float scale_log2;
+};
+
+constexpr int kQ4B = 256, kQ4D = 128, kQ4Stages = 2;
+constexpr int kQ4Codes = kQ4B * kQ4D / 2;       // 16 KB per K or V tile
+constexpr int kQ4Sb = kQ4B * 8;                 // 2 KB scale/bias per tile
+constexpr int kQ4Stage = 2 * kQ4Codes + 2 * kQ4Sb;
+constexpr int kQ4Smem = 1024 + kQ4Stages * kQ4Stage;
+
+__device__ __forceinline__ uint32_t movmatrix_t(uint32_t x) {
+  uint32_t y;
+  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
+  return y;
+}
+
+// two nibbles (bits [0,4) and [16,20) after the shift) -> fp16x2 exact codes
+__device__ __forceinline__ uint32_t nib2h(uint32_t w) {
+  const uint32_t m = (w & 0x000F000Fu) | 0x64006400u;
+  const __half2 r = __hsub2(*reinterpret_cast<const __half2*>(&m), __half2(__ushort_as_half(0x6400), __ushort_as_half(0x6400)));
+  return *reinterpret_cast<const uint32_t*>(&r);
+}
+
+__global__ void __launch_bounds__(128, 2)
+q4_attn_kernel(const __grid_constant__ Q4Params p, const __grid_constant__ CUtensorMap tk,
+               const __grid_constant__ CUtensorMap tv) {
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ uint64_t full[kQ4Stages], empty[kQ4Stages];
+  __shared__ int s_last;
+  __shared__ float sM[16], sL[16];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int g = lane >> 2, c = lane & 3;
+  int bid = blockIdx.x;
+  const int a = bid % p.n_seq;
+  bid /= p.n_seq;
+  const int h = bid % p.hkv;
+  const int chunk = bid / p.hkv;
+
+  int L = p.seq_len[a];
+  if (L < 0 || L > p.max_blocks * kQ4B) {
+    if (threadIdx.x == 0 && chunk == 0) set_err(p.status, KVS_DEVERR_SEQ_LEN);
+    L = L < 0 ? 0 : p.max_blocks * kQ4B;
+  }
+  const int nblk = (L + kQ4B - 1) / kQ4B;
+  const int nch = (nblk + p.bpc - 1) / p.bpc;
+  if (nblk == 0) {
+    if (chunk == 0)
+      for (int i = threadIdx.x; i < p.g * kQ4D; i += blockDim.x) p.out[((size_t)a * p.hq + h * p.g) * kQ4D + i] = 0.f;
+    return;
+  }
+  if (chunk >= nch) return;
+  const int b0 = chunk * p.bpc;
+  const int n_mine = min(p.bpc, nblk - b0);
+  uint8_t* base = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  const int32_t* trow = p.block_table + (size_t)a * p.max_blocks;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kQ4Stages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], kAttnWarps);
+    }
+    fence_barrier_init();
+  }
+  __syncthreads();
+
+  auto issue = [&](int i, int s) {
+    uint64_t* bar = &full[s];
+    const int phys = __ldg(trow + b0 + i);
+    if (phys < 0 || phys >= p.capacity) {
+      set_err(p.status, KVS_DEVERR_BLOCK_ID);
+      mbar_arrive(bar);
+      return;
+    }
+    mbar_arrive_expect_tx(bar, kQ4Stage);
+    uint8_t* st = base + s * kQ4Stage;
+    const int row = (phys * p.hkv + h) * kQ4B;
+    tma_load_2d(st, &tk, 0, row, bar);
+    tma_load_2d(st + kQ4Codes, &tv, 0, row, bar);
+    bulk_load(st + 2 * kQ4Codes, p.ksb + (size_t)row * 8, kQ4Sb, bar);
+    bulk_load(st + 2 * kQ4Codes + kQ4Sb, p.vsb + (size_t)row * 8, kQ4Sb, bar);
+  };
+  if (threadIdx.x == 0)
+    for (int i = 0; i < kQ4Stages && i < n_mine; ++i) issue(i, i);
+
+  // ---- query as the B operand (k = head dim, n = query head), fp16, with the
+  // k-order permutation shared with the code loads; plus per-group sums.
+  const int G_ = p.g;
+  const uint16_t* qbase = p.q + ((size_t)a * p.hq + h * G_) * kQ4D;
+  uint32_t qb[2][4][2];
+  float qs[2][2];   // [group][column 2c / 2c+1]
+  {
+    const bool ok = g < G_;
+#pragma unroll
+    for (int grp = 0; grp < 2; ++grp) {
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int d0 = grp * 64 + 16 * c + 8 * (j >> 1) + 2 * (j & 1);
+        // pair A: nibbles (2sub, 2sub+4) -> d0, d0+4 ; pair B: d0+1, d0+5
+        float x0 = 0.f, x1 = 0.f, x2 = 0.f, x3 = 0.f;
+        if (ok) {
+          x0 = __uint_as_float((uint32_t)qbase[g * kQ4D + d0] << 16);
+          x1 = __uint_as_float((uint32_t)qbase[g * kQ4D + d0 + 4] << 16);
+          x2 = __uint_as_float((uint32_t)qbase[g * kQ4D + d0 + 1] << 16);
+          x3 = __uint_as_float((uint32_t)qbase[g * kQ4D + d0 + 5] << 16);
+        }
+        qb[grp][j][0] = pack_f16(x0, x1);
+        qb[grp][j][1] = pack_f16(x2, x3);
+      }
+#pragma unroll
+      for (int cc = 0; cc < 2; ++cc) {
+        const int r = 2 * c + cc;
+        float sum = 0.f;
+        if (r < G_)
+          for (int d = 0; d < 64; ++d)
+            sum += __half2float(__float2half_rn(__uint_as_float((uint32_t)qbase[r * kQ4D + grp * 64 + d] << 16)));
+        qs[grp][cc] = sum;
+      }
+    }
+  }
+
+  float m[2] = {-INFINITY, -INFINITY}, l[2] = {0.f, 0.f};
+  float acc[8][4];
+  float corr[2][2] = {{0.f, 0.f}, {0.f, 0.f}};
+#pragma unroll
+  for (int i = 0; i < 8; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
+
+  bool timed_out = false;
+  for (int i = 0; i < n_mine; ++i) {
+    const int s = i % kQ4Stages;
+    if (!mbar_wait_bounded(&full[s], (i / kQ4Stages) & 1, p.status)) {
+      timed_out = true;
+      break;
+    }
+    const int b = b0 + i;
+    const int phys = __ldg(trow + b);
+    const int nv = min(kQ4B, L - b * kQ4B);
+    const int tw = warp * 64;   // this warp's first token in the block
+    if (phys >= 0 && phys < p.capacity && tw < nv) {
+      const uint8_t* kc = base + s * kQ4Stage;
+      const uint8_t* vc = kc + kQ4Codes;
+      const uint8_t* ksb = kc + 2 * kQ4Codes;
+      const uint8_t* vsb = ksb + kQ4Sb;
+      float sc[4][4];
+#pragma unroll
+      for (int mt = 0; mt < 4; ++mt) {
+        const int t0 = tw + 16 * mt + g, t1 = t0 + 8;
+        float cg[2][4];
+#pragma unroll
+        for (int grp = 0; grp < 2; ++grp) {
+          cg[grp][0] = cg[grp][1] = cg[grp][2] = cg[grp][3] = 0.f;
+          const uint2 w0 = *reinterpret_cast<const uint2*>(kc + swz64(t0 * 64 + 32 * grp + 8 * c));
+          const uint2 w1 = *reinterpret_cast<const uint2*>(kc + swz64(t1 * 64 + 32 * grp + 8 * c));
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const uint32_t r0 = (j >> 1) ? w0.y : w0.x;
+            const uint32_t r1 = (j >> 1) ? w1.y : w1.x;
+            const int sh = 8 * (j & 1);
+            mma_f16(cg[grp], nib2h(r0 >> sh), nib2h(r1 >> sh), nib2h(r0 >> (sh + 4)), nib2h(r1 >> (sh + 4)),
+                    qb[grp][j][0], qb[grp][j][1]);
+          }
+        }
+        const uint2 sb0 = *reinterpret_cast<const uint2*>(ksb + t0 * 8);
+        const uint2 sb1 = *reinterpret_cast<const uint2*>(ksb + t1 * 8);
+        const float2 g00 = __half22float2(*reinterpret_cast<const __half2*>(&sb0.x));   // (s, b) group 0, t0
+        const float2 g01 = __half22float2(*reinterpret_cast<const __half2*>(&sb0.y));   // group 1, t0
+        const float2 g10 = __half22float2(*reinterpret_cast<const __half2*>(&sb1.x));
+        const float2 g11 = __half22float2(*reinterpret_cast<const __half2*>(&sb1.y));
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int cc = e & 1;
+          const float2 s0 = (e < 2) ? g00 : g10;
+          const float2 s1 = (e < 2) ? g01 : g11;
+          float x = s0.x * cg[0][e] + s0.y * qs[0][cc] + s1.x * cg[1][e] + s1.y * qs[1][cc];
+          const int tok = (e < 2) ? t0 : t1;
+          sc[mt][e] = tok < nv ? x * p.scale_log2 : -INFINITY;
+        }
+      }
+      // online softmax over this warp's 64 tokens, per query column
+      float mx[2] = {-INFINITY, -INFINITY};
+#pragma unroll
+      for (int mt = 0; mt < 4; ++mt) {
+        mx[0] = fmaxf(mx[0], fmaxf(sc[mt][0], sc[mt][2]));
+        mx[1] = fmaxf(mx[1], fmaxf(sc[mt][1], sc[mt][3]));
+      }
+#pragma unroll
+      for (int o = 4; o < 32; o <<= 1) {
+        mx[0] = fmaxf(mx[0], __shfl_xor_sync(0xffffffffu, mx[0], o));
+        mx[1] = fmaxf(mx[1], __shfl_xor_sync(0xffffffffu, mx[1], o));
+      }
+      float al[2];
+#pragma unroll
+      for (int cc = 0; cc < 2; ++cc) {
+        const float mn = fmaxf(m[cc], mx[cc]);
+        al[cc] = fast_exp2(m[cc] - mn);
+        m[cc] = mn;
+        l[cc] *= al[cc];
+        corr[0][cc] *= al[cc];
+        corr[1][cc] *= al[cc];
+      }
+#pragma unroll
+      for (int i2 = 0; i2 < 8; ++i2) {
+        acc[i2][0] *= al[0]; acc[i2][1] *= al[1];
+        acc[i2][2] *= al[0]; acc[i2][3] *= al[1];
+      }
+#pragma unroll
+      for (int mt = 0; mt < 4; ++mt) {
+        const int t0 = tw + 16 * mt + g, t1 = t0 + 8;
+        float pv[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) pv[e] = fast_exp2(sc[mt][e] - m[e & 1]);
+        l[0] += pv[0] + pv[2];
+        l[1] += pv[1] + pv[3];
+        const uint2 sb0 = *reinterpret_cast<const uint2*>(vsb + t0 * 8);
+        const uint2 sb1 = *reinterpret_cast<const uint2*>(vsb + t1 * 8);
+        const float2 v00 = __half22float2(*reinterpret_cast<const __half2*>(&sb0.x));
+        const float2 v01 = __half22float2(*reinterpret_cast<const __half2*>(&sb0.y));
+        const float2 v10 = __half22float2(*reinterpret_cast<const __half2*>(&sb1.x));
+        const float2 v11 = __half22float2(*reinterpret_cast<const __half2*>(&sb1.y));
+        // B operands (k = token, n = query head) per group, via transposition
+        uint32_t bb[2][2];
+        bb[0][0] = movmatrix_t(pack_f16(pv[0] * v00.x, pv[1] * v00.x));
+        bb[0][1] = movmatrix_t(pack_f16(pv[2] * v10.x, pv[3] * v10.x));
+        bb[1][0] = movmatrix_t(pack_f16(pv[0] * v01.x, pv[1] * v01.x));
+        bb[1][1] = movmatrix_t(pack_f16(pv[2] * v11.x, pv[3] * v11.x));
+        corr[0][0] += pv[0] * v00.y + pv[2] * v10.y;
+        corr[0][1] += pv[1] * v00.y + pv[3] * v10.y;
+        corr[1][0] += pv[0] * v01.y + pv[2] * v11.y;
+        corr[1][1] += pv[1] * v01.y + pv[3] * v11.y;
+        // A operand: V codes, m = head dim (permuted), k = token
+        const int tb = tw + 16 * mt;
+        const int tr[4] = {tb + 2 * c, tb + 2 * c + 1, tb + 2 * c + 8, tb + 2 * c + 9};
+#pragma unroll
+        for (int grp = 0; grp < 2; ++grp) {
+          uint32_t wv[4];
+#pragma unroll
+          for (int u = 0; u < 4; ++u) wv[u] = *reinterpret_cast<const uint32_t*>(vc + swz64(tr[u] * 64 + 32 * grp + 4 * g));
+#pragma unroll
+          for (int lm = 0; lm < 4; ++lm) {
+            const uint32_t sel = (uint32_t)lm | ((uint32_t)(4 + lm) << 8);
+            const uint32_t x01 = __byte_perm(wv[0], wv[1], sel);
+            const uint32_t x89 = __byte_perm(wv[2], wv[3], sel);
+            mma_f16(acc[grp * 4 + lm], nib2h(x01), nib2h(x01 >> 4), nib2h(x89), nib2h(x89 >> 4), bb[grp][0],
+                    bb[grp][1]);
+          }
+        }
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[s]);
+    if (threadIdx.x == 0 && i + kQ4Stages < n_mine) {
+      if (!mbar_wait_bounded(&empty[s], (i / kQ4Stages) & 1, p.status)) {
+        timed_out = true;
+      } else {
+        fence_proxy_async_smem();
+        issue(i + kQ4Stages, s);
+      }
+    }
+    if (__shfl_sync(0xffffffffu, timed_out ? 1 : 0, 0)) break;
+  }
+  if (timed_out) {
+    m[0] = m[1] = -INFINITY;
+    l[0] = l[1] = 0.f;
+  }
+  // reduce l and the bias corrections over the 8 token lanes of each column
+#pragma unroll
+  for (int o = 4; o < 32; o <<= 1) {
+#pragma unroll
+    for (int cc = 0; cc < 2; ++cc) {
+      l[cc] += __shfl_xor_sync(0xffffffffu, l[cc], o);
+      corr[0][cc] += __shfl_xor_sync(0xffffffffu, corr[0][cc], o);
+      corr[1][cc] += __shfl_xor_sync(0xffffffffu, corr[1][cc], o);
+    }
+  }
+  const size_t sidx = (((size_t)a * p.hkv + h) * p.n_chunks + chunk) * kAttnWarps + warp;
+  float* pr = p.part + sidx * G_ * kQ4D;
+#pragma unroll
+  for (int cc = 0; cc < 2; ++cc) {
+    const int r = 2 * c + cc;
+    if (r >= G_) continue;
+#pragma unroll
+    for (int grp = 0; grp < 2; ++grp) {
+#pragma unroll
+      for (int lm = 0; lm < 4; ++lm) {
+        const int d0 = grp * 64 + 8 * g + 2 * lm;
+        __stcg(reinterpret_cast<float2*>(pr + r * kQ4D + d0),
+               make_float2(acc[grp * 4 + lm][cc] + corr[grp][cc], acc[grp * 4 + lm][2 + cc] + corr[grp][cc]));
+      }
+    }
+    if (g == 0) __stcg(reinterpret_cast<float2*>(p.part_ml + (sidx * G_ + r) * 2), make_float2(m[cc], l[cc]));
+  }
+  if (!arrive_last(p.tickets + a * p.hkv + h, nch, &s_last)) return;
+  const size_t s0 = ((size_t)a * p.hkv + h) * p.n_chunks * kAttnWarps;
+  merge_splits<kQ4D>(p.part, p.part_ml, s0, nch * kAttnWarps, G_, p.out + ((size_t)a * p.hq + h * G_) * kQ4D, sM, sL);
+}
+
+AttnPlan q4_plan(const kvs_pool* pool, int n_seq, int max_blocks) {
+  const long long work = (long long)n_seq * pool->desc.num_kv_heads * max_blocks;
+  const long long target = (long long)pool->num_sms * 8;
+  long long bpc = (work + target - 1) / target;
+  if (bpc < 1) bpc = 1;
+  if (bpc > 64) bpc = 64;
+  AttnPlan pl;
+  pl.bpc = static_cast<int>(bpc);
+  pl.n_chunks = (max_blocks + pl.bpc - 1) / pl.bpc;
+  if (pl.n_chunks < 1) pl.n_chunks = 1;
+  return pl;
+}
+
+}  // namespace kvs
+
+using namespace kvs;
+
+extern "C" kvs_status kvs_quantize_q4(kvs_pool* pool, int32_t layer, const void* k_src_dev, const void* v_src_dev,
+                                      const int32_t* dst_blocks_dev, int32_t n_blocks, cudaStream_t stream) {
+  if (!pool) return fail(KVS_ERR_INVALID_ARG, "quantize_q4: null pool");
+  const kvs_pool_desc& d = pool->desc;
+  if (d.dtype != KVS_DTYPE_Q4G64) return fail(KVS_ERR_INVALID_ARG, "quantize_q4: pool is not Q4G64");
+  if (layer < 0 || layer >= d.num_layers) return fail(KVS_ERR_INVALID_ARG, "quantize_q4: layer out of range");
+  if (n_blocks < 0) return fail(KVS_ERR_INVALID_ARG, "quantize_q4: n_blocks < 0");
+  if (n_blocks == 0) return KVS_OK;
+  if (!k_src_dev || !v_src_dev || !dst_blocks_dev) return fail(KVS_ERR_INVALID_ARG, "quantize_q4: null pointer");
+  if (!aligned16(k_src_dev) || !aligned16(v_src_dev)) return fail(KVS_ERR_INVALID_ARG, "quantize_q4: sources must be 16-byte aligned");
+  const long long threads = 2ll * n_blocks * d.num_kv_heads * d.block_tokens * (d.head_dim / 64);
+  const int tb = 128;
+  q4_quantize_kernel<<<(unsigned)((threads + tb - 1) / tb), tb, 0, stream>>>(
+      static_cast<const uint16_t*>(k_src_dev), static_cast<const uint16_t*>(v_src_dev), dst_blocks_dev, n_blocks,
+      d.num_kv_heads, d.block_tokens, d.capacity_blocks, static_cast<uint8_t*>(pool->k[layer]),
+      static_cast<uint8_t*>(pool->v[layer]), static_cast<__half*>(pool->ksb[layer]), static_cast<__half*>(pool->vsb[layer]),
+      pool->status);
+  count_launch();
+  return check_launch("quantize_q4");
+}
+
+extern "C" kvs_status kvs_decode_attn_q4(kvs_pool* pool, int32_t layer, const void* q_dev, int32_t n_q_heads,
+                                         const int32_t* block_table_dev, int32_t max_blocks, const int32_t* seq_len_dev,
+                                         int32_t n_seq, float scale, float* out_dev, void* ws, size_t ws_bytes,
+                                         cudaStream_t stream) {
+  if (!pool) return fail(KVS_ERR_INVALID_ARG, "decode_attn_q4: null pool");
+  const kvs_pool_desc& d = pool->desc;
+  if (d.dtype != KVS_DTYPE_Q4G64) return fail(KVS_ERR_INVALID_ARG, "decode_attn_q4: pool is not Q4G64");
+  if (layer < 0 || layer >= d.num_layers) return fail(KVS_ERR_INVALID_ARG, "decode_attn_q4: layer out of range");
+  if (n_seq < 0 || n_seq > d.max_seqs) return fail(KVS_ERR_CAPACITY, "decode_attn_q4: n_seq exceeds the pool's max_seqs");
+  if (n_seq == 0) return KVS_OK;
+  if (!q_dev || !block_table_dev || !seq_len_dev || !out_dev || !ws)
+    return fail(KVS_ERR_INVALID_ARG, "decode_attn_q4: null pointer");
+  if (!aligned16(q_dev) || !aligned16(out_dev) || !aligned16(ws))
+    return fail(KVS_ERR_INVALID_ARG, "decode_attn_q4: q, out and ws must be 16-byte aligned");
+  if (max_blocks < 1) return fail(KVS_ERR_INVALID_ARG, "decode_attn_q4: max_blocks must be >= 1");
+  if (n_q_heads < 1 || n_q_heads % d.num_kv_heads) return fail(KVS_ERR_INVALID_ARG, "decode_attn_q4: n_q_heads must be a multiple of num_kv_heads");
+  const int g = n_q_heads / d.num_kv_heads;
+  if (g > 8) return fail(KVS_ERR_UNSUPPORTED, "decode_attn_q4: more than 8 query heads per KV head");
+  const AttnPlan plan = q4_plan(pool, n_seq, max_blocks);
+  size_t need = 0;
+  kvs_workspace_size(pool, KVS_OP_DECODE_ATTN_Q4, n_seq, max_blocks, n_q_heads, &need);
+  if (ws_bytes < need) return fail(KVS_ERR_CAPACITY, "decode_attn_q4: workspace too small");
+  const long long grid = (long long)n_seq * d.num_kv_heads * plan.n_chunks;
+  if (grid > 0x7fffffffll) return fail(KVS_ERR_CAPACITY, "decode_attn_q4: grid too large");
+  Q4Params prm{};
+  prm.q = static_cast<const uint16_t*>(q_dev);
+  prm.block_table = block_table_dev;
+  prm.seq_len = seq_len_dev;
+  prm.ksb = static_cast<const uint8_t*>(pool->ksb[layer]);
+  prm.vsb = static_cast<const uint8_t*>(pool->vsb[layer]);
+  prm.out = out_dev;
+  const size_t splits = (size_t)n_seq * d.num_kv_heads * plan.n_chunks * kAttnWarps;
+  prm.part = static_cast<float*>(ws);
+  prm.part_ml = prm.part + splits * g * kQ4D;
+  prm.tickets = pool->tickets;
+  prm.status = pool->status;
+  prm.max_blocks = max_blocks;
+  prm.n_seq = n_seq;
+  prm.hkv = d.num_kv_heads;
+  prm.g = g;
+  prm.hq = n_q_heads;
+  prm.bpc = plan.bpc;
+  prm.n_chunks = plan.n_chunks;
+  prm.capacity = d.capacity_blocks;
+  prm.scale_log2 = scale * 1.4426950408889634f;
+  static bool attr_set = false;
+  if (!attr_set) {
+    if (cudaFuncSetAttribute(q4_attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kQ4Smem) != cudaSuccess)
+      return fail(KVS_ERR_CUDA, "decode_attn_q4: cannot raise the shared-memory limit");
+    attr_set = true;
+  }
+  q4_attn_kernel<<<(int)grid, 128, kQ4Smem, stream>>>(prm, pool->tk[layer], pool->tv[layer]);
+  count_launch();
+  return check_launch("decode_attn_q4");
+}

@@ -1,0 +1,118 @@
+// Batched RoPE re-rotation of reused K blocks (INMS walkthrough §3.2: a
+// block stored from p_s and reused at p_t is rotated by an angle depending
+// only on p_t - p_s; V untouched; TokenDance summary section 2: one batched
+// RoPE call per layer for the whole group of requests).
+//
+// Rotate-half pairing (i, i + d/2), frequency theta^(-2i/d); the per-job
+// cos/sin table (d/2 entries) is built once per CTA in shared memory with the
+// Cody-Waite reduced evaluation of common.cuh.  One CTA = one job x 16 tokens;
+// threads stream 16-byte vectors of the low and high halves (coalesced
+// 128-byte runs per token-head), rotate in fp32, round to bf16 (RNE).
+#include "common.cuh"
+#include "internal.h"
+
+namespace kvs {
+
+struct RopeParams {
+  uint16_t* slab;             // this layer's K slab, bf16 [cap][hkv][B][D]
+  const int4* jobs;           // pairs of int4: (src_row, src_tok0, dst_row, dst_tok0), (n_tok, src_pos, dst_pos, -)
+  const int32_t* src_table;
+  const int32_t* dst_table;
+  uint32_t* status;
+  int n_jobs, max_blocks, hkv, B, capacity, tok_per_cta;
+  RopeSplit rs;
+};
+
+template <int D>
+__global__ void __launch_bounds__(128) rope_rerotate_kernel(const __grid_constant__ RopeParams p) {
+  constexpr int VEC = 8;                 // bf16 per 16-byte vector
+  constexpr int NV = D / 2 / VEC;        // vectors per half row
+  __shared__ float cs[D / 2], sn[D / 2];
+  const int job = blockIdx.x;
+  const int4 j0 = p.jobs[2 * job], j1 = p.jobs[2 * job + 1];
+  const int n_tok = j1.x;
+  const int t0 = blockIdx.y * p.tok_per_cta;
+  if (t0 >= n_tok) return;
+  const int delta = j1.z - j1.y;
+  if (delta <= -(1 << 18) || delta >= (1 << 18)) {
+    if (threadIdx.x == 0) set_err(p.status, KVS_DEVERR_ROPE_RANGE);
+    return;
+  }
+  for (int i = threadIdx.x; i < D / 2; i += blockDim.x) rope_cos_sin(p.rs, i, delta, cs[i], sn[i]);
+  __syncthreads();
+  const int t1 = min(n_tok, t0 + p.tok_per_cta);
+  const int items = (t1 - t0) * p.hkv * NV;
+  for (int it = threadIdx.x; it < items; it += blockDim.x) {
+    const int v = it % NV;
+    const int rest = it / NV;
+    const int h = rest % p.hkv;
+    const int t = t0 + rest / p.hkv;
+    const int ts = j0.y + t, td = j0.w + t;
+    if (ts < 0 || td < 0 || ts / p.B >= p.max_blocks || td / p.B >= p.max_blocks) {
+      set_err(p.status, KVS_DEVERR_JOB);
+      continue;
+    }
+    const int ps = p.src_table[(size_t)j0.x * p.max_blocks + ts / p.B];
+    const int pd = p.dst_table[(size_t)j0.z * p.max_blocks + td / p.B];
+    if (ps < 0 || ps >= p.capacity || pd < 0 || pd >= p.capacity) {
+      set_err(p.status, KVS_DEVERR_BLOCK_ID);
+      continue;
+    }
+    const size_t rs = (((size_t)ps * p.hkv + h) * p.B + ts % p.B) * D;
+    const size_t rd = (((size_t)pd * p.hkv + h) * p.B + td % p.B) * D;
+    const uint4 lo = __ldg(reinterpret_cast<const uint4*>(p.slab + rs + v * VEC));
+    const uint4 hi = __ldg(reinterpret_cast<const uint4*>(p.slab + rs + D / 2 + v * VEC));
+    const uint32_t lw[4] = {lo.x, lo.y, lo.z, lo.w};
+    const uint32_t hw[4] = {hi.x, hi.y, hi.z, hi.w};
+    uint32_t ol[4], oh[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int i0 = v * VEC + 2 * e;
+      const float a0 = bf16_lo(lw[e]), a1 = bf16_hi(lw[e]);
+      const float b0 = bf16_lo(hw[e]), b1 = bf16_hi(hw[e]);
+      ol[e] = pack_bf16(a0 * cs[i0] - b0 * sn[i0], a1 * cs[i0 + 1] - b1 * sn[i0 + 1]);
+      oh[e] = pack_bf16(b0 * cs[i0] + a0 * sn[i0], b1 * cs[i0 + 1] + a1 * sn[i0 + 1]);
+    }
+    *reinterpret_cast<uint4*>(p.slab + rd + v * VEC) = make_uint4(ol[0], ol[1], ol[2], ol[3]);
+    *reinterpret_cast<uint4*>(p.slab + rd + D / 2 + v * VEC) = make_uint4(oh[0], oh[1], oh[2], oh[3]);
+  }
+}
+
+}  // namespace kvs
+
+using namespace kvs;
+
+extern "C" kvs_status kvs_rope_rerotate(kvs_pool* pool, int32_t layer, const kvs_rope_job* jobs_dev, int32_t n_jobs,
+                                        int32_t max_job_tokens, float theta, const int32_t* src_table_dev,
+                                        const int32_t* dst_table_dev, int32_t max_blocks, cudaStream_t stream) {
+  if (!pool) return fail(KVS_ERR_INVALID_ARG, "rope_rerotate: null pool");
+  const kvs_pool_desc& d = pool->desc;
+  if (d.dtype != KVS_DTYPE_BF16) return fail(KVS_ERR_INVALID_ARG, "rope_rerotate: bf16 pools only");
+  if (layer < 0 || layer >= d.num_layers) return fail(KVS_ERR_INVALID_ARG, "rope_rerotate: layer out of range");
+  if (n_jobs < 0 || max_job_tokens < 0 || max_blocks < 1) return fail(KVS_ERR_INVALID_ARG, "rope_rerotate: bad sizes");
+  if (!(theta > 0.f)) return fail(KVS_ERR_INVALID_ARG, "rope_rerotate: theta must be positive");
+  if (n_jobs == 0 || max_job_tokens == 0) return KVS_OK;
+  if (!jobs_dev || !src_table_dev || !dst_table_dev) return fail(KVS_ERR_INVALID_ARG, "rope_rerotate: null pointer");
+  if (!aligned16(jobs_dev)) return fail(KVS_ERR_INVALID_ARG, "rope_rerotate: jobs must be 16-byte aligned");
+  RopeParams p{};
+  p.slab = static_cast<uint16_t*>(pool->k[layer]);
+  p.jobs = reinterpret_cast<const int4*>(jobs_dev);
+  p.src_table = src_table_dev;
+  p.dst_table = dst_table_dev;
+  p.status = pool->status;
+  p.n_jobs = n_jobs;
+  p.max_blocks = max_blocks;
+  p.hkv = d.num_kv_heads;
+  p.B = d.block_tokens;
+  p.capacity = d.capacity_blocks;
+  p.tok_per_cta = 16;
+  rope_split_host(theta, d.head_dim, p.rs.c);
+  dim3 grid(n_jobs, (max_job_tokens + p.tok_per_cta - 1) / p.tok_per_cta);
+  if (grid.y > 65535) return fail(KVS_ERR_CAPACITY, "rope_rerotate: max_job_tokens too large");
+  if (d.head_dim == 128)
+    rope_rerotate_kernel<128><<<grid, 128, 0, stream>>>(p);
+  else
+    rope_rerotate_kernel<64><<<grid, 128, 0, stream>>>(p);
+  count_launch();
+  return check_launch("rope_rerotate");
+}

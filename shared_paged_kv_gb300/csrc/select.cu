@@ -1,0 +1,179 @@
+// Critical-position selection by K difference (TokenDance summary, section 2:
+// at check layers one batched difference computation finds, per request, the
+// positions whose cached and newly computed K differ most).
+//
+// Pass 1 (HBM-bound): one warp per position row streams both bf16 rows with
+// 16-byte loads and reduces sum((a-b)^2) in fp32 — the squared L2 norm, whose
+// order equals the norm's.  Pass 2: one CTA per agent finds the k-th largest
+// score by a 4 x 8-bit radix select on the float bits (scores are >= 0, so
+// the bit pattern orders them), then emits, in ascending position order, every
+// position above the threshold and the lowest-positioned ones equal to it.
+#include "common.cuh"
+#include "internal.h"
+
+namespace kvs {
+
+// Rows beyond the score buffer (cap_rows) are never read or written.
+__device__ __forceinline__ int agent_rows(const int64_t* row_off, int a, long long cap_rows) {
+  long long r0 = row_off[a], r1 = row_off[a + 1];
+  if (r0 < 0) r0 = 0;
+  if (r1 > cap_rows) r1 = cap_rows;
+  return r1 > r0 ? static_cast<int>(r1 - r0) : 0;
+}
+
+__global__ void sel_scores(const uint16_t* __restrict__ kc, const uint16_t* __restrict__ kn,
+                           const int64_t* __restrict__ row_off, int n_agents, int row_elems,
+                           long long cap_rows, float* __restrict__ scores) {
+  const long long row = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (row >= row_off[n_agents] || row >= cap_rows) return;
+  const uint4* a = reinterpret_cast<const uint4*>(kc + row * row_elems);
+  const uint4* b = reinterpret_cast<const uint4*>(kn + row * row_elems);
+  float acc = 0.f;
+  for (int v = lane; v < row_elems / 8; v += 32) {
+    const uint4 x = __ldg(a + v), y = __ldg(b + v);
+    const uint32_t xs[4] = {x.x, x.y, x.z, x.w}, ys[4] = {y.x, y.y, y.z, y.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float d0 = bf16_lo(xs[e]) - bf16_lo(ys[e]);
+      const float d1 = bf16_hi(xs[e]) - bf16_hi(ys[e]);
+      acc = fmaf(d0, d0, acc);
+      acc = fmaf(d1, d1, acc);
+    }
+  }
+#pragma unroll
+  for (int o = 16; o; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+  if (lane == 0) scores[row] = acc;
+}
+
+__device__ __forceinline__ int count_for(float ratio, int n) {
+  double k = ceil(static_cast<double>(ratio) * static_cast<double>(n));
+  if (k < 0) k = 0;
+  if (k > n) k = n;
+  return static_cast<int>(k);
+}
+
+__device__ __forceinline__ int block_exclusive_scan(int x, int* warp_sums, int& total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int incl = x;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  if (lane == 31) warp_sums[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    int w = lane < (int)(blockDim.x >> 5) ? warp_sums[lane] : 0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, w, o);
+      if (lane >= o) w += y;
+    }
+    warp_sums[lane] = w;
+  }
+  __syncthreads();
+  const int res = incl - x + (warp ? warp_sums[warp - 1] : 0);
+  total = warp_sums[(blockDim.x >> 5) - 1];
+  __syncthreads();
+  return res;
+}
+
+__global__ void __launch_bounds__(1024) sel_topk(const float* __restrict__ scores, const int64_t* __restrict__ row_off,
+                                                 int n_agents, float ratio, long long cap_rows,
+                                                 int32_t* __restrict__ idx_out, int64_t* __restrict__ idx_off) {
+  __shared__ unsigned hist[256];
+  __shared__ int warp_sums[32];
+  __shared__ unsigned s_prefix;
+  __shared__ int s_remaining;
+  const int a = blockIdx.x;
+  const int64_t r0 = row_off[a];
+  const int n = agent_rows(row_off, a, cap_rows);
+  const int k = count_for(ratio, n);
+  // exclusive prefix of k over agents
+  if (threadIdx.x == 0) {
+    int64_t o = 0;
+    for (int b = 0; b < a; ++b) o += count_for(ratio, agent_rows(row_off, b, cap_rows));
+    idx_off[a] = o;
+    if (a == n_agents - 1) idx_off[n_agents] = o + k;
+    s_prefix = 0u;
+    s_remaining = k;
+  }
+  __syncthreads();
+  const int64_t out0 = idx_off[a];
+  if (k == 0) return;
+  const unsigned* sb = reinterpret_cast<const unsigned*>(scores + r0);
+  // radix select of the k-th largest bit pattern, 8 bits at a time from the top
+  unsigned mask = 0u;
+  for (int shift = 24; shift >= 0; shift -= 8) {
+    for (int i = threadIdx.x; i < 256; i += blockDim.x) hist[i] = 0u;
+    __syncthreads();
+    const unsigned pre = s_prefix;
+    for (int i = threadIdx.x; i < n; i += blockDim.x) {
+      const unsigned v = sb[i];
+      if ((v & mask) == pre) atomicAdd(&hist[(v >> shift) & 255u], 1u);
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      int rem = s_remaining;
+      int digit = 255;
+      for (; digit > 0; --digit) {
+        if ((int)hist[digit] >= rem) break;
+        rem -= hist[digit];
+      }
+      s_prefix = pre | ((unsigned)digit << shift);
+      s_remaining = rem;
+    }
+    __syncthreads();
+    mask |= 255u << shift;
+  }
+  const unsigned thr = s_prefix;
+  const int need_eq = s_remaining;    // how many positions equal to thr to keep
+  // ordered emission
+  int base_out = 0, eq_seen = 0;
+  for (int c0 = 0; c0 < n; c0 += blockDim.x) {
+    const int i = c0 + threadIdx.x;
+    const unsigned v = i < n ? sb[i] : 0u;
+    const int is_eq = (i < n && v == thr) ? 1 : 0;
+    int eq_total;
+    const int eq_rank = block_exclusive_scan(is_eq, warp_sums, eq_total) + eq_seen;
+    const int take = (i < n && (v > thr || (is_eq && eq_rank < need_eq))) ? 1 : 0;
+    int take_total;
+    const int pos = block_exclusive_scan(take, warp_sums, take_total);
+    if (take) idx_out[out0 + base_out + pos] = i;
+    base_out += take_total;
+    eq_seen += eq_total;
+  }
+}
+
+}  // namespace kvs
+
+using namespace kvs;
+
+extern "C" kvs_status kvs_select_critical(const void* k_cached_dev, const void* k_new_dev, const int64_t* row_off_dev,
+                                          int32_t n_agents, int32_t max_rows_per_agent, int32_t row_elems, float ratio,
+                                          int32_t* idx_out_dev, int64_t* idx_off_dev, void* ws, size_t ws_bytes,
+                                          cudaStream_t stream) {
+  if (n_agents < 0 || max_rows_per_agent < 0 || max_rows_per_agent > 65536 || row_elems < 8 || row_elems % 8)
+    return fail(KVS_ERR_INVALID_ARG, "select_critical: bad sizes (row_elems must be a positive multiple of 8)");
+  if (!row_off_dev || !idx_off_dev) return fail(KVS_ERR_INVALID_ARG, "select_critical: null pointer");
+  if (n_agents == 0) return KVS_OK;
+  if (!k_cached_dev || !k_new_dev || !idx_out_dev || !ws) return fail(KVS_ERR_INVALID_ARG, "select_critical: null pointer");
+  if (!aligned16(k_cached_dev) || !aligned16(k_new_dev) || !aligned16(ws))
+    return fail(KVS_ERR_INVALID_ARG, "select_critical: K buffers and ws must be 16-byte aligned");
+  if (!(ratio >= 0.f)) return fail(KVS_ERR_INVALID_ARG, "select_critical: ratio must be >= 0");
+  const long long rows = (long long)n_agents * max_rows_per_agent;
+  if ((size_t)rows * sizeof(float) > ws_bytes) return fail(KVS_ERR_CAPACITY, "select_critical: workspace too small");
+  float* scores = static_cast<float*>(ws);
+  const long long threads = rows * 32;
+  const int tb = 256;
+  if (rows > 0) {
+    sel_scores<<<(unsigned)((threads + tb - 1) / tb), tb, 0, stream>>>(
+        static_cast<const uint16_t*>(k_cached_dev), static_cast<const uint16_t*>(k_new_dev), row_off_dev, n_agents,
+        row_elems, rows, scores);
+    count_launch();
+  }
+  sel_topk<<<n_agents, 1024, 0, stream>>>(scores, row_off_dev, n_agents, ratio, rows, idx_out_dev, idx_off_dev);
+  count_launch();
+  return check_launch("select_critical");
+}

@@ -1,0 +1,231 @@
+"""Thin ctypes binding of libkvs (the C ABI in include/kvs.h).
+
+Argument marshalling only: torch tensors become raw device pointers, the
+current torch CUDA stream becomes the cudaStream_t, and a non-OK status raises
+KvsError with the library's error string.  Every step of the hot path runs in
+the library's CUDA kernels; there is no fallback when the library is missing —
+loading fails loudly.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional, Sequence
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libkvs.so")
+
+KVS_OK = 0
+KVS_ERR_INVALID_ARG = 1
+KVS_ERR_CAPACITY = 2
+KVS_ERR_CUDA = 3
+KVS_ERR_DEVICE_BOUNDS = 4
+KVS_ERR_UNSUPPORTED = 5
+
+KVS_DEVERR_BLOCK_ID = 0x1
+KVS_DEVERR_SEQ_LEN = 0x2
+KVS_DEVERR_CAPACITY = 0x4
+KVS_DEVERR_DIFF_ID = 0x8
+KVS_DEVERR_WAIT_TIMEOUT = 0x10
+KVS_DEVERR_ROPE_RANGE = 0x20
+KVS_DEVERR_JOB = 0x40
+
+KVS_DTYPE_BF16 = 0
+KVS_DTYPE_Q4G64 = 1
+KVS_DEDUP_TEST_WEAK_KEYS = 0x1
+KVS_OP_DEDUP, KVS_OP_DECODE_ATTN, KVS_OP_DECODE_ATTN_Q4, KVS_OP_SELECT = 0, 1, 2, 3
+
+EXPORTED = [
+    "kvs_pool_create", "kvs_pool_destroy", "kvs_fingerprint_dedup", "kvs_rope_rerotate",
+    "kvs_select_critical", "kvs_decode_attn", "kvs_decode_attn_q4", "kvs_quantize_q4",
+    "kvs_workspace_size", "kvs_pool_check", "kvs_pool_stats", "kvs_last_error_string",
+    "kvs_launch_count",
+]
+
+
+class KvsError(RuntimeError):
+    def __init__(self, status: int, msg: str):
+        super().__init__(f"kvs status {status}: {msg}")
+        self.status = status
+
+
+class PoolDesc(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int32) for n in (
+        "num_layers", "num_kv_heads", "head_dim", "block_tokens", "dtype",
+        "capacity_blocks", "diff_capacity_blocks", "max_seqs")]
+
+
+class Stats(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int64) for n in (
+        "unique_blocks", "shared_blocks", "total_refs", "pool_bytes", "dense_bytes")]
+
+
+_lib = None
+
+
+def load(path: str = LIB_PATH):
+    """Load libkvs.so (raises if it has not been built)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise RuntimeError(f"libkvs.so not found at {path}; run __graft_entry__.build() first")
+    lib = ctypes.CDLL(path)
+    P, I32, I64, U32, F32, SZ = (ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64,
+                                 ctypes.c_uint32, ctypes.c_float, ctypes.c_size_t)
+    sigs = {
+        "kvs_pool_create": [ctypes.POINTER(PoolDesc), P, P, P, P, P, P, ctypes.POINTER(P)],
+        "kvs_pool_destroy": [P],
+        "kvs_fingerprint_dedup": [P, P, P, I32, P, P, P, P, P, I32, P, P, U32, P, SZ, P],
+        "kvs_rope_rerotate": [P, I32, P, I32, I32, F32, P, P, I32, P],
+        "kvs_select_critical": [P, P, P, I32, I32, I32, F32, P, P, P, SZ, P],
+        "kvs_decode_attn": [P, I32, P, I32, P, I32, P, I32, P, P, P, F32, F32, P, P, SZ, P],
+        "kvs_decode_attn_q4": [P, I32, P, I32, P, I32, P, I32, F32, P, P, SZ, P],
+        "kvs_quantize_q4": [P, I32, P, P, P, I32, P],
+        "kvs_workspace_size": [P, I32, I32, I32, I32, ctypes.POINTER(SZ)],
+        "kvs_pool_check": [P, P, ctypes.POINTER(U32)],
+        "kvs_pool_stats": [P, P, P, P, ctypes.POINTER(Stats)],
+    }
+    for name, args in sigs.items():
+        fn = getattr(lib, name)
+        fn.argtypes = args
+        fn.restype = ctypes.c_int
+    lib.kvs_last_error_string.argtypes = []
+    lib.kvs_last_error_string.restype = ctypes.c_char_p
+    lib.kvs_launch_count.argtypes = []
+    lib.kvs_launch_count.restype = ctypes.c_uint64
+    _lib = lib
+    return lib
+
+
+def _check(st: int):
+    if st != KVS_OK:
+        raise KvsError(st, load().kvs_last_error_string().decode())
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    if t is None:
+        return None
+    if not t.is_contiguous():
+        raise ValueError("tensors passed to libkvs must be contiguous")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream=None):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _ptr_array(ts: Optional[Sequence[torch.Tensor]]):
+    if ts is None:
+        return None
+    arr = (ctypes.c_void_p * len(ts))(*[t.data_ptr() for t in ts])
+    return arr
+
+
+class Pool:
+    """Owns a kvs_pool handle and keeps the slab tensors alive."""
+
+    def __init__(self, handle, desc: PoolDesc, keep):
+        self.handle = handle
+        self.desc = desc
+        self._keep = keep
+
+    def __del__(self):
+        try:
+            if self.handle:
+                kvs_pool_destroy(self)
+        except Exception:
+            pass
+
+
+def kvs_pool_create(num_layers, num_kv_heads, head_dim, block_tokens, dtype, capacity_blocks,
+                    max_seqs, k_layers, v_layers, k_sb_layers=None, v_sb_layers=None,
+                    dk_layers=None, dv_layers=None, diff_capacity_blocks=0) -> Pool:
+    lib = load()
+    d = PoolDesc(num_layers, num_kv_heads, head_dim, block_tokens, dtype, capacity_blocks,
+                 diff_capacity_blocks, max_seqs)
+    arrs = [_ptr_array(x) for x in (k_layers, v_layers, k_sb_layers, v_sb_layers, dk_layers, dv_layers)]
+    h = ctypes.c_void_p()
+    _check(lib.kvs_pool_create(ctypes.byref(d), *arrs, ctypes.byref(h)))
+    keep = [k_layers, v_layers, k_sb_layers, v_sb_layers, dk_layers, dv_layers]
+    return Pool(h, d, keep)
+
+
+def kvs_pool_destroy(pool: Pool):
+    if pool.handle:
+        _check(load().kvs_pool_destroy(pool.handle))
+        pool.handle = None
+
+
+def kvs_workspace_size(pool: Pool, op: int, n_seq: int, max_blocks: int, n_q_heads: int = 0) -> int:
+    out = ctypes.c_size_t()
+    _check(load().kvs_workspace_size(pool.handle, op, n_seq, max_blocks, n_q_heads, ctypes.byref(out)))
+    return out.value
+
+
+def kvs_fingerprint_dedup(pool: Pool, tokens, seq_off, n_seq, tier, seg_off, seg_blocks, fp_out,
+                          block_table, max_blocks, refcount, n_phys, ws, flags=0, stream=None):
+    _check(load().kvs_fingerprint_dedup(
+        pool.handle, _ptr(tokens), _ptr(seq_off), n_seq, _ptr(tier), _ptr(seg_off), _ptr(seg_blocks),
+        _ptr(fp_out), _ptr(block_table), max_blocks, _ptr(refcount), _ptr(n_phys), flags,
+        _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)))
+
+
+def kvs_rope_rerotate(pool: Pool, layer, jobs, n_jobs, max_job_tokens, theta, src_table, dst_table,
+                      max_blocks, stream=None):
+    _check(load().kvs_rope_rerotate(pool.handle, layer, _ptr(jobs), n_jobs, max_job_tokens, theta,
+                                    _ptr(src_table), _ptr(dst_table), max_blocks, _stream(stream)))
+
+
+def kvs_select_critical(k_cached, k_new, row_off, n_agents, max_rows_per_agent, row_elems, ratio,
+                        idx_out, idx_off, ws, stream=None):
+    _check(load().kvs_select_critical(_ptr(k_cached), _ptr(k_new), _ptr(row_off), n_agents,
+                                      max_rows_per_agent, row_elems, ratio, _ptr(idx_out), _ptr(idx_off),
+                                      _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)))
+
+
+def kvs_decode_attn(pool: Pool, layer, q, n_q_heads, block_table, max_blocks, seq_len, n_seq,
+                    diff_table, rope_off, rope_segs, theta, scale, out, ws, stream=None):
+    _check(load().kvs_decode_attn(pool.handle, layer, _ptr(q), n_q_heads, _ptr(block_table), max_blocks,
+                                  _ptr(seq_len), n_seq, _ptr(diff_table), _ptr(rope_off), _ptr(rope_segs),
+                                  theta, scale, _ptr(out), _ptr(ws), ws.numel() * ws.element_size(),
+                                  _stream(stream)))
+
+
+def kvs_decode_attn_q4(pool: Pool, layer, q, n_q_heads, block_table, max_blocks, seq_len, n_seq,
+                       scale, out, ws, stream=None):
+    _check(load().kvs_decode_attn_q4(pool.handle, layer, _ptr(q), n_q_heads, _ptr(block_table), max_blocks,
+                                     _ptr(seq_len), n_seq, scale, _ptr(out), _ptr(ws),
+                                     ws.numel() * ws.element_size(), _stream(stream)))
+
+
+def kvs_quantize_q4(pool: Pool, layer, k_src, v_src, dst_blocks, n_blocks, stream=None):
+    _check(load().kvs_quantize_q4(pool.handle, layer, _ptr(k_src), _ptr(v_src), _ptr(dst_blocks),
+                                  n_blocks, _stream(stream)))
+
+
+def kvs_pool_check(pool: Pool, stream=None) -> int:
+    """Returns the device error bits (0 = clean); synchronises the stream."""
+    flags = ctypes.c_uint32()
+    st = load().kvs_pool_check(pool.handle, _stream(stream), ctypes.byref(flags))
+    if st not in (KVS_OK, KVS_ERR_DEVICE_BOUNDS):
+        _check(st)
+    return flags.value
+
+
+def kvs_pool_stats(pool: Pool, refcount, n_phys, stream=None) -> dict:
+    s = Stats()
+    _check(load().kvs_pool_stats(pool.handle, _ptr(refcount), _ptr(n_phys), _stream(stream), ctypes.byref(s)))
+    return {n: getattr(s, n) for n, _ in Stats._fields_}
+
+
+def kvs_last_error_string() -> str:
+    return load().kvs_last_error_string().decode()
+
+
+def kvs_launch_count() -> int:
+    return int(load().kvs_launch_count())

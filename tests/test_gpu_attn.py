@@ -1,0 +1,190 @@
+"""GPU decode attention (bf16 pool, fused diff overlay and segment rotation)
+vs the fp64 oracle: max|delta| <= 1e-2 and relative L2 <= 2e-3."""
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+from shared_paged_kv_gb300 import kvs as K
+from shared_paged_kv_gb300 import workloads as W
+from oracle import attention as OA, fingerprint as OF
+import harness as H
+
+f32 = W.bf16_bits_to_f32
+
+
+def oracle_out(w, pool, table, q_bits, layer=0, seq_len=None, diff=True, rope=True, agents=None, heads=None):
+    hst = pool.host[layer]
+    dk = f32(hst["dk"]) if diff and "dk" in hst else None
+    dv = f32(hst["dv"]) if diff and "dv" in hst else None
+    return OA.decode_attention(f32(q_bits), f32(hst["k"]), f32(hst["v"]), table,
+                               w.seq_len if seq_len is None else seq_len, w.block_tokens, w.scale,
+                               diff_table=w.diff_table if diff else None, dk_pool=dk, dv_pool=dv,
+                               rope_off=w.rope_off if rope else None, rope_segs=w.rope_segs if rope else None,
+                               theta=w.theta, agents=agents, heads=heads)
+
+
+def run_case(w, diff=True, rope=True, seq_len=None):
+    segs = w.seg_start_off is not None
+    ref = OF.dedup(w.tokens, w.seq_off, w.tier, w.block_tokens, w.max_blocks,
+                   w.seg_start_off if segs else None, w.seg_start_blocks if segs else None)
+    pool = H.bf16_pool(w)
+    q_bits = w.q_layer(0)
+    got = H.attn(pool, 0, q_bits, w, ref["block_table"], seq_len=seq_len, diff=diff, rope=rope)
+    exp = oracle_out(w, pool, ref["block_table"], q_bits, seq_len=seq_len, diff=diff, rope=rope)
+    H.assert_close_attn(got, exp)
+    assert K.kvs_pool_check(pool) == 0
+    return got, exp
+
+
+def test_tiny_with_mirror_diffs():
+    run_case(W.make_tiny())
+
+
+def test_tiny_without_diffs():
+    run_case(W.make_tiny(), diff=False)
+
+
+def test_mha_small_ragged():
+    w = W.make_prefix_shared("mha_small", 3, 4, 4, 128, 1, 24 * 16, [16 * 16 + 5, 16 * 13, 16 * 17 + 11], seed=11)
+    run_case(w)
+
+
+def test_gqa_small_ragged():
+    run_case(W.make_gqa_fanout(n_seq=5, prefix_tokens=256, priv_lo=30, priv_hi=300, hq=16, hkv=2, d=128))
+
+
+def test_gqa_group16_d64():
+    run_case(W.make_gqa_fanout(n_seq=3, prefix_tokens=100, priv_lo=1, priv_hi=200, hq=32, hkv=2, d=64))
+
+
+def test_group12_d128_sixteen_row_kernel():
+    # query groups of 9..16 heads take the 16-row (heads as M) kernel
+    w = W.make_allgather(seed=5, n_seq=3, n_segs=4, priv_blocks_lo=2, priv_blocks_hi=7, hq=24, hkv=2, n_layers=1)
+    run_case(w)
+
+
+def test_allgather_small_rotation_and_diffs():
+    w = W.make_allgather(n_seq=4, n_segs=6, priv_blocks_lo=3, priv_blocks_hi=9, hq=10, hkv=2, n_layers=1)
+    run_case(w)
+    run_case(w, rope=False)
+
+
+def test_allgather_d64_rotation():
+    w = W.make_allgather(seed=9, n_seq=3, n_segs=5, priv_blocks_lo=2, priv_blocks_hi=5, hq=4, hkv=2, d=64,
+                         n_layers=1, theta=1e4)
+    run_case(w)
+
+
+def test_edge_lengths():
+    # empty context -> zeros; a single token -> that token's V; exact block
+    # multiples and one-past.
+    w = W.make_gqa_fanout(n_seq=5, prefix_tokens=64, priv_lo=40, priv_hi=90, hq=8, hkv=2, d=128)
+    sl = w.seq_len.copy()
+    sl[0], sl[1], sl[2], sl[3] = 0, 1, 64, 17
+    got, exp = run_case(w, seq_len=sl)
+    assert np.all(got[0] == 0)
+
+
+def test_shared_layout_equals_private_layout_on_gpu():
+    # The same values in a deduplicated pool and in a fully private pool give
+    # the same GPU output (and both match the oracle).
+    w = W.make_gqa_fanout(n_seq=4, prefix_tokens=160, priv_lo=16, priv_hi=64, hq=8, hkv=2, d=128)
+    ref = OF.dedup(w.tokens, w.seq_off, w.tier, w.block_tokens, w.max_blocks)
+    pool = H.bf16_pool(w)
+    q_bits = w.q_layer(0)
+    o1 = H.attn(pool, 0, q_bits, w, ref["block_table"])
+    tb = ref["block_table"]
+    kb, vb = pool.host[0]["k"], pool.host[0]["v"]
+    rows_k, rows_v, priv = [], [], np.full_like(tb, -1)
+    for a in range(w.n_seq):
+        for b in range(w.max_blocks):
+            if tb[a, b] >= 0:
+                priv[a, b] = len(rows_k)
+                rows_k.append(kb[tb[a, b]])
+                rows_v.append(vb[tb[a, b]])
+    w2 = W.Workload(**{**w.__dict__, "capacity_blocks": len(rows_k)})
+    pool2 = H.bf16_pool(w2, layers_np=[(np.stack(rows_k), np.stack(rows_v))])
+    o2 = H.attn(pool2, 0, q_bits, w2, priv)
+    np.testing.assert_array_equal(o1, o2)
+
+
+def test_bad_block_id_is_flagged_not_faulted():
+    w = W.make_tiny()
+    ref = OF.dedup(w.tokens, w.seq_off, w.tier, w.block_tokens, w.max_blocks)
+    tb = ref["block_table"].copy()
+    tb[1, 3] = w.capacity_blocks + 7
+    pool = H.bf16_pool(w)
+    H.attn(pool, 0, w.q_layer(0), w, tb)
+    assert K.kvs_pool_check(pool) & K.KVS_DEVERR_BLOCK_ID
+    assert K.kvs_pool_check(pool) == 0     # reading clears the word
+
+
+def test_repeatable_bitwise():
+    w = W.make_allgather(n_seq=4, n_segs=6, priv_blocks_lo=3, priv_blocks_hi=9, hq=10, hkv=2, n_layers=1)
+    ref = OF.dedup(w.tokens, w.seq_off, w.tier, w.block_tokens, w.max_blocks, w.seg_start_off, w.seg_start_blocks)
+    pool = H.bf16_pool(w)
+    q = w.q_layer(0)
+    a = H.attn(pool, 0, q, w, ref["block_table"])
+    b = H.attn(pool, 0, q, w, ref["block_table"])
+    np.testing.assert_array_equal(a, b)
+
+
+# ---------------------------------------------------------------- full size ---
+def full_size_sampled(w, samples, layer_seed=0):
+    """Full-size pool generated on the device by torch's seeded generator;
+    the oracle recomputes sampled (agent, head) outputs from a host copy of
+    the head's slab."""
+    segs = w.seg_start_off is not None
+    ref = OF.dedup(w.tokens, w.seq_off, w.tier, w.block_tokens, w.max_blocks,
+                   w.seg_start_off if segs else None, w.seg_start_blocks if segs else None)
+    cap = ref["n_phys"]
+    g = torch.Generator(device=H.DEV).manual_seed(1234 + layer_seed)
+    shape = (cap, w.n_kv_heads, w.block_tokens, w.head_dim)
+    k = torch.randn(shape, generator=g, device=H.DEV).to(torch.bfloat16)
+    v = torch.randn(shape, generator=g, device=H.DEV).to(torch.bfloat16)
+    dks = dvs = None
+    if w.diff_capacity_blocks:
+        dshape = (w.diff_capacity_blocks,) + shape[1:]
+        dks = [(0.1 * torch.randn(dshape, generator=g, device=H.DEV)).to(torch.bfloat16)]
+        dvs = [(0.1 * torch.randn(dshape, generator=g, device=H.DEV)).to(torch.bfloat16)]
+    pool = K.kvs_pool_create(1, w.n_kv_heads, w.head_dim, w.block_tokens, K.KVS_DTYPE_BF16, cap, w.n_seq,
+                             [k.view(torch.int16)], [v.view(torch.int16)],
+                             dk_layers=[x.view(torch.int16) for x in dks] if dks else None,
+                             dv_layers=[x.view(torch.int16) for x in dvs] if dvs else None,
+                             diff_capacity_blocks=w.diff_capacity_blocks)
+    q_bits = w.q_layer(0)
+    got = H.attn(pool, 0, q_bits, w, ref["block_table"])
+    assert K.kvs_pool_check(pool) == 0
+    assert np.isfinite(got).all()
+    G = w.group
+    for (a, hq) in samples:
+        h = hq // G
+        kh = k[:, h:h + 1].float().cpu().numpy().astype(np.float64)
+        vh = v[:, h:h + 1].float().cpu().numpy().astype(np.float64)
+        dkh = dks[0][:, h:h + 1].float().cpu().numpy().astype(np.float64) if dks else None
+        dvh = dvs[0][:, h:h + 1].float().cpu().numpy().astype(np.float64) if dvs else None
+        q1 = f32(q_bits[a:a + 1, hq:hq + 1]).astype(np.float64)
+        tb = ref["block_table"][a:a + 1]
+        dt = w.diff_table[a:a + 1] if w.diff_table is not None else None
+        ro = rsg = None
+        if w.rope_off is not None:
+            ro = np.array([0, w.rope_off[a + 1] - w.rope_off[a]], np.int32)
+            rsg = w.rope_segs[w.rope_off[a]:w.rope_off[a + 1]]
+        exp = OA.decode_attention(q1, kh, vh, tb, w.seq_len[a:a + 1], w.block_tokens, w.scale,
+                                  diff_table=dt, dk_pool=dkh, dv_pool=dvh, rope_off=ro, rope_segs=rsg,
+                                  theta=w.theta)
+        H.assert_close_attn(got[a:a + 1, hq:hq + 1], exp)
+
+
+def test_full_size_mha7b_sampled():
+    full_size_sampled(W.make_mha7b(n_layers=1), [(0, 0), (3, 17), (7, 31)])
+
+
+def test_full_size_gqa_fanout_sampled():
+    full_size_sampled(W.make_gqa_fanout(n_layers=1), [(0, 0), (13, 9), (31, 15)])
+
+
+def test_full_size_allgather_sampled():
+    full_size_sampled(W.make_allgather(n_layers=1), [(0, 0), (21, 17), (63, 39)])

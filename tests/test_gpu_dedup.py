@@ -1,0 +1,101 @@
+"""GPU fingerprint + dedup vs the oracle: bit-exact fingerprints, block
+tables, refcounts and physical-block counts."""
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+from shared_paged_kv_gb300 import kvs as K
+from shared_paged_kv_gb300 import workloads as W
+from oracle import fingerprint as OF
+import harness as H
+
+
+def check(w, flags=0, segments=True, tier=None, capacity=None):
+    pool = H.bf16_pool(w, capacity=capacity, with_diff=False) if capacity is None else \
+        K.kvs_pool_create(1, w.n_kv_heads, w.head_dim, w.block_tokens, K.KVS_DTYPE_BF16, capacity, w.n_seq,
+                          [torch.zeros(16, dtype=torch.int16, device=H.DEV)],
+                          [torch.zeros(16, dtype=torch.int16, device=H.DEV)])
+    got = H.gpu_dedup(pool, w, flags=flags, segments=segments, tier=tier)
+    t = w.tier if tier is None else tier
+    so, sb = (w.seg_start_off, w.seg_start_blocks) if segments else (None, None)
+    ref = OF.dedup(w.tokens, w.seq_off, t, w.block_tokens, w.max_blocks, so, sb)
+    assert got["n_phys"] == ref["n_phys"]
+    np.testing.assert_array_equal(got["block_table"], ref["block_table"])
+    np.testing.assert_array_equal(got["refcount"], ref["refcount"])
+    np.testing.assert_array_equal(got["fp"], ref["fp"])
+    assert (got["refcount_full"][ref["n_phys"]:] == 0).all()
+    assert K.kvs_pool_check(pool) == 0
+    return got, ref
+
+
+def test_tiny():
+    got, ref = check(W.make_tiny())
+    assert ref["n_phys"] == 16 + sum(-(-(l - 256) // 16) for l in W.make_tiny().seq_len)
+
+
+def test_gqa_small_ragged():
+    check(W.make_gqa_fanout(n_seq=7, prefix_tokens=200, priv_lo=1, priv_hi=90, hq=4, hkv=2, d=64))
+
+
+def test_segments_allgather_small():
+    w = W.make_allgather(n_seq=5, n_segs=7, priv_blocks_lo=2, priv_blocks_hi=6, hq=4, hkv=2, d=64, n_layers=1)
+    got, ref = check(w)
+    # every master segment is stored once: 7 segments x 8 blocks shared by 5 agents
+    assert (ref["refcount"] == 5).sum() == 7 * 8
+    check(w, segments=False)   # prefix hashing of the same tokens shares nothing
+
+
+def test_tiers_and_private():
+    w = W.make_gqa_fanout(n_seq=6, prefix_tokens=96, priv_lo=0, priv_hi=40, hq=4, hkv=2, d=64)
+    tier = np.array([0, 1, 0, W.PRIVATE_TIER, 1, 0], dtype=np.uint32)
+    check(w, tier=tier)
+
+
+@pytest.mark.parametrize("seed", [0, 1, 2])
+def test_collision_path_is_exact(seed):
+    # 6-bit table keys force many hash collisions; the token compare and the
+    # exact fallback must still give the oracle's result.
+    rng = np.random.default_rng(seed)
+    w = W.make_gqa_fanout(seed=seed, n_seq=6, prefix_tokens=int(rng.integers(16, 120)), priv_lo=0, priv_hi=70,
+                          hq=4, hkv=2, d=64)
+    check(w, flags=K.KVS_DEDUP_TEST_WEAK_KEYS)
+    w2 = W.make_allgather(seed=seed, n_seq=4, n_segs=5, priv_blocks_lo=1, priv_blocks_hi=4, hq=4, hkv=2, d=64,
+                          n_layers=1)
+    check(w2, flags=K.KVS_DEDUP_TEST_WEAK_KEYS)
+
+
+def test_empty_and_short_sequences():
+    seqs = [np.arange(0, dtype=np.uint32), np.arange(5, dtype=np.uint32), np.arange(16, dtype=np.uint32),
+            np.arange(40, dtype=np.uint32), np.arange(0, dtype=np.uint32)]
+    off = np.concatenate([[0], np.cumsum([len(s) for s in seqs])]).astype(np.int64)
+    w = W.Workload("edge", len(seqs), 2, 1, 64, 16, 1, 1e4, np.concatenate(seqs).astype(np.uint32), off,
+                   np.zeros(len(seqs), np.uint32), 3, 8)
+    got, ref = check(w)
+    assert (got["block_table"][0] == -1).all() and (got["block_table"][4] == -1).all()
+
+
+def test_too_long_sequence_is_flagged():
+    w = W.make_gqa_fanout(n_seq=3, prefix_tokens=64, priv_lo=10, priv_hi=20, hq=4, hkv=2, d=64)
+    w.max_blocks -= 1      # the longest sequence no longer fits its table row
+    pool = H.bf16_pool(w, with_diff=False)
+    H.gpu_dedup(pool, w)
+    assert K.kvs_pool_check(pool) & K.KVS_DEVERR_SEQ_LEN
+
+
+def test_capacity_overflow_is_flagged():
+    w = W.make_gqa_fanout(n_seq=4, prefix_tokens=64, priv_lo=40, priv_hi=60, hq=4, hkv=2, d=64)
+    pool = K.kvs_pool_create(1, 2, 64, 16, K.KVS_DTYPE_BF16, 5, 4,
+                             [torch.zeros(5 * 2 * 16 * 64, dtype=torch.int16, device=H.DEV)],
+                             [torch.zeros(5 * 2 * 16 * 64, dtype=torch.int16, device=H.DEV)])
+    H.gpu_dedup(pool, w)
+    assert K.kvs_pool_check(pool) & K.KVS_DEVERR_CAPACITY
+
+
+@pytest.mark.parametrize("name", ["mha7b", "gqa_fanout", "allgather"])
+def test_full_size(name):
+    w = {"mha7b": W.make_mha7b, "gqa_fanout": W.make_gqa_fanout, "allgather": W.make_allgather}[name]()
+    got, ref = check(w, capacity=w.capacity_blocks)
+    if name == "mha7b":
+        assert ref["n_phys"] == 614 + 8 * 410
