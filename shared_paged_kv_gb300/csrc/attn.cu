@@ -63,12 +63,6 @@ __host__ __device__ constexpr int attn_smem_bytes() {
   return 1024 + kAttnWarps * attn_stages<D, DIFF>() * (DIFF ? 4 : 2) * AttnCfg<D>::TILE;
 }
 
-// Byte offset of (token t, column col) inside a swizzled [t][D/64][64] tile.
-template <int D>
-__device__ __forceinline__ uint32_t tile_off(int t, int col) {
-  const uint32_t o = ((uint32_t)(t * (D / 64) + (col >> 6)) << 7) + ((uint32_t)(col & 63) << 1);
-  return swz128(o);
-}
 
 template <int D, bool DIFF, bool ROPE>
 __global__ void __launch_bounds__(128, 2)
@@ -146,12 +140,12 @@ attn_bf16_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ C
     mbar_arrive_expect_tx(bar, (did >= 0 ? 4 : 2) * TILE);
     uint8_t* st = wbase + s * STAGE;
     const int row = (phys * p.hkv + h) * B;
-    tma_load_3d(st, &tk, 0, 0, row, bar);
-    tma_load_3d(st + TILE, &tv, 0, 0, row, bar);
+    tma_load_kv_tile<D>(st, &tk, row, bar);
+    tma_load_kv_tile<D>(st + TILE, &tv, row, bar);
     if (DIFF && did >= 0) {
       const int drow_ = (did * p.hkv + h) * B;
-      tma_load_3d(st + 2 * TILE, &tdk, 0, 0, drow_, bar);
-      tma_load_3d(st + 3 * TILE, &tdv, 0, 0, drow_, bar);
+      tma_load_kv_tile<D>(st + 2 * TILE, &tdk, drow_, bar);
+      tma_load_kv_tile<D>(st + 3 * TILE, &tdv, drow_, bar);
     }
   };
 
@@ -217,8 +211,8 @@ attn_bf16_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ C
     const int tv_ = ((mi & 1) << 3) + r, cv = (mi >> 1) << 3;
 #pragma unroll
     for (int kk = 0; kk < KS; ++kk) {
-      koff[kk] = tile_off<D>(tk_, kk * 16 + ck);
-      voff[kk] = tile_off<D>(tv_, kk * 16 + cv);
+      koff[kk] = kv_tile_off<D>(tk_, kk * 16 + ck);
+      voff[kk] = kv_tile_off<D>(tv_, kk * 16 + cv);
     }
   }
 

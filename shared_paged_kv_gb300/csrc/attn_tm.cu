@@ -63,11 +63,6 @@ __host__ __device__ constexpr int tm_smem_bytes() {
   return 1024 + kTmWarps * tm_stages<D, DIFF>() * 2 * (16 * D * 2);
 }
 
-template <int D>
-__device__ __forceinline__ uint32_t tm_tile_off(int t, int col) {
-  const uint32_t o = ((uint32_t)(t * (D / 64) + (col >> 6)) << 7) + ((uint32_t)(col & 63) << 1);
-  return swz128(o);
-}
 
 __device__ __forceinline__ uint32_t movm_t(uint32_t x) {
   uint32_t y;
@@ -86,7 +81,9 @@ attn_tm_kernel(const __grid_constant__ TmParams p, const __grid_constant__ CUten
   extern __shared__ uint8_t smem_raw[];
   __shared__ uint64_t bars[kTmWarps][S];
   __shared__ int st_item[kTmWarps][S];
-  __shared__ int st_block[kTmWarps][S];   // block index; bit 30 set: the next position holds its diff
+  // block index; bit 30: the next position holds the block's diff tiles;
+  // bit 29: the block id was out of range and nothing was loaded
+  __shared__ int st_block[kTmWarps][S];
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, c = lane & 3;
@@ -136,8 +133,8 @@ attn_tm_kernel(const __grid_constant__ TmParams p, const __grid_constant__ CUten
     uint8_t* st = wbase + s * STAGE;
     if (DIFF && pend_drow >= 0) {
       mbar_arrive_expect_tx(bar, 2 * TILE);
-      tma_load_3d(st, &tdk, 0, 0, pend_drow, bar);
-      tma_load_3d(st + TILE, &tdv, 0, 0, pend_drow, bar);
+      tma_load_kv_tile<D>(st, &tdk, pend_drow, bar);
+      tma_load_kv_tile<D>(st + TILE, &tdv, pend_drow, bar);
       pend_drow = -1;
       return;
     }
@@ -153,6 +150,7 @@ attn_tm_kernel(const __grid_constant__ TmParams p, const __grid_constant__ CUten
     const int phys = __ldg(p.block_table + (size_t)p_a * p.max_blocks + b);
     if (phys < 0 || phys >= p.capacity) {
       set_err(p.status, KVS_DEVERR_BLOCK_ID);
+      st_block[warp][s] = b | (1 << 29);   // nothing loaded: skip this block
       mbar_arrive(bar);
       return;
     }
@@ -167,8 +165,8 @@ attn_tm_kernel(const __grid_constant__ TmParams p, const __grid_constant__ CUten
     }
     mbar_arrive_expect_tx(bar, 2 * TILE);
     const int row = (phys * p.hkv + p_h) * B;
-    tma_load_3d(st, &tk, 0, 0, row, bar);
-    tma_load_3d(st + TILE, &tv, 0, 0, row, bar);
+    tma_load_kv_tile<D>(st, &tk, row, bar);
+    tma_load_kv_tile<D>(st + TILE, &tv, row, bar);
   };
   if (lane == 0)
     for (int s = 0; s < S; ++s) issue(s);
@@ -179,8 +177,8 @@ attn_tm_kernel(const __grid_constant__ TmParams p, const __grid_constant__ CUten
     const int mi = lane >> 3, r = lane & 7;
 #pragma unroll
     for (int kk = 0; kk < KS; ++kk) {
-      koff[kk] = tm_tile_off<D>(((mi & 1) << 3) + r, kk * 16 + ((mi >> 1) << 3));   // A = K [token][d]
-      voff[kk] = tm_tile_off<D>(((mi >> 1) << 3) + r, kk * 16 + ((mi & 1) << 3));   // A = V^T via .trans
+      koff[kk] = kv_tile_off<D>(((mi & 1) << 3) + r, kk * 16 + ((mi >> 1) << 3));   // A = K [token][d]
+      voff[kk] = kv_tile_off<D>(((mi >> 1) << 3) + r, kk * 16 + ((mi & 1) << 3));   // A = V^T via .trans
     }
   }
 
@@ -244,19 +242,19 @@ attn_tm_kernel(const __grid_constant__ TmParams p, const __grid_constant__ CUten
         if (g == 0) __stcg(reinterpret_cast<float2*>(p.part_ml + ((size_t)cur * p.g + r) * 2), make_float2(m[cc], cc ? lt1 : lt0));
       }
     }
-    __threadfence();
     __syncwarp();
     const int nb = seq_blocks(ca);
     const int nch = (nb + p.ib - 1) / p.ib;
     int last = 0;
     if (lane == 0) {
+      __threadfence();   // the warp's split stores (ordered by __syncwarp) before the arrival
       const int t = atomicAdd(p.tickets + ca * p.hkv + ch_, 1);
       last = (t == nch - 1);
       if (last) p.tickets[ca * p.hkv + ch_] = 0;
     }
     last = __shfl_sync(0xffffffffu, last, 0);
     if (!last) return;
-    __threadfence();
+    __threadfence();   // acquire side: other warps' splits are visible
     // merge: item ids of (ca, ch_) for chunks 0..nch-1
     for (int r = 0; r < p.g; ++r) {
       float M = -INFINITY;
@@ -289,7 +287,8 @@ attn_tm_kernel(const __grid_constant__ TmParams p, const __grid_constant__ CUten
     const int bword = st_block[warp][s];
     if (item < 0) break;
     const bool has_diff = DIFF && (bword >> 30) != 0;
-    const int b = bword & ((1 << 30) - 1);
+    const int b = bword & ((1 << 29) - 1);
+    const bool loaded = ((bword >> 29) & 1) == 0;
     const int s2 = (i + 1) % S;
     if (has_diff && !mbar_wait_bounded(&bars[warp][s2], ((i + 1) / S) & 1, p.status)) break;
     if (item != cur) {
@@ -313,8 +312,7 @@ attn_tm_kernel(const __grid_constant__ TmParams p, const __grid_constant__ CUten
         seg_end = p.rope_off[ca + 1];
       }
     }
-    const int phys = __ldg(p.block_table + (size_t)ca * p.max_blocks + b);
-    if (phys >= 0 && phys < p.capacity) {
+    if (loaded) {
       if (ROPE && (b < seg_lo || b >= seg_hi)) {
         int found = 0x7fffffff, fd = 0, flo = 0, fhi = 0;
         for (int e = seg_beg + lane; e < seg_end; e += 32) {
@@ -349,19 +347,23 @@ attn_tm_kernel(const __grid_constant__ TmParams p, const __grid_constant__ CUten
       const uint32_t tkb = wbase_u32 + s * STAGE, tvb = tkb + TILE;
       const uint32_t dkb = wbase_u32 + s2 * STAGE, dvb = dkb + TILE;   // diff tiles (if any)
       // S^T = K q^T : 16 tokens x 8 query heads
-      float sc[4] = {0.f, 0.f, 0.f, 0.f};
+      // two independent accumulation chains (even / odd k-steps)
+      float sc[4] = {0.f, 0.f, 0.f, 0.f}, sd[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int kk = 0; kk < KS; ++kk) {
+        float* acc_s = (kk & 1) ? sd : sc;
         uint32_t a[4];
         ldsm_x4(tkb + koff[kk], a[0], a[1], a[2], a[3]);
-        mma_bf16(sc, a, qb[kk][0], qb[kk][1]);
-        if (ROPE && q_has_lo) mma_bf16(sc, a, qlo[ROPE ? kk : 0][0], qlo[ROPE ? kk : 0][1]);
+        mma_bf16(acc_s, a, qb[kk][0], qb[kk][1]);
+        if (ROPE && q_has_lo) mma_bf16(acc_s, a, qlo[ROPE ? kk : 0][0], qlo[ROPE ? kk : 0][1]);
         if (has_diff) {
           ldsm_x4(dkb + koff[kk], a[0], a[1], a[2], a[3]);
-          mma_bf16(sc, a, qb[kk][0], qb[kk][1]);
-          if (ROPE && q_has_lo) mma_bf16(sc, a, qlo[ROPE ? kk : 0][0], qlo[ROPE ? kk : 0][1]);
+          mma_bf16(acc_s, a, qb[kk][0], qb[kk][1]);
+          if (ROPE && q_has_lo) mma_bf16(acc_s, a, qlo[ROPE ? kk : 0][0], qlo[ROPE ? kk : 0][1]);
         }
       }
+#pragma unroll
+      for (int e = 0; e < 4; ++e) sc[e] += sd[e];
       const int nv = min(B, cL - b * B);
       // sc: (t=g, r=2c), (g, 2c+1), (g+8, 2c), (g+8, 2c+1)
 #pragma unroll
@@ -448,12 +450,13 @@ static kvs_status launch_tm(TmParams& prm, const kvs_pool* pool, int layer, cuda
   return check_launch("decode_attn");
 }
 
-// Work-item size: about a dozen items per resident warp so the dynamic
-// schedule balances ragged contexts, capped to keep splits cheap to merge.
+// Work-item size: about eight items per resident warp so the dynamic
+// schedule balances ragged contexts while the per-item split write and
+// arrival stay rare.
 int tm_item_blocks(const kvs_pool* pool, int n_seq, int max_blocks) {
   const long long work = (long long)n_seq * pool->desc.num_kv_heads * max_blocks;
   const long long warps = (long long)pool->num_sms * 3 * kTmWarps;
-  long long ib = work / (warps * 12);
+  long long ib = work / (warps * 8);
   int r = 4;
   while (r < ib && r < 64) r <<= 1;
   return r;

@@ -104,6 +104,22 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t b
 __device__ __forceinline__ uint32_t swz128(uint32_t o) { return o ^ (((o >> 7) & 7u) << 4); }
 __device__ __forceinline__ uint32_t swz64(uint32_t o) { return o ^ (((o >> 7) & 3u) << 4); }
 
+// A bf16 KV tile of one 16-token block and one KV head, head_dim D, is loaded
+// as D/64 TMA boxes of 16 rows x 64 elements (128-byte rows, 128-byte
+// swizzle) stacked as [D/64][16][64].  Consecutive tokens are consecutive
+// 128-byte rows, so the swizzle spreads any 8 consecutive tokens over all
+// eight 16-byte bank groups (ldmatrix without conflicts).
+template <int D>
+__device__ __forceinline__ void tma_load_kv_tile(void* dst, const CUtensorMap* map, int row, uint64_t* bar) {
+#pragma unroll
+  for (int h = 0; h < D / 64; ++h) tma_load_2d(static_cast<uint8_t*>(dst) + h * 2048, map, h * 64, row, bar);
+}
+
+template <int D>
+__device__ __forceinline__ uint32_t kv_tile_off(int t, int col) {
+  return swz128(((uint32_t)((col >> 6) * 16 + t) << 7) + ((uint32_t)(col & 63) << 1));
+}
+
 // ------------------------------------------------------- tensor-core mma ---
 __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
   asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
