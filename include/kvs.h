@@ -181,6 +181,31 @@ kvs_status kvs_select_critical(const void* k_cached_dev, const void* k_new_dev,
                                int32_t* idx_out_dev, int64_t* idx_off_dev,
                                void* ws, size_t ws_bytes, cudaStream_t stream);
 
+/* Same selection as kvs_select_critical, for callers that cannot allocate
+ * device memory on the call path — for example a serving process that has
+ * handed all free device memory to its KV pool and caching allocator up front
+ * (a further cudaMalloc would fail or fragment it), a latency-critical step
+ * that cannot afford cudaMalloc/cudaFree's implicit device synchronisation,
+ * or a plain C caller that does not want to size and own a workspace.  The
+ * pages have no counterpart to this entry point.
+ * Scratch: a fixed device array of 2^20 fp32 scores inside the library,
+ * reserved on every GPU that loads the library and held until the process
+ * exits.  n_agents * max_rows_per_agent must not exceed 2^20, otherwise
+ * KVS_ERR_CAPACITY is returned before anything is enqueued.  The caller still
+ * passes all inputs and outputs (same meaning as kvs_select_critical).
+ * Allocates nothing: no cudaMalloc, cudaFree or allocating library call.
+ * The first call made with a given device current looks up the array's
+ * device address (cudaGetSymbolAddress, which can load the library's device
+ * code); make that first call before any stream capture.
+ * All calls on a device share the one array and it keeps the previous call's
+ * contents; every value a call reads is written earlier in the same call.
+ * Calls whose work can overlap on the GPU (different streams, or threads
+ * without ordering) race on the array and give undefined results. */
+kvs_status kvs_select_critical_noalloc(const void* k_cached_dev, const void* k_new_dev,
+                                       const int64_t* row_off_dev, int32_t n_agents,
+                                       int32_t max_rows_per_agent, int32_t row_elems, float ratio,
+                                       int32_t* idx_out_dev, int64_t* idx_off_dev, cudaStream_t stream);
+
 /* ---------------------------------------------------------------------------
  * Paged decode attention with the mirror-diff overlay and segment RoPE
  * restore fused into the read ([TD] section 3, Fig. 8: blocks with a diff

@@ -8,6 +8,9 @@
 // score by a 4 x 8-bit radix select on the float bits (scores are >= 0, so
 // the bit pattern orders them), then emits, in ascending position order, every
 // position above the threshold and the lowest-positioned ones equal to it.
+#include <mutex>
+#include <string>
+
 #include "common.cuh"
 #include "internal.h"
 
@@ -176,4 +179,67 @@ extern "C" kvs_status kvs_select_critical(const void* k_cached_dev, const void* 
   sel_topk<<<n_agents, 1024, 0, stream>>>(scores, row_off_dev, n_agents, ratio, rows, idx_out_dev, idx_off_dev);
   count_launch();
   return check_launch("select_critical");
+}
+
+// ---------------------------------------------------------------------------
+// kvs_select_critical_noalloc: the same selection for callers that cannot
+// allocate device memory on the call path.  Its only scratch (one fp32 score
+// per position row) lives in this file-scope device array, reserved once per
+// device when the library's device code is loaded and held until the process
+// exits.  Host code never uses the array's name as a pointer: the device
+// address is fetched with cudaGetSymbolAddress once per device (on the first
+// call made with that device current) and cached.
+namespace kvs {
+constexpr long long kSelNoallocMaxRows = 1ll << 20;   // 4 MiB of scores
+static __device__ __align__(256) float g_sel_scores[kSelNoallocMaxRows];
+static float* g_sel_scores_dev[64] = {};
+static std::mutex g_sel_scores_mu;
+}  // namespace kvs
+
+extern "C" kvs_status kvs_select_critical_noalloc(const void* k_cached_dev, const void* k_new_dev,
+                                                  const int64_t* row_off_dev, int32_t n_agents,
+                                                  int32_t max_rows_per_agent, int32_t row_elems, float ratio,
+                                                  int32_t* idx_out_dev, int64_t* idx_off_dev,
+                                                  cudaStream_t stream) {
+  if (n_agents < 0 || max_rows_per_agent < 0 || max_rows_per_agent > 65536 || row_elems < 8 || row_elems % 8)
+    return fail(KVS_ERR_INVALID_ARG, "select_critical_noalloc: bad sizes (row_elems must be a positive multiple of 8)");
+  const long long rows = (long long)n_agents * max_rows_per_agent;
+  if (rows > kSelNoallocMaxRows)
+    return fail(KVS_ERR_CAPACITY, "select_critical_noalloc: n_agents * max_rows_per_agent exceeds the fixed scratch "
+                                  "of 1048576 rows; use kvs_select_critical with a caller workspace");
+  if (!row_off_dev || !idx_off_dev) return fail(KVS_ERR_INVALID_ARG, "select_critical_noalloc: null pointer");
+  if (n_agents == 0) return KVS_OK;
+  if (!k_cached_dev || !k_new_dev || !idx_out_dev) return fail(KVS_ERR_INVALID_ARG, "select_critical_noalloc: null pointer");
+  if (!aligned16(k_cached_dev) || !aligned16(k_new_dev))
+    return fail(KVS_ERR_INVALID_ARG, "select_critical_noalloc: K buffers must be 16-byte aligned");
+  if (!(ratio >= 0.f)) return fail(KVS_ERR_INVALID_ARG, "select_critical_noalloc: ratio must be >= 0");
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64)
+    return fail(KVS_ERR_CUDA, "select_critical_noalloc: cannot identify the current device");
+  float* scores = nullptr;
+  {
+    std::lock_guard<std::mutex> lock(g_sel_scores_mu);
+    if (!g_sel_scores_dev[dev]) {
+      void* ptr = nullptr;
+      const cudaError_t e = cudaGetSymbolAddress(&ptr, g_sel_scores);
+      if (e != cudaSuccess || !ptr)
+        return fail(KVS_ERR_CUDA, std::string("select_critical_noalloc: cudaGetSymbolAddress failed: ") +
+                                      cudaGetErrorString(e));
+      g_sel_scores_dev[dev] = static_cast<float*>(ptr);
+    }
+    scores = g_sel_scores_dev[dev];
+  }
+  // Every score the selection reads is written by sel_scores in this call, so
+  // nothing in the array has to start at zero.
+  const long long threads = rows * 32;
+  const int tb = 256;
+  if (rows > 0) {
+    sel_scores<<<(unsigned)((threads + tb - 1) / tb), tb, 0, stream>>>(
+        static_cast<const uint16_t*>(k_cached_dev), static_cast<const uint16_t*>(k_new_dev), row_off_dev, n_agents,
+        row_elems, rows, scores);
+    count_launch();
+  }
+  sel_topk<<<n_agents, 1024, 0, stream>>>(scores, row_off_dev, n_agents, ratio, rows, idx_out_dev, idx_off_dev);
+  count_launch();
+  return check_launch("select_critical_noalloc");
 }

@@ -39,7 +39,7 @@ KVS_OP_DEDUP, KVS_OP_DECODE_ATTN, KVS_OP_DECODE_ATTN_Q4, KVS_OP_SELECT = 0, 1, 2
 
 EXPORTED = [
     "kvs_pool_create", "kvs_pool_destroy", "kvs_fingerprint_dedup", "kvs_rope_rerotate",
-    "kvs_select_critical", "kvs_decode_attn", "kvs_decode_attn_q4", "kvs_quantize_q4",
+    "kvs_select_critical", "kvs_select_critical_noalloc", "kvs_decode_attn", "kvs_decode_attn_q4", "kvs_quantize_q4",
     "kvs_workspace_size", "kvs_pool_check", "kvs_pool_stats", "kvs_last_error_string",
     "kvs_launch_count",
 ]
@@ -81,6 +81,7 @@ def load(path: str = LIB_PATH):
         "kvs_fingerprint_dedup": [P, P, P, I32, P, P, P, P, P, I32, P, P, U32, P, SZ, P],
         "kvs_rope_rerotate": [P, I32, P, I32, I32, F32, P, P, I32, P],
         "kvs_select_critical": [P, P, P, I32, I32, I32, F32, P, P, P, SZ, P],
+        "kvs_select_critical_noalloc": [P, P, P, I32, I32, I32, F32, P, P, P],
         "kvs_decode_attn": [P, I32, P, I32, P, I32, P, I32, P, P, P, F32, F32, P, P, SZ, P],
         "kvs_decode_attn_q4": [P, I32, P, I32, P, I32, P, I32, F32, P, P, SZ, P],
         "kvs_quantize_q4": [P, I32, P, P, P, I32, P],
@@ -186,6 +187,15 @@ def kvs_select_critical(k_cached, k_new, row_off, n_agents, max_rows_per_agent, 
     _check(load().kvs_select_critical(_ptr(k_cached), _ptr(k_new), _ptr(row_off), n_agents,
                                       max_rows_per_agent, row_elems, ratio, _ptr(idx_out), _ptr(idx_off),
                                       _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)))
+
+
+def kvs_select_critical_noalloc(k_cached, k_new, row_off, n_agents, max_rows_per_agent, row_elems, ratio,
+                                idx_out, idx_off, stream=None):
+    """kvs_select_critical without a workspace argument: the library's fixed
+    device scratch (2^20 rows) is used instead; nothing is allocated."""
+    _check(load().kvs_select_critical_noalloc(_ptr(k_cached), _ptr(k_new), _ptr(row_off), n_agents,
+                                              max_rows_per_agent, row_elems, ratio, _ptr(idx_out), _ptr(idx_off),
+                                              _stream(stream)))
 
 
 def kvs_decode_attn(pool: Pool, layer, q, n_q_heads, block_table, max_blocks, seq_len, n_seq,
