@@ -53,6 +53,8 @@ def parse():
     ap.add_argument("--no-rope", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--layers", type=int, default=32)
+    ap.add_argument("--workload", default="mha7b", choices=["mha7b", "tiny", "gqa_fanout", "allgather", "q4"],
+                    help="mha7b is the headline workload; the others print a per-workload record for profiling")
     return ap.parse_args()
 
 
@@ -218,6 +220,9 @@ def main():
     from shared_paged_kv_gb300 import kvs as K
     from shared_paged_kv_gb300 import workloads as W
 
+    if args.workload != "mha7b":
+        return bench_workload(args, torch, K, W)
+
     if world > 1:
         dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
     dev = torch.device("cuda", local_rank)
@@ -366,6 +371,112 @@ def main():
         print(json.dumps(line))
     if world > 1:
         dist.destroy_process_group()
+    return 0
+
+
+def bench_workload(args, torch, K, W):
+    """One-GPU record for a non-headline workload: GPU dedup + decode attention
+    on every layer (Q4: attention only), timed with CUDA events."""
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream()
+    mk = {"tiny": W.make_tiny, "gqa_fanout": W.make_gqa_fanout, "allgather": W.make_allgather, "q4": W.make_q4}
+    w = mk[args.workload]()
+    L = min(w.n_layers, args.layers)
+    N, H, D, B = w.n_seq, w.n_kv_heads, w.head_dim, w.block_tokens
+    q4 = args.workload == "q4"
+    tokens = torch.from_numpy(w.tokens.view(np.int32)).to(dev)
+    seq_off = torch.from_numpy(w.seq_off).to(dev)
+    seq_len = torch.from_numpy(w.seq_len).to(dev)
+    tier = torch.from_numpy(w.tier.view(np.int32)).to(dev) if (w.tier != 0).any() else None
+    so = sb = None
+    if w.seg_start_off is not None:
+        so = torch.from_numpy(w.seg_start_off).to(dev)
+        sb = torch.from_numpy(w.seg_start_blocks).to(dev)
+    fp = torch.zeros((N, w.max_blocks), dtype=torch.int64, device=dev)
+    table = torch.zeros((N, w.max_blocks), dtype=torch.int32, device=dev)
+    # dedup once on a pool whose capacity is the upper bound, to size the slabs
+    dummy = torch.zeros(16, dtype=torch.int16, device=dev)
+    if q4:
+        d8 = torch.zeros(16, dtype=torch.uint8, device=dev)
+        dh = torch.zeros(16, dtype=torch.float16, device=dev)
+        probe = K.kvs_pool_create(1, H, D, B, K.KVS_DTYPE_Q4G64, w.capacity_blocks, N, [d8], [d8], [dh], [dh])
+    else:
+        probe = K.kvs_pool_create(1, H, D, B, K.KVS_DTYPE_BF16, w.capacity_blocks, N, [dummy], [dummy])
+    refc = torch.zeros(w.capacity_blocks, dtype=torch.int32, device=dev)
+    nphys = torch.zeros(1, dtype=torch.int32, device=dev)
+    ws_d = torch.zeros(K.kvs_workspace_size(probe, K.KVS_OP_DEDUP, N, w.max_blocks), dtype=torch.uint8, device=dev)
+    K.kvs_fingerprint_dedup(probe, tokens, seq_off, N, tier, so, sb, fp, table, w.max_blocks, refc, nphys, ws_d)
+    cap = int(nphys.item())
+    gen = torch.Generator(device=dev).manual_seed(7)
+    if q4:
+        ks = [torch.empty(cap * H * B * D // 2, dtype=torch.uint8, device=dev) for _ in range(L)]
+        vs = [torch.empty_like(ks[0]) for _ in range(L)]
+        ksb = [torch.empty(cap * H * B * 4, dtype=torch.float16, device=dev) for _ in range(L)]
+        vsb = [torch.empty_like(ksb[0]) for _ in range(L)]
+        pool = K.kvs_pool_create(L, H, D, B, K.KVS_DTYPE_Q4G64, cap, N, ks, vs, ksb, vsb)
+        ids = torch.arange(cap, dtype=torch.int32, device=dev)
+        for l in range(L):
+            src_k = torch.randn((cap, H, B, D), generator=gen, device=dev, dtype=torch.bfloat16)
+            src_v = torch.randn((cap, H, B, D), generator=gen, device=dev, dtype=torch.bfloat16)
+            K.kvs_quantize_q4(pool, l, src_k.view(torch.int16), src_v.view(torch.int16), ids, cap)
+            del src_k, src_v
+        per_launch = cap * H * B * 144
+    else:
+        ks = [torch.randn((cap, H, B, D), generator=gen, device=dev, dtype=torch.bfloat16).view(torch.int16) for _ in range(L)]
+        vs = [torch.randn((cap, H, B, D), generator=gen, device=dev, dtype=torch.bfloat16).view(torch.int16) for _ in range(L)]
+        nd = w.diff_capacity_blocks
+        dks = [(0.1 * torch.randn((nd, H, B, D), generator=gen, device=dev)).to(torch.bfloat16).view(torch.int16)
+               for _ in range(L)] if nd else None
+        dvs = [(0.1 * torch.randn((nd, H, B, D), generator=gen, device=dev)).to(torch.bfloat16).view(torch.int16)
+               for _ in range(L)] if nd else None
+        pool = K.kvs_pool_create(L, H, D, B, K.KVS_DTYPE_BF16, cap, N, ks, vs, dk_layers=dks, dv_layers=dvs,
+                                 diff_capacity_blocks=nd)
+        per_launch = (cap + nd) * H * B * D * 2 * 2
+    per_launch += N * w.n_q_heads * D * (2 + 4) + N * w.max_blocks * 4 * (2 if w.diff_table is not None else 1)
+    refc = torch.zeros(cap, dtype=torch.int32, device=dev)
+    q = torch.randn((L, N, w.n_q_heads, D), generator=gen, device=dev, dtype=torch.bfloat16)
+    out = torch.zeros((L, N, w.n_q_heads, D), dtype=torch.float32, device=dev)
+    dt = torch.from_numpy(w.diff_table).to(dev) if w.diff_table is not None else None
+    ro = torch.from_numpy(w.rope_off).to(dev) if w.rope_off is not None else None
+    rs = torch.from_numpy(w.rope_segs).to(dev) if w.rope_segs is not None else None
+    op = K.KVS_OP_DECODE_ATTN_Q4 if q4 else K.KVS_OP_DECODE_ATTN
+    ws_a = torch.zeros(K.kvs_workspace_size(pool, op, N, w.max_blocks, w.n_q_heads), dtype=torch.uint8, device=dev)
+    ev_a = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps * L)]
+    ev_b = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps * L)]
+
+    def step(i=None):
+        if not q4:
+            K.kvs_fingerprint_dedup(pool, tokens, seq_off, N, tier, so, sb, fp, table, w.max_blocks, refc, nphys, ws_d)
+        for l in range(L):
+            if i is not None:
+                ev_a[i * L + l].record(stream)
+            if q4:
+                K.kvs_decode_attn_q4(pool, l, q[l], w.n_q_heads, table, w.max_blocks, seq_len, N, w.scale, out[l], ws_a)
+            else:
+                K.kvs_decode_attn(pool, l, q[l], w.n_q_heads, table, w.max_blocks, seq_len, N, dt, ro, rs, w.theta,
+                                  w.scale, out[l], ws_a)
+            if i is not None:
+                ev_b[i * L + l].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    flags = K.kvs_pool_check(pool)
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for i in range(args.steps):
+        step(i)
+    t1.record(stream)
+    torch.cuda.synchronize()
+    ms_step = t0.elapsed_time(t1) / args.steps
+    attn_ms = sum(a.elapsed_time(b) for a, b in zip(ev_a, ev_b)) / len(ev_a)
+    peak, kind = read_peaks()
+    print(json.dumps({"workload": args.workload, "tokens_per_s": N / (ms_step * 1e-3), "ms_per_step": ms_step,
+                      "layers": L, "attn_avg_ms": attn_ms, "attn_bytes_per_launch": per_launch,
+                      "attn_gbs": per_launch / (attn_ms * 1e-3) / 1e9,
+                      "attn_frac_of_measured_peak": per_launch / (attn_ms * 1e-3) / 1e9 / peak,
+                      "n_phys": cap, "status_flags": flags}))
     return 0
 
 

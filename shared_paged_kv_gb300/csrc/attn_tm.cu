@@ -25,6 +25,8 @@
 //  * Rotation is applied to the query (R(-delta) q, as a bf16 hi + lo pair)
 //    whenever the RoPE segment changes; the diff overlay adds DK / DV tiles
 //    through the same MMAs (linearity).
+#include <algorithm>
+
 #include "common.cuh"
 #include "internal.h"
 
@@ -53,9 +55,15 @@ constexpr int kTmWarps = 4;
 // Ring stages per warp.  A stage holds one block's K and V tiles; a block
 // that carries a mirror diff takes two consecutive positions (K/V, then
 // DK/DV), so diff blocks need no larger stages.
+#ifndef KVS_TM_STAGES_D128
+#define KVS_TM_STAGES_D128 2
+#endif
+#ifndef KVS_TM_MIN_CTAS
+#define KVS_TM_MIN_CTAS 3
+#endif
 template <int D, bool DIFF>
 __host__ __device__ constexpr int tm_stages() {
-  return DIFF ? 3 : (D == 128 ? 2 : 4);
+  return DIFF ? 3 : (D == 128 ? KVS_TM_STAGES_D128 : 4);
 }
 
 template <int D, bool DIFF>
@@ -71,7 +79,7 @@ __device__ __forceinline__ uint32_t movm_t(uint32_t x) {
 }
 
 template <int D, bool DIFF, bool ROPE>
-__global__ void __launch_bounds__(128, 3)
+__global__ void __launch_bounds__(128, KVS_TM_MIN_CTAS)
 attn_tm_kernel(const __grid_constant__ TmParams p, const __grid_constant__ CUtensorMap tk,
                const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdk,
                const __grid_constant__ CUtensorMap tdv) {
@@ -96,17 +104,24 @@ attn_tm_kernel(const __grid_constant__ TmParams p, const __grid_constant__ CUten
   }
   __syncwarp();
 
-  // ------------------------------------------------ producer (lane 0) state
-  int p_item = -1, p_a = 0, p_h = 0, p_b = 0, p_bend = 0;
+  // ------------------------------------------ producer state (warp-uniform)
+  // The whole warp runs the producer logic; lane 0 alone issues the atomics
+  // and the TMA copies.  When an item is claimed, lane j loads the item's
+  // j-th block-table (and diff-table) entry once, so issuing a block costs a
+  // shuffle instead of a global load.
+  int p_item = -1, p_a = 0, p_h = 0, p_b = 0, p_b0 = 0, p_bend = 0;
+  int tab_ent = -1, dif_ent = -1;
   bool p_done = false;
   auto seq_blocks = [&](int a) {
     int L = p.seq_len[a];
     if (L < 0 || L > p.max_blocks * B) L = L < 0 ? 0 : p.max_blocks * B;
     return (L + B - 1) / B;
   };
-  auto claim = [&]() {   // lane 0 only: next non-empty item, or done
+  auto claim = [&]() {
     while (true) {
-      const int id = atomicAdd(p.sched, 1);
+      int id = 0;
+      if (lane == 0) id = atomicAdd(p.sched, 1);
+      id = __shfl_sync(0xffffffffu, id, 0);
       if (id >= p.n_items) {
         p_done = true;
         return;
@@ -114,40 +129,52 @@ attn_tm_kernel(const __grid_constant__ TmParams p, const __grid_constant__ CUten
       const int a = id % p.n_seq, rest = id / p.n_seq;
       const int h = rest % p.hkv, ch = rest / p.hkv;
       const int Lr = p.seq_len[a];
-      if (ch == 0 && (Lr < 0 || Lr > p.max_blocks * B)) set_err(p.status, KVS_DEVERR_SEQ_LEN);
+      if (lane == 0 && ch == 0 && (Lr < 0 || Lr > p.max_blocks * B)) set_err(p.status, KVS_DEVERR_SEQ_LEN);
       const int nb = seq_blocks(a);
       if (nb == 0) {
         if (ch == 0)
-          for (int i = 0; i < p.g * D; ++i) p.out[((size_t)a * p.hq + h * p.g) * D + i] = 0.f;
+          for (int i = lane; i < p.g * D; i += 32) p.out[((size_t)a * p.hq + h * p.g) * D + i] = 0.f;
         continue;
       }
       const int b0 = ch * p.ib;
       if (b0 >= nb) continue;
-      p_item = id; p_a = a; p_h = h; p_b = b0; p_bend = min(b0 + p.ib, nb);
+      p_item = id; p_a = a; p_h = h; p_b = b0; p_b0 = b0; p_bend = min(b0 + p.ib, nb);
+      tab_ent = lane < p_bend - b0 ? __ldg(p.block_table + (size_t)a * p.max_blocks + b0 + lane) : -1;
+      if (DIFF) dif_ent = lane < p_bend - b0 ? __ldg(p.diff_table + (size_t)a * p.max_blocks + b0 + lane) : -1;
       return;
     }
   };
   int pend_drow = -1;   // a diff tile pair still to issue for the last block
-  auto issue = [&](int s) {   // lane 0 only
+  auto issue = [&](int s) {   // whole warp; lane 0 issues
     uint64_t* bar = &bars[warp][s];
     uint8_t* st = wbase + s * STAGE;
     if (DIFF && pend_drow >= 0) {
-      mbar_arrive_expect_tx(bar, 2 * TILE);
-      tma_load_kv_tile<D>(st, &tdk, pend_drow, bar);
-      tma_load_kv_tile<D>(st + TILE, &tdv, pend_drow, bar);
+      if (lane == 0) {
+        mbar_arrive_expect_tx(bar, 2 * TILE);
+        tma_load_kv_tile<D>(st, &tdk, pend_drow, bar);
+        tma_load_kv_tile<D>(st + TILE, &tdv, pend_drow, bar);
+      }
       pend_drow = -1;
       return;
     }
     if (!p_done && p_b >= p_bend) claim();
     if (p_done) {
-      st_item[warp][s] = -1;
-      mbar_arrive(bar);
+      if (lane == 0) {
+        st_item[warp][s] = -1;
+        mbar_arrive(bar);
+      }
       return;
     }
     const int b = p_b++;
+    const int phys = __shfl_sync(0xffffffffu, tab_ent, b - p_b0);
+    const int did = DIFF ? __shfl_sync(0xffffffffu, dif_ent, b - p_b0) : -1;
+    if (lane != 0) {
+      if (DIFF && phys >= 0 && phys < p.capacity && did >= 0 && did < p.diff_capacity)
+        pend_drow = (did * p.hkv + p_h) * B;
+      return;
+    }
     st_item[warp][s] = p_item;
     st_block[warp][s] = b;
-    const int phys = __ldg(p.block_table + (size_t)p_a * p.max_blocks + b);
     if (phys < 0 || phys >= p.capacity) {
       set_err(p.status, KVS_DEVERR_BLOCK_ID);
       st_block[warp][s] = b | (1 << 29);   // nothing loaded: skip this block
@@ -155,7 +182,6 @@ attn_tm_kernel(const __grid_constant__ TmParams p, const __grid_constant__ CUten
       return;
     }
     if (DIFF) {
-      const int did = __ldg(p.diff_table + (size_t)p_a * p.max_blocks + b);
       if (did >= p.diff_capacity) {
         set_err(p.status, KVS_DEVERR_DIFF_ID);
       } else if (did >= 0) {
@@ -168,8 +194,7 @@ attn_tm_kernel(const __grid_constant__ TmParams p, const __grid_constant__ CUten
     tma_load_kv_tile<D>(st, &tk, row, bar);
     tma_load_kv_tile<D>(st + TILE, &tv, row, bar);
   };
-  if (lane == 0)
-    for (int s = 0; s < S; ++s) issue(s);
+  for (int s = 0; s < S; ++s) issue(s);
 
   // --------------------------------------------------- per-lane constants
   uint32_t koff[KS], voff[KS];
@@ -255,28 +280,46 @@ attn_tm_kernel(const __grid_constant__ TmParams p, const __grid_constant__ CUten
     last = __shfl_sync(0xffffffffu, last, 0);
     if (!last) return;
     __threadfence();   // acquire side: other warps' splits are visible
-    // merge: item ids of (ca, ch_) for chunks 0..nch-1
+    // merge the nch splits of (ca, ch_): chunk k's split is item ((k*hkv + ch_)*n_seq + ca).
+    // Lanes first take one split each for the max and the normaliser; then
+    // every lane owns D/32 consecutive columns and walks the splits with
+    // several independent loads in flight.
+    constexpr int CPL = D / 32;                 // columns per lane
+    const size_t kstride = (size_t)p.hkv * p.n_seq;
+    const size_t it0 = (size_t)ch_ * p.n_seq + ca;
     for (int r = 0; r < p.g; ++r) {
       float M = -INFINITY;
-      for (int k = 0; k < nch; ++k) {
-        const size_t it = ((size_t)k * p.hkv + ch_) * p.n_seq + ca;
-        M = fmaxf(M, __ldcg(p.part_ml + (it * p.g + r) * 2));
-      }
-      float Ls = 0.f, v[D / 32];
+      for (int k = lane; k < nch; k += 32) M = fmaxf(M, __ldcg(p.part_ml + ((it0 + k * kstride) * p.g + r) * 2));
 #pragma unroll
-      for (int j = 0; j < D / 32; ++j) v[j] = 0.f;
+      for (int o = 16; o; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+      float Ls = 0.f;
+      float v[CPL];
+#pragma unroll
+      for (int j = 0; j < CPL; ++j) v[j] = 0.f;
+      // no shuffles in this loop: every lane reads the (m, l) of split k
+      // itself (one broadcast transaction), so the loads of several splits
+      // can be in flight at once
+#pragma unroll 8
       for (int k = 0; k < nch; ++k) {
-        const size_t it = ((size_t)k * p.hkv + ch_) * p.n_seq + ca;
-        const float2 ml = __ldcg(reinterpret_cast<const float2*>(p.part_ml + (it * p.g + r) * 2));
-        if (!(ml.y > 0.f)) continue;
-        const float wgt = fast_exp2(ml.x - M);
+        const size_t it = (it0 + k * kstride) * p.g + r;
+        const float2 ml = __ldcg(reinterpret_cast<const float2*>(p.part_ml + it * 2));
+        const float* src = p.part + it * D + lane * CPL;
+        float x[CPL];
+        if (CPL == 4) {
+          const float4 t = __ldcg(reinterpret_cast<const float4*>(src));
+          x[0] = t.x; x[1 % CPL] = t.y; x[2 % CPL] = t.z; x[3 % CPL] = t.w;
+        } else {
+          const float2 t = __ldcg(reinterpret_cast<const float2*>(src));
+          x[0] = t.x; x[1 % CPL] = t.y;
+        }
+        const float wgt = ml.y > 0.f ? fast_exp2(ml.x - M) : 0.f;
         Ls += wgt * ml.y;
 #pragma unroll
-        for (int j = 0; j < D / 32; ++j) v[j] += wgt * __ldcg(p.part + (it * p.g + r) * D + lane + 32 * j);
+        for (int j = 0; j < CPL; ++j) v[j] += wgt * x[j];
       }
-      float* o = p.out + ((size_t)ca * p.hq + ch_ * p.g + r) * D;
+      float* o = p.out + ((size_t)ca * p.hq + ch_ * p.g + r) * D + lane * CPL;
 #pragma unroll
-      for (int j = 0; j < D / 32; ++j) o[lane + 32 * j] = Ls > 0.f ? v[j] / Ls : 0.f;
+      for (int j = 0; j < CPL; ++j) o[j] = Ls > 0.f ? v[j] / Ls : 0.f;
     }
   };
 
@@ -314,12 +357,16 @@ attn_tm_kernel(const __grid_constant__ TmParams p, const __grid_constant__ CUten
     }
     if (loaded) {
       if (ROPE && (b < seg_lo || b >= seg_hi)) {
-        int found = 0x7fffffff, fd = 0, flo = 0, fhi = 0;
+        // find the segment covering b; if none, the gap around b (delta 0)
+        // is cached instead, so unrotated stretches are not rescanned
+        int found = 0x7fffffff, fd = 0, flo = 0, fhi = 0, gap_lo = 0, gap_hi = 0x7fffffff;
         for (int e = seg_beg + lane; e < seg_end; e += 32) {
           const int4 sg = __ldg(p.rope_segs + e);
           if (b >= sg.x && b < sg.x + sg.y && e < found) {
             found = e; fd = sg.z; flo = sg.x; fhi = sg.x + sg.y;
           }
+          if (sg.x > b) gap_hi = min(gap_hi, sg.x);
+          if (sg.x + sg.y <= b) gap_lo = max(gap_lo, sg.x + sg.y);
         }
 #pragma unroll
         for (int o = 16; o; o >>= 1) {
@@ -328,12 +375,14 @@ attn_tm_kernel(const __grid_constant__ TmParams p, const __grid_constant__ CUten
           const int lo2 = __shfl_xor_sync(0xffffffffu, flo, o);
           const int hi2 = __shfl_xor_sync(0xffffffffu, fhi, o);
           if (f2 < found) { found = f2; fd = d2; flo = lo2; fhi = hi2; }
+          gap_hi = min(gap_hi, __shfl_xor_sync(0xffffffffu, gap_hi, o));
+          gap_lo = max(gap_lo, __shfl_xor_sync(0xffffffffu, gap_lo, o));
         }
         int nd = 0;
         if (found != 0x7fffffff) {
           nd = fd; seg_lo = flo; seg_hi = fhi;
         } else {
-          seg_lo = seg_hi = 0;
+          seg_lo = gap_lo; seg_hi = gap_hi;
         }
         if (nd <= -(1 << 18) || nd >= (1 << 18)) {
           if (lane == 0) set_err(p.status, KVS_DEVERR_ROPE_RANGE);
@@ -411,11 +460,9 @@ attn_tm_kernel(const __grid_constant__ TmParams p, const __grid_constant__ CUten
       }
     }
     __syncwarp();
-    if (lane == 0) {
-      fence_proxy_async_smem();
-      issue(s);
-      if (has_diff) issue(s2);
-    }
+    if (lane == 0) fence_proxy_async_smem();
+    issue(s);
+    if (has_diff) issue(s2);
     i += has_diff ? 2 : 1;
   }
   if (cur >= 0) flush();
@@ -441,7 +488,9 @@ static kvs_status launch_tm(TmParams& prm, const kvs_pool* pool, int layer, cuda
         blocks_per_sm < 1)
       return fail(KVS_ERR_CUDA, "decode_attn: cannot configure the token-major kernel");
   }
-  const int grid = pool->num_sms * blocks_per_sm;
+  // persistent grid: every SM filled once, but never more warps than items
+  // (idle warps would only contend on the work counter)
+  const int grid = std::max(1, std::min(pool->num_sms * blocks_per_sm, (prm.n_items + kTmWarps - 1) / kTmWarps));
   prm.total_warps = grid * kTmWarps;
   const CUtensorMap& dk = DIFF ? pool->tdk[layer] : pool->tk[layer];
   const CUtensorMap& dv = DIFF ? pool->tdv[layer] : pool->tv[layer];
@@ -450,15 +499,18 @@ static kvs_status launch_tm(TmParams& prm, const kvs_pool* pool, int layer, cuda
   return check_launch("decode_attn");
 }
 
-// Work-item size: about eight items per resident warp so the dynamic
-// schedule balances ragged contexts while the per-item split write and
-// arrival stay rare.
+// Work-item size (blocks): about eight items per resident warp so the dynamic
+// schedule balances ragged contexts, but at least max_blocks/64 so one
+// (sequence, kv head) never has more than ~64 splits to merge, and at most
+// 32 (one block-table entry per lane).
 int tm_item_blocks(const kvs_pool* pool, int n_seq, int max_blocks) {
   const long long work = (long long)n_seq * pool->desc.num_kv_heads * max_blocks;
-  const long long warps = (long long)pool->num_sms * 3 * kTmWarps;
+  const long long warps = (long long)pool->num_sms * KVS_TM_MIN_CTAS * kTmWarps;
   long long ib = work / (warps * 8);
+  const long long min_ib = (max_blocks + 63) / 64;
+  if (ib < min_ib) ib = min_ib;
   int r = 4;
-  while (r < ib && r < 64) r <<= 1;
+  while (r < ib && r < 32) r <<= 1;
   return r;
 }
 

@@ -184,7 +184,8 @@ __device__ __forceinline__ void split_bf16(float x, float y, uint32_t& hi, uint3
 // into c0 + c1 + c2 + c3 where c0, c1, c2 hold 6 fraction bits each at fixed
 // positions (2^-1..2^-6, 2^-7..2^-12, 2^-13..2^-18), so delta*c0..c2 are exact
 // in float32 and their fractional parts are exact; delta*c3 < 1 carries only
-// float32 rounding.  The reduced turn count is fed to sincospif.
+// float32 rounding.  The reduced angle lies in [-pi, pi], where the hardware
+// __sincosf is accurate to about 4e-7 absolute.
 struct RopeSplit {
   float c[4][64];   // [piece][frequency index], up to head_dim 128
 };
@@ -196,7 +197,7 @@ __device__ __forceinline__ void rope_cos_sin(const RopeSplit& rs, int i, int del
   float t2 = d * rs.c[2][i];
   float turns = (t0 - floorf(t0)) + (t1 - floorf(t1)) + (t2 - floorf(t2)) + d * rs.c[3][i];
   turns -= rintf(turns);
-  sincospif(2.0f * turns, &sn, &cs);
+  __sincosf(6.28318530717958647692f * turns, &sn, &cs);
 }
 
 }  // namespace kvs

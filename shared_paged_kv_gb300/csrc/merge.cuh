@@ -28,7 +28,10 @@ __device__ __forceinline__ bool arrive_last(int32_t* counter, int expected, int*
   return last;
 }
 
-// 128-thread CTA merge of nsplit splits for g rows of width D.
+// 128-thread CTA merge of nsplit splits for g rows of width D: one warp per
+// row finds the max and the normaliser with its lanes spread over the
+// splits; then every thread accumulates a 4-column slice of a row, walking the
+// splits with the loop unrolled so several loads are in flight.
 template <int D>
 __device__ __forceinline__ void merge_splits(const float* part, const float* part_ml, size_t s0, int nsplit, int g,
                                              float* out_rows, float* sM, float* sL) {
@@ -41,7 +44,7 @@ __device__ __forceinline__ void merge_splits(const float* part, const float* par
     float Ls = 0.f;
     for (int s = lane; s < nsplit; s += 32) {
       const float2 ml = __ldcg(reinterpret_cast<const float2*>(part_ml + ((s0 + s) * g + r) * 2));
-      if (ml.y > 0.f) Ls += fast_exp2(ml.x - M) * ml.y;
+      Ls += ml.y > 0.f ? fast_exp2(ml.x - M) * ml.y : 0.f;
     }
 #pragma unroll
     for (int o = 16; o; o >>= 1) Ls += __shfl_xor_sync(0xffffffffu, Ls, o);
@@ -51,16 +54,20 @@ __device__ __forceinline__ void merge_splits(const float* part, const float* par
     }
   }
   __syncthreads();
-  for (int e = threadIdx.x; e < g * D; e += blockDim.x) {
-    const int r = e / D, col = e - r * D;
+  for (int e = threadIdx.x; e < g * (D / 4); e += blockDim.x) {
+    const int r = e / (D / 4), col = (e - r * (D / 4)) * 4;
     const float M = sM[r];
-    float v = 0.f;
+    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 8
     for (int s = 0; s < nsplit; ++s) {
       const float2 ml = __ldcg(reinterpret_cast<const float2*>(part_ml + ((s0 + s) * g + r) * 2));
-      if (ml.y > 0.f) v += fast_exp2(ml.x - M) * __ldcg(part + ((s0 + s) * g + r) * D + col);
+      const float4 x = __ldcg(reinterpret_cast<const float4*>(part + ((s0 + s) * g + r) * D + col));
+      const float ws = ml.y > 0.f ? fast_exp2(ml.x - M) : 0.f;
+      v.x += ws * x.x; v.y += ws * x.y; v.z += ws * x.z; v.w += ws * x.w;
     }
     const float Ls = sL[r];
-    out_rows[(size_t)r * D + col] = Ls > 0.f ? v / Ls : 0.f;
+    const float inv = Ls > 0.f ? 1.f / Ls : 0.f;
+    *reinterpret_cast<float4*>(out_rows + (size_t)r * D + col) = make_float4(v.x * inv, v.y * inv, v.z * inv, v.w * inv);
   }
 }
 

@@ -208,15 +208,22 @@ q4_attn_kernel(const __grid_constant__ Q4Params p, const __grid_constant__ CUten
         qb[grp][j][0] = pack_f16(x0, x1);
         qb[grp][j][1] = pack_f16(x2, x3);
       }
+    }
+    // per-group query sums: this lane's 16 values of row g per group, summed
+    // over the 4 lanes of the row, then fetched for columns 2c and 2c+1
 #pragma unroll
-      for (int cc = 0; cc < 2; ++cc) {
-        const int r = 2 * c + cc;
-        float sum = 0.f;
-        if (r < G_)
-          for (int d = 0; d < 64; ++d)
-            sum += __half2float(__float2half_rn(__uint_as_float((uint32_t)qbase[r * kQ4D + grp * 64 + d] << 16)));
-        qs[grp][cc] = sum;
+    for (int grp = 0; grp < 2; ++grp) {
+      float sum = 0.f;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const float2 a0 = __half22float2(*reinterpret_cast<const __half2*>(&qb[grp][j][0]));
+        const float2 a1 = __half22float2(*reinterpret_cast<const __half2*>(&qb[grp][j][1]));
+        sum += (a0.x + a0.y) + (a1.x + a1.y);
       }
+      sum += __shfl_xor_sync(0xffffffffu, sum, 1);
+      sum += __shfl_xor_sync(0xffffffffu, sum, 2);
+      qs[grp][0] = __shfl_sync(0xffffffffu, sum, (2 * c) * 4);
+      qs[grp][1] = __shfl_sync(0xffffffffu, sum, (2 * c + 1) * 4);
     }
   }
 
@@ -396,8 +403,10 @@ q4_attn_kernel(const __grid_constant__ Q4Params p, const __grid_constant__ CUten
 }
 
 AttnPlan q4_plan(const kvs_pool* pool, int n_seq, int max_blocks) {
+  // about one wave of CTAs (two resident per SM): each CTA streams several
+  // 256-token blocks so its pipeline start-up is amortised
   const long long work = (long long)n_seq * pool->desc.num_kv_heads * max_blocks;
-  const long long target = (long long)pool->num_sms * 8;
+  const long long target = (long long)pool->num_sms * 2;
   long long bpc = (work + target - 1) / target;
   if (bpc < 1) bpc = 1;
   if (bpc > 64) bpc = 64;
