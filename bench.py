@@ -256,13 +256,16 @@ def main():
     ev_b = [[torch.cuda.Event(enable_timing=True) for _ in range(L)] for _ in range(args.steps)]
 
     def step(i=None):
+        # block tables change per step: fingerprint + dedup, then one work
+        # plan for all layers, then attention on every layer
         K.kvs_fingerprint_dedup(pool, tokens, seq_off, N, None, None, None, fp, table, w.max_blocks, refc,
                                 nphys, ws_d)
+        K.kvs_decode_plan(pool, w.n_q_heads, table, w.max_blocks, seq_len, N, None, None, ws_a)
         for l in range(L):
             if i is not None:
                 ev_a[i][l].record(stream)
-            K.kvs_decode_attn(pool, l, q[l], w.n_q_heads, table, w.max_blocks, seq_len, N, None, None, None,
-                              w.theta, w.scale, out[l], ws_a)
+            K.kvs_decode_attn_planned(pool, l, q[l], w.n_q_heads, table, w.max_blocks, seq_len, N, None, None,
+                                      None, w.theta, w.scale, out[l], ws_a)
             if i is not None:
                 ev_b[i][l].record(stream)
 
@@ -321,9 +324,10 @@ def main():
             d_q.copy_(h_q, non_blocking=True)
             K.kvs_fingerprint_dedup(pool, d_tok, d_off, N, None, None, None, fp, table, w.max_blocks, refc,
                                     nphys, ws_d)
+            K.kvs_decode_plan(pool, w.n_q_heads, table, w.max_blocks, seq_len, N, None, None, ws_a)
             for l in range(L):
-                K.kvs_decode_attn(pool, l, d_q[l], w.n_q_heads, table, w.max_blocks, seq_len, N, None, None,
-                                  None, w.theta, w.scale, out[l], ws_a)
+                K.kvs_decode_attn_planned(pool, l, d_q[l], w.n_q_heads, table, w.max_blocks, seq_len, N, None,
+                                          None, None, w.theta, w.scale, out[l], ws_a)
             h_out.copy_(out, non_blocking=True)
             torch.cuda.synchronize()
 
@@ -448,14 +452,15 @@ def bench_workload(args, torch, K, W):
     def step(i=None):
         if not q4:
             K.kvs_fingerprint_dedup(pool, tokens, seq_off, N, tier, so, sb, fp, table, w.max_blocks, refc, nphys, ws_d)
+            K.kvs_decode_plan(pool, w.n_q_heads, table, w.max_blocks, seq_len, N, dt, ro, ws_a)
         for l in range(L):
             if i is not None:
                 ev_a[i * L + l].record(stream)
             if q4:
                 K.kvs_decode_attn_q4(pool, l, q[l], w.n_q_heads, table, w.max_blocks, seq_len, N, w.scale, out[l], ws_a)
             else:
-                K.kvs_decode_attn(pool, l, q[l], w.n_q_heads, table, w.max_blocks, seq_len, N, dt, ro, rs, w.theta,
-                                  w.scale, out[l], ws_a)
+                K.kvs_decode_attn_planned(pool, l, q[l], w.n_q_heads, table, w.max_blocks, seq_len, N, dt, ro, rs,
+                                          w.theta, w.scale, out[l], ws_a)
             if i is not None:
                 ev_b[i * L + l].record(stream)
 

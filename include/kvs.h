@@ -66,6 +66,7 @@ typedef enum {
 #define KVS_DEVERR_WAIT_TIMEOUT 0x10u /* a bounded wait on a TMA copy ran out */
 #define KVS_DEVERR_ROPE_RANGE   0x20u /* |position shift| >= 2^18 */
 #define KVS_DEVERR_JOB          0x40u /* a RoPE job addresses tokens outside its table row */
+#define KVS_DEVERR_PLAN         0x80u /* kvs_decode_attn_planned saw no matching plan in ws */
 
 typedef enum { KVS_DTYPE_BF16 = 0, KVS_DTYPE_Q4G64 = 1 } kvs_dtype;
 
@@ -235,6 +236,31 @@ kvs_status kvs_decode_attn(kvs_pool* pool, int32_t layer, const void* q_dev, int
                            const int32_t* rope_off_dev, const kvs_seg_rope* rope_segs_dev,
                            float theta, float scale, float* out_dev,
                            void* ws, size_t ws_bytes, cudaStream_t stream);
+
+/* The same attention split in two steps so that the per-step work plan is
+ * built once and reused by every layer (block tables change per decode step,
+ * not per layer).  kvs_decode_plan writes the plan into ws (sized by
+ * kvs_workspace_size(KVS_OP_DECODE_ATTN)): for query groups G <= 8 it records,
+ * for groups of R = 8/G sequences (R = 1 when rope_off is given), which
+ * logical blocks every member that reaches them holds in the same physical
+ * block, and lists the work items.  kvs_decode_attn_planned then runs one
+ * layer with arguments that must match the plan's call (same tables, seq_len,
+ * n_seq, max_blocks, n_q_heads, diff table presence and rope_off presence);
+ * a mismatch in shapes is detected on the device (KVS_DEVERR_PLAN, no output
+ * written), a change of table contents without a new plan is not.
+ * kvs_decode_attn is kvs_decode_plan followed by kvs_decode_attn_planned.
+ * Groups of more than 8 query heads need no plan (the calls accept them). */
+kvs_status kvs_decode_plan(kvs_pool* pool, int32_t n_q_heads, const int32_t* block_table_dev,
+                           int32_t max_blocks, const int32_t* seq_len_dev, int32_t n_seq,
+                           const int32_t* diff_table_dev, const int32_t* rope_off_dev,
+                           void* ws, size_t ws_bytes, cudaStream_t stream);
+kvs_status kvs_decode_attn_planned(kvs_pool* pool, int32_t layer, const void* q_dev, int32_t n_q_heads,
+                                   const int32_t* block_table_dev, int32_t max_blocks,
+                                   const int32_t* seq_len_dev, int32_t n_seq,
+                                   const int32_t* diff_table_dev,
+                                   const int32_t* rope_off_dev, const kvs_seg_rope* rope_segs_dev,
+                                   float theta, float scale, float* out_dev,
+                                   void* ws, size_t ws_bytes, cudaStream_t stream);
 
 /* Decode attention reading a Q4G64 pool directly, dequantising in registers
  * ([Q4] §2.2).  Same meaning as kvs_decode_attn without diffs or rotation. */

@@ -425,39 +425,59 @@ static kvs_status launch_attn(const AttnParams& prm, const kvs_pool* pool, int l
 
 using namespace kvs;
 
-extern "C" kvs_status kvs_decode_attn(kvs_pool* pool, int32_t layer, const void* q_dev, int32_t n_q_heads,
-                                      const int32_t* block_table_dev, int32_t max_blocks,
-                                      const int32_t* seq_len_dev, int32_t n_seq, const int32_t* diff_table_dev,
-                                      const int32_t* rope_off_dev, const kvs_seg_rope* rope_segs_dev,
-                                      float theta, float scale, float* out_dev, void* ws, size_t ws_bytes,
-                                      cudaStream_t stream) {
+// Host checks shared by the decode-attention entry points.
+static kvs_status attn_check(kvs_pool* pool, int32_t layer, const void* q_dev, int32_t n_q_heads,
+                             const int32_t* block_table_dev, int32_t max_blocks, const int32_t* seq_len_dev,
+                             int32_t n_seq, const int32_t* diff_table_dev, const int32_t* rope_off_dev,
+                             const kvs_seg_rope* rope_segs_dev, float theta, const float* out_dev, const void* ws,
+                             size_t ws_bytes, bool need_q) {
   if (!pool) return fail(KVS_ERR_INVALID_ARG, "decode_attn: null pool");
   const kvs_pool_desc& d = pool->desc;
   if (d.dtype != KVS_DTYPE_BF16) return fail(KVS_ERR_INVALID_ARG, "decode_attn: pool is not bf16 (use kvs_decode_attn_q4)");
-  if (layer < 0 || layer >= d.num_layers) return fail(KVS_ERR_INVALID_ARG, "decode_attn: layer out of range");
+  if (need_q && (layer < 0 || layer >= d.num_layers)) return fail(KVS_ERR_INVALID_ARG, "decode_attn: layer out of range");
   if (n_seq < 0 || n_seq > d.max_seqs) return fail(KVS_ERR_CAPACITY, "decode_attn: n_seq exceeds the pool's max_seqs");
   if (n_seq == 0) return KVS_OK;
-  if (!q_dev || !block_table_dev || !seq_len_dev || !out_dev || !ws)
+  if (!block_table_dev || !seq_len_dev || !ws || (need_q && (!q_dev || !out_dev)))
     return fail(KVS_ERR_INVALID_ARG, "decode_attn: null pointer");
-  if (!aligned16(q_dev) || !aligned16(out_dev) || !aligned16(ws))
+  if ((need_q && (!aligned16(q_dev) || !aligned16(out_dev))) || !aligned16(ws))
     return fail(KVS_ERR_INVALID_ARG, "decode_attn: q, out and ws must be 16-byte aligned");
   if (max_blocks < 1) return fail(KVS_ERR_INVALID_ARG, "decode_attn: max_blocks must be >= 1");
   if (n_q_heads < 1 || n_q_heads % d.num_kv_heads) return fail(KVS_ERR_INVALID_ARG, "decode_attn: n_q_heads must be a multiple of num_kv_heads");
-  const int g = n_q_heads / d.num_kv_heads;
-  if (g > 16) return fail(KVS_ERR_UNSUPPORTED, "decode_attn: more than 16 query heads per KV head");
+  if (n_q_heads / d.num_kv_heads > 16) return fail(KVS_ERR_UNSUPPORTED, "decode_attn: more than 16 query heads per KV head");
   if (diff_table_dev && d.diff_capacity_blocks == 0) return fail(KVS_ERR_INVALID_ARG, "decode_attn: diff table given but the pool has no diff slabs");
-  if ((rope_off_dev == nullptr) != (rope_segs_dev == nullptr)) return fail(KVS_ERR_INVALID_ARG, "decode_attn: rope_off and rope_segs go together");
-  if (rope_off_dev && !(theta > 0.f)) return fail(KVS_ERR_INVALID_ARG, "decode_attn: theta must be positive");
+  if (need_q && (rope_off_dev == nullptr) != (rope_segs_dev == nullptr)) return fail(KVS_ERR_INVALID_ARG, "decode_attn: rope_off and rope_segs go together");
+  if (need_q && rope_off_dev && !(theta > 0.f)) return fail(KVS_ERR_INVALID_ARG, "decode_attn: theta must be positive");
   size_t need = 0;
   kvs_workspace_size(pool, KVS_OP_DECODE_ATTN, n_seq, max_blocks, n_q_heads, &need);
   if (ws_bytes < need) return fail(KVS_ERR_CAPACITY, "decode_attn: workspace too small");
+  return KVS_OK;
+}
+
+extern "C" kvs_status kvs_decode_plan(kvs_pool* pool, int32_t n_q_heads, const int32_t* block_table_dev,
+                                      int32_t max_blocks, const int32_t* seq_len_dev, int32_t n_seq,
+                                      const int32_t* diff_table_dev, const int32_t* rope_off_dev, void* ws,
+                                      size_t ws_bytes, cudaStream_t stream) {
+  kvs_status st = attn_check(pool, 0, nullptr, n_q_heads, block_table_dev, max_blocks, seq_len_dev, n_seq,
+                             diff_table_dev, rope_off_dev, nullptr, 1.f, nullptr, ws, ws_bytes, false);
+  if (st != KVS_OK || n_seq == 0) return st;
+  if (n_q_heads / pool->desc.num_kv_heads > kTmMaxGroup) return KVS_OK;   // the 16-row kernel needs no plan
+  return decode_plan_token_major(pool, n_q_heads, block_table_dev, max_blocks, seq_len_dev, n_seq, diff_table_dev,
+                                 rope_off_dev != nullptr, ws, stream);
+}
+
+static kvs_status attn_launch(kvs_pool* pool, int32_t layer, const void* q_dev, int32_t n_q_heads,
+                              const int32_t* block_table_dev, int32_t max_blocks, const int32_t* seq_len_dev,
+                              int32_t n_seq, const int32_t* diff_table_dev, const int32_t* rope_off_dev,
+                              const kvs_seg_rope* rope_segs_dev, float theta, float scale, float* out_dev, void* ws,
+                              cudaStream_t stream) {
+  const kvs_pool_desc& d = pool->desc;
+  const int g = n_q_heads / d.num_kv_heads;
   if (g <= kTmMaxGroup)
     return decode_attn_token_major(pool, layer, q_dev, n_q_heads, block_table_dev, max_blocks, seq_len_dev, n_seq,
                                    diff_table_dev, rope_off_dev, rope_segs_dev, theta, scale, out_dev, ws, stream);
   const AttnPlan plan = attn_plan(pool, n_seq, max_blocks);
   const long long grid = (long long)n_seq * d.num_kv_heads * plan.n_chunks;
   if (grid > 0x7fffffffll) return fail(KVS_ERR_CAPACITY, "decode_attn: grid too large");
-
   AttnParams prm{};
   prm.q = static_cast<const uint16_t*>(q_dev);
   prm.block_table = block_table_dev;
@@ -495,4 +515,33 @@ extern "C" kvs_status kvs_decode_attn(kvs_pool* pool, int32_t layer, const void*
                         : launch_attn<64, true, false>(prm, pool, layer, gr, stream);
   return rope ? launch_attn<64, false, true>(prm, pool, layer, gr, stream)
               : launch_attn<64, false, false>(prm, pool, layer, gr, stream);
+}
+
+extern "C" kvs_status kvs_decode_attn_planned(kvs_pool* pool, int32_t layer, const void* q_dev, int32_t n_q_heads,
+                                              const int32_t* block_table_dev, int32_t max_blocks,
+                                              const int32_t* seq_len_dev, int32_t n_seq,
+                                              const int32_t* diff_table_dev, const int32_t* rope_off_dev,
+                                              const kvs_seg_rope* rope_segs_dev, float theta, float scale,
+                                              float* out_dev, void* ws, size_t ws_bytes, cudaStream_t stream) {
+  kvs_status st = attn_check(pool, layer, q_dev, n_q_heads, block_table_dev, max_blocks, seq_len_dev, n_seq,
+                             diff_table_dev, rope_off_dev, rope_segs_dev, theta, out_dev, ws, ws_bytes, true);
+  if (st != KVS_OK || n_seq == 0) return st;
+  return attn_launch(pool, layer, q_dev, n_q_heads, block_table_dev, max_blocks, seq_len_dev, n_seq, diff_table_dev,
+                     rope_off_dev, rope_segs_dev, theta, scale, out_dev, ws, stream);
+}
+
+extern "C" kvs_status kvs_decode_attn(kvs_pool* pool, int32_t layer, const void* q_dev, int32_t n_q_heads,
+                                      const int32_t* block_table_dev, int32_t max_blocks,
+                                      const int32_t* seq_len_dev, int32_t n_seq, const int32_t* diff_table_dev,
+                                      const int32_t* rope_off_dev, const kvs_seg_rope* rope_segs_dev,
+                                      float theta, float scale, float* out_dev, void* ws, size_t ws_bytes,
+                                      cudaStream_t stream) {
+  kvs_status st = attn_check(pool, layer, q_dev, n_q_heads, block_table_dev, max_blocks, seq_len_dev, n_seq,
+                             diff_table_dev, rope_off_dev, rope_segs_dev, theta, out_dev, ws, ws_bytes, true);
+  if (st != KVS_OK || n_seq == 0) return st;
+  st = kvs_decode_plan(pool, n_q_heads, block_table_dev, max_blocks, seq_len_dev, n_seq, diff_table_dev,
+                       rope_off_dev, ws, ws_bytes, stream);
+  if (st != KVS_OK) return st;
+  return attn_launch(pool, layer, q_dev, n_q_heads, block_table_dev, max_blocks, seq_len_dev, n_seq, diff_table_dev,
+                     rope_off_dev, rope_segs_dev, theta, scale, out_dev, ws, stream);
 }

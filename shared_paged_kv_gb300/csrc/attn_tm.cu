@@ -8,23 +8,26 @@
 //
 // GB300 layout of the work:
 //  * The 16 tokens of a block are the M dimension of mma.sync m16n8k16 and
-//    the <= 8 query heads of a KV head are the N dimension: S^T = K q^T and
-//    O^T = V^T P^T.  K is the A operand straight from shared memory
-//    (ldmatrix), V^T too (ldmatrix.trans); P^T reaches the B operand through
-//    movmatrix.  Per 16-token block this is 8 + 16 MMAs (P enters as a bf16
-//    hi + lo pair) instead of padding the query group to 16 rows.
-//  * Persistent warps: the grid fills every SM once; each warp claims work
-//    items (sequence, kv head, run of IB logical blocks) from an atomic
-//    counter in chunk-major, sequence-minor order, so the sequences sharing a
-//    prefix stream the same physical blocks at about the same time and L2
-//    serves the repeats.  Lane 0 runs ahead of the warp's own compute through
-//    a ring of S TMA stages, claiming the next item as soon as it has issued
-//    the current one, so the pipeline never drains between items.
-//  * Each item leaves an (m, l, acc) split; the last warp to finish a
-//    (sequence, kv head) merges its splits (arrival counter, no spinning).
-//  * Rotation is applied to the query (R(-delta) q, as a bf16 hi + lo pair)
-//    whenever the RoPE segment changes; the diff overlay adds DK / DV tiles
-//    through the same MMAs (linearity).
+//    eight query columns are the N dimension: S^T = K q^T and O^T = V^T P^T.
+//    K is the A operand straight from shared memory (ldmatrix), V^T too
+//    (ldmatrix.trans); P^T reaches the B operand through movmatrix.  P and a
+//    rotated query enter as bf16 hi + lo pairs.
+//  * Shared blocks computed once (the INMS walkthrough §6.1 idea of sharing
+//    attention work on a common prefix, not only its KV): sequences are taken
+//    in groups of R = 8 / G (G = query heads per KV head), so one 8-column MMA
+//    tile holds the queries of a whole group.  A per-step plan marks, per
+//    group and logical block, whether every member that reaches that block
+//    holds the same physical block (no mirror diff, full block).  "Shared
+//    items" stream such blocks once for all members; "private items" stream
+//    each sequence's remaining blocks with only its own columns live.
+//  * Persistent warps claim items from an atomic counter over the plan's
+//    compact item list; lane 0 runs a ring of TMA stages ahead of the warp's
+//    compute across item boundaries.  Each item leaves one (m, l, acc) split
+//    per sequence it touched; the last warp to finish a (sequence, kv head)
+//    merges its splits (arrival counter, no spinning).
+//  * Rotation is applied to the query (R(-delta) q) whenever the RoPE segment
+//    changes; the diff overlay adds DK / DV tiles through the same MMAs.
+//    Calls with rotation use groups of one sequence.
 #include <algorithm>
 
 #include "common.cuh"
@@ -32,6 +35,231 @@
 
 namespace kvs {
 
+constexpr int kTmWarps = 4;
+constexpr int kTmMaxIb = 32;
+constexpr int kPlanMagic = 0x6b76730a;
+
+#ifndef KVS_TM_STAGES_D128
+#define KVS_TM_STAGES_D128 2
+#endif
+#ifndef KVS_TM_MIN_CTAS
+#define KVS_TM_MIN_CTAS 3
+#endif
+
+// Ring stages per warp.  A stage holds one block's K and V tiles; a block
+// that carries a mirror diff takes two consecutive positions (K/V, then
+// DK/DV), so diff blocks need no larger stages.
+template <int D>
+__host__ __device__ constexpr int tm_stages() {
+  return D == 128 ? KVS_TM_STAGES_D128 : 4;
+}
+
+template <int D>
+__host__ __device__ constexpr int tm_smem_bytes() {
+  return 1024 + kTmWarps * tm_stages<D>() * 2 * (16 * D * 2);
+}
+
+// ------------------------------------------------------------- plan layout
+struct TmLayout {
+  int R, ib, n_chunks, n_groups, words;
+  size_t max_entries;
+  size_t off_hdr, off_items, off_shb, off_pne, off_spm, off_tix, off_p1, off_p2, total;
+};
+
+static size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+// Work-item size (blocks): about eight items per resident warp, at least
+// max_blocks/64 (so one sequence never has more than ~64 splits per kind), at
+// most 32 (one block-table entry per lane).
+int tm_item_blocks(const kvs_pool* pool, int n_seq, int max_blocks) {
+  const long long work = (long long)n_seq * pool->desc.num_kv_heads * max_blocks;
+  const long long warps = (long long)pool->num_sms * KVS_TM_MIN_CTAS * kTmWarps;
+  long long ib = work / (warps * 8);
+  const long long min_ib = (max_blocks + 63) / 64;
+  if (ib < min_ib) ib = min_ib;
+  int r = 4;
+  while (r < ib && r < kTmMaxIb) r <<= 1;
+  return r;
+}
+
+static TmLayout tm_layout(const kvs_pool* pool, int n_seq, int max_blocks, int g, bool rope) {
+  TmLayout L{};
+  L.R = rope ? 1 : std::max(1, 8 / g);
+  L.ib = tm_item_blocks(pool, n_seq, max_blocks);
+  L.n_chunks = (max_blocks + L.ib - 1) / L.ib;
+  L.n_groups = (n_seq + L.R - 1) / L.R;
+  L.words = (max_blocks + 31) / 32;
+  L.max_entries = (size_t)(n_seq + L.n_groups) * L.n_chunks;
+  const size_t splits = (size_t)n_seq * pool->desc.num_kv_heads * L.n_chunks;
+  const size_t split_bytes = splits * g * (pool->desc.head_dim + 2) * sizeof(float);
+  size_t o = 0;
+  L.off_hdr = o; o = align256(o + 64);
+  L.off_items = o; o = align256(o + L.max_entries * sizeof(int2));
+  L.off_shb = o; o = align256(o + (size_t)n_seq * L.words * 4);
+  L.off_pne = o; o = align256(o + (size_t)n_seq * L.n_chunks);
+  L.off_spm = o; o = align256(o + (size_t)L.n_groups * L.n_chunks);
+  L.off_tix = o; o = align256(o + (size_t)n_seq * 4);
+  L.off_p1 = o; o = align256(o + split_bytes);
+  L.off_p2 = o; o = align256(o + (L.R > 1 ? split_bytes : 0));
+  L.total = o;
+  return L;
+}
+
+size_t tm_workspace_bytes(const kvs_pool* pool, int n_seq, int max_blocks, int g) {
+  // sized for grouping (no rotation), which is the larger layout
+  return tm_layout(pool, n_seq, max_blocks, g, false).total + 256;
+}
+
+// ------------------------------------------------------------------- plan
+struct PlanParams {
+  const int32_t* block_table;
+  const int32_t* seq_len;
+  const int32_t* diff_table;
+  int* hdr;
+  int2* items;
+  uint32_t* shb;
+  uint8_t* pne;
+  uint8_t* spm;
+  int* tix;
+  int n_seq, max_blocks, R, G, ib, n_chunks, n_groups, words, capacity, diff_capacity, hkv;
+};
+
+__device__ __forceinline__ int plan_seq_blocks(const int32_t* seq_len, int a, int max_blocks) {
+  int L = seq_len[a];
+  if (L < 0) L = 0;
+  if (L > max_blocks * 16) L = max_blocks * 16;
+  return (L + 15) / 16;
+}
+
+// One CTA of 1024 threads builds the whole plan (it depends on the tables
+// only, so one plan serves every layer of a decode step).
+__global__ void __launch_bounds__(1024) tm_plan_kernel(PlanParams pp) {
+  __shared__ int warp_sums[32];
+  __shared__ int s_carry;
+  const int tid = threadIdx.x, nt = blockDim.x;
+  for (int i = tid; i < pp.n_seq * pp.words; i += nt) pp.shb[i] = 0u;
+  __syncthreads();
+  // 1. group-shared blocks: the same valid physical block for every member
+  //    that reaches b (at least two), full blocks only, no mirror diff
+  if (pp.R > 1) {
+    for (int i = tid; i < pp.n_groups * pp.max_blocks; i += nt) {
+      const int gi = i / pp.max_blocks, b = i - gi * pp.max_blocks;
+      int cnt = 0, phys = -1;
+      bool ok = true;
+      uint32_t mask = 0;
+      for (int r = 0; r < pp.R; ++r) {
+        const int a = gi * pp.R + r;
+        if (a >= pp.n_seq) break;
+        const int L = min(max(pp.seq_len[a], 0), pp.max_blocks * 16);
+        if (b * 16 >= L) continue;
+        const int ph = pp.block_table[(size_t)a * pp.max_blocks + b];
+        const bool full = (b + 1) * 16 <= L;
+        const int d = pp.diff_table ? pp.diff_table[(size_t)a * pp.max_blocks + b] : -1;
+        if (!full || d >= 0 || ph < 0 || ph >= pp.capacity) ok = false;
+        if (cnt == 0) phys = ph;
+        else if (ph != phys) ok = false;
+        ++cnt;
+        mask |= 1u << r;
+      }
+      if (ok && cnt >= 2)
+        for (int r = 0; r < pp.R; ++r)
+          if ((mask >> r) & 1u) atomicOr(pp.shb + (size_t)(gi * pp.R + r) * pp.words + (b >> 5), 1u << (b & 31));
+    }
+  }
+  __syncthreads();
+  // 2. chunk occupancy: private chunks with unshared work; shared-chunk
+  //    participation per member
+  for (int i = tid; i < pp.n_seq * pp.n_chunks; i += nt) {
+    const int a = i / pp.n_chunks, c = i - a * pp.n_chunks;
+    const int nb = plan_seq_blocks(pp.seq_len, a, pp.max_blocks);
+    int any_priv = 0;
+    for (int b = c * pp.ib; b < min((c + 1) * pp.ib, nb); ++b)
+      any_priv |= !((pp.shb[(size_t)a * pp.words + (b >> 5)] >> (b & 31)) & 1u);
+    pp.pne[i] = (uint8_t)any_priv;
+  }
+  for (int i = tid; i < pp.n_groups * pp.n_chunks; i += nt) {
+    const int gi = i / pp.n_chunks, c = i - gi * pp.n_chunks;
+    uint32_t m = 0;
+    for (int r = 0; r < pp.R; ++r) {
+      const int a = gi * pp.R + r;
+      if (a >= pp.n_seq) break;
+      const int nb = plan_seq_blocks(pp.seq_len, a, pp.max_blocks);
+      for (int b = c * pp.ib; b < min((c + 1) * pp.ib, nb); ++b)
+        if ((pp.shb[(size_t)a * pp.words + (b >> 5)] >> (b & 31)) & 1u) {
+          m |= 1u << r;
+          break;
+        }
+    }
+    pp.spm[i] = (uint8_t)m;
+  }
+  __syncthreads();
+  // 3. arrivals expected per (sequence, kv head)
+  for (int a = tid; a < pp.n_seq; a += nt) {
+    int t = 0;
+    const int gi = a / pp.R, r = a - gi * pp.R;
+    for (int c = 0; c < pp.n_chunks; ++c) {
+      t += pp.pne[a * pp.n_chunks + c];
+      t += (pp.spm[gi * pp.n_chunks + c] >> r) & 1;
+    }
+    pp.tix[a] = t;
+  }
+  // 4. compact item list: shared items (group, chunk) first, then private
+  //    items (sequence, chunk), chunk-major
+  const int n_sh = pp.n_groups * pp.n_chunks, n_pr = pp.n_seq * pp.n_chunks;
+  const int total = n_sh + n_pr;
+  if (tid == 0) s_carry = 0;
+  __syncthreads();
+  const int lane = tid & 31, warp = tid >> 5;
+  for (int base = 0; base < total; base += nt) {
+    const int i = base + tid;
+    int keep = 0;
+    int2 item = make_int2(0, 0);
+    if (i < n_sh) {
+      const int c = i / pp.n_groups, gi = i - c * pp.n_groups;
+      keep = pp.spm[gi * pp.n_chunks + c] != 0;
+      item = make_int2((1 << 30) | gi, c);
+    } else if (i < total) {
+      const int j = i - n_sh;
+      const int c = j / pp.n_seq, a = j - c * pp.n_seq;
+      keep = pp.pne[a * pp.n_chunks + c];
+      item = make_int2(a, c);
+    }
+    int x = keep;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, x, o);
+      if (lane >= o) x += y;
+    }
+    if (lane == 31) warp_sums[warp] = x;
+    __syncthreads();
+    if (warp == 0) {
+      int w = warp_sums[lane];
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, w, o);
+        if (lane >= o) w += y;
+      }
+      warp_sums[lane] = w;
+    }
+    __syncthreads();
+    const int pos = s_carry + x - keep + (warp ? warp_sums[warp - 1] : 0);
+    if (keep) pp.items[pos] = item;
+    __syncthreads();
+    if (tid == nt - 1) s_carry = pos + keep;
+    __syncthreads();
+  }
+  if (tid == 0) {
+    pp.hdr[0] = s_carry;
+    pp.hdr[1] = kPlanMagic;
+    pp.hdr[2] = pp.n_seq;
+    pp.hdr[3] = pp.max_blocks;
+    pp.hdr[4] = pp.R;
+    pp.hdr[5] = pp.ib;
+    pp.hdr[6] = pp.hkv;
+  }
+}
+
+// -------------------------------------------------------------- attention
 struct TmParams {
   const uint16_t* q;
   const int32_t* block_table;
@@ -40,37 +268,23 @@ struct TmParams {
   const int32_t* rope_off;
   const int4* rope_segs;
   float* out;
-  float* part;       // [n_items][g][D]
-  float* part_ml;    // [n_items][g][2]
-  int32_t* tickets;  // [n_seq * hkv]
-  int32_t* sched;    // [0] work counter, [1] finished-warp counter
+  float* p1;          // private splits [n_seq][hkv][n_chunks][g][D]
+  float* p1_ml;       // [n_seq][hkv][n_chunks][g][2]
+  float* p2;          // shared splits, same shape
+  float* p2_ml;
+  const int* hdr;
+  const int2* items;
+  const uint32_t* shb;
+  const uint8_t* pne;
+  const uint8_t* spm;
+  const int* tix;
+  int32_t* tickets;   // [n_seq * hkv]
+  int32_t* sched;     // [0] work counter, [1] finished-warp counter
   uint32_t* status;
-  int max_blocks, n_seq, hkv, g, hq, ib, n_chunks, n_items, capacity, diff_capacity, total_warps;
+  int max_blocks, n_seq, hkv, g, hq, ib, n_chunks, R, capacity, diff_capacity, total_warps, words;
   float scale_log2;
   RopeSplit rs;
 };
-
-constexpr int kTmWarps = 4;
-
-// Ring stages per warp.  A stage holds one block's K and V tiles; a block
-// that carries a mirror diff takes two consecutive positions (K/V, then
-// DK/DV), so diff blocks need no larger stages.
-#ifndef KVS_TM_STAGES_D128
-#define KVS_TM_STAGES_D128 2
-#endif
-#ifndef KVS_TM_MIN_CTAS
-#define KVS_TM_MIN_CTAS 3
-#endif
-template <int D, bool DIFF>
-__host__ __device__ constexpr int tm_stages() {
-  return DIFF ? 3 : (D == 128 ? KVS_TM_STAGES_D128 : 4);
-}
-
-template <int D, bool DIFF>
-__host__ __device__ constexpr int tm_smem_bytes() {
-  return 1024 + kTmWarps * tm_stages<D, DIFF>() * 2 * (16 * D * 2);
-}
-
 
 __device__ __forceinline__ uint32_t movm_t(uint32_t x) {
   uint32_t y;
@@ -84,7 +298,7 @@ attn_tm_kernel(const __grid_constant__ TmParams p, const __grid_constant__ CUten
                const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdk,
                const __grid_constant__ CUtensorMap tdv) {
   constexpr int B = 16, TILE = B * D * 2, KS = D / 16;
-  constexpr int S = tm_stages<D, DIFF>();
+  constexpr int S = tm_stages<D>();
   constexpr int STAGE = 2 * TILE;
   extern __shared__ uint8_t smem_raw[];
   __shared__ uint64_t bars[kTmWarps][S];
@@ -92,6 +306,7 @@ attn_tm_kernel(const __grid_constant__ TmParams p, const __grid_constant__ CUten
   // block index; bit 30: the next position holds the block's diff tiles;
   // bit 29: the block id was out of range and nothing was loaded
   __shared__ int st_block[kTmWarps][S];
+  __shared__ int st_mask[kTmWarps][S];   // group members whose columns take this block
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, c = lane & 3;
@@ -104,43 +319,77 @@ attn_tm_kernel(const __grid_constant__ TmParams p, const __grid_constant__ CUten
   }
   __syncwarp();
 
-  // ------------------------------------------ producer state (warp-uniform)
-  // The whole warp runs the producer logic; lane 0 alone issues the atomics
-  // and the TMA copies.  When an item is claimed, lane j loads the item's
-  // j-th block-table (and diff-table) entry once, so issuing a block costs a
-  // shuffle instead of a global load.
-  int p_item = -1, p_a = 0, p_h = 0, p_b = 0, p_b0 = 0, p_bend = 0;
-  int tab_ent = -1, dif_ent = -1;
-  bool p_done = false;
+  // empty contexts produce zero output (they have no work items)
+  for (size_t e = (size_t)blockIdx.x * blockDim.x + threadIdx.x; e < (size_t)p.n_seq * p.hq * D;
+       e += (size_t)gridDim.x * blockDim.x)
+    if (p.seq_len[e / ((size_t)p.hq * D)] <= 0) p.out[e] = 0.f;
+
+  // the plan must have been built for this call's shapes
+  const bool plan_ok = p.hdr[1] == kPlanMagic && p.hdr[2] == p.n_seq && p.hdr[3] == p.max_blocks &&
+                       p.hdr[4] == p.R && p.hdr[5] == p.ib && p.hdr[6] == p.hkv;
+  if (!plan_ok && threadIdx.x == 0 && blockIdx.x == 0) set_err(p.status, KVS_DEVERR_PLAN);
+  const int n_claims = plan_ok ? p.hdr[0] * p.hkv : 0;
+  const int R = p.R;
   auto seq_blocks = [&](int a) {
     int L = p.seq_len[a];
     if (L < 0 || L > p.max_blocks * B) L = L < 0 ? 0 : p.max_blocks * B;
     return (L + B - 1) / B;
   };
+
+  // ------------------------------------------ producer state (warp-uniform)
+  // The whole warp runs the producer logic; lane 0 alone issues the atomics
+  // and the TMA copies.  When an item is claimed, lane j loads what block
+  // b0 + j of the item needs (physical id, diff id, sharing), so issuing a
+  // block costs shuffles instead of global loads.
+  int p_claim = -1, p_kind = 0, p_h = 0, p_b = 0, p_b0 = 0, p_bend = 0, p_mask = 0;
+  int tab_ent = -1, dif_ent = -1, aux_ent = 0;
+  bool p_done = false;
   auto claim = [&]() {
     while (true) {
       int id = 0;
       if (lane == 0) id = atomicAdd(p.sched, 1);
       id = __shfl_sync(0xffffffffu, id, 0);
-      if (id >= p.n_items) {
+      if (id >= n_claims) {
         p_done = true;
         return;
       }
-      const int a = id % p.n_seq, rest = id / p.n_seq;
-      const int h = rest % p.hkv, ch = rest / p.hkv;
-      const int Lr = p.seq_len[a];
-      if (lane == 0 && ch == 0 && (Lr < 0 || Lr > p.max_blocks * B)) set_err(p.status, KVS_DEVERR_SEQ_LEN);
-      const int nb = seq_blocks(a);
-      if (nb == 0) {
-        if (ch == 0)
-          for (int i = lane; i < p.g * D; i += 32) p.out[((size_t)a * p.hq + h * p.g) * D + i] = 0.f;
-        continue;
+      const int2 it = p.items[id / p.hkv];
+      const int h = id - (id / p.hkv) * p.hkv;
+      const int b0 = it.y * p.ib;
+      p_claim = id; p_h = h; p_b = b0; p_b0 = b0;
+      if (it.x >> 30) {   // shared item of group it.x & mask
+        const int gi = it.x & ((1 << 30) - 1);
+        p_kind = 1;
+        int nbmax = 0;
+        for (int r = 0; r < R; ++r)
+          if (gi * R + r < p.n_seq) nbmax = max(nbmax, seq_blocks(gi * R + r));
+        p_bend = min(b0 + p.ib, nbmax);
+        const int b = b0 + lane;
+        int msk = 0, ph = -1;
+        if (b < p_bend) {
+          for (int r = 0; r < R; ++r) {
+            const int a = gi * R + r;
+            if (a >= p.n_seq) break;
+            if ((p.shb[(size_t)a * p.words + (b >> 5)] >> (b & 31)) & 1u) {
+              msk |= 1 << r;
+              ph = p.block_table[(size_t)a * p.max_blocks + b];
+            }
+          }
+        }
+        tab_ent = ph;
+        aux_ent = msk;
+        dif_ent = -1;
+      } else {           // private item of sequence it.x
+        const int a = it.x;
+        p_kind = 0;
+        p_bend = min(b0 + p.ib, seq_blocks(a));
+        p_mask = 1 << (a % R);
+        const int b = b0 + lane;
+        const bool in = b < p_bend;
+        tab_ent = in ? __ldg(p.block_table + (size_t)a * p.max_blocks + b) : -1;
+        aux_ent = in ? (int)((p.shb[(size_t)a * p.words + (b >> 5)] >> (b & 31)) & 1u) : 1;   // 1 = skip
+        if (DIFF) dif_ent = in ? __ldg(p.diff_table + (size_t)a * p.max_blocks + b) : -1;
       }
-      const int b0 = ch * p.ib;
-      if (b0 >= nb) continue;
-      p_item = id; p_a = a; p_h = h; p_b = b0; p_b0 = b0; p_bend = min(b0 + p.ib, nb);
-      tab_ent = lane < p_bend - b0 ? __ldg(p.block_table + (size_t)a * p.max_blocks + b0 + lane) : -1;
-      if (DIFF) dif_ent = lane < p_bend - b0 ? __ldg(p.diff_table + (size_t)a * p.max_blocks + b0 + lane) : -1;
       return;
     }
   };
@@ -157,7 +406,25 @@ attn_tm_kernel(const __grid_constant__ TmParams p, const __grid_constant__ CUten
       pend_drow = -1;
       return;
     }
-    if (!p_done && p_b >= p_bend) claim();
+    int phys = -1, did = -1, mask = 0, b = 0;
+    while (true) {
+      if (!p_done && p_b >= p_bend) claim();
+      if (p_done) break;
+      const int j = p_b - p_b0;
+      b = p_b++;
+      const int ent = __shfl_sync(0xffffffffu, tab_ent, j);
+      const int aux = __shfl_sync(0xffffffffu, aux_ent, j);
+      if (p_kind == 0) {
+        if (aux) continue;          // computed by the group's shared item
+        mask = p_mask;
+        if (DIFF) did = __shfl_sync(0xffffffffu, dif_ent, j);
+      } else {
+        if (aux == 0) continue;     // not shared at this block
+        mask = aux;
+      }
+      phys = ent;
+      break;
+    }
     if (p_done) {
       if (lane == 0) {
         st_item[warp][s] = -1;
@@ -165,30 +432,20 @@ attn_tm_kernel(const __grid_constant__ TmParams p, const __grid_constant__ CUten
       }
       return;
     }
-    const int b = p_b++;
-    const int phys = __shfl_sync(0xffffffffu, tab_ent, b - p_b0);
-    const int did = DIFF ? __shfl_sync(0xffffffffu, dif_ent, b - p_b0) : -1;
-    if (lane != 0) {
-      if (DIFF && phys >= 0 && phys < p.capacity && did >= 0 && did < p.diff_capacity)
-        pend_drow = (did * p.hkv + p_h) * B;
-      return;
-    }
-    st_item[warp][s] = p_item;
-    st_block[warp][s] = b;
-    if (phys < 0 || phys >= p.capacity) {
+    const bool valid = phys >= 0 && phys < p.capacity;
+    const bool dval = DIFF && valid && did >= 0 && did < p.diff_capacity;
+    if (dval) pend_drow = (did * p.hkv + p_h) * B;
+    if (lane != 0) return;
+    st_item[warp][s] = p_claim;
+    st_mask[warp][s] = mask;
+    if (!valid) {
       set_err(p.status, KVS_DEVERR_BLOCK_ID);
       st_block[warp][s] = b | (1 << 29);   // nothing loaded: skip this block
       mbar_arrive(bar);
       return;
     }
-    if (DIFF) {
-      if (did >= p.diff_capacity) {
-        set_err(p.status, KVS_DEVERR_DIFF_ID);
-      } else if (did >= 0) {
-        st_block[warp][s] = b | (1 << 30);
-        pend_drow = (did * p.hkv + p_h) * B;
-      }
-    }
+    if (DIFF && did >= p.diff_capacity) set_err(p.status, KVS_DEVERR_DIFF_ID);
+    st_block[warp][s] = dval ? (b | (1 << 30)) : b;
     mbar_arrive_expect_tx(bar, 2 * TILE);
     const int row = (phys * p.hkv + p_h) * B;
     tma_load_kv_tile<D>(st, &tk, row, bar);
@@ -208,7 +465,12 @@ attn_tm_kernel(const __grid_constant__ TmParams p, const __grid_constant__ CUten
   }
 
   // ------------------------------------------------------ consumer state
-  int cur = -1, ca = 0, ch_ = 0, cL = 0;
+  // Column j of the 8-wide tile belongs to group member j / G (query head
+  // j % G).  colslot / colL: member and context length of this lane's two
+  // score columns (2c, 2c+1); slot 31 marks a column that is never live.
+  int cur = -1, ckind = 0, cidx = 0, ch_ = 0, cchunk = 0, cact = 0;
+  int colL[2] = {0, 0};
+  int colslot[2] = {31, 31};
   float m[2], l[2], acc[D / 16][4];
   uint32_t qb[KS][2];
   uint32_t qlo[ROPE ? KS : 1][2];
@@ -246,81 +508,133 @@ attn_tm_kernel(const __grid_constant__ TmParams p, const __grid_constant__ CUten
     }
   };
 
-  // write the current item's split, count it, merge if this was the last one
+  // merge every split of sequence a, kv head h: private splits of chunks with
+  // unshared work and shared splits of chunks a takes part in
+  constexpr int CPL = D / 32;   // columns per lane
+  auto merge = [&](int a, int h) {
+    const int gi = a / R, slot = a - gi * R;
+    const size_t sbase = ((size_t)a * p.hkv + h) * p.n_chunks;
+    for (int hh = 0; hh < p.g; ++hh) {
+      float M = -INFINITY, Ls = 0.f, v[CPL];
+#pragma unroll
+      for (int j = 0; j < CPL; ++j) v[j] = 0.f;
+      for (int pass = 0; pass < 2; ++pass) {
+        for (int c0 = 0; c0 < p.n_chunks; c0 += 32) {
+          // which splits of these 32 chunks exist: one ballot per kind
+          const int ck = c0 + lane;
+          const bool pv = ck < p.n_chunks && p.pne[a * p.n_chunks + ck];
+          const bool sv = ck < p.n_chunks && ((p.spm[gi * p.n_chunks + ck] >> slot) & 1);
+          const unsigned pm = __ballot_sync(0xffffffffu, pv), sm = __ballot_sync(0xffffffffu, sv);
+          if (pass == 0) {
+            // this lane's own splits for the maximum
+            if (pv) M = fmaxf(M, __ldcg(p.p1_ml + ((sbase + ck) * p.g + hh) * 2));
+            if (sv) M = fmaxf(M, __ldcg(p.p2_ml + ((sbase + ck) * p.g + hh) * 2));
+            continue;
+          }
+          // all lanes walk the same splits, four independent loads at a time
+          unsigned bits[2] = {pm, sm};
+#pragma unroll
+          for (int kind = 0; kind < 2; ++kind) {
+            const float* P = kind ? p.p2 : p.p1;
+            const float* PML = kind ? p.p2_ml : p.p1_ml;
+            unsigned mk = bits[kind];
+            while (mk) {
+              int idx[4];
+              int n = 0;
+#pragma unroll
+              for (int u = 0; u < 4; ++u) {
+                idx[u] = -1;
+                if (mk) {
+                  idx[u] = __ffs(mk) - 1;
+                  mk &= mk - 1;
+                  ++n;
+                }
+              }
+              float2 ml[4];
+              float x[4][CPL];
+#pragma unroll
+              for (int u = 0; u < 4; ++u) {
+                if (idx[u] < 0) continue;
+                const size_t it = (sbase + c0 + idx[u]) * p.g + hh;
+                ml[u] = __ldcg(reinterpret_cast<const float2*>(PML + it * 2));
+                const float* src = P + it * D + lane * CPL;
+                if (CPL == 4) {
+                  const float4 t = __ldcg(reinterpret_cast<const float4*>(src));
+                  x[u][0] = t.x; x[u][1 % CPL] = t.y; x[u][2 % CPL] = t.z; x[u][3 % CPL] = t.w;
+                } else {
+                  const float2 t = __ldcg(reinterpret_cast<const float2*>(src));
+                  x[u][0] = t.x; x[u][1 % CPL] = t.y;
+                }
+              }
+#pragma unroll
+              for (int u = 0; u < 4; ++u) {
+                if (idx[u] < 0) continue;
+                const float wgt = ml[u].y > 0.f ? fast_exp2(ml[u].x - M) : 0.f;
+                Ls += wgt * ml[u].y;
+#pragma unroll
+                for (int j = 0; j < CPL; ++j) v[j] += wgt * x[u][j];
+              }
+              (void)n;
+            }
+          }
+        }
+        if (pass == 0) {
+#pragma unroll
+          for (int o = 16; o; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+        }
+      }
+      float* o = p.out + ((size_t)a * p.hq + h * p.g + hh) * D + lane * CPL;
+#pragma unroll
+      for (int j = 0; j < CPL; ++j) o[j] = Ls > 0.f ? v[j] / Ls : 0.f;
+    }
+  };
+
+  // write the current item's split(s), count arrivals, merge what completed
   auto flush = [&]() {
-    float lt0 = l[0], lt1 = l[1];
+    float lt[2] = {l[0], l[1]};
 #pragma unroll
     for (int o = 4; o < 32; o <<= 1) {
-      lt0 += __shfl_xor_sync(0xffffffffu, lt0, o);
-      lt1 += __shfl_xor_sync(0xffffffffu, lt1, o);
+      lt[0] += __shfl_xor_sync(0xffffffffu, lt[0], o);
+      lt[1] += __shfl_xor_sync(0xffffffffu, lt[1], o);
     }
-    float* pr = p.part + (size_t)cur * p.g * D;
+    float* dst = ckind ? p.p2 : p.p1;
+    float* dml = ckind ? p.p2_ml : p.p1_ml;
 #pragma unroll
     for (int cc = 0; cc < 2; ++cc) {
-      const int r = 2 * c + cc;
-      if (r < p.g) {
+      const int j = 2 * c + cc;
+      const int slot = colslot[cc];
+      if (slot != 31) {
+        const int a = ckind ? cidx * R + slot : cidx;
+        const int hh = j - slot * p.g;
+        const size_t it = (((size_t)a * p.hkv + ch_) * p.n_chunks + cchunk) * p.g + hh;
+        float* pr = dst + it * D;
 #pragma unroll
         for (int mt = 0; mt < D / 16; ++mt) {
-          __stcg(pr + r * D + mt * 16 + g, acc[mt][cc]);
-          __stcg(pr + r * D + mt * 16 + g + 8, acc[mt][2 + cc]);
+          __stcg(pr + mt * 16 + g, acc[mt][cc]);
+          __stcg(pr + mt * 16 + g + 8, acc[mt][2 + cc]);
         }
-        if (g == 0) __stcg(reinterpret_cast<float2*>(p.part_ml + ((size_t)cur * p.g + r) * 2), make_float2(m[cc], cc ? lt1 : lt0));
+        if (g == 0) __stcg(reinterpret_cast<float2*>(dml + it * 2), make_float2(m[cc], lt[cc]));
       }
     }
     __syncwarp();
-    const int nb = seq_blocks(ca);
-    const int nch = (nb + p.ib - 1) / p.ib;
     int last = 0;
     if (lane == 0) {
-      __threadfence();   // the warp's split stores (ordered by __syncwarp) before the arrival
-      const int t = atomicAdd(p.tickets + ca * p.hkv + ch_, 1);
-      last = (t == nch - 1);
-      if (last) p.tickets[ca * p.hkv + ch_] = 0;
+      __threadfence();   // the warp's split stores (ordered by __syncwarp) before the arrivals
+      for (int slot = 0; slot < R; ++slot) {
+        if (!((cact >> slot) & 1)) continue;
+        const int a = ckind ? cidx * R + slot : cidx;
+        const int t = atomicAdd(p.tickets + a * p.hkv + ch_, 1);
+        if (t == p.tix[a] - 1) {
+          p.tickets[a * p.hkv + ch_] = 0;
+          last |= 1 << slot;
+        }
+      }
     }
     last = __shfl_sync(0xffffffffu, last, 0);
     if (!last) return;
     __threadfence();   // acquire side: other warps' splits are visible
-    // merge the nch splits of (ca, ch_): chunk k's split is item ((k*hkv + ch_)*n_seq + ca).
-    // Lanes first take one split each for the max and the normaliser; then
-    // every lane owns D/32 consecutive columns and walks the splits with
-    // several independent loads in flight.
-    constexpr int CPL = D / 32;                 // columns per lane
-    const size_t kstride = (size_t)p.hkv * p.n_seq;
-    const size_t it0 = (size_t)ch_ * p.n_seq + ca;
-    for (int r = 0; r < p.g; ++r) {
-      float M = -INFINITY;
-      for (int k = lane; k < nch; k += 32) M = fmaxf(M, __ldcg(p.part_ml + ((it0 + k * kstride) * p.g + r) * 2));
-#pragma unroll
-      for (int o = 16; o; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-      float Ls = 0.f;
-      float v[CPL];
-#pragma unroll
-      for (int j = 0; j < CPL; ++j) v[j] = 0.f;
-      // no shuffles in this loop: every lane reads the (m, l) of split k
-      // itself (one broadcast transaction), so the loads of several splits
-      // can be in flight at once
-#pragma unroll 8
-      for (int k = 0; k < nch; ++k) {
-        const size_t it = (it0 + k * kstride) * p.g + r;
-        const float2 ml = __ldcg(reinterpret_cast<const float2*>(p.part_ml + it * 2));
-        const float* src = p.part + it * D + lane * CPL;
-        float x[CPL];
-        if (CPL == 4) {
-          const float4 t = __ldcg(reinterpret_cast<const float4*>(src));
-          x[0] = t.x; x[1 % CPL] = t.y; x[2 % CPL] = t.z; x[3 % CPL] = t.w;
-        } else {
-          const float2 t = __ldcg(reinterpret_cast<const float2*>(src));
-          x[0] = t.x; x[1 % CPL] = t.y;
-        }
-        const float wgt = ml.y > 0.f ? fast_exp2(ml.x - M) : 0.f;
-        Ls += wgt * ml.y;
-#pragma unroll
-        for (int j = 0; j < CPL; ++j) v[j] += wgt * x[j];
-      }
-      float* o = p.out + ((size_t)ca * p.hq + ch_ * p.g + r) * D + lane * CPL;
-#pragma unroll
-      for (int j = 0; j < CPL; ++j) o[j] = Ls > 0.f ? v[j] / Ls : 0.f;
-    }
+    for (int slot = 0; slot < R; ++slot)
+      if ((last >> slot) & 1) merge(ckind ? cidx * R + slot : cidx, ch_);
   };
 
   for (int i = 0;;) {
@@ -328,6 +642,7 @@ attn_tm_kernel(const __grid_constant__ TmParams p, const __grid_constant__ CUten
     if (!mbar_wait_bounded(&bars[warp][s], (i / S) & 1, p.status)) break;
     const int item = st_item[warp][s];
     const int bword = st_block[warp][s];
+    const int emask = st_mask[warp][s];
     if (item < 0) break;
     const bool has_diff = DIFF && (bword >> 30) != 0;
     const int b = bword & ((1 << 29) - 1);
@@ -337,22 +652,42 @@ attn_tm_kernel(const __grid_constant__ TmParams p, const __grid_constant__ CUten
     if (item != cur) {
       if (cur >= 0) flush();
       cur = item;
-      ca = item % p.n_seq;
-      ch_ = (item / p.n_seq) % p.hkv;
-      int L = p.seq_len[ca];
-      cL = L < 0 ? 0 : min(L, p.max_blocks * B);
+      const int2 it = p.items[item / p.hkv];
+      ch_ = item - (item / p.hkv) * p.hkv;
+      cchunk = it.y;
+      ckind = it.x >> 30;
+      cidx = it.x & ((1 << 30) - 1);
+      int agent_of_col = -1;   // sequence of this lane's query column (n = g)
+      if (ckind) {
+        cact = p.spm[cidx * p.n_chunks + cchunk];
+        const int slot = g / p.g;
+        if (g < R * p.g && ((cact >> slot) & 1)) agent_of_col = cidx * R + slot;
+      } else {
+        const int slot = cidx % R;
+        cact = 1 << slot;
+        if (g / p.g == slot && g < R * p.g) agent_of_col = cidx;
+      }
+      qok = agent_of_col >= 0;
+      qrow = p.q + ((size_t)(qok ? agent_of_col : 0) * p.hq + ch_ * p.g + (g % p.g)) * D;
+#pragma unroll
+      for (int cc = 0; cc < 2; ++cc) {
+        const int j = 2 * c + cc;
+        const int slot = j / p.g;
+        int a = -1;
+        if (j < R * p.g && ((cact >> slot) & 1)) a = ckind ? cidx * R + slot : cidx;
+        colslot[cc] = a >= 0 ? slot : 31;
+        colL[cc] = a >= 0 ? min(max(p.seq_len[a], 0), p.max_blocks * B) : 0;
+      }
       m[0] = m[1] = -INFINITY;
       l[0] = l[1] = 0.f;
 #pragma unroll
       for (int mt = 0; mt < D / 16; ++mt) acc[mt][0] = acc[mt][1] = acc[mt][2] = acc[mt][3] = 0.f;
-      qok = g < p.g;
-      qrow = p.q + ((size_t)ca * p.hq + ch_ * p.g + g) * D;
       load_q();
       cur_delta = 0;
       seg_lo = seg_hi = 0;
       if (ROPE) {
-        seg_beg = p.rope_off[ca];
-        seg_end = p.rope_off[ca + 1];
+        seg_beg = p.rope_off[cidx];
+        seg_end = p.rope_off[cidx + 1];
       }
     }
     if (loaded) {
@@ -395,8 +730,7 @@ attn_tm_kernel(const __grid_constant__ TmParams p, const __grid_constant__ CUten
       }
       const uint32_t tkb = wbase_u32 + s * STAGE, tvb = tkb + TILE;
       const uint32_t dkb = wbase_u32 + s2 * STAGE, dvb = dkb + TILE;   // diff tiles (if any)
-      // S^T = K q^T : 16 tokens x 8 query heads
-      // two independent accumulation chains (even / odd k-steps)
+      // S^T = K q^T : 16 tokens x 8 query columns, two accumulation chains
       float sc[4] = {0.f, 0.f, 0.f, 0.f}, sd[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int kk = 0; kk < KS; ++kk) {
@@ -413,12 +747,14 @@ attn_tm_kernel(const __grid_constant__ TmParams p, const __grid_constant__ CUten
       }
 #pragma unroll
       for (int e = 0; e < 4; ++e) sc[e] += sd[e];
-      const int nv = min(B, cL - b * B);
-      // sc: (t=g, r=2c), (g, 2c+1), (g+8, 2c), (g+8, 2c+1)
+      // sc: (t=g, col 2c), (g, 2c+1), (g+8, 2c), (g+8, 2c+1); a column is live
+      // if its member takes this block and the token is inside its context
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         const int t = g + ((e >> 1) << 3);
-        sc[e] = t < nv ? sc[e] * p.scale_log2 : -INFINITY;
+        const int cc = e & 1;
+        const bool live = colslot[cc] != 31 && ((emask >> colslot[cc]) & 1) && b * B + t < colL[cc];
+        sc[e] = live ? sc[e] * p.scale_log2 : -INFINITY;
       }
       float mx0 = fmaxf(sc[0], sc[2]), mx1 = fmaxf(sc[1], sc[3]);
 #pragma unroll
@@ -427,13 +763,15 @@ attn_tm_kernel(const __grid_constant__ TmParams p, const __grid_constant__ CUten
         mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
       }
       const float mn0 = fmaxf(m[0], mx0), mn1 = fmaxf(m[1], mx1);
-      const float al0 = fast_exp2(m[0] - mn0), al1 = fast_exp2(m[1] - mn1);
+      // a column with nothing live yet keeps (m, l, acc) = (-inf, 0, 0)
+      const float al0 = mn0 == -INFINITY ? 1.f : fast_exp2(m[0] - mn0);
+      const float al1 = mn1 == -INFINITY ? 1.f : fast_exp2(m[1] - mn1);
       m[0] = mn0;
       m[1] = mn1;
-      sc[0] = fast_exp2(sc[0] - mn0);
-      sc[1] = fast_exp2(sc[1] - mn1);
-      sc[2] = fast_exp2(sc[2] - mn0);
-      sc[3] = fast_exp2(sc[3] - mn1);
+      sc[0] = mn0 == -INFINITY ? 0.f : fast_exp2(sc[0] - mn0);
+      sc[1] = mn1 == -INFINITY ? 0.f : fast_exp2(sc[1] - mn1);
+      sc[2] = mn0 == -INFINITY ? 0.f : fast_exp2(sc[2] - mn0);
+      sc[3] = mn1 == -INFINITY ? 0.f : fast_exp2(sc[3] - mn1);
       l[0] = l[0] * al0 + sc[0] + sc[2];
       l[1] = l[1] * al1 + sc[1] + sc[3];
 #pragma unroll
@@ -441,7 +779,7 @@ attn_tm_kernel(const __grid_constant__ TmParams p, const __grid_constant__ CUten
         acc[mt][0] *= al0; acc[mt][1] *= al1;
         acc[mt][2] *= al0; acc[mt][3] *= al1;
       }
-      // P^T as the B operand (k = token, n = query head), bf16 hi + lo
+      // P^T as the B operand (k = token, n = query column), bf16 hi + lo
       uint32_t h0, l0_, h1, l1_;
       split_bf16(sc[0], sc[1], h0, l0_);
       split_bf16(sc[2], sc[3], h1, l1_);
@@ -478,9 +816,9 @@ attn_tm_kernel(const __grid_constant__ TmParams p, const __grid_constant__ CUten
 }
 
 template <int D, bool DIFF, bool ROPE>
-static kvs_status launch_tm(TmParams& prm, const kvs_pool* pool, int layer, cudaStream_t st) {
+static kvs_status launch_tm(TmParams& prm, const kvs_pool* pool, int layer, int max_claims, cudaStream_t st) {
   auto kern = attn_tm_kernel<D, DIFF, ROPE>;
-  constexpr int smem = tm_smem_bytes<D, DIFF>();
+  constexpr int smem = tm_smem_bytes<D>();
   static int blocks_per_sm = 0;
   if (!blocks_per_sm) {
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess ||
@@ -488,9 +826,9 @@ static kvs_status launch_tm(TmParams& prm, const kvs_pool* pool, int layer, cuda
         blocks_per_sm < 1)
       return fail(KVS_ERR_CUDA, "decode_attn: cannot configure the token-major kernel");
   }
-  // persistent grid: every SM filled once, but never more warps than items
-  // (idle warps would only contend on the work counter)
-  const int grid = std::max(1, std::min(pool->num_sms * blocks_per_sm, (prm.n_items + kTmWarps - 1) / kTmWarps));
+  // persistent grid: every SM filled once, but never more warps than the
+  // largest possible number of claims (idle warps would only contend)
+  const int grid = std::max(1, std::min(pool->num_sms * blocks_per_sm, (max_claims + kTmWarps - 1) / kTmWarps));
   prm.total_warps = grid * kTmWarps;
   const CUtensorMap& dk = DIFF ? pool->tdk[layer] : pool->tk[layer];
   const CUtensorMap& dv = DIFF ? pool->tdv[layer] : pool->tv[layer];
@@ -499,19 +837,36 @@ static kvs_status launch_tm(TmParams& prm, const kvs_pool* pool, int layer, cuda
   return check_launch("decode_attn");
 }
 
-// Work-item size (blocks): about eight items per resident warp so the dynamic
-// schedule balances ragged contexts, but at least max_blocks/64 so one
-// (sequence, kv head) never has more than ~64 splits to merge, and at most
-// 32 (one block-table entry per lane).
-int tm_item_blocks(const kvs_pool* pool, int n_seq, int max_blocks) {
-  const long long work = (long long)n_seq * pool->desc.num_kv_heads * max_blocks;
-  const long long warps = (long long)pool->num_sms * KVS_TM_MIN_CTAS * kTmWarps;
-  long long ib = work / (warps * 8);
-  const long long min_ib = (max_blocks + 63) / 64;
-  if (ib < min_ib) ib = min_ib;
-  int r = 4;
-  while (r < ib && r < 32) r <<= 1;
-  return r;
+kvs_status decode_plan_token_major(kvs_pool* pool, int n_q_heads, const int32_t* table, int max_blocks,
+                                   const int32_t* seq_len, int n_seq, const int32_t* diff, bool rope, void* ws,
+                                   cudaStream_t stream) {
+  const int g = n_q_heads / pool->desc.num_kv_heads;
+  const TmLayout L = tm_layout(pool, n_seq, max_blocks, g, rope);
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  PlanParams pp{};
+  pp.block_table = table;
+  pp.seq_len = seq_len;
+  pp.diff_table = diff;
+  pp.hdr = reinterpret_cast<int*>(w + L.off_hdr);
+  pp.items = reinterpret_cast<int2*>(w + L.off_items);
+  pp.shb = reinterpret_cast<uint32_t*>(w + L.off_shb);
+  pp.pne = w + L.off_pne;
+  pp.spm = w + L.off_spm;
+  pp.tix = reinterpret_cast<int*>(w + L.off_tix);
+  pp.n_seq = n_seq;
+  pp.max_blocks = max_blocks;
+  pp.R = L.R;
+  pp.G = g;
+  pp.ib = L.ib;
+  pp.n_chunks = L.n_chunks;
+  pp.n_groups = L.n_groups;
+  pp.words = L.words;
+  pp.capacity = pool->desc.capacity_blocks;
+  pp.diff_capacity = pool->desc.diff_capacity_blocks;
+  pp.hkv = pool->desc.num_kv_heads;
+  tm_plan_kernel<<<1, 1024, 0, stream>>>(pp);
+  count_launch();
+  return check_launch("decode_plan");
 }
 
 kvs_status decode_attn_token_major(kvs_pool* pool, int layer, const void* q, int n_q_heads, const int32_t* table,
@@ -520,6 +875,10 @@ kvs_status decode_attn_token_major(kvs_pool* pool, int layer, const void* q, int
                                    float scale, float* out, void* ws, cudaStream_t stream) {
   const kvs_pool_desc& d = pool->desc;
   const int g = n_q_heads / d.num_kv_heads;
+  const bool rope = rope_off != nullptr, dif = diff != nullptr;
+  const TmLayout L = tm_layout(pool, n_seq, max_blocks, g, rope);
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  const size_t splits = (size_t)n_seq * d.num_kv_heads * L.n_chunks;
   TmParams prm{};
   prm.q = static_cast<const uint16_t*>(q);
   prm.block_table = table;
@@ -528,11 +887,16 @@ kvs_status decode_attn_token_major(kvs_pool* pool, int layer, const void* q, int
   prm.rope_off = rope_off;
   prm.rope_segs = reinterpret_cast<const int4*>(rope_segs);
   prm.out = out;
-  prm.ib = tm_item_blocks(pool, n_seq, max_blocks);
-  prm.n_chunks = (max_blocks + prm.ib - 1) / prm.ib;
-  prm.n_items = n_seq * d.num_kv_heads * prm.n_chunks;
-  prm.part = static_cast<float*>(ws);
-  prm.part_ml = prm.part + (size_t)prm.n_items * g * d.head_dim;
+  prm.p1 = reinterpret_cast<float*>(w + L.off_p1);
+  prm.p1_ml = prm.p1 + splits * g * d.head_dim;
+  prm.p2 = reinterpret_cast<float*>(w + L.off_p2);
+  prm.p2_ml = prm.p2 + (L.R > 1 ? splits * g * d.head_dim : 0);
+  prm.hdr = reinterpret_cast<const int*>(w + L.off_hdr);
+  prm.items = reinterpret_cast<const int2*>(w + L.off_items);
+  prm.shb = reinterpret_cast<const uint32_t*>(w + L.off_shb);
+  prm.pne = w + L.off_pne;
+  prm.spm = w + L.off_spm;
+  prm.tix = reinterpret_cast<const int*>(w + L.off_tix);
   prm.tickets = pool->tickets;
   prm.sched = pool->sched;
   prm.status = pool->status;
@@ -541,23 +905,25 @@ kvs_status decode_attn_token_major(kvs_pool* pool, int layer, const void* q, int
   prm.hkv = d.num_kv_heads;
   prm.g = g;
   prm.hq = n_q_heads;
+  prm.ib = L.ib;
+  prm.n_chunks = L.n_chunks;
+  prm.R = L.R;
+  prm.words = L.words;
   prm.capacity = d.capacity_blocks;
   prm.diff_capacity = d.diff_capacity_blocks;
   prm.scale_log2 = scale * 1.4426950408889634f;
-  const bool rope = rope_off != nullptr, dif = diff != nullptr;
   if (rope) rope_split_host(theta, d.head_dim, prm.rs.c);
+  const int max_claims = (int)std::min<size_t>(L.max_entries * d.num_kv_heads, 0x7fffffff);
   if (d.head_dim == 128) {
-    if (dif) return rope ? launch_tm<128, true, true>(prm, pool, layer, stream) : launch_tm<128, true, false>(prm, pool, layer, stream);
-    return rope ? launch_tm<128, false, true>(prm, pool, layer, stream) : launch_tm<128, false, false>(prm, pool, layer, stream);
+    if (dif) return rope ? launch_tm<128, true, true>(prm, pool, layer, max_claims, stream)
+                         : launch_tm<128, true, false>(prm, pool, layer, max_claims, stream);
+    return rope ? launch_tm<128, false, true>(prm, pool, layer, max_claims, stream)
+                : launch_tm<128, false, false>(prm, pool, layer, max_claims, stream);
   }
-  if (dif) return rope ? launch_tm<64, true, true>(prm, pool, layer, stream) : launch_tm<64, true, false>(prm, pool, layer, stream);
-  return rope ? launch_tm<64, false, true>(prm, pool, layer, stream) : launch_tm<64, false, false>(prm, pool, layer, stream);
-}
-
-size_t tm_workspace_bytes(const kvs_pool* pool, int n_seq, int max_blocks, int g) {
-  const int ib = tm_item_blocks(pool, n_seq, max_blocks);
-  const size_t items = (size_t)n_seq * pool->desc.num_kv_heads * ((max_blocks + ib - 1) / ib);
-  return items * g * (pool->desc.head_dim + 2) * sizeof(float) + 256;
+  if (dif) return rope ? launch_tm<64, true, true>(prm, pool, layer, max_claims, stream)
+                       : launch_tm<64, true, false>(prm, pool, layer, max_claims, stream);
+  return rope ? launch_tm<64, false, true>(prm, pool, layer, max_claims, stream)
+              : launch_tm<64, false, false>(prm, pool, layer, max_claims, stream);
 }
 
 }  // namespace kvs

@@ -31,6 +31,7 @@ KVS_DEVERR_DIFF_ID = 0x8
 KVS_DEVERR_WAIT_TIMEOUT = 0x10
 KVS_DEVERR_ROPE_RANGE = 0x20
 KVS_DEVERR_JOB = 0x40
+KVS_DEVERR_PLAN = 0x80
 
 KVS_DTYPE_BF16 = 0
 KVS_DTYPE_Q4G64 = 1
@@ -39,7 +40,8 @@ KVS_OP_DEDUP, KVS_OP_DECODE_ATTN, KVS_OP_DECODE_ATTN_Q4, KVS_OP_SELECT = 0, 1, 2
 
 EXPORTED = [
     "kvs_pool_create", "kvs_pool_destroy", "kvs_fingerprint_dedup", "kvs_rope_rerotate",
-    "kvs_select_critical", "kvs_select_critical_noalloc", "kvs_decode_attn", "kvs_decode_attn_q4", "kvs_quantize_q4",
+    "kvs_select_critical", "kvs_select_critical_noalloc", "kvs_decode_plan", "kvs_decode_attn_planned",
+    "kvs_decode_attn", "kvs_decode_attn_q4", "kvs_quantize_q4",
     "kvs_workspace_size", "kvs_pool_check", "kvs_pool_stats", "kvs_last_error_string",
     "kvs_launch_count",
 ]
@@ -83,6 +85,8 @@ def load(path: str = LIB_PATH):
         "kvs_select_critical": [P, P, P, I32, I32, I32, F32, P, P, P, SZ, P],
         "kvs_select_critical_noalloc": [P, P, P, I32, I32, I32, F32, P, P, P],
         "kvs_decode_attn": [P, I32, P, I32, P, I32, P, I32, P, P, P, F32, F32, P, P, SZ, P],
+        "kvs_decode_attn_planned": [P, I32, P, I32, P, I32, P, I32, P, P, P, F32, F32, P, P, SZ, P],
+        "kvs_decode_plan": [P, I32, P, I32, P, I32, P, P, P, SZ, P],
         "kvs_decode_attn_q4": [P, I32, P, I32, P, I32, P, I32, F32, P, P, SZ, P],
         "kvs_quantize_q4": [P, I32, P, P, P, I32, P],
         "kvs_workspace_size": [P, I32, I32, I32, I32, ctypes.POINTER(SZ)],
@@ -204,6 +208,21 @@ def kvs_decode_attn(pool: Pool, layer, q, n_q_heads, block_table, max_blocks, se
                                   _ptr(seq_len), n_seq, _ptr(diff_table), _ptr(rope_off), _ptr(rope_segs),
                                   theta, scale, _ptr(out), _ptr(ws), ws.numel() * ws.element_size(),
                                   _stream(stream)))
+
+
+def kvs_decode_plan(pool: Pool, n_q_heads, block_table, max_blocks, seq_len, n_seq, diff_table, rope_off, ws,
+                    stream=None):
+    _check(load().kvs_decode_plan(pool.handle, n_q_heads, _ptr(block_table), max_blocks, _ptr(seq_len), n_seq,
+                                  _ptr(diff_table), _ptr(rope_off), _ptr(ws), ws.numel() * ws.element_size(),
+                                  _stream(stream)))
+
+
+def kvs_decode_attn_planned(pool: Pool, layer, q, n_q_heads, block_table, max_blocks, seq_len, n_seq,
+                            diff_table, rope_off, rope_segs, theta, scale, out, ws, stream=None):
+    _check(load().kvs_decode_attn_planned(pool.handle, layer, _ptr(q), n_q_heads, _ptr(block_table), max_blocks,
+                                          _ptr(seq_len), n_seq, _ptr(diff_table), _ptr(rope_off), _ptr(rope_segs),
+                                          theta, scale, _ptr(out), _ptr(ws), ws.numel() * ws.element_size(),
+                                          _stream(stream)))
 
 
 def kvs_decode_attn_q4(pool: Pool, layer, q, n_q_heads, block_table, max_blocks, seq_len, n_seq,

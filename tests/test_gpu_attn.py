@@ -107,7 +107,47 @@ def test_shared_layout_equals_private_layout_on_gpu():
     w2 = W.Workload(**{**w.__dict__, "capacity_blocks": len(rows_k)})
     pool2 = H.bf16_pool(w2, layers_np=[(np.stack(rows_k), np.stack(rows_v))])
     o2 = H.attn(pool2, 0, q_bits, w2, priv)
-    np.testing.assert_array_equal(o1, o2)
+    # the deduplicated layout lets a group of sequences share one pass over a
+    # common block, so only the fp32 summation order differs
+    np.testing.assert_allclose(o1, o2, rtol=1e-5, atol=1e-6)
+    exp = oracle_out(w, pool, ref["block_table"], q_bits)
+    H.assert_close_attn(o1, exp)
+
+
+def test_plan_reused_across_layers_and_mismatch_flagged():
+    # one plan per step serves every layer; a call whose shapes do not match
+    # the plan is reported on the device and writes nothing
+    w = W.make_mha7b(n_seq=5, total_blocks=40, shared_blocks=25, n_layers=2, heads=4)
+    ref = OF.dedup(w.tokens, w.seq_off, w.tier, w.block_tokens, w.max_blocks)
+    pool = H.bf16_pool(w, n_layers=2)
+    tb, sl = H.i32(ref["block_table"]), H.i32(w.seq_len)
+    ws = H.workspace(K.kvs_workspace_size(pool, K.KVS_OP_DECODE_ATTN, w.n_seq, w.max_blocks, w.n_q_heads))
+    K.kvs_decode_plan(pool, w.n_q_heads, tb, w.max_blocks, sl, w.n_seq, None, None, ws)
+    for layer in range(2):
+        q_bits = w.q_layer(layer)
+        out = torch.full((w.n_seq, w.n_q_heads, w.head_dim), float("nan"), device=H.DEV)
+        K.kvs_decode_attn_planned(pool, layer, H.bits_to_dev(q_bits), w.n_q_heads, tb, w.max_blocks, sl, w.n_seq,
+                                  None, None, None, w.theta, w.scale, out, ws)
+        torch.cuda.synchronize()
+        exp = oracle_out(w, pool, ref["block_table"], q_bits, layer=layer)
+        H.assert_close_attn(out.cpu().numpy().astype(np.float64), exp)
+    assert K.kvs_pool_check(pool) == 0
+    out = torch.full((w.n_seq - 1, w.n_q_heads, w.head_dim), 7.0, device=H.DEV)
+    K.kvs_decode_attn_planned(pool, 0, H.bits_to_dev(w.q_layer(0)[:-1]), w.n_q_heads, tb, w.max_blocks, sl,
+                              w.n_seq - 1, None, None, None, w.theta, w.scale, out, ws)
+    assert K.kvs_pool_check(pool) & K.KVS_DEVERR_PLAN
+    assert torch.all(out == 7.0)
+
+
+def test_group_sharing_partial_groups_and_ragged_prefix_ends():
+    # MHA (groups of 8): 11 sequences -> a full and a partial group; contexts
+    # of different lengths end inside and after the shared prefix
+    w = W.make_prefix_shared("mha_groups", 11, 2, 2, 128, 1, 30 * 16,
+                             [0, 5, 16 * 3, 16 * 9 + 1, 7, 16 * 20, 16 * 2 + 15, 40, 16, 3, 16 * 6], seed=21)
+    sl = w.seq_len.copy()
+    sl[0] = 16 * 12          # ends inside the shared prefix
+    sl[3] = 16 * 30          # exactly at its end
+    run_case(w, seq_len=sl)
 
 
 def test_bad_block_id_is_flagged_not_faulted():
