@@ -46,14 +46,14 @@ WORKLOAD = ("mha7b: 8 agents x 16384-token context, 60% shared prefix (614 share
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=40)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-rope", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--layers", type=int, default=32)
-    ap.add_argument("--workload", default="mha7b", choices=["mha7b", "tiny", "gqa_fanout", "allgather", "q4"],
+    ap.add_argument("--workload", default="mha7b", choices=["mha7b", "tiny", "gqa_fanout", "allgather", "q4", "select"],
                     help="mha7b is the headline workload; the others print a per-workload record for profiling")
     return ap.parse_args()
 
@@ -113,7 +113,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits",
-                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+                 "-lms", "50"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except (OSError, FileNotFoundError):
             self.proc = None
         return self
@@ -378,12 +378,48 @@ def main():
     return 0
 
 
+def bench_select(args, torch, K, dev, stream):
+    """Critical-position selection of the all-gather round at one check layer:
+    64 agents x 8192 shared positions x 8 KV heads x 128 dims, top 15 %."""
+    n, rows, E = 64, 8192, 1024
+    gen = torch.Generator(device=dev).manual_seed(11)
+    kc = torch.randn((n * rows, E), generator=gen, device=dev)
+    sig = 0.05 + 0.45 * torch.rand((n * rows, 1), generator=gen, device=dev)
+    kn = (kc + torch.randn((n * rows, E), generator=gen, device=dev) * sig).to(torch.bfloat16).view(torch.int16)
+    kc = kc.to(torch.bfloat16).view(torch.int16)
+    off = torch.arange(n + 1, dtype=torch.int64, device=dev) * rows
+    ws = torch.zeros(4 * n * rows, dtype=torch.uint8, device=dev)
+    idx = torch.zeros(n * rows, dtype=torch.int32, device=dev)
+    idx_off = torch.zeros(n + 1, dtype=torch.int64, device=dev)
+
+    def run():
+        K.kvs_select_critical(kc, kn, off, n, rows, E, 0.15, idx, idx_off, ws)
+
+    for _ in range(args.warmup):
+        run()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        run()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / args.steps
+    byts = 2 * n * rows * E * 2
+    peak, _ = read_peaks()
+    print(json.dumps({"workload": "select", "ms_per_call": ms, "rows_per_s": n * rows / (ms * 1e-3),
+                      "gbs": byts / (ms * 1e-3) / 1e9, "frac_of_measured_peak": byts / (ms * 1e-3) / 1e9 / peak}))
+    return 0
+
+
 def bench_workload(args, torch, K, W):
     """One-GPU record for a non-headline workload: GPU dedup + decode attention
     on every layer (Q4: attention only), timed with CUDA events."""
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
     stream = torch.cuda.current_stream()
+    if args.workload == "select":
+        return bench_select(args, torch, K, dev, stream)
     mk = {"tiny": W.make_tiny, "gqa_fanout": W.make_gqa_fanout, "allgather": W.make_allgather, "q4": W.make_q4}
     w = mk[args.workload]()
     L = min(w.n_layers, args.layers)
