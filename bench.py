@@ -412,6 +412,83 @@ def bench_select(args, torch, K, dev, stream):
     return 0
 
 
+def graph_replay_ms(torch, fn, reps, flush):
+    """Device time of one replay of fn captured in a CUDA graph (host launch
+    cost removed).  The L2 is flushed (a buffer larger than L2 is written)
+    before every replay, outside the timed events."""
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        fn()
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        fn()
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize()
+    st = torch.cuda.current_stream()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+    for a, b in ev:
+        flush.add_(1)
+        a.record(st)
+        g.replay()
+        b.record(st)
+    torch.cuda.synchronize()
+    return sum(a.elapsed_time(b) for a, b in ev) / reps
+
+
+def bench_tiny_replicated(torch, K, W, dev, reps, flush, n_inst=4096):
+    """The tiny workload replicated: n_inst independent copies (own physical
+    blocks, own mirror diffs) decoded by one plan + one attention launch."""
+    w = W.make_tiny()
+    N, H, D, B = w.n_seq, w.n_kv_heads, w.head_dim, w.block_tokens
+    tokens = torch.from_numpy(w.tokens.view(np.int32)).to(dev)
+    seq_off = torch.from_numpy(w.seq_off).to(dev)
+    probe_k = torch.zeros(16, dtype=torch.int16, device=dev)
+    probe = K.kvs_pool_create(1, H, D, B, K.KVS_DTYPE_BF16, w.capacity_blocks, N, [probe_k], [probe_k])
+    fp = torch.zeros((N, w.max_blocks), dtype=torch.int64, device=dev)
+    table = torch.zeros((N, w.max_blocks), dtype=torch.int32, device=dev)
+    refc = torch.zeros(w.capacity_blocks, dtype=torch.int32, device=dev)
+    nphys = torch.zeros(1, dtype=torch.int32, device=dev)
+    ws_d = torch.zeros(K.kvs_workspace_size(probe, K.KVS_OP_DEDUP, N, w.max_blocks), dtype=torch.uint8, device=dev)
+    K.kvs_fingerprint_dedup(probe, tokens, seq_off, N, None, None, None, fp, table, w.max_blocks, refc, nphys, ws_d)
+    n_phys = int(nphys.item())
+    nd = w.diff_capacity_blocks
+    rep = torch.arange(n_inst, device=dev, dtype=torch.int32).view(n_inst, 1, 1)
+    t1 = table.view(1, N, w.max_blocks)
+    table_r = torch.where(t1 >= 0, t1 + rep * n_phys, t1).reshape(n_inst * N, w.max_blocks).contiguous()
+    d1 = torch.from_numpy(w.diff_table).to(dev).view(1, N, w.max_blocks)
+    diff_r = torch.where(d1 >= 0, d1 + rep * nd, d1).reshape(n_inst * N, w.max_blocks).contiguous()
+    seq_len = torch.from_numpy(w.seq_len).to(dev).repeat(n_inst)
+    NS, cap, ndr = n_inst * N, n_inst * n_phys, n_inst * nd
+    gen = torch.Generator(device=dev).manual_seed(17)
+    k = torch.randn((cap, H, B, D), generator=gen, device=dev, dtype=torch.bfloat16).view(torch.int16)
+    v = torch.randn((cap, H, B, D), generator=gen, device=dev, dtype=torch.bfloat16).view(torch.int16)
+    dk = (0.1 * torch.randn((ndr, H, B, D), generator=gen, device=dev)).to(torch.bfloat16).view(torch.int16)
+    dv = (0.1 * torch.randn((ndr, H, B, D), generator=gen, device=dev)).to(torch.bfloat16).view(torch.int16)
+    pool = K.kvs_pool_create(1, H, D, B, K.KVS_DTYPE_BF16, cap, NS, [k], [v], dk_layers=[dk], dv_layers=[dv],
+                             diff_capacity_blocks=ndr)
+    q = torch.randn((NS, w.n_q_heads, D), generator=gen, device=dev, dtype=torch.bfloat16)
+    out = torch.zeros((NS, w.n_q_heads, D), dtype=torch.float32, device=dev)
+    ws = torch.zeros(K.kvs_workspace_size(pool, K.KVS_OP_DECODE_ATTN, NS, w.max_blocks, w.n_q_heads),
+                     dtype=torch.uint8, device=dev)
+
+    def run():
+        K.kvs_decode_plan(pool, w.n_q_heads, table_r, w.max_blocks, seq_len, NS, diff_r, None, ws)
+        K.kvs_decode_attn_planned(pool, 0, q, w.n_q_heads, table_r, w.max_blocks, seq_len, NS, diff_r, None,
+                                  None, w.theta, w.scale, out, ws)
+
+    ms = graph_replay_ms(torch, run, reps, flush)
+    flags = K.kvs_pool_check(pool)
+    byts = (cap + ndr) * H * B * D * 2 * 2 + NS * w.n_q_heads * D * (2 + 4) + NS * w.max_blocks * 4 * 2
+    peak, _ = read_peaks()
+    return {"instances": n_inst, "sequences": NS, "ms_plan_plus_attn": ms, "tokens_per_s": NS / (ms * 1e-3),
+            "bytes": byts, "gbs": byts / (ms * 1e-3) / 1e9, "frac_of_measured_peak": byts / (ms * 1e-3) / 1e9 / peak,
+            "status_flags": flags}
+
+
 def bench_workload(args, torch, K, W):
     """One-GPU record for a non-headline workload: GPU dedup + decode attention
     on every layer (Q4: attention only), timed with CUDA events."""
@@ -513,11 +590,32 @@ def bench_workload(args, torch, K, W):
     ms_step = t0.elapsed_time(t1) / args.steps
     attn_ms = sum(a.elapsed_time(b) for a, b in zip(ev_a, ev_b)) / len(ev_a)
     peak, kind = read_peaks()
-    print(json.dumps({"workload": args.workload, "tokens_per_s": N / (ms_step * 1e-3), "ms_per_step": ms_step,
-                      "layers": L, "attn_avg_ms": attn_ms, "attn_bytes_per_launch": per_launch,
-                      "attn_gbs": per_launch / (attn_ms * 1e-3) / 1e9,
-                      "attn_frac_of_measured_peak": per_launch / (attn_ms * 1e-3) / 1e9 / peak,
-                      "n_phys": cap, "status_flags": flags}))
+    # the same work replayed from CUDA graphs, so host launch cost is not
+    # counted: the whole step, and the attention launches alone
+    flush = torch.zeros(64 << 20, dtype=torch.float32, device=dev)
+    g_step = graph_replay_ms(torch, step, args.steps, flush)
+
+    def attn_only():
+        for l in range(L):
+            if q4:
+                K.kvs_decode_attn_q4(pool, l, q[l], w.n_q_heads, table, w.max_blocks, seq_len, N, w.scale, out[l], ws_a)
+            else:
+                K.kvs_decode_attn_planned(pool, l, q[l], w.n_q_heads, table, w.max_blocks, seq_len, N, dt, ro, rs,
+                                          w.theta, w.scale, out[l], ws_a)
+
+    g_attn = graph_replay_ms(torch, attn_only, args.steps, flush) / L
+    rec = {"workload": args.workload, "tokens_per_s": N / (ms_step * 1e-3), "ms_per_step": ms_step,
+           "layers": L, "attn_avg_ms": attn_ms, "attn_bytes_per_launch": per_launch,
+           "attn_gbs": per_launch / (attn_ms * 1e-3) / 1e9,
+           "attn_frac_of_measured_peak": per_launch / (attn_ms * 1e-3) / 1e9 / peak,
+           "graph": {"ms_per_step": g_step, "tokens_per_s": N / (g_step * 1e-3), "attn_ms_per_layer": g_attn,
+                     "attn_gbs": per_launch / (g_attn * 1e-3) / 1e9,
+                     "attn_frac_of_measured_peak": per_launch / (g_attn * 1e-3) / 1e9 / peak,
+                     "l2": "flushed before every replay"},
+           "n_phys": cap, "status_flags": flags | K.kvs_pool_check(pool)}
+    if args.workload == "tiny":
+        rec["replicated"] = bench_tiny_replicated(torch, K, W, dev, args.steps, flush)
+    print(json.dumps(rec))
     return 0
 
 

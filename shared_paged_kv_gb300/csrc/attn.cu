@@ -408,12 +408,8 @@ template <int D, bool DIFF, bool ROPE>
 static kvs_status launch_attn(const AttnParams& prm, const kvs_pool* pool, int layer, int grid, cudaStream_t st) {
   auto kern = attn_bf16_kernel<D, DIFF, ROPE>;
   constexpr int smem = attn_smem_bytes<D, DIFF>();
-  static bool attr_set = false;
-  if (!attr_set) {
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
-      return fail(KVS_ERR_CUDA, "decode_attn: cannot raise the shared-memory limit");
-    attr_set = true;
-  }
+  if (!smem_limit_once<attn_bf16_kernel<D, DIFF, ROPE>>(smem, pool->device))
+    return fail(KVS_ERR_CUDA, "decode_attn: cannot raise the shared-memory limit");
   const CUtensorMap& dk = DIFF ? pool->tdk[layer] : pool->tk[layer];
   const CUtensorMap& dv = DIFF ? pool->tdv[layer] : pool->tv[layer];
   kern<<<grid, 128, smem, st>>>(prm, pool->tk[layer], pool->tv[layer], dk, dv);

@@ -23,8 +23,9 @@
 //  * Persistent warps claim items from an atomic counter over the plan's
 //    compact item list; lane 0 runs a ring of TMA stages ahead of the warp's
 //    compute across item boundaries.  Each item leaves one (m, l, acc) split
-//    per sequence it touched; the last warp to finish a (sequence, kv head)
-//    merges its splits (arrival counter, no spinning).
+//    per sequence it touched; tm_merge_kernel, queued behind the attention
+//    kernel as a programmatic dependent launch, merges them with one warp per
+//    (sequence, query head).
 //  * Rotation is applied to the query (R(-delta) q) whenever the RoPE segment
 //    changes; the diff overlay adds DK / DV tiles through the same MMAs.
 //    Calls with rotation use groups of one sequence.
@@ -63,7 +64,7 @@ __host__ __device__ constexpr int tm_smem_bytes() {
 struct TmLayout {
   int R, ib, n_chunks, n_groups, words;
   size_t max_entries;
-  size_t off_hdr, off_items, off_shb, off_pne, off_spm, off_tix, off_p1, off_p2, total;
+  size_t off_hdr, off_items, off_shb, off_pne, off_spm, off_p1, off_p2, total;
 };
 
 static size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
@@ -98,7 +99,6 @@ static TmLayout tm_layout(const kvs_pool* pool, int n_seq, int max_blocks, int g
   L.off_shb = o; o = align256(o + (size_t)n_seq * L.words * 4);
   L.off_pne = o; o = align256(o + (size_t)n_seq * L.n_chunks);
   L.off_spm = o; o = align256(o + (size_t)L.n_groups * L.n_chunks);
-  L.off_tix = o; o = align256(o + (size_t)n_seq * 4);
   L.off_p1 = o; o = align256(o + split_bytes);
   L.off_p2 = o; o = align256(o + (L.R > 1 ? split_bytes : 0));
   L.total = o;
@@ -120,7 +120,6 @@ struct PlanParams {
   uint32_t* shb;
   uint8_t* pne;
   uint8_t* spm;
-  int* tix;
   int n_seq, max_blocks, R, G, ib, n_chunks, n_groups, words, capacity, diff_capacity, hkv;
 };
 
@@ -193,17 +192,7 @@ __global__ void __launch_bounds__(1024) tm_plan_kernel(PlanParams pp) {
     pp.spm[i] = (uint8_t)m;
   }
   __syncthreads();
-  // 3. arrivals expected per (sequence, kv head)
-  for (int a = tid; a < pp.n_seq; a += nt) {
-    int t = 0;
-    const int gi = a / pp.R, r = a - gi * pp.R;
-    for (int c = 0; c < pp.n_chunks; ++c) {
-      t += pp.pne[a * pp.n_chunks + c];
-      t += (pp.spm[gi * pp.n_chunks + c] >> r) & 1;
-    }
-    pp.tix[a] = t;
-  }
-  // 4. compact item list: shared items (group, chunk) first, then private
+  // 3. compact item list: shared items (group, chunk) first, then private
   //    items (sequence, chunk), chunk-major
   const int n_sh = pp.n_groups * pp.n_chunks, n_pr = pp.n_seq * pp.n_chunks;
   const int total = n_sh + n_pr;
@@ -277,8 +266,6 @@ struct TmParams {
   const uint32_t* shb;
   const uint8_t* pne;
   const uint8_t* spm;
-  const int* tix;
-  int32_t* tickets;   // [n_seq * hkv]
   int32_t* sched;     // [0] work counter, [1] finished-warp counter
   uint32_t* status;
   int max_blocks, n_seq, hkv, g, hq, ib, n_chunks, R, capacity, diff_capacity, total_warps, words;
@@ -310,6 +297,9 @@ attn_tm_kernel(const __grid_constant__ TmParams p, const __grid_constant__ CUten
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, c = lane & 3;
+  // a merge kernel queued behind this one (programmatic dependent launch) may
+  // be scheduled now; it waits for this grid to complete before reading
+  asm volatile("griddepcontrol.launch_dependents;");
   uint8_t* base = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   uint8_t* wbase = base + warp * S * STAGE;
   const uint32_t wbase_u32 = smem_u32(wbase);
@@ -471,7 +461,7 @@ attn_tm_kernel(const __grid_constant__ TmParams p, const __grid_constant__ CUten
   int cur = -1, ckind = 0, cidx = 0, ch_ = 0, cchunk = 0, cact = 0;
   int colL[2] = {0, 0};
   int colslot[2] = {31, 31};
-  float m[2], l[2], acc[D / 16][4];
+  float m[2] = {-INFINITY, -INFINITY}, l[2] = {0.f, 0.f}, acc[D / 16][4];
   uint32_t qb[KS][2];
   uint32_t qlo[ROPE ? KS : 1][2];
   bool q_has_lo = false;
@@ -508,88 +498,7 @@ attn_tm_kernel(const __grid_constant__ TmParams p, const __grid_constant__ CUten
     }
   };
 
-  // merge every split of sequence a, kv head h: private splits of chunks with
-  // unshared work and shared splits of chunks a takes part in
-  constexpr int CPL = D / 32;   // columns per lane
-  auto merge = [&](int a, int h) {
-    const int gi = a / R, slot = a - gi * R;
-    const size_t sbase = ((size_t)a * p.hkv + h) * p.n_chunks;
-    for (int hh = 0; hh < p.g; ++hh) {
-      float M = -INFINITY, Ls = 0.f, v[CPL];
-#pragma unroll
-      for (int j = 0; j < CPL; ++j) v[j] = 0.f;
-      for (int pass = 0; pass < 2; ++pass) {
-        for (int c0 = 0; c0 < p.n_chunks; c0 += 32) {
-          // which splits of these 32 chunks exist: one ballot per kind
-          const int ck = c0 + lane;
-          const bool pv = ck < p.n_chunks && p.pne[a * p.n_chunks + ck];
-          const bool sv = ck < p.n_chunks && ((p.spm[gi * p.n_chunks + ck] >> slot) & 1);
-          const unsigned pm = __ballot_sync(0xffffffffu, pv), sm = __ballot_sync(0xffffffffu, sv);
-          if (pass == 0) {
-            // this lane's own splits for the maximum
-            if (pv) M = fmaxf(M, __ldcg(p.p1_ml + ((sbase + ck) * p.g + hh) * 2));
-            if (sv) M = fmaxf(M, __ldcg(p.p2_ml + ((sbase + ck) * p.g + hh) * 2));
-            continue;
-          }
-          // all lanes walk the same splits, four independent loads at a time
-          unsigned bits[2] = {pm, sm};
-#pragma unroll
-          for (int kind = 0; kind < 2; ++kind) {
-            const float* P = kind ? p.p2 : p.p1;
-            const float* PML = kind ? p.p2_ml : p.p1_ml;
-            unsigned mk = bits[kind];
-            while (mk) {
-              int idx[4];
-              int n = 0;
-#pragma unroll
-              for (int u = 0; u < 4; ++u) {
-                idx[u] = -1;
-                if (mk) {
-                  idx[u] = __ffs(mk) - 1;
-                  mk &= mk - 1;
-                  ++n;
-                }
-              }
-              float2 ml[4];
-              float x[4][CPL];
-#pragma unroll
-              for (int u = 0; u < 4; ++u) {
-                if (idx[u] < 0) continue;
-                const size_t it = (sbase + c0 + idx[u]) * p.g + hh;
-                ml[u] = __ldcg(reinterpret_cast<const float2*>(PML + it * 2));
-                const float* src = P + it * D + lane * CPL;
-                if (CPL == 4) {
-                  const float4 t = __ldcg(reinterpret_cast<const float4*>(src));
-                  x[u][0] = t.x; x[u][1 % CPL] = t.y; x[u][2 % CPL] = t.z; x[u][3 % CPL] = t.w;
-                } else {
-                  const float2 t = __ldcg(reinterpret_cast<const float2*>(src));
-                  x[u][0] = t.x; x[u][1 % CPL] = t.y;
-                }
-              }
-#pragma unroll
-              for (int u = 0; u < 4; ++u) {
-                if (idx[u] < 0) continue;
-                const float wgt = ml[u].y > 0.f ? fast_exp2(ml[u].x - M) : 0.f;
-                Ls += wgt * ml[u].y;
-#pragma unroll
-                for (int j = 0; j < CPL; ++j) v[j] += wgt * x[u][j];
-              }
-              (void)n;
-            }
-          }
-        }
-        if (pass == 0) {
-#pragma unroll
-          for (int o = 16; o; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-        }
-      }
-      float* o = p.out + ((size_t)a * p.hq + h * p.g + hh) * D + lane * CPL;
-#pragma unroll
-      for (int j = 0; j < CPL; ++j) o[j] = Ls > 0.f ? v[j] / Ls : 0.f;
-    }
-  };
-
-  // write the current item's split(s), count arrivals, merge what completed
+  // write the current item's split(s); tm_merge_kernel combines them
   auto flush = [&]() {
     float lt[2] = {l[0], l[1]};
 #pragma unroll
@@ -616,25 +525,6 @@ attn_tm_kernel(const __grid_constant__ TmParams p, const __grid_constant__ CUten
         if (g == 0) __stcg(reinterpret_cast<float2*>(dml + it * 2), make_float2(m[cc], lt[cc]));
       }
     }
-    __syncwarp();
-    int last = 0;
-    if (lane == 0) {
-      __threadfence();   // the warp's split stores (ordered by __syncwarp) before the arrivals
-      for (int slot = 0; slot < R; ++slot) {
-        if (!((cact >> slot) & 1)) continue;
-        const int a = ckind ? cidx * R + slot : cidx;
-        const int t = atomicAdd(p.tickets + a * p.hkv + ch_, 1);
-        if (t == p.tix[a] - 1) {
-          p.tickets[a * p.hkv + ch_] = 0;
-          last |= 1 << slot;
-        }
-      }
-    }
-    last = __shfl_sync(0xffffffffu, last, 0);
-    if (!last) return;
-    __threadfence();   // acquire side: other warps' splits are visible
-    for (int slot = 0; slot < R; ++slot)
-      if ((last >> slot) & 1) merge(ckind ? cidx * R + slot : cidx, ch_);
   };
 
   for (int i = 0;;) {
@@ -815,16 +705,159 @@ attn_tm_kernel(const __grid_constant__ TmParams p, const __grid_constant__ CUten
   }
 }
 
+// Split merge: one warp per (sequence, query head) row, so every row of every
+// (sequence, kv head) merges in parallel, each lane keeping up to
+// kMergeBatch independent split loads in flight.  The split order is fixed
+// (chunk order, private then shared per 32-chunk window), so the result does
+// not depend on which warp computed which split.
+constexpr int kMergeWarps = 8;
+constexpr int kMergeBatch = 12;   // independent split loads in flight per lane
+
+template <int D>
+__global__ void __launch_bounds__(kMergeWarps * 32, 2) tm_merge_kernel(const __grid_constant__ TmParams p) {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  constexpr int CPL = D / 32;   // columns per lane
+  const int lane = threadIdx.x & 31;
+  const int row = blockIdx.x * kMergeWarps + (threadIdx.x >> 5);   // sequence * hq + query head
+  if (row >= p.n_seq * p.hq) return;
+  // the attention kernel has flagged a plan built for other shapes and
+  // computed nothing; leave the output untouched as well
+  if (!(p.hdr[1] == kPlanMagic && p.hdr[2] == p.n_seq && p.hdr[3] == p.max_blocks && p.hdr[4] == p.R &&
+        p.hdr[5] == p.ib && p.hdr[6] == p.hkv))
+    return;
+  const int a = row / p.hq, qh = row - a * p.hq, h = qh / p.g, hh = qh - h * p.g;
+  const int gi = a / p.R, slot = a - gi * p.R;
+  const size_t sbase = ((size_t)a * p.hkv + h) * p.n_chunks;
+  float* o = p.out + (size_t)row * D + lane * CPL;
+  if (p.seq_len[a] <= 0) {
+#pragma unroll
+    for (int j = 0; j < CPL; ++j) o[j] = 0.f;
+    return;
+  }
+  // lane k owns chunks c0 + k of every 32-chunk window; the first two windows
+  // keep their (m, l) in registers between the passes
+  float2 cp0 = make_float2(0.f, 0.f), cs0 = cp0, cp1 = cp0, cs1 = cp0;
+  bool hp0 = false, hs0 = false, hp1 = false, hs1 = false;
+  auto own = [&](int c0, bool& pv, bool& sv, float2& mp, float2& ms) {
+    const int ck = c0 + lane;
+    pv = ck < p.n_chunks && p.pne[a * p.n_chunks + ck];
+    sv = p.R > 1 && ck < p.n_chunks && ((p.spm[gi * p.n_chunks + ck] >> slot) & 1);
+    mp = pv ? __ldcg(reinterpret_cast<const float2*>(p.p1_ml + ((sbase + ck) * p.g + hh) * 2)) : make_float2(0.f, 0.f);
+    ms = sv ? __ldcg(reinterpret_cast<const float2*>(p.p2_ml + ((sbase + ck) * p.g + hh) * 2)) : make_float2(0.f, 0.f);
+  };
+  float M = -INFINITY;
+  for (int c0 = 0, w = 0; c0 < p.n_chunks; c0 += 32, ++w) {
+    bool pv, sv;
+    float2 mp, ms;
+    own(c0, pv, sv, mp, ms);
+    if (pv && mp.y > 0.f) M = fmaxf(M, mp.x);
+    if (sv && ms.y > 0.f) M = fmaxf(M, ms.x);
+    if (w == 0) {
+      hp0 = pv; hs0 = sv; cp0 = mp; cs0 = ms;
+    } else if (w == 1) {
+      hp1 = pv; hs1 = sv; cp1 = mp; cs1 = ms;
+    }
+  }
+#pragma unroll
+  for (int off = 16; off; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+  float Ls = 0.f, v[CPL];
+#pragma unroll
+  for (int j = 0; j < CPL; ++j) v[j] = 0.f;
+  for (int c0 = 0, w = 0; c0 < p.n_chunks; c0 += 32, ++w) {
+    bool pv, sv;
+    float2 mp, ms;
+    if (w == 0) {
+      pv = hp0; sv = hs0; mp = cp0; ms = cs0;
+    } else if (w == 1) {
+      pv = hp1; sv = hs1; mp = cp1; ms = cs1;
+    } else {
+      own(c0, pv, sv, mp, ms);
+    }
+    const float wp = pv && mp.y > 0.f ? fast_exp2(mp.x - M) : 0.f;
+    const float ws = sv && ms.y > 0.f ? fast_exp2(ms.x - M) : 0.f;
+    Ls += wp * mp.y + ws * ms.y;
+#pragma unroll
+    for (int kind = 0; kind < 2; ++kind) {
+      const float* P = kind ? p.p2 : p.p1;
+      const float wk = kind ? ws : wp;
+      unsigned mk = __ballot_sync(0xffffffffu, kind ? sv : pv);
+      while (mk) {   // warp-uniform
+        int idx[kMergeBatch];
+#pragma unroll
+        for (int u = 0; u < kMergeBatch; ++u) {
+          idx[u] = -1;
+          if (mk) {
+            idx[u] = __ffs(mk) - 1;
+            mk &= mk - 1;
+          }
+        }
+        float x[kMergeBatch][CPL];
+#pragma unroll
+        for (int u = 0; u < kMergeBatch; ++u) {
+          if (idx[u] < 0) continue;
+          const float* src = P + ((sbase + c0 + idx[u]) * p.g + hh) * D + lane * CPL;
+          if (CPL == 4) {
+            const float4 t = __ldcg(reinterpret_cast<const float4*>(src));
+            x[u][0] = t.x; x[u][1 % CPL] = t.y; x[u][2 % CPL] = t.z; x[u][3 % CPL] = t.w;
+          } else {
+            const float2 t = __ldcg(reinterpret_cast<const float2*>(src));
+            x[u][0] = t.x; x[u][1 % CPL] = t.y;
+          }
+        }
+#pragma unroll
+        for (int u = 0; u < kMergeBatch; ++u) {
+          if (idx[u] < 0) continue;
+          const float wgt = __shfl_sync(0xffffffffu, wk, idx[u]);
+#pragma unroll
+          for (int j = 0; j < CPL; ++j) v[j] += wgt * x[u][j];
+        }
+      }
+    }
+  }
+#pragma unroll
+  for (int off = 16; off; off >>= 1) Ls += __shfl_xor_sync(0xffffffffu, Ls, off);
+  const float inv = Ls > 0.f ? 1.f / Ls : 0.f;
+  if (CPL == 4) {
+    *reinterpret_cast<float4*>(o) = make_float4(v[0] * inv, v[1 % CPL] * inv, v[2 % CPL] * inv, v[3 % CPL] * inv);
+  } else {
+    *reinterpret_cast<float2*>(o) = make_float2(v[0] * inv, v[1 % CPL] * inv);
+  }
+}
+
+template <int D>
+static kvs_status launch_merge(const TmParams& prm, cudaStream_t st) {
+  const int rows = prm.n_seq * prm.hq;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((rows + kMergeWarps - 1) / kMergeWarps);
+  cfg.blockDim = dim3(kMergeWarps * 32);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, tm_merge_kernel<D>, prm) != cudaSuccess)
+    return fail(KVS_ERR_CUDA, "decode_attn: merge launch failed");
+  count_launch();
+  return check_launch("decode_attn_merge");
+}
+
 template <int D, bool DIFF, bool ROPE>
 static kvs_status launch_tm(TmParams& prm, const kvs_pool* pool, int layer, int max_claims, cudaStream_t st) {
   auto kern = attn_tm_kernel<D, DIFF, ROPE>;
   constexpr int smem = tm_smem_bytes<D>();
-  static int blocks_per_sm = 0;
+  // occupancy depends only on the kernel and the device type (one type of
+  // device per process is assumed for the cached count)
+  static std::atomic<int> occ{0};
+  int blocks_per_sm = occ.load(std::memory_order_relaxed);
+  if (!smem_limit_once<attn_tm_kernel<D, DIFF, ROPE>>(smem, pool->device))
+    return fail(KVS_ERR_CUDA, "decode_attn: cannot raise the shared-memory limit");
   if (!blocks_per_sm) {
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess ||
-        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks_per_sm, kern, 128, smem) != cudaSuccess ||
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks_per_sm, kern, 128, smem) != cudaSuccess ||
         blocks_per_sm < 1)
       return fail(KVS_ERR_CUDA, "decode_attn: cannot configure the token-major kernel");
+    occ.store(blocks_per_sm, std::memory_order_relaxed);
   }
   // persistent grid: every SM filled once, but never more warps than the
   // largest possible number of claims (idle warps would only contend)
@@ -834,7 +867,9 @@ static kvs_status launch_tm(TmParams& prm, const kvs_pool* pool, int layer, int 
   const CUtensorMap& dv = DIFF ? pool->tdv[layer] : pool->tv[layer];
   kern<<<grid, 128, smem, st>>>(prm, pool->tk[layer], pool->tv[layer], dk, dv);
   count_launch();
-  return check_launch("decode_attn");
+  const kvs_status s = check_launch("decode_attn");
+  if (s != KVS_OK) return s;
+  return launch_merge<D>(prm, st);
 }
 
 kvs_status decode_plan_token_major(kvs_pool* pool, int n_q_heads, const int32_t* table, int max_blocks,
@@ -852,7 +887,6 @@ kvs_status decode_plan_token_major(kvs_pool* pool, int n_q_heads, const int32_t*
   pp.shb = reinterpret_cast<uint32_t*>(w + L.off_shb);
   pp.pne = w + L.off_pne;
   pp.spm = w + L.off_spm;
-  pp.tix = reinterpret_cast<int*>(w + L.off_tix);
   pp.n_seq = n_seq;
   pp.max_blocks = max_blocks;
   pp.R = L.R;
@@ -896,8 +930,6 @@ kvs_status decode_attn_token_major(kvs_pool* pool, int layer, const void* q, int
   prm.shb = reinterpret_cast<const uint32_t*>(w + L.off_shb);
   prm.pne = w + L.off_pne;
   prm.spm = w + L.off_spm;
-  prm.tix = reinterpret_cast<const int*>(w + L.off_tix);
-  prm.tickets = pool->tickets;
   prm.sched = pool->sched;
   prm.status = pool->status;
   prm.max_blocks = max_blocks;

@@ -1,6 +1,7 @@
 // Host-side internals of libkvs shared by the translation units.
 #pragma once
 
+#include <atomic>
 #include <cstdint>
 #include <string>
 #include <vector>
@@ -28,6 +29,19 @@ kvs_status fail(kvs_status st, const std::string& msg);
 kvs_status check_launch(const char* what);
 void count_launch(uint64_t n = 1);
 bool aligned16(const void* p);
+
+// Raises a kernel's dynamic shared-memory limit once per device (the
+// attribute belongs to the device's context).  Safe to call from several
+// threads: a repeated set is harmless.  Returns false on a CUDA error.
+template <auto Kern>
+bool smem_limit_once(int smem, int device) {
+  static std::atomic<uint64_t> done{0};   // bit d: set on device d < 64
+  const uint64_t bit = device >= 0 && device < 64 ? (uint64_t{1} << device) : 0;
+  if (bit && (done.load(std::memory_order_acquire) & bit)) return true;
+  if (cudaFuncSetAttribute(Kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess) return false;
+  done.fetch_or(bit, std::memory_order_release);
+  return true;
+}
 
 // RoPE frequency split (see common.cuh): c[piece][i] for i < head_dim/2.
 void rope_split_host(float theta, int head_dim, float out[4][64]);

@@ -487,12 +487,8 @@ extern "C" kvs_status kvs_decode_attn_q4(kvs_pool* pool, int32_t layer, const vo
   prm.n_chunks = plan.n_chunks;
   prm.capacity = d.capacity_blocks;
   prm.scale_log2 = scale * 1.4426950408889634f;
-  static bool attr_set = false;
-  if (!attr_set) {
-    if (cudaFuncSetAttribute(q4_attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kQ4Smem) != cudaSuccess)
-      return fail(KVS_ERR_CUDA, "decode_attn_q4: cannot raise the shared-memory limit");
-    attr_set = true;
-  }
+  if (!smem_limit_once<q4_attn_kernel>(kQ4Smem, pool->device))
+    return fail(KVS_ERR_CUDA, "decode_attn_q4: cannot raise the shared-memory limit");
   q4_attn_kernel<<<(int)grid, 128, kQ4Smem, stream>>>(prm, pool->tk[layer], pool->tv[layer]);
   count_launch();
   return check_launch("decode_attn_q4");

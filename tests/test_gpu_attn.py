@@ -55,6 +55,14 @@ def test_gqa_small_ragged():
     run_case(W.make_gqa_fanout(n_seq=5, prefix_tokens=256, priv_lo=30, priv_hi=300, hq=16, hkv=2, d=128))
 
 
+def test_long_context_many_splits_separate_merge():
+    # 2 sequences over a 24,000-token common prefix: about 2,500 blocks, 32-block
+    # items, 79 chunks per sequence, so the separate merge walks three
+    # 32-chunk windows of private and group-shared splits
+    w = W.make_prefix_shared("long", 2, 4, 2, 64, 1, 24000, [16000 + 7, 9000], seed=21)
+    run_case(w)
+
+
 def test_gqa_group16_d64():
     run_case(W.make_gqa_fanout(n_seq=3, prefix_tokens=100, priv_lo=1, priv_hi=200, hq=32, hkv=2, d=64))
 
