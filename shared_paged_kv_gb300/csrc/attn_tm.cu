@@ -20,12 +20,17 @@
 //    holds the same physical block (no mirror diff, full block).  "Shared
 //    items" stream such blocks once for all members; "private items" stream
 //    each sequence's remaining blocks with only its own columns live.
-//  * Persistent warps claim items from an atomic counter over the plan's
-//    compact item list; lane 0 runs a ring of TMA stages ahead of the warp's
-//    compute across item boundaries.  Each item leaves one (m, l, acc) split
-//    per sequence it touched; tm_merge_kernel, queued behind the attention
-//    kernel as a programmatic dependent launch, merges them with one warp per
-//    (sequence, query head).
+//  * Persistent warps take the plan's items in a fixed round-robin order, so
+//    a warp knows its next items in advance: the item entry two ahead and the
+//    block-table entries of the next item are in flight while the current
+//    item computes, and the next item's query rows are prefetched into L1.
+//    The whole warp runs the producer logic (lane j holds block j of the
+//    item); lane 0 issues a ring of TMA stages that runs ahead across item
+//    boundaries.  What the consumer needs about an item reaches it through a
+//    small shared-memory ring of claim records.
+//  * Each item leaves one (m, l, acc) split per sequence it touched;
+//    tm_merge_kernel, queued behind the attention kernel as a programmatic
+//    dependent launch, merges them.
 //  * Rotation is applied to the query (R(-delta) q) whenever the RoPE segment
 //    changes; the diff overlay adds DK / DV tiles through the same MMAs.
 //    Calls with rotation use groups of one sequence.
@@ -38,6 +43,7 @@ namespace kvs {
 
 constexpr int kTmWarps = 4;
 constexpr int kTmMaxIb = 32;
+constexpr int kTmRec = 8;   // claim records per warp (more than stages + 1)
 constexpr int kPlanMagic = 0x6b76730a;
 
 #ifndef KVS_TM_STAGES_D128
@@ -45,6 +51,12 @@ constexpr int kPlanMagic = 0x6b76730a;
 #endif
 #ifndef KVS_TM_MIN_CTAS
 #define KVS_TM_MIN_CTAS 3
+#endif
+#ifndef KVS_TM_ITEMS_PER_WARP
+#define KVS_TM_ITEMS_PER_WARP 8
+#endif
+#ifndef KVS_TM_MAX_SPLITS
+#define KVS_TM_MAX_SPLITS 64
 #endif
 
 // Ring stages per warp.  A stage holds one block's K and V tiles; a block
@@ -62,21 +74,21 @@ __host__ __device__ constexpr int tm_smem_bytes() {
 
 // ------------------------------------------------------------- plan layout
 struct TmLayout {
-  int R, ib, n_chunks, n_groups, words;
-  size_t max_entries;
-  size_t off_hdr, off_items, off_shb, off_pne, off_spm, off_p1, off_p2, total;
+  int R, ib, n_chunks, n_groups;
+  size_t max_items;
+  size_t off_hdr, off_items, off_gmask, off_gphys, off_pne, off_spm, off_p1, off_p2, total;
 };
 
 static size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
-// Work-item size (blocks): about eight items per resident warp, at least
-// max_blocks/64 (so one sequence never has more than ~64 splits per kind), at
-// most 32 (one block-table entry per lane).
+// Work-item size (blocks): about KVS_TM_ITEMS_PER_WARP items per resident
+// warp, at least max_blocks / KVS_TM_MAX_SPLITS (bounding the splits of one
+// sequence per kind), at most 32 (one block-table entry per lane).
 int tm_item_blocks(const kvs_pool* pool, int n_seq, int max_blocks) {
   const long long work = (long long)n_seq * pool->desc.num_kv_heads * max_blocks;
   const long long warps = (long long)pool->num_sms * KVS_TM_MIN_CTAS * kTmWarps;
-  long long ib = work / (warps * 8);
-  const long long min_ib = (max_blocks + 63) / 64;
+  long long ib = work / (warps * KVS_TM_ITEMS_PER_WARP);
+  const long long min_ib = (max_blocks + KVS_TM_MAX_SPLITS - 1) / KVS_TM_MAX_SPLITS;
   if (ib < min_ib) ib = min_ib;
   int r = 4;
   while (r < ib && r < kTmMaxIb) r <<= 1;
@@ -89,16 +101,17 @@ static TmLayout tm_layout(const kvs_pool* pool, int n_seq, int max_blocks, int g
   L.ib = tm_item_blocks(pool, n_seq, max_blocks);
   L.n_chunks = (max_blocks + L.ib - 1) / L.ib;
   L.n_groups = (n_seq + L.R - 1) / L.R;
-  L.words = (max_blocks + 31) / 32;
-  L.max_entries = (size_t)(n_seq + L.n_groups) * L.n_chunks;
+  const size_t grp = L.R > 1 ? (size_t)L.n_groups : 0;   // group arrays exist only with grouping
+  L.max_items = (grp + n_seq) * L.n_chunks;
   const size_t splits = (size_t)n_seq * pool->desc.num_kv_heads * L.n_chunks;
   const size_t split_bytes = splits * g * (pool->desc.head_dim + 2) * sizeof(float);
   size_t o = 0;
   L.off_hdr = o; o = align256(o + 64);
-  L.off_items = o; o = align256(o + L.max_entries * sizeof(int2));
-  L.off_shb = o; o = align256(o + (size_t)n_seq * L.words * 4);
+  L.off_items = o; o = align256(o + L.max_items * sizeof(int4));
+  L.off_gmask = o; o = align256(o + grp * max_blocks);
+  L.off_gphys = o; o = align256(o + grp * max_blocks * sizeof(int32_t));
   L.off_pne = o; o = align256(o + (size_t)n_seq * L.n_chunks);
-  L.off_spm = o; o = align256(o + (size_t)L.n_groups * L.n_chunks);
+  L.off_spm = o; o = align256(o + grp * L.n_chunks);
   L.off_p1 = o; o = align256(o + split_bytes);
   L.off_p2 = o; o = align256(o + (L.R > 1 ? split_bytes : 0));
   L.total = o;
@@ -106,21 +119,26 @@ static TmLayout tm_layout(const kvs_pool* pool, int n_seq, int max_blocks, int g
 }
 
 size_t tm_workspace_bytes(const kvs_pool* pool, int n_seq, int max_blocks, int g) {
-  // sized for grouping (no rotation), which is the larger layout
-  return tm_layout(pool, n_seq, max_blocks, g, false).total + 256;
+  return std::max(tm_layout(pool, n_seq, max_blocks, g, false).total,
+                  tm_layout(pool, n_seq, max_blocks, g, true).total) + 256;
 }
 
 // ------------------------------------------------------------------- plan
+// Items are int4 {x: kind (bit 30) | group or sequence, y: chunk, z: end
+// block (exclusive), w: member mask of the columns that take part}.
 struct PlanParams {
   const int32_t* block_table;
   const int32_t* seq_len;
   const int32_t* diff_table;
   int* hdr;
-  int2* items;
-  uint32_t* shb;
-  uint8_t* pne;
-  uint8_t* spm;
-  int n_seq, max_blocks, R, G, ib, n_chunks, n_groups, words, capacity, diff_capacity, hkv;
+  int4* items;
+  uint8_t* gmask;   // [n_groups][max_blocks] members computed by the group's shared item (R > 1)
+  int32_t* gphys;   // [n_groups][max_blocks] that shared physical block, or -1 (R > 1)
+  uint8_t* pne;     // [n_seq][n_chunks] private chunk has unshared work
+  uint8_t* spm;     // [n_groups][n_chunks] members taking part in the shared chunk (R > 1)
+  float* p1_ml;     // (m, l) of the private splits [n_seq][hkv][n_chunks][g]
+  float* p2_ml;     // (m, l) of the shared splits, same shape (R > 1)
+  int n_seq, max_blocks, R, G, ib, n_chunks, n_groups, capacity, hkv;
 };
 
 __device__ __forceinline__ int plan_seq_blocks(const int32_t* seq_len, int a, int max_blocks) {
@@ -130,121 +148,124 @@ __device__ __forceinline__ int plan_seq_blocks(const int32_t* seq_len, int a, in
   return (L + 15) / 16;
 }
 
-// One CTA of 1024 threads builds the whole plan (it depends on the tables
-// only, so one plan serves every layer of a decode step).
-__global__ void __launch_bounds__(1024) tm_plan_kernel(PlanParams pp) {
-  __shared__ int warp_sums[32];
-  __shared__ int s_carry;
+// Plan, part 1 (it depends on the tables only, so one plan serves every
+// layer of a decode step).  One CTA per group of R sequences:
+//  * gmask / gphys: a member's logical block is group-shared when every
+//    member that reaches it holds the same valid full physical block with no
+//    mirror diff (at least two members);
+//  * pne / spm: which private chunks have unshared work, which members take
+//    part in each shared chunk;
+//  * the (m, l) of every split that will not be written is set to (-inf, 0),
+//    so the merge can read all of them without consulting pne / spm first.
+__global__ void __launch_bounds__(256) tm_plan_groups(PlanParams pp) {
   const int tid = threadIdx.x, nt = blockDim.x;
-  for (int i = tid; i < pp.n_seq * pp.words; i += nt) pp.shb[i] = 0u;
-  __syncthreads();
-  // 1. group-shared blocks: the same valid physical block for every member
-  //    that reaches b (at least two), full blocks only, no mirror diff
-  if (pp.R > 1) {
-    for (int i = tid; i < pp.n_groups * pp.max_blocks; i += nt) {
-      const int gi = i / pp.max_blocks, b = i - gi * pp.max_blocks;
-      int cnt = 0, phys = -1;
-      bool ok = true;
-      uint32_t mask = 0;
-      for (int r = 0; r < pp.R; ++r) {
-        const int a = gi * pp.R + r;
-        if (a >= pp.n_seq) break;
-        const int L = min(max(pp.seq_len[a], 0), pp.max_blocks * 16);
-        if (b * 16 >= L) continue;
-        const int ph = pp.block_table[(size_t)a * pp.max_blocks + b];
-        const bool full = (b + 1) * 16 <= L;
-        const int d = pp.diff_table ? pp.diff_table[(size_t)a * pp.max_blocks + b] : -1;
-        if (!full || d >= 0 || ph < 0 || ph >= pp.capacity) ok = false;
-        if (cnt == 0) phys = ph;
-        else if (ph != phys) ok = false;
-        ++cnt;
-        mask |= 1u << r;
-      }
-      if (ok && cnt >= 2)
-        for (int r = 0; r < pp.R; ++r)
-          if ((mask >> r) & 1u) atomicOr(pp.shb + (size_t)(gi * pp.R + r) * pp.words + (b >> 5), 1u << (b & 31));
-    }
-  }
-  __syncthreads();
-  // 2. chunk occupancy: private chunks with unshared work; shared-chunk
-  //    participation per member
-  for (int i = tid; i < pp.n_seq * pp.n_chunks; i += nt) {
-    const int a = i / pp.n_chunks, c = i - a * pp.n_chunks;
-    const int nb = plan_seq_blocks(pp.seq_len, a, pp.max_blocks);
-    int any_priv = 0;
-    for (int b = c * pp.ib; b < min((c + 1) * pp.ib, nb); ++b)
-      any_priv |= !((pp.shb[(size_t)a * pp.words + (b >> 5)] >> (b & 31)) & 1u);
-    pp.pne[i] = (uint8_t)any_priv;
-  }
-  for (int i = tid; i < pp.n_groups * pp.n_chunks; i += nt) {
-    const int gi = i / pp.n_chunks, c = i - gi * pp.n_chunks;
-    uint32_t m = 0;
-    for (int r = 0; r < pp.R; ++r) {
-      const int a = gi * pp.R + r;
-      if (a >= pp.n_seq) break;
-      const int nb = plan_seq_blocks(pp.seq_len, a, pp.max_blocks);
-      for (int b = c * pp.ib; b < min((c + 1) * pp.ib, nb); ++b)
-        if ((pp.shb[(size_t)a * pp.words + (b >> 5)] >> (b & 31)) & 1u) {
-          m |= 1u << r;
-          break;
-        }
-    }
-    pp.spm[i] = (uint8_t)m;
-  }
-  __syncthreads();
-  // 3. compact item list: shared items (group, chunk) first, then private
-  //    items (sequence, chunk), chunk-major
-  const int n_sh = pp.n_groups * pp.n_chunks, n_pr = pp.n_seq * pp.n_chunks;
-  const int total = n_sh + n_pr;
-  if (tid == 0) s_carry = 0;
-  __syncthreads();
-  const int lane = tid & 31, warp = tid >> 5;
-  for (int base = 0; base < total; base += nt) {
-    const int i = base + tid;
-    int keep = 0;
-    int2 item = make_int2(0, 0);
-    if (i < n_sh) {
-      const int c = i / pp.n_groups, gi = i - c * pp.n_groups;
-      keep = pp.spm[gi * pp.n_chunks + c] != 0;
-      item = make_int2((1 << 30) | gi, c);
-    } else if (i < total) {
-      const int j = i - n_sh;
-      const int c = j / pp.n_seq, a = j - c * pp.n_seq;
-      keep = pp.pne[a * pp.n_chunks + c];
-      item = make_int2(a, c);
-    }
-    int x = keep;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int y = __shfl_up_sync(0xffffffffu, x, o);
-      if (lane >= o) x += y;
-    }
-    if (lane == 31) warp_sums[warp] = x;
-    __syncthreads();
-    if (warp == 0) {
-      int w = warp_sums[lane];
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int y = __shfl_up_sync(0xffffffffu, w, o);
-        if (lane >= o) w += y;
-      }
-      warp_sums[lane] = w;
-    }
-    __syncthreads();
-    const int pos = s_carry + x - keep + (warp ? warp_sums[warp - 1] : 0);
-    if (keep) pp.items[pos] = item;
-    __syncthreads();
-    if (tid == nt - 1) s_carry = pos + keep;
-    __syncthreads();
-  }
-  if (tid == 0) {
-    pp.hdr[0] = s_carry;
+  if (blockIdx.x == 0 && tid == 0) {
+    pp.hdr[0] = 0;   // item count, accumulated by tm_plan_items
     pp.hdr[1] = kPlanMagic;
     pp.hdr[2] = pp.n_seq;
     pp.hdr[3] = pp.max_blocks;
     pp.hdr[4] = pp.R;
     pp.hdr[5] = pp.ib;
     pp.hdr[6] = pp.hkv;
+  }
+  const float2 none = make_float2(-INFINITY, 0.f);
+  for (int gi = blockIdx.x; gi < pp.n_groups; gi += gridDim.x) {
+    const int a0 = gi * pp.R, nm = min(pp.R, pp.n_seq - a0);
+    // 1. sharing per logical block
+    if (pp.R > 1) {
+      for (int b = tid; b < pp.max_blocks; b += nt) {
+        int cnt = 0, phys = -1;
+        bool ok = true;
+        uint32_t mask = 0;
+        for (int r = 0; r < nm; ++r) {
+          const int a = a0 + r;
+          const int L = min(max(pp.seq_len[a], 0), pp.max_blocks * 16);
+          if (b * 16 >= L) continue;
+          const int ph = pp.block_table[(size_t)a * pp.max_blocks + b];
+          const bool full = (b + 1) * 16 <= L;
+          const int d = pp.diff_table ? pp.diff_table[(size_t)a * pp.max_blocks + b] : -1;
+          if (!full || d >= 0 || ph < 0 || ph >= pp.capacity) ok = false;
+          if (cnt == 0) phys = ph;
+          else if (ph != phys) ok = false;
+          ++cnt;
+          mask |= 1u << r;
+        }
+        const bool sh = ok && cnt >= 2;
+        pp.gmask[(size_t)gi * pp.max_blocks + b] = sh ? (uint8_t)mask : 0;
+        pp.gphys[(size_t)gi * pp.max_blocks + b] = sh ? phys : -1;
+      }
+      __syncthreads();
+    }
+    // 2. chunk occupancy
+    for (int i = tid; i < nm * pp.n_chunks; i += nt) {
+      const int r = i / pp.n_chunks, c = i - r * pp.n_chunks, a = a0 + r;
+      const int nb = plan_seq_blocks(pp.seq_len, a, pp.max_blocks);
+      int any_priv = 0;
+      for (int b = c * pp.ib; b < min((c + 1) * pp.ib, nb); ++b)
+        any_priv |= pp.R > 1 ? !((pp.gmask[(size_t)gi * pp.max_blocks + b] >> r) & 1u) : 1;
+      pp.pne[(size_t)a * pp.n_chunks + c] = (uint8_t)any_priv;
+    }
+    if (pp.R > 1) {
+      for (int c = tid; c < pp.n_chunks; c += nt) {
+        uint32_t m = 0;
+        for (int b = c * pp.ib; b < min((c + 1) * pp.ib, pp.max_blocks); ++b)
+          m |= pp.gmask[(size_t)gi * pp.max_blocks + b];
+        pp.spm[(size_t)gi * pp.n_chunks + c] = (uint8_t)m;
+      }
+    }
+    __syncthreads();
+    // 3. splits that no item writes
+    const int per_seq = pp.hkv * pp.n_chunks * pp.G;
+    for (int i = tid; i < nm * per_seq; i += nt) {
+      const int r = i / per_seq, rem = i - r * per_seq;
+      const int c = (rem / pp.G) % pp.n_chunks;
+      const int a = a0 + r;
+      const size_t e = (size_t)a * per_seq + rem;   // [a][h][c][hh]
+      if (!pp.pne[(size_t)a * pp.n_chunks + c]) reinterpret_cast<float2*>(pp.p1_ml)[e] = none;
+      if (pp.R > 1 && !((pp.spm[(size_t)gi * pp.n_chunks + c] >> r) & 1u))
+        reinterpret_cast<float2*>(pp.p2_ml)[e] = none;
+    }
+    __syncthreads();
+  }
+}
+
+// Plan, part 2: the compact item list, shared items (group, chunk) then
+// private items (sequence, chunk), chunk-major.  Each CTA compacts a run of
+// slots and reserves its place with one atomic add, so the list is
+// chunk-major up to the interleaving of CTAs; results do not depend on the
+// order (every split has a fixed slot and a fixed merge order).
+__global__ void __launch_bounds__(256) tm_plan_items(PlanParams pp) {
+  __shared__ int warp_sums[32];
+  __shared__ int s_base;
+  const int n_sh = pp.R > 1 ? pp.n_groups * pp.n_chunks : 0, n_pr = pp.n_seq * pp.n_chunks;
+  const int total = n_sh + n_pr;
+  for (int base = blockIdx.x * blockDim.x; base < total; base += gridDim.x * blockDim.x) {
+    const int i = base + threadIdx.x;
+    int keep = 0;
+    int4 item = make_int4(0, 0, 0, 0);
+    if (i < n_sh) {
+      const int c = i / pp.n_groups, gi = i - c * pp.n_groups;
+      const int m = pp.spm[(size_t)gi * pp.n_chunks + c];
+      keep = m != 0;
+      if (keep) {
+        int nb = 0;
+        for (int r = 0; r < pp.R && gi * pp.R + r < pp.n_seq; ++r)
+          nb = max(nb, plan_seq_blocks(pp.seq_len, gi * pp.R + r, pp.max_blocks));
+        item = make_int4((1 << 30) | gi, c, min((c + 1) * pp.ib, nb), m);
+      }
+    } else if (i < total) {
+      const int j = i - n_sh;
+      const int c = j / pp.n_seq, a = j - c * pp.n_seq;
+      keep = pp.pne[(size_t)a * pp.n_chunks + c];
+      if (keep)
+        item = make_int4(a, c, min((c + 1) * pp.ib, plan_seq_blocks(pp.seq_len, a, pp.max_blocks)), 1 << (a % pp.R));
+    }
+    int cnt;
+    const int pos = block_exclusive_scan(keep, warp_sums, cnt);
+    if (threadIdx.x == 0) s_base = cnt ? atomicAdd(pp.hdr, cnt) : 0;
+    __syncthreads();
+    if (keep) pp.items[s_base + pos] = item;
+    __syncthreads();
   }
 }
 
@@ -262,21 +283,35 @@ struct TmParams {
   float* p2;          // shared splits, same shape
   float* p2_ml;
   const int* hdr;
-  const int2* items;
-  const uint32_t* shb;
-  const uint8_t* pne;
-  const uint8_t* spm;
-  int32_t* sched;     // [0] work counter, [1] finished-warp counter
+  const int4* items;
+  const uint8_t* gmask;
+  const int32_t* gphys;
   uint32_t* status;
-  int max_blocks, n_seq, hkv, g, hq, ib, n_chunks, R, capacity, diff_capacity, total_warps, words;
+  int max_blocks, n_seq, hkv, g, hq, ib, n_chunks, R, capacity, diff_capacity;
+  int mwpr;           // merge warps per output row
   float scale_log2;
   RopeSplit rs;
+};
+
+// What the consumer needs about a claimed item, written by the producer.
+struct TmRec {
+  int id;                  // item * hkv + kv head
+  int x;                   // kind (bit 30) | group or sequence
+  int chunk;
+  int cact;                // members whose columns take part
+  int seg_beg, seg_end;    // the sequence's RoPE segment range (rotation calls)
+  int len[kTmMaxGroup];    // context lengths: of each member (shared), of the sequence in len[0] (private)
+  int pad[2];
 };
 
 __device__ __forceinline__ uint32_t movm_t(uint32_t x) {
   uint32_t y;
   asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
   return y;
+}
+
+__device__ __forceinline__ void prefetch_l1(const void* ptr) {
+  asm volatile("prefetch.global.L1 [%0];" ::"l"(ptr));
 }
 
 template <int D, bool DIFF, bool ROPE>
@@ -287,13 +322,15 @@ attn_tm_kernel(const __grid_constant__ TmParams p, const __grid_constant__ CUten
   constexpr int B = 16, TILE = B * D * 2, KS = D / 16;
   constexpr int S = tm_stages<D>();
   constexpr int STAGE = 2 * TILE;
+  static_assert(kTmRec > S + 1, "claim records must outnumber the items a ring can hold");
   extern __shared__ uint8_t smem_raw[];
   __shared__ uint64_t bars[kTmWarps][S];
-  __shared__ int st_item[kTmWarps][S];
+  __shared__ int st_ord[kTmWarps][S];    // claim ordinal of the block in the stage; -1: no more work
   // block index; bit 30: the next position holds the block's diff tiles;
   // bit 29: the block id was out of range and nothing was loaded
   __shared__ int st_block[kTmWarps][S];
   __shared__ int st_mask[kTmWarps][S];   // group members whose columns take this block
+  __shared__ TmRec recs[kTmWarps][kTmRec];
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, c = lane & 3;
@@ -309,79 +346,100 @@ attn_tm_kernel(const __grid_constant__ TmParams p, const __grid_constant__ CUten
   }
   __syncwarp();
 
-  // empty contexts produce zero output (they have no work items)
-  for (size_t e = (size_t)blockIdx.x * blockDim.x + threadIdx.x; e < (size_t)p.n_seq * p.hq * D;
-       e += (size_t)gridDim.x * blockDim.x)
-    if (p.seq_len[e / ((size_t)p.hq * D)] <= 0) p.out[e] = 0.f;
-
   // the plan must have been built for this call's shapes
   const bool plan_ok = p.hdr[1] == kPlanMagic && p.hdr[2] == p.n_seq && p.hdr[3] == p.max_blocks &&
                        p.hdr[4] == p.R && p.hdr[5] == p.ib && p.hdr[6] == p.hkv;
   if (!plan_ok && threadIdx.x == 0 && blockIdx.x == 0) set_err(p.status, KVS_DEVERR_PLAN);
   const int n_claims = plan_ok ? p.hdr[0] * p.hkv : 0;
   const int R = p.R;
-  auto seq_blocks = [&](int a) {
-    int L = p.seq_len[a];
-    if (L < 0 || L > p.max_blocks * B) L = L < 0 ? 0 : p.max_blocks * B;
-    return (L + B - 1) / B;
-  };
 
   // ------------------------------------------ producer state (warp-uniform)
-  // The whole warp runs the producer logic; lane 0 alone issues the atomics
-  // and the TMA copies.  When an item is claimed, lane j loads what block
-  // b0 + j of the item needs (physical id, diff id, sharing), so issuing a
-  // block costs shuffles instead of global loads.
-  int p_claim = -1, p_kind = 0, p_h = 0, p_b = 0, p_b0 = 0, p_bend = 0, p_mask = 0;
+  // This warp's claims are gw, gw + T, gw + 2T, ... (claim id = item * hkv +
+  // kv head).  The item entry of the claim after next and the per-lane block
+  // entries of the next claim are loaded one claim early, so they have
+  // arrived by the time they are used.
+  const int T = gridDim.x * kTmWarps;
+  int n_id = blockIdx.x * kTmWarps + warp;   // next claim
+  int4 n_it = make_int4(0, 0, 0, 0), nn_it = n_it;
+  int n_tab = -1, n_aux = 0, n_dif = -1, n_len = 0, n_sg = 0;
+  auto load_item = [&](int id) {
+    return id < n_claims ? __ldg(p.items + id / p.hkv) : make_int4(0, 0, 0, 0);
+  };
+  // issue the loads for claim id (item entry it); nothing here consumes them
+  auto prepare = [&](int id, const int4& it) {
+    n_tab = -1; n_aux = 0; n_dif = -1; n_len = 0; n_sg = 0;
+    if (id >= n_claims) return;
+    const int kind = it.x >> 30, idx = it.x & ((1 << 30) - 1);
+    const int b = it.y * p.ib + lane;
+    const bool in = b < it.z;
+    if (kind) {
+      if (in) {
+        n_tab = __ldg(p.gphys + (size_t)idx * p.max_blocks + b);
+        n_aux = __ldg(p.gmask + (size_t)idx * p.max_blocks + b);
+      }
+      if (lane < R && idx * R + lane < p.n_seq) n_len = __ldg(p.seq_len + idx * R + lane);
+    } else {
+      if (in) {
+        n_tab = __ldg(p.block_table + (size_t)idx * p.max_blocks + b);
+        if (R > 1) n_aux = __ldg(p.gmask + (size_t)(idx / R) * p.max_blocks + b);   // raw member bits
+        if (DIFF) n_dif = __ldg(p.diff_table + (size_t)idx * p.max_blocks + b);
+      }
+      if (lane == 0) n_len = __ldg(p.seq_len + idx);
+      if (ROPE && lane < 2) n_sg = __ldg(p.rope_off + idx + lane);
+    }
+    // the query rows of the item's live columns, into L1 for the consumer
+    constexpr int LPR = D * 2 / 128;   // 128-byte lines per query row
+    const int col = lane / LPR, part = lane - col * LPR;
+    const int h = id - (id / p.hkv) * p.hkv;
+    if (col < 8 && col < R * p.g) {
+      const int slot = col / p.g, hh = col - slot * p.g;
+      if ((it.w >> slot) & 1) {
+        const int a = kind ? idx * R + slot : idx;
+        if (a < p.n_seq) prefetch_l1(p.q + ((size_t)a * p.hq + h * p.g + hh) * D + part * 64);
+      }
+    }
+  };
+  n_it = load_item(n_id);
+  nn_it = load_item(n_id + T);
+  prepare(n_id, n_it);
+
+  int ord = -1;   // ordinal of the current claim
+  int p_kind = 0, p_h = 0, p_b = 0, p_b0 = 0, p_bend = 0, p_mask = 0, p_slot = 0;
   int tab_ent = -1, dif_ent = -1, aux_ent = 0;
   bool p_done = false;
   auto claim = [&]() {
-    while (true) {
-      int id = 0;
-      if (lane == 0) id = atomicAdd(p.sched, 1);
-      id = __shfl_sync(0xffffffffu, id, 0);
-      if (id >= n_claims) {
-        p_done = true;
-        return;
-      }
-      const int2 it = p.items[id / p.hkv];
-      const int h = id - (id / p.hkv) * p.hkv;
-      const int b0 = it.y * p.ib;
-      p_claim = id; p_h = h; p_b = b0; p_b0 = b0;
-      if (it.x >> 30) {   // shared item of group it.x & mask
-        const int gi = it.x & ((1 << 30) - 1);
-        p_kind = 1;
-        int nbmax = 0;
-        for (int r = 0; r < R; ++r)
-          if (gi * R + r < p.n_seq) nbmax = max(nbmax, seq_blocks(gi * R + r));
-        p_bend = min(b0 + p.ib, nbmax);
-        const int b = b0 + lane;
-        int msk = 0, ph = -1;
-        if (b < p_bend) {
-          for (int r = 0; r < R; ++r) {
-            const int a = gi * R + r;
-            if (a >= p.n_seq) break;
-            if ((p.shb[(size_t)a * p.words + (b >> 5)] >> (b & 31)) & 1u) {
-              msk |= 1 << r;
-              ph = p.block_table[(size_t)a * p.max_blocks + b];
-            }
-          }
-        }
-        tab_ent = ph;
-        aux_ent = msk;
-        dif_ent = -1;
-      } else {           // private item of sequence it.x
-        const int a = it.x;
-        p_kind = 0;
-        p_bend = min(b0 + p.ib, seq_blocks(a));
-        p_mask = 1 << (a % R);
-        const int b = b0 + lane;
-        const bool in = b < p_bend;
-        tab_ent = in ? __ldg(p.block_table + (size_t)a * p.max_blocks + b) : -1;
-        aux_ent = in ? (int)((p.shb[(size_t)a * p.words + (b >> 5)] >> (b & 31)) & 1u) : 1;   // 1 = skip
-        if (DIFF) dif_ent = in ? __ldg(p.diff_table + (size_t)a * p.max_blocks + b) : -1;
-      }
+    if (n_id >= n_claims) {
+      p_done = true;
       return;
     }
+    const int4 it = n_it;
+    ++ord;
+    p_kind = it.x >> 30;
+    p_h = n_id - (n_id / p.hkv) * p.hkv;
+    p_b0 = p_b = it.y * p.ib;
+    p_bend = it.z;
+    p_mask = it.w;
+    p_slot = p_kind ? 0 : (it.x & ((1 << 30) - 1)) % R;
+    tab_ent = n_tab;
+    aux_ent = n_aux;
+    dif_ent = n_dif;
+    TmRec& rec = recs[warp][ord & (kTmRec - 1)];
+    if (lane == 0) {
+      rec.id = n_id;
+      rec.x = it.x;
+      rec.chunk = it.y;
+      rec.cact = it.w;
+    }
+    if (lane < kTmMaxGroup) rec.len[lane] = n_len;
+    if (ROPE) {
+      if (lane == 0) rec.seg_beg = n_sg;
+      if (lane == 1) rec.seg_end = n_sg;
+    }
+    // advance: the next claim's entries, then the entry of the one after
+    n_id += T;
+    n_it = nn_it;
+    prepare(n_id, n_it);
+    nn_it = load_item(n_id + T);
   };
   int pend_drow = -1;   // a diff tile pair still to issue for the last block
   auto issue = [&](int s) {   // whole warp; lane 0 issues
@@ -405,11 +463,11 @@ attn_tm_kernel(const __grid_constant__ TmParams p, const __grid_constant__ CUten
       const int ent = __shfl_sync(0xffffffffu, tab_ent, j);
       const int aux = __shfl_sync(0xffffffffu, aux_ent, j);
       if (p_kind == 0) {
-        if (aux) continue;          // computed by the group's shared item
+        if ((aux >> p_slot) & 1) continue;   // computed by the group's shared item
         mask = p_mask;
         if (DIFF) did = __shfl_sync(0xffffffffu, dif_ent, j);
       } else {
-        if (aux == 0) continue;     // not shared at this block
+        if (aux == 0) continue;              // not shared at this block
         mask = aux;
       }
       phys = ent;
@@ -417,7 +475,7 @@ attn_tm_kernel(const __grid_constant__ TmParams p, const __grid_constant__ CUten
     }
     if (p_done) {
       if (lane == 0) {
-        st_item[warp][s] = -1;
+        st_ord[warp][s] = -1;
         mbar_arrive(bar);
       }
       return;
@@ -426,7 +484,7 @@ attn_tm_kernel(const __grid_constant__ TmParams p, const __grid_constant__ CUten
     const bool dval = DIFF && valid && did >= 0 && did < p.diff_capacity;
     if (dval) pend_drow = (did * p.hkv + p_h) * B;
     if (lane != 0) return;
-    st_item[warp][s] = p_claim;
+    st_ord[warp][s] = ord;
     st_mask[warp][s] = mask;
     if (!valid) {
       set_err(p.status, KVS_DEVERR_BLOCK_ID);
@@ -530,7 +588,7 @@ attn_tm_kernel(const __grid_constant__ TmParams p, const __grid_constant__ CUten
   for (int i = 0;;) {
     const int s = i % S;
     if (!mbar_wait_bounded(&bars[warp][s], (i / S) & 1, p.status)) break;
-    const int item = st_item[warp][s];
+    const int item = st_ord[warp][s];
     const int bword = st_block[warp][s];
     const int emask = st_mask[warp][s];
     if (item < 0) break;
@@ -542,20 +600,17 @@ attn_tm_kernel(const __grid_constant__ TmParams p, const __grid_constant__ CUten
     if (item != cur) {
       if (cur >= 0) flush();
       cur = item;
-      const int2 it = p.items[item / p.hkv];
-      ch_ = item - (item / p.hkv) * p.hkv;
-      cchunk = it.y;
-      ckind = it.x >> 30;
-      cidx = it.x & ((1 << 30) - 1);
+      __syncwarp();   // the record was written by several lanes
+      const TmRec& rec = recs[warp][item & (kTmRec - 1)];
+      ch_ = rec.id - (rec.id / p.hkv) * p.hkv;
+      cchunk = rec.chunk;
+      ckind = rec.x >> 30;
+      cidx = rec.x & ((1 << 30) - 1);
+      cact = rec.cact;
       int agent_of_col = -1;   // sequence of this lane's query column (n = g)
-      if (ckind) {
-        cact = p.spm[cidx * p.n_chunks + cchunk];
+      {
         const int slot = g / p.g;
-        if (g < R * p.g && ((cact >> slot) & 1)) agent_of_col = cidx * R + slot;
-      } else {
-        const int slot = cidx % R;
-        cact = 1 << slot;
-        if (g / p.g == slot && g < R * p.g) agent_of_col = cidx;
+        if (g < R * p.g && ((cact >> slot) & 1)) agent_of_col = ckind ? cidx * R + slot : cidx;
       }
       qok = agent_of_col >= 0;
       qrow = p.q + ((size_t)(qok ? agent_of_col : 0) * p.hq + ch_ * p.g + (g % p.g)) * D;
@@ -563,10 +618,9 @@ attn_tm_kernel(const __grid_constant__ TmParams p, const __grid_constant__ CUten
       for (int cc = 0; cc < 2; ++cc) {
         const int j = 2 * c + cc;
         const int slot = j / p.g;
-        int a = -1;
-        if (j < R * p.g && ((cact >> slot) & 1)) a = ckind ? cidx * R + slot : cidx;
-        colslot[cc] = a >= 0 ? slot : 31;
-        colL[cc] = a >= 0 ? min(max(p.seq_len[a], 0), p.max_blocks * B) : 0;
+        const bool on = j < R * p.g && ((cact >> slot) & 1);
+        colslot[cc] = on ? slot : 31;
+        colL[cc] = on ? min(max(rec.len[ckind ? slot : 0], 0), p.max_blocks * B) : 0;
       }
       m[0] = m[1] = -INFINITY;
       l[0] = l[1] = 0.f;
@@ -576,8 +630,8 @@ attn_tm_kernel(const __grid_constant__ TmParams p, const __grid_constant__ CUten
       cur_delta = 0;
       seg_lo = seg_hi = 0;
       if (ROPE) {
-        seg_beg = p.rope_off[cidx];
-        seg_end = p.rope_off[cidx + 1];
+        seg_beg = rec.seg_beg;
+        seg_end = rec.seg_end;
       }
     }
     if (loaded) {
@@ -694,68 +748,62 @@ attn_tm_kernel(const __grid_constant__ TmParams p, const __grid_constant__ CUten
     i += has_diff ? 2 : 1;
   }
   if (cur >= 0) flush();
-  // the last warp of the launch to finish resets the scheduler for the next one
-  if (lane == 0) {
-    __threadfence();
-    const int done = atomicAdd(p.sched + 1, 1);
-    if (done == p.total_warps - 1) {
-      p.sched[0] = 0;
-      p.sched[1] = 0;
-    }
-  }
 }
 
-// Split merge: one warp per (sequence, query head) row, so every row of every
-// (sequence, kv head) merges in parallel, each lane keeping up to
-// kMergeBatch independent split loads in flight.  The split order is fixed
-// (chunk order, private then shared per 32-chunk window), so the result does
-// not depend on which warp computed which split.
+// Split merge: p.mwpr warps (1, 2, 4 or 8) per (sequence, query head) row,
+// eight warps per CTA.  Each warp merges a fixed range of about ten of the
+// row's chunks (every lane keeping up to kMergeBatch independent split loads
+// in flight), then the partial states of a row combine through shared memory.
+// The partition and the order are fixed, so the result does not depend on
+// which warp computed which split.
 constexpr int kMergeWarps = 8;
-constexpr int kMergeBatch = 12;   // independent split loads in flight per lane
+constexpr int kMergeBatch = 10;
 
 template <int D>
 __global__ void __launch_bounds__(kMergeWarps * 32, 2) tm_merge_kernel(const __grid_constant__ TmParams p) {
   asm volatile("griddepcontrol.wait;" ::: "memory");
   constexpr int CPL = D / 32;   // columns per lane
-  const int lane = threadIdx.x & 31;
-  const int row = blockIdx.x * kMergeWarps + (threadIdx.x >> 5);   // sequence * hq + query head
-  if (row >= p.n_seq * p.hq) return;
+  __shared__ float sM[kMergeWarps], sL[kMergeWarps];
+  __shared__ __align__(16) float sv[kMergeWarps][D];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int wpr = p.mwpr;
+  const int rl = warp / wpr, wq = warp - rl * wpr;
+  const int row = blockIdx.x * (kMergeWarps / wpr) + rl;   // sequence * hq + query head
   // the attention kernel has flagged a plan built for other shapes and
   // computed nothing; leave the output untouched as well
-  if (!(p.hdr[1] == kPlanMagic && p.hdr[2] == p.n_seq && p.hdr[3] == p.max_blocks && p.hdr[4] == p.R &&
-        p.hdr[5] == p.ib && p.hdr[6] == p.hkv))
-    return;
-  const int a = row / p.hq, qh = row - a * p.hq, h = qh / p.g, hh = qh - h * p.g;
-  const int gi = a / p.R, slot = a - gi * p.R;
+  const bool plan_ok = p.hdr[1] == kPlanMagic && p.hdr[2] == p.n_seq && p.hdr[3] == p.max_blocks &&
+                       p.hdr[4] == p.R && p.hdr[5] == p.ib && p.hdr[6] == p.hkv;
+  const bool in_range = row < p.n_seq * p.hq;
+  const int a = in_range ? row / p.hq : 0, qh = row - a * p.hq, h = qh / p.g, hh = qh - h * p.g;
+  const bool live = plan_ok && in_range && p.seq_len[a] > 0;
   const size_t sbase = ((size_t)a * p.hkv + h) * p.n_chunks;
-  float* o = p.out + (size_t)row * D + lane * CPL;
-  if (p.seq_len[a] <= 0) {
-#pragma unroll
-    for (int j = 0; j < CPL; ++j) o[j] = 0.f;
-    return;
-  }
-  // lane k owns chunks c0 + k of every 32-chunk window; the first two windows
-  // keep their (m, l) in registers between the passes
-  float2 cp0 = make_float2(0.f, 0.f), cs0 = cp0, cp1 = cp0, cs1 = cp0;
-  bool hp0 = false, hs0 = false, hp1 = false, hs1 = false;
-  auto own = [&](int c0, bool& pv, bool& sv, float2& mp, float2& ms) {
+  const int cpw = (p.n_chunks + wpr - 1) / wpr;
+  const int cbeg = wq * cpw, cend = live ? min(p.n_chunks, cbeg + cpw) : 0;
+
+  // lane k owns chunks c0 + k of each 32-chunk window of this warp's range;
+  // the first window keeps its (m, l) in registers between the passes.  The
+  // plan set the (m, l) of splits that no item writes to (-inf, 0), so a
+  // split exists exactly when its l is positive.
+  auto own = [&](int c0, bool& pv, bool& sv_, float2& mp, float2& ms) {
     const int ck = c0 + lane;
-    pv = ck < p.n_chunks && p.pne[a * p.n_chunks + ck];
-    sv = p.R > 1 && ck < p.n_chunks && ((p.spm[gi * p.n_chunks + ck] >> slot) & 1);
-    mp = pv ? __ldcg(reinterpret_cast<const float2*>(p.p1_ml + ((sbase + ck) * p.g + hh) * 2)) : make_float2(0.f, 0.f);
-    ms = sv ? __ldcg(reinterpret_cast<const float2*>(p.p2_ml + ((sbase + ck) * p.g + hh) * 2)) : make_float2(0.f, 0.f);
+    const bool in = ck < cend;
+    mp = in ? __ldcg(reinterpret_cast<const float2*>(p.p1_ml + ((sbase + ck) * p.g + hh) * 2)) : make_float2(0.f, 0.f);
+    ms = in && p.R > 1 ? __ldcg(reinterpret_cast<const float2*>(p.p2_ml + ((sbase + ck) * p.g + hh) * 2))
+                       : make_float2(0.f, 0.f);
+    pv = mp.y > 0.f;
+    sv_ = ms.y > 0.f;
   };
+  float2 cp0 = make_float2(0.f, 0.f), cs0 = cp0;
+  bool hp0 = false, hs0 = false;
   float M = -INFINITY;
-  for (int c0 = 0, w = 0; c0 < p.n_chunks; c0 += 32, ++w) {
-    bool pv, sv;
+  for (int c0 = cbeg; c0 < cend; c0 += 32) {
+    bool pv, sv_;
     float2 mp, ms;
-    own(c0, pv, sv, mp, ms);
-    if (pv && mp.y > 0.f) M = fmaxf(M, mp.x);
-    if (sv && ms.y > 0.f) M = fmaxf(M, ms.x);
-    if (w == 0) {
-      hp0 = pv; hs0 = sv; cp0 = mp; cs0 = ms;
-    } else if (w == 1) {
-      hp1 = pv; hs1 = sv; cp1 = mp; cs1 = ms;
+    own(c0, pv, sv_, mp, ms);
+    if (pv) M = fmaxf(M, mp.x);
+    if (sv_) M = fmaxf(M, ms.x);
+    if (c0 == cbeg) {
+      hp0 = pv; hs0 = sv_; cp0 = mp; cs0 = ms;
     }
   }
 #pragma unroll
@@ -763,24 +811,22 @@ __global__ void __launch_bounds__(kMergeWarps * 32, 2) tm_merge_kernel(const __g
   float Ls = 0.f, v[CPL];
 #pragma unroll
   for (int j = 0; j < CPL; ++j) v[j] = 0.f;
-  for (int c0 = 0, w = 0; c0 < p.n_chunks; c0 += 32, ++w) {
-    bool pv, sv;
+  for (int c0 = cbeg; c0 < cend; c0 += 32) {
+    bool pv, sv_;
     float2 mp, ms;
-    if (w == 0) {
-      pv = hp0; sv = hs0; mp = cp0; ms = cs0;
-    } else if (w == 1) {
-      pv = hp1; sv = hs1; mp = cp1; ms = cs1;
+    if (c0 == cbeg) {
+      pv = hp0; sv_ = hs0; mp = cp0; ms = cs0;
     } else {
-      own(c0, pv, sv, mp, ms);
+      own(c0, pv, sv_, mp, ms);
     }
-    const float wp = pv && mp.y > 0.f ? fast_exp2(mp.x - M) : 0.f;
-    const float ws = sv && ms.y > 0.f ? fast_exp2(ms.x - M) : 0.f;
+    const float wp = pv ? fast_exp2(mp.x - M) : 0.f;
+    const float ws = sv_ ? fast_exp2(ms.x - M) : 0.f;
     Ls += wp * mp.y + ws * ms.y;
 #pragma unroll
     for (int kind = 0; kind < 2; ++kind) {
       const float* P = kind ? p.p2 : p.p1;
       const float wk = kind ? ws : wp;
-      unsigned mk = __ballot_sync(0xffffffffu, kind ? sv : pv);
+      unsigned mk = __ballot_sync(0xffffffffu, kind ? sv_ : pv);
       while (mk) {   // warp-uniform
         int idx[kMergeBatch];
 #pragma unroll
@@ -816,11 +862,41 @@ __global__ void __launch_bounds__(kMergeWarps * 32, 2) tm_merge_kernel(const __g
   }
 #pragma unroll
   for (int off = 16; off; off >>= 1) Ls += __shfl_xor_sync(0xffffffffu, Ls, off);
-  const float inv = Ls > 0.f ? 1.f / Ls : 0.f;
+  float* o = p.out + (size_t)row * D + lane * CPL;
+  float Mt = M, Lt = Ls, r[CPL];
+#pragma unroll
+  for (int j = 0; j < CPL; ++j) r[j] = v[j];
+  if (wpr > 1) {
+    if (lane == 0) {
+      sM[warp] = M;
+      sL[warp] = Ls;
+    }
+#pragma unroll
+    for (int j = 0; j < CPL; ++j) sv[warp][lane * CPL + j] = v[j];
+    __syncthreads();
+    if (wq != 0) return;
+    const int w0 = rl * wpr;
+    Mt = -INFINITY;
+    for (int w = 0; w < wpr; ++w)
+      if (sL[w0 + w] > 0.f) Mt = fmaxf(Mt, sM[w0 + w]);
+    Lt = 0.f;
+#pragma unroll
+    for (int j = 0; j < CPL; ++j) r[j] = 0.f;
+    for (int w = 0; w < wpr; ++w) {
+      const float lw = sL[w0 + w];
+      const float wt = lw > 0.f ? fast_exp2(sM[w0 + w] - Mt) : 0.f;
+      Lt += wt * lw;
+#pragma unroll
+      for (int j = 0; j < CPL; ++j) r[j] += wt * sv[w0 + w][lane * CPL + j];
+    }
+  }
+  if (!in_range || !plan_ok) return;
+  // an empty context (no splits at all) gives a zero output
+  const float inv = Lt > 0.f ? 1.f / Lt : 0.f;
   if (CPL == 4) {
-    *reinterpret_cast<float4*>(o) = make_float4(v[0] * inv, v[1 % CPL] * inv, v[2 % CPL] * inv, v[3 % CPL] * inv);
+    *reinterpret_cast<float4*>(o) = make_float4(r[0] * inv, r[1 % CPL] * inv, r[2 % CPL] * inv, r[3 % CPL] * inv);
   } else {
-    *reinterpret_cast<float2*>(o) = make_float2(v[0] * inv, v[1 % CPL] * inv);
+    *reinterpret_cast<float2*>(o) = make_float2(r[0] * inv, r[1 % CPL] * inv);
   }
 }
 
@@ -828,7 +904,8 @@ template <int D>
 static kvs_status launch_merge(const TmParams& prm, cudaStream_t st) {
   const int rows = prm.n_seq * prm.hq;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((rows + kMergeWarps - 1) / kMergeWarps);
+  const int rows_per_cta = kMergeWarps / prm.mwpr;
+  cfg.gridDim = dim3((rows + rows_per_cta - 1) / rows_per_cta);
   cfg.blockDim = dim3(kMergeWarps * 32);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = st;
@@ -842,6 +919,7 @@ static kvs_status launch_merge(const TmParams& prm, cudaStream_t st) {
   count_launch();
   return check_launch("decode_attn_merge");
 }
+
 
 template <int D, bool DIFF, bool ROPE>
 static kvs_status launch_tm(TmParams& prm, const kvs_pool* pool, int layer, int max_claims, cudaStream_t st) {
@@ -860,9 +938,8 @@ static kvs_status launch_tm(TmParams& prm, const kvs_pool* pool, int layer, int 
     occ.store(blocks_per_sm, std::memory_order_relaxed);
   }
   // persistent grid: every SM filled once, but never more warps than the
-  // largest possible number of claims (idle warps would only contend)
+  // largest possible number of claims
   const int grid = std::max(1, std::min(pool->num_sms * blocks_per_sm, (max_claims + kTmWarps - 1) / kTmWarps));
-  prm.total_warps = grid * kTmWarps;
   const CUtensorMap& dk = DIFF ? pool->tdk[layer] : pool->tk[layer];
   const CUtensorMap& dv = DIFF ? pool->tdv[layer] : pool->tv[layer];
   kern<<<grid, 128, smem, st>>>(prm, pool->tk[layer], pool->tv[layer], dk, dv);
@@ -872,21 +949,52 @@ static kvs_status launch_tm(TmParams& prm, const kvs_pool* pool, int layer, int 
   return launch_merge<D>(prm, st);
 }
 
+// workspace pointers shared by the plan and the launch
+struct TmPtrs {
+  int* hdr;
+  int4* items;
+  uint8_t* gmask;
+  int32_t* gphys;
+  uint8_t* pne;
+  uint8_t* spm;
+  float *p1, *p1_ml, *p2, *p2_ml;
+};
+
+static TmPtrs tm_ptrs(const TmLayout& L, const kvs_pool* pool, int n_seq, int g, void* ws) {
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  const size_t split_vals = (size_t)n_seq * pool->desc.num_kv_heads * L.n_chunks * g * pool->desc.head_dim;
+  TmPtrs t{};
+  t.hdr = reinterpret_cast<int*>(w + L.off_hdr);
+  t.items = reinterpret_cast<int4*>(w + L.off_items);
+  t.gmask = w + L.off_gmask;
+  t.gphys = reinterpret_cast<int32_t*>(w + L.off_gphys);
+  t.pne = w + L.off_pne;
+  t.spm = w + L.off_spm;
+  t.p1 = reinterpret_cast<float*>(w + L.off_p1);
+  t.p1_ml = t.p1 + split_vals;
+  t.p2 = reinterpret_cast<float*>(w + L.off_p2);
+  t.p2_ml = t.p2 + (L.R > 1 ? split_vals : 0);
+  return t;
+}
+
 kvs_status decode_plan_token_major(kvs_pool* pool, int n_q_heads, const int32_t* table, int max_blocks,
                                    const int32_t* seq_len, int n_seq, const int32_t* diff, bool rope, void* ws,
                                    cudaStream_t stream) {
   const int g = n_q_heads / pool->desc.num_kv_heads;
   const TmLayout L = tm_layout(pool, n_seq, max_blocks, g, rope);
-  uint8_t* w = static_cast<uint8_t*>(ws);
+  const TmPtrs t = tm_ptrs(L, pool, n_seq, g, ws);
   PlanParams pp{};
   pp.block_table = table;
   pp.seq_len = seq_len;
   pp.diff_table = diff;
-  pp.hdr = reinterpret_cast<int*>(w + L.off_hdr);
-  pp.items = reinterpret_cast<int2*>(w + L.off_items);
-  pp.shb = reinterpret_cast<uint32_t*>(w + L.off_shb);
-  pp.pne = w + L.off_pne;
-  pp.spm = w + L.off_spm;
+  pp.hdr = t.hdr;
+  pp.items = t.items;
+  pp.gmask = t.gmask;
+  pp.gphys = t.gphys;
+  pp.pne = t.pne;
+  pp.spm = t.spm;
+  pp.p1_ml = t.p1_ml;
+  pp.p2_ml = t.p2_ml;
   pp.n_seq = n_seq;
   pp.max_blocks = max_blocks;
   pp.R = L.R;
@@ -894,11 +1002,16 @@ kvs_status decode_plan_token_major(kvs_pool* pool, int n_q_heads, const int32_t*
   pp.ib = L.ib;
   pp.n_chunks = L.n_chunks;
   pp.n_groups = L.n_groups;
-  pp.words = L.words;
   pp.capacity = pool->desc.capacity_blocks;
-  pp.diff_capacity = pool->desc.diff_capacity_blocks;
   pp.hkv = pool->desc.num_kv_heads;
-  tm_plan_kernel<<<1, 1024, 0, stream>>>(pp);
+  const int g1 = std::max(1, std::min(L.n_groups, pool->num_sms * 4));
+  tm_plan_groups<<<g1, 256, 0, stream>>>(pp);
+  count_launch();
+  kvs_status st = check_launch("decode_plan");
+  if (st != KVS_OK) return st;
+  const long long slots = (long long)L.max_items;
+  const int g2 = (int)std::max<long long>(1, std::min<long long>((slots + 255) / 256, pool->num_sms * 8));
+  tm_plan_items<<<g2, 256, 0, stream>>>(pp);
   count_launch();
   return check_launch("decode_plan");
 }
@@ -911,8 +1024,7 @@ kvs_status decode_attn_token_major(kvs_pool* pool, int layer, const void* q, int
   const int g = n_q_heads / d.num_kv_heads;
   const bool rope = rope_off != nullptr, dif = diff != nullptr;
   const TmLayout L = tm_layout(pool, n_seq, max_blocks, g, rope);
-  uint8_t* w = static_cast<uint8_t*>(ws);
-  const size_t splits = (size_t)n_seq * d.num_kv_heads * L.n_chunks;
+  const TmPtrs t = tm_ptrs(L, pool, n_seq, g, ws);
   TmParams prm{};
   prm.q = static_cast<const uint16_t*>(q);
   prm.block_table = table;
@@ -921,16 +1033,14 @@ kvs_status decode_attn_token_major(kvs_pool* pool, int layer, const void* q, int
   prm.rope_off = rope_off;
   prm.rope_segs = reinterpret_cast<const int4*>(rope_segs);
   prm.out = out;
-  prm.p1 = reinterpret_cast<float*>(w + L.off_p1);
-  prm.p1_ml = prm.p1 + splits * g * d.head_dim;
-  prm.p2 = reinterpret_cast<float*>(w + L.off_p2);
-  prm.p2_ml = prm.p2 + (L.R > 1 ? splits * g * d.head_dim : 0);
-  prm.hdr = reinterpret_cast<const int*>(w + L.off_hdr);
-  prm.items = reinterpret_cast<const int2*>(w + L.off_items);
-  prm.shb = reinterpret_cast<const uint32_t*>(w + L.off_shb);
-  prm.pne = w + L.off_pne;
-  prm.spm = w + L.off_spm;
-  prm.sched = pool->sched;
+  prm.p1 = t.p1;
+  prm.p1_ml = t.p1_ml;
+  prm.p2 = t.p2;
+  prm.p2_ml = t.p2_ml;
+  prm.hdr = t.hdr;
+  prm.items = t.items;
+  prm.gmask = t.gmask;
+  prm.gphys = t.gphys;
   prm.status = pool->status;
   prm.max_blocks = max_blocks;
   prm.n_seq = n_seq;
@@ -940,12 +1050,14 @@ kvs_status decode_attn_token_major(kvs_pool* pool, int layer, const void* q, int
   prm.ib = L.ib;
   prm.n_chunks = L.n_chunks;
   prm.R = L.R;
-  prm.words = L.words;
   prm.capacity = d.capacity_blocks;
   prm.diff_capacity = d.diff_capacity_blocks;
   prm.scale_log2 = scale * 1.4426950408889634f;
+  // about ten chunks per merge warp
+  prm.mwpr = 1;
+  while (prm.mwpr < kMergeWarps && prm.mwpr * kMergeBatch < L.n_chunks) prm.mwpr <<= 1;
   if (rope) rope_split_host(theta, d.head_dim, prm.rs.c);
-  const int max_claims = (int)std::min<size_t>(L.max_entries * d.num_kv_heads, 0x7fffffff);
+  const int max_claims = (int)std::min<size_t>(L.max_items * d.num_kv_heads, 0x7fffffff);
   if (d.head_dim == 128) {
     if (dif) return rope ? launch_tm<128, true, true>(prm, pool, layer, max_claims, stream)
                          : launch_tm<128, true, false>(prm, pool, layer, max_claims, stream);

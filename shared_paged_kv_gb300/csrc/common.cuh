@@ -200,4 +200,34 @@ __device__ __forceinline__ void rope_cos_sin(const RopeSplit& rs, int i, int del
   __sincosf(6.28318530717958647692f * turns, &sn, &cs);
 }
 
+
+// Exclusive prefix sum of x over the CTA (blockDim.x a multiple of 32, at
+// most 1024 threads); total receives the CTA-wide sum.  warp_sums needs one
+// int per warp.  Every thread of the CTA must call it.
+__device__ __forceinline__ int block_exclusive_scan(int x, int* warp_sums, int& total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int incl = x;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  if (lane == 31) warp_sums[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    int w = lane < (int)(blockDim.x >> 5) ? warp_sums[lane] : 0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, w, o);
+      if (lane >= o) w += y;
+    }
+    warp_sums[lane] = w;
+  }
+  __syncthreads();
+  const int res = incl - x + (warp ? warp_sums[warp - 1] : 0);
+  total = warp_sums[(blockDim.x >> 5) - 1];
+  __syncthreads();
+  return res;
+}
+
 }  // namespace kvs

@@ -19,7 +19,6 @@ struct kvs_pool {
   uint32_t* status = nullptr;                   // device status word (owned)
   int32_t* tickets = nullptr;                   // split-K arrival counters (owned)
   size_t n_tickets = 0;
-  int32_t* sched = nullptr;                     // persistent-kernel work counters (owned, 2 ints)
 };
 
 namespace kvs {

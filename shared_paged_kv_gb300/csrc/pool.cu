@@ -206,12 +206,10 @@ kvs_status kvs_pool_create(const kvs_pool_desc* d, void* const* k_layers, void* 
   p->n_tickets = static_cast<size_t>(d->max_seqs) * d->num_kv_heads;
   if (cudaMalloc(&p->status, 16) != cudaSuccess ||
       cudaMalloc(&p->tickets, p->n_tickets * sizeof(int32_t)) != cudaSuccess ||
-      cudaMalloc(&p->sched, 16) != cudaSuccess || cudaMemset(p->status, 0, 16) != cudaSuccess ||
-      cudaMemset(p->tickets, 0, p->n_tickets * sizeof(int32_t)) != cudaSuccess ||
-      cudaMemset(p->sched, 0, 16) != cudaSuccess) {
+      cudaMemset(p->status, 0, 16) != cudaSuccess ||
+      cudaMemset(p->tickets, 0, p->n_tickets * sizeof(int32_t)) != cudaSuccess) {
     cudaFree(p->status);
     cudaFree(p->tickets);
-    cudaFree(p->sched);
     delete p;
     return fail(KVS_ERR_CUDA, "pool_create: cannot allocate the status word / counters");
   }
@@ -223,7 +221,6 @@ kvs_status kvs_pool_destroy(kvs_pool* p) {
   if (!p) return fail(KVS_ERR_INVALID_ARG, "pool_destroy: null pool");
   cudaFree(p->status);
   cudaFree(p->tickets);
-  cudaFree(p->sched);
   delete p;
   return KVS_OK;
 }

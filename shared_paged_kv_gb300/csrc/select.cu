@@ -56,32 +56,6 @@ __device__ __forceinline__ int count_for(float ratio, int n) {
   return static_cast<int>(k);
 }
 
-__device__ __forceinline__ int block_exclusive_scan(int x, int* warp_sums, int& total) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  int incl = x;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int y = __shfl_up_sync(0xffffffffu, incl, o);
-    if (lane >= o) incl += y;
-  }
-  if (lane == 31) warp_sums[warp] = incl;
-  __syncthreads();
-  if (warp == 0) {
-    int w = lane < (int)(blockDim.x >> 5) ? warp_sums[lane] : 0;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int y = __shfl_up_sync(0xffffffffu, w, o);
-      if (lane >= o) w += y;
-    }
-    warp_sums[lane] = w;
-  }
-  __syncthreads();
-  const int res = incl - x + (warp ? warp_sums[warp - 1] : 0);
-  total = warp_sums[(blockDim.x >> 5) - 1];
-  __syncthreads();
-  return res;
-}
-
 __global__ void __launch_bounds__(1024) sel_topk(const float* __restrict__ scores, const int64_t* __restrict__ row_off,
                                                  int n_agents, float ratio, long long cap_rows,
                                                  int32_t* __restrict__ idx_out, int64_t* __restrict__ idx_off) {

@@ -63,6 +63,15 @@ def test_long_context_many_splits_separate_merge():
     run_case(w)
 
 
+def test_many_sequences_multi_cta_plan():
+    # 1,400 sequences in 700 groups of two over a 3-block common prefix: the
+    # plan walks its groups with a grid-stride loop and compacts the item list
+    # from many CTAs; some sequences hold only shared blocks
+    rng = np.random.default_rng(5)
+    w = W.make_prefix_shared("many", 1400, 8, 2, 64, 1, 48, rng.integers(0, 80, size=1400), seed=23)
+    run_case(w)
+
+
 def test_gqa_group16_d64():
     run_case(W.make_gqa_fanout(n_seq=3, prefix_tokens=100, priv_lo=1, priv_hi=200, hq=32, hkv=2, d=64))
 
