@@ -260,7 +260,7 @@ def main():
         # plan for all layers, then attention on every layer
         K.kvs_fingerprint_dedup(pool, tokens, seq_off, N, None, None, None, fp, table, w.max_blocks, refc,
                                 nphys, ws_d)
-        K.kvs_decode_plan(pool, w.n_q_heads, table, w.max_blocks, seq_len, N, None, None, ws_a)
+        K.kvs_decode_plan(pool, w.n_q_heads, table, w.max_blocks, seq_len, N, None, None, None, ws_a)
         for l in range(L):
             if i is not None:
                 ev_a[i][l].record(stream)
@@ -324,7 +324,7 @@ def main():
             d_q.copy_(h_q, non_blocking=True)
             K.kvs_fingerprint_dedup(pool, d_tok, d_off, N, None, None, None, fp, table, w.max_blocks, refc,
                                     nphys, ws_d)
-            K.kvs_decode_plan(pool, w.n_q_heads, table, w.max_blocks, seq_len, N, None, None, ws_a)
+            K.kvs_decode_plan(pool, w.n_q_heads, table, w.max_blocks, seq_len, N, None, None, None, ws_a)
             for l in range(L):
                 K.kvs_decode_attn_planned(pool, l, d_q[l], w.n_q_heads, table, w.max_blocks, seq_len, N, None,
                                           None, None, w.theta, w.scale, out[l], ws_a)
@@ -476,7 +476,7 @@ def bench_tiny_replicated(torch, K, W, dev, reps, flush, n_inst=4096):
                      dtype=torch.uint8, device=dev)
 
     def run():
-        K.kvs_decode_plan(pool, w.n_q_heads, table_r, w.max_blocks, seq_len, NS, diff_r, None, ws)
+        K.kvs_decode_plan(pool, w.n_q_heads, table_r, w.max_blocks, seq_len, NS, diff_r, None, None, ws)
         K.kvs_decode_attn_planned(pool, 0, q, w.n_q_heads, table_r, w.max_blocks, seq_len, NS, diff_r, None,
                                   None, w.theta, w.scale, out, ws)
 
@@ -565,7 +565,7 @@ def bench_workload(args, torch, K, W):
     def step(i=None):
         if not q4:
             K.kvs_fingerprint_dedup(pool, tokens, seq_off, N, tier, so, sb, fp, table, w.max_blocks, refc, nphys, ws_d)
-            K.kvs_decode_plan(pool, w.n_q_heads, table, w.max_blocks, seq_len, N, dt, ro, ws_a)
+            K.kvs_decode_plan(pool, w.n_q_heads, table, w.max_blocks, seq_len, N, dt, ro, rs, ws_a)
         for l in range(L):
             if i is not None:
                 ev_a[i * L + l].record(stream)

@@ -222,7 +222,8 @@ kvs_status kvs_select_critical_noalloc(const void* k_cached_dev, const void* k_n
  * diff_table_dev  int32 [n_seq][max_blocks] diff block id or -1; or NULL.
  * rope_off_dev / rope_segs_dev  optional CSR: int32 [n_seq+1] offsets into
  *               kvs_seg_rope entries {first_block, n_blocks, delta}; blocks
- *               outside every entry are not rotated; |delta| < 2^18.
+ *               outside every entry are not rotated; where entries overlap,
+ *               the last one covering a block applies; |delta| < 2^18.
  * out_dev       float32 [n_seq][n_q_heads][head_dim]; an empty context
  *               (seq_len 0) yields zeros.
  * ws            kvs_workspace_size(KVS_OP_DECODE_ATTN) bytes of device memory.
@@ -243,17 +244,21 @@ kvs_status kvs_decode_attn(kvs_pool* pool, int32_t layer, const void* q_dev, int
  * kvs_workspace_size(KVS_OP_DECODE_ATTN)): for query groups G <= 8 it records,
  * for groups of R = 8/G sequences (R = 1 when rope_off is given), which
  * logical blocks every member that reaches them holds in the same physical
- * block, and lists the work items.  kvs_decode_attn_planned then runs one
- * layer with arguments that must match the plan's call (same tables, seq_len,
- * n_seq, max_blocks, n_q_heads, diff table presence and rope_off presence);
- * a mismatch in shapes is detected on the device (KVS_DEVERR_PLAN, no output
- * written), a change of table contents without a new plan is not.
+ * block, the RoPE shift of every logical block (when rope_off is given: the
+ * last rope_segs entry covering the block; |delta| >= 2^18 sets
+ * KVS_DEVERR_ROPE_RANGE and that block is not rotated), and lists the work
+ * items.  kvs_decode_attn_planned then runs one layer with arguments that
+ * must match the plan's call (same tables, seq_len, n_seq, max_blocks,
+ * n_q_heads, diff table and RoPE segments); a mismatch in shapes is detected
+ * on the device (KVS_DEVERR_PLAN, no output written), a change of table or
+ * segment contents without a new plan is not.
  * kvs_decode_attn is kvs_decode_plan followed by kvs_decode_attn_planned.
  * Groups of more than 8 query heads need no plan (the calls accept them). */
 kvs_status kvs_decode_plan(kvs_pool* pool, int32_t n_q_heads, const int32_t* block_table_dev,
                            int32_t max_blocks, const int32_t* seq_len_dev, int32_t n_seq,
                            const int32_t* diff_table_dev, const int32_t* rope_off_dev,
-                           void* ws, size_t ws_bytes, cudaStream_t stream);
+                           const kvs_seg_rope* rope_segs_dev, void* ws, size_t ws_bytes,
+                           cudaStream_t stream);
 kvs_status kvs_decode_attn_planned(kvs_pool* pool, int32_t layer, const void* q_dev, int32_t n_q_heads,
                                    const int32_t* block_table_dev, int32_t max_blocks,
                                    const int32_t* seq_len_dev, int32_t n_seq,

@@ -441,7 +441,7 @@ static kvs_status attn_check(kvs_pool* pool, int32_t layer, const void* q_dev, i
   if (n_q_heads < 1 || n_q_heads % d.num_kv_heads) return fail(KVS_ERR_INVALID_ARG, "decode_attn: n_q_heads must be a multiple of num_kv_heads");
   if (n_q_heads / d.num_kv_heads > 16) return fail(KVS_ERR_UNSUPPORTED, "decode_attn: more than 16 query heads per KV head");
   if (diff_table_dev && d.diff_capacity_blocks == 0) return fail(KVS_ERR_INVALID_ARG, "decode_attn: diff table given but the pool has no diff slabs");
-  if (need_q && (rope_off_dev == nullptr) != (rope_segs_dev == nullptr)) return fail(KVS_ERR_INVALID_ARG, "decode_attn: rope_off and rope_segs go together");
+  if ((rope_off_dev == nullptr) != (rope_segs_dev == nullptr)) return fail(KVS_ERR_INVALID_ARG, "decode_attn: rope_off and rope_segs go together");
   if (need_q && rope_off_dev && !(theta > 0.f)) return fail(KVS_ERR_INVALID_ARG, "decode_attn: theta must be positive");
   size_t need = 0;
   kvs_workspace_size(pool, KVS_OP_DECODE_ATTN, n_seq, max_blocks, n_q_heads, &need);
@@ -451,14 +451,15 @@ static kvs_status attn_check(kvs_pool* pool, int32_t layer, const void* q_dev, i
 
 extern "C" kvs_status kvs_decode_plan(kvs_pool* pool, int32_t n_q_heads, const int32_t* block_table_dev,
                                       int32_t max_blocks, const int32_t* seq_len_dev, int32_t n_seq,
-                                      const int32_t* diff_table_dev, const int32_t* rope_off_dev, void* ws,
-                                      size_t ws_bytes, cudaStream_t stream) {
+                                      const int32_t* diff_table_dev, const int32_t* rope_off_dev,
+                                      const kvs_seg_rope* rope_segs_dev, void* ws, size_t ws_bytes,
+                                      cudaStream_t stream) {
   kvs_status st = attn_check(pool, 0, nullptr, n_q_heads, block_table_dev, max_blocks, seq_len_dev, n_seq,
-                             diff_table_dev, rope_off_dev, nullptr, 1.f, nullptr, ws, ws_bytes, false);
+                             diff_table_dev, rope_off_dev, rope_segs_dev, 1.f, nullptr, ws, ws_bytes, false);
   if (st != KVS_OK || n_seq == 0) return st;
   if (n_q_heads / pool->desc.num_kv_heads > kTmMaxGroup) return KVS_OK;   // the 16-row kernel needs no plan
   return decode_plan_token_major(pool, n_q_heads, block_table_dev, max_blocks, seq_len_dev, n_seq, diff_table_dev,
-                                 rope_off_dev != nullptr, ws, stream);
+                                 rope_off_dev, rope_segs_dev, ws, stream);
 }
 
 static kvs_status attn_launch(kvs_pool* pool, int32_t layer, const void* q_dev, int32_t n_q_heads,
@@ -536,7 +537,7 @@ extern "C" kvs_status kvs_decode_attn(kvs_pool* pool, int32_t layer, const void*
                              diff_table_dev, rope_off_dev, rope_segs_dev, theta, out_dev, ws, ws_bytes, true);
   if (st != KVS_OK || n_seq == 0) return st;
   st = kvs_decode_plan(pool, n_q_heads, block_table_dev, max_blocks, seq_len_dev, n_seq, diff_table_dev,
-                       rope_off_dev, ws, ws_bytes, stream);
+                       rope_off_dev, rope_segs_dev, ws, ws_bytes, stream);
   if (st != KVS_OK) return st;
   return attn_launch(pool, layer, q_dev, n_q_heads, block_table_dev, max_blocks, seq_len_dev, n_seq, diff_table_dev,
                      rope_off_dev, rope_segs_dev, theta, scale, out_dev, ws, stream);

@@ -76,7 +76,7 @@ __host__ __device__ constexpr int tm_smem_bytes() {
 struct TmLayout {
   int R, ib, n_chunks, n_groups;
   size_t max_items;
-  size_t off_hdr, off_items, off_gmask, off_gphys, off_pne, off_spm, off_p1, off_p2, total;
+  size_t off_hdr, off_items, off_gmask, off_gphys, off_bdelta, off_pne, off_spm, off_p1, off_p2, total;
 };
 
 static size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
@@ -110,6 +110,7 @@ static TmLayout tm_layout(const kvs_pool* pool, int n_seq, int max_blocks, int g
   L.off_items = o; o = align256(o + L.max_items * sizeof(int4));
   L.off_gmask = o; o = align256(o + grp * max_blocks);
   L.off_gphys = o; o = align256(o + grp * max_blocks * sizeof(int32_t));
+  L.off_bdelta = o; o = align256(o + (rope ? (size_t)n_seq * max_blocks * sizeof(int32_t) : 0));
   L.off_pne = o; o = align256(o + (size_t)n_seq * L.n_chunks);
   L.off_spm = o; o = align256(o + grp * L.n_chunks);
   L.off_p1 = o; o = align256(o + split_bytes);
@@ -136,6 +137,10 @@ struct PlanParams {
   int32_t* gphys;   // [n_groups][max_blocks] that shared physical block, or -1 (R > 1)
   uint8_t* pne;     // [n_seq][n_chunks] private chunk has unshared work
   uint8_t* spm;     // [n_groups][n_chunks] members taking part in the shared chunk (R > 1)
+  const int32_t* rope_off;   // rotation calls: segment CSR
+  const int4* rope_segs;
+  int32_t* bdelta;  // [n_seq][max_blocks] RoPE shift of each logical block (rotation calls)
+  uint32_t* status;
   float* p1_ml;     // (m, l) of the private splits [n_seq][hkv][n_chunks][g]
   float* p2_ml;     // (m, l) of the shared splits, same shape (R > 1)
   int n_seq, max_blocks, R, G, ib, n_chunks, n_groups, capacity, hkv;
@@ -156,7 +161,9 @@ __device__ __forceinline__ int plan_seq_blocks(const int32_t* seq_len, int a, in
 //  * pne / spm: which private chunks have unshared work, which members take
 //    part in each shared chunk;
 //  * the (m, l) of every split that will not be written is set to (-inf, 0),
-//    so the merge can read all of them without consulting pne / spm first.
+//    so the merge can read all of them without consulting pne / spm first;
+//  * rotation calls: bdelta, the shift of the segment covering each logical
+//    block (the last entry covering it; 0 outside every entry).
 __global__ void __launch_bounds__(256) tm_plan_groups(PlanParams pp) {
   const int tid = threadIdx.x, nt = blockDim.x;
   if (blockIdx.x == 0 && tid == 0) {
@@ -195,6 +202,21 @@ __global__ void __launch_bounds__(256) tm_plan_groups(PlanParams pp) {
         pp.gphys[(size_t)gi * pp.max_blocks + b] = sh ? phys : -1;
       }
       __syncthreads();
+    }
+    if (pp.rope_off) {   // R == 1: the group is sequence a0
+      const int e0 = pp.rope_off[a0], e1 = pp.rope_off[a0 + 1];
+      for (int b = tid; b < pp.max_blocks; b += nt) {
+        int dl = 0;
+        for (int e = e0; e < e1; ++e) {
+          const int4 sg = __ldg(pp.rope_segs + e);
+          if (b >= sg.x && b - sg.x < sg.y) dl = sg.z;
+        }
+        if (dl <= -(1 << 18) || dl >= (1 << 18)) {
+          set_err(pp.status, KVS_DEVERR_ROPE_RANGE);
+          dl = 0;
+        }
+        pp.bdelta[(size_t)a0 * pp.max_blocks + b] = dl;
+      }
     }
     // 2. chunk occupancy
     for (int i = tid; i < nm * pp.n_chunks; i += nt) {
@@ -275,8 +297,7 @@ struct TmParams {
   const int32_t* block_table;
   const int32_t* seq_len;
   const int32_t* diff_table;
-  const int32_t* rope_off;
-  const int4* rope_segs;
+  const int32_t* bdelta;   // RoPE shift per logical block (rotation calls)
   float* out;
   float* p1;          // private splits [n_seq][hkv][n_chunks][g][D]
   float* p1_ml;       // [n_seq][hkv][n_chunks][g][2]
@@ -299,9 +320,8 @@ struct TmRec {
   int x;                   // kind (bit 30) | group or sequence
   int chunk;
   int cact;                // members whose columns take part
-  int seg_beg, seg_end;    // the sequence's RoPE segment range (rotation calls)
   int len[kTmMaxGroup];    // context lengths: of each member (shared), of the sequence in len[0] (private)
-  int pad[2];
+  int pad[4];
 };
 
 __device__ __forceinline__ uint32_t movm_t(uint32_t x) {
@@ -330,6 +350,7 @@ attn_tm_kernel(const __grid_constant__ TmParams p, const __grid_constant__ CUten
   // bit 29: the block id was out of range and nothing was loaded
   __shared__ int st_block[kTmWarps][S];
   __shared__ int st_mask[kTmWarps][S];   // group members whose columns take this block
+  __shared__ int st_delta[kTmWarps][ROPE ? S : 1];   // RoPE shift of the block (rotation calls)
   __shared__ TmRec recs[kTmWarps][kTmRec];
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -361,13 +382,13 @@ attn_tm_kernel(const __grid_constant__ TmParams p, const __grid_constant__ CUten
   const int T = gridDim.x * kTmWarps;
   int n_id = blockIdx.x * kTmWarps + warp;   // next claim
   int4 n_it = make_int4(0, 0, 0, 0), nn_it = n_it;
-  int n_tab = -1, n_aux = 0, n_dif = -1, n_len = 0, n_sg = 0;
+  int n_tab = -1, n_aux = 0, n_dif = -1, n_len = 0, n_dlt = 0;
   auto load_item = [&](int id) {
     return id < n_claims ? __ldg(p.items + id / p.hkv) : make_int4(0, 0, 0, 0);
   };
   // issue the loads for claim id (item entry it); nothing here consumes them
   auto prepare = [&](int id, const int4& it) {
-    n_tab = -1; n_aux = 0; n_dif = -1; n_len = 0; n_sg = 0;
+    n_tab = -1; n_aux = 0; n_dif = -1; n_len = 0; n_dlt = 0;
     if (id >= n_claims) return;
     const int kind = it.x >> 30, idx = it.x & ((1 << 30) - 1);
     const int b = it.y * p.ib + lane;
@@ -383,9 +404,9 @@ attn_tm_kernel(const __grid_constant__ TmParams p, const __grid_constant__ CUten
         n_tab = __ldg(p.block_table + (size_t)idx * p.max_blocks + b);
         if (R > 1) n_aux = __ldg(p.gmask + (size_t)(idx / R) * p.max_blocks + b);   // raw member bits
         if (DIFF) n_dif = __ldg(p.diff_table + (size_t)idx * p.max_blocks + b);
+        if (ROPE) n_dlt = __ldg(p.bdelta + (size_t)idx * p.max_blocks + b);
       }
       if (lane == 0) n_len = __ldg(p.seq_len + idx);
-      if (ROPE && lane < 2) n_sg = __ldg(p.rope_off + idx + lane);
     }
     // the query rows of the item's live columns, into L1 for the consumer
     constexpr int LPR = D * 2 / 128;   // 128-byte lines per query row
@@ -405,7 +426,7 @@ attn_tm_kernel(const __grid_constant__ TmParams p, const __grid_constant__ CUten
 
   int ord = -1;   // ordinal of the current claim
   int p_kind = 0, p_h = 0, p_b = 0, p_b0 = 0, p_bend = 0, p_mask = 0, p_slot = 0;
-  int tab_ent = -1, dif_ent = -1, aux_ent = 0;
+  int tab_ent = -1, dif_ent = -1, aux_ent = 0, dlt_ent = 0;
   bool p_done = false;
   auto claim = [&]() {
     if (n_id >= n_claims) {
@@ -423,6 +444,7 @@ attn_tm_kernel(const __grid_constant__ TmParams p, const __grid_constant__ CUten
     tab_ent = n_tab;
     aux_ent = n_aux;
     dif_ent = n_dif;
+    dlt_ent = n_dlt;
     TmRec& rec = recs[warp][ord & (kTmRec - 1)];
     if (lane == 0) {
       rec.id = n_id;
@@ -431,10 +453,6 @@ attn_tm_kernel(const __grid_constant__ TmParams p, const __grid_constant__ CUten
       rec.cact = it.w;
     }
     if (lane < kTmMaxGroup) rec.len[lane] = n_len;
-    if (ROPE) {
-      if (lane == 0) rec.seg_beg = n_sg;
-      if (lane == 1) rec.seg_end = n_sg;
-    }
     // advance: the next claim's entries, then the entry of the one after
     n_id += T;
     n_it = nn_it;
@@ -454,7 +472,7 @@ attn_tm_kernel(const __grid_constant__ TmParams p, const __grid_constant__ CUten
       pend_drow = -1;
       return;
     }
-    int phys = -1, did = -1, mask = 0, b = 0;
+    int phys = -1, did = -1, mask = 0, b = 0, dlt = 0;
     while (true) {
       if (!p_done && p_b >= p_bend) claim();
       if (p_done) break;
@@ -466,6 +484,7 @@ attn_tm_kernel(const __grid_constant__ TmParams p, const __grid_constant__ CUten
         if ((aux >> p_slot) & 1) continue;   // computed by the group's shared item
         mask = p_mask;
         if (DIFF) did = __shfl_sync(0xffffffffu, dif_ent, j);
+        if (ROPE) dlt = __shfl_sync(0xffffffffu, dlt_ent, j);
       } else {
         if (aux == 0) continue;              // not shared at this block
         mask = aux;
@@ -486,6 +505,7 @@ attn_tm_kernel(const __grid_constant__ TmParams p, const __grid_constant__ CUten
     if (lane != 0) return;
     st_ord[warp][s] = ord;
     st_mask[warp][s] = mask;
+    if (ROPE) st_delta[warp][s] = dlt;
     if (!valid) {
       set_err(p.status, KVS_DEVERR_BLOCK_ID);
       st_block[warp][s] = b | (1 << 29);   // nothing loaded: skip this block
@@ -523,7 +543,7 @@ attn_tm_kernel(const __grid_constant__ TmParams p, const __grid_constant__ CUten
   uint32_t qb[KS][2];
   uint32_t qlo[ROPE ? KS : 1][2];
   bool q_has_lo = false;
-  int cur_delta = 0, seg_lo = 0, seg_hi = 0, seg_beg = 0, seg_end = 0;
+  int cur_delta = 0;
   const uint16_t* qrow = nullptr;
   bool qok = false;
 
@@ -536,16 +556,31 @@ attn_tm_kernel(const __grid_constant__ TmParams p, const __grid_constant__ CUten
       qb[kk][1] = qok ? __ldg(reinterpret_cast<const uint32_t*>(qrow + col + 8)) : 0u;
     }
   };
-  auto rotate_q = [&](int delta) {   // q' = R(-delta) q, as bf16 hi + lo
+  // q' = R(-delta) q, as bf16 hi + lo.  Lane (g, c) holds head dims
+  // kk*16 + 2c + half*8 + {0, 1} (and the same + D/2), so the angles it needs
+  // depend on c only: the 8 lanes sharing c each compute 2*KS/8 of them and
+  // exchange the rest by shuffles.
+  auto rotate_q = [&](int delta) {
     q_has_lo = true;
+    constexpr int PER = (2 * KS) / 8;   // angles computed per lane
+    float cs_own[PER], sn_own[PER];
+#pragma unroll
+    for (int u = 0; u < PER; ++u) {
+      const int idx = g * PER + u;      // idx = (kk * 2 + half) * 2 + e
+      const int e = idx & 1, half = (idx >> 1) & 1, kk = idx >> 2;
+      rope_cos_sin(p.rs, kk * 16 + 2 * c + half * 8 + e, delta, cs_own[u], sn_own[u]);
+    }
 #pragma unroll
     for (int kk = 0; kk < KS / 2; ++kk) {
 #pragma unroll
       for (int half = 0; half < 2; ++half) {
         const int col = kk * 16 + 2 * c + half * 8;
-        float cs0, sn0, cs1, sn1;
-        rope_cos_sin(p.rs, col, delta, cs0, sn0);
-        rope_cos_sin(p.rs, col + 1, delta, cs1, sn1);
+        const int i0 = (kk * 2 + half) * 2, i1 = i0 + 1;
+        const int src0 = ((i0 / PER) << 2) | c, src1 = ((i1 / PER) << 2) | c;
+        const float cs0 = __shfl_sync(0xffffffffu, cs_own[i0 % PER], src0);
+        const float sn0 = __shfl_sync(0xffffffffu, sn_own[i0 % PER], src0);
+        const float cs1 = __shfl_sync(0xffffffffu, cs_own[i1 % PER], src1);
+        const float sn1 = __shfl_sync(0xffffffffu, sn_own[i1 % PER], src1);
         const uint32_t lo = qok ? __ldg(reinterpret_cast<const uint32_t*>(qrow + col)) : 0u;
         const uint32_t hi = qok ? __ldg(reinterpret_cast<const uint32_t*>(qrow + col + D / 2)) : 0u;
         const float l0 = bf16_lo(lo), l1 = bf16_hi(lo), h0 = bf16_lo(hi), h1 = bf16_hi(hi);
@@ -628,45 +663,10 @@ attn_tm_kernel(const __grid_constant__ TmParams p, const __grid_constant__ CUten
       for (int mt = 0; mt < D / 16; ++mt) acc[mt][0] = acc[mt][1] = acc[mt][2] = acc[mt][3] = 0.f;
       load_q();
       cur_delta = 0;
-      seg_lo = seg_hi = 0;
-      if (ROPE) {
-        seg_beg = rec.seg_beg;
-        seg_end = rec.seg_end;
-      }
     }
     if (loaded) {
-      if (ROPE && (b < seg_lo || b >= seg_hi)) {
-        // find the segment covering b; if none, the gap around b (delta 0)
-        // is cached instead, so unrotated stretches are not rescanned
-        int found = 0x7fffffff, fd = 0, flo = 0, fhi = 0, gap_lo = 0, gap_hi = 0x7fffffff;
-        for (int e = seg_beg + lane; e < seg_end; e += 32) {
-          const int4 sg = __ldg(p.rope_segs + e);
-          if (b >= sg.x && b < sg.x + sg.y && e < found) {
-            found = e; fd = sg.z; flo = sg.x; fhi = sg.x + sg.y;
-          }
-          if (sg.x > b) gap_hi = min(gap_hi, sg.x);
-          if (sg.x + sg.y <= b) gap_lo = max(gap_lo, sg.x + sg.y);
-        }
-#pragma unroll
-        for (int o = 16; o; o >>= 1) {
-          const int f2 = __shfl_xor_sync(0xffffffffu, found, o);
-          const int d2 = __shfl_xor_sync(0xffffffffu, fd, o);
-          const int lo2 = __shfl_xor_sync(0xffffffffu, flo, o);
-          const int hi2 = __shfl_xor_sync(0xffffffffu, fhi, o);
-          if (f2 < found) { found = f2; fd = d2; flo = lo2; fhi = hi2; }
-          gap_hi = min(gap_hi, __shfl_xor_sync(0xffffffffu, gap_hi, o));
-          gap_lo = max(gap_lo, __shfl_xor_sync(0xffffffffu, gap_lo, o));
-        }
-        int nd = 0;
-        if (found != 0x7fffffff) {
-          nd = fd; seg_lo = flo; seg_hi = fhi;
-        } else {
-          seg_lo = gap_lo; seg_hi = gap_hi;
-        }
-        if (nd <= -(1 << 18) || nd >= (1 << 18)) {
-          if (lane == 0) set_err(p.status, KVS_DEVERR_ROPE_RANGE);
-          nd = 0;
-        }
+      if (ROPE) {
+        const int nd = st_delta[warp][s];   // the plan checked |nd| < 2^18
         if (nd != cur_delta) {
           if (nd == 0) load_q(); else rotate_q(nd);
           cur_delta = nd;
@@ -692,13 +692,15 @@ attn_tm_kernel(const __grid_constant__ TmParams p, const __grid_constant__ CUten
 #pragma unroll
       for (int e = 0; e < 4; ++e) sc[e] += sd[e];
       // sc: (t=g, col 2c), (g, 2c+1), (g+8, 2c), (g+8, 2c+1); a column is live
-      // if its member takes this block and the token is inside its context
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int t = g + ((e >> 1) << 3);
-        const int cc = e & 1;
-        const bool live = colslot[cc] != 31 && ((emask >> colslot[cc]) & 1) && b * B + t < colL[cc];
-        sc[e] = live ? sc[e] * p.scale_log2 : -INFINITY;
+      // if its member takes this block (slot 31 never does: emask < 2^8) and
+      // the token is inside its context
+      {
+        const int lim0 = ((emask >> colslot[0]) & 1) ? colL[0] - b * B : 0;
+        const int lim1 = ((emask >> colslot[1]) & 1) ? colL[1] - b * B : 0;
+        sc[0] = g < lim0 ? sc[0] * p.scale_log2 : -INFINITY;
+        sc[1] = g < lim1 ? sc[1] * p.scale_log2 : -INFINITY;
+        sc[2] = g + 8 < lim0 ? sc[2] * p.scale_log2 : -INFINITY;
+        sc[3] = g + 8 < lim1 ? sc[3] * p.scale_log2 : -INFINITY;
       }
       float mx0 = fmaxf(sc[0], sc[2]), mx1 = fmaxf(sc[1], sc[3]);
 #pragma unroll
@@ -707,21 +709,25 @@ attn_tm_kernel(const __grid_constant__ TmParams p, const __grid_constant__ CUten
         mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
       }
       const float mn0 = fmaxf(m[0], mx0), mn1 = fmaxf(m[1], mx1);
-      // a column with nothing live yet keeps (m, l, acc) = (-inf, 0, 0)
-      const float al0 = mn0 == -INFINITY ? 1.f : fast_exp2(m[0] - mn0);
-      const float al1 = mn1 == -INFINITY ? 1.f : fast_exp2(m[1] - mn1);
+      // a column with nothing live yet keeps (m, l, acc) = (-inf, 0, 0): its
+      // reference point is taken as 0 so that exp2(-inf - 0) = 0
+      const float r0 = mn0 == -INFINITY ? 0.f : mn0, r1 = mn1 == -INFINITY ? 0.f : mn1;
+      const float al0 = fast_exp2(m[0] - r0), al1 = fast_exp2(m[1] - r1);
       m[0] = mn0;
       m[1] = mn1;
-      sc[0] = mn0 == -INFINITY ? 0.f : fast_exp2(sc[0] - mn0);
-      sc[1] = mn1 == -INFINITY ? 0.f : fast_exp2(sc[1] - mn1);
-      sc[2] = mn0 == -INFINITY ? 0.f : fast_exp2(sc[2] - mn0);
-      sc[3] = mn1 == -INFINITY ? 0.f : fast_exp2(sc[3] - mn1);
+      sc[0] = fast_exp2(sc[0] - r0);
+      sc[1] = fast_exp2(sc[1] - r1);
+      sc[2] = fast_exp2(sc[2] - r0);
+      sc[3] = fast_exp2(sc[3] - r1);
       l[0] = l[0] * al0 + sc[0] + sc[2];
       l[1] = l[1] * al1 + sc[1] + sc[3];
+      // rescale the accumulators only when some column's maximum moved
+      if (__any_sync(0xffffffffu, al0 != 1.f || al1 != 1.f)) {
 #pragma unroll
-      for (int mt = 0; mt < D / 16; ++mt) {
-        acc[mt][0] *= al0; acc[mt][1] *= al1;
-        acc[mt][2] *= al0; acc[mt][3] *= al1;
+        for (int mt = 0; mt < D / 16; ++mt) {
+          acc[mt][0] *= al0; acc[mt][1] *= al1;
+          acc[mt][2] *= al0; acc[mt][3] *= al1;
+        }
       }
       // P^T as the B operand (k = token, n = query column), bf16 hi + lo
       uint32_t h0, l0_, h1, l1_;
@@ -957,6 +963,7 @@ struct TmPtrs {
   int32_t* gphys;
   uint8_t* pne;
   uint8_t* spm;
+  int32_t* bdelta;
   float *p1, *p1_ml, *p2, *p2_ml;
 };
 
@@ -970,6 +977,7 @@ static TmPtrs tm_ptrs(const TmLayout& L, const kvs_pool* pool, int n_seq, int g,
   t.gphys = reinterpret_cast<int32_t*>(w + L.off_gphys);
   t.pne = w + L.off_pne;
   t.spm = w + L.off_spm;
+  t.bdelta = reinterpret_cast<int32_t*>(w + L.off_bdelta);
   t.p1 = reinterpret_cast<float*>(w + L.off_p1);
   t.p1_ml = t.p1 + split_vals;
   t.p2 = reinterpret_cast<float*>(w + L.off_p2);
@@ -978,8 +986,9 @@ static TmPtrs tm_ptrs(const TmLayout& L, const kvs_pool* pool, int n_seq, int g,
 }
 
 kvs_status decode_plan_token_major(kvs_pool* pool, int n_q_heads, const int32_t* table, int max_blocks,
-                                   const int32_t* seq_len, int n_seq, const int32_t* diff, bool rope, void* ws,
-                                   cudaStream_t stream) {
+                                   const int32_t* seq_len, int n_seq, const int32_t* diff, const int32_t* rope_off,
+                                   const kvs_seg_rope* rope_segs, void* ws, cudaStream_t stream) {
+  const bool rope = rope_off != nullptr;
   const int g = n_q_heads / pool->desc.num_kv_heads;
   const TmLayout L = tm_layout(pool, n_seq, max_blocks, g, rope);
   const TmPtrs t = tm_ptrs(L, pool, n_seq, g, ws);
@@ -993,6 +1002,10 @@ kvs_status decode_plan_token_major(kvs_pool* pool, int n_q_heads, const int32_t*
   pp.gphys = t.gphys;
   pp.pne = t.pne;
   pp.spm = t.spm;
+  pp.rope_off = rope_off;
+  pp.rope_segs = reinterpret_cast<const int4*>(rope_segs);
+  pp.bdelta = t.bdelta;
+  pp.status = pool->status;
   pp.p1_ml = t.p1_ml;
   pp.p2_ml = t.p2_ml;
   pp.n_seq = n_seq;
@@ -1030,8 +1043,7 @@ kvs_status decode_attn_token_major(kvs_pool* pool, int layer, const void* q, int
   prm.block_table = table;
   prm.seq_len = seq_len;
   prm.diff_table = diff;
-  prm.rope_off = rope_off;
-  prm.rope_segs = reinterpret_cast<const int4*>(rope_segs);
+  prm.bdelta = rope ? t.bdelta : nullptr;
   prm.out = out;
   prm.p1 = t.p1;
   prm.p1_ml = t.p1_ml;

@@ -61,8 +61,8 @@ kvs_status decode_attn_token_major(kvs_pool* pool, int layer, const void* q, int
                                    float scale, float* out, void* ws, cudaStream_t stream);
 size_t tm_workspace_bytes(const kvs_pool* pool, int n_seq, int max_blocks, int g);
 kvs_status decode_plan_token_major(kvs_pool* pool, int n_q_heads, const int32_t* table, int max_blocks,
-                                   const int32_t* seq_len, int n_seq, const int32_t* diff, bool rope, void* ws,
-                                   cudaStream_t stream);
+                                   const int32_t* seq_len, int n_seq, const int32_t* diff, const int32_t* rope_off,
+                                   const kvs_seg_rope* rope_segs, void* ws, cudaStream_t stream);
 constexpr int kTmMaxGroup = 8;
 
 }  // namespace kvs

@@ -86,7 +86,7 @@ def load(path: str = LIB_PATH):
         "kvs_select_critical_noalloc": [P, P, P, I32, I32, I32, F32, P, P, P],
         "kvs_decode_attn": [P, I32, P, I32, P, I32, P, I32, P, P, P, F32, F32, P, P, SZ, P],
         "kvs_decode_attn_planned": [P, I32, P, I32, P, I32, P, I32, P, P, P, F32, F32, P, P, SZ, P],
-        "kvs_decode_plan": [P, I32, P, I32, P, I32, P, P, P, SZ, P],
+        "kvs_decode_plan": [P, I32, P, I32, P, I32, P, P, P, P, SZ, P],
         "kvs_decode_attn_q4": [P, I32, P, I32, P, I32, P, I32, F32, P, P, SZ, P],
         "kvs_quantize_q4": [P, I32, P, P, P, I32, P],
         "kvs_workspace_size": [P, I32, I32, I32, I32, ctypes.POINTER(SZ)],
@@ -210,11 +210,11 @@ def kvs_decode_attn(pool: Pool, layer, q, n_q_heads, block_table, max_blocks, se
                                   _stream(stream)))
 
 
-def kvs_decode_plan(pool: Pool, n_q_heads, block_table, max_blocks, seq_len, n_seq, diff_table, rope_off, ws,
-                    stream=None):
+def kvs_decode_plan(pool: Pool, n_q_heads, block_table, max_blocks, seq_len, n_seq, diff_table, rope_off,
+                    rope_segs, ws, stream=None):
     _check(load().kvs_decode_plan(pool.handle, n_q_heads, _ptr(block_table), max_blocks, _ptr(seq_len), n_seq,
-                                  _ptr(diff_table), _ptr(rope_off), _ptr(ws), ws.numel() * ws.element_size(),
-                                  _stream(stream)))
+                                  _ptr(diff_table), _ptr(rope_off), _ptr(rope_segs), _ptr(ws),
+                                  ws.numel() * ws.element_size(), _stream(stream)))
 
 
 def kvs_decode_attn_planned(pool: Pool, layer, q, n_q_heads, block_table, max_blocks, seq_len, n_seq,

@@ -72,6 +72,16 @@ def test_many_sequences_multi_cta_plan():
     run_case(w)
 
 
+@pytest.mark.parametrize("hq,hkv,d", [(10, 2, 128), (12, 2, 64), (14, 2, 128), (16, 2, 64)])
+def test_wide_groups_two_column_tiles(hq, hkv, d):
+    # 5 to 8 query heads per kv head: two 8-column tiles per warp, so 3 or 2
+    # sequences share each tile over the common prefix (7 sequences: the last
+    # group is partial); ragged private tails with mirror diffs off
+    rng = np.random.default_rng(hq * 100 + d)
+    w = W.make_prefix_shared("wide", 7, hq, hkv, d, 1, 20 * 16 + 3, rng.integers(1, 300, size=7), seed=hq + d)
+    run_case(w)
+
+
 def test_gqa_group16_d64():
     run_case(W.make_gqa_fanout(n_seq=3, prefix_tokens=100, priv_lo=1, priv_hi=200, hq=32, hkv=2, d=64))
 
@@ -86,6 +96,21 @@ def test_allgather_small_rotation_and_diffs():
     w = W.make_allgather(n_seq=4, n_segs=6, priv_blocks_lo=3, priv_blocks_hi=9, hq=10, hkv=2, n_layers=1)
     run_case(w)
     run_case(w, rope=False)
+
+
+def test_overlapping_rope_segments_last_entry_wins():
+    # an extra entry for agent 0 covers the second half of its first shared
+    # segment with another shift; where entries overlap, the last entry
+    # covering a block applies (the oracle's rule and the plan's)
+    import dataclasses
+    w = W.make_allgather(n_seq=3, n_segs=4, priv_blocks_lo=2, priv_blocks_hi=5, hq=10, hkv=2, n_layers=1)
+    ro, rs = w.rope_off.copy(), w.rope_segs.copy()
+    fb, nb, dl, _ = rs[ro[0]]
+    extra = np.array([[fb + nb // 2, nb - nb // 2, dl + 37, 0]], dtype=rs.dtype)
+    rs2 = np.concatenate([rs[:ro[1]], extra, rs[ro[1]:]])
+    ro2 = ro.copy()
+    ro2[1:] += 1
+    run_case(dataclasses.replace(w, rope_off=ro2, rope_segs=rs2))
 
 
 def test_allgather_d64_rotation():
@@ -139,7 +164,7 @@ def test_plan_reused_across_layers_and_mismatch_flagged():
     pool = H.bf16_pool(w, n_layers=2)
     tb, sl = H.i32(ref["block_table"]), H.i32(w.seq_len)
     ws = H.workspace(K.kvs_workspace_size(pool, K.KVS_OP_DECODE_ATTN, w.n_seq, w.max_blocks, w.n_q_heads))
-    K.kvs_decode_plan(pool, w.n_q_heads, tb, w.max_blocks, sl, w.n_seq, None, None, ws)
+    K.kvs_decode_plan(pool, w.n_q_heads, tb, w.max_blocks, sl, w.n_seq, None, None, None, ws)
     for layer in range(2):
         q_bits = w.q_layer(layer)
         out = torch.full((w.n_seq, w.n_q_heads, w.head_dim), float("nan"), device=H.DEV)
