@@ -78,6 +78,11 @@ attn_bf16_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ C
   __shared__ uint64_t bars[kAttnWarps][S];
   __shared__ int s_last;
   __shared__ float sM[16], sL[16];
+  __shared__ float rsc[ROPE ? 4 * 64 : 1];   // RoPE frequency pieces (rotation calls)
+  if (ROPE) {
+    for (int i = threadIdx.x; i < 4 * 64; i += blockDim.x) rsc[i] = p.rs.c[i >> 6][i & 63];
+    __syncthreads();
+  }
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, c = lane & 3;
@@ -181,8 +186,8 @@ attn_bf16_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ C
       for (int half = 0; half < 2; ++half) {   // columns +0/+1 and +8/+9
         const int col = kk * 16 + 2 * c + half * 8;
         float cs0, sn0, cs1, sn1;
-        rope_cos_sin(p.rs, col, delta, cs0, sn0);
-        rope_cos_sin(p.rs, col + 1, delta, cs1, sn1);
+        rope_cos_sin(rsc, col, delta, cs0, sn0);
+        rope_cos_sin(rsc, col + 1, delta, cs1, sn1);
 #pragma unroll
         for (int row = 0; row < 2; ++row) {
           const bool ok = row ? r1ok : r0ok;

@@ -352,6 +352,7 @@ attn_tm_kernel(const __grid_constant__ TmParams p, const __grid_constant__ CUten
   __shared__ int st_mask[kTmWarps][S];   // group members whose columns take this block
   __shared__ int st_delta[kTmWarps][ROPE ? S : 1];   // RoPE shift of the block (rotation calls)
   __shared__ TmRec recs[kTmWarps][kTmRec];
+  __shared__ float rsc[ROPE ? 4 * 64 : 1];   // RoPE frequency pieces (rotation calls)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, c = lane & 3;
@@ -364,6 +365,10 @@ attn_tm_kernel(const __grid_constant__ TmParams p, const __grid_constant__ CUten
   if (lane == 0) {
     for (int s = 0; s < S; ++s) mbar_init(&bars[warp][s], 1);
     fence_barrier_init();
+  }
+  if (ROPE) {
+    for (int i = threadIdx.x; i < 4 * 64; i += blockDim.x) rsc[i] = p.rs.c[i >> 6][i & 63];
+    __syncthreads();
   }
   __syncwarp();
 
@@ -568,7 +573,7 @@ attn_tm_kernel(const __grid_constant__ TmParams p, const __grid_constant__ CUten
     for (int u = 0; u < PER; ++u) {
       const int idx = g * PER + u;      // idx = (kk * 2 + half) * 2 + e
       const int e = idx & 1, half = (idx >> 1) & 1, kk = idx >> 2;
-      rope_cos_sin(p.rs, kk * 16 + 2 * c + half * 8 + e, delta, cs_own[u], sn_own[u]);
+      rope_cos_sin(rsc, kk * 16 + 2 * c + half * 8 + e, delta, cs_own[u], sn_own[u]);
     }
 #pragma unroll
     for (int kk = 0; kk < KS / 2; ++kk) {

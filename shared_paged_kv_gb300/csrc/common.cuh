@@ -190,12 +190,14 @@ struct RopeSplit {
   float c[4][64];   // [piece][frequency index], up to head_dim 128
 };
 
-__device__ __forceinline__ void rope_cos_sin(const RopeSplit& rs, int i, int delta, float& cs, float& sn) {
+// c points at a copy of RopeSplit::c in shared memory (lanes index it with
+// different i; indexed loads from the kernel-parameter bank would serialise).
+__device__ __forceinline__ void rope_cos_sin(const float* c, int i, int delta, float& cs, float& sn) {
   const float d = static_cast<float>(delta);
-  float t0 = d * rs.c[0][i];
-  float t1 = d * rs.c[1][i];
-  float t2 = d * rs.c[2][i];
-  float turns = (t0 - floorf(t0)) + (t1 - floorf(t1)) + (t2 - floorf(t2)) + d * rs.c[3][i];
+  float t0 = d * c[i];
+  float t1 = d * c[64 + i];
+  float t2 = d * c[128 + i];
+  float turns = (t0 - floorf(t0)) + (t1 - floorf(t1)) + (t2 - floorf(t2)) + d * c[192 + i];
   turns -= rintf(turns);
   __sincosf(6.28318530717958647692f * turns, &sn, &cs);
 }
