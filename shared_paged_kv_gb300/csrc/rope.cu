@@ -3,11 +3,14 @@
 // only on p_t - p_s; V untouched; TokenDance summary section 2: one batched
 // RoPE call per layer for the whole group of requests).
 //
-// Rotate-half pairing (i, i + d/2), frequency theta^(-2i/d); the per-job
-// cos/sin table (d/2 entries) is built once per CTA in shared memory with the
-// Cody-Waite reduced evaluation of common.cuh.  One CTA = one job x 16 tokens;
-// threads stream 16-byte vectors of the low and high halves (coalesced
-// 128-byte runs per token-head), rotate in fp32, round to bf16 (RNE).
+// Rotate-half pairing (i, i + d/2), frequency theta^(-2i/d), angles by the
+// Cody-Waite reduced evaluation of common.cuh.  One CTA = one job x 64
+// tokens, eight warps.  A warp step covers TPW tokens of one KV head: lane
+// (token tl, vector v) holds head dims [8v, 8v+8) and [d/2 + 8v, d/2 + 8v+8)
+// of its token as two 16-byte vectors, so the 8 cos/sin pairs a lane needs
+// depend on v only and stay in registers for the whole job; each token's
+// low and high halves are 128-byte (d = 128) coalesced runs.  Rotation in
+// fp32, rounding to bf16 (RNE).
 #include "common.cuh"
 #include "internal.h"
 
@@ -23,11 +26,15 @@ struct RopeParams {
   RopeSplit rs;
 };
 
+constexpr int kRopeWarps = 8;
+constexpr int kRopeTokPerCta = 64;
+
 template <int D>
-__global__ void __launch_bounds__(128) rope_rerotate_kernel(const __grid_constant__ RopeParams p) {
+__global__ void __launch_bounds__(kRopeWarps * 32) rope_rerotate_kernel(const __grid_constant__ RopeParams p) {
   constexpr int VEC = 8;                 // bf16 per 16-byte vector
   constexpr int NV = D / 2 / VEC;        // vectors per half row
-  __shared__ float cs[D / 2], sn[D / 2];
+  constexpr int TPW = 32 / NV;           // tokens per warp step
+  __shared__ float rsc[4 * 64];          // RoPE frequency pieces (lanes index them differently)
   const int job = blockIdx.x;
   const int4 j0 = p.jobs[2 * job], j1 = p.jobs[2 * job + 1];
   const int n_tok = j1.x;
@@ -38,43 +45,48 @@ __global__ void __launch_bounds__(128) rope_rerotate_kernel(const __grid_constan
     if (threadIdx.x == 0) set_err(p.status, KVS_DEVERR_ROPE_RANGE);
     return;
   }
-  for (int i = threadIdx.x; i < D / 2; i += blockDim.x) rope_cos_sin(p.rs, i, delta, cs[i], sn[i]);
+  for (int i = threadIdx.x; i < 4 * 64; i += blockDim.x) rsc[i] = p.rs.c[i >> 6][i & 63];
   __syncthreads();
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int v = lane % NV, tl = lane / NV;
+  float cs[VEC], sn[VEC];
+#pragma unroll
+  for (int e = 0; e < VEC; ++e) rope_cos_sin(rsc, v * VEC + e, delta, cs[e], sn[e]);
   const int t1 = min(n_tok, t0 + p.tok_per_cta);
-  const int items = (t1 - t0) * p.hkv * NV;
-  for (int it = threadIdx.x; it < items; it += blockDim.x) {
-    const int v = it % NV;
-    const int rest = it / NV;
-    const int h = rest % p.hkv;
-    const int t = t0 + rest / p.hkv;
+  const int steps = (t1 - t0 + TPW - 1) / TPW;
+  const long long lim = (long long)p.max_blocks * p.B;
+  for (int u = warp; u < steps * p.hkv; u += kRopeWarps) {
+    const int st = u / p.hkv, h = u - st * p.hkv;
+    const int t = t0 + st * TPW + tl;
+    if (t >= t1) continue;
     const int ts = j0.y + t, td = j0.w + t;
-    if (ts < 0 || td < 0 || ts / p.B >= p.max_blocks || td / p.B >= p.max_blocks) {
+    if (ts < 0 || td < 0 || ts >= lim || td >= lim) {
       set_err(p.status, KVS_DEVERR_JOB);
       continue;
     }
-    const int ps = p.src_table[(size_t)j0.x * p.max_blocks + ts / p.B];
-    const int pd = p.dst_table[(size_t)j0.z * p.max_blocks + td / p.B];
+    const int bs = ts / p.B, bd = td / p.B;
+    const int ps = __ldg(p.src_table + (size_t)j0.x * p.max_blocks + bs);
+    const int pd = __ldg(p.dst_table + (size_t)j0.z * p.max_blocks + bd);
     if (ps < 0 || ps >= p.capacity || pd < 0 || pd >= p.capacity) {
       set_err(p.status, KVS_DEVERR_BLOCK_ID);
       continue;
     }
-    const size_t rs = (((size_t)ps * p.hkv + h) * p.B + ts % p.B) * D;
-    const size_t rd = (((size_t)pd * p.hkv + h) * p.B + td % p.B) * D;
-    const uint4 lo = __ldg(reinterpret_cast<const uint4*>(p.slab + rs + v * VEC));
-    const uint4 hi = __ldg(reinterpret_cast<const uint4*>(p.slab + rs + D / 2 + v * VEC));
+    const size_t rs = (((size_t)ps * p.hkv + h) * p.B + (ts - bs * p.B)) * D + v * VEC;
+    const size_t rd = (((size_t)pd * p.hkv + h) * p.B + (td - bd * p.B)) * D + v * VEC;
+    const uint4 lo = __ldg(reinterpret_cast<const uint4*>(p.slab + rs));
+    const uint4 hi = __ldg(reinterpret_cast<const uint4*>(p.slab + rs + D / 2));
     const uint32_t lw[4] = {lo.x, lo.y, lo.z, lo.w};
     const uint32_t hw[4] = {hi.x, hi.y, hi.z, hi.w};
     uint32_t ol[4], oh[4];
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
-      const int i0 = v * VEC + 2 * e;
       const float a0 = bf16_lo(lw[e]), a1 = bf16_hi(lw[e]);
       const float b0 = bf16_lo(hw[e]), b1 = bf16_hi(hw[e]);
-      ol[e] = pack_bf16(a0 * cs[i0] - b0 * sn[i0], a1 * cs[i0 + 1] - b1 * sn[i0 + 1]);
-      oh[e] = pack_bf16(b0 * cs[i0] + a0 * sn[i0], b1 * cs[i0 + 1] + a1 * sn[i0 + 1]);
+      ol[e] = pack_bf16(a0 * cs[2 * e] - b0 * sn[2 * e], a1 * cs[2 * e + 1] - b1 * sn[2 * e + 1]);
+      oh[e] = pack_bf16(b0 * cs[2 * e] + a0 * sn[2 * e], b1 * cs[2 * e + 1] + a1 * sn[2 * e + 1]);
     }
-    *reinterpret_cast<uint4*>(p.slab + rd + v * VEC) = make_uint4(ol[0], ol[1], ol[2], ol[3]);
-    *reinterpret_cast<uint4*>(p.slab + rd + D / 2 + v * VEC) = make_uint4(oh[0], oh[1], oh[2], oh[3]);
+    *reinterpret_cast<uint4*>(p.slab + rd) = make_uint4(ol[0], ol[1], ol[2], ol[3]);
+    *reinterpret_cast<uint4*>(p.slab + rd + D / 2) = make_uint4(oh[0], oh[1], oh[2], oh[3]);
   }
 }
 
@@ -105,14 +117,14 @@ extern "C" kvs_status kvs_rope_rerotate(kvs_pool* pool, int32_t layer, const kvs
   p.hkv = d.num_kv_heads;
   p.B = d.block_tokens;
   p.capacity = d.capacity_blocks;
-  p.tok_per_cta = 16;
+  p.tok_per_cta = kRopeTokPerCta;
   rope_split_host(theta, d.head_dim, p.rs.c);
   dim3 grid(n_jobs, (max_job_tokens + p.tok_per_cta - 1) / p.tok_per_cta);
   if (grid.y > 65535) return fail(KVS_ERR_CAPACITY, "rope_rerotate: max_job_tokens too large");
   if (d.head_dim == 128)
-    rope_rerotate_kernel<128><<<grid, 128, 0, stream>>>(p);
+    rope_rerotate_kernel<128><<<grid, kRopeWarps * 32, 0, stream>>>(p);
   else
-    rope_rerotate_kernel<64><<<grid, 128, 0, stream>>>(p);
+    rope_rerotate_kernel<64><<<grid, kRopeWarps * 32, 0, stream>>>(p);
   count_launch();
   return check_launch("rope_rerotate");
 }
