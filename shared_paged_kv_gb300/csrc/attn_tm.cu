@@ -345,12 +345,11 @@ attn_tm_kernel(const __grid_constant__ TmParams p, const __grid_constant__ CUten
   static_assert(kTmRec > S + 1, "claim records must outnumber the items a ring can hold");
   extern __shared__ uint8_t smem_raw[];
   __shared__ uint64_t bars[kTmWarps][S];
-  __shared__ int st_ord[kTmWarps][S];    // claim ordinal of the block in the stage; -1: no more work
-  // block index; bit 30: the next position holds the block's diff tiles;
-  // bit 29: the block id was out of range and nothing was loaded
-  __shared__ int st_block[kTmWarps][S];
-  __shared__ int st_mask[kTmWarps][S];   // group members whose columns take this block
-  __shared__ int st_delta[kTmWarps][ROPE ? S : 1];   // RoPE shift of the block (rotation calls)
+  // per stage {claim ordinal (-1: no more work), block index (bit 30: the
+  // next position holds the block's diff tiles; bit 29: the block id was out
+  // of range and nothing was loaded), group members whose columns take this
+  // block, RoPE shift of the block (rotation calls)}
+  __shared__ int4 st_rec[kTmWarps][S];
   __shared__ TmRec recs[kTmWarps][kTmRec];
   __shared__ float rsc[ROPE ? 4 * 64 : 1];   // RoPE frequency pieces (rotation calls)
 
@@ -499,7 +498,7 @@ attn_tm_kernel(const __grid_constant__ TmParams p, const __grid_constant__ CUten
     }
     if (p_done) {
       if (lane == 0) {
-        st_ord[warp][s] = -1;
+        st_rec[warp][s] = make_int4(-1, 0, 0, 0);
         mbar_arrive(bar);
       }
       return;
@@ -508,17 +507,14 @@ attn_tm_kernel(const __grid_constant__ TmParams p, const __grid_constant__ CUten
     const bool dval = DIFF && valid && did >= 0 && did < p.diff_capacity;
     if (dval) pend_drow = (did * p.hkv + p_h) * B;
     if (lane != 0) return;
-    st_ord[warp][s] = ord;
-    st_mask[warp][s] = mask;
-    if (ROPE) st_delta[warp][s] = dlt;
     if (!valid) {
       set_err(p.status, KVS_DEVERR_BLOCK_ID);
-      st_block[warp][s] = b | (1 << 29);   // nothing loaded: skip this block
+      st_rec[warp][s] = make_int4(ord, b | (1 << 29), mask, dlt);   // nothing loaded: skip this block
       mbar_arrive(bar);
       return;
     }
     if (DIFF && did >= p.diff_capacity) set_err(p.status, KVS_DEVERR_DIFF_ID);
-    st_block[warp][s] = dval ? (b | (1 << 30)) : b;
+    st_rec[warp][s] = make_int4(ord, dval ? (b | (1 << 30)) : b, mask, dlt);
     mbar_arrive_expect_tx(bar, 2 * TILE);
     const int row = (phys * p.hkv + p_h) * B;
     tma_load_kv_tile<D>(st, &tk, row, bar);
@@ -628,9 +624,8 @@ attn_tm_kernel(const __grid_constant__ TmParams p, const __grid_constant__ CUten
   for (int i = 0;;) {
     const int s = i % S;
     if (!mbar_wait_bounded(&bars[warp][s], (i / S) & 1, p.status)) break;
-    const int item = st_ord[warp][s];
-    const int bword = st_block[warp][s];
-    const int emask = st_mask[warp][s];
+    const int4 srec = st_rec[warp][s];
+    const int item = srec.x, bword = srec.y, emask = srec.z;
     if (item < 0) break;
     const bool has_diff = DIFF && (bword >> 30) != 0;
     const int b = bword & ((1 << 29) - 1);
@@ -671,7 +666,7 @@ attn_tm_kernel(const __grid_constant__ TmParams p, const __grid_constant__ CUten
     }
     if (loaded) {
       if (ROPE) {
-        const int nd = st_delta[warp][s];   // the plan checked |nd| < 2^18
+        const int nd = srec.w;   // the plan checked |nd| < 2^18
         if (nd != cur_delta) {
           if (nd == 0) load_q(); else rotate_q(nd);
           cur_delta = nd;

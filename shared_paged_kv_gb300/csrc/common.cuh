@@ -105,14 +105,13 @@ __device__ __forceinline__ uint32_t swz128(uint32_t o) { return o ^ (((o >> 7) &
 __device__ __forceinline__ uint32_t swz64(uint32_t o) { return o ^ (((o >> 7) & 3u) << 4); }
 
 // A bf16 KV tile of one 16-token block and one KV head, head_dim D, is loaded
-// as D/64 TMA boxes of 16 rows x 64 elements (128-byte rows, 128-byte
-// swizzle) stacked as [D/64][16][64].  Consecutive tokens are consecutive
-// 128-byte rows, so the swizzle spreads any 8 consecutive tokens over all
-// eight 16-byte bank groups (ldmatrix without conflicts).
+// by one 3-D TMA box as D/64 panels of 16 rows x 64 elements (128-byte rows,
+// 128-byte swizzle) stacked as [D/64][16][64].  Consecutive tokens are
+// consecutive 128-byte rows, so the swizzle spreads any 8 consecutive tokens
+// over all eight 16-byte bank groups (ldmatrix without conflicts).
 template <int D>
 __device__ __forceinline__ void tma_load_kv_tile(void* dst, const CUtensorMap* map, int row, uint64_t* bar) {
-#pragma unroll
-  for (int h = 0; h < D / 64; ++h) tma_load_2d(static_cast<uint8_t*>(dst) + h * 2048, map, h * 64, row, bar);
+  tma_load_3d(dst, map, 0, row, 0, bar);   // all D/64 halves of the tile in one copy
 }
 
 template <int D>

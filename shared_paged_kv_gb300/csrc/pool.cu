@@ -84,16 +84,20 @@ static PFN_cuTensorMapEncodeTiled_v12000 get_encoder() {
   return fn;
 }
 
-// bf16 slab [rows][head_dim] as a 2-D tensor; box {64 elements, block_tokens
-// rows} with 128-byte swizzle (a block tile is head_dim/64 such boxes).
+// bf16 slab [rows][head_dim] seen as a 3-D tensor {64 elements, rows,
+// head_dim/64 halves} (row stride head_dim*2 bytes, half stride 128 bytes), so
+// one box {64, block_tokens, head_dim/64} with 128-byte swizzle brings a whole
+// block tile in one copy, laid out in shared memory as [half][row][64]: each
+// half is a 16-row x 128-byte swizzled panel, which keeps ldmatrix free of
+// bank conflicts.
 static bool encode_bf16_slab(CUtensorMap* m, void* base, long long rows, int head_dim, int box_rows) {
   auto enc = get_encoder();
   if (!enc) return false;
-  cuuint64_t dims[2] = {static_cast<cuuint64_t>(head_dim), static_cast<cuuint64_t>(rows)};
-  cuuint64_t strides[1] = {static_cast<cuuint64_t>(head_dim) * 2};
-  cuuint32_t box[2] = {64, static_cast<cuuint32_t>(box_rows)};
-  cuuint32_t es[2] = {1, 1};
-  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims, strides, box, es,
+  cuuint64_t dims[3] = {64, static_cast<cuuint64_t>(rows), static_cast<cuuint64_t>(head_dim / 64)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(head_dim) * 2, 128};
+  cuuint32_t box[3] = {64, static_cast<cuuint32_t>(box_rows), static_cast<cuuint32_t>(head_dim / 64)};
+  cuuint32_t es[3] = {1, 1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, base, dims, strides, box, es,
                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
