@@ -83,11 +83,14 @@ static size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 // Work-item size (blocks): about KVS_TM_ITEMS_PER_WARP items per resident
 // warp, at least max_blocks / KVS_TM_MAX_SPLITS (bounding the splits of one
-// sequence per kind), at most 32 (one block-table entry per lane).
-int tm_item_blocks(const kvs_pool* pool, int n_seq, int max_blocks) {
+// sequence per kind), at most 32 (one block-table entry per lane).  The work
+// estimate counts every sequence's blocks; with groups (R > 1) the blocks a
+// group shares become one item for all members, so fewer items result and
+// the target is doubled.
+int tm_item_blocks(const kvs_pool* pool, int n_seq, int max_blocks, int R) {
   const long long work = (long long)n_seq * pool->desc.num_kv_heads * max_blocks;
   const long long warps = (long long)pool->num_sms * KVS_TM_MIN_CTAS * kTmWarps;
-  long long ib = work / (warps * KVS_TM_ITEMS_PER_WARP);
+  long long ib = work / (warps * KVS_TM_ITEMS_PER_WARP * (R > 1 ? 2 : 1));
   const long long min_ib = (max_blocks + KVS_TM_MAX_SPLITS - 1) / KVS_TM_MAX_SPLITS;
   if (ib < min_ib) ib = min_ib;
   int r = 4;
@@ -98,7 +101,7 @@ int tm_item_blocks(const kvs_pool* pool, int n_seq, int max_blocks) {
 static TmLayout tm_layout(const kvs_pool* pool, int n_seq, int max_blocks, int g, bool rope) {
   TmLayout L{};
   L.R = rope ? 1 : std::max(1, 8 / g);
-  L.ib = tm_item_blocks(pool, n_seq, max_blocks);
+  L.ib = tm_item_blocks(pool, n_seq, max_blocks, L.R);
   L.n_chunks = (max_blocks + L.ib - 1) / L.ib;
   L.n_groups = (n_seq + L.R - 1) / L.R;
   const size_t grp = L.R > 1 ? (size_t)L.n_groups : 0;   // group arrays exist only with grouping

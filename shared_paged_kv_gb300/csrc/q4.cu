@@ -116,6 +116,11 @@ __device__ __forceinline__ uint32_t movmatrix_t(uint32_t x) {
   return y;
 }
 
+// fp16x2 (1024 + nibble) from bits [0,4) and [16,20) of w, and
+// (1024 + 16 * nibble) from bits [4,8) and [20,24): one LOP3 each, exact
+__device__ __forceinline__ uint32_t nib_lo1024(uint32_t w) { return (w & 0x000F000Fu) | 0x64006400u; }
+__device__ __forceinline__ uint32_t nib_hi1024(uint32_t w) { return (w & 0x00F000F0u) | 0x64006400u; }
+
 // two nibbles (bits [0,4) and [16,20) after the shift) -> fp16x2 exact codes
 __device__ __forceinline__ uint32_t nib2h(uint32_t w) {
   const uint32_t m = (w & 0x000F000Fu) | 0x64006400u;
@@ -184,46 +189,49 @@ q4_attn_kernel(const __grid_constant__ Q4Params p, const __grid_constant__ CUten
   if (threadIdx.x == 0)
     for (int i = 0; i < kQ4Stages && i < n_mine; ++i) issue(i, i);
 
-  // ---- query as the B operand (k = head dim, n = query head), fp16, with the
-  // k-order permutation shared with the code loads; plus per-group sums.
+  // ---- query as the B operand (k = head dim, n = query head), fp16.  Each
+  // 32-bit code word w (elements 8w..8w+7 of this thread's 16 head dims of a
+  // group) feeds two MMAs: "lo" takes the low nibbles (elements 0,4 and 2,6,
+  // as 1024 + c) and "hi" the high nibbles (elements 1,5 and 3,7, as
+  // 1024 + 16c); the query is laid out in the same k order.  Per group and
+  // column: qs = sum of q, off = 1024 * sum(q over lo dims) + 64 * sum(q
+  // over hi dims), from the same fp16 values the MMAs use, so that
+  //   q . c = acc_lo + acc_hi / 16 - off   (exactly, up to fp32 accumulation).
   const int G_ = p.g;
   const uint16_t* qbase = p.q + ((size_t)a * p.hq + h * G_) * kQ4D;
-  uint32_t qb[2][4][2];
-  float qs[2][2];   // [group][column 2c / 2c+1]
+  uint32_t qlo[2][2][2], qhi[2][2][2];   // [group][word][k half]
+  float qs[2][2], qoff[2][2];            // [group][column 2c / 2c+1]
   {
     const bool ok = g < G_;
+    auto qv = [&](int d) { return ok ? __uint_as_float((uint32_t)qbase[g * kQ4D + d] << 16) : 0.f; };
 #pragma unroll
     for (int grp = 0; grp < 2; ++grp) {
+      float slo = 0.f, shi = 0.f;
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const int d0 = grp * 64 + 16 * c + 8 * (j >> 1) + 2 * (j & 1);
-        // pair A: nibbles (2sub, 2sub+4) -> d0, d0+4 ; pair B: d0+1, d0+5
-        float x0 = 0.f, x1 = 0.f, x2 = 0.f, x3 = 0.f;
-        if (ok) {
-          x0 = __uint_as_float((uint32_t)qbase[g * kQ4D + d0] << 16);
-          x1 = __uint_as_float((uint32_t)qbase[g * kQ4D + d0 + 4] << 16);
-          x2 = __uint_as_float((uint32_t)qbase[g * kQ4D + d0 + 1] << 16);
-          x3 = __uint_as_float((uint32_t)qbase[g * kQ4D + d0 + 5] << 16);
+      for (int w = 0; w < 2; ++w) {
+        const int base = grp * 64 + 16 * c + 8 * w;
+        qlo[grp][w][0] = pack_f16(qv(base + 0), qv(base + 4));
+        qlo[grp][w][1] = pack_f16(qv(base + 2), qv(base + 6));
+        qhi[grp][w][0] = pack_f16(qv(base + 1), qv(base + 5));
+        qhi[grp][w][1] = pack_f16(qv(base + 3), qv(base + 7));
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+          const float2 l2 = __half22float2(*reinterpret_cast<const __half2*>(&qlo[grp][w][k]));
+          const float2 h2 = __half22float2(*reinterpret_cast<const __half2*>(&qhi[grp][w][k]));
+          slo += l2.x + l2.y;
+          shi += h2.x + h2.y;
         }
-        qb[grp][j][0] = pack_f16(x0, x1);
-        qb[grp][j][1] = pack_f16(x2, x3);
       }
-    }
-    // per-group query sums: this lane's 16 values of row g per group, summed
-    // over the 4 lanes of the row, then fetched for columns 2c and 2c+1
-#pragma unroll
-    for (int grp = 0; grp < 2; ++grp) {
-      float sum = 0.f;
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const float2 a0 = __half22float2(*reinterpret_cast<const __half2*>(&qb[grp][j][0]));
-        const float2 a1 = __half22float2(*reinterpret_cast<const __half2*>(&qb[grp][j][1]));
-        sum += (a0.x + a0.y) + (a1.x + a1.y);
-      }
-      sum += __shfl_xor_sync(0xffffffffu, sum, 1);
-      sum += __shfl_xor_sync(0xffffffffu, sum, 2);
+      // sums over the 4 lanes of row g, then fetched for columns 2c and 2c+1
+      slo += __shfl_xor_sync(0xffffffffu, slo, 1);
+      slo += __shfl_xor_sync(0xffffffffu, slo, 2);
+      shi += __shfl_xor_sync(0xffffffffu, shi, 1);
+      shi += __shfl_xor_sync(0xffffffffu, shi, 2);
+      const float sum = slo + shi, off = 1024.f * slo + 64.f * shi;
       qs[grp][0] = __shfl_sync(0xffffffffu, sum, (2 * c) * 4);
       qs[grp][1] = __shfl_sync(0xffffffffu, sum, (2 * c + 1) * 4);
+      qoff[grp][0] = __shfl_sync(0xffffffffu, off, (2 * c) * 4);
+      qoff[grp][1] = __shfl_sync(0xffffffffu, off, (2 * c + 1) * 4);
     }
   }
 
@@ -253,20 +261,21 @@ q4_attn_kernel(const __grid_constant__ Q4Params p, const __grid_constant__ CUten
 #pragma unroll
       for (int mt = 0; mt < 4; ++mt) {
         const int t0 = tw + 16 * mt + g, t1 = t0 + 8;
-        float cg[2][4];
+        float cg[2][4];   // q . c per group, rows (t0, t1) x columns (2c, 2c+1)
 #pragma unroll
         for (int grp = 0; grp < 2; ++grp) {
-          cg[grp][0] = cg[grp][1] = cg[grp][2] = cg[grp][3] = 0.f;
+          float al_[4] = {0.f, 0.f, 0.f, 0.f}, ah_[4] = {0.f, 0.f, 0.f, 0.f};
           const uint2 w0 = *reinterpret_cast<const uint2*>(kc + swz64(t0 * 64 + 32 * grp + 8 * c));
           const uint2 w1 = *reinterpret_cast<const uint2*>(kc + swz64(t1 * 64 + 32 * grp + 8 * c));
 #pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const uint32_t r0 = (j >> 1) ? w0.y : w0.x;
-            const uint32_t r1 = (j >> 1) ? w1.y : w1.x;
-            const int sh = 8 * (j & 1);
-            mma_f16(cg[grp], nib2h(r0 >> sh), nib2h(r1 >> sh), nib2h(r0 >> (sh + 4)), nib2h(r1 >> (sh + 4)),
-                    qb[grp][j][0], qb[grp][j][1]);
+          for (int w = 0; w < 2; ++w) {
+            const uint32_t r0 = w ? w0.y : w0.x, r1 = w ? w1.y : w1.x;
+            const uint32_t s0 = r0 >> 8, s1 = r1 >> 8;
+            mma_f16(al_, nib_lo1024(r0), nib_lo1024(r1), nib_lo1024(s0), nib_lo1024(s1), qlo[grp][w][0], qlo[grp][w][1]);
+            mma_f16(ah_, nib_hi1024(r0), nib_hi1024(r1), nib_hi1024(s0), nib_hi1024(s1), qhi[grp][w][0], qhi[grp][w][1]);
           }
+#pragma unroll
+          for (int e = 0; e < 4; ++e) cg[grp][e] = fmaf(ah_[e], 0.0625f, al_[e]) - qoff[grp][e & 1];
         }
         const uint2 sb0 = *reinterpret_cast<const uint2*>(ksb + t0 * 8);
         const uint2 sb1 = *reinterpret_cast<const uint2*>(ksb + t1 * 8);
