@@ -284,11 +284,44 @@ kvs_status kvs_quantize_q4(kvs_pool* pool, int32_t layer, const void* k_src_dev,
                            const void* v_src_dev, const int32_t* dst_blocks_dev,
                            int32_t n_blocks, cudaStream_t stream);
 
+/* ---------------------------------------------------------------------------
+ * Mirror construction from refreshed critical positions ([TD] section 2: at
+ * the check layers only each request's critical positions of its cached K/V
+ * are refreshed; section 3, Fig. 7: one master cache, every other cache kept
+ * as block-sparse K/V differences from it; Fig. 8: a diff is applied before
+ * the RoPE positions are restored, so it lives in the master's frame).
+ * For agent a, idx_dev[idx_off_dev[a] .. idx_off_dev[a+1]) are logical token
+ * positions of its sequence, strictly ascending and < seq_len[a]; row r of
+ * k_new_dev / v_new_dev (bf16 [rows][num_kv_heads][head_dim]) holds the
+ * refreshed values of position idx_dev[r], K in the agent's frame.  The master
+ * value of position t is row t % block_tokens of physical block
+ * block_table[a][t / block_tokens] of `layer`.
+ * Writes diff_table_dev (int32 [n_seq][max_blocks]): -1 for a block with no
+ * refreshed position, else its diff block id; ids are consecutive from 0 in
+ * agent order, then logical-block order, and *n_diff_dev (device int32)
+ * receives their number.  Each dirty block's tiles in the pool's diff slabs of
+ * `layer` get, on a refreshed row, bf16(R(-delta) k_new - K_master) and
+ * bf16(v_new - V_master) (delta: the RoPE shift of the block's segment as in
+ * kvs_decode_attn, 0 without rope_off_dev), and zero on every other row.
+ * Those diff slabs then serve kvs_decode_attn as the agent's mirror diffs.
+ * Device-detected errors: a position out of order or out of range
+ * (KVS_DEVERR_JOB, the row is ignored), a block id out of range
+ * (KVS_DEVERR_BLOCK_ID, the block's tiles are zeroed), more dirty blocks than
+ * diff_capacity_blocks (KVS_DEVERR_DIFF_ID, the excess is not written).
+ * ws: kvs_workspace_size(KVS_OP_MIRROR) bytes.  BF16 pools with diff slabs. */
+kvs_status kvs_mirror_build(kvs_pool* pool, int32_t layer, const int32_t* block_table_dev, int32_t max_blocks,
+                            const int32_t* seq_len_dev, int32_t n_seq, const int32_t* idx_dev,
+                            const int64_t* idx_off_dev, const void* k_new_dev, const void* v_new_dev,
+                            const int32_t* rope_off_dev, const kvs_seg_rope* rope_segs_dev, float theta,
+                            int32_t* diff_table_dev, int32_t* n_diff_dev, void* ws, size_t ws_bytes,
+                            cudaStream_t stream);
+
 /* Workspace bytes for an operation with the given call shape. */
 #define KVS_OP_DEDUP 0
 #define KVS_OP_DECODE_ATTN 1
 #define KVS_OP_DECODE_ATTN_Q4 2
 #define KVS_OP_SELECT 3
+#define KVS_OP_MIRROR 4
 kvs_status kvs_workspace_size(const kvs_pool* pool, int32_t op, int32_t n_seq,
                               int32_t max_blocks, int32_t n_q_heads, size_t* bytes);
 

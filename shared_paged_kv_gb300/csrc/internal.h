@@ -65,4 +65,7 @@ kvs_status decode_plan_token_major(kvs_pool* pool, int n_q_heads, const int32_t*
                                    const kvs_seg_rope* rope_segs, void* ws, cudaStream_t stream);
 constexpr int kTmMaxGroup = 8;
 
+// Mirror construction (mirror.cu).
+size_t mirror_workspace_bytes(int n_seq, int max_blocks);
+
 }  // namespace kvs

@@ -1,0 +1,342 @@
+// Mirror construction from refreshed critical positions (TokenDance summary,
+// section 2: only the critical positions of each request's cached K/V are
+// refreshed; section 3, Fig. 7: one master cache, the other caches of the
+// family kept as block-sparse K/V differences from it; Fig. 8: the diff is
+// applied before the RoPE positions are restored, so it lives in the
+// master's frame).
+//
+// Steps, all on the device:
+//  1. mir_mark    one CTA per agent: validate the refreshed positions, flag
+//                 the logical blocks that hold one, and (rotation calls) the
+//                 shift of every logical block (the last covering entry);
+//  2. mir_count / mir_scan / mir_apply: a deterministic exclusive scan of
+//                 the flags in (agent, block) order gives the diff ids, the
+//                 diff table and the list of dirty (agent, block) slots;
+//  3. mir_write   one warp per (dirty block, kv head): 16 rows, each found in
+//                 the agent's ascending position list by binary search; a
+//                 refreshed row becomes bf16(R(-delta) k_new - K_master) and
+//                 bf16(v_new - V_master), every other row zero.  Lane (row,
+//                 v) holds head dims [8v, 8v+8) and [d/2+8v, d/2+8v+8), so the
+//                 rotate-half partners sit in the same lane.
+#include "common.cuh"
+#include "internal.h"
+
+namespace kvs {
+
+constexpr int kMirChunk = 2048;   // flags per CTA in the id scan
+constexpr int kMirB = 16;         // block tokens this path supports
+
+static size_t mir_align(size_t x) { return (x + 255) & ~size_t(255); }
+
+struct MirLayout {
+  int n_chunks;
+  size_t off_flags, off_counts, off_list, off_delta, total;
+};
+
+static MirLayout mir_layout(int n_seq, int max_blocks) {
+  const size_t slots = (size_t)n_seq * max_blocks;
+  MirLayout L{};
+  L.n_chunks = (int)((slots + kMirChunk - 1) / kMirChunk);
+  size_t o = 0;
+  L.off_flags = o; o = mir_align(o + slots);
+  L.off_counts = o; o = mir_align(o + (size_t)(L.n_chunks + 1) * sizeof(int32_t));
+  L.off_list = o; o = mir_align(o + slots * sizeof(int32_t));
+  L.off_delta = o; o = mir_align(o + slots * sizeof(int32_t));
+  L.total = o;
+  return L;
+}
+
+size_t mirror_workspace_bytes(int n_seq, int max_blocks) { return mir_layout(n_seq, max_blocks).total + 256; }
+
+struct MirParams {
+  const int32_t* table;
+  const int32_t* seq_len;
+  const int32_t* idx;
+  const int64_t* idx_off;
+  const uint16_t* k_new;
+  const uint16_t* v_new;
+  const int32_t* rope_off;
+  const int4* rope_segs;
+  const uint16_t* kslab;
+  const uint16_t* vslab;
+  uint16_t* dk;
+  uint16_t* dv;
+  int32_t* diff_table;
+  int32_t* n_diff;
+  uint8_t* flags;     // [n_seq][max_blocks] 1 = dirty
+  int32_t* counts;    // [n_chunks + 1] per-chunk dirty counts, then their exclusive scan
+  int32_t* list;      // [n_diff] dirty slot (a * max_blocks + b) of each diff id
+  int32_t* bdelta;    // [n_seq][max_blocks] RoPE shift per block (rotation calls)
+  uint32_t* status;
+  int n_seq, max_blocks, hkv, capacity, diff_capacity, n_chunks;
+  RopeSplit rs;
+};
+
+// 1. positions -> dirty flags; per-block shifts
+__global__ void __launch_bounds__(256) mir_mark(const __grid_constant__ MirParams p) {
+  for (int a = blockIdx.x; a < p.n_seq; a += gridDim.x) {
+    const long long r0 = p.idx_off[a], r1 = p.idx_off[a + 1];
+    int L = p.seq_len[a];
+    if (L < 0 || L > p.max_blocks * kMirB) {
+      if (threadIdx.x == 0) set_err(p.status, KVS_DEVERR_SEQ_LEN);
+      L = L < 0 ? 0 : p.max_blocks * kMirB;
+    }
+    if (r0 < 0 || r1 < r0) {
+      if (threadIdx.x == 0) set_err(p.status, KVS_DEVERR_JOB);
+    } else {
+      for (long long r = r0 + threadIdx.x; r < r1; r += blockDim.x) {
+        const int t = p.idx[r];
+        if (t < 0 || t >= L || (r > r0 && p.idx[r - 1] >= t)) {
+          set_err(p.status, KVS_DEVERR_JOB);
+          continue;
+        }
+        p.flags[(size_t)a * p.max_blocks + t / kMirB] = 1;   // equal-value writes
+      }
+    }
+    if (p.rope_off) {
+      const int e0 = p.rope_off[a], e1 = p.rope_off[a + 1];
+      for (int b = threadIdx.x; b < p.max_blocks; b += blockDim.x) {
+        int dl = 0;
+        for (int e = e0; e < e1; ++e) {
+          const int4 sg = __ldg(p.rope_segs + e);
+          if (b >= sg.x && b - sg.x < sg.y) dl = sg.z;
+        }
+        if (dl <= -(1 << 18) || dl >= (1 << 18)) {
+          set_err(p.status, KVS_DEVERR_ROPE_RANGE);
+          dl = 0;
+        }
+        p.bdelta[(size_t)a * p.max_blocks + b] = dl;
+      }
+    }
+  }
+}
+
+// 2a. dirty blocks per chunk of kMirChunk slots
+__global__ void __launch_bounds__(256) mir_count(const __grid_constant__ MirParams p) {
+  __shared__ int warp_sums[32];
+  const size_t slots = (size_t)p.n_seq * p.max_blocks;
+  for (int ch = blockIdx.x; ch < p.n_chunks; ch += gridDim.x) {
+    const size_t b0 = (size_t)ch * kMirChunk;
+    int cnt = 0;
+    for (int i = threadIdx.x; i < kMirChunk; i += blockDim.x)
+      if (b0 + i < slots) cnt += p.flags[b0 + i];
+    int total;
+    block_exclusive_scan(cnt, warp_sums, total);
+    if (threadIdx.x == 0) p.counts[ch] = total;
+  }
+}
+
+// 2b. exclusive scan of the chunk counts (one CTA); the total is n_diff
+__global__ void __launch_bounds__(1024) mir_scan(const __grid_constant__ MirParams p) {
+  __shared__ int warp_sums[32];
+  int carry = 0;
+  for (int base = 0; base < p.n_chunks; base += blockDim.x) {
+    const int i = base + threadIdx.x;
+    const int x = i < p.n_chunks ? p.counts[i] : 0;
+    int total;
+    const int ex = block_exclusive_scan(x, warp_sums, total);
+    if (i < p.n_chunks) p.counts[i] = carry + ex;
+    carry += total;
+  }
+  if (threadIdx.x == 0) {
+    p.counts[p.n_chunks] = carry;
+    *p.n_diff = carry;
+    if (carry > p.diff_capacity) set_err(p.status, KVS_DEVERR_DIFF_ID);
+  }
+}
+
+// 2c. ids in (agent, block) order: diff table and dirty list
+__global__ void __launch_bounds__(256) mir_apply(const __grid_constant__ MirParams p) {
+  __shared__ int warp_sums[32];
+  const size_t slots = (size_t)p.n_seq * p.max_blocks;
+  for (int ch = blockIdx.x; ch < p.n_chunks; ch += gridDim.x) {
+    const size_t b0 = (size_t)ch * kMirChunk;
+    int carry = p.counts[ch];
+    for (int base = 0; base < kMirChunk; base += blockDim.x) {
+      const size_t s = b0 + base + threadIdx.x;
+      const int f = s < slots ? p.flags[s] : 0;
+      int total;
+      const int ex = block_exclusive_scan(f, warp_sums, total);
+      if (s < slots) {
+        const int id = carry + ex;
+        p.diff_table[s] = f ? id : -1;
+        if (f) p.list[id] = (int)s;
+      }
+      carry += total;
+    }
+  }
+}
+
+// 3. diff tiles of every dirty (block, kv head)
+template <int D>
+__global__ void __launch_bounds__(256) mir_write(const __grid_constant__ MirParams p) {
+  constexpr int VEC = 8;              // bf16 per 16-byte vector
+  constexpr int NV = D / 2 / VEC;     // lanes per row
+  constexpr int RPS = 32 / NV;        // rows per warp step
+  __shared__ float rsc[4 * 64];       // RoPE frequency pieces (rotation calls)
+  if (p.rope_off) {
+    for (int i = threadIdx.x; i < 4 * 64; i += blockDim.x) rsc[i] = p.rs.c[i >> 6][i & 63];
+    __syncthreads();
+  }
+  const int lane = threadIdx.x & 31;
+  const int v = lane % NV, rl = lane / NV;
+  const int n_diff = min(*p.n_diff, p.diff_capacity);
+  const long long units = (long long)n_diff * p.hkv;
+  const int wpb = blockDim.x >> 5;
+  for (long long u = (long long)blockIdx.x * wpb + (threadIdx.x >> 5); u < units; u += (long long)gridDim.x * wpb) {
+    const int id = (int)(u / p.hkv), h = (int)(u - (long long)id * p.hkv);
+    const int slot = p.list[id];
+    const int a = slot / p.max_blocks, b = slot - a * p.max_blocks;
+    const int phys = p.table[slot];
+    const bool valid = phys >= 0 && phys < p.capacity;
+    if (!valid && lane == 0 && h == 0) set_err(p.status, KVS_DEVERR_BLOCK_ID);
+    // lane j < 16: the position list row of token j of the block (or -1)
+    const long long r0 = p.idx_off[a], r1 = p.idx_off[a + 1];
+    int myrow = -1;
+    if (lane < kMirB && r0 >= 0 && r1 > r0) {
+      const int t = b * kMirB + lane;
+      long long lo = r0, hi = r1 - 1;
+      while (lo <= hi) {
+        const long long mid = (lo + hi) >> 1;
+        const int x = p.idx[mid];
+        if (x == t) {
+          myrow = (int)mid;
+          break;
+        }
+        if (x < t) lo = mid + 1;
+        else hi = mid - 1;
+      }
+    }
+    float cs[VEC], sn[VEC];
+    const int delta = p.rope_off ? p.bdelta[slot] : 0;
+#pragma unroll
+    for (int e = 0; e < VEC; ++e) {
+      cs[e] = 1.f;
+      sn[e] = 0.f;
+    }
+    if (delta != 0) {
+#pragma unroll
+      for (int e = 0; e < VEC; ++e) rope_cos_sin(rsc, v * VEC + e, delta, cs[e], sn[e]);
+    }
+    const size_t tile = ((size_t)id * p.hkv + h) * kMirB;
+    const size_t mtile = ((size_t)(valid ? phys : 0) * p.hkv + h) * kMirB;
+#pragma unroll
+    for (int st = 0; st < kMirB / RPS; ++st) {
+      const int row = st * RPS + rl;
+      const int r = __shfl_sync(0xffffffffu, myrow, row);
+      uint4 dkl = make_uint4(0, 0, 0, 0), dkh = dkl, dvl = dkl, dvh = dkl;
+      if (r >= 0 && valid) {
+        const size_t mo = (mtile + row) * D + v * VEC;
+        const size_t no = ((size_t)r * p.hkv + h) * D + v * VEC;
+        const uint4 kml = __ldg(reinterpret_cast<const uint4*>(p.kslab + mo));
+        const uint4 kmh = __ldg(reinterpret_cast<const uint4*>(p.kslab + mo + D / 2));
+        const uint4 vml = __ldg(reinterpret_cast<const uint4*>(p.vslab + mo));
+        const uint4 vmh = __ldg(reinterpret_cast<const uint4*>(p.vslab + mo + D / 2));
+        const uint4 knl = __ldg(reinterpret_cast<const uint4*>(p.k_new + no));
+        const uint4 knh = __ldg(reinterpret_cast<const uint4*>(p.k_new + no + D / 2));
+        const uint4 vnl = __ldg(reinterpret_cast<const uint4*>(p.v_new + no));
+        const uint4 vnh = __ldg(reinterpret_cast<const uint4*>(p.v_new + no + D / 2));
+        const uint32_t a_kml[4] = {kml.x, kml.y, kml.z, kml.w}, a_kmh[4] = {kmh.x, kmh.y, kmh.z, kmh.w};
+        const uint32_t a_vml[4] = {vml.x, vml.y, vml.z, vml.w}, a_vmh[4] = {vmh.x, vmh.y, vmh.z, vmh.w};
+        const uint32_t a_knl[4] = {knl.x, knl.y, knl.z, knl.w}, a_knh[4] = {knh.x, knh.y, knh.z, knh.w};
+        const uint32_t a_vnl[4] = {vnl.x, vnl.y, vnl.z, vnl.w}, a_vnh[4] = {vnh.x, vnh.y, vnh.z, vnh.w};
+        uint32_t o_kl[4], o_kh[4], o_vl[4], o_vh[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          // R(-delta): lo' = lo cos + hi sin, hi' = hi cos - lo sin
+          const float x0 = bf16_lo(a_knl[e]), x1 = bf16_hi(a_knl[e]);
+          const float y0 = bf16_lo(a_knh[e]), y1 = bf16_hi(a_knh[e]);
+          const float l0 = x0 * cs[2 * e] + y0 * sn[2 * e], l1 = x1 * cs[2 * e + 1] + y1 * sn[2 * e + 1];
+          const float h0 = y0 * cs[2 * e] - x0 * sn[2 * e], h1 = y1 * cs[2 * e + 1] - x1 * sn[2 * e + 1];
+          o_kl[e] = pack_bf16(l0 - bf16_lo(a_kml[e]), l1 - bf16_hi(a_kml[e]));
+          o_kh[e] = pack_bf16(h0 - bf16_lo(a_kmh[e]), h1 - bf16_hi(a_kmh[e]));
+          o_vl[e] = pack_bf16(bf16_lo(a_vnl[e]) - bf16_lo(a_vml[e]), bf16_hi(a_vnl[e]) - bf16_hi(a_vml[e]));
+          o_vh[e] = pack_bf16(bf16_lo(a_vnh[e]) - bf16_lo(a_vmh[e]), bf16_hi(a_vnh[e]) - bf16_hi(a_vmh[e]));
+        }
+        dkl = make_uint4(o_kl[0], o_kl[1], o_kl[2], o_kl[3]);
+        dkh = make_uint4(o_kh[0], o_kh[1], o_kh[2], o_kh[3]);
+        dvl = make_uint4(o_vl[0], o_vl[1], o_vl[2], o_vl[3]);
+        dvh = make_uint4(o_vh[0], o_vh[1], o_vh[2], o_vh[3]);
+      }
+      const size_t dofs = (tile + row) * D + v * VEC;
+      *reinterpret_cast<uint4*>(p.dk + dofs) = dkl;
+      *reinterpret_cast<uint4*>(p.dk + dofs + D / 2) = dkh;
+      *reinterpret_cast<uint4*>(p.dv + dofs) = dvl;
+      *reinterpret_cast<uint4*>(p.dv + dofs + D / 2) = dvh;
+    }
+  }
+}
+
+}  // namespace kvs
+
+using namespace kvs;
+
+extern "C" kvs_status kvs_mirror_build(kvs_pool* pool, int32_t layer, const int32_t* block_table_dev,
+                                       int32_t max_blocks, const int32_t* seq_len_dev, int32_t n_seq,
+                                       const int32_t* idx_dev, const int64_t* idx_off_dev, const void* k_new_dev,
+                                       const void* v_new_dev, const int32_t* rope_off_dev,
+                                       const kvs_seg_rope* rope_segs_dev, float theta, int32_t* diff_table_dev,
+                                       int32_t* n_diff_dev, void* ws, size_t ws_bytes, cudaStream_t stream) {
+  if (!pool) return fail(KVS_ERR_INVALID_ARG, "mirror_build: null pool");
+  const kvs_pool_desc& d = pool->desc;
+  if (d.dtype != KVS_DTYPE_BF16) return fail(KVS_ERR_INVALID_ARG, "mirror_build: bf16 pools only");
+  if (d.diff_capacity_blocks <= 0) return fail(KVS_ERR_INVALID_ARG, "mirror_build: the pool has no diff slabs");
+  if (d.block_tokens != kMirB) return fail(KVS_ERR_UNSUPPORTED, "mirror_build: block_tokens must be 16");
+  if (layer < 0 || layer >= d.num_layers) return fail(KVS_ERR_INVALID_ARG, "mirror_build: layer out of range");
+  if (n_seq < 0 || max_blocks < 1) return fail(KVS_ERR_INVALID_ARG, "mirror_build: bad sizes");
+  if ((rope_off_dev == nullptr) != (rope_segs_dev == nullptr))
+    return fail(KVS_ERR_INVALID_ARG, "mirror_build: rope_off and rope_segs go together");
+  if (rope_off_dev && !(theta > 0.f)) return fail(KVS_ERR_INVALID_ARG, "mirror_build: theta must be positive");
+  if (!n_diff_dev) return fail(KVS_ERR_INVALID_ARG, "mirror_build: null n_diff");
+  if (n_seq == 0) return cudaMemsetAsync(n_diff_dev, 0, 4, stream) == cudaSuccess ? KVS_OK : fail(KVS_ERR_CUDA, "mirror_build: memset failed");
+  if (!block_table_dev || !seq_len_dev || !idx_dev || !idx_off_dev || !k_new_dev || !v_new_dev || !diff_table_dev ||
+      !ws)
+    return fail(KVS_ERR_INVALID_ARG, "mirror_build: null pointer");
+  if (!aligned16(k_new_dev) || !aligned16(v_new_dev) || !aligned16(ws))
+    return fail(KVS_ERR_INVALID_ARG, "mirror_build: k_new, v_new and ws must be 16-byte aligned");
+  const MirLayout L = mir_layout(n_seq, max_blocks);
+  if (ws_bytes < L.total) return fail(KVS_ERR_CAPACITY, "mirror_build: workspace too small");
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  MirParams p{};
+  p.table = block_table_dev;
+  p.seq_len = seq_len_dev;
+  p.idx = idx_dev;
+  p.idx_off = idx_off_dev;
+  p.k_new = static_cast<const uint16_t*>(k_new_dev);
+  p.v_new = static_cast<const uint16_t*>(v_new_dev);
+  p.rope_off = rope_off_dev;
+  p.rope_segs = reinterpret_cast<const int4*>(rope_segs_dev);
+  p.kslab = static_cast<const uint16_t*>(pool->k[layer]);
+  p.vslab = static_cast<const uint16_t*>(pool->v[layer]);
+  p.dk = static_cast<uint16_t*>(pool->dk[layer]);
+  p.dv = static_cast<uint16_t*>(pool->dv[layer]);
+  p.diff_table = diff_table_dev;
+  p.n_diff = n_diff_dev;
+  p.flags = w + L.off_flags;
+  p.counts = reinterpret_cast<int32_t*>(w + L.off_counts);
+  p.list = reinterpret_cast<int32_t*>(w + L.off_list);
+  p.bdelta = reinterpret_cast<int32_t*>(w + L.off_delta);
+  p.status = pool->status;
+  p.n_seq = n_seq;
+  p.max_blocks = max_blocks;
+  p.hkv = d.num_kv_heads;
+  p.capacity = d.capacity_blocks;
+  p.diff_capacity = d.diff_capacity_blocks;
+  p.n_chunks = L.n_chunks;
+  if (rope_off_dev) rope_split_host(theta, d.head_dim, p.rs.c);
+  if (cudaMemsetAsync(p.flags, 0, (size_t)n_seq * max_blocks, stream) != cudaSuccess)
+    return fail(KVS_ERR_CUDA, "mirror_build: memset failed");
+  const int sms = pool->num_sms;
+  mir_mark<<<std::min(n_seq, sms * 8), 256, 0, stream>>>(p);
+  mir_count<<<std::min(L.n_chunks, sms * 8), 256, 0, stream>>>(p);
+  mir_scan<<<1, 1024, 0, stream>>>(p);
+  mir_apply<<<std::min(L.n_chunks, sms * 8), 256, 0, stream>>>(p);
+  // the dirty count is only known on the device: a persistent grid of warps
+  // walks the (dirty block, kv head) units
+  if (d.head_dim == 128)
+    mir_write<128><<<sms * 8, 256, 0, stream>>>(p);
+  else
+    mir_write<64><<<sms * 8, 256, 0, stream>>>(p);
+  count_launch(5);
+  return check_launch("mirror_build");
+}

@@ -262,6 +262,9 @@ kvs_status kvs_workspace_size(const kvs_pool* p, int32_t op, int32_t n_seq, int3
       b = static_cast<size_t>(n_seq) * max_blocks * sizeof(float) + 256;
       break;
     }
+    case KVS_OP_MIRROR:
+      b = mirror_workspace_bytes(n_seq, max_blocks);
+      break;
     default:
       return fail(KVS_ERR_INVALID_ARG, "workspace_size: unknown op");
   }

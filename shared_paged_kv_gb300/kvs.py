@@ -36,12 +36,12 @@ KVS_DEVERR_PLAN = 0x80
 KVS_DTYPE_BF16 = 0
 KVS_DTYPE_Q4G64 = 1
 KVS_DEDUP_TEST_WEAK_KEYS = 0x1
-KVS_OP_DEDUP, KVS_OP_DECODE_ATTN, KVS_OP_DECODE_ATTN_Q4, KVS_OP_SELECT = 0, 1, 2, 3
+KVS_OP_DEDUP, KVS_OP_DECODE_ATTN, KVS_OP_DECODE_ATTN_Q4, KVS_OP_SELECT, KVS_OP_MIRROR = 0, 1, 2, 3, 4
 
 EXPORTED = [
     "kvs_pool_create", "kvs_pool_destroy", "kvs_fingerprint_dedup", "kvs_rope_rerotate",
     "kvs_select_critical", "kvs_select_critical_noalloc", "kvs_decode_plan", "kvs_decode_attn_planned",
-    "kvs_decode_attn", "kvs_decode_attn_q4", "kvs_quantize_q4",
+    "kvs_decode_attn", "kvs_decode_attn_q4", "kvs_quantize_q4", "kvs_mirror_build",
     "kvs_workspace_size", "kvs_pool_check", "kvs_pool_stats", "kvs_last_error_string",
     "kvs_launch_count",
 ]
@@ -84,6 +84,7 @@ def load(path: str = LIB_PATH):
         "kvs_rope_rerotate": [P, I32, P, I32, I32, F32, P, P, I32, P],
         "kvs_select_critical": [P, P, P, I32, I32, I32, F32, P, P, P, SZ, P],
         "kvs_select_critical_noalloc": [P, P, P, I32, I32, I32, F32, P, P, P],
+        "kvs_mirror_build": [P, I32, P, I32, P, I32, P, P, P, P, P, P, F32, P, P, P, SZ, P],
         "kvs_decode_attn": [P, I32, P, I32, P, I32, P, I32, P, P, P, F32, F32, P, P, SZ, P],
         "kvs_decode_attn_planned": [P, I32, P, I32, P, I32, P, I32, P, P, P, F32, F32, P, P, SZ, P],
         "kvs_decode_plan": [P, I32, P, I32, P, I32, P, P, P, P, SZ, P],
@@ -191,6 +192,17 @@ def kvs_select_critical(k_cached, k_new, row_off, n_agents, max_rows_per_agent, 
     _check(load().kvs_select_critical(_ptr(k_cached), _ptr(k_new), _ptr(row_off), n_agents,
                                       max_rows_per_agent, row_elems, ratio, _ptr(idx_out), _ptr(idx_off),
                                       _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)))
+
+
+def kvs_mirror_build(pool: Pool, layer, block_table, max_blocks, seq_len, n_seq, idx, idx_off, k_new, v_new,
+                     rope_off, rope_segs, theta, diff_table, n_diff, ws, stream=None):
+    """Diff table and block-sparse diff tiles (written into the pool's diff
+    slabs of `layer`) of every agent's refreshed positions against its master
+    blocks; n_diff (device int32 [1]) receives the number of diff blocks."""
+    _check(load().kvs_mirror_build(pool.handle, layer, _ptr(block_table), max_blocks, _ptr(seq_len), n_seq, _ptr(idx),
+                                   _ptr(idx_off), _ptr(k_new), _ptr(v_new), _ptr(rope_off), _ptr(rope_segs), theta,
+                                   _ptr(diff_table), _ptr(n_diff), _ptr(ws), ws.numel() * ws.element_size(),
+                                   _stream(stream)))
 
 
 def kvs_select_critical_noalloc(k_cached, k_new, row_off, n_agents, max_rows_per_agent, row_elems, ratio,
