@@ -53,7 +53,7 @@ def parse():
     ap.add_argument("--no-rope", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--layers", type=int, default=32)
-    ap.add_argument("--workload", default="mha7b", choices=["mha7b", "tiny", "gqa_fanout", "allgather", "q4", "select"],
+    ap.add_argument("--workload", default="mha7b", choices=["mha7b", "tiny", "gqa_fanout", "allgather", "q4", "select", "mirror"],
                     help="mha7b is the headline workload; the others print a per-workload record for profiling")
     return ap.parse_args()
 
@@ -489,6 +489,70 @@ def bench_tiny_replicated(torch, K, W, dev, reps, flush, n_inst=4096):
             "status_flags": flags}
 
 
+def bench_mirror(args, torch, K, W, dev, stream):
+    """Mirror construction of the all-gather round at one layer: 64 agents,
+    each refreshing every row of 31 blocks among its 512 shared-segment
+    blocks (the round's mirror structure), K rotated back by the segment
+    shift."""
+    w = W.make_allgather(n_layers=1)
+    rng = np.random.default_rng(5)
+    tokens = torch.from_numpy(w.tokens.view(np.int32)).to(dev)
+    seq_off = torch.from_numpy(w.seq_off).to(dev)
+    so = torch.from_numpy(w.seg_start_off).to(dev)
+    sb = torch.from_numpy(w.seg_start_blocks).to(dev)
+    N, H, D = w.n_seq, w.n_kv_heads, w.head_dim
+    d16 = torch.zeros(16, dtype=torch.int16, device=dev)
+    probe = K.kvs_pool_create(1, H, D, 16, K.KVS_DTYPE_BF16, w.capacity_blocks, N, [d16], [d16])
+    fp = torch.zeros((N, w.max_blocks), dtype=torch.int64, device=dev)
+    table = torch.zeros((N, w.max_blocks), dtype=torch.int32, device=dev)
+    refc = torch.zeros(w.capacity_blocks, dtype=torch.int32, device=dev)
+    nphys = torch.zeros(1, dtype=torch.int32, device=dev)
+    ws_d = torch.zeros(K.kvs_workspace_size(probe, K.KVS_OP_DEDUP, N, w.max_blocks), dtype=torch.uint8, device=dev)
+    K.kvs_fingerprint_dedup(probe, tokens, seq_off, N, None, so, sb, fp, table, w.max_blocks, refc, nphys, ws_d)
+    cap = int(nphys.item())
+    idx, off = [], [0]
+    for a in range(N):
+        fb = int(w.rope_segs[w.rope_off[a]][0])
+        for b in np.sort(rng.choice(512, size=31, replace=False)) + fb:
+            idx.extend(range(int(b) * 16, int(b) * 16 + 16))
+        off.append(len(idx))
+    n_rows = len(idx)
+    gen = torch.Generator(device=dev).manual_seed(9)
+    k = torch.randn((cap, H, 16, D), generator=gen, device=dev, dtype=torch.bfloat16).view(torch.int16)
+    v = torch.randn((cap, H, 16, D), generator=gen, device=dev, dtype=torch.bfloat16).view(torch.int16)
+    kn = torch.randn((n_rows, H, D), generator=gen, device=dev, dtype=torch.bfloat16).view(torch.int16)
+    vn = torch.randn((n_rows, H, D), generator=gen, device=dev, dtype=torch.bfloat16).view(torch.int16)
+    cap_d = N * 31
+    dk = torch.zeros((cap_d, H, 16, D), dtype=torch.int16, device=dev)
+    dv = torch.zeros_like(dk)
+    pool = K.kvs_pool_create(1, H, D, 16, K.KVS_DTYPE_BF16, cap, N, [k], [v], dk_layers=[dk], dv_layers=[dv],
+                             diff_capacity_blocks=cap_d)
+    idx_t = torch.tensor(idx, dtype=torch.int32, device=dev)
+    off_t = torch.tensor(off, dtype=torch.int64, device=dev)
+    ro = torch.from_numpy(w.rope_off).to(dev)
+    rs = torch.from_numpy(w.rope_segs).to(dev)
+    sl = torch.from_numpy(w.seq_len).to(dev)
+    diff_table = torch.zeros((N, w.max_blocks), dtype=torch.int32, device=dev)
+    n_diff = torch.zeros(1, dtype=torch.int32, device=dev)
+    ws = torch.zeros(K.kvs_workspace_size(pool, K.KVS_OP_MIRROR, N, w.max_blocks), dtype=torch.uint8, device=dev)
+
+    def run():
+        K.kvs_mirror_build(pool, 0, table, w.max_blocks, sl, N, idx_t, off_t, kn, vn, ro, rs, w.theta,
+                           diff_table, n_diff, ws)
+
+    flush = torch.zeros(64 << 20, dtype=torch.float32, device=dev)
+    ms = graph_replay_ms(torch, run, args.steps, flush)
+    flags = K.kvs_pool_check(pool)
+    tile = 16 * D * 2
+    byts = (cap_d * H * tile * 2) * 3 + n_rows * 4 + N * w.max_blocks * 4 * 2
+    peak, _ = read_peaks()
+    print(json.dumps({"workload": "mirror", "ms_per_call": ms, "dirty_blocks": cap_d, "rows": n_rows,
+                      "bytes": byts, "gbs": byts / (ms * 1e-3) / 1e9,
+                      "frac_of_measured_peak": byts / (ms * 1e-3) / 1e9 / peak,
+                      "l2": "flushed before every replay", "status_flags": flags}))
+    return 0
+
+
 def bench_workload(args, torch, K, W):
     """One-GPU record for a non-headline workload: GPU dedup + decode attention
     on every layer (Q4: attention only), timed with CUDA events."""
@@ -497,6 +561,8 @@ def bench_workload(args, torch, K, W):
     stream = torch.cuda.current_stream()
     if args.workload == "select":
         return bench_select(args, torch, K, dev, stream)
+    if args.workload == "mirror":
+        return bench_mirror(args, torch, K, W, dev, stream)
     mk = {"tiny": W.make_tiny, "gqa_fanout": W.make_gqa_fanout, "allgather": W.make_allgather, "q4": W.make_q4}
     w = mk[args.workload]()
     L = min(w.n_layers, args.layers)

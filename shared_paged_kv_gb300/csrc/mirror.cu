@@ -6,15 +6,17 @@
 // master's frame).
 //
 // Steps, all on the device:
-//  1. mir_mark    one CTA per agent: validate the refreshed positions, flag
-//                 the logical blocks that hold one, and (rotation calls) the
-//                 shift of every logical block (the last covering entry);
-//  2. mir_count / mir_scan / mir_apply: a deterministic exclusive scan of
-//                 the flags in (agent, block) order gives the diff ids, the
-//                 diff table and the list of dirty (agent, block) slots;
-//  3. mir_write   one warp per (dirty block, kv head): 16 rows, each found in
-//                 the agent's ascending position list by binary search; a
-//                 refreshed row becomes bf16(R(-delta) k_new - K_master) and
+//  1. mir_agent   one CTA per agent: validate the refreshed positions, flag
+//                 the logical blocks holding one and record, per (block,
+//                 row), which refreshed row it is; then count the agent's
+//                 dirty blocks;
+//  2. mir_scan    exclusive scan of the per-agent counts (one CTA): diff ids
+//                 are consecutive in agent order, then block order;
+//  3. mir_apply   one CTA per agent: diff table, the list of dirty slots and,
+//                 for rotation calls, each dirty block's shift (the last
+//                 covering segment entry);
+//  4. mir_write   one warp per (dirty block, kv head): 16 rows, a refreshed
+//                 row becoming bf16(R(-delta) k_new - K_master) and
 //                 bf16(v_new - V_master), every other row zero.  Lane (row,
 //                 v) holds head dims [8v, 8v+8) and [d/2+8v, d/2+8v+8), so the
 //                 rotate-half partners sit in the same lane.
@@ -23,23 +25,21 @@
 
 namespace kvs {
 
-constexpr int kMirChunk = 2048;   // flags per CTA in the id scan
 constexpr int kMirB = 16;         // block tokens this path supports
 
 static size_t mir_align(size_t x) { return (x + 255) & ~size_t(255); }
 
 struct MirLayout {
-  int n_chunks;
-  size_t off_flags, off_counts, off_list, off_delta, total;
+  size_t off_flags, off_rowmap, off_counts, off_list, off_delta, total;
 };
 
 static MirLayout mir_layout(int n_seq, int max_blocks) {
   const size_t slots = (size_t)n_seq * max_blocks;
   MirLayout L{};
-  L.n_chunks = (int)((slots + kMirChunk - 1) / kMirChunk);
   size_t o = 0;
   L.off_flags = o; o = mir_align(o + slots);
-  L.off_counts = o; o = mir_align(o + (size_t)(L.n_chunks + 1) * sizeof(int32_t));
+  L.off_rowmap = o; o = mir_align(o + slots * kMirB * sizeof(int32_t));
+  L.off_counts = o; o = mir_align(o + (size_t)(n_seq + 1) * sizeof(int32_t));
   L.off_list = o; o = mir_align(o + slots * sizeof(int32_t));
   L.off_delta = o; o = mir_align(o + slots * sizeof(int32_t));
   L.total = o;
@@ -64,16 +64,18 @@ struct MirParams {
   int32_t* diff_table;
   int32_t* n_diff;
   uint8_t* flags;     // [n_seq][max_blocks] 1 = dirty
-  int32_t* counts;    // [n_chunks + 1] per-chunk dirty counts, then their exclusive scan
+  int32_t* rowmap;    // [n_seq][max_blocks][16] refreshed row of each token, -1 if none
+  int32_t* counts;    // [n_seq + 1] dirty blocks per agent, then their exclusive scan
   int32_t* list;      // [n_diff] dirty slot (a * max_blocks + b) of each diff id
-  int32_t* bdelta;    // [n_seq][max_blocks] RoPE shift per block (rotation calls)
+  int32_t* dlt;       // [n_diff] RoPE shift of each dirty block (rotation calls)
   uint32_t* status;
-  int n_seq, max_blocks, hkv, capacity, diff_capacity, n_chunks;
+  int n_seq, max_blocks, hkv, capacity, diff_capacity;
   RopeSplit rs;
 };
 
-// 1. positions -> dirty flags; per-block shifts
-__global__ void __launch_bounds__(256) mir_mark(const __grid_constant__ MirParams p) {
+// 1. positions -> dirty flags and row map; dirty blocks per agent
+__global__ void __launch_bounds__(256) mir_agent(const __grid_constant__ MirParams p) {
+  __shared__ int warp_sums[32];
   for (int a = blockIdx.x; a < p.n_seq; a += gridDim.x) {
     const long long r0 = p.idx_off[a], r1 = p.idx_off[a + 1];
     int L = p.seq_len[a];
@@ -81,6 +83,7 @@ __global__ void __launch_bounds__(256) mir_mark(const __grid_constant__ MirParam
       if (threadIdx.x == 0) set_err(p.status, KVS_DEVERR_SEQ_LEN);
       L = L < 0 ? 0 : p.max_blocks * kMirB;
     }
+    uint8_t* fl = p.flags + (size_t)a * p.max_blocks;
     if (r0 < 0 || r1 < r0) {
       if (threadIdx.x == 0) set_err(p.status, KVS_DEVERR_JOB);
     } else {
@@ -90,84 +93,96 @@ __global__ void __launch_bounds__(256) mir_mark(const __grid_constant__ MirParam
           set_err(p.status, KVS_DEVERR_JOB);
           continue;
         }
-        p.flags[(size_t)a * p.max_blocks + t / kMirB] = 1;   // equal-value writes
+        fl[t / kMirB] = 1;   // equal-value writes
+        p.rowmap[((size_t)a * p.max_blocks + t / kMirB) * kMirB + t % kMirB] = (int)r;
       }
     }
-    if (p.rope_off) {
-      const int e0 = p.rope_off[a], e1 = p.rope_off[a + 1];
-      for (int b = threadIdx.x; b < p.max_blocks; b += blockDim.x) {
-        int dl = 0;
-        for (int e = e0; e < e1; ++e) {
-          const int4 sg = __ldg(p.rope_segs + e);
-          if (b >= sg.x && b - sg.x < sg.y) dl = sg.z;
-        }
-        if (dl <= -(1 << 18) || dl >= (1 << 18)) {
-          set_err(p.status, KVS_DEVERR_ROPE_RANGE);
-          dl = 0;
-        }
-        p.bdelta[(size_t)a * p.max_blocks + b] = dl;
-      }
-    }
-  }
-}
-
-// 2a. dirty blocks per chunk of kMirChunk slots
-__global__ void __launch_bounds__(256) mir_count(const __grid_constant__ MirParams p) {
-  __shared__ int warp_sums[32];
-  const size_t slots = (size_t)p.n_seq * p.max_blocks;
-  for (int ch = blockIdx.x; ch < p.n_chunks; ch += gridDim.x) {
-    const size_t b0 = (size_t)ch * kMirChunk;
+    __syncthreads();
     int cnt = 0;
-    for (int i = threadIdx.x; i < kMirChunk; i += blockDim.x)
-      if (b0 + i < slots) cnt += p.flags[b0 + i];
+    for (int b = threadIdx.x; b < p.max_blocks; b += blockDim.x) cnt += fl[b];
     int total;
     block_exclusive_scan(cnt, warp_sums, total);
-    if (threadIdx.x == 0) p.counts[ch] = total;
+    if (threadIdx.x == 0) p.counts[a] = total;
   }
 }
 
-// 2b. exclusive scan of the chunk counts (one CTA); the total is n_diff
+// 2. exclusive scan of the per-agent counts (one CTA); the total is n_diff
 __global__ void __launch_bounds__(1024) mir_scan(const __grid_constant__ MirParams p) {
   __shared__ int warp_sums[32];
   int carry = 0;
-  for (int base = 0; base < p.n_chunks; base += blockDim.x) {
+  for (int base = 0; base < p.n_seq; base += blockDim.x) {
     const int i = base + threadIdx.x;
-    const int x = i < p.n_chunks ? p.counts[i] : 0;
+    const int x = i < p.n_seq ? p.counts[i] : 0;
     int total;
     const int ex = block_exclusive_scan(x, warp_sums, total);
-    if (i < p.n_chunks) p.counts[i] = carry + ex;
+    if (i < p.n_seq) p.counts[i] = carry + ex;
     carry += total;
   }
   if (threadIdx.x == 0) {
-    p.counts[p.n_chunks] = carry;
+    p.counts[p.n_seq] = carry;
     *p.n_diff = carry;
     if (carry > p.diff_capacity) set_err(p.status, KVS_DEVERR_DIFF_ID);
   }
 }
 
-// 2c. ids in (agent, block) order: diff table and dirty list
+// 3. diff table, dirty list and shifts, one CTA per agent
+constexpr int kMirSegChunk = 256;   // segment entries staged in shared memory at a time
+
 __global__ void __launch_bounds__(256) mir_apply(const __grid_constant__ MirParams p) {
   __shared__ int warp_sums[32];
-  const size_t slots = (size_t)p.n_seq * p.max_blocks;
-  for (int ch = blockIdx.x; ch < p.n_chunks; ch += gridDim.x) {
-    const size_t b0 = (size_t)ch * kMirChunk;
-    int carry = p.counts[ch];
-    for (int base = 0; base < kMirChunk; base += blockDim.x) {
-      const size_t s = b0 + base + threadIdx.x;
-      const int f = s < slots ? p.flags[s] : 0;
+  __shared__ int4 segs[kMirSegChunk];
+  for (int a = blockIdx.x; a < p.n_seq; a += gridDim.x) {
+    const uint8_t* fl = p.flags + (size_t)a * p.max_blocks;
+    const int first = p.counts[a];
+    int carry = first;
+    for (int base = 0; base < p.max_blocks; base += blockDim.x) {
+      const int b = base + threadIdx.x;
+      const int f = b < p.max_blocks ? fl[b] : 0;
       int total;
       const int ex = block_exclusive_scan(f, warp_sums, total);
-      if (s < slots) {
+      if (b < p.max_blocks) {
+        const size_t slot = (size_t)a * p.max_blocks + b;
         const int id = carry + ex;
-        p.diff_table[s] = f ? id : -1;
-        if (f) p.list[id] = (int)s;
+        p.diff_table[slot] = f ? id : -1;
+        if (f && id < p.diff_capacity) {
+          p.list[id] = (int)slot;
+          if (!p.rope_off) p.dlt[id] = 0;
+        }
       }
       carry += total;
     }
+    if (!p.rope_off) continue;
+    // shifts of this agent's dirty blocks: the last covering entry, the
+    // segment list streamed through shared memory
+    __syncthreads();   // the list entries above are read by other threads
+    const int n_dirty = min(carry, p.diff_capacity) - min(first, p.diff_capacity);
+    const int e0 = p.rope_off[a], e1 = p.rope_off[a + 1];
+    for (int i0 = 0; i0 < n_dirty; i0 += blockDim.x) {
+      const int i = i0 + threadIdx.x;
+      const int b = i < n_dirty ? p.list[first + i] - a * p.max_blocks : -1;
+      int dl = 0;
+      for (int c0 = e0; c0 < e1; c0 += kMirSegChunk) {
+        __syncthreads();
+        for (int e = c0 + threadIdx.x; e < min(e1, c0 + kMirSegChunk); e += blockDim.x) segs[e - c0] = __ldg(p.rope_segs + e);
+        __syncthreads();
+        const int ne = min(e1, c0 + kMirSegChunk) - c0;
+        if (b >= 0)
+          for (int e = 0; e < ne; ++e)
+            if (b >= segs[e].x && b - segs[e].x < segs[e].y) dl = segs[e].z;
+      }
+      if (b >= 0) {
+        if (dl <= -(1 << 18) || dl >= (1 << 18)) {
+          set_err(p.status, KVS_DEVERR_ROPE_RANGE);
+          dl = 0;
+        }
+        p.dlt[first + i] = dl;
+      }
+    }
+    __syncthreads();
   }
 }
 
-// 3. diff tiles of every dirty (block, kv head)
+// 4. diff tiles of every dirty (block, kv head)
 template <int D>
 __global__ void __launch_bounds__(256) mir_write(const __grid_constant__ MirParams p) {
   constexpr int VEC = 8;              // bf16 per 16-byte vector
@@ -186,29 +201,13 @@ __global__ void __launch_bounds__(256) mir_write(const __grid_constant__ MirPara
   for (long long u = (long long)blockIdx.x * wpb + (threadIdx.x >> 5); u < units; u += (long long)gridDim.x * wpb) {
     const int id = (int)(u / p.hkv), h = (int)(u - (long long)id * p.hkv);
     const int slot = p.list[id];
-    const int a = slot / p.max_blocks, b = slot - a * p.max_blocks;
     const int phys = p.table[slot];
     const bool valid = phys >= 0 && phys < p.capacity;
     if (!valid && lane == 0 && h == 0) set_err(p.status, KVS_DEVERR_BLOCK_ID);
-    // lane j < 16: the position list row of token j of the block (or -1)
-    const long long r0 = p.idx_off[a], r1 = p.idx_off[a + 1];
-    int myrow = -1;
-    if (lane < kMirB && r0 >= 0 && r1 > r0) {
-      const int t = b * kMirB + lane;
-      long long lo = r0, hi = r1 - 1;
-      while (lo <= hi) {
-        const long long mid = (lo + hi) >> 1;
-        const int x = p.idx[mid];
-        if (x == t) {
-          myrow = (int)mid;
-          break;
-        }
-        if (x < t) lo = mid + 1;
-        else hi = mid - 1;
-      }
-    }
+    // lane j < 16: the refreshed row of token j of the block (or -1)
+    const int myrow = lane < kMirB ? p.rowmap[(size_t)slot * kMirB + lane] : -1;
     float cs[VEC], sn[VEC];
-    const int delta = p.rope_off ? p.bdelta[slot] : 0;
+    const int delta = p.rope_off ? p.dlt[id] : 0;
 #pragma unroll
     for (int e = 0; e < VEC; ++e) {
       cs[e] = 1.f;
@@ -313,30 +312,32 @@ extern "C" kvs_status kvs_mirror_build(kvs_pool* pool, int32_t layer, const int3
   p.diff_table = diff_table_dev;
   p.n_diff = n_diff_dev;
   p.flags = w + L.off_flags;
+  p.rowmap = reinterpret_cast<int32_t*>(w + L.off_rowmap);
   p.counts = reinterpret_cast<int32_t*>(w + L.off_counts);
   p.list = reinterpret_cast<int32_t*>(w + L.off_list);
-  p.bdelta = reinterpret_cast<int32_t*>(w + L.off_delta);
+  p.dlt = reinterpret_cast<int32_t*>(w + L.off_delta);
   p.status = pool->status;
   p.n_seq = n_seq;
   p.max_blocks = max_blocks;
   p.hkv = d.num_kv_heads;
   p.capacity = d.capacity_blocks;
   p.diff_capacity = d.diff_capacity_blocks;
-  p.n_chunks = L.n_chunks;
   if (rope_off_dev) rope_split_host(theta, d.head_dim, p.rs.c);
-  if (cudaMemsetAsync(p.flags, 0, (size_t)n_seq * max_blocks, stream) != cudaSuccess)
+  const size_t slots = (size_t)n_seq * max_blocks;
+  if (cudaMemsetAsync(p.flags, 0, slots, stream) != cudaSuccess ||
+      cudaMemsetAsync(p.rowmap, 0xff, slots * kMirB * sizeof(int32_t), stream) != cudaSuccess)
     return fail(KVS_ERR_CUDA, "mirror_build: memset failed");
   const int sms = pool->num_sms;
-  mir_mark<<<std::min(n_seq, sms * 8), 256, 0, stream>>>(p);
-  mir_count<<<std::min(L.n_chunks, sms * 8), 256, 0, stream>>>(p);
+  const int agent_grid = std::min(n_seq, sms * 8);
+  mir_agent<<<agent_grid, 256, 0, stream>>>(p);
   mir_scan<<<1, 1024, 0, stream>>>(p);
-  mir_apply<<<std::min(L.n_chunks, sms * 8), 256, 0, stream>>>(p);
+  mir_apply<<<agent_grid, 256, 0, stream>>>(p);
   // the dirty count is only known on the device: a persistent grid of warps
   // walks the (dirty block, kv head) units
   if (d.head_dim == 128)
     mir_write<128><<<sms * 8, 256, 0, stream>>>(p);
   else
     mir_write<64><<<sms * 8, 256, 0, stream>>>(p);
-  count_launch(5);
+  count_launch(4);
   return check_launch("mirror_build");
 }
