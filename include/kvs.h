@@ -67,6 +67,7 @@ typedef enum {
 #define KVS_DEVERR_ROPE_RANGE   0x20u /* |position shift| >= 2^18 */
 #define KVS_DEVERR_JOB          0x40u /* a RoPE job addresses tokens outside its table row */
 #define KVS_DEVERR_PLAN         0x80u /* kvs_decode_attn_planned saw no matching plan in ws */
+#define KVS_DEVERR_REFCOUNT     0x100u /* a release took a reference count below zero */
 
 typedef enum { KVS_DTYPE_BF16 = 0, KVS_DTYPE_Q4G64 = 1 } kvs_dtype;
 
@@ -316,12 +317,56 @@ kvs_status kvs_mirror_build(kvs_pool* pool, int32_t layer, const int32_t* block_
                             int32_t* diff_table_dev, int32_t* n_diff_dev, void* ws, size_t ws_bytes,
                             cudaStream_t stream);
 
+/* ---------------------------------------------------------------------------
+ * Block lifetime: copy-on-write and sequence release ([INMS] §2.2: shared
+ * blocks are read-only; a sequence about to write into a block that others
+ * also reference gets a private copy, the old block's reference count drops,
+ * otherwise it writes in place; §3.3: destroying a sequence decrements the
+ * counts of its blocks and reclaims what becomes unused; §5.3: a missed
+ * release leaks).  State, all caller-owned device memory: refcount_dev int32
+ * [capacity] (as kvs_fingerprint_dedup writes it), a free stack free_ids_dev
+ * int32 [capacity] with n_free_dev int32 [1] (entries [0, n_free), the top at
+ * n_free - 1).  Blocks are pushed in descending id order, so the smallest id
+ * is on top and taken first.  A block of sequence a is referenced at logical
+ * block b < ceil(seq_len[a] / block_tokens).  ws: kvs_workspace_size(
+ * KVS_OP_BLOCKS, n_items = max(n_writes, n_seq)) bytes.
+ *
+ * kvs_blocks_init_free: the stack = every block whose count is 0.
+ *
+ * kvs_block_write: applies the writes w = 0 .. n_writes-1 in list order, each
+ * to logical block write_block[w] of sequence write_seq[w], with the pages'
+ * write_to_block rule: when the block's count is above 1 the sequence takes
+ * the block on top of the stack, every layer's K and V (Q4: codes and
+ * scale/bias) of the old block are copied into it, its count becomes 1, the
+ * old one's drops by 1 and the table entry is redirected; otherwise nothing
+ * changes (the caller writes in place).  A write whose (sequence, block)
+ * appeared earlier in the batch targets the private copy made then.  An empty
+ * stack leaves the write on the shared block (KVS_DEVERR_CAPACITY); a bad
+ * sequence/block index (KVS_DEVERR_JOB) or table entry (KVS_DEVERR_BLOCK_ID)
+ * skips the write.
+ *
+ * kvs_seq_release: for every sequence listed (duplicates count once),
+ * decrements the counts of its referenced blocks, sets its table row to -1
+ * and seq_len to 0; the blocks that reached 0 are pushed.  A count going
+ * below zero sets KVS_DEVERR_REFCOUNT. */
+kvs_status kvs_blocks_init_free(kvs_pool* pool, const int32_t* refcount_dev, int32_t* free_ids_dev,
+                                int32_t* n_free_dev, void* ws, size_t ws_bytes, cudaStream_t stream);
+kvs_status kvs_block_write(kvs_pool* pool, int32_t* block_table_dev, int32_t max_blocks, int32_t n_seq,
+                           const int32_t* write_seq_dev, const int32_t* write_block_dev, int32_t n_writes,
+                           int32_t* refcount_dev, int32_t* free_ids_dev, int32_t* n_free_dev, void* ws,
+                           size_t ws_bytes, cudaStream_t stream);
+kvs_status kvs_seq_release(kvs_pool* pool, int32_t* block_table_dev, int32_t max_blocks, int32_t* seq_len_dev,
+                           int32_t n_seq, const int32_t* release_seq_dev, int32_t n_release,
+                           int32_t* refcount_dev, int32_t* free_ids_dev, int32_t* n_free_dev, void* ws,
+                           size_t ws_bytes, cudaStream_t stream);
+
 /* Workspace bytes for an operation with the given call shape. */
 #define KVS_OP_DEDUP 0
 #define KVS_OP_DECODE_ATTN 1
 #define KVS_OP_DECODE_ATTN_Q4 2
 #define KVS_OP_SELECT 3
 #define KVS_OP_MIRROR 4
+#define KVS_OP_BLOCKS 5   /* n_seq = n_items = max(n_writes, n_seq); max_blocks unused */
 kvs_status kvs_workspace_size(const kvs_pool* pool, int32_t op, int32_t n_seq,
                               int32_t max_blocks, int32_t n_q_heads, size_t* bytes);
 

@@ -50,6 +50,9 @@ class BlockManager:
     def write_to_block(self, a: int, b: int) -> None:
         """The pages' write_to_block: copy-on-write when the block is shared."""
         old = int(self.table[a, b])
+        if old < 0 or old >= len(self.ref):
+            self.errors.add("block_id")
+            return
         if self.ref[old] > 1:
             if not self.free:
                 self.errors.add("capacity")

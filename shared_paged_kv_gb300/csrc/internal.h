@@ -19,6 +19,12 @@ struct kvs_pool {
   uint32_t* status = nullptr;                   // device status word (owned)
   int32_t* tickets = nullptr;                   // split-K arrival counters (owned)
   size_t n_tickets = 0;
+  // every per-layer slab that holds block contents (K, V and, for Q4, the
+  // scale/bias slabs) with its bytes per physical block, on the device
+  // (owned): what a block copy must move
+  void** blk_slabs = nullptr;
+  long long* blk_bytes = nullptr;
+  int n_blk_slabs = 0;
 };
 
 namespace kvs {
@@ -67,5 +73,8 @@ constexpr int kTmMaxGroup = 8;
 
 // Mirror construction (mirror.cu).
 size_t mirror_workspace_bytes(int n_seq, int max_blocks);
+
+// Block lifetime (blocks.cu).
+size_t blocks_workspace_bytes(int capacity, int n_items);
 
 }  // namespace kvs

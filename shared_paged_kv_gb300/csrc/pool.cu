@@ -207,6 +207,31 @@ kvs_status kvs_pool_create(const kvs_pool_desc* d, void* const* k_layers, void* 
       return fail(KVS_ERR_CUDA, "pool_create: cuTensorMapEncodeTiled failed");
     }
   }
+  // slabs a block copy moves, with their bytes per physical block
+  std::vector<void*> slabs;
+  std::vector<long long> sbytes;
+  const long long per_block_rows = static_cast<long long>(d->num_kv_heads) * d->block_tokens;
+  for (int l = 0; l < L; ++l) {
+    const long long row = q4 ? d->head_dim / 2 : d->head_dim * 2;
+    slabs.push_back(p->k[l]); sbytes.push_back(per_block_rows * row);
+    slabs.push_back(p->v[l]); sbytes.push_back(per_block_rows * row);
+    if (q4) {
+      const long long sb = (d->head_dim / 64) * 4;   // fp16 scale + bias per 64-element group
+      slabs.push_back(p->ksb[l]); sbytes.push_back(per_block_rows * sb);
+      slabs.push_back(p->vsb[l]); sbytes.push_back(per_block_rows * sb);
+    }
+  }
+  p->n_blk_slabs = static_cast<int>(slabs.size());
+  if (cudaMalloc(&p->blk_slabs, slabs.size() * sizeof(void*)) != cudaSuccess ||
+      cudaMalloc(&p->blk_bytes, sbytes.size() * sizeof(long long)) != cudaSuccess ||
+      cudaMemcpy(p->blk_slabs, slabs.data(), slabs.size() * sizeof(void*), cudaMemcpyHostToDevice) != cudaSuccess ||
+      cudaMemcpy(p->blk_bytes, sbytes.data(), sbytes.size() * sizeof(long long), cudaMemcpyHostToDevice) !=
+          cudaSuccess) {
+    cudaFree(p->blk_slabs);
+    cudaFree(p->blk_bytes);
+    delete p;
+    return fail(KVS_ERR_CUDA, "pool_create: cannot allocate the slab list");
+  }
   p->n_tickets = static_cast<size_t>(d->max_seqs) * d->num_kv_heads;
   if (cudaMalloc(&p->status, 16) != cudaSuccess ||
       cudaMalloc(&p->tickets, p->n_tickets * sizeof(int32_t)) != cudaSuccess ||
@@ -214,6 +239,8 @@ kvs_status kvs_pool_create(const kvs_pool_desc* d, void* const* k_layers, void* 
       cudaMemset(p->tickets, 0, p->n_tickets * sizeof(int32_t)) != cudaSuccess) {
     cudaFree(p->status);
     cudaFree(p->tickets);
+    cudaFree(p->blk_slabs);
+    cudaFree(p->blk_bytes);
     delete p;
     return fail(KVS_ERR_CUDA, "pool_create: cannot allocate the status word / counters");
   }
@@ -225,6 +252,8 @@ kvs_status kvs_pool_destroy(kvs_pool* p) {
   if (!p) return fail(KVS_ERR_INVALID_ARG, "pool_destroy: null pool");
   cudaFree(p->status);
   cudaFree(p->tickets);
+  cudaFree(p->blk_slabs);
+  cudaFree(p->blk_bytes);
   delete p;
   return KVS_OK;
 }
@@ -264,6 +293,9 @@ kvs_status kvs_workspace_size(const kvs_pool* p, int32_t op, int32_t n_seq, int3
     }
     case KVS_OP_MIRROR:
       b = mirror_workspace_bytes(n_seq, max_blocks);
+      break;
+    case KVS_OP_BLOCKS:
+      b = blocks_workspace_bytes(p->desc.capacity_blocks, n_seq);
       break;
     default:
       return fail(KVS_ERR_INVALID_ARG, "workspace_size: unknown op");

@@ -32,16 +32,18 @@ KVS_DEVERR_WAIT_TIMEOUT = 0x10
 KVS_DEVERR_ROPE_RANGE = 0x20
 KVS_DEVERR_JOB = 0x40
 KVS_DEVERR_PLAN = 0x80
+KVS_DEVERR_REFCOUNT = 0x100
 
 KVS_DTYPE_BF16 = 0
 KVS_DTYPE_Q4G64 = 1
 KVS_DEDUP_TEST_WEAK_KEYS = 0x1
-KVS_OP_DEDUP, KVS_OP_DECODE_ATTN, KVS_OP_DECODE_ATTN_Q4, KVS_OP_SELECT, KVS_OP_MIRROR = 0, 1, 2, 3, 4
+KVS_OP_DEDUP, KVS_OP_DECODE_ATTN, KVS_OP_DECODE_ATTN_Q4, KVS_OP_SELECT, KVS_OP_MIRROR, KVS_OP_BLOCKS = 0, 1, 2, 3, 4, 5
 
 EXPORTED = [
     "kvs_pool_create", "kvs_pool_destroy", "kvs_fingerprint_dedup", "kvs_rope_rerotate",
     "kvs_select_critical", "kvs_select_critical_noalloc", "kvs_decode_plan", "kvs_decode_attn_planned",
     "kvs_decode_attn", "kvs_decode_attn_q4", "kvs_quantize_q4", "kvs_mirror_build",
+    "kvs_blocks_init_free", "kvs_block_write", "kvs_seq_release",
     "kvs_workspace_size", "kvs_pool_check", "kvs_pool_stats", "kvs_last_error_string",
     "kvs_launch_count",
 ]
@@ -85,6 +87,9 @@ def load(path: str = LIB_PATH):
         "kvs_select_critical": [P, P, P, I32, I32, I32, F32, P, P, P, SZ, P],
         "kvs_select_critical_noalloc": [P, P, P, I32, I32, I32, F32, P, P, P],
         "kvs_mirror_build": [P, I32, P, I32, P, I32, P, P, P, P, P, P, F32, P, P, P, SZ, P],
+        "kvs_blocks_init_free": [P, P, P, P, P, SZ, P],
+        "kvs_block_write": [P, P, I32, I32, P, P, I32, P, P, P, P, SZ, P],
+        "kvs_seq_release": [P, P, I32, P, I32, P, I32, P, P, P, P, SZ, P],
         "kvs_decode_attn": [P, I32, P, I32, P, I32, P, I32, P, P, P, F32, F32, P, P, SZ, P],
         "kvs_decode_attn_planned": [P, I32, P, I32, P, I32, P, I32, P, P, P, F32, F32, P, P, SZ, P],
         "kvs_decode_plan": [P, I32, P, I32, P, I32, P, P, P, P, SZ, P],
@@ -203,6 +208,28 @@ def kvs_mirror_build(pool: Pool, layer, block_table, max_blocks, seq_len, n_seq,
                                    _ptr(idx_off), _ptr(k_new), _ptr(v_new), _ptr(rope_off), _ptr(rope_segs), theta,
                                    _ptr(diff_table), _ptr(n_diff), _ptr(ws), ws.numel() * ws.element_size(),
                                    _stream(stream)))
+
+
+def kvs_blocks_init_free(pool: Pool, refcount, free_ids, n_free, ws, stream=None):
+    """Free stack = every block whose reference count is 0 (smallest id on top)."""
+    _check(load().kvs_blocks_init_free(pool.handle, _ptr(refcount), _ptr(free_ids), _ptr(n_free), _ptr(ws),
+                                       ws.numel() * ws.element_size(), _stream(stream)))
+
+
+def kvs_block_write(pool: Pool, block_table, max_blocks, n_seq, write_seq, write_block, n_writes, refcount,
+                    free_ids, n_free, ws, stream=None):
+    """Copy-on-write for a batch of block writes, applied in list order."""
+    _check(load().kvs_block_write(pool.handle, _ptr(block_table), max_blocks, n_seq, _ptr(write_seq),
+                                  _ptr(write_block), n_writes, _ptr(refcount), _ptr(free_ids), _ptr(n_free), _ptr(ws),
+                                  ws.numel() * ws.element_size(), _stream(stream)))
+
+
+def kvs_seq_release(pool: Pool, block_table, max_blocks, seq_len, n_seq, release_seq, n_release, refcount,
+                    free_ids, n_free, ws, stream=None):
+    """Destroy sequences: decrement their blocks' counts, reclaim the zeros."""
+    _check(load().kvs_seq_release(pool.handle, _ptr(block_table), max_blocks, _ptr(seq_len), n_seq,
+                                  _ptr(release_seq), n_release, _ptr(refcount), _ptr(free_ids), _ptr(n_free),
+                                  _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)))
 
 
 def kvs_select_critical_noalloc(k_cached, k_new, row_off, n_agents, max_rows_per_agent, row_elems, ratio,

@@ -119,3 +119,9 @@ def test_copy_without_free_blocks_is_an_error():
     m = OB.BlockManager(np.array([[0], [0]], np.int32), np.array([16, 16]), np.array([2]), 16)
     m.write_batch([0], [0])
     assert "capacity" in m.errors and m.table.tolist() == [[0], [0]]
+
+
+def test_write_to_an_unmapped_block_is_an_error():
+    m = OB.BlockManager(np.array([[0, -1]], np.int32), np.array([16]), np.array([1, 0]), 16)
+    m.write_batch([0], [1])
+    assert "block_id" in m.errors and m.table.tolist() == [[0, -1]]
