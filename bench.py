@@ -53,7 +53,7 @@ def parse():
     ap.add_argument("--no-rope", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--layers", type=int, default=32)
-    ap.add_argument("--workload", default="mha7b", choices=["mha7b", "tiny", "gqa_fanout", "allgather", "q4", "select", "mirror"],
+    ap.add_argument("--workload", default="mha7b", choices=["mha7b", "tiny", "gqa_fanout", "allgather", "q4", "select", "mirror", "cow"],
                     help="mha7b is the headline workload; the others print a per-workload record for profiling")
     return ap.parse_args()
 
@@ -553,6 +553,68 @@ def bench_mirror(args, torch, K, W, dev, stream):
     return 0
 
 
+def bench_cow(args, torch, K, W, dev, stream):
+    """Copy-on-write burst on the 7B multi-head tables (32 layers x 32 KV
+    heads): agent 0 writes into all 614 shared blocks, so each is copied (K
+    and V of every layer, 8 MiB per block); then all 8 sequences are
+    released.  Tables, counts and the free stack are restored before every
+    timed call, outside the timed region."""
+    w = W.make_mha7b(n_layers=1)
+    N, L, H, D = w.n_seq, 32, 32, 128
+    tokens = torch.from_numpy(w.tokens.view(np.int32)).to(dev)
+    seq_off = torch.from_numpy(w.seq_off).to(dev)
+    cap = 614 + N * 410 + 614
+    ks = [torch.zeros((cap, H, 16, D), dtype=torch.int16, device=dev) for _ in range(L)]
+    vs = [torch.zeros_like(ks[0]) for _ in range(L)]
+    pool = K.kvs_pool_create(L, H, D, 16, K.KVS_DTYPE_BF16, cap, N, ks, vs)
+    fp = torch.zeros((N, w.max_blocks), dtype=torch.int64, device=dev)
+    table0 = torch.zeros((N, w.max_blocks), dtype=torch.int32, device=dev)
+    ref0 = torch.zeros(cap, dtype=torch.int32, device=dev)
+    nphys = torch.zeros(1, dtype=torch.int32, device=dev)
+    ws_d = torch.zeros(K.kvs_workspace_size(pool, K.KVS_OP_DEDUP, N, w.max_blocks), dtype=torch.uint8, device=dev)
+    K.kvs_fingerprint_dedup(pool, tokens, seq_off, N, None, None, None, fp, table0, w.max_blocks, ref0, nphys, ws_d)
+    ws = torch.zeros(K.kvs_workspace_size(pool, K.KVS_OP_BLOCKS, 1024, 0), dtype=torch.uint8, device=dev)
+    free0 = torch.zeros(cap, dtype=torch.int32, device=dev)
+    nfree0 = torch.zeros(1, dtype=torch.int32, device=dev)
+    K.kvs_blocks_init_free(pool, ref0, free0, nfree0, ws)
+    table, ref, free, nfree = table0.clone(), ref0.clone(), free0.clone(), nfree0.clone()
+    sl0 = torch.from_numpy(w.seq_len).to(dev)
+    sl = sl0.clone()
+    wseq = torch.zeros(614, dtype=torch.int32, device=dev)
+    wblk = torch.arange(614, dtype=torch.int32, device=dev)
+    rel = torch.arange(N, dtype=torch.int32, device=dev)
+
+    def restore():
+        table.copy_(table0); ref.copy_(ref0); free.copy_(free0); nfree.copy_(nfree0); sl.copy_(sl0)
+
+    times_w, times_r = [], []
+    for it in range(args.warmup + args.steps):
+        restore()
+        torch.cuda.synchronize()
+        e0, e1, e2 = (torch.cuda.Event(enable_timing=True) for _ in range(3))
+        e0.record(stream)
+        K.kvs_block_write(pool, table, w.max_blocks, N, wseq, wblk, 614, ref, free, nfree, ws)
+        e1.record(stream)
+        K.kvs_seq_release(pool, table, w.max_blocks, sl, N, rel, N, ref, free, nfree, ws)
+        e2.record(stream)
+        torch.cuda.synchronize()
+        if it >= args.warmup:
+            times_w.append(e0.elapsed_time(e1))
+            times_r.append(e1.elapsed_time(e2))
+    flags = K.kvs_pool_check(pool)
+    ok = int(nfree.item()) == cap and int(ref.abs().sum().item()) == 0
+    ms_w = sum(times_w) / len(times_w)
+    ms_r = sum(times_r) / len(times_r)
+    byts = 614 * L * 2 * (H * 16 * D * 2) * 2   # every copied byte read once and written once
+    peak, _ = read_peaks()
+    print(json.dumps({"workload": "cow", "copies": 614, "bytes_per_copy": L * 2 * H * 16 * D * 2,
+                      "write_batch_ms": ms_w, "gbs": byts / (ms_w * 1e-3) / 1e9,
+                      "frac_of_measured_peak": byts / (ms_w * 1e-3) / 1e9 / peak,
+                      "release_ms": ms_r, "released_blocks": cap - 614, "all_blocks_free_after": ok,
+                      "status_flags": flags}))
+    return 0
+
+
 def bench_workload(args, torch, K, W):
     """One-GPU record for a non-headline workload: GPU dedup + decode attention
     on every layer (Q4: attention only), timed with CUDA events."""
@@ -563,6 +625,8 @@ def bench_workload(args, torch, K, W):
         return bench_select(args, torch, K, dev, stream)
     if args.workload == "mirror":
         return bench_mirror(args, torch, K, W, dev, stream)
+    if args.workload == "cow":
+        return bench_cow(args, torch, K, W, dev, stream)
     mk = {"tiny": W.make_tiny, "gqa_fanout": W.make_gqa_fanout, "allgather": W.make_allgather, "q4": W.make_q4}
     w = mk[args.workload]()
     L = min(w.n_layers, args.layers)
