@@ -53,7 +53,7 @@ def parse():
     ap.add_argument("--no-rope", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--layers", type=int, default=32)
-    ap.add_argument("--workload", default="mha7b", choices=["mha7b", "tiny", "gqa_fanout", "allgather", "q4", "select", "mirror", "cow"],
+    ap.add_argument("--workload", default="mha7b", choices=["mha7b", "tiny", "gqa_fanout", "allgather", "q4", "select", "mirror", "cow", "evict"],
                     help="mha7b is the headline workload; the others print a per-workload record for profiling")
     return ap.parse_args()
 
@@ -615,6 +615,45 @@ def bench_cow(args, torch, K, W, dev, stream):
     return 0
 
 
+def bench_evict(args, torch, K, W, dev, stream):
+    """Block-granular eviction scoring: 64 agents x 16,384 tokens (1,024
+    blocks each), five regions with the MemDecay post's suggested initial
+    scores, each agent evicting a quarter of its blocks."""
+    n, mb, B = 64, 1024, 16
+    T = mb * B
+    rng = np.random.default_rng(3)
+    region = np.full((n, T), 4, np.uint8)
+    region[:, :64] = 0
+    region[rng.random((n, T)) < 0.03] = 1
+    region[rng.random((n, T)) < 0.05] = 2
+    region[:, T - 256:] = 3
+    created = np.tile(np.arange(T, dtype=np.int32), (n, 1))
+    access = rng.poisson(1.5, size=(n, T)).astype(np.int32)
+    d16 = torch.zeros(16, dtype=torch.int16, device=dev)
+    pool = K.kvs_pool_create(1, 1, 64, B, K.KVS_DTYPE_BF16, 1, 1, [d16], [d16])
+    reg_t = torch.from_numpy(region).to(dev)
+    cr_t = torch.from_numpy(created).to(dev)
+    ac_t = torch.from_numpy(access).to(dev)
+    sl = torch.full((n,), T, dtype=torch.int32, device=dev)
+    k = torch.full((n,), mb // 4, dtype=torch.int32, device=dev)
+    scores = torch.zeros((n, mb), dtype=torch.float32, device=dev)
+    victims = torch.zeros(n * mb // 4, dtype=torch.int32, device=dev)
+    voff = torch.zeros(n + 1, dtype=torch.int64, device=dev)
+    init, decay = [100.0, 10.0, 5.0, 2.0, 1.0], [0.0, 0.0092, 0.02, 0.05, 0.1]
+
+    def run():
+        K.kvs_evict_score(pool, reg_t, cr_t, ac_t, sl, n, mb, init, decay, T + 10, k, scores, victims, voff)
+
+    flush = torch.zeros(64 << 20, dtype=torch.float32, device=dev)
+    ms = graph_replay_ms(torch, run, args.steps, flush)
+    byts = n * T * 9 + n * mb * 4 + n * mb // 4 * 4
+    print(json.dumps({"workload": "evict", "ms_per_call": ms, "blocks_scored": n * mb, "victims": n * mb // 4,
+                      "blocks_per_s": n * mb / (ms * 1e-3), "bytes": byts, "gbs": byts / (ms * 1e-3) / 1e9,
+                      "note": "9.4 MB per call: latency-bound", "l2": "flushed before every replay",
+                      "status_flags": K.kvs_pool_check(pool)}))
+    return 0
+
+
 def bench_workload(args, torch, K, W):
     """One-GPU record for a non-headline workload: GPU dedup + decode attention
     on every layer (Q4: attention only), timed with CUDA events."""
@@ -627,6 +666,8 @@ def bench_workload(args, torch, K, W):
         return bench_mirror(args, torch, K, W, dev, stream)
     if args.workload == "cow":
         return bench_cow(args, torch, K, W, dev, stream)
+    if args.workload == "evict":
+        return bench_evict(args, torch, K, W, dev, stream)
     mk = {"tiny": W.make_tiny, "gqa_fanout": W.make_gqa_fanout, "allgather": W.make_allgather, "q4": W.make_q4}
     w = mk[args.workload]()
     L = min(w.n_layers, args.layers)

@@ -360,6 +360,27 @@ kvs_status kvs_seq_release(kvs_pool* pool, int32_t* block_table_dev, int32_t max
                            int32_t* refcount_dev, int32_t* free_ids_dev, int32_t* n_free_dev, void* ws,
                            size_t ws_bytes, cudaStream_t stream);
 
+/* ---------------------------------------------------------------------------
+ * Block-granular eviction scoring ([MD] §3.2: a token's current score is its
+ * region's initial score times exp(-decay * (step - created)); §4.1 scoring
+ * code: times (1 + 0.1 ln(1 + access)) when access > 0; §5.3: whole blocks
+ * are evicted, judged by the mean score of their tokens; lowest first).
+ * region_dev uint8, created_dev int32, access_dev int32: per logical token,
+ * [n_seq][max_blocks * block_tokens] (token t of sequence a at
+ * a * max_blocks * block_tokens + t); only t < seq_len[a] is read.
+ * init / decay: host arrays of n_regions (1..16) finite non-negative floats.
+ * Writes scores_dev (float [n_seq][max_blocks]: the mean score of each
+ * logical block holding a stored token, +inf past the sequence's blocks) and,
+ * for every sequence, the min(k_dev[a], blocks) lowest-scored logical blocks
+ * (ties: the lower block index) in ascending order into victims_dev, with
+ * offsets victims_off_dev int64 [n_seq + 1].  Scores are float32; a region id
+ * >= n_regions scores 0 and sets KVS_DEVERR_JOB.  block_tokens <= 16. */
+kvs_status kvs_evict_score(kvs_pool* pool, const uint8_t* region_dev, const int32_t* created_dev,
+                           const int32_t* access_dev, const int32_t* seq_len_dev, int32_t n_seq, int32_t max_blocks,
+                           const float* init, const float* decay, int32_t n_regions, int64_t step,
+                           const int32_t* k_dev, float* scores_dev, int32_t* victims_dev, int64_t* victims_off_dev,
+                           cudaStream_t stream);
+
 /* Workspace bytes for an operation with the given call shape. */
 #define KVS_OP_DEDUP 0
 #define KVS_OP_DECODE_ATTN 1

@@ -9,6 +9,8 @@ loading fails loudly.
 from __future__ import annotations
 
 import ctypes
+
+import numpy as np
 import os
 from typing import Optional, Sequence
 
@@ -43,7 +45,7 @@ EXPORTED = [
     "kvs_pool_create", "kvs_pool_destroy", "kvs_fingerprint_dedup", "kvs_rope_rerotate",
     "kvs_select_critical", "kvs_select_critical_noalloc", "kvs_decode_plan", "kvs_decode_attn_planned",
     "kvs_decode_attn", "kvs_decode_attn_q4", "kvs_quantize_q4", "kvs_mirror_build",
-    "kvs_blocks_init_free", "kvs_block_write", "kvs_seq_release",
+    "kvs_blocks_init_free", "kvs_block_write", "kvs_seq_release", "kvs_evict_score",
     "kvs_workspace_size", "kvs_pool_check", "kvs_pool_stats", "kvs_last_error_string",
     "kvs_launch_count",
 ]
@@ -90,6 +92,7 @@ def load(path: str = LIB_PATH):
         "kvs_blocks_init_free": [P, P, P, P, P, SZ, P],
         "kvs_block_write": [P, P, I32, I32, P, P, I32, P, P, P, P, SZ, P],
         "kvs_seq_release": [P, P, I32, P, I32, P, I32, P, P, P, P, SZ, P],
+        "kvs_evict_score": [P, P, P, P, P, I32, I32, P, P, I32, I64, P, P, P, P, P],
         "kvs_decode_attn": [P, I32, P, I32, P, I32, P, I32, P, P, P, F32, F32, P, P, SZ, P],
         "kvs_decode_attn_planned": [P, I32, P, I32, P, I32, P, I32, P, P, P, F32, F32, P, P, SZ, P],
         "kvs_decode_plan": [P, I32, P, I32, P, I32, P, P, P, P, SZ, P],
@@ -230,6 +233,17 @@ def kvs_seq_release(pool: Pool, block_table, max_blocks, seq_len, n_seq, release
     _check(load().kvs_seq_release(pool.handle, _ptr(block_table), max_blocks, _ptr(seq_len), n_seq,
                                   _ptr(release_seq), n_release, _ptr(refcount), _ptr(free_ids), _ptr(n_free),
                                   _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)))
+
+
+def kvs_evict_score(pool: Pool, region, created, access, seq_len, n_seq, max_blocks, init, decay, step, k, scores,
+                    victims, victims_off, stream=None):
+    """Block scores and per-sequence lowest-scored victim blocks.  init and
+    decay are host sequences of floats (one per region)."""
+    init_a = np.ascontiguousarray(init, dtype=np.float32)
+    decay_a = np.ascontiguousarray(decay, dtype=np.float32)
+    _check(load().kvs_evict_score(pool.handle, _ptr(region), _ptr(created), _ptr(access), _ptr(seq_len), n_seq,
+                                  max_blocks, init_a.ctypes.data, decay_a.ctypes.data, len(init_a), int(step), _ptr(k),
+                                  _ptr(scores), _ptr(victims), _ptr(victims_off), _stream(stream)))
 
 
 def kvs_select_critical_noalloc(k_cached, k_new, row_off, n_agents, max_rows_per_agent, row_elems, ratio,
