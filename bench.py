@@ -53,7 +53,7 @@ def parse():
     ap.add_argument("--no-rope", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--layers", type=int, default=32)
-    ap.add_argument("--workload", default="mha7b", choices=["mha7b", "tiny", "gqa_fanout", "allgather", "q4", "select", "mirror", "cow", "evict"],
+    ap.add_argument("--workload", default="mha7b", choices=["mha7b", "tiny", "gqa_fanout", "allgather", "q4", "select", "mirror", "cow", "evict", "io"],
                     help="mha7b is the headline workload; the others print a per-workload record for profiling")
     return ap.parse_args()
 
@@ -654,6 +654,38 @@ def bench_evict(args, torch, K, W, dev, stream):
     return 0
 
 
+def bench_io(args, torch, K, W, dev, stream):
+    """Export and import of the Q4 configuration's whole pool: 12 agents x 32
+    blocks of 256 tokens, 32 layers x 8 KV heads (codes and scale/bias), the
+    device side of saving and reloading a persistent Q4 cache."""
+    w = W.make_q4(n_layers=1)
+    L, H, cap = 32, w.n_kv_heads, w.capacity_blocks
+    g = torch.Generator(device=dev).manual_seed(4)
+    codes = [torch.randint(0, 256, (cap, H, 256, 64), generator=g, device=dev, dtype=torch.int32).to(torch.uint8)
+             for _ in range(2 * L)]
+    sbs = [torch.randn((cap, H, 256, 4), generator=g, device=dev).to(torch.float16) for _ in range(2 * L)]
+    pool = K.kvs_pool_create(L, H, 128, 256, K.KVS_DTYPE_Q4G64, 2 * cap, w.n_seq,
+                             [torch.cat([c, torch.zeros_like(c)]) for c in codes[0::2]],
+                             [torch.cat([c, torch.zeros_like(c)]) for c in codes[1::2]],
+                             [torch.cat([s_, torch.zeros_like(s_)]) for s_ in sbs[0::2]],
+                             [torch.cat([s_, torch.zeros_like(s_)]) for s_ in sbs[1::2]])
+    del codes, sbs
+    rec = K.kvs_pool_block_bytes(pool)
+    packed = torch.zeros(cap * rec, dtype=torch.uint8, device=dev)
+    src = torch.arange(cap, dtype=torch.int32, device=dev)
+    dst = src + cap
+    flush = torch.zeros(64 << 20, dtype=torch.float32, device=dev)
+    ms_e = graph_replay_ms(torch, lambda: K.kvs_pool_export(pool, src, cap, packed), args.steps, flush)
+    ms_i = graph_replay_ms(torch, lambda: K.kvs_pool_import(pool, dst, cap, packed), args.steps, flush)
+    byts = 2 * cap * rec
+    peak, _ = read_peaks()
+    print(json.dumps({"workload": "io", "blocks": cap, "record_bytes": rec, "export_ms": ms_e, "import_ms": ms_i,
+                      "export_gbs": byts / (ms_e * 1e-3) / 1e9, "import_gbs": byts / (ms_i * 1e-3) / 1e9,
+                      "frac_of_measured_peak": [byts / (ms_e * 1e-3) / 1e9 / peak, byts / (ms_i * 1e-3) / 1e9 / peak],
+                      "status_flags": K.kvs_pool_check(pool)}))
+    return 0
+
+
 def bench_workload(args, torch, K, W):
     """One-GPU record for a non-headline workload: GPU dedup + decode attention
     on every layer (Q4: attention only), timed with CUDA events."""
@@ -668,6 +700,8 @@ def bench_workload(args, torch, K, W):
         return bench_cow(args, torch, K, W, dev, stream)
     if args.workload == "evict":
         return bench_evict(args, torch, K, W, dev, stream)
+    if args.workload == "io":
+        return bench_io(args, torch, K, W, dev, stream)
     mk = {"tiny": W.make_tiny, "gqa_fanout": W.make_gqa_fanout, "allgather": W.make_allgather, "q4": W.make_q4}
     w = mk[args.workload]()
     L = min(w.n_layers, args.layers)

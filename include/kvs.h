@@ -381,6 +381,24 @@ kvs_status kvs_evict_score(kvs_pool* pool, const uint8_t* region_dev, const int3
                            const int32_t* k_dev, float* scores_dev, int32_t* victims_dev, int64_t* victims_off_dev,
                            cudaStream_t stream);
 
+/* ---------------------------------------------------------------------------
+ * Block export / import ([Q4] §2.1: each agent's cache is kept as fixed-size
+ * Q4 blocks in a persistent file and survives restarts; §2.2: the blocks are
+ * loaded straight back into attention, without re-prefill; the file itself
+ * is the caller's).  A packed record of one physical block holds, layer by
+ * layer, its K then V bytes (Q4 pools: K codes, V codes, K scale/bias,
+ * V scale/bias), each as stored in the slab; kvs_pool_block_bytes gives the
+ * record size.  kvs_pool_export writes the records of blocks_dev[0 ..
+ * n_blocks) to dst_dev in list order; kvs_pool_import writes records from
+ * src_dev into those blocks (e.g. blocks taken off the free stack).  Buffers
+ * are device memory, 16-byte aligned, >= n_blocks records; a block id out of
+ * range sets KVS_DEVERR_BLOCK_ID and is skipped. */
+kvs_status kvs_pool_block_bytes(const kvs_pool* pool, size_t* bytes);
+kvs_status kvs_pool_export(kvs_pool* pool, const int32_t* blocks_dev, int32_t n_blocks, void* dst_dev,
+                           size_t dst_bytes, cudaStream_t stream);
+kvs_status kvs_pool_import(kvs_pool* pool, const int32_t* blocks_dev, int32_t n_blocks, const void* src_dev,
+                           size_t src_bytes, cudaStream_t stream);
+
 /* Workspace bytes for an operation with the given call shape. */
 #define KVS_OP_DEDUP 0
 #define KVS_OP_DECODE_ATTN 1

@@ -305,9 +305,62 @@ __global__ void __launch_bounds__(256) rel_dec(const __grid_constant__ RelParams
   }
 }
 
+// ---------------------------------------------------------- export/import ---
+// blockIdx.x: listed block i; blockIdx.y: slab.  to_pack: slab -> record.
+__global__ void __launch_bounds__(256) pool_io(void** slabs, const long long* sbytes, const long long* soffs,
+                                               const int32_t* blocks, int n_blocks, long long record, uint8_t* packed,
+                                               int capacity, bool to_pack, uint32_t* status) {
+  const int i = blockIdx.x;
+  const int ph = blocks[i];
+  if (ph < 0 || ph >= capacity) {
+    if (threadIdx.x == 0 && blockIdx.y == 0) set_err(status, KVS_DEVERR_BLOCK_ID);
+    return;
+  }
+  const long long nb = sbytes[blockIdx.y];
+  uint4* slab = reinterpret_cast<uint4*>(static_cast<uint8_t*>(slabs[blockIdx.y]) + (long long)ph * nb);
+  uint4* rec = reinterpret_cast<uint4*>(packed + (long long)i * record + soffs[blockIdx.y]);
+  if (to_pack)
+    for (long long v = threadIdx.x; v < nb / 16; v += blockDim.x) rec[v] = __ldg(slab + v);
+  else
+    for (long long v = threadIdx.x; v < nb / 16; v += blockDim.x) slab[v] = __ldg(rec + v);
+}
+
 }  // namespace kvs
 
 using namespace kvs;
+
+static kvs_status pool_io_call(kvs_pool* pool, const int32_t* blocks, int32_t n_blocks, void* buf, size_t bytes,
+                               bool to_pack, cudaStream_t stream, const char* what) {
+  if (!pool) return fail(KVS_ERR_INVALID_ARG, std::string(what) + ": null pool");
+  if (n_blocks < 0) return fail(KVS_ERR_INVALID_ARG, std::string(what) + ": bad n_blocks");
+  if (n_blocks == 0) return KVS_OK;
+  if (!blocks || !buf) return fail(KVS_ERR_INVALID_ARG, std::string(what) + ": null pointer");
+  if (!aligned16(buf)) return fail(KVS_ERR_INVALID_ARG, std::string(what) + ": buffer must be 16-byte aligned");
+  if (bytes < (size_t)n_blocks * (size_t)pool->blk_record) return fail(KVS_ERR_CAPACITY, std::string(what) + ": buffer too small");
+  if (pool->n_blk_slabs > 65535) return fail(KVS_ERR_UNSUPPORTED, std::string(what) + ": too many layers");
+  pool_io<<<dim3(n_blocks, pool->n_blk_slabs), 256, 0, stream>>>(pool->blk_slabs, pool->blk_bytes, pool->blk_offs,
+                                                                 blocks, n_blocks, pool->blk_record,
+                                                                 static_cast<uint8_t*>(buf), pool->desc.capacity_blocks,
+                                                                 to_pack, pool->status);
+  count_launch();
+  return check_launch(what);
+}
+
+extern "C" kvs_status kvs_pool_block_bytes(const kvs_pool* pool, size_t* bytes) {
+  if (!pool || !bytes) return fail(KVS_ERR_INVALID_ARG, "pool_block_bytes: null argument");
+  *bytes = (size_t)pool->blk_record;
+  return KVS_OK;
+}
+
+extern "C" kvs_status kvs_pool_export(kvs_pool* pool, const int32_t* blocks_dev, int32_t n_blocks, void* dst_dev,
+                                      size_t dst_bytes, cudaStream_t stream) {
+  return pool_io_call(pool, blocks_dev, n_blocks, dst_dev, dst_bytes, true, stream, "pool_export");
+}
+
+extern "C" kvs_status kvs_pool_import(kvs_pool* pool, const int32_t* blocks_dev, int32_t n_blocks, const void* src_dev,
+                                      size_t src_bytes, cudaStream_t stream) {
+  return pool_io_call(pool, blocks_dev, n_blocks, const_cast<void*>(src_dev), src_bytes, false, stream, "pool_import");
+}
 
 static kvs_status blk_common(const kvs_pool* pool, const int32_t* refcount, const int32_t* free_ids,
                              const int32_t* n_free, const void* ws, const char* what) {

@@ -24,7 +24,9 @@ struct kvs_pool {
   // (owned): what a block copy must move
   void** blk_slabs = nullptr;
   long long* blk_bytes = nullptr;
+  long long* blk_offs = nullptr;   // offset of each slab's bytes inside one packed block record
   int n_blk_slabs = 0;
+  long long blk_record = 0;        // bytes of one packed block record (all slabs)
 };
 
 namespace kvs {

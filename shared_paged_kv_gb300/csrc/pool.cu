@@ -221,14 +221,24 @@ kvs_status kvs_pool_create(const kvs_pool_desc* d, void* const* k_layers, void* 
       slabs.push_back(p->vsb[l]); sbytes.push_back(per_block_rows * sb);
     }
   }
+  std::vector<long long> soffs(sbytes.size());
+  long long rec = 0;
+  for (size_t i = 0; i < sbytes.size(); ++i) {
+    soffs[i] = rec;
+    rec += sbytes[i];
+  }
   p->n_blk_slabs = static_cast<int>(slabs.size());
+  p->blk_record = rec;
   if (cudaMalloc(&p->blk_slabs, slabs.size() * sizeof(void*)) != cudaSuccess ||
       cudaMalloc(&p->blk_bytes, sbytes.size() * sizeof(long long)) != cudaSuccess ||
+      cudaMalloc(&p->blk_offs, soffs.size() * sizeof(long long)) != cudaSuccess ||
       cudaMemcpy(p->blk_slabs, slabs.data(), slabs.size() * sizeof(void*), cudaMemcpyHostToDevice) != cudaSuccess ||
       cudaMemcpy(p->blk_bytes, sbytes.data(), sbytes.size() * sizeof(long long), cudaMemcpyHostToDevice) !=
-          cudaSuccess) {
+          cudaSuccess ||
+      cudaMemcpy(p->blk_offs, soffs.data(), soffs.size() * sizeof(long long), cudaMemcpyHostToDevice) != cudaSuccess) {
     cudaFree(p->blk_slabs);
     cudaFree(p->blk_bytes);
+    cudaFree(p->blk_offs);
     delete p;
     return fail(KVS_ERR_CUDA, "pool_create: cannot allocate the slab list");
   }
@@ -241,6 +251,7 @@ kvs_status kvs_pool_create(const kvs_pool_desc* d, void* const* k_layers, void* 
     cudaFree(p->tickets);
     cudaFree(p->blk_slabs);
     cudaFree(p->blk_bytes);
+    cudaFree(p->blk_offs);
     delete p;
     return fail(KVS_ERR_CUDA, "pool_create: cannot allocate the status word / counters");
   }
@@ -254,6 +265,7 @@ kvs_status kvs_pool_destroy(kvs_pool* p) {
   cudaFree(p->tickets);
   cudaFree(p->blk_slabs);
   cudaFree(p->blk_bytes);
+  cudaFree(p->blk_offs);
   delete p;
   return KVS_OK;
 }

@@ -46,6 +46,7 @@ EXPORTED = [
     "kvs_select_critical", "kvs_select_critical_noalloc", "kvs_decode_plan", "kvs_decode_attn_planned",
     "kvs_decode_attn", "kvs_decode_attn_q4", "kvs_quantize_q4", "kvs_mirror_build",
     "kvs_blocks_init_free", "kvs_block_write", "kvs_seq_release", "kvs_evict_score",
+    "kvs_pool_block_bytes", "kvs_pool_export", "kvs_pool_import",
     "kvs_workspace_size", "kvs_pool_check", "kvs_pool_stats", "kvs_last_error_string",
     "kvs_launch_count",
 ]
@@ -93,6 +94,9 @@ def load(path: str = LIB_PATH):
         "kvs_block_write": [P, P, I32, I32, P, P, I32, P, P, P, P, SZ, P],
         "kvs_seq_release": [P, P, I32, P, I32, P, I32, P, P, P, P, SZ, P],
         "kvs_evict_score": [P, P, P, P, P, I32, I32, P, P, I32, I64, P, P, P, P, P],
+        "kvs_pool_block_bytes": [P, ctypes.POINTER(SZ)],
+        "kvs_pool_export": [P, P, I32, P, SZ, P],
+        "kvs_pool_import": [P, P, I32, P, SZ, P],
         "kvs_decode_attn": [P, I32, P, I32, P, I32, P, I32, P, P, P, F32, F32, P, P, SZ, P],
         "kvs_decode_attn_planned": [P, I32, P, I32, P, I32, P, I32, P, P, P, F32, F32, P, P, SZ, P],
         "kvs_decode_plan": [P, I32, P, I32, P, I32, P, P, P, P, SZ, P],
@@ -244,6 +248,25 @@ def kvs_evict_score(pool: Pool, region, created, access, seq_len, n_seq, max_blo
     _check(load().kvs_evict_score(pool.handle, _ptr(region), _ptr(created), _ptr(access), _ptr(seq_len), n_seq,
                                   max_blocks, init_a.ctypes.data, decay_a.ctypes.data, len(init_a), int(step), _ptr(k),
                                   _ptr(scores), _ptr(victims), _ptr(victims_off), _stream(stream)))
+
+
+def kvs_pool_block_bytes(pool: Pool) -> int:
+    """Bytes of one packed block record (every layer's slabs)."""
+    b = ctypes.c_size_t(0)
+    _check(load().kvs_pool_block_bytes(pool.handle, ctypes.byref(b)))
+    return b.value
+
+
+def kvs_pool_export(pool: Pool, blocks, n_blocks, dst, stream=None):
+    """Pack the listed physical blocks (all layers) into dst, in list order."""
+    _check(load().kvs_pool_export(pool.handle, _ptr(blocks), n_blocks, _ptr(dst), dst.numel() * dst.element_size(),
+                                  _stream(stream)))
+
+
+def kvs_pool_import(pool: Pool, blocks, n_blocks, src, stream=None):
+    """Unpack records from src into the listed physical blocks."""
+    _check(load().kvs_pool_import(pool.handle, _ptr(blocks), n_blocks, _ptr(src), src.numel() * src.element_size(),
+                                  _stream(stream)))
 
 
 def kvs_select_critical_noalloc(k_cached, k_new, row_off, n_agents, max_rows_per_agent, row_elems, ratio,
