@@ -399,6 +399,16 @@ kvs_status kvs_pool_export(kvs_pool* pool, const int32_t* blocks_dev, int32_t n_
 kvs_status kvs_pool_import(kvs_pool* pool, const int32_t* blocks_dev, int32_t n_blocks, const void* src_dev,
                            size_t src_bytes, cudaStream_t stream);
 
+/* Test-only switches.  KVS_TEST_STALL_ONE_STAGE: the next kvs_decode_attn /
+ * kvs_decode_attn_planned launch with a query group <= 8 leaves one ring
+ * stage of one warp unarmed, so that warp's bounded wait runs out (about a
+ * second); it records KVS_DEVERR_WAIT_TIMEOUT, waits briefly for its other
+ * copies in flight and stops, leaving the CUDA context usable.  The flag is
+ * consumed by that launch.  It exists to test the timeout path without a
+ * device fault; nothing else sets it. */
+#define KVS_TEST_STALL_ONE_STAGE 0x1u
+kvs_status kvs_pool_set_test_flags(kvs_pool* pool, uint32_t flags);
+
 /* Workspace bytes for an operation with the given call shape. */
 #define KVS_OP_DEDUP 0
 #define KVS_OP_DECODE_ATTN 1

@@ -313,6 +313,7 @@ struct TmParams {
   uint32_t* status;
   int max_blocks, n_seq, hkv, g, hq, ib, n_chunks, R, capacity, diff_capacity;
   int mwpr;           // merge warps per output row
+  int stall_first;    // test-only (KVS_TEST_STALL_ONE_STAGE): leave one stage unarmed
   float scale_log2;
   RopeSplit rs;
 };
@@ -467,6 +468,7 @@ attn_tm_kernel(const __grid_constant__ TmParams p, const __grid_constant__ CUten
     nn_it = load_item(n_id + T);
   };
   int pend_drow = -1;   // a diff tile pair still to issue for the last block
+  bool stall_pending = blockIdx.x == 0 && warp == 0;
   auto issue = [&](int s) {   // whole warp; lane 0 issues
     uint64_t* bar = &bars[warp][s];
     uint8_t* st = wbase + s * STAGE;
@@ -510,6 +512,12 @@ attn_tm_kernel(const __grid_constant__ TmParams p, const __grid_constant__ CUten
     const bool dval = DIFF && valid && did >= 0 && did < p.diff_capacity;
     if (dval) pend_drow = (did * p.hkv + p_h) * B;
     if (lane != 0) return;
+    if (p.stall_first && stall_pending) {
+      // test-only: this stage is never armed, so its wait runs out
+      stall_pending = false;
+      st_rec[warp][s] = make_int4(ord, b | (1 << 29), mask, dlt);
+      return;
+    }
     if (!valid) {
       set_err(p.status, KVS_DEVERR_BLOCK_ID);
       st_rec[warp][s] = make_int4(ord, b | (1 << 29), mask, dlt);   // nothing loaded: skip this block
@@ -624,9 +632,14 @@ attn_tm_kernel(const __grid_constant__ TmParams p, const __grid_constant__ CUten
     }
   };
 
-  for (int i = 0;;) {
+  int i = 0;
+  bool timed_out = false;
+  for (;;) {
     const int s = i % S;
-    if (!mbar_wait_bounded(&bars[warp][s], (i / S) & 1, p.status)) break;
+    if (!mbar_wait_bounded(&bars[warp][s], (i / S) & 1, p.status)) {
+      timed_out = true;
+      break;
+    }
     const int4 srec = st_rec[warp][s];
     const int item = srec.x, bword = srec.y, emask = srec.z;
     if (item < 0) break;
@@ -634,7 +647,11 @@ attn_tm_kernel(const __grid_constant__ TmParams p, const __grid_constant__ CUten
     const int b = bword & ((1 << 29) - 1);
     const bool loaded = ((bword >> 29) & 1) == 0;
     const int s2 = (i + 1) % S;
-    if (has_diff && !mbar_wait_bounded(&bars[warp][s2], ((i + 1) / S) & 1, p.status)) break;
+    if (has_diff && !mbar_wait_bounded(&bars[warp][s2], ((i + 1) / S) & 1, p.status)) {
+      timed_out = true;
+      ++i;   // the stage at i was consumed; drain from the one that timed out
+      break;
+    }
     if (item != cur) {
       if (cur >= 0) flush();
       cur = item;
@@ -755,6 +772,11 @@ attn_tm_kernel(const __grid_constant__ TmParams p, const __grid_constant__ CUten
     issue(s);
     if (has_diff) issue(s2);
     i += has_diff ? 2 : 1;
+  }
+  if (timed_out) {
+    // the other stages may still have copies in flight: let them land (with
+    // a limit) before the shared memory goes away
+    for (int j = 1; j < S; ++j) mbar_drain(&bars[warp][(i + j) % S], ((i + j) / S) & 1);
   }
   if (cur >= 0) flush();
 }
@@ -1072,6 +1094,8 @@ kvs_status decode_attn_token_major(kvs_pool* pool, int layer, const void* q, int
   prm.mwpr = 1;
   while (prm.mwpr < kMergeWarps && prm.mwpr * kMergeBatch < L.n_chunks) prm.mwpr <<= 1;
   if (rope) rope_split_host(theta, d.head_dim, prm.rs.c);
+  prm.stall_first = (pool->test_flags & KVS_TEST_STALL_ONE_STAGE) ? 1 : 0;
+  pool->test_flags &= ~KVS_TEST_STALL_ONE_STAGE;   // one launch only
   const int max_claims = (int)std::min<size_t>(L.max_items * d.num_kv_heads, 0x7fffffff);
   if (d.head_dim == 128) {
     if (dif) return rope ? launch_tm<128, true, true>(prm, pool, layer, max_claims, stream)

@@ -59,6 +59,15 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 
 // Bounded wait: gives up after ~2^31 cycles (about a second at GB300 clocks),
 // records KVS_DEVERR_WAIT_TIMEOUT and returns false.  Never spins forever.
+// Wait for a phase with a short limit and no error report: used after a
+// timed-out wait to let the copies still in flight land before the CTA's
+// shared memory is released.
+__device__ __forceinline__ void mbar_drain(uint64_t* bar, uint32_t parity) {
+  const long long t0 = clock64();
+  while (!mbar_try_wait(bar, parity) && clock64() - t0 < (1ll << 24)) {
+  }
+}
+
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, uint32_t* status) {
   if (mbar_try_wait(bar, parity)) return true;
   const long long t0 = clock64();

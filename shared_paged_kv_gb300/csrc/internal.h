@@ -27,6 +27,7 @@ struct kvs_pool {
   long long* blk_offs = nullptr;   // offset of each slab's bytes inside one packed block record
   int n_blk_slabs = 0;
   long long blk_record = 0;        // bytes of one packed block record (all slabs)
+  uint32_t test_flags = 0;         // KVS_TEST_* (tests only)
 };
 
 namespace kvs {

@@ -316,6 +316,12 @@ kvs_status kvs_workspace_size(const kvs_pool* p, int32_t op, int32_t n_seq, int3
   return KVS_OK;
 }
 
+kvs_status kvs_pool_set_test_flags(kvs_pool* p, uint32_t flags) {
+  if (!p) return fail(KVS_ERR_INVALID_ARG, "pool_set_test_flags: null pool");
+  p->test_flags = flags;
+  return KVS_OK;
+}
+
 kvs_status kvs_pool_check(kvs_pool* p, cudaStream_t s, uint32_t* flags) {
   if (!p || !flags) return fail(KVS_ERR_INVALID_ARG, "pool_check: null argument");
   uint32_t h = 0;

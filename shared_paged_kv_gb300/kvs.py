@@ -35,6 +35,7 @@ KVS_DEVERR_ROPE_RANGE = 0x20
 KVS_DEVERR_JOB = 0x40
 KVS_DEVERR_PLAN = 0x80
 KVS_DEVERR_REFCOUNT = 0x100
+KVS_TEST_STALL_ONE_STAGE = 0x1
 
 KVS_DTYPE_BF16 = 0
 KVS_DTYPE_Q4G64 = 1
@@ -46,7 +47,7 @@ EXPORTED = [
     "kvs_select_critical", "kvs_select_critical_noalloc", "kvs_decode_plan", "kvs_decode_attn_planned",
     "kvs_decode_attn", "kvs_decode_attn_q4", "kvs_quantize_q4", "kvs_mirror_build",
     "kvs_blocks_init_free", "kvs_block_write", "kvs_seq_release", "kvs_evict_score",
-    "kvs_pool_block_bytes", "kvs_pool_export", "kvs_pool_import",
+    "kvs_pool_block_bytes", "kvs_pool_export", "kvs_pool_import", "kvs_pool_set_test_flags",
     "kvs_workspace_size", "kvs_pool_check", "kvs_pool_stats", "kvs_last_error_string",
     "kvs_launch_count",
 ]
@@ -95,6 +96,7 @@ def load(path: str = LIB_PATH):
         "kvs_seq_release": [P, P, I32, P, I32, P, I32, P, P, P, P, SZ, P],
         "kvs_evict_score": [P, P, P, P, P, I32, I32, P, P, I32, I64, P, P, P, P, P],
         "kvs_pool_block_bytes": [P, ctypes.POINTER(SZ)],
+        "kvs_pool_set_test_flags": [P, U32],
         "kvs_pool_export": [P, P, I32, P, SZ, P],
         "kvs_pool_import": [P, P, I32, P, SZ, P],
         "kvs_decode_attn": [P, I32, P, I32, P, I32, P, I32, P, P, P, F32, F32, P, P, SZ, P],
@@ -267,6 +269,11 @@ def kvs_pool_import(pool: Pool, blocks, n_blocks, src, stream=None):
     """Unpack records from src into the listed physical blocks."""
     _check(load().kvs_pool_import(pool.handle, _ptr(blocks), n_blocks, _ptr(src), src.numel() * src.element_size(),
                                   _stream(stream)))
+
+
+def kvs_pool_set_test_flags(pool: Pool, flags: int):
+    """Test-only switches (KVS_TEST_*); see include/kvs.h."""
+    _check(load().kvs_pool_set_test_flags(pool.handle, flags))
 
 
 def kvs_select_critical_noalloc(k_cached, k_new, row_off, n_agents, max_rows_per_agent, row_elems, ratio,
