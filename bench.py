@@ -58,6 +58,32 @@ def parse():
     return ap.parse_args()
 
 
+# ----------------------------------------------------------- multi-rank ----
+def rank_agents(n_per_rank: int, world: int, rank: int):
+    """Global agent ids of this rank's replica: ranks hold disjoint,
+    contiguous blocks of n_per_rank agents (weak scaling, no collective on
+    the data path)."""
+    if not 0 <= rank < world:
+        raise ValueError("rank outside the world")
+    return range(rank * n_per_rank, (rank + 1) * n_per_rank)
+
+
+def max_over_ranks(value: float, world: int, device=None) -> float:
+    """The job's time is the slowest rank's: an all-reduce MAX when world > 1."""
+    if world <= 1:
+        return float(value)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tokens_per_s(n_per_rank: int, world: int, ms_step_max: float) -> float:
+    """Whole-job decode tokens/s: every rank's agents over the slowest rank's step."""
+    return world * n_per_rank / (ms_step_max * 1e-3)
+
+
 # --------------------------------------------------------------- helpers ----
 def read_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
@@ -292,11 +318,7 @@ def main():
     if world > 1:
         dist.barrier()
     launches = K.kvs_launch_count() - launches0
-    ms = t0.elapsed_time(t1)
-    if world > 1:
-        tt = torch.tensor([ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        ms = float(tt.item())
+    ms = max_over_ranks(t0.elapsed_time(t1), world, dev)
     ms_step = ms / args.steps
     attn_ms = [ev_a[i][l].elapsed_time(ev_b[i][l]) for i in range(args.steps) for l in range(L)]
     attn_avg_ms = sum(attn_ms) / len(attn_ms)
@@ -307,7 +329,7 @@ def main():
     peak, peak_kind = read_peaks()
     achieved = attn_bytes / (attn_avg_ms * 1e-3) / 1e9
     step_bytes = L * attn_bytes + w.tokens.nbytes + N * w.max_blocks * (8 + 4)
-    value = world * N / (ms_step * 1e-3)
+    value = job_tokens_per_s(N, world, ms_step)
 
     # ---- end to end through the public API with pinned host buffers
     e2e = None
@@ -333,11 +355,13 @@ def main():
 
         for _ in range(2):
             e2e_step()
+        if world > 1:
+            dist.barrier()
         t_a = time.perf_counter()
         for _ in range(args.steps):
             e2e_step()
-        e2e_s = (time.perf_counter() - t_a) / args.steps
-        e2e = {"value": world * N / e2e_s, "unit": UNIT,
+        e2e_s = max_over_ranks((time.perf_counter() - t_a) / args.steps, world, dev)
+        e2e = {"value": job_tokens_per_s(N, world, e2e_s * 1e3), "unit": UNIT,
                "h2d_bytes_per_step": int(h_tok.numel() * 4 + h_off.numel() * 8 + h_q.numel() * 2),
                "d2h_bytes_per_step": int(h_out.numel() * 4)}
 
