@@ -73,10 +73,18 @@ __host__ __device__ constexpr int tm_smem_bytes() {
 }
 
 // ------------------------------------------------------------- plan layout
+// Sharing groups.  Without a wide tile, sequences are taken in groups of
+// R = 8 / G, so one 8-column token-major tile holds a whole group's queries.
+// With a wide tile (head_dim 128, G >= 4, no rotation), groups hold
+// W = min(32, 128 / G) sequences whose W * G query rows fill the M = 128 rows
+// of a tcgen05 tile (attn_wide.cu); the token-major kernel then takes single
+// sequences (R = 1) and only their unshared blocks.  SG is the group size
+// either way (1: no groups).
 struct TmLayout {
-  int R, ib, n_chunks, n_groups;
-  size_t max_items;
-  size_t off_hdr, off_items, off_gmask, off_gphys, off_bdelta, off_pne, off_spm, off_p1, off_p2, total;
+  int R, SG, ib, n_chunks, n_groups;
+  bool wide;
+  size_t max_items, max_witems;
+  size_t off_hdr, off_items, off_witems, off_gmask, off_gphys, off_bdelta, off_pne, off_spm, off_p1, off_p2, total;
 };
 
 static size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
@@ -98,26 +106,34 @@ int tm_item_blocks(const kvs_pool* pool, int n_seq, int max_blocks, int R) {
   return r;
 }
 
+bool tm_wide_tile(const kvs_pool* pool, int g, bool rope) {
+  return !rope && pool->desc.head_dim == 128 && g >= 4 && g <= kTmMaxGroup && !pool->tk1.empty();
+}
+
 static TmLayout tm_layout(const kvs_pool* pool, int n_seq, int max_blocks, int g, bool rope) {
   TmLayout L{};
-  L.R = rope ? 1 : std::max(1, 8 / g);
+  L.wide = tm_wide_tile(pool, g, rope);
+  L.R = (rope || L.wide) ? 1 : std::max(1, 8 / g);
+  L.SG = L.wide ? std::min(32, 128 / g) : L.R;
   L.ib = tm_item_blocks(pool, n_seq, max_blocks, L.R);
   L.n_chunks = (max_blocks + L.ib - 1) / L.ib;
-  L.n_groups = (n_seq + L.R - 1) / L.R;
-  const size_t grp = L.R > 1 ? (size_t)L.n_groups : 0;   // group arrays exist only with grouping
-  L.max_items = (grp + n_seq) * L.n_chunks;
+  L.n_groups = (n_seq + L.SG - 1) / L.SG;
+  const size_t grp = L.SG > 1 ? (size_t)L.n_groups : 0;   // group arrays exist only with grouping
+  L.max_items = ((L.wide ? 0 : grp) + n_seq) * L.n_chunks;
+  L.max_witems = L.wide ? grp * L.n_chunks : 0;
   const size_t splits = (size_t)n_seq * pool->desc.num_kv_heads * L.n_chunks;
   const size_t split_bytes = splits * g * (pool->desc.head_dim + 2) * sizeof(float);
   size_t o = 0;
   L.off_hdr = o; o = align256(o + 64);
   L.off_items = o; o = align256(o + L.max_items * sizeof(int4));
-  L.off_gmask = o; o = align256(o + grp * max_blocks);
+  L.off_witems = o; o = align256(o + L.max_witems * sizeof(int4));
+  L.off_gmask = o; o = align256(o + grp * max_blocks * sizeof(uint32_t));
   L.off_gphys = o; o = align256(o + grp * max_blocks * sizeof(int32_t));
   L.off_bdelta = o; o = align256(o + (rope ? (size_t)n_seq * max_blocks * sizeof(int32_t) : 0));
   L.off_pne = o; o = align256(o + (size_t)n_seq * L.n_chunks);
-  L.off_spm = o; o = align256(o + grp * L.n_chunks);
+  L.off_spm = o; o = align256(o + grp * L.n_chunks * sizeof(uint32_t));
   L.off_p1 = o; o = align256(o + split_bytes);
-  L.off_p2 = o; o = align256(o + (L.R > 1 ? split_bytes : 0));
+  L.off_p2 = o; o = align256(o + (L.SG > 1 ? split_bytes : 0));
   L.total = o;
   return L;
 }
@@ -129,24 +145,30 @@ size_t tm_workspace_bytes(const kvs_pool* pool, int n_seq, int max_blocks, int g
 
 // ------------------------------------------------------------------- plan
 // Items are int4 {x: kind (bit 30) | group or sequence, y: chunk, z: end
-// block (exclusive), w: member mask of the columns that take part}.
+// block (exclusive), w: member mask of the columns that take part}.  With a
+// wide tile the shared items form their own list (witems), taken by the
+// tcgen05 kernel; the token-major list then holds private items only.
+//
+// Header: [0] token-major items, [1] magic, [2] n_seq, [3] max_blocks, [4] R,
+// [5] ib, [6] hkv, [7] SG, [8] wide items.
 struct PlanParams {
   const int32_t* block_table;
   const int32_t* seq_len;
   const int32_t* diff_table;
   int* hdr;
   int4* items;
-  uint8_t* gmask;   // [n_groups][max_blocks] members computed by the group's shared item (R > 1)
-  int32_t* gphys;   // [n_groups][max_blocks] that shared physical block, or -1 (R > 1)
-  uint8_t* pne;     // [n_seq][n_chunks] private chunk has unshared work
-  uint8_t* spm;     // [n_groups][n_chunks] members taking part in the shared chunk (R > 1)
+  int4* witems;      // wide shared items (wide tile only)
+  uint32_t* gmask;   // [n_groups][max_blocks] members computed by the group's shared item (SG > 1)
+  int32_t* gphys;    // [n_groups][max_blocks] that shared physical block, or -1 (SG > 1)
+  uint8_t* pne;      // [n_seq][n_chunks] private chunk has unshared work
+  uint32_t* spm;     // [n_groups][n_chunks] members taking part in the shared chunk (SG > 1)
   const int32_t* rope_off;   // rotation calls: segment CSR
   const int4* rope_segs;
-  int32_t* bdelta;  // [n_seq][max_blocks] RoPE shift of each logical block (rotation calls)
+  int32_t* bdelta;   // [n_seq][max_blocks] RoPE shift of each logical block (rotation calls)
   uint32_t* status;
-  float* p1_ml;     // (m, l) of the private splits [n_seq][hkv][n_chunks][g]
-  float* p2_ml;     // (m, l) of the shared splits, same shape (R > 1)
-  int n_seq, max_blocks, R, G, ib, n_chunks, n_groups, capacity, hkv;
+  float* p1_ml;      // (m, l) of the private splits [n_seq][hkv][n_chunks][g]
+  float* p2_ml;      // (m, l) of the shared splits, same shape (SG > 1)
+  int n_seq, max_blocks, R, SG, G, ib, n_chunks, n_groups, capacity, hkv, wide;
 };
 
 __device__ __forceinline__ int plan_seq_blocks(const int32_t* seq_len, int a, int max_blocks) {
@@ -157,10 +179,12 @@ __device__ __forceinline__ int plan_seq_blocks(const int32_t* seq_len, int a, in
 }
 
 // Plan, part 1 (it depends on the tables only, so one plan serves every
-// layer of a decode step).  One CTA per group of R sequences:
-//  * gmask / gphys: a member's logical block is group-shared when every
-//    member that reaches it holds the same valid full physical block with no
-//    mirror diff (at least two members);
+// layer of a decode step).  One CTA per group of SG sequences:
+//  * gmask / gphys: at each logical block, the members eligible to share it
+//    (a valid full physical block, no mirror diff) are grouped by physical
+//    block; the largest such set (the earliest member's on a tie) shares the
+//    block when it has at least two members.  The others take the block in
+//    their private items;
 //  * pne / spm: which private chunks have unshared work, which members take
 //    part in each shared chunk;
 //  * the (m, l) of every split that will not be written is set to (-inf, 0),
@@ -170,43 +194,52 @@ __device__ __forceinline__ int plan_seq_blocks(const int32_t* seq_len, int a, in
 __global__ void __launch_bounds__(256) tm_plan_groups(PlanParams pp) {
   const int tid = threadIdx.x, nt = blockDim.x;
   if (blockIdx.x == 0 && tid == 0) {
-    pp.hdr[0] = 0;   // item count, accumulated by tm_plan_items
+    pp.hdr[0] = 0;   // item counts, accumulated by tm_plan_items
     pp.hdr[1] = kPlanMagic;
     pp.hdr[2] = pp.n_seq;
     pp.hdr[3] = pp.max_blocks;
     pp.hdr[4] = pp.R;
     pp.hdr[5] = pp.ib;
     pp.hdr[6] = pp.hkv;
+    pp.hdr[7] = pp.SG;
+    pp.hdr[8] = 0;
   }
   const float2 none = make_float2(-INFINITY, 0.f);
+  const int SG = pp.SG;
   for (int gi = blockIdx.x; gi < pp.n_groups; gi += gridDim.x) {
-    const int a0 = gi * pp.R, nm = min(pp.R, pp.n_seq - a0);
+    const int a0 = gi * SG, nm = min(SG, pp.n_seq - a0);
     // 1. sharing per logical block
-    if (pp.R > 1) {
+    if (SG > 1) {
       for (int b = tid; b < pp.max_blocks; b += nt) {
-        int cnt = 0, phys = -1;
-        bool ok = true;
-        uint32_t mask = 0;
+        int ph[32];
         for (int r = 0; r < nm; ++r) {
           const int a = a0 + r;
           const int L = min(max(pp.seq_len[a], 0), pp.max_blocks * 16);
-          if (b * 16 >= L) continue;
-          const int ph = pp.block_table[(size_t)a * pp.max_blocks + b];
+          const int e = pp.block_table[(size_t)a * pp.max_blocks + b];
           const bool full = (b + 1) * 16 <= L;
           const int d = pp.diff_table ? pp.diff_table[(size_t)a * pp.max_blocks + b] : -1;
-          if (!full || d >= 0 || ph < 0 || ph >= pp.capacity) ok = false;
-          if (cnt == 0) phys = ph;
-          else if (ph != phys) ok = false;
-          ++cnt;
-          mask |= 1u << r;
+          ph[r] = (full && d < 0 && e >= 0 && e < pp.capacity) ? e : -1;
         }
-        const bool sh = ok && cnt >= 2;
-        pp.gmask[(size_t)gi * pp.max_blocks + b] = sh ? (uint8_t)mask : 0;
-        pp.gphys[(size_t)gi * pp.max_blocks + b] = sh ? phys : -1;
+        // the first member of the largest set of equal physical blocks
+        int best = -1, bestc = 1;
+        for (int r = 0; r < nm; ++r) {
+          if (ph[r] < 0) continue;
+          int cnt = 0;
+          for (int r2 = r; r2 < nm; ++r2) cnt += ph[r2] == ph[r];
+          if (cnt > bestc) {
+            bestc = cnt;
+            best = ph[r];
+          }
+        }
+        uint32_t mask = 0;
+        if (best >= 0)
+          for (int r = 0; r < nm; ++r) mask |= (ph[r] == best ? 1u : 0u) << r;
+        pp.gmask[(size_t)gi * pp.max_blocks + b] = mask;
+        pp.gphys[(size_t)gi * pp.max_blocks + b] = best;
       }
       __syncthreads();
     }
-    if (pp.rope_off) {   // R == 1: the group is sequence a0
+    if (pp.rope_off) {   // SG == 1: the group is sequence a0
       const int e0 = pp.rope_off[a0], e1 = pp.rope_off[a0 + 1];
       for (int b = tid; b < pp.max_blocks; b += nt) {
         int dl = 0;
@@ -227,15 +260,15 @@ __global__ void __launch_bounds__(256) tm_plan_groups(PlanParams pp) {
       const int nb = plan_seq_blocks(pp.seq_len, a, pp.max_blocks);
       int any_priv = 0;
       for (int b = c * pp.ib; b < min((c + 1) * pp.ib, nb); ++b)
-        any_priv |= pp.R > 1 ? !((pp.gmask[(size_t)gi * pp.max_blocks + b] >> r) & 1u) : 1;
+        any_priv |= SG > 1 ? !((pp.gmask[(size_t)gi * pp.max_blocks + b] >> r) & 1u) : 1;
       pp.pne[(size_t)a * pp.n_chunks + c] = (uint8_t)any_priv;
     }
-    if (pp.R > 1) {
+    if (SG > 1) {
       for (int c = tid; c < pp.n_chunks; c += nt) {
         uint32_t m = 0;
         for (int b = c * pp.ib; b < min((c + 1) * pp.ib, pp.max_blocks); ++b)
           m |= pp.gmask[(size_t)gi * pp.max_blocks + b];
-        pp.spm[(size_t)gi * pp.n_chunks + c] = (uint8_t)m;
+        pp.spm[(size_t)gi * pp.n_chunks + c] = m;
       }
     }
     __syncthreads();
@@ -247,36 +280,36 @@ __global__ void __launch_bounds__(256) tm_plan_groups(PlanParams pp) {
       const int a = a0 + r;
       const size_t e = (size_t)a * per_seq + rem;   // [a][h][c][hh]
       if (!pp.pne[(size_t)a * pp.n_chunks + c]) reinterpret_cast<float2*>(pp.p1_ml)[e] = none;
-      if (pp.R > 1 && !((pp.spm[(size_t)gi * pp.n_chunks + c] >> r) & 1u))
+      if (SG > 1 && !((pp.spm[(size_t)gi * pp.n_chunks + c] >> r) & 1u))
         reinterpret_cast<float2*>(pp.p2_ml)[e] = none;
     }
     __syncthreads();
   }
 }
 
-// Plan, part 2: the compact item list, shared items (group, chunk) then
+// Plan, part 2: the compact item lists, shared items (group, chunk) then
 // private items (sequence, chunk), chunk-major.  Each CTA compacts a run of
-// slots and reserves its place with one atomic add, so the list is
+// slots and reserves its place with one atomic add per list, so a list is
 // chunk-major up to the interleaving of CTAs; results do not depend on the
 // order (every split has a fixed slot and a fixed merge order).
 __global__ void __launch_bounds__(256) tm_plan_items(PlanParams pp) {
   __shared__ int warp_sums[32];
-  __shared__ int s_base;
-  const int n_sh = pp.R > 1 ? pp.n_groups * pp.n_chunks : 0, n_pr = pp.n_seq * pp.n_chunks;
+  __shared__ int s_base, s_wbase;
+  const int n_sh = pp.SG > 1 ? pp.n_groups * pp.n_chunks : 0, n_pr = pp.n_seq * pp.n_chunks;
   const int total = n_sh + n_pr;
   for (int base = blockIdx.x * blockDim.x; base < total; base += gridDim.x * blockDim.x) {
     const int i = base + threadIdx.x;
-    int keep = 0;
+    int keep = 0, keep_w = 0;
     int4 item = make_int4(0, 0, 0, 0);
     if (i < n_sh) {
       const int c = i / pp.n_groups, gi = i - c * pp.n_groups;
-      const int m = pp.spm[(size_t)gi * pp.n_chunks + c];
-      keep = m != 0;
-      if (keep) {
+      const uint32_t m = pp.spm[(size_t)gi * pp.n_chunks + c];
+      if (m != 0) {
         int nb = 0;
-        for (int r = 0; r < pp.R && gi * pp.R + r < pp.n_seq; ++r)
-          nb = max(nb, plan_seq_blocks(pp.seq_len, gi * pp.R + r, pp.max_blocks));
-        item = make_int4((1 << 30) | gi, c, min((c + 1) * pp.ib, nb), m);
+        for (int r = 0; r < pp.SG && gi * pp.SG + r < pp.n_seq; ++r)
+          nb = max(nb, plan_seq_blocks(pp.seq_len, gi * pp.SG + r, pp.max_blocks));
+        item = make_int4((1 << 30) | gi, c, min((c + 1) * pp.ib, nb), (int)m);
+        if (pp.wide) keep_w = 1; else keep = 1;
       }
     } else if (i < total) {
       const int j = i - n_sh;
@@ -285,11 +318,16 @@ __global__ void __launch_bounds__(256) tm_plan_items(PlanParams pp) {
       if (keep)
         item = make_int4(a, c, min((c + 1) * pp.ib, plan_seq_blocks(pp.seq_len, a, pp.max_blocks)), 1 << (a % pp.R));
     }
-    int cnt;
+    int cnt, cnt_w = 0, pos_w = 0;
     const int pos = block_exclusive_scan(keep, warp_sums, cnt);
-    if (threadIdx.x == 0) s_base = cnt ? atomicAdd(pp.hdr, cnt) : 0;
+    if (pp.wide) pos_w = block_exclusive_scan(keep_w, warp_sums, cnt_w);
+    if (threadIdx.x == 0) {
+      s_base = cnt ? atomicAdd(pp.hdr, cnt) : 0;
+      s_wbase = cnt_w ? atomicAdd(pp.hdr + 8, cnt_w) : 0;
+    }
     __syncthreads();
     if (keep) pp.items[s_base + pos] = item;
+    if (keep_w) pp.witems[s_wbase + pos_w] = item;
     __syncthreads();
   }
 }
@@ -308,10 +346,10 @@ struct TmParams {
   float* p2_ml;
   const int* hdr;
   const int4* items;
-  const uint8_t* gmask;
+  const uint32_t* gmask;
   const int32_t* gphys;
   uint32_t* status;
-  int max_blocks, n_seq, hkv, g, hq, ib, n_chunks, R, capacity, diff_capacity;
+  int max_blocks, n_seq, hkv, g, hq, ib, n_chunks, R, SG, capacity, diff_capacity;
   int mwpr;           // merge warps per output row
   int stall_first;    // test-only (KVS_TEST_STALL_ONE_STAGE): leave one stage unarmed
   float scale_log2;
@@ -377,7 +415,7 @@ attn_tm_kernel(const __grid_constant__ TmParams p, const __grid_constant__ CUten
 
   // the plan must have been built for this call's shapes
   const bool plan_ok = p.hdr[1] == kPlanMagic && p.hdr[2] == p.n_seq && p.hdr[3] == p.max_blocks &&
-                       p.hdr[4] == p.R && p.hdr[5] == p.ib && p.hdr[6] == p.hkv;
+                       p.hdr[4] == p.R && p.hdr[5] == p.ib && p.hdr[6] == p.hkv && p.hdr[7] == p.SG;
   if (!plan_ok && threadIdx.x == 0 && blockIdx.x == 0) set_err(p.status, KVS_DEVERR_PLAN);
   const int n_claims = plan_ok ? p.hdr[0] * p.hkv : 0;
   const int R = p.R;
@@ -404,13 +442,13 @@ attn_tm_kernel(const __grid_constant__ TmParams p, const __grid_constant__ CUten
     if (kind) {
       if (in) {
         n_tab = __ldg(p.gphys + (size_t)idx * p.max_blocks + b);
-        n_aux = __ldg(p.gmask + (size_t)idx * p.max_blocks + b);
+        n_aux = (int)__ldg(p.gmask + (size_t)idx * p.max_blocks + b);
       }
       if (lane < R && idx * R + lane < p.n_seq) n_len = __ldg(p.seq_len + idx * R + lane);
     } else {
       if (in) {
         n_tab = __ldg(p.block_table + (size_t)idx * p.max_blocks + b);
-        if (R > 1) n_aux = __ldg(p.gmask + (size_t)(idx / R) * p.max_blocks + b);   // raw member bits
+        if (p.SG > 1) n_aux = (int)__ldg(p.gmask + (size_t)(idx / p.SG) * p.max_blocks + b);   // raw member bits
         if (DIFF) n_dif = __ldg(p.diff_table + (size_t)idx * p.max_blocks + b);
         if (ROPE) n_dlt = __ldg(p.bdelta + (size_t)idx * p.max_blocks + b);
       }
@@ -448,7 +486,7 @@ attn_tm_kernel(const __grid_constant__ TmParams p, const __grid_constant__ CUten
     p_b0 = p_b = it.y * p.ib;
     p_bend = it.z;
     p_mask = it.w;
-    p_slot = p_kind ? 0 : (it.x & ((1 << 30) - 1)) % R;
+    p_slot = p_kind ? 0 : (it.x & ((1 << 30) - 1)) % p.SG;
     tab_ent = n_tab;
     aux_ent = n_aux;
     dif_ent = n_dif;
@@ -803,7 +841,7 @@ __global__ void __launch_bounds__(kMergeWarps * 32, 2) tm_merge_kernel(const __g
   // the attention kernel has flagged a plan built for other shapes and
   // computed nothing; leave the output untouched as well
   const bool plan_ok = p.hdr[1] == kPlanMagic && p.hdr[2] == p.n_seq && p.hdr[3] == p.max_blocks &&
-                       p.hdr[4] == p.R && p.hdr[5] == p.ib && p.hdr[6] == p.hkv;
+                       p.hdr[4] == p.R && p.hdr[5] == p.ib && p.hdr[6] == p.hkv && p.hdr[7] == p.SG;
   const bool in_range = row < p.n_seq * p.hq;
   const int a = in_range ? row / p.hq : 0, qh = row - a * p.hq, h = qh / p.g, hh = qh - h * p.g;
   const bool live = plan_ok && in_range && p.seq_len[a] > 0;
@@ -819,7 +857,7 @@ __global__ void __launch_bounds__(kMergeWarps * 32, 2) tm_merge_kernel(const __g
     const int ck = c0 + lane;
     const bool in = ck < cend;
     mp = in ? __ldcg(reinterpret_cast<const float2*>(p.p1_ml + ((sbase + ck) * p.g + hh) * 2)) : make_float2(0.f, 0.f);
-    ms = in && p.R > 1 ? __ldcg(reinterpret_cast<const float2*>(p.p2_ml + ((sbase + ck) * p.g + hh) * 2))
+    ms = in && p.SG > 1 ? __ldcg(reinterpret_cast<const float2*>(p.p2_ml + ((sbase + ck) * p.g + hh) * 2))
                        : make_float2(0.f, 0.f);
     pv = mp.y > 0.f;
     sv_ = ms.y > 0.f;
@@ -984,10 +1022,11 @@ static kvs_status launch_tm(TmParams& prm, const kvs_pool* pool, int layer, int 
 struct TmPtrs {
   int* hdr;
   int4* items;
-  uint8_t* gmask;
+  int4* witems;
+  uint32_t* gmask;
   int32_t* gphys;
   uint8_t* pne;
-  uint8_t* spm;
+  uint32_t* spm;
   int32_t* bdelta;
   float *p1, *p1_ml, *p2, *p2_ml;
 };
@@ -998,15 +1037,16 @@ static TmPtrs tm_ptrs(const TmLayout& L, const kvs_pool* pool, int n_seq, int g,
   TmPtrs t{};
   t.hdr = reinterpret_cast<int*>(w + L.off_hdr);
   t.items = reinterpret_cast<int4*>(w + L.off_items);
-  t.gmask = w + L.off_gmask;
+  t.gmask = reinterpret_cast<uint32_t*>(w + L.off_gmask);
   t.gphys = reinterpret_cast<int32_t*>(w + L.off_gphys);
   t.pne = w + L.off_pne;
-  t.spm = w + L.off_spm;
+  t.spm = reinterpret_cast<uint32_t*>(w + L.off_spm);
+  t.witems = reinterpret_cast<int4*>(w + L.off_witems);
   t.bdelta = reinterpret_cast<int32_t*>(w + L.off_bdelta);
   t.p1 = reinterpret_cast<float*>(w + L.off_p1);
   t.p1_ml = t.p1 + split_vals;
   t.p2 = reinterpret_cast<float*>(w + L.off_p2);
-  t.p2_ml = t.p2 + (L.R > 1 ? split_vals : 0);
+  t.p2_ml = t.p2 + (L.SG > 1 ? split_vals : 0);
   return t;
 }
 
@@ -1036,6 +1076,9 @@ kvs_status decode_plan_token_major(kvs_pool* pool, int n_q_heads, const int32_t*
   pp.n_seq = n_seq;
   pp.max_blocks = max_blocks;
   pp.R = L.R;
+  pp.SG = L.SG;
+  pp.wide = L.wide ? 1 : 0;
+  pp.witems = t.witems;
   pp.G = g;
   pp.ib = L.ib;
   pp.n_chunks = L.n_chunks;
@@ -1047,7 +1090,7 @@ kvs_status decode_plan_token_major(kvs_pool* pool, int n_q_heads, const int32_t*
   count_launch();
   kvs_status st = check_launch("decode_plan");
   if (st != KVS_OK) return st;
-  const long long slots = (long long)L.max_items;
+  const long long slots = (long long)(L.max_items + L.max_witems);
   const int g2 = (int)std::max<long long>(1, std::min<long long>((slots + 255) / 256, pool->num_sms * 8));
   tm_plan_items<<<g2, 256, 0, stream>>>(pp);
   count_launch();
@@ -1087,6 +1130,7 @@ kvs_status decode_attn_token_major(kvs_pool* pool, int layer, const void* q, int
   prm.ib = L.ib;
   prm.n_chunks = L.n_chunks;
   prm.R = L.R;
+  prm.SG = L.SG;
   prm.capacity = d.capacity_blocks;
   prm.diff_capacity = d.diff_capacity_blocks;
   prm.scale_log2 = scale * 1.4426950408889634f;
@@ -1097,6 +1141,34 @@ kvs_status decode_attn_token_major(kvs_pool* pool, int layer, const void* q, int
   prm.stall_first = (pool->test_flags & KVS_TEST_STALL_ONE_STAGE) ? 1 : 0;
   pool->test_flags &= ~KVS_TEST_STALL_ONE_STAGE;   // one launch only
   const int max_claims = (int)std::min<size_t>(L.max_items * d.num_kv_heads, 0x7fffffff);
+  if (L.wide) {
+    // the shared chunks of every sharing group, on the tensor cores; they
+    // write the shared splits, disjoint from what the token-major kernel writes
+    WideParams wp{};
+    wp.q = prm.q;
+    wp.witems = t.witems;
+    wp.hdr = t.hdr;
+    wp.gmask = t.gmask;
+    wp.gphys = t.gphys;
+    wp.p2 = t.p2;
+    wp.p2_ml = t.p2_ml;
+    wp.status = pool->status;
+    wp.n_seq = n_seq;
+    wp.max_blocks = max_blocks;
+    wp.hkv = d.num_kv_heads;
+    wp.g = g;
+    wp.hq = n_q_heads;
+    wp.W = L.SG;
+    wp.ib = L.ib;
+    wp.n_chunks = L.n_chunks;
+    wp.R = L.R;
+    wp.capacity = d.capacity_blocks;
+    wp.magic = kPlanMagic;
+    wp.scale_log2 = prm.scale_log2;
+    const int wide_claims = (int)std::min<size_t>(L.max_witems * d.num_kv_heads, 0x7fffffff);
+    const kvs_status ws_ = launch_wide_tile(wp, pool, layer, wide_claims, stream);
+    if (ws_ != KVS_OK) return ws_;
+  }
   if (d.head_dim == 128) {
     if (dif) return rope ? launch_tm<128, true, true>(prm, pool, layer, max_claims, stream)
                          : launch_tm<128, true, false>(prm, pool, layer, max_claims, stream);

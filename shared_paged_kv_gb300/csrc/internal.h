@@ -16,6 +16,7 @@ struct kvs_pool {
   int num_sms = 0;
   std::vector<void*> k, v, ksb, vsb, dk, dv;    // per-layer device slabs (not owned)
   std::vector<CUtensorMap> tk, tv, tdk, tdv;    // TMA maps per layer
+  std::vector<CUtensorMap> tk1, tv1;           // bf16 head_dim 128: one 64-column half of a block per copy
   uint32_t* status = nullptr;                   // device status word (owned)
   int32_t* tickets = nullptr;                   // split-K arrival counters (owned)
   size_t n_tickets = 0;
@@ -69,10 +70,30 @@ kvs_status decode_attn_token_major(kvs_pool* pool, int layer, const void* q, int
                                    const int32_t* rope_off, const kvs_seg_rope* rope_segs, float theta,
                                    float scale, float* out, void* ws, cudaStream_t stream);
 size_t tm_workspace_bytes(const kvs_pool* pool, int n_seq, int max_blocks, int g);
+bool tm_wide_tile(const kvs_pool* pool, int g, bool rope);
 kvs_status decode_plan_token_major(kvs_pool* pool, int n_q_heads, const int32_t* table, int max_blocks,
                                    const int32_t* seq_len, int n_seq, const int32_t* diff, const int32_t* rope_off,
                                    const kvs_seg_rope* rope_segs, void* ws, cudaStream_t stream);
 constexpr int kTmMaxGroup = 8;
+
+// Wide shared tile (attn_wide.cu): tcgen05 attention of a sharing group's
+// W * G query rows over the blocks the group shares.  Writes the shared splits
+// (p2, p2_ml) of the token-major plan; the split merge combines them.
+struct WideParams {
+  const uint16_t* q;        // [n_seq][hq][128] bf16
+  const int4* witems;       // {kind | group, chunk, end block, member mask}
+  const int* hdr;           // plan header ([8]: number of wide items)
+  const uint32_t* gmask;    // [n_groups][max_blocks] sharing members per block
+  const int32_t* gphys;     // [n_groups][max_blocks] shared physical block
+  float* p2;                // [n_seq][hkv][n_chunks][g][128]
+  float* p2_ml;             // [n_seq][hkv][n_chunks][g][2]
+  uint32_t* status;
+  int n_seq, max_blocks, hkv, g, hq, W, ib, n_chunks, R, capacity;
+  int magic;                // plan header check: magic, n_seq, max_blocks, R, ib, hkv, W
+  float scale_log2;
+};
+kvs_status launch_wide_tile(const WideParams& p, const kvs_pool* pool, int layer, int max_claims,
+                            cudaStream_t stream);
 
 // Mirror construction (mirror.cu).
 size_t mirror_workspace_bytes(int n_seq, int max_blocks);

@@ -90,12 +90,16 @@ static PFN_cuTensorMapEncodeTiled_v12000 get_encoder() {
 // block tile in one copy, laid out in shared memory as [half][row][64]: each
 // half is a 16-row x 128-byte swizzled panel, which keeps ldmatrix free of
 // bank conflicts.
-static bool encode_bf16_slab(CUtensorMap* m, void* base, long long rows, int head_dim, int box_rows) {
+// With halves = 1 the box takes one 64-column half of a block (used where a
+// tile of several blocks is laid out as [half][token][64]).
+static bool encode_bf16_slab(CUtensorMap* m, void* base, long long rows, int head_dim, int box_rows,
+                             int halves = 0) {
   auto enc = get_encoder();
   if (!enc) return false;
   cuuint64_t dims[3] = {64, static_cast<cuuint64_t>(rows), static_cast<cuuint64_t>(head_dim / 64)};
   cuuint64_t strides[2] = {static_cast<cuuint64_t>(head_dim) * 2, 128};
-  cuuint32_t box[3] = {64, static_cast<cuuint32_t>(box_rows), static_cast<cuuint32_t>(head_dim / 64)};
+  cuuint32_t box[3] = {64, static_cast<cuuint32_t>(box_rows),
+                       static_cast<cuuint32_t>(halves > 0 ? halves : head_dim / 64)};
   cuuint32_t es[3] = {1, 1, 1};
   CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, base, dims, strides, box, es,
                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -198,6 +202,14 @@ kvs_status kvs_pool_create(const kvs_pool_desc* d, void* const* k_layers, void* 
     } else {
       ok = encode_bf16_slab(&p->tk[l], p->k[l], rows, d->head_dim, d->block_tokens) &&
            encode_bf16_slab(&p->tv[l], p->v[l], rows, d->head_dim, d->block_tokens);
+      if (ok && d->head_dim == 128 && d->block_tokens == 16) {
+        if (p->tk1.empty()) {
+          p->tk1.resize(L);
+          p->tv1.resize(L);
+        }
+        ok = encode_bf16_slab(&p->tk1[l], p->k[l], rows, d->head_dim, d->block_tokens, 1) &&
+             encode_bf16_slab(&p->tv1[l], p->v[l], rows, d->head_dim, d->block_tokens, 1);
+      }
       if (ok && d->diff_capacity_blocks > 0)
         ok = encode_bf16_slab(&p->tdk[l], p->dk[l], drows, d->head_dim, d->block_tokens) &&
              encode_bf16_slab(&p->tdv[l], p->dv[l], drows, d->head_dim, d->block_tokens);
