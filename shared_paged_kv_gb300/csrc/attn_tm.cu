@@ -81,25 +81,27 @@ __host__ __device__ constexpr int tm_smem_bytes() {
 // sequences (R = 1) and only their unshared blocks.  SG is the group size
 // either way (1: no groups).
 struct TmLayout {
-  int R, SG, ib, n_chunks, n_groups;
+  int R, SG, ib, n_chunks, ibs, n_chunks_s, n_groups;   // private and shared chunk sizes / counts
   bool wide;
   size_t max_items, max_witems;
-  size_t off_hdr, off_items, off_witems, off_gmask, off_gphys, off_bdelta, off_pne, off_spm, off_p1, off_p2, total;
+  int max_sub;   // 8-block sub-tiles per wide item
+  size_t off_hdr, off_items, off_witems, off_wsub, off_gmask, off_gphys, off_bdelta, off_pne, off_spm, off_p1, off_p2, total;
 };
 
 static size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 // Work-item size (blocks): about KVS_TM_ITEMS_PER_WARP items per resident
-// warp, at least max_blocks / KVS_TM_MAX_SPLITS (bounding the splits of one
-// sequence per kind), at most 32 (one block-table entry per lane).  The work
+// warp, at least max_blocks / (KVS_TM_MAX_SPLITS * split_mult) (bounding the
+// splits of one sequence per kind), at most 32 (one block-table entry per lane).  The work
 // estimate counts every sequence's blocks; with groups (R > 1) the blocks a
 // group shares become one item for all members, so fewer items result and
 // the target is doubled.
-int tm_item_blocks(const kvs_pool* pool, int n_seq, int max_blocks, int R) {
+int tm_item_blocks(const kvs_pool* pool, int n_seq, int max_blocks, int R, int split_mult) {
   const long long work = (long long)n_seq * pool->desc.num_kv_heads * max_blocks;
   const long long warps = (long long)pool->num_sms * KVS_TM_MIN_CTAS * kTmWarps;
   long long ib = work / (warps * KVS_TM_ITEMS_PER_WARP * (R > 1 ? 2 : 1));
-  const long long min_ib = (max_blocks + KVS_TM_MAX_SPLITS - 1) / KVS_TM_MAX_SPLITS;
+  const long long max_splits = (long long)KVS_TM_MAX_SPLITS * split_mult;
+  const long long min_ib = (max_blocks + max_splits - 1) / max_splits;
   if (ib < min_ib) ib = min_ib;
   int r = 4;
   while (r < ib && r < kTmMaxIb) r <<= 1;
@@ -115,25 +117,32 @@ static TmLayout tm_layout(const kvs_pool* pool, int n_seq, int max_blocks, int g
   L.wide = tm_wide_tile(pool, g, rope);
   L.R = (rope || L.wide) ? 1 : std::max(1, 8 / g);
   L.SG = L.wide ? std::min(32, 128 / g) : L.R;
-  L.ib = tm_item_blocks(pool, n_seq, max_blocks, L.R);
+  // With a wide tile, shared chunks are whole 8-block sub-tiles of the wide
+  // tile (the private chunks keep their own size).
+  L.ib = tm_item_blocks(pool, n_seq, max_blocks, L.R, 1);
   L.n_chunks = (max_blocks + L.ib - 1) / L.ib;
+  L.ibs = L.ib;
+  if (L.wide) L.ibs = (std::max(tm_item_blocks(pool, n_seq, max_blocks, 1, 1), 8) + 7) / 8 * 8;
+  L.n_chunks_s = (max_blocks + L.ibs - 1) / L.ibs;
   L.n_groups = (n_seq + L.SG - 1) / L.SG;
   const size_t grp = L.SG > 1 ? (size_t)L.n_groups : 0;   // group arrays exist only with grouping
-  L.max_items = ((L.wide ? 0 : grp) + n_seq) * L.n_chunks;
-  L.max_witems = L.wide ? grp * L.n_chunks : 0;
-  const size_t splits = (size_t)n_seq * pool->desc.num_kv_heads * L.n_chunks;
-  const size_t split_bytes = splits * g * (pool->desc.head_dim + 2) * sizeof(float);
+  L.max_items = (L.wide ? 0 : grp * L.n_chunks_s) + (size_t)n_seq * L.n_chunks;
+  L.max_witems = L.wide ? grp * L.n_chunks_s : 0;
+  L.max_sub = (L.ibs + 7) / 8;
+  const size_t per_split = (size_t)n_seq * pool->desc.num_kv_heads * g * (pool->desc.head_dim + 2) * sizeof(float);
+  const size_t split_bytes = per_split * L.n_chunks, split_bytes_s = per_split * L.n_chunks_s;
   size_t o = 0;
   L.off_hdr = o; o = align256(o + 64);
   L.off_items = o; o = align256(o + L.max_items * sizeof(int4));
   L.off_witems = o; o = align256(o + L.max_witems * sizeof(int4));
+  L.off_wsub = o; o = align256(o + L.max_witems * L.max_sub * 8 * sizeof(int2));
   L.off_gmask = o; o = align256(o + grp * max_blocks * sizeof(uint32_t));
   L.off_gphys = o; o = align256(o + grp * max_blocks * sizeof(int32_t));
   L.off_bdelta = o; o = align256(o + (rope ? (size_t)n_seq * max_blocks * sizeof(int32_t) : 0));
   L.off_pne = o; o = align256(o + (size_t)n_seq * L.n_chunks);
-  L.off_spm = o; o = align256(o + grp * L.n_chunks * sizeof(uint32_t));
+  L.off_spm = o; o = align256(o + grp * L.n_chunks_s * sizeof(uint32_t));
   L.off_p1 = o; o = align256(o + split_bytes);
-  L.off_p2 = o; o = align256(o + (L.SG > 1 ? split_bytes : 0));
+  L.off_p2 = o; o = align256(o + (L.SG > 1 ? split_bytes_s : 0));
   L.total = o;
   return L;
 }
@@ -150,7 +159,7 @@ size_t tm_workspace_bytes(const kvs_pool* pool, int n_seq, int max_blocks, int g
 // tcgen05 kernel; the token-major list then holds private items only.
 //
 // Header: [0] token-major items, [1] magic, [2] n_seq, [3] max_blocks, [4] R,
-// [5] ib, [6] hkv, [7] SG, [8] wide items.
+// [5] ib, [6] hkv, [7] SG, [8] wide items, [9] ibs.
 struct PlanParams {
   const int32_t* block_table;
   const int32_t* seq_len;
@@ -158,17 +167,18 @@ struct PlanParams {
   int* hdr;
   int4* items;
   int4* witems;      // wide shared items (wide tile only)
+  int2* wsub;        // per wide item and 8-block sub-tile: {members, physical block} of each block
   uint32_t* gmask;   // [n_groups][max_blocks] members computed by the group's shared item (SG > 1)
   int32_t* gphys;    // [n_groups][max_blocks] that shared physical block, or -1 (SG > 1)
   uint8_t* pne;      // [n_seq][n_chunks] private chunk has unshared work
-  uint32_t* spm;     // [n_groups][n_chunks] members taking part in the shared chunk (SG > 1)
+  uint32_t* spm;     // [n_groups][n_chunks_s] members taking part in the shared chunk (SG > 1)
   const int32_t* rope_off;   // rotation calls: segment CSR
   const int4* rope_segs;
   int32_t* bdelta;   // [n_seq][max_blocks] RoPE shift of each logical block (rotation calls)
   uint32_t* status;
   float* p1_ml;      // (m, l) of the private splits [n_seq][hkv][n_chunks][g]
-  float* p2_ml;      // (m, l) of the shared splits, same shape (SG > 1)
-  int n_seq, max_blocks, R, SG, G, ib, n_chunks, n_groups, capacity, hkv, wide;
+  float* p2_ml;      // (m, l) of the shared splits [n_seq][hkv][n_chunks_s][g] (SG > 1)
+  int n_seq, max_blocks, R, SG, G, ib, n_chunks, ibs, n_chunks_s, n_groups, capacity, hkv, wide, max_sub;
 };
 
 __device__ __forceinline__ int plan_seq_blocks(const int32_t* seq_len, int a, int max_blocks) {
@@ -203,6 +213,7 @@ __global__ void __launch_bounds__(256) tm_plan_groups(PlanParams pp) {
     pp.hdr[6] = pp.hkv;
     pp.hdr[7] = pp.SG;
     pp.hdr[8] = 0;
+    pp.hdr[9] = pp.ibs;
   }
   const float2 none = make_float2(-INFINITY, 0.f);
   const int SG = pp.SG;
@@ -264,11 +275,11 @@ __global__ void __launch_bounds__(256) tm_plan_groups(PlanParams pp) {
       pp.pne[(size_t)a * pp.n_chunks + c] = (uint8_t)any_priv;
     }
     if (SG > 1) {
-      for (int c = tid; c < pp.n_chunks; c += nt) {
+      for (int c = tid; c < pp.n_chunks_s; c += nt) {
         uint32_t m = 0;
-        for (int b = c * pp.ib; b < min((c + 1) * pp.ib, pp.max_blocks); ++b)
+        for (int b = c * pp.ibs; b < min((c + 1) * pp.ibs, pp.max_blocks); ++b)
           m |= pp.gmask[(size_t)gi * pp.max_blocks + b];
-        pp.spm[(size_t)gi * pp.n_chunks + c] = m;
+        pp.spm[(size_t)gi * pp.n_chunks_s + c] = m;
       }
     }
     __syncthreads();
@@ -280,8 +291,15 @@ __global__ void __launch_bounds__(256) tm_plan_groups(PlanParams pp) {
       const int a = a0 + r;
       const size_t e = (size_t)a * per_seq + rem;   // [a][h][c][hh]
       if (!pp.pne[(size_t)a * pp.n_chunks + c]) reinterpret_cast<float2*>(pp.p1_ml)[e] = none;
-      if (SG > 1 && !((pp.spm[(size_t)gi * pp.n_chunks + c] >> r) & 1u))
-        reinterpret_cast<float2*>(pp.p2_ml)[e] = none;
+    }
+    if (SG > 1) {
+      const int per_seq_s = pp.hkv * pp.n_chunks_s * pp.G;
+      for (int i = tid; i < nm * per_seq_s; i += nt) {
+        const int r = i / per_seq_s, rem = i - r * per_seq_s;
+        const int c = (rem / pp.G) % pp.n_chunks_s;
+        if (!((pp.spm[(size_t)gi * pp.n_chunks_s + c] >> r) & 1u))
+          reinterpret_cast<float2*>(pp.p2_ml)[(size_t)(a0 + r) * per_seq_s + rem] = none;
+      }
     }
     __syncthreads();
   }
@@ -295,7 +313,7 @@ __global__ void __launch_bounds__(256) tm_plan_groups(PlanParams pp) {
 __global__ void __launch_bounds__(256) tm_plan_items(PlanParams pp) {
   __shared__ int warp_sums[32];
   __shared__ int s_base, s_wbase;
-  const int n_sh = pp.SG > 1 ? pp.n_groups * pp.n_chunks : 0, n_pr = pp.n_seq * pp.n_chunks;
+  const int n_sh = pp.SG > 1 ? pp.n_groups * pp.n_chunks_s : 0, n_pr = pp.n_seq * pp.n_chunks;
   const int total = n_sh + n_pr;
   for (int base = blockIdx.x * blockDim.x; base < total; base += gridDim.x * blockDim.x) {
     const int i = base + threadIdx.x;
@@ -303,12 +321,12 @@ __global__ void __launch_bounds__(256) tm_plan_items(PlanParams pp) {
     int4 item = make_int4(0, 0, 0, 0);
     if (i < n_sh) {
       const int c = i / pp.n_groups, gi = i - c * pp.n_groups;
-      const uint32_t m = pp.spm[(size_t)gi * pp.n_chunks + c];
+      const uint32_t m = pp.spm[(size_t)gi * pp.n_chunks_s + c];
       if (m != 0) {
         int nb = 0;
         for (int r = 0; r < pp.SG && gi * pp.SG + r < pp.n_seq; ++r)
           nb = max(nb, plan_seq_blocks(pp.seq_len, gi * pp.SG + r, pp.max_blocks));
-        item = make_int4((1 << 30) | gi, c, min((c + 1) * pp.ib, nb), (int)m);
+        item = make_int4((1 << 30) | gi, c, min((c + 1) * pp.ibs, nb), (int)m);
         if (pp.wide) keep_w = 1; else keep = 1;
       }
     } else if (i < total) {
@@ -327,7 +345,19 @@ __global__ void __launch_bounds__(256) tm_plan_items(PlanParams pp) {
     }
     __syncthreads();
     if (keep) pp.items[s_base + pos] = item;
-    if (keep_w) pp.witems[s_wbase + pos_w] = item;
+    if (keep_w) {
+      // the item's blocks as one record per 8-block sub-tile, so the tile
+      // kernel reads a sub-tile's members and physical blocks in one load
+      const int wi = s_wbase + pos_w, gi = item.x & ((1 << 30) - 1), b0 = item.y * pp.ibs;
+      pp.witems[wi] = item;
+      for (int e = 0; e < pp.max_sub * 8; ++e) {
+        const int b = b0 + e;
+        int2 v = make_int2(0, -1);
+        if (b < item.z && e < pp.ibs)
+          v = make_int2((int)pp.gmask[(size_t)gi * pp.max_blocks + b], pp.gphys[(size_t)gi * pp.max_blocks + b]);
+        pp.wsub[(size_t)wi * pp.max_sub * 8 + e] = v;
+      }
+    }
     __syncthreads();
   }
 }
@@ -349,7 +379,7 @@ struct TmParams {
   const uint32_t* gmask;
   const int32_t* gphys;
   uint32_t* status;
-  int max_blocks, n_seq, hkv, g, hq, ib, n_chunks, R, SG, capacity, diff_capacity;
+  int max_blocks, n_seq, hkv, g, hq, ib, n_chunks, ibs, n_chunks_s, R, SG, capacity, diff_capacity;
   int mwpr;           // merge warps per output row
   int stall_first;    // test-only (KVS_TEST_STALL_ONE_STAGE): leave one stage unarmed
   float scale_log2;
@@ -415,7 +445,8 @@ attn_tm_kernel(const __grid_constant__ TmParams p, const __grid_constant__ CUten
 
   // the plan must have been built for this call's shapes
   const bool plan_ok = p.hdr[1] == kPlanMagic && p.hdr[2] == p.n_seq && p.hdr[3] == p.max_blocks &&
-                       p.hdr[4] == p.R && p.hdr[5] == p.ib && p.hdr[6] == p.hkv && p.hdr[7] == p.SG;
+                       p.hdr[4] == p.R && p.hdr[5] == p.ib && p.hdr[6] == p.hkv && p.hdr[7] == p.SG &&
+                       p.hdr[9] == p.ibs;
   if (!plan_ok && threadIdx.x == 0 && blockIdx.x == 0) set_err(p.status, KVS_DEVERR_PLAN);
   const int n_claims = plan_ok ? p.hdr[0] * p.hkv : 0;
   const int R = p.R;
@@ -658,7 +689,7 @@ attn_tm_kernel(const __grid_constant__ TmParams p, const __grid_constant__ CUten
       if (slot != 31) {
         const int a = ckind ? cidx * R + slot : cidx;
         const int hh = j - slot * p.g;
-        const size_t it = (((size_t)a * p.hkv + ch_) * p.n_chunks + cchunk) * p.g + hh;
+        const size_t it = (((size_t)a * p.hkv + ch_) * (ckind ? p.n_chunks_s : p.n_chunks) + cchunk) * p.g + hh;
         float* pr = dst + it * D;
 #pragma unroll
         for (int mt = 0; mt < D / 16; ++mt) {
@@ -817,16 +848,22 @@ attn_tm_kernel(const __grid_constant__ TmParams p, const __grid_constant__ CUten
     for (int j = 1; j < S; ++j) mbar_drain(&bars[warp][(i + j) % S], ((i + j) / S) & 1);
   }
   if (cur >= 0) flush();
+  // when this grid was launched behind the wide tile (programmatic dependent
+  // launch) it must not complete before that grid has: the merge queued
+  // behind this one reads both grids' splits (no-op otherwise)
+  asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
 // Split merge: p.mwpr warps (1, 2, 4 or 8) per (sequence, query head) row,
-// eight warps per CTA.  Each warp merges a fixed range of about ten of the
-// row's chunks (every lane keeping up to kMergeBatch independent split loads
-// in flight), then the partial states of a row combine through shared memory.
-// The partition and the order are fixed, so the result does not depend on
-// which warp computed which split.
+// eight warps per CTA.  A row's splits sit in "slots": the private split of
+// each chunk, then (with sharing groups) the shared split of each chunk.
+// Each warp takes a fixed range of about kMergeBatch slots: one pass loads
+// their (m, l) (one slot per lane), a second loads every existing split of
+// the range at once (each lane a D/32 slice), and the warps' partial states
+// combine through shared memory.  The partition and the order are fixed, so
+// the result does not depend on which warp computed which split.
 constexpr int kMergeWarps = 8;
-constexpr int kMergeBatch = 10;
+constexpr int kMergeBatch = 12;
 
 template <int D>
 __global__ void __launch_bounds__(kMergeWarps * 32, 2) tm_merge_kernel(const __grid_constant__ TmParams p) {
@@ -838,94 +875,84 @@ __global__ void __launch_bounds__(kMergeWarps * 32, 2) tm_merge_kernel(const __g
   const int wpr = p.mwpr;
   const int rl = warp / wpr, wq = warp - rl * wpr;
   const int row = blockIdx.x * (kMergeWarps / wpr) + rl;   // sequence * hq + query head
-  // the attention kernel has flagged a plan built for other shapes and
-  // computed nothing; leave the output untouched as well
-  const bool plan_ok = p.hdr[1] == kPlanMagic && p.hdr[2] == p.n_seq && p.hdr[3] == p.max_blocks &&
-                       p.hdr[4] == p.R && p.hdr[5] == p.ib && p.hdr[6] == p.hkv && p.hdr[7] == p.SG;
   const bool in_range = row < p.n_seq * p.hq;
   const int a = in_range ? row / p.hq : 0, qh = row - a * p.hq, h = qh / p.g, hh = qh - h * p.g;
-  const bool live = plan_ok && in_range && p.seq_len[a] > 0;
-  const size_t sbase = ((size_t)a * p.hkv + h) * p.n_chunks;
-  const int cpw = (p.n_chunks + wpr - 1) / wpr;
-  const int cbeg = wq * cpw, cend = live ? min(p.n_chunks, cbeg + cpw) : 0;
-
-  // lane k owns chunks c0 + k of each 32-chunk window of this warp's range;
-  // the first window keeps its (m, l) in registers between the passes.  The
-  // plan set the (m, l) of splits that no item writes to (-inf, 0), so a
-  // split exists exactly when its l is positive.
-  auto own = [&](int c0, bool& pv, bool& sv_, float2& mp, float2& ms) {
-    const int ck = c0 + lane;
-    const bool in = ck < cend;
-    mp = in ? __ldcg(reinterpret_cast<const float2*>(p.p1_ml + ((sbase + ck) * p.g + hh) * 2)) : make_float2(0.f, 0.f);
-    ms = in && p.SG > 1 ? __ldcg(reinterpret_cast<const float2*>(p.p2_ml + ((sbase + ck) * p.g + hh) * 2))
-                       : make_float2(0.f, 0.f);
-    pv = mp.y > 0.f;
-    sv_ = ms.y > 0.f;
+  const size_t sbase = ((size_t)a * p.hkv + h) * p.n_chunks, sbase_s = ((size_t)a * p.hkv + h) * p.n_chunks_s;
+  const int n_slots = p.n_chunks + (p.SG > 1 ? p.n_chunks_s : 0);
+  const int spw = (n_slots + wpr - 1) / wpr;
+  const int sbeg = wq * spw, send = in_range ? min(n_slots, sbeg + spw) : sbeg;
+  auto slot_off = [&](int sl) {   // split index of a slot
+    return sl < p.n_chunks ? (sbase + sl) * p.g + hh : (sbase_s + (sl - p.n_chunks)) * p.g + hh;
   };
-  float2 cp0 = make_float2(0.f, 0.f), cs0 = cp0;
-  bool hp0 = false, hs0 = false;
-  float M = -INFINITY;
-  for (int c0 = cbeg; c0 < cend; c0 += 32) {
-    bool pv, sv_;
-    float2 mp, ms;
-    own(c0, pv, sv_, mp, ms);
-    if (pv) M = fmaxf(M, mp.x);
-    if (sv_) M = fmaxf(M, ms.x);
-    if (c0 == cbeg) {
-      hp0 = pv; hs0 = sv_; cp0 = mp; cs0 = ms;
+  // the attention kernel has flagged a plan built for other shapes and
+  // computed nothing; leave the output untouched as well (the header loads
+  // go out together with the first (m, l) loads)
+  const bool plan_ok = p.hdr[1] == kPlanMagic && p.hdr[2] == p.n_seq && p.hdr[3] == p.max_blocks &&
+                       p.hdr[4] == p.R && p.hdr[5] == p.ib && p.hdr[6] == p.hkv && p.hdr[7] == p.SG &&
+                       p.hdr[9] == p.ibs;
+
+  // lane k owns slot w0 + k of each 32-slot window of this warp's range; the
+  // first window keeps its (m, l) in registers between the passes.  The plan
+  // set the (m, l) of splits that no item writes to (-inf, 0), so a split
+  // exists exactly when its l is positive.
+  auto own = [&](int w0, float2& ml) {
+    const int sl = w0 + lane;
+    ml = make_float2(0.f, 0.f);
+    if (sl < send) {
+      const float* base = sl >= p.n_chunks ? p.p2_ml : p.p1_ml;
+      ml = __ldcg(reinterpret_cast<const float2*>(base + slot_off(sl) * 2));
     }
+  };
+  float2 ml0 = make_float2(0.f, 0.f);
+  float M = -INFINITY;
+  for (int w0 = sbeg; w0 < send; w0 += 32) {
+    float2 ml;
+    own(w0, ml);
+    if (ml.y > 0.f) M = fmaxf(M, ml.x);
+    if (w0 == sbeg) ml0 = ml;
   }
 #pragma unroll
   for (int off = 16; off; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
   float Ls = 0.f, v[CPL];
 #pragma unroll
   for (int j = 0; j < CPL; ++j) v[j] = 0.f;
-  for (int c0 = cbeg; c0 < cend; c0 += 32) {
-    bool pv, sv_;
-    float2 mp, ms;
-    if (c0 == cbeg) {
-      pv = hp0; sv_ = hs0; mp = cp0; ms = cs0;
-    } else {
-      own(c0, pv, sv_, mp, ms);
-    }
-    const float wp = pv ? fast_exp2(mp.x - M) : 0.f;
-    const float ws = sv_ ? fast_exp2(ms.x - M) : 0.f;
-    Ls += wp * mp.y + ws * ms.y;
+  for (int w0 = sbeg; w0 < send; w0 += 32) {
+    float2 ml;
+    if (w0 == sbeg) ml = ml0; else own(w0, ml);
+    const bool ex = ml.y > 0.f;
+    const float wk = ex ? fast_exp2(ml.x - M) : 0.f;
+    Ls += wk * ml.y;
+    unsigned mk = __ballot_sync(0xffffffffu, ex);
+    while (mk) {   // warp-uniform
+      int idx[kMergeBatch];
 #pragma unroll
-    for (int kind = 0; kind < 2; ++kind) {
-      const float* P = kind ? p.p2 : p.p1;
-      const float wk = kind ? ws : wp;
-      unsigned mk = __ballot_sync(0xffffffffu, kind ? sv_ : pv);
-      while (mk) {   // warp-uniform
-        int idx[kMergeBatch];
-#pragma unroll
-        for (int u = 0; u < kMergeBatch; ++u) {
-          idx[u] = -1;
-          if (mk) {
-            idx[u] = __ffs(mk) - 1;
-            mk &= mk - 1;
-          }
+      for (int u = 0; u < kMergeBatch; ++u) {
+        idx[u] = -1;
+        if (mk) {
+          idx[u] = __ffs(mk) - 1;
+          mk &= mk - 1;
         }
-        float x[kMergeBatch][CPL];
+      }
+      float x[kMergeBatch][CPL];
 #pragma unroll
-        for (int u = 0; u < kMergeBatch; ++u) {
-          if (idx[u] < 0) continue;
-          const float* src = P + ((sbase + c0 + idx[u]) * p.g + hh) * D + lane * CPL;
-          if (CPL == 4) {
-            const float4 t = __ldcg(reinterpret_cast<const float4*>(src));
-            x[u][0] = t.x; x[u][1 % CPL] = t.y; x[u][2 % CPL] = t.z; x[u][3 % CPL] = t.w;
-          } else {
-            const float2 t = __ldcg(reinterpret_cast<const float2*>(src));
-            x[u][0] = t.x; x[u][1 % CPL] = t.y;
-          }
+      for (int u = 0; u < kMergeBatch; ++u) {
+        if (idx[u] < 0) continue;
+        const int sl = w0 + idx[u];
+        const float* src = (sl >= p.n_chunks ? p.p2 : p.p1) + slot_off(sl) * D + lane * CPL;
+        if (CPL == 4) {
+          const float4 t = __ldcg(reinterpret_cast<const float4*>(src));
+          x[u][0] = t.x; x[u][1 % CPL] = t.y; x[u][2 % CPL] = t.z; x[u][3 % CPL] = t.w;
+        } else {
+          const float2 t = __ldcg(reinterpret_cast<const float2*>(src));
+          x[u][0] = t.x; x[u][1 % CPL] = t.y;
         }
+      }
 #pragma unroll
-        for (int u = 0; u < kMergeBatch; ++u) {
-          if (idx[u] < 0) continue;
-          const float wgt = __shfl_sync(0xffffffffu, wk, idx[u]);
+      for (int u = 0; u < kMergeBatch; ++u) {
+        if (idx[u] < 0) continue;
+        const float wgt = __shfl_sync(0xffffffffu, wk, idx[u]);
 #pragma unroll
-          for (int j = 0; j < CPL; ++j) v[j] += wgt * x[u][j];
-        }
+        for (int j = 0; j < CPL; ++j) v[j] += wgt * x[u][j];
       }
     }
   }
@@ -991,7 +1018,8 @@ static kvs_status launch_merge(const TmParams& prm, cudaStream_t st) {
 
 
 template <int D, bool DIFF, bool ROPE>
-static kvs_status launch_tm(TmParams& prm, const kvs_pool* pool, int layer, int max_claims, cudaStream_t st) {
+static kvs_status launch_tm(TmParams& prm, const kvs_pool* pool, int layer, int max_claims, bool after_wide,
+                            cudaStream_t st) {
   auto kern = attn_tm_kernel<D, DIFF, ROPE>;
   constexpr int smem = tm_smem_bytes<D>();
   // occupancy depends only on the kernel and the device type (one type of
@@ -1011,7 +1039,18 @@ static kvs_status launch_tm(TmParams& prm, const kvs_pool* pool, int layer, int 
   const int grid = std::max(1, std::min(pool->num_sms * blocks_per_sm, (max_claims + kTmWarps - 1) / kTmWarps));
   const CUtensorMap& dk = DIFF ? pool->tdk[layer] : pool->tk[layer];
   const CUtensorMap& dv = DIFF ? pool->tdv[layer] : pool->tv[layer];
-  kern<<<grid, 128, smem, st>>>(prm, pool->tk[layer], pool->tv[layer], dk, dv);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(128);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = after_wide ? 1 : 0;   // behind the wide tile: start on the SMs it leaves free
+  if (cudaLaunchKernelEx(&cfg, kern, (const TmParams)prm, pool->tk[layer], pool->tv[layer], dk, dv) != cudaSuccess)
+    return fail(KVS_ERR_CUDA, "decode_attn: launch failed");
   count_launch();
   const kvs_status s = check_launch("decode_attn");
   if (s != KVS_OK) return s;
@@ -1023,6 +1062,7 @@ struct TmPtrs {
   int* hdr;
   int4* items;
   int4* witems;
+  int2* wsub;
   uint32_t* gmask;
   int32_t* gphys;
   uint8_t* pne;
@@ -1033,7 +1073,8 @@ struct TmPtrs {
 
 static TmPtrs tm_ptrs(const TmLayout& L, const kvs_pool* pool, int n_seq, int g, void* ws) {
   uint8_t* w = static_cast<uint8_t*>(ws);
-  const size_t split_vals = (size_t)n_seq * pool->desc.num_kv_heads * L.n_chunks * g * pool->desc.head_dim;
+  const size_t per_chunk = (size_t)n_seq * pool->desc.num_kv_heads * g * pool->desc.head_dim;
+  const size_t split_vals = per_chunk * L.n_chunks, split_vals_s = per_chunk * L.n_chunks_s;
   TmPtrs t{};
   t.hdr = reinterpret_cast<int*>(w + L.off_hdr);
   t.items = reinterpret_cast<int4*>(w + L.off_items);
@@ -1042,11 +1083,12 @@ static TmPtrs tm_ptrs(const TmLayout& L, const kvs_pool* pool, int n_seq, int g,
   t.pne = w + L.off_pne;
   t.spm = reinterpret_cast<uint32_t*>(w + L.off_spm);
   t.witems = reinterpret_cast<int4*>(w + L.off_witems);
+  t.wsub = reinterpret_cast<int2*>(w + L.off_wsub);
   t.bdelta = reinterpret_cast<int32_t*>(w + L.off_bdelta);
   t.p1 = reinterpret_cast<float*>(w + L.off_p1);
   t.p1_ml = t.p1 + split_vals;
   t.p2 = reinterpret_cast<float*>(w + L.off_p2);
-  t.p2_ml = t.p2 + (L.SG > 1 ? split_vals : 0);
+  t.p2_ml = t.p2 + (L.SG > 1 ? split_vals_s : 0);
   return t;
 }
 
@@ -1079,9 +1121,13 @@ kvs_status decode_plan_token_major(kvs_pool* pool, int n_q_heads, const int32_t*
   pp.SG = L.SG;
   pp.wide = L.wide ? 1 : 0;
   pp.witems = t.witems;
+  pp.wsub = t.wsub;
+  pp.max_sub = L.max_sub;
   pp.G = g;
   pp.ib = L.ib;
   pp.n_chunks = L.n_chunks;
+  pp.ibs = L.ibs;
+  pp.n_chunks_s = L.n_chunks_s;
   pp.n_groups = L.n_groups;
   pp.capacity = pool->desc.capacity_blocks;
   pp.hkv = pool->desc.num_kv_heads;
@@ -1129,18 +1175,23 @@ kvs_status decode_attn_token_major(kvs_pool* pool, int layer, const void* q, int
   prm.hq = n_q_heads;
   prm.ib = L.ib;
   prm.n_chunks = L.n_chunks;
+  prm.ibs = L.ibs;
+  prm.n_chunks_s = L.n_chunks_s;
   prm.R = L.R;
   prm.SG = L.SG;
   prm.capacity = d.capacity_blocks;
   prm.diff_capacity = d.diff_capacity_blocks;
   prm.scale_log2 = scale * 1.4426950408889634f;
-  // about ten chunks per merge warp
+  // about two batches of split slots per merge warp (of which typically
+  // fewer than half exist), so that the merge grid stays within one wave
   prm.mwpr = 1;
-  while (prm.mwpr < kMergeWarps && prm.mwpr * kMergeBatch < L.n_chunks) prm.mwpr <<= 1;
+  const int n_slots = L.n_chunks + (L.SG > 1 ? L.n_chunks_s : 0);
+  while (prm.mwpr < kMergeWarps && prm.mwpr * 2 * kMergeBatch < n_slots) prm.mwpr <<= 1;
   if (rope) rope_split_host(theta, d.head_dim, prm.rs.c);
   prm.stall_first = (pool->test_flags & KVS_TEST_STALL_ONE_STAGE) ? 1 : 0;
   pool->test_flags &= ~KVS_TEST_STALL_ONE_STAGE;   // one launch only
   const int max_claims = (int)std::min<size_t>(L.max_items * d.num_kv_heads, 0x7fffffff);
+  bool wide_launched = false;
   if (L.wide) {
     // the shared chunks of every sharing group, on the tensor cores; they
     // write the shared splits, disjoint from what the token-major kernel writes
@@ -1148,8 +1199,8 @@ kvs_status decode_attn_token_major(kvs_pool* pool, int layer, const void* q, int
     wp.q = prm.q;
     wp.witems = t.witems;
     wp.hdr = t.hdr;
-    wp.gmask = t.gmask;
-    wp.gphys = t.gphys;
+    wp.wsub = t.wsub;
+    wp.max_sub = L.max_sub;
     wp.p2 = t.p2;
     wp.p2_ml = t.p2_ml;
     wp.status = pool->status;
@@ -1159,8 +1210,9 @@ kvs_status decode_attn_token_major(kvs_pool* pool, int layer, const void* q, int
     wp.g = g;
     wp.hq = n_q_heads;
     wp.W = L.SG;
-    wp.ib = L.ib;
-    wp.n_chunks = L.n_chunks;
+    wp.ib = L.ibs;
+    wp.ibp = L.ib;
+    wp.n_chunks = L.n_chunks_s;
     wp.R = L.R;
     wp.capacity = d.capacity_blocks;
     wp.magic = kPlanMagic;
@@ -1168,17 +1220,18 @@ kvs_status decode_attn_token_major(kvs_pool* pool, int layer, const void* q, int
     const int wide_claims = (int)std::min<size_t>(L.max_witems * d.num_kv_heads, 0x7fffffff);
     const kvs_status ws_ = launch_wide_tile(wp, pool, layer, wide_claims, stream);
     if (ws_ != KVS_OK) return ws_;
+    wide_launched = wide_claims > 0;
   }
   if (d.head_dim == 128) {
-    if (dif) return rope ? launch_tm<128, true, true>(prm, pool, layer, max_claims, stream)
-                         : launch_tm<128, true, false>(prm, pool, layer, max_claims, stream);
-    return rope ? launch_tm<128, false, true>(prm, pool, layer, max_claims, stream)
-                : launch_tm<128, false, false>(prm, pool, layer, max_claims, stream);
+    if (dif) return rope ? launch_tm<128, true, true>(prm, pool, layer, max_claims, wide_launched, stream)
+                         : launch_tm<128, true, false>(prm, pool, layer, max_claims, wide_launched, stream);
+    return rope ? launch_tm<128, false, true>(prm, pool, layer, max_claims, wide_launched, stream)
+                : launch_tm<128, false, false>(prm, pool, layer, max_claims, wide_launched, stream);
   }
-  if (dif) return rope ? launch_tm<64, true, true>(prm, pool, layer, max_claims, stream)
-                       : launch_tm<64, true, false>(prm, pool, layer, max_claims, stream);
-  return rope ? launch_tm<64, false, true>(prm, pool, layer, max_claims, stream)
-              : launch_tm<64, false, false>(prm, pool, layer, max_claims, stream);
+  if (dif) return rope ? launch_tm<64, true, true>(prm, pool, layer, max_claims, wide_launched, stream)
+                       : launch_tm<64, true, false>(prm, pool, layer, max_claims, wide_launched, stream);
+  return rope ? launch_tm<64, false, true>(prm, pool, layer, max_claims, wide_launched, stream)
+              : launch_tm<64, false, false>(prm, pool, layer, max_claims, wide_launched, stream);
 }
 
 }  // namespace kvs

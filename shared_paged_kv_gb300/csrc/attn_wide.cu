@@ -37,7 +37,9 @@ constexpr int kWdThreads = 192;          // 4 row warps, MMA warp, TMA warp
 constexpr int kWdSubBlocks = 8;          // blocks per sub-tile (128 tokens)
 constexpr int kWdHalf = 128 * 128;       // one [128][64] bf16 half of a 128-row tile, bytes
 constexpr int kWdTile = 2 * kWdHalf;     // a 128 x 128 bf16 tile
-constexpr int kWdSmem = 1024 + kWdTile * 5;   // Q + 2 stages of K and V
+// Q + ST stages of K and V (one stage when every item is a single sub-tile)
+template <int ST>
+constexpr int wd_smem() { return 1024 + kWdTile * (1 + 2 * ST); }
 constexpr uint32_t kWdCols = 512;        // S/P buffers at 0 and 128, O at 256
 
 __device__ __forceinline__ bool wd_wait(uint64_t* bar, uint32_t parity, uint32_t* status) {
@@ -45,16 +47,49 @@ __device__ __forceinline__ bool wd_wait(uint64_t* bar, uint32_t parity, uint32_t
   return __all_sync(0xffffffffu, ok);
 }
 
-// Sharing members of the blocks of one sub-tile (gm[j], 0 past the chunk
-// end); bit j of the result: block j is loaded (somebody shares it).
-__device__ __forceinline__ uint32_t wd_masks(const WideParams& p, int gw, int b0, int nb, uint32_t (&gm)[kWdSubBlocks]) {
-  uint32_t lm = 0;
-#pragma unroll
-  for (int j = 0; j < kWdSubBlocks; ++j) {
-    gm[j] = j < nb ? __ldg(p.gmask + (size_t)gw * p.max_blocks + b0 + j) : 0u;
-    lm |= (gm[j] != 0u ? 1u : 0u) << j;
+// Position in this CTA's work: claim cl (item cl / hkv, KV head cl % hkv),
+// sub-tile j of the item.  Lane k < 8 holds block k's record {sharing
+// members, physical block} (members 0 past the chunk end).  The next
+// position's item and record are loaded one position ahead: their addresses
+// follow from the claim and sub-tile numbers alone.
+struct WdCursor {
+  int cl, j, n_cl, n_j;
+  int4 it, n_it;
+  int2 rec, n_rec;
+};
+
+__device__ __forceinline__ int wd_nsub(const WideParams& p, const int4& it) {
+  return (it.z - it.y * p.ib + kWdSubBlocks - 1) / kWdSubBlocks;
+}
+
+__device__ __forceinline__ int2 wd_rec(const WideParams& p, int cl, int j, int lane) {
+  return lane < kWdSubBlocks ? __ldg(p.wsub + ((size_t)(cl / p.hkv) * p.max_sub + j) * kWdSubBlocks + lane)
+                             : make_int2(0, -1);
+}
+
+__device__ __forceinline__ void wd_prefetch(const WideParams& p, WdCursor& c, int n_claims, int lane) {
+  c.n_cl = c.cl;
+  c.n_j = c.j + 1;
+  c.n_it = c.it;
+  if (c.n_j >= wd_nsub(p, c.it)) {
+    c.n_cl = c.cl + gridDim.x;
+    c.n_j = 0;
+    if (c.n_cl < n_claims) c.n_it = __ldg(p.witems + c.n_cl / p.hkv);
   }
-  return lm;
+  c.n_rec = c.n_cl < n_claims ? wd_rec(p, c.n_cl, c.n_j, lane) : make_int2(0, -1);
+}
+
+__device__ __forceinline__ void wd_advance(const WideParams& p, WdCursor& c, int n_claims, int lane) {
+  c.cl = c.n_cl;
+  c.j = c.n_j;
+  c.it = c.n_it;
+  c.rec = c.n_rec;
+  if (c.cl < n_claims) wd_prefetch(p, c, n_claims, lane);
+}
+
+// blocks of the sub-tile that somebody shares (bit j: block j is loaded)
+__device__ __forceinline__ uint32_t wd_loaded(const int2& rec) {
+  return __ballot_sync(0xffffffffu, rec.x != 0) & 0xffu;
 }
 
 struct WdBars {
@@ -63,6 +98,7 @@ struct WdBars {
 
 }  // namespace
 
+template <int ST>
 __global__ void __launch_bounds__(kWdThreads, 1)
 attn_wide_kernel(const __grid_constant__ WideParams p, const __grid_constant__ CUtensorMap tk,
                  const __grid_constant__ CUtensorMap tv) {
@@ -70,16 +106,28 @@ attn_wide_kernel(const __grid_constant__ WideParams p, const __grid_constant__ C
   __shared__ WdBars bars;
   __shared__ uint32_t s_tmem;
   __shared__ volatile int s_abort;
+  // the token-major kernel queued behind this one (programmatic dependent
+  // launch) computes other splits: let it start on the SMs left free
+  asm volatile("griddepcontrol.launch_dependents;");
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   uint8_t* base = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   uint8_t* sQ = base;                                   // [2][128][64]
   auto sK = [&](int s) { return base + kWdTile * (1 + 2 * s); };
   auto sV = [&](int s) { return base + kWdTile * (2 + 2 * s); };
 
+  // the plan header, the first item and its first record are independent
+  // loads: issue them together (the grid never exceeds the item capacity)
+  WdCursor cur;
+  cur.cl = blockIdx.x;
+  cur.j = 0;
+  cur.it = __ldg(p.witems + blockIdx.x / p.hkv);
+  cur.rec = wd_rec(p, blockIdx.x, 0, lane);
   const bool plan_ok = p.hdr[1] == p.magic && p.hdr[2] == p.n_seq && p.hdr[3] == p.max_blocks &&
-                       p.hdr[4] == p.R && p.hdr[5] == p.ib && p.hdr[6] == p.hkv && p.hdr[7] == p.W;
+                       p.hdr[4] == p.R && p.hdr[5] == p.ibp && p.hdr[6] == p.hkv && p.hdr[7] == p.W &&
+                       p.hdr[9] == p.ib;
   const int n_claims = plan_ok ? p.hdr[8] * p.hkv : 0;
   if ((int)blockIdx.x >= n_claims) return;   // uniform over the CTA: nothing allocated yet
+  wd_prefetch(p, cur, n_claims, lane);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < 2; ++s) {
@@ -108,59 +156,52 @@ attn_wide_kernel(const __grid_constant__ WideParams p, const __grid_constant__ C
 
   if (warp == 5) {
     // ------------------------------------------------------ TMA producer
+    // lane k < 8 copies block k of the sub-tile: both 64-column halves of K
+    // and of V into the [half][token][64] stage
     int n = 0;
     int armed[2] = {-1, -1};
     bool quit = false;
-    for (int cl = blockIdx.x; cl < n_claims && !quit; cl += gridDim.x) {
-      const int4 it = __ldg(p.witems + cl / p.hkv);
-      const int h = cl % p.hkv, gw = it.x & ((1 << 30) - 1);
-      for (int b0 = it.y * p.ib; b0 < it.z; b0 += kWdSubBlocks) {
-        if (stop()) { quit = true; break; }
-        const int nb = min(kWdSubBlocks, it.z - b0);
-        uint32_t gm[kWdSubBlocks];
-        const uint32_t lm = wd_masks(p, gw, b0, nb, gm);
-        if (!lm) continue;
-        const int s = n & 1;
-        if (n >= 2 && !wd_wait(&bars.kv_empty[s], ((n - 2) >> 1) & 1, p.status)) {
-          s_abort = 1;
-          quit = true;
-          break;
-        }
-        int phys = lane < nb ? __ldg(p.gphys + (size_t)gw * p.max_blocks + b0 + lane) : 0;
-        if (lane == 0) {
-          mbar_arrive_expect_tx(&bars.kv_full[s], (uint32_t)__popc(lm) * 4u * 2048u);
-          armed[s] = n;
-        }
-#pragma unroll
-        for (int j = 0; j < kWdSubBlocks; ++j) {
-          int ph = __shfl_sync(0xffffffffu, phys, j);
-          if (lane == 0 && ((lm >> j) & 1u)) {
-            if (ph < 0 || ph >= p.capacity) {   // the plan shares valid blocks only
-              set_err(p.status, KVS_DEVERR_BLOCK_ID);
-              ph = 0;
-            }
-            const int row = (ph * p.hkv + h) * 16;
-#pragma unroll
-            for (int hf = 0; hf < 2; ++hf) {
-              tma_load_3d(sK(s) + hf * kWdHalf + j * 2048, &tk, 0, row, hf, &bars.kv_full[s]);
-              tma_load_3d(sV(s) + hf * kWdHalf + j * 2048, &tv, 0, row, hf, &bars.kv_full[s]);
-            }
-          }
-        }
-        __syncwarp();
-        ++n;
+    for (; cur.cl < n_claims; wd_advance(p, cur, n_claims, lane)) {
+      if (stop()) { quit = true; break; }
+      const uint32_t lm = wd_loaded(cur.rec);
+      if (!lm) continue;
+      const int s = n % ST;
+      if (n >= ST && !wd_wait(&bars.kv_empty[s], ((n - ST) / ST) & 1, p.status)) {
+        s_abort = 1;
+        quit = true;
+        break;
       }
+      if (lane == 0) {
+        mbar_arrive_expect_tx(&bars.kv_full[s], (uint32_t)__popc(lm) * 4u * 2048u);
+        armed[s] = n;
+      }
+      __syncwarp();
+      if ((lm >> lane) & 1u) {
+        int ph = cur.rec.y;
+        if (ph < 0 || ph >= p.capacity) {   // the plan shares valid blocks only
+          set_err(p.status, KVS_DEVERR_BLOCK_ID);
+          ph = 0;
+        }
+        const int row = (ph * p.hkv + cur.cl % p.hkv) * 16;
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf) {
+          tma_load_3d(sK(s) + hf * kWdHalf + lane * 2048, &tk, 0, row, hf, &bars.kv_full[s]);
+          tma_load_3d(sV(s) + hf * kWdHalf + lane * 2048, &tv, 0, row, hf, &bars.kv_full[s]);
+        }
+      }
+      __syncwarp();
+      ++n;
     }
     if (quit) {   // copies still in flight land before the shared memory goes away
-      for (int s = 0; s < 2; ++s)
-        if (armed[s] >= 0) mbar_drain(&bars.kv_full[s], (armed[s] >> 1) & 1);
+      for (int s = 0; s < ST; ++s)
+        if (armed[s] >= 0) mbar_drain(&bars.kv_full[s], (armed[s] / ST) & 1);
     }
   } else if (warp == 4) {
     // ----------------------------------------------------------- MMA issue
     constexpr uint32_t idS = umma_idesc_bf16(128, 128, false, false);
     constexpr uint32_t idO = umma_idesc_bf16(128, 128, false, true);
     const uint32_t tO = tmem + 256;
-    int n = 0, k = 0;
+    int n = 0, k = -1;
     bool first_pv = true;
     int pend = -1;
     uint32_t pend_lm = 0;
@@ -175,39 +216,38 @@ attn_wide_kernel(const __grid_constant__ WideParams p, const __grid_constant__ C
 #pragma unroll
         for (int j = 0; j < kWdSubBlocks; ++j) {
           if (!((lmm >> j) & 1u)) continue;
-          const uint64_t bv = umma_desc_sw128(smem_u32(sV(m & 1)) + j * 2048, kWdHalf, 1024);
-          umma_ts(tO, tP + 8 * j, bv, idO, acc ? 1u : 0u);
-          umma_ts(tO, tP + 64 + 8 * j, bv, idO, 1u);
+          const uint64_t bv = umma_desc_sw128(smem_u32(sV(m % ST)) + j * 2048, kWdHalf, 1024);
+          const uint32_t pj = tP + 32 * (j >> 1) + 8 * (j & 1);   // block j's P hi; its lo 16 columns on
+          umma_ts(tO, pj, bv, idO, acc ? 1u : 0u);
+          umma_ts(tO, pj + 16, bv, idO, 1u);
           acc = true;
         }
         umma_commit(&bars.pv_done[m & 1]);
-        umma_commit(&bars.kv_empty[m & 1]);
+        umma_commit(&bars.kv_empty[m % ST]);
       }
       __syncwarp();
       first_pv = false;
       return true;
     };
-    for (int cl = blockIdx.x; cl < n_claims; cl += gridDim.x, ++k) {
+    for (; cur.cl < n_claims; wd_advance(p, cur, n_claims, lane)) {
       if (stop()) { ok = false; break; }
-      if (!wd_wait(&bars.q_full, k & 1, p.status)) { ok = false; break; }
-      const int4 it = __ldg(p.witems + cl / p.hkv);
-      const int gw = it.x & ((1 << 30) - 1);
-      first_pv = true;
-      pend = -1;
-      for (int b0 = it.y * p.ib; b0 < it.z; b0 += kWdSubBlocks) {
-        const int nb = min(kWdSubBlocks, it.z - b0);
-        uint32_t gm[kWdSubBlocks];
-        const uint32_t lm = wd_masks(p, gw, b0, nb, gm);
-        if (!lm) continue;
-        const int s = n & 1;
-        if (!wd_wait(&bars.kv_full[s], (n >> 1) & 1, p.status)) { ok = false; break; }
+      if (cur.j == 0) {   // a new claim: its query tile must be in place
+        ++k;
+        if (!wd_wait(&bars.q_full, k & 1, p.status)) { ok = false; break; }
+        first_pv = true;
+        pend = -1;
+      }
+      const uint32_t lm = wd_loaded(cur.rec);
+      if (lm) {
+        const int s = n & 1, ks = n % ST;   // TMEM buffer, shared-memory stage
+        if (!wd_wait(&bars.kv_full[ks], (n / ST) & 1, p.status)) { ok = false; break; }
         if (n >= 2 && !wd_wait(&bars.pv_done[s], ((n - 2) >> 1) & 1, p.status)) { ok = false; break; }
         tc_fence_after();
         if (lane == 0) {
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk) {
             const uint64_t a = umma_desc_sw128(smem_u32(sQ) + (kk >> 2) * kWdHalf + (kk & 3) * 32, 16, 1024);
-            const uint64_t b = umma_desc_sw128(smem_u32(sK(s)) + (kk >> 2) * kWdHalf + (kk & 3) * 32, 16, 1024);
+            const uint64_t b = umma_desc_sw128(smem_u32(sK(ks)) + (kk >> 2) * kWdHalf + (kk & 3) * 32, 16, 1024);
             umma_ss(tmem + 128u * s, a, b, idS, kk > 0 ? 1u : 0u);
           }
           umma_commit(&bars.s_full[s]);
@@ -218,12 +258,14 @@ attn_wide_kernel(const __grid_constant__ WideParams p, const __grid_constant__ C
         pend_lm = lm;
         ++n;
       }
-      if (!ok) break;
-      if (pend >= 0) {
-        if (!issue_pv(pend, pend_lm)) { ok = false; break; }
-      } else if (k >= 1 && !wd_wait(&bars.o_free, (k - 1) & 1, p.status)) {
-        ok = false;
-        break;
+      if (cur.n_cl != cur.cl) {   // the claim's last sub-tile
+        if (pend >= 0) {
+          if (!issue_pv(pend, pend_lm)) { ok = false; break; }
+          pend = -1;
+        } else if (k >= 1 && !wd_wait(&bars.o_free, (k - 1) & 1, p.status)) {
+          ok = false;
+          break;
+        }
       }
     }
     if (!ok) s_abort = 1;
@@ -238,98 +280,126 @@ attn_wide_kernel(const __grid_constant__ WideParams p, const __grid_constant__ C
     const uint32_t tO = tmem + lane_off + 256;
     const int slot = r / p.g, hh = r - slot * p.g;
     const float sl2 = p.scale_log2;
-    int n = 0, k = 0;
-    bool ok = true, pend_epi = false, e_ok = false;
-    int e_a = 0, e_h = 0, e_c = 0, e_last = 0;
+    uint8_t* stg = sQ + warp * 4096;   // this warp's query rows of half 0, reused to stage O
+    int n = 0, k = -1;
+    bool ok = true, pend_epi = false;
+    int e_gw = 0, e_h = 0, e_c = 0, e_last = 0;
+    uint32_t e_spm = 0;
     float e_m = 0.f, e_l = 0.f;
-    // the finished chunk's split of this row: O from tensor memory, (m, l)
+    float m = -INFINITY, l = 0.f;
+    bool first = true, row_ok = false;
+    // The finished chunk's splits of this warp's 32 rows.  Each 32-column
+    // slice of O goes from tensor memory through shared memory (128-byte
+    // rows, XOR-swizzled) so that stores cover whole row segments.
     auto epilogue = [&]() {
-      const size_t it = (((size_t)e_a * p.hkv + e_h) * p.n_chunks + e_c) * p.g + hh;
-      float* dst = p.p2 + it * 128;
-#pragma unroll
+#pragma unroll 1
       for (int q = 0; q < 4; ++q) {
         uint32_t v[32];
         tmem_ld32(tO + 32 * q, v);
-        if (e_ok) {
 #pragma unroll
-          for (int e = 0; e < 8; ++e)
-            __stcg(reinterpret_cast<float4*>(dst + 32 * q + 4 * e),
-                   make_float4(__uint_as_float(v[4 * e]), __uint_as_float(v[4 * e + 1]),
-                               __uint_as_float(v[4 * e + 2]), __uint_as_float(v[4 * e + 3])));
+        for (int e = 0; e < 8; ++e)
+          *reinterpret_cast<uint4*>(stg + lane * 128 + ((e ^ (lane & 7)) << 4)) =
+              make_uint4(v[4 * e], v[4 * e + 1], v[4 * e + 2], v[4 * e + 3]);
+        __syncwarp();
+#pragma unroll
+        for (int t = 0; t < 8; ++t) {
+          const int jr = 4 * t + (lane >> 3), e = lane & 7;
+          const int r2 = warp * 32 + jr, sl = r2 / p.g, h2 = r2 - sl * p.g, a2 = e_gw * p.W + sl;
+          if (sl < p.W && a2 < p.n_seq && ((e_spm >> sl) & 1u)) {
+            const size_t it2 = (((size_t)a2 * p.hkv + e_h) * p.n_chunks + e_c) * p.g + h2;
+            __stcg(reinterpret_cast<uint4*>(p.p2 + it2 * 128 + 32 * q + 4 * e),
+                   *reinterpret_cast<const uint4*>(stg + jr * 128 + ((e ^ (jr & 7)) << 4)));
+          }
         }
+        __syncwarp();
       }
-      if (e_ok) __stcg(reinterpret_cast<float2*>(p.p2_ml + it * 2), make_float2(e_m, e_l));
+      const int a = e_gw * p.W + slot;
+      if (slot < p.W && a < p.n_seq && ((e_spm >> slot) & 1u)) {
+        const size_t it = (((size_t)a * p.hkv + e_h) * p.n_chunks + e_c) * p.g + hh;
+        __stcg(reinterpret_cast<float2*>(p.p2_ml + it * 2), make_float2(e_m, e_l));
+      }
     };
-    for (int cl = blockIdx.x; cl < n_claims; cl += gridDim.x, ++k) {
+    for (; cur.cl < n_claims; wd_advance(p, cur, n_claims, lane)) {
       if (stop()) { ok = false; break; }
-      const int4 it = __ldg(p.witems + cl / p.hkv);
-      const int h = cl % p.hkv, gw = it.x & ((1 << 30) - 1);
-      const int a = gw * p.W + slot;
-      const bool row_ok = slot < p.W && a < p.n_seq;
-      // this claim's query rows into the Q tile ([half][row][64], 128-byte
-      // swizzle); every S of the previous claim has completed
-      {
+      const int gw = cur.it.x & ((1 << 30) - 1), h = cur.cl % p.hkv;
+      if (cur.j == 0) {   // a new claim
+        ++k;
+        if (k >= 1) {
+          if (pend_epi) {
+            if (!wd_wait(&bars.pv_done[e_last & 1], (e_last >> 1) & 1, p.status)) { ok = false; break; }
+            tc_fence_after();
+            epilogue();
+            pend_epi = false;
+          }
+          tc_fence_before();
+          mbar_arrive(&bars.o_free);
+        }
+        // this claim's query rows into the Q tile ([half][row][64], 128-byte
+        // swizzle); every S of the previous claim has completed
+        const int a = gw * p.W + slot;
+        row_ok = slot < p.W && a < p.n_seq;
         const uint4* src = reinterpret_cast<const uint4*>(p.q + ((size_t)(row_ok ? a : 0) * p.hq + h * p.g + hh) * 128);
 #pragma unroll
-        for (int c16 = 0; c16 < 16; ++c16) {
-          const uint4 v = row_ok ? __ldg(src + c16) : make_uint4(0u, 0u, 0u, 0u);
-          *reinterpret_cast<uint4*>(sQ + (c16 >> 3) * kWdHalf + r * 128 + (((c16 & 7) ^ (r & 7)) << 4)) = v;
+        for (int hf = 0; hf < 2; ++hf) {
+          uint4 qv[8];
+#pragma unroll
+          for (int c = 0; c < 8; ++c) qv[c] = row_ok ? __ldg(src + hf * 8 + c) : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+          for (int c = 0; c < 8; ++c)
+            *reinterpret_cast<uint4*>(sQ + hf * kWdHalf + r * 128 + ((c ^ (r & 7)) << 4)) = qv[c];
         }
+        fence_proxy_async_smem();
+        mbar_arrive(&bars.q_full);
+        m = -INFINITY;
+        l = 0.f;
+        first = true;
       }
-      fence_proxy_async_smem();
-      mbar_arrive(&bars.q_full);
-      if (k >= 1) {
-        if (pend_epi) {
-          if (!wd_wait(&bars.pv_done[e_last & 1], (e_last >> 1) & 1, p.status)) { ok = false; break; }
-          tc_fence_after();
-          epilogue();
-          pend_epi = false;
-        }
-        tc_fence_before();
-        mbar_arrive(&bars.o_free);
-      }
-      float m = -INFINITY, l = 0.f;
-      bool first = true;
-      for (int b0 = it.y * p.ib; b0 < it.z; b0 += kWdSubBlocks) {
-        const int nb = min(kWdSubBlocks, it.z - b0);
-        uint32_t gm[kWdSubBlocks];
-        const uint32_t lm = wd_masks(p, gw, b0, nb, gm);
-        if (!lm) continue;
+      const uint32_t lm = wd_loaded(cur.rec);
+      if (lm) {
         const int s = n & 1;
-        if (!wd_wait(&bars.s_full[s], (n >> 1) & 1, p.status)) { ok = false; break; }
-        tc_fence_after();
         uint32_t rl = 0;   // blocks this row takes
 #pragma unroll
-        for (int j = 0; j < kWdSubBlocks; ++j) rl |= ((row_ok && ((gm[j] >> slot) & 1u)) ? 1u : 0u) << j;
+        for (int j = 0; j < kWdSubBlocks; ++j) {
+          const uint32_t gm = (uint32_t)__shfl_sync(0xffffffffu, cur.rec.x, j);
+          rl |= ((row_ok && ((gm >> slot) & 1u)) ? 1u : 0u) << j;
+        }
+        if (!wd_wait(&bars.s_full[s], (n >> 1) & 1, p.status)) { ok = false; break; }
+        tc_fence_after();
         const uint32_t tS = tmem + lane_off + 128u * s;
-        uint32_t sv[128];
-        tmem_ld32(tS, sv);
-        tmem_ld32(tS + 32, sv + 32);
-        tmem_ld32(tS + 64, sv + 64);
-        tmem_ld32(tS + 96, sv + 96);
+        // two passes over the S row in tensor memory (32 columns at a time):
+        // its maximum, then P; only one slice is held in registers
         float mx = -INFINITY;
+#pragma unroll 1
+        for (int q = 0; q < 4; ++q) {
+          uint32_t v[32];
+          tmem_ld32(tS + 32 * q, v);
+          const uint32_t lq = (rl >> (2 * q)) & 3u;
 #pragma unroll
-        for (int t = 0; t < 128; ++t)
-          if ((rl >> (t >> 4)) & 1u) mx = fmaxf(mx, __uint_as_float(sv[t]) * sl2);
+          for (int t = 0; t < 32; ++t)
+            if ((lq >> (t >> 4)) & 1u) mx = fmaxf(mx, __uint_as_float(v[t]) * sl2);
+        }
         const float mn = fmaxf(m, mx);
         // nothing live yet: reference point 0, so that 2^(-inf - 0) = 0
         const float ref = mn == -INFINITY ? 0.f : mn;
         const float alpha = fast_exp2(m - ref);
         float sum = 0.f;
-#pragma unroll
+#pragma unroll 1
         for (int q = 0; q < 4; ++q) {
-          uint32_t hi[16], lo[16];
+          uint32_t v[32], hi[16], lo[16];
+          tmem_ld32(tS + 32 * q, v);
+          const uint32_t lq = (rl >> (2 * q)) & 3u;
 #pragma unroll
           for (int e = 0; e < 16; ++e) {
-            const int t = 32 * q + 2 * e;
-            const bool live = (rl >> (t >> 4)) & 1u;
-            const float p0 = live ? fast_exp2(__uint_as_float(sv[t]) * sl2 - ref) : 0.f;
-            const float p1 = live ? fast_exp2(__uint_as_float(sv[t + 1]) * sl2 - ref) : 0.f;
+            const bool live = (lq >> (e >> 3)) & 1u;
+            const float p0 = live ? fast_exp2(__uint_as_float(v[2 * e]) * sl2 - ref) : 0.f;
+            const float p1 = live ? fast_exp2(__uint_as_float(v[2 * e + 1]) * sl2 - ref) : 0.f;
             sum += p0 + p1;
             split_bf16(p0, p1, hi[e], lo[e]);
           }
-          tmem_st16(tS + 16 * q, hi);        // P hi: tokens 32q.. as packed pairs
-          tmem_st16(tS + 64 + 16 * q, lo);   // P lo
+          // P of tokens 32q..32q+31 as packed bf16 pairs, hi then lo, in the
+          // slice's own (already read) columns
+          tmem_st16(tS + 32 * q, hi);
+          tmem_st16(tS + 32 * q + 16, lo);
         }
         // a row whose maximum moved rescales its O once the previous P V is done
         const bool need = !first && m != -INFINITY && mn > m;
@@ -337,7 +407,7 @@ attn_wide_kernel(const __grid_constant__ WideParams p, const __grid_constant__ C
           if (!wd_wait(&bars.pv_done[(n - 1) & 1], ((n - 1) >> 1) & 1, p.status)) { ok = false; break; }
           tc_fence_after();
           const float f = need ? alpha : 1.f;
-#pragma unroll
+#pragma unroll 1
           for (int q = 0; q < 4; ++q) {
             uint32_t v[32];
             tmem_ld32(tO + 32 * q, v);
@@ -354,13 +424,12 @@ attn_wide_kernel(const __grid_constant__ WideParams p, const __grid_constant__ C
         first = false;
         ++n;
       }
-      if (!ok) break;
-      if (!first) {
+      if (cur.n_cl != cur.cl && !first) {   // the claim's last sub-tile: its split is pending
         pend_epi = true;
-        e_ok = row_ok && ((((uint32_t)it.w) >> slot) & 1u);
-        e_a = a;
+        e_gw = gw;
         e_h = h;
-        e_c = it.y;
+        e_c = cur.it.y;
+        e_spm = (uint32_t)cur.it.w;
         e_last = n - 1;
         e_m = m;
         e_l = l;
@@ -385,17 +454,23 @@ attn_wide_kernel(const __grid_constant__ WideParams p, const __grid_constant__ C
   }
 }
 
+template <int ST>
+static kvs_status launch_wide(const WideParams& p, const kvs_pool* pool, int layer, int grid, cudaStream_t stream) {
+  if (!smem_limit_once<attn_wide_kernel<ST>>(wd_smem<ST>(), pool->device))
+    return fail(KVS_ERR_CUDA, "decode_attn: cannot raise the shared-memory limit (wide tile)");
+  attn_wide_kernel<ST><<<grid, kWdThreads, wd_smem<ST>(), stream>>>(p, pool->tk1[layer], pool->tv1[layer]);
+  count_launch();
+  return check_launch("decode_attn_wide");
+}
+
 kvs_status launch_wide_tile(const WideParams& p, const kvs_pool* pool, int layer, int max_claims,
                             cudaStream_t stream) {
   if (max_claims <= 0) return KVS_OK;
-  if (!smem_limit_once<attn_wide_kernel>(kWdSmem, pool->device))
-    return fail(KVS_ERR_CUDA, "decode_attn: cannot raise the shared-memory limit (wide tile)");
-  // one CTA per SM (its shared memory and 512 TMEM columns), claims taken
-  // round-robin; CTAs beyond the plan's item count return at once
+  // one CTA per SM (its 512 TMEM columns), claims taken round-robin; CTAs
+  // beyond the plan's item count return at once.  Items of one sub-tile need
+  // no second stage, which leaves room on the SM for a token-major CTA.
   const int grid = std::max(1, std::min(pool->num_sms, max_claims));
-  attn_wide_kernel<<<grid, kWdThreads, kWdSmem, stream>>>(p, pool->tk1[layer], pool->tv1[layer]);
-  count_launch();
-  return check_launch("decode_attn_wide");
+  return p.max_sub > 1 ? launch_wide<2>(p, pool, layer, grid, stream) : launch_wide<1>(p, pool, layer, grid, stream);
 }
 
 }  // namespace kvs

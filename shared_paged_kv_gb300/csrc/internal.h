@@ -83,13 +83,13 @@ struct WideParams {
   const uint16_t* q;        // [n_seq][hq][128] bf16
   const int4* witems;       // {kind | group, chunk, end block, member mask}
   const int* hdr;           // plan header ([8]: number of wide items)
-  const uint32_t* gmask;    // [n_groups][max_blocks] sharing members per block
-  const int32_t* gphys;     // [n_groups][max_blocks] shared physical block
+  const int2* wsub;        // [item][max_sub][8] {sharing members, physical block} per block
   float* p2;                // [n_seq][hkv][n_chunks][g][128]
   float* p2_ml;             // [n_seq][hkv][n_chunks][g][2]
   uint32_t* status;
-  int n_seq, max_blocks, hkv, g, hq, W, ib, n_chunks, R, capacity;
-  int magic;                // plan header check: magic, n_seq, max_blocks, R, ib, hkv, W
+  int n_seq, max_blocks, hkv, g, hq, W, ib, n_chunks, R, capacity, max_sub;   // ib, n_chunks: shared chunks
+  int ibp;                  // private chunk blocks (plan header check)
+  int magic;                // plan header check: magic, n_seq, max_blocks, R, ibp, hkv, W, ib
   float scale_log2;
 };
 kvs_status launch_wide_tile(const WideParams& p, const kvs_pool* pool, int layer, int max_claims,
