@@ -35,6 +35,7 @@
 //    changes; the diff overlay adds DK / DV tiles through the same MMAs.
 //    Calls with rotation use groups of one sequence.
 #include <algorithm>
+#include <cstring>
 
 #include "common.cuh"
 #include "internal.h"
@@ -82,10 +83,10 @@ __host__ __device__ constexpr int tm_smem_bytes() {
 // either way (1: no groups).
 struct TmLayout {
   int R, SG, ib, n_chunks, ibs, n_chunks_s, n_groups;   // private and shared chunk sizes / counts
-  bool wide;
+  bool wide, runs;   // runs: rotation call on the wide tile (shared 8-block segment runs)
   size_t max_items, max_witems;
   int max_sub;   // 8-block sub-tiles per wide item
-  size_t off_hdr, off_items, off_witems, off_wsub, off_gmask, off_gphys, off_bdelta, off_pne, off_spm, off_p1, off_p2, total;
+  size_t off_hdr, off_items, off_witems, off_wsub, off_wmem, off_wclaims, off_gmask, off_gphys, off_bdelta, off_pne, off_spm, off_p1, off_p2, total;
 };
 
 static size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
@@ -95,9 +96,10 @@ static size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 // splits of one sequence per kind), at most 32 (one block-table entry per lane).  The work
 // estimate counts every sequence's blocks; with groups (R > 1) the blocks a
 // group shares become one item for all members, so fewer items result and
-// the target is doubled.
-int tm_item_blocks(const kvs_pool* pool, int n_seq, int max_blocks, int R, int split_mult) {
-  const long long work = (long long)n_seq * pool->desc.num_kv_heads * max_blocks;
+// the target is doubled.  With a wide tile the token-major kernel sees only
+// unshared blocks, so the work estimate is halved (work_div).
+int tm_item_blocks(const kvs_pool* pool, int n_seq, int max_blocks, int R, int split_mult, int work_div) {
+  const long long work = (long long)n_seq * pool->desc.num_kv_heads * max_blocks / work_div;
   const long long warps = (long long)pool->num_sms * KVS_TM_MIN_CTAS * kTmWarps;
   long long ib = work / (warps * KVS_TM_ITEMS_PER_WARP * (R > 1 ? 2 : 1));
   const long long max_splits = (long long)KVS_TM_MAX_SPLITS * split_mult;
@@ -109,25 +111,29 @@ int tm_item_blocks(const kvs_pool* pool, int n_seq, int max_blocks, int R, int s
 }
 
 bool tm_wide_tile(const kvs_pool* pool, int g, bool rope) {
-  return !rope && pool->desc.head_dim == 128 && g >= 4 && g <= kTmMaxGroup && !pool->tk1.empty();
+  (void)rope;
+  return pool->desc.head_dim == 128 && g >= 4 && g <= kTmMaxGroup && !pool->tk1.empty();
 }
 
 static TmLayout tm_layout(const kvs_pool* pool, int n_seq, int max_blocks, int g, bool rope) {
   TmLayout L{};
   L.wide = tm_wide_tile(pool, g, rope);
+  L.runs = L.wide && rope;
   L.R = (rope || L.wide) ? 1 : std::max(1, 8 / g);
   L.SG = L.wide ? std::min(32, 128 / g) : L.R;
   // With a wide tile, shared chunks are whole 8-block sub-tiles of the wide
   // tile (the private chunks keep their own size).
-  L.ib = tm_item_blocks(pool, n_seq, max_blocks, L.R, 1);
+  L.ib = tm_item_blocks(pool, n_seq, max_blocks, L.R, 1, L.wide ? 2 : 1);
   L.n_chunks = (max_blocks + L.ib - 1) / L.ib;
   L.ibs = L.ib;
-  if (L.wide) L.ibs = (std::max(tm_item_blocks(pool, n_seq, max_blocks, 1, 1), 8) + 7) / 8 * 8;
+  if (L.wide) L.ibs = L.runs ? 8 : (std::max(tm_item_blocks(pool, n_seq, max_blocks, 1, 1, 1), 8) + 7) / 8 * 8;
   L.n_chunks_s = (max_blocks + L.ibs - 1) / L.ibs;
   L.n_groups = (n_seq + L.SG - 1) / L.SG;
   const size_t grp = L.SG > 1 ? (size_t)L.n_groups : 0;   // group arrays exist only with grouping
   L.max_items = (L.wide ? 0 : grp * L.n_chunks_s) + (size_t)n_seq * L.n_chunks;
-  L.max_witems = L.wide ? grp * L.n_chunks_s : 0;
+  // a rotation call's items are 8-block runs keyed by physical block: a group
+  // can hold up to half its members' runs as items
+  L.max_witems = L.wide ? grp * L.n_chunks_s * (L.runs ? std::max(1, L.SG / 2) : 1) : 0;
   L.max_sub = (L.ibs + 7) / 8;
   const size_t per_split = (size_t)n_seq * pool->desc.num_kv_heads * g * (pool->desc.head_dim + 2) * sizeof(float);
   const size_t split_bytes = per_split * L.n_chunks, split_bytes_s = per_split * L.n_chunks_s;
@@ -136,6 +142,8 @@ static TmLayout tm_layout(const kvs_pool* pool, int n_seq, int max_blocks, int g
   L.off_items = o; o = align256(o + L.max_items * sizeof(int4));
   L.off_witems = o; o = align256(o + L.max_witems * sizeof(int4));
   L.off_wsub = o; o = align256(o + L.max_witems * L.max_sub * 8 * sizeof(int2));
+  L.off_wmem = o; o = align256(o + (L.runs ? L.max_witems * 32 * sizeof(int2) : 0));
+  L.off_wclaims = o; o = align256(o + (L.runs ? L.max_witems * sizeof(int4) : 0));
   L.off_gmask = o; o = align256(o + grp * max_blocks * sizeof(uint32_t));
   L.off_gphys = o; o = align256(o + grp * max_blocks * sizeof(int32_t));
   L.off_bdelta = o; o = align256(o + (rope ? (size_t)n_seq * max_blocks * sizeof(int32_t) : 0));
@@ -159,7 +167,8 @@ size_t tm_workspace_bytes(const kvs_pool* pool, int n_seq, int max_blocks, int g
 // tcgen05 kernel; the token-major list then holds private items only.
 //
 // Header: [0] token-major items, [1] magic, [2] n_seq, [3] max_blocks, [4] R,
-// [5] ib, [6] hkv, [7] SG, [8] wide items, [9] ibs.
+// [5] ib, [6] hkv, [7] SG, [8] wide items, [9] ibs, [10] wide claims (rotation
+// calls: ranges of run items).
 struct PlanParams {
   const int32_t* block_table;
   const int32_t* seq_len;
@@ -168,6 +177,8 @@ struct PlanParams {
   int4* items;
   int4* witems;      // wide shared items (wide tile only)
   int2* wsub;        // per wide item and 8-block sub-tile: {members, physical block} of each block
+  int2* wmem;        // rotation calls: per wide item and member, {split slot, RoPE shift}
+  int4* wclaims;     // rotation calls: claims {group, first item, items | slot << 16, members}
   uint32_t* gmask;   // [n_groups][max_blocks] members computed by the group's shared item (SG > 1)
   int32_t* gphys;    // [n_groups][max_blocks] that shared physical block, or -1 (SG > 1)
   uint8_t* pne;      // [n_seq][n_chunks] private chunk has unshared work
@@ -178,7 +189,8 @@ struct PlanParams {
   uint32_t* status;
   float* p1_ml;      // (m, l) of the private splits [n_seq][hkv][n_chunks][g]
   float* p2_ml;      // (m, l) of the shared splits [n_seq][hkv][n_chunks_s][g] (SG > 1)
-  int n_seq, max_blocks, R, SG, G, ib, n_chunks, ibs, n_chunks_s, n_groups, capacity, hkv, wide, max_sub;
+  int n_seq, max_blocks, R, SG, G, ib, n_chunks, ibs, n_chunks_s, n_groups, capacity, hkv, wide, max_sub, runs;
+  int max_witems;
 };
 
 __device__ __forceinline__ int plan_seq_blocks(const int32_t* seq_len, int a, int max_blocks) {
@@ -201,10 +213,181 @@ __device__ __forceinline__ int plan_seq_blocks(const int32_t* seq_len, int a, in
 //    so the merge can read all of them without consulting pne / spm first;
 //  * rotation calls: bdelta, the shift of the segment covering each logical
 //    block (the last entry covering it; 0 outside every entry).
+// Rotation calls on the wide tile: the group's shared work is keyed by
+// physical block instead of logical position.  A "run" is 8 logical blocks of
+// one member, inside one RoPE segment (one shift, the covering entry of every
+// block), full, without mirror diffs, holding 8 consecutive physical blocks;
+// runs of different members with the same first physical block hold the same
+// K and V and differ only in the shift, which the tile applies to each
+// member's query.  A block of a run that carries a mirror diff for a member
+// is left to that member's private items (the rest of the run is shared).
+// Runs found by at least two members become wide items; a member's other
+// blocks stay private.  All threads of the CTA call this.
+constexpr int kRunCap = 2048;
+constexpr int kRunsPerClaim = 8;   // run items per wide-tile claim (at least)
+constexpr int kMaxRanges = 256;    // claims per group (at most)
+
+__device__ void plan_runs(const PlanParams& pp, int gi, int a0, int nm, unsigned long long* s_key, int* s_dl,
+                          uint8_t* s_ex, int* s_n) {
+  const int tid = threadIdx.x, nt = blockDim.x;
+  if (tid == 0) *s_n = 0;
+  for (int b = tid; b < pp.max_blocks; b += nt) pp.gmask[(size_t)gi * pp.max_blocks + b] = 0u;
+  for (int c = tid; c < pp.n_chunks_s; c += nt) pp.spm[(size_t)gi * pp.n_chunks_s + c] = 0u;
+  __syncthreads();
+  // candidates {first physical block, member, first logical block; shift;
+  // blocks with a mirror diff}
+  for (int r = 0; r < nm; ++r) {
+    const int a = a0 + r;
+    const int L = min(max(pp.seq_len[a], 0), pp.max_blocks * 16);
+    const int e0 = pp.rope_off[a], e1 = pp.rope_off[a + 1];
+    for (int e = e0 + tid; e < e1; e += nt) {
+      const int4 sg = __ldg(pp.rope_segs + e);
+      if (sg.z <= -(1 << 18) || sg.z >= (1 << 18) || sg.x < 0) continue;
+      for (int b = sg.x; b + 8 <= sg.x + sg.y && b + 8 <= pp.max_blocks && (b + 8) * 16 <= L; b += 8) {
+        const int* row = pp.block_table + (size_t)a * pp.max_blocks;
+        const int ph0 = row[b];
+        bool ok = ph0 >= 0 && ph0 <= pp.capacity - 8;
+        // this entry must be the last one covering each of the 8 blocks, so
+        // that a logical block belongs to one run at most
+        for (int e2 = e + 1; e2 < e1 && ok; ++e2) {
+          const int4 s2 = __ldg(pp.rope_segs + e2);
+          ok = s2.y <= 0 || s2.x >= b + 8 || s2.x + s2.y <= b;
+        }
+        uint32_t ex = 0;
+        for (int k = 0; k < 8 && ok; ++k) {
+          ok = row[b + k] == ph0 + k && pp.bdelta[(size_t)a * pp.max_blocks + b + k] == sg.z;
+          if (ok && pp.diff_table && pp.diff_table[(size_t)a * pp.max_blocks + b + k] >= 0) ex |= 1u << k;
+        }
+        if (!ok || ex == 0xffu) continue;
+        const int idx = atomicAdd(s_n, 1);
+        if (idx < kRunCap) {
+          s_key[idx] = ((unsigned long long)(unsigned)ph0 << 32) | ((unsigned long long)r << 20) | (unsigned)b;
+          s_dl[idx] = sg.z;
+          s_ex[idx] = (uint8_t)ex;
+        }
+      }
+    }
+  }
+  __syncthreads();
+  const int n = min(*s_n, kRunCap);
+  int P = 1;
+  while (P < n) P <<= 1;
+  for (int i = n + tid; i < P; i += nt) {
+    s_key[i] = ~0ull;
+    s_dl[i] = 0;
+    s_ex[i] = 0;
+  }
+  __syncthreads();
+  // bitonic sort by (physical block, member, logical block): deterministic
+  for (int k = 2; k <= P; k <<= 1)
+    for (int j = k >> 1; j > 0; j >>= 1) {
+      for (int i = tid; i < P; i += nt) {
+        const int ixj = i ^ j;
+        if (ixj > i) {
+          const bool up = (i & k) == 0;
+          const unsigned long long x = s_key[i], y = s_key[ixj];
+          if ((x > y) == up) {
+            s_key[i] = y;
+            s_key[ixj] = x;
+            const int t = s_dl[i];
+            s_dl[i] = s_dl[ixj];
+            s_dl[ixj] = t;
+            const uint8_t u = s_ex[i];
+            s_ex[i] = s_ex[ixj];
+            s_ex[ixj] = u;
+          }
+        }
+      }
+      __syncthreads();
+    }
+  // one item per physical run held by two or more members (a member's first
+  // run with that block, by logical position).  Each thread takes a
+  // contiguous range of the sorted candidates, so the group's items get
+  // consecutive indices in key order.
+  const int per = (n + nt - 1) / nt, i0 = min(n, tid * per), i1 = min(n, i0 + per);
+  auto is_item = [&](int i, uint32_t& mask, int& j) {
+    const unsigned key = (unsigned)(s_key[i] >> 32);
+    if (i > 0 && (unsigned)(s_key[i - 1] >> 32) == key) return false;
+    mask = 0;
+    int cnt = 0;
+    for (j = i; j < n && (unsigned)(s_key[j] >> 32) == key; ++j) {
+      const int r = (int)((s_key[j] >> 20) & 31u);
+      if (!((mask >> r) & 1u)) {
+        mask |= 1u << r;
+        ++cnt;
+      }
+    }
+    return cnt >= 2;
+  };
+  int mine = 0;
+  for (int i = i0; i < i1; ++i) {
+    uint32_t mask;
+    int j;
+    mine += is_item(i, mask, j) ? 1 : 0;
+  }
+  __shared__ int warp_sums[32];
+  __shared__ int s_base, s_rbase, s_created, s_rg;
+  __shared__ uint32_t s_rmask[kMaxRanges];
+  int total;
+  const int off = block_exclusive_scan(mine, warp_sums, total);
+  if (tid == 0) {
+    const int base = total ? atomicAdd(pp.hdr + 8, total) : 0;
+    const int created = max(0, min(total, pp.max_witems - base));   // beyond the capacity: stays private
+    // claims of the wide tile: ranges of consecutive items (one split per
+    // member and range); at most min(n_chunks_s, kMaxRanges) ranges
+    const int rg = max(kRunsPerClaim, (created + min(pp.n_chunks_s, kMaxRanges) - 1) / min(pp.n_chunks_s, kMaxRanges));
+    const int n_r = (created + rg - 1) / rg;
+    s_base = base;
+    s_created = created;
+    s_rg = rg;
+    s_rbase = n_r ? atomicAdd(pp.hdr + 10, n_r) : 0;
+  }
+  for (int q = tid; q < kMaxRanges; q += nt) s_rmask[q] = 0u;
+  __syncthreads();
+  int k = off;
+  for (int i = i0; i < i1; ++i) {
+    uint32_t mask;
+    int j;
+    if (!is_item(i, mask, j)) continue;
+    const int kk = k++;
+    if (kk >= s_created) continue;
+    const int wi = s_base + kk, q_r = kk / s_rg;
+    const unsigned key = (unsigned)(s_key[i] >> 32);
+    pp.witems[wi] = make_int4((1 << 30) | gi, 0, 8, (int)mask);
+    for (int r = 0; r < 32; ++r) pp.wmem[(size_t)wi * 32 + r] = make_int2(q_r, 0);
+    uint32_t seen = 0, bm[8] = {0, 0, 0, 0, 0, 0, 0, 0};   // members taking each block
+    for (int q = i; q < j; ++q) {
+      const int r = (int)((s_key[q] >> 20) & 31u), b = (int)(s_key[q] & 0xFFFFFu);
+      if ((seen >> r) & 1u) continue;
+      seen |= 1u << r;
+      pp.wmem[(size_t)wi * 32 + r] = make_int2(q_r, s_dl[q]);
+      for (int kb = 0; kb < 8; ++kb) {
+        if ((s_ex[q] >> kb) & 1u) continue;   // diff block: private for this member
+        bm[kb] |= 1u << r;
+        atomicOr(pp.gmask + (size_t)gi * pp.max_blocks + b + kb, 1u << r);
+      }
+    }
+    for (int kb = 0; kb < 8; ++kb) pp.wsub[(size_t)wi * 8 + kb] = make_int2((int)bm[kb], (int)key + kb);
+    atomicOr(&s_rmask[q_r], mask);
+  }
+  __syncthreads();
+  const int n_r = (s_created + s_rg - 1) / s_rg;
+  for (int q = tid; q < n_r; q += nt) {
+    const int first = q * s_rg, cnt = min(s_rg, s_created - first);
+    if (s_rbase + q < pp.max_witems)
+      pp.wclaims[s_rbase + q] = make_int4(gi, s_base + first, cnt | (q << 16), (int)s_rmask[q]);
+    pp.spm[(size_t)gi * pp.n_chunks_s + q] = s_rmask[q];
+  }
+}
+
 __global__ void __launch_bounds__(256) tm_plan_groups(PlanParams pp) {
+  __shared__ unsigned long long s_key[kRunCap];
+  __shared__ int s_dl[kRunCap];
+  __shared__ uint8_t s_ex[kRunCap];
+  __shared__ int s_n;
   const int tid = threadIdx.x, nt = blockDim.x;
   if (blockIdx.x == 0 && tid == 0) {
-    pp.hdr[0] = 0;   // item counts, accumulated by tm_plan_items
+    pp.hdr[0] = 0;   // item counts, accumulated by tm_plan_items (and, for runs, here)
     pp.hdr[1] = kPlanMagic;
     pp.hdr[2] = pp.n_seq;
     pp.hdr[3] = pp.max_blocks;
@@ -212,15 +395,36 @@ __global__ void __launch_bounds__(256) tm_plan_groups(PlanParams pp) {
     pp.hdr[5] = pp.ib;
     pp.hdr[6] = pp.hkv;
     pp.hdr[7] = pp.SG;
-    pp.hdr[8] = 0;
     pp.hdr[9] = pp.ibs;
   }
   const float2 none = make_float2(-INFINITY, 0.f);
   const int SG = pp.SG;
   for (int gi = blockIdx.x; gi < pp.n_groups; gi += gridDim.x) {
     const int a0 = gi * SG, nm = min(SG, pp.n_seq - a0);
-    // 1. sharing per logical block
-    if (SG > 1) {
+    // 0. rotation calls: the shift of every member's logical blocks (the last
+    // entry covering the block; 0 outside every entry)
+    if (pp.rope_off) {
+      for (int i = tid; i < nm * pp.max_blocks; i += nt) {
+        const int r = i / pp.max_blocks, b = i - r * pp.max_blocks, a = a0 + r;
+        const int e0 = pp.rope_off[a], e1 = pp.rope_off[a + 1];
+        int dl = 0;
+        for (int e = e0; e < e1; ++e) {
+          const int4 sg = __ldg(pp.rope_segs + e);
+          if (b >= sg.x && b - sg.x < sg.y) dl = sg.z;
+        }
+        if (dl <= -(1 << 18) || dl >= (1 << 18)) {
+          set_err(pp.status, KVS_DEVERR_ROPE_RANGE);
+          dl = 0;
+        }
+        pp.bdelta[(size_t)a * pp.max_blocks + b] = dl;
+      }
+      __syncthreads();
+    }
+    // 1. sharing
+    if (SG > 1 && pp.runs) {
+      plan_runs(pp, gi, a0, nm, s_key, s_dl, s_ex, &s_n);
+      __syncthreads();
+    } else if (SG > 1) {
       for (int b = tid; b < pp.max_blocks; b += nt) {
         int ph[32];
         for (int r = 0; r < nm; ++r) {
@@ -250,21 +454,6 @@ __global__ void __launch_bounds__(256) tm_plan_groups(PlanParams pp) {
       }
       __syncthreads();
     }
-    if (pp.rope_off) {   // SG == 1: the group is sequence a0
-      const int e0 = pp.rope_off[a0], e1 = pp.rope_off[a0 + 1];
-      for (int b = tid; b < pp.max_blocks; b += nt) {
-        int dl = 0;
-        for (int e = e0; e < e1; ++e) {
-          const int4 sg = __ldg(pp.rope_segs + e);
-          if (b >= sg.x && b - sg.x < sg.y) dl = sg.z;
-        }
-        if (dl <= -(1 << 18) || dl >= (1 << 18)) {
-          set_err(pp.status, KVS_DEVERR_ROPE_RANGE);
-          dl = 0;
-        }
-        pp.bdelta[(size_t)a0 * pp.max_blocks + b] = dl;
-      }
-    }
     // 2. chunk occupancy
     for (int i = tid; i < nm * pp.n_chunks; i += nt) {
       const int r = i / pp.n_chunks, c = i - r * pp.n_chunks, a = a0 + r;
@@ -274,7 +463,7 @@ __global__ void __launch_bounds__(256) tm_plan_groups(PlanParams pp) {
         any_priv |= SG > 1 ? !((pp.gmask[(size_t)gi * pp.max_blocks + b] >> r) & 1u) : 1;
       pp.pne[(size_t)a * pp.n_chunks + c] = (uint8_t)any_priv;
     }
-    if (SG > 1) {
+    if (SG > 1 && !pp.runs) {
       for (int c = tid; c < pp.n_chunks_s; c += nt) {
         uint32_t m = 0;
         for (int b = c * pp.ibs; b < min((c + 1) * pp.ibs, pp.max_blocks); ++b)
@@ -313,7 +502,7 @@ __global__ void __launch_bounds__(256) tm_plan_groups(PlanParams pp) {
 __global__ void __launch_bounds__(256) tm_plan_items(PlanParams pp) {
   __shared__ int warp_sums[32];
   __shared__ int s_base, s_wbase;
-  const int n_sh = pp.SG > 1 ? pp.n_groups * pp.n_chunks_s : 0, n_pr = pp.n_seq * pp.n_chunks;
+  const int n_sh = (pp.SG > 1 && !pp.runs) ? pp.n_groups * pp.n_chunks_s : 0, n_pr = pp.n_seq * pp.n_chunks;
   const int total = n_sh + n_pr;
   for (int base = blockIdx.x * blockDim.x; base < total; base += gridDim.x * blockDim.x) {
     const int i = base + threadIdx.x;
@@ -1063,6 +1252,8 @@ struct TmPtrs {
   int4* items;
   int4* witems;
   int2* wsub;
+  int2* wmem;
+  int4* wclaims;
   uint32_t* gmask;
   int32_t* gphys;
   uint8_t* pne;
@@ -1084,6 +1275,8 @@ static TmPtrs tm_ptrs(const TmLayout& L, const kvs_pool* pool, int n_seq, int g,
   t.spm = reinterpret_cast<uint32_t*>(w + L.off_spm);
   t.witems = reinterpret_cast<int4*>(w + L.off_witems);
   t.wsub = reinterpret_cast<int2*>(w + L.off_wsub);
+  t.wmem = reinterpret_cast<int2*>(w + L.off_wmem);
+  t.wclaims = reinterpret_cast<int4*>(w + L.off_wclaims);
   t.bdelta = reinterpret_cast<int32_t*>(w + L.off_bdelta);
   t.p1 = reinterpret_cast<float*>(w + L.off_p1);
   t.p1_ml = t.p1 + split_vals;
@@ -1122,7 +1315,11 @@ kvs_status decode_plan_token_major(kvs_pool* pool, int n_q_heads, const int32_t*
   pp.wide = L.wide ? 1 : 0;
   pp.witems = t.witems;
   pp.wsub = t.wsub;
+  pp.wmem = t.wmem;
+  pp.wclaims = t.wclaims;
   pp.max_sub = L.max_sub;
+  pp.runs = L.runs ? 1 : 0;
+  pp.max_witems = (int)std::min<size_t>(L.max_witems, 0x7fffffff);
   pp.G = g;
   pp.ib = L.ib;
   pp.n_chunks = L.n_chunks;
@@ -1131,6 +1328,8 @@ kvs_status decode_plan_token_major(kvs_pool* pool, int n_q_heads, const int32_t*
   pp.n_groups = L.n_groups;
   pp.capacity = pool->desc.capacity_blocks;
   pp.hkv = pool->desc.num_kv_heads;
+  // item counters start at zero (several CTAs add to them)
+  if (cudaMemsetAsync(t.hdr, 0, 64, stream) != cudaSuccess) return fail(KVS_ERR_CUDA, "decode_plan: memset failed");
   const int g1 = std::max(1, std::min(L.n_groups, pool->num_sms * 4));
   tm_plan_groups<<<g1, 256, 0, stream>>>(pp);
   count_launch();
@@ -1200,7 +1399,12 @@ kvs_status decode_attn_token_major(kvs_pool* pool, int layer, const void* q, int
     wp.witems = t.witems;
     wp.hdr = t.hdr;
     wp.wsub = t.wsub;
+    wp.wmem = t.wmem;
+    wp.wclaims = t.wclaims;
     wp.max_sub = L.max_sub;
+    wp.max_witems = (int)std::min<size_t>(L.max_witems, 0x7fffffff);
+    wp.runs = L.runs ? 1 : 0;
+    if (L.runs) std::memcpy(wp.rs, prm.rs.c, sizeof(wp.rs));
     wp.p2 = t.p2;
     wp.p2_ml = t.p2_ml;
     wp.status = pool->status;
@@ -1220,7 +1424,9 @@ kvs_status decode_attn_token_major(kvs_pool* pool, int layer, const void* q, int
     const int wide_claims = (int)std::min<size_t>(L.max_witems * d.num_kv_heads, 0x7fffffff);
     const kvs_status ws_ = launch_wide_tile(wp, pool, layer, wide_claims, stream);
     if (ws_ != KVS_OK) return ws_;
-    wide_launched = wide_claims > 0;
+    // rotation calls leave the token-major kernel the heavier part (private
+    // blocks and mirror diffs); it runs after the tile at full occupancy
+    wide_launched = wide_claims > 0 && !L.runs;
   }
   if (d.head_dim == 128) {
     if (dif) return rope ? launch_tm<128, true, true>(prm, pool, layer, max_claims, wide_launched, stream)

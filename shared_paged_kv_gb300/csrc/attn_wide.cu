@@ -38,8 +38,9 @@ constexpr int kWdSubBlocks = 8;          // blocks per sub-tile (128 tokens)
 constexpr int kWdHalf = 128 * 128;       // one [128][64] bf16 half of a 128-row tile, bytes
 constexpr int kWdTile = 2 * kWdHalf;     // a 128 x 128 bf16 tile
 // Q + ST stages of K and V (one stage when every item is a single sub-tile)
-template <int ST>
-constexpr int wd_smem() { return 1024 + kWdTile * (1 + 2 * ST); }
+// (rotation calls: Q hi and Q lo tiles)
+template <int ST, bool RUNS>
+constexpr int wd_smem() { return 1024 + kWdTile * ((RUNS ? 2 : 1) + 2 * ST); }
 constexpr uint32_t kWdCols = 512;        // S/P buffers at 0 and 128, O at 256
 
 __device__ __forceinline__ bool wd_wait(uint64_t* bar, uint32_t parity, uint32_t* status) {
@@ -47,44 +48,77 @@ __device__ __forceinline__ bool wd_wait(uint64_t* bar, uint32_t parity, uint32_t
   return __all_sync(0xffffffffu, ok);
 }
 
-// Position in this CTA's work: claim cl (item cl / hkv, KV head cl % hkv),
-// sub-tile j of the item.  Lane k < 8 holds block k's record {sharing
-// members, physical block} (members 0 past the chunk end).  The next
-// position's item and record are loaded one position ahead: their addresses
-// follow from the claim and sub-tile numbers alone.
+// Position in this CTA's work: claim cl (KV head cl % hkv) and sub-tile j.
+//  * Shared chunks: the claim is item cl / hkv, its sub-tiles the 8-block
+//    pieces of the item's chunk.
+//  * Rotation calls: the claim is range cl / hkv of a group's run items
+//    (cr = {group, first item, items | split slot << 16, members}), sub-tile
+//    j is item cr.y + j (one 8-block run).
+// Lane k < 8 holds block k's record {sharing members, physical block}
+// (members 0 past the chunk end).  The next position's item and record are
+// loaded one position ahead.
 struct WdCursor {
   int cl, j, n_cl, n_j;
-  int4 it, n_it;
+  int4 cr, n_cr;   // rotation calls: the claim's range
+  int4 it, n_it;   // the sub-tile's item
   int2 rec, n_rec;
 };
 
-__device__ __forceinline__ int wd_nsub(const WideParams& p, const int4& it) {
-  return (it.z - it.y * p.ib + kWdSubBlocks - 1) / kWdSubBlocks;
+template <bool RUNS>
+__device__ __forceinline__ int wd_nsub(const WideParams& p, const WdCursor& c) {
+  return RUNS ? (c.cr.z & 0xffff) : (c.it.z - c.it.y * p.ib + kWdSubBlocks - 1) / kWdSubBlocks;
 }
 
-__device__ __forceinline__ int2 wd_rec(const WideParams& p, int cl, int j, int lane) {
-  return lane < kWdSubBlocks ? __ldg(p.wsub + ((size_t)(cl / p.hkv) * p.max_sub + j) * kWdSubBlocks + lane)
-                             : make_int2(0, -1);
+// the item index of a position
+template <bool RUNS>
+__device__ __forceinline__ int wd_item(const WideParams& p, int cl, const int4& cr, int j) {
+  return RUNS ? cr.y + j : cl / p.hkv;
 }
 
+template <bool RUNS>
+__device__ __forceinline__ int2 wd_rec(const WideParams& p, int item, int j, int lane) {
+  const size_t o = RUNS ? (size_t)item * kWdSubBlocks : ((size_t)item * p.max_sub + j) * kWdSubBlocks;
+  return lane < kWdSubBlocks ? __ldg(p.wsub + o + lane) : make_int2(0, -1);
+}
+
+template <bool RUNS>
+__device__ __forceinline__ void wd_start(const WideParams& p, WdCursor& c, int lane) {
+  c.cl = blockIdx.x;
+  c.j = 0;
+  c.cr = RUNS ? __ldg(p.wclaims + blockIdx.x / p.hkv) : make_int4(0, 0, 0, 0);
+  // speculative (before the plan check): keep the index inside the arrays
+  const int item = RUNS ? min(max(c.cr.y, 0), p.max_witems - 1) : wd_item<RUNS>(p, c.cl, c.cr, 0);
+  c.it = __ldg(p.witems + item);
+  c.rec = wd_rec<RUNS>(p, item, 0, lane);
+}
+
+template <bool RUNS>
 __device__ __forceinline__ void wd_prefetch(const WideParams& p, WdCursor& c, int n_claims, int lane) {
   c.n_cl = c.cl;
   c.n_j = c.j + 1;
-  c.n_it = c.it;
-  if (c.n_j >= wd_nsub(p, c.it)) {
+  c.n_cr = c.cr;
+  if (c.n_j >= wd_nsub<RUNS>(p, c)) {
     c.n_cl = c.cl + gridDim.x;
     c.n_j = 0;
-    if (c.n_cl < n_claims) c.n_it = __ldg(p.witems + c.n_cl / p.hkv);
+    if (RUNS && c.n_cl < n_claims) c.n_cr = __ldg(p.wclaims + c.n_cl / p.hkv);
   }
-  c.n_rec = c.n_cl < n_claims ? wd_rec(p, c.n_cl, c.n_j, lane) : make_int2(0, -1);
+  c.n_it = c.it;
+  c.n_rec = make_int2(0, -1);
+  if (c.n_cl < n_claims) {
+    const int item = wd_item<RUNS>(p, c.n_cl, c.n_cr, c.n_j);
+    if (RUNS || c.n_cl != c.cl) c.n_it = __ldg(p.witems + item);
+    c.n_rec = wd_rec<RUNS>(p, item, c.n_j, lane);
+  }
 }
 
+template <bool RUNS>
 __device__ __forceinline__ void wd_advance(const WideParams& p, WdCursor& c, int n_claims, int lane) {
   c.cl = c.n_cl;
   c.j = c.n_j;
+  c.cr = c.n_cr;
   c.it = c.n_it;
   c.rec = c.n_rec;
-  if (c.cl < n_claims) wd_prefetch(p, c, n_claims, lane);
+  if (c.cl < n_claims) wd_prefetch<RUNS>(p, c, n_claims, lane);
 }
 
 // blocks of the sub-tile that somebody shares (bit j: block j is loaded)
@@ -98,7 +132,7 @@ struct WdBars {
 
 }  // namespace
 
-template <int ST>
+template <int ST, bool RUNS>
 __global__ void __launch_bounds__(kWdThreads, 1)
 attn_wide_kernel(const __grid_constant__ WideParams p, const __grid_constant__ CUtensorMap tk,
                  const __grid_constant__ CUtensorMap tv) {
@@ -106,28 +140,27 @@ attn_wide_kernel(const __grid_constant__ WideParams p, const __grid_constant__ C
   __shared__ WdBars bars;
   __shared__ uint32_t s_tmem;
   __shared__ volatile int s_abort;
+  __shared__ float rsc[RUNS ? 4 * 64 : 1];   // RoPE frequency pieces (rotation calls)
+  constexpr int QT = RUNS ? 2 : 1;           // query tiles: Q (or Q hi, Q lo)
   // the token-major kernel queued behind this one (programmatic dependent
   // launch) computes other splits: let it start on the SMs left free
   asm volatile("griddepcontrol.launch_dependents;");
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   uint8_t* base = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-  uint8_t* sQ = base;                                   // [2][128][64]
-  auto sK = [&](int s) { return base + kWdTile * (1 + 2 * s); };
-  auto sV = [&](int s) { return base + kWdTile * (2 + 2 * s); };
+  uint8_t* sQ = base;                                   // [2][128][64] (rotation calls: then Q lo)
+  auto sK = [&](int s) { return base + kWdTile * (QT + 2 * s); };
+  auto sV = [&](int s) { return base + kWdTile * (QT + 1 + 2 * s); };
 
   // the plan header, the first item and its first record are independent
   // loads: issue them together (the grid never exceeds the item capacity)
   WdCursor cur;
-  cur.cl = blockIdx.x;
-  cur.j = 0;
-  cur.it = __ldg(p.witems + blockIdx.x / p.hkv);
-  cur.rec = wd_rec(p, blockIdx.x, 0, lane);
+  wd_start<RUNS>(p, cur, lane);
   const bool plan_ok = p.hdr[1] == p.magic && p.hdr[2] == p.n_seq && p.hdr[3] == p.max_blocks &&
                        p.hdr[4] == p.R && p.hdr[5] == p.ibp && p.hdr[6] == p.hkv && p.hdr[7] == p.W &&
                        p.hdr[9] == p.ib;
-  const int n_claims = plan_ok ? p.hdr[8] * p.hkv : 0;
+  const int n_claims = plan_ok ? min(p.hdr[RUNS ? 10 : 8], p.max_witems) * p.hkv : 0;
   if ((int)blockIdx.x >= n_claims) return;   // uniform over the CTA: nothing allocated yet
-  wd_prefetch(p, cur, n_claims, lane);
+  wd_prefetch<RUNS>(p, cur, n_claims, lane);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < 2; ++s) {
@@ -143,6 +176,8 @@ attn_wide_kernel(const __grid_constant__ WideParams p, const __grid_constant__ C
     s_abort = 0;
     fence_barrier_init();
   }
+  if (RUNS)
+    for (int i = threadIdx.x; i < 4 * 64; i += blockDim.x) rsc[i] = p.rs[i >> 6][i & 63];
   if (warp == 0) {
     tmem_alloc(&s_tmem, kWdCols);
     tmem_relinquish();
@@ -161,7 +196,7 @@ attn_wide_kernel(const __grid_constant__ WideParams p, const __grid_constant__ C
     int n = 0;
     int armed[2] = {-1, -1};
     bool quit = false;
-    for (; cur.cl < n_claims; wd_advance(p, cur, n_claims, lane)) {
+    for (; cur.cl < n_claims; wd_advance<RUNS>(p, cur, n_claims, lane)) {
       if (stop()) { quit = true; break; }
       const uint32_t lm = wd_loaded(cur.rec);
       if (!lm) continue;
@@ -201,7 +236,7 @@ attn_wide_kernel(const __grid_constant__ WideParams p, const __grid_constant__ C
     constexpr uint32_t idS = umma_idesc_bf16(128, 128, false, false);
     constexpr uint32_t idO = umma_idesc_bf16(128, 128, false, true);
     const uint32_t tO = tmem + 256;
-    int n = 0, k = -1;
+    int n = 0, k = -1, qn = 0;
     bool first_pv = true;
     int pend = -1;
     uint32_t pend_lm = 0;
@@ -229,25 +264,29 @@ attn_wide_kernel(const __grid_constant__ WideParams p, const __grid_constant__ C
       first_pv = false;
       return true;
     };
-    for (; cur.cl < n_claims; wd_advance(p, cur, n_claims, lane)) {
+    for (; cur.cl < n_claims; wd_advance<RUNS>(p, cur, n_claims, lane)) {
       if (stop()) { ok = false; break; }
       if (cur.j == 0) {   // a new claim: its query tile must be in place
         ++k;
-        if (!wd_wait(&bars.q_full, k & 1, p.status)) { ok = false; break; }
+        if (!RUNS && !wd_wait(&bars.q_full, (qn++) & 1, p.status)) { ok = false; break; }
         first_pv = true;
         pend = -1;
       }
       const uint32_t lm = wd_loaded(cur.rec);
       if (lm) {
+        // rotation calls: every run has its own (rotated) query tile
+        if (RUNS && !wd_wait(&bars.q_full, (qn++) & 1, p.status)) { ok = false; break; }
         const int s = n & 1, ks = n % ST;   // TMEM buffer, shared-memory stage
         if (!wd_wait(&bars.kv_full[ks], (n / ST) & 1, p.status)) { ok = false; break; }
         if (n >= 2 && !wd_wait(&bars.pv_done[s], ((n - 2) >> 1) & 1, p.status)) { ok = false; break; }
         tc_fence_after();
         if (lane == 0) {
 #pragma unroll
-          for (int kk = 0; kk < 8; ++kk) {
-            const uint64_t a = umma_desc_sw128(smem_u32(sQ) + (kk >> 2) * kWdHalf + (kk & 3) * 32, 16, 1024);
-            const uint64_t b = umma_desc_sw128(smem_u32(sK(ks)) + (kk >> 2) * kWdHalf + (kk & 3) * 32, 16, 1024);
+          for (int kk = 0; kk < 8 * QT; ++kk) {   // rotation calls: Q hi, then Q lo
+            const uint64_t a =
+                umma_desc_sw128(smem_u32(sQ) + (kk >> 3) * kWdTile + ((kk >> 2) & 1) * kWdHalf + (kk & 3) * 32, 16, 1024);
+            const uint64_t b =
+                umma_desc_sw128(smem_u32(sK(ks)) + ((kk >> 2) & 1) * kWdHalf + (kk & 3) * 32, 16, 1024);
             umma_ss(tmem + 128u * s, a, b, idS, kk > 0 ? 1u : 0u);
           }
           umma_commit(&bars.s_full[s]);
@@ -319,7 +358,55 @@ attn_wide_kernel(const __grid_constant__ WideParams p, const __grid_constant__ C
         __stcg(reinterpret_cast<float2*>(p.p2_ml + it * 2), make_float2(e_m, e_l));
       }
     };
-    for (; cur.cl < n_claims; wd_advance(p, cur, n_claims, lane)) {
+    // The query rows of a claim (a rotation call: of one run item) into the
+    // Q tile ([half][row][64], 128-byte swizzle); the S MMAs that read the
+    // previous contents have completed.
+    auto load_q = [&](int gw, int h, const int4& it, int item) {
+      const int a = gw * p.W + slot;
+      row_ok = slot < p.W && a < p.n_seq;
+      const uint4* src = reinterpret_cast<const uint4*>(p.q + ((size_t)(row_ok ? a : 0) * p.hq + h * p.g + hh) * 128);
+      if (RUNS) {
+        // this member's query rotated back by its shift on this run,
+        // q' = R(-delta) q (rotate-half pairs i, i + 64), as bf16 hi (first
+        // tile) + lo (second tile); rows of non-members are zero
+        const bool mem = row_ok && ((((uint32_t)it.w) >> slot) & 1u);
+        const int dl = mem ? __ldg(p.wmem + (size_t)item * 32 + slot).y : 0;
+        const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll 1
+        for (int c = 0; c < 8; ++c) {   // dims 8c..8c+7 and their partners 64 + 8c..
+          const uint4 xv = mem ? __ldg(src + c) : z, yv = mem ? __ldg(src + 8 + c) : z;
+          const uint32_t xs[4] = {xv.x, xv.y, xv.z, xv.w}, ys[4] = {yv.x, yv.y, yv.z, yv.w};
+          uint32_t xh[4], xl[4], yh[4], yl[4];
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const float x0 = bf16_lo(xs[u]), x1 = bf16_hi(xs[u]), y0 = bf16_lo(ys[u]), y1 = bf16_hi(ys[u]);
+            float c0, s0, c1, s1;
+            rope_cos_sin(rsc, 8 * c + 2 * u, dl, c0, s0);
+            rope_cos_sin(rsc, 8 * c + 2 * u + 1, dl, c1, s1);
+            split_bf16(x0 * c0 + y0 * s0, x1 * c1 + y1 * s1, xh[u], xl[u]);
+            split_bf16(y0 * c0 - x0 * s0, y1 * c1 - x1 * s1, yh[u], yl[u]);
+          }
+          const uint32_t off = r * 128 + ((c ^ (r & 7)) << 4);
+          *reinterpret_cast<uint4*>(sQ + off) = make_uint4(xh[0], xh[1], xh[2], xh[3]);
+          *reinterpret_cast<uint4*>(sQ + kWdHalf + off) = make_uint4(yh[0], yh[1], yh[2], yh[3]);
+          *reinterpret_cast<uint4*>(sQ + kWdTile + off) = make_uint4(xl[0], xl[1], xl[2], xl[3]);
+          *reinterpret_cast<uint4*>(sQ + kWdTile + kWdHalf + off) = make_uint4(yl[0], yl[1], yl[2], yl[3]);
+        }
+      } else {
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf) {
+          uint4 qv[8];
+#pragma unroll
+          for (int c = 0; c < 8; ++c) qv[c] = row_ok ? __ldg(src + hf * 8 + c) : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+          for (int c = 0; c < 8; ++c)
+            *reinterpret_cast<uint4*>(sQ + hf * kWdHalf + r * 128 + ((c ^ (r & 7)) << 4)) = qv[c];
+        }
+      }
+      fence_proxy_async_smem();
+      mbar_arrive(&bars.q_full);
+    };
+    for (; cur.cl < n_claims; wd_advance<RUNS>(p, cur, n_claims, lane)) {
       if (stop()) { ok = false; break; }
       const int gw = cur.it.x & ((1 << 30) - 1), h = cur.cl % p.hkv;
       if (cur.j == 0) {   // a new claim
@@ -334,28 +421,16 @@ attn_wide_kernel(const __grid_constant__ WideParams p, const __grid_constant__ C
           tc_fence_before();
           mbar_arrive(&bars.o_free);
         }
-        // this claim's query rows into the Q tile ([half][row][64], 128-byte
-        // swizzle); every S of the previous claim has completed
         const int a = gw * p.W + slot;
         row_ok = slot < p.W && a < p.n_seq;
-        const uint4* src = reinterpret_cast<const uint4*>(p.q + ((size_t)(row_ok ? a : 0) * p.hq + h * p.g + hh) * 128);
-#pragma unroll
-        for (int hf = 0; hf < 2; ++hf) {
-          uint4 qv[8];
-#pragma unroll
-          for (int c = 0; c < 8; ++c) qv[c] = row_ok ? __ldg(src + hf * 8 + c) : make_uint4(0u, 0u, 0u, 0u);
-#pragma unroll
-          for (int c = 0; c < 8; ++c)
-            *reinterpret_cast<uint4*>(sQ + hf * kWdHalf + r * 128 + ((c ^ (r & 7)) << 4)) = qv[c];
-        }
-        fence_proxy_async_smem();
-        mbar_arrive(&bars.q_full);
+        if (!RUNS) load_q(gw, h, cur.it, 0);
         m = -INFINITY;
         l = 0.f;
         first = true;
       }
       const uint32_t lm = wd_loaded(cur.rec);
       if (lm) {
+        if (RUNS) load_q(gw, h, cur.it, cur.cr.y + cur.j);
         const int s = n & 1;
         uint32_t rl = 0;   // blocks this row takes
 #pragma unroll
@@ -428,8 +503,8 @@ attn_wide_kernel(const __grid_constant__ WideParams p, const __grid_constant__ C
         pend_epi = true;
         e_gw = gw;
         e_h = h;
-        e_c = cur.it.y;
-        e_spm = (uint32_t)cur.it.w;
+        e_c = RUNS ? (cur.cr.z >> 16) : cur.it.y;   // the claim's split slot
+        e_spm = (uint32_t)(RUNS ? cur.cr.w : cur.it.w);
         e_last = n - 1;
         e_m = m;
         e_l = l;
@@ -454,11 +529,11 @@ attn_wide_kernel(const __grid_constant__ WideParams p, const __grid_constant__ C
   }
 }
 
-template <int ST>
+template <int ST, bool RUNS>
 static kvs_status launch_wide(const WideParams& p, const kvs_pool* pool, int layer, int grid, cudaStream_t stream) {
-  if (!smem_limit_once<attn_wide_kernel<ST>>(wd_smem<ST>(), pool->device))
+  if (!smem_limit_once<attn_wide_kernel<ST, RUNS>>(wd_smem<ST, RUNS>(), pool->device))
     return fail(KVS_ERR_CUDA, "decode_attn: cannot raise the shared-memory limit (wide tile)");
-  attn_wide_kernel<ST><<<grid, kWdThreads, wd_smem<ST>(), stream>>>(p, pool->tk1[layer], pool->tv1[layer]);
+  attn_wide_kernel<ST, RUNS><<<grid, kWdThreads, wd_smem<ST, RUNS>(), stream>>>(p, pool->tk1[layer], pool->tv1[layer]);
   count_launch();
   return check_launch("decode_attn_wide");
 }
@@ -470,7 +545,11 @@ kvs_status launch_wide_tile(const WideParams& p, const kvs_pool* pool, int layer
   // beyond the plan's item count return at once.  Items of one sub-tile need
   // no second stage, which leaves room on the SM for a token-major CTA.
   const int grid = std::max(1, std::min(pool->num_sms, max_claims));
-  return p.max_sub > 1 ? launch_wide<2>(p, pool, layer, grid, stream) : launch_wide<1>(p, pool, layer, grid, stream);
+  // the MMA thread issues S of the next sub-tile before P V of the current
+  // one, so claims of several sub-tiles (and rotation ranges) need two stages
+  if (p.runs) return launch_wide<2, true>(p, pool, layer, grid, stream);
+  return p.max_sub > 1 ? launch_wide<2, false>(p, pool, layer, grid, stream)
+                      : launch_wide<1, false>(p, pool, layer, grid, stream);
 }
 
 }  // namespace kvs

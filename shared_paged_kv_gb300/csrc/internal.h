@@ -84,13 +84,18 @@ struct WideParams {
   const int4* witems;       // {kind | group, chunk, end block, member mask}
   const int* hdr;           // plan header ([8]: number of wide items)
   const int2* wsub;        // [item][max_sub][8] {sharing members, physical block} per block
+  const int2* wmem;        // rotation calls: [item][32] {split slot, RoPE shift} per member
+  const int4* wclaims;     // rotation calls: claims {group, first item, items | slot << 16, members}
   float* p2;                // [n_seq][hkv][n_chunks][g][128]
   float* p2_ml;             // [n_seq][hkv][n_chunks][g][2]
   uint32_t* status;
   int n_seq, max_blocks, hkv, g, hq, W, ib, n_chunks, R, capacity, max_sub;   // ib, n_chunks: shared chunks
   int ibp;                  // private chunk blocks (plan header check)
+  int max_witems;           // item capacity (the plan's counter may run past it)
+  int runs;                 // rotation call: items are 8-block runs, per-member shift and slot
   int magic;                // plan header check: magic, n_seq, max_blocks, R, ibp, hkv, W, ib
   float scale_log2;
+  float rs[4][64];          // RoPE frequency pieces (rotation calls), as RopeSplit::c
 };
 kvs_status launch_wide_tile(const WideParams& p, const kvs_pool* pool, int layer, int max_claims,
                             cudaStream_t stream);

@@ -146,3 +146,105 @@ def test_plan_routes_shared_chunks_to_the_wide_tile():
         hdr = ws[:64].cpu().numpy().view(np.int32)
         assert hdr[7] == 16
         assert (hdr[8] > 0) == expect_items
+
+
+def rope_case(table, seq_len, rope_off, rope_segs, hq, hkv, kf, vf, seed, diff_table=None, dkf=None, dvf=None):
+    """Rotation call over an explicit table, segment list and pool vs the
+    oracle (theta 1e6)."""
+    n, max_blocks = table.shape
+    d = kf.shape[-1]
+    kb, vb = W.f32_to_bf16_bits(kf), W.f32_to_bf16_bits(vf)
+    rng = np.random.default_rng(seed)
+    q_bits = W.f32_to_bf16_bits(rng.standard_normal((n, hq, d)).astype(np.float32))
+    kw = {}
+    dkb = dvb = None
+    if diff_table is not None:
+        dkb, dvb = W.f32_to_bf16_bits(dkf), W.f32_to_bf16_bits(dvf)
+        kw = dict(dk_layers=[H.bits_to_dev(dkb)], dv_layers=[H.bits_to_dev(dvb)], diff_capacity_blocks=dkb.shape[0])
+    pool = K.kvs_pool_create(1, hkv, d, 16, K.KVS_DTYPE_BF16, kb.shape[0], n, [H.bits_to_dev(kb)],
+                             [H.bits_to_dev(vb)], **kw)
+    w = SimpleNamespace(n_seq=n, n_q_heads=hq, head_dim=d, diff_table=diff_table, rope_off=rope_off,
+                        rope_segs=rope_segs, max_blocks=max_blocks, theta=1e6, scale=1.0 / np.sqrt(d),
+                        seq_len=seq_len)
+    got = H.attn(pool, 0, q_bits, w, table)
+    exp = OA.decode_attention(f32(q_bits), f32(kb), f32(vb), table, seq_len, 16, w.scale,
+                              diff_table=diff_table, dk_pool=f32(dkb) if dkb is not None else None,
+                              dv_pool=f32(dvb) if dvb is not None else None, rope_off=rope_off,
+                              rope_segs=rope_segs, theta=1e6)
+    H.assert_close_attn(got, exp)
+    assert K.kvs_pool_check(pool) == 0
+    return got
+
+
+def test_rotation_runs_shared_across_positions_and_shifts():
+    """G = 5 rotation call (groups of 25).  Three 8-block physical runs are
+    placed by each of 9 members after a private prefix of its own length, in
+    its own order and with its own shift: the tile shares each run across
+    members at different logical positions.  Corners: a member holds one run
+    twice (the first use is shared, the second private), a context ends
+    inside a run (that run stays private), a mirror diff on one block keeps
+    that member's run private, and two overlapping entries with equal shifts
+    (only runs inside the last covering entry may be shared)."""
+    rng = np.random.default_rng(61)
+    hq, hkv, d, n = 10, 2, 128, 9
+    runs = [np.arange(8) + 8 * j for j in range(3)]       # physical blocks 0..23
+    nxt = 24
+    rows, segs, lens = [], [], []
+    for a in range(n):
+        pre = int(rng.integers(0, 6))
+        order = list(rng.permutation(3)) + ([1] if a == 2 else [])
+        row = list(range(nxt, nxt + pre))
+        nxt += pre
+        sg = []
+        if pre:
+            sg.append([0, pre, int(rng.integers(-50, 50)), 0])
+        for j in order:
+            sg.append([len(row), 8, int(rng.integers(-3000, 3000)), 0])
+            row += list(runs[j])
+        if a == 4:   # equal-shift overlap: a later entry over the middle of the first two runs
+            f0 = sg[1 if pre else 0][0]
+            sg[1 if pre else 0][2] = sg[2 if pre else 1][2] = 777
+            sg.append([f0 + 4, 8, 777, 0])
+        tail = int(rng.integers(0, 4))
+        row += list(range(nxt, nxt + tail))
+        nxt += tail
+        L = 16 * len(row)
+        if a == 6:   # ends inside its last run: 5 of its 8 blocks, mid-block
+            row = row[:len(row) - tail - 3]
+            L = 16 * len(row) - 7
+        rows.append(row)
+        segs.append(sg)
+        lens.append(L)
+    max_blocks = max(len(r) for r in rows)
+    table = np.full((n, max_blocks), -1, np.int32)
+    for a, r in enumerate(rows):
+        table[a, :len(r)] = r
+    seq_len = np.array(lens, np.int32)
+    rope_off = np.zeros(n + 1, np.int32)
+    rope_off[1:] = np.cumsum([len(s) for s in segs])
+    rope_segs = np.array([x for s in segs for x in s], np.int32).reshape(-1, 4)
+    diff_table = np.full((n, max_blocks), -1, np.int32)
+    diff_table[7, int(np.where(table[7] == 11)[0][0])] = 0   # member 7: a diff inside run 1
+    cap = nxt
+    kf = rng.standard_normal((cap, hkv, 16, d)).astype(np.float32)
+    vf = rng.standard_normal((cap, hkv, 16, d)).astype(np.float32)
+    dkf = 0.1 * rng.standard_normal((1, hkv, 16, d)).astype(np.float32)
+    dvf = 0.1 * rng.standard_normal((1, hkv, 16, d)).astype(np.float32)
+    rope_case(table, seq_len, rope_off, rope_segs, hq, hkv, kf, vf, seed=62, diff_table=diff_table, dkf=dkf,
+              dvf=dvf)
+
+
+def test_plan_routes_rotation_runs_to_the_wide_tile():
+    """A rotation call with G = 5 (all-gather shape): the plan groups 25
+    sequences and turns the shared 128-token segments into wide run items."""
+    w = W.make_allgather(seed=13, n_seq=6, n_segs=6, priv_blocks_lo=3, priv_blocks_hi=9, hq=10, hkv=2, n_layers=1)
+    from oracle import fingerprint as OF
+    ref = OF.dedup(w.tokens, w.seq_off, w.tier, w.block_tokens, w.max_blocks, w.seg_start_off, w.seg_start_blocks)
+    pool = H.bf16_pool(w)
+    ws = H.workspace(K.kvs_workspace_size(pool, K.KVS_OP_DECODE_ATTN, w.n_seq, w.max_blocks, w.n_q_heads))
+    K.kvs_decode_plan(pool, w.n_q_heads, H.i32(ref["block_table"]), w.max_blocks, H.i32(w.seq_len), w.n_seq,
+                      H.i32(w.diff_table), H.i32(w.rope_off), H.i32(w.rope_segs), ws)
+    torch.cuda.synchronize()
+    hdr = ws[:64].cpu().numpy().view(np.int32)
+    assert hdr[7] == 25
+    assert hdr[8] >= 4   # most of the 6 segments are shared by at least two of the 6 agents
