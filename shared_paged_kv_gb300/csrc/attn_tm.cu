@@ -191,6 +191,7 @@ struct PlanParams {
   float* p2_ml;      // (m, l) of the shared splits [n_seq][hkv][n_chunks_s][g] (SG > 1)
   int n_seq, max_blocks, R, SG, G, ib, n_chunks, ibs, n_chunks_s, n_groups, capacity, hkv, wide, max_sub, runs;
   int max_witems;
+  int wide_ctas;     // CTAs of the wide tile's grid (rotation calls size their claims to it)
 };
 
 __device__ __forceinline__ int plan_seq_blocks(const int32_t* seq_len, int a, int max_blocks) {
@@ -224,7 +225,6 @@ __device__ __forceinline__ int plan_seq_blocks(const int32_t* seq_len, int a, in
 // Runs found by at least two members become wide items; a member's other
 // blocks stay private.  All threads of the CTA call this.
 constexpr int kRunCap = 2048;
-constexpr int kRunsPerClaim = 8;   // run items per wide-tile claim (at least)
 constexpr int kMaxRanges = 256;    // claims per group (at most)
 
 __device__ void plan_runs(const PlanParams& pp, int gi, int a0, int nm, unsigned long long* s_key, int* s_dl,
@@ -334,8 +334,14 @@ __device__ void plan_runs(const PlanParams& pp, int gi, int a0, int nm, unsigned
     const int base = total ? atomicAdd(pp.hdr + 8, total) : 0;
     const int created = max(0, min(total, pp.max_witems - base));   // beyond the capacity: stays private
     // claims of the wide tile: ranges of consecutive items (one split per
-    // member and range); at most min(n_chunks_s, kMaxRanges) ranges
-    const int rg = max(kRunsPerClaim, (created + min(pp.n_chunks_s, kMaxRanges) - 1) / min(pp.n_chunks_s, kMaxRanges));
+    // member and range).  Every group's runs cost the same per item, so each
+    // group takes an equal share of the wide grid's CTAs per KV head and
+    // cuts its items into that many ranges: one claim per CTA, the fewest
+    // items per CTA, one split per member and range.  At most
+    // min(n_chunks_s, kMaxRanges) ranges (the split slots).
+    const int share = max(1, pp.wide_ctas / max(1, pp.hkv * pp.n_groups));
+    const int max_r = min(min(pp.n_chunks_s, kMaxRanges), share);
+    const int rg = max(1, (created + max_r - 1) / max_r);
     const int n_r = (created + rg - 1) / rg;
     s_base = base;
     s_created = created;
@@ -1328,6 +1334,7 @@ kvs_status decode_plan_token_major(kvs_pool* pool, int n_q_heads, const int32_t*
   pp.n_groups = L.n_groups;
   pp.capacity = pool->desc.capacity_blocks;
   pp.hkv = pool->desc.num_kv_heads;
+  pp.wide_ctas = pool->num_sms;   // the wide tile's grid is at most one CTA per SM
   // item counters start at zero (several CTAs add to them)
   if (cudaMemsetAsync(t.hdr, 0, 64, stream) != cudaSuccess) return fail(KVS_ERR_CUDA, "decode_plan: memset failed");
   const int g1 = std::max(1, std::min(L.n_groups, pool->num_sms * 4));
