@@ -84,10 +84,14 @@ __host__ __device__ constexpr int tm_smem_bytes() {
 struct TmLayout {
   int R, SG, ib, n_chunks, ibs, n_chunks_s, n_groups;   // private and shared chunk sizes / counts
   bool wide, runs;   // runs: rotation call on the wide tile (shared 8-block segment runs)
+  bool compact;      // private items over each member's list of unshared blocks
   size_t max_items, max_witems;
   int max_sub;   // 8-block sub-tiles per wide item
-  size_t off_hdr, off_items, off_witems, off_wsub, off_wmem, off_wclaims, off_gmask, off_gphys, off_bdelta, off_pne, off_spm, off_p1, off_p2, total;
+  size_t off_hdr, off_items, off_witems, off_wsub, off_wmem, off_wclaims, off_gmask, off_gphys, off_bdelta, off_pne, off_spm,
+      off_plist, off_pcnt, off_p1, off_p2, total;
 };
+
+constexpr int kMaxRanges = 256;    // wide-tile claims (split slots) per group, at most
 
 static size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
@@ -130,10 +134,21 @@ static TmLayout tm_layout(const kvs_pool* pool, int n_seq, int max_blocks, int g
   L.n_chunks_s = (max_blocks + L.ibs - 1) / L.ibs;
   L.n_groups = (n_seq + L.SG - 1) / L.SG;
   const size_t grp = L.SG > 1 ? (size_t)L.n_groups : 0;   // group arrays exist only with grouping
-  L.max_items = (L.wide ? 0 : grp * L.n_chunks_s) + (size_t)n_seq * L.n_chunks;
   // a rotation call's items are 8-block runs keyed by physical block: a group
   // can hold up to half its members' runs as items
   L.max_witems = L.wide ? grp * L.n_chunks_s * (L.runs ? std::max(1, L.SG / 2) : 1) : 0;
+  if (L.runs) {
+    // the shared splits of a rotation call are one per claim range, and a
+    // group cuts its runs into at most its share of the wide grid's CTAs
+    const int share = std::max(1, pool->num_sms / std::max(1, pool->desc.num_kv_heads * L.n_groups));
+    L.n_chunks_s = std::min(std::min(L.n_chunks_s, kMaxRanges), share);
+  }
+  // Rotation calls: a member's unshared blocks are its private history plus
+  // the scattered segment blocks that carry a mirror diff.  Its private items
+  // are taken over the list of those blocks (positions k, k + n, k + 2n, ...
+  // for item k of n), so that the diff blocks spread over all its items.
+  L.compact = L.runs;
+  L.max_items = (L.wide ? 0 : grp * L.n_chunks_s) + (size_t)n_seq * L.n_chunks;
   L.max_sub = (L.ibs + 7) / 8;
   const size_t per_split = (size_t)n_seq * pool->desc.num_kv_heads * g * (pool->desc.head_dim + 2) * sizeof(float);
   const size_t split_bytes = per_split * L.n_chunks, split_bytes_s = per_split * L.n_chunks_s;
@@ -149,6 +164,8 @@ static TmLayout tm_layout(const kvs_pool* pool, int n_seq, int max_blocks, int g
   L.off_bdelta = o; o = align256(o + (rope ? (size_t)n_seq * max_blocks * sizeof(int32_t) : 0));
   L.off_pne = o; o = align256(o + (size_t)n_seq * L.n_chunks);
   L.off_spm = o; o = align256(o + grp * L.n_chunks_s * sizeof(uint32_t));
+  L.off_plist = o; o = align256(o + (L.compact ? (size_t)n_seq * max_blocks * sizeof(int32_t) : 0));
+  L.off_pcnt = o; o = align256(o + (L.compact ? (size_t)n_seq * sizeof(int32_t) : 0));
   L.off_p1 = o; o = align256(o + split_bytes);
   L.off_p2 = o; o = align256(o + (L.SG > 1 ? split_bytes_s : 0));
   L.total = o;
@@ -168,7 +185,7 @@ size_t tm_workspace_bytes(const kvs_pool* pool, int n_seq, int max_blocks, int g
 //
 // Header: [0] token-major items, [1] magic, [2] n_seq, [3] max_blocks, [4] R,
 // [5] ib, [6] hkv, [7] SG, [8] wide items, [9] ibs, [10] wide claims (rotation
-// calls: ranges of run items).
+// calls: ranges of run items), [11] compact private items.
 struct PlanParams {
   const int32_t* block_table;
   const int32_t* seq_len;
@@ -192,6 +209,9 @@ struct PlanParams {
   int n_seq, max_blocks, R, SG, G, ib, n_chunks, ibs, n_chunks_s, n_groups, capacity, hkv, wide, max_sub, runs;
   int max_witems;
   int wide_ctas;     // CTAs of the wide tile's grid (rotation calls size their claims to it)
+  int32_t* plist;    // compact items: [n_seq][max_blocks] each member's unshared logical blocks, in order
+  int32_t* pcnt;     // compact items: [n_seq] length of that list
+  int compact;
 };
 
 __device__ __forceinline__ int plan_seq_blocks(const int32_t* seq_len, int a, int max_blocks) {
@@ -225,7 +245,6 @@ __device__ __forceinline__ int plan_seq_blocks(const int32_t* seq_len, int a, in
 // Runs found by at least two members become wide items; a member's other
 // blocks stay private.  All threads of the CTA call this.
 constexpr int kRunCap = 2048;
-constexpr int kMaxRanges = 256;    // claims per group (at most)
 
 __device__ void plan_runs(const PlanParams& pp, int gi, int a0, int nm, unsigned long long* s_key, int* s_dl,
                           uint8_t* s_ex, int* s_n) {
@@ -391,6 +410,7 @@ __global__ void __launch_bounds__(256) tm_plan_groups(PlanParams pp) {
   __shared__ int s_dl[kRunCap];
   __shared__ uint8_t s_ex[kRunCap];
   __shared__ int s_n;
+  __shared__ int s_wsum[32];
   const int tid = threadIdx.x, nt = blockDim.x;
   if (blockIdx.x == 0 && tid == 0) {
     pp.hdr[0] = 0;   // item counts, accumulated by tm_plan_items (and, for runs, here)
@@ -402,6 +422,7 @@ __global__ void __launch_bounds__(256) tm_plan_groups(PlanParams pp) {
     pp.hdr[6] = pp.hkv;
     pp.hdr[7] = pp.SG;
     pp.hdr[9] = pp.ibs;
+    pp.hdr[11] = pp.compact;
   }
   const float2 none = make_float2(-INFINITY, 0.f);
   const int SG = pp.SG;
@@ -460,7 +481,25 @@ __global__ void __launch_bounds__(256) tm_plan_groups(PlanParams pp) {
       }
       __syncthreads();
     }
-    // 2. chunk occupancy
+    // 2. chunk occupancy (compact items: the list of unshared blocks first)
+    if (pp.compact) {
+      for (int r = 0; r < nm; ++r) {
+        const int a = a0 + r;
+        const int nb = plan_seq_blocks(pp.seq_len, a, pp.max_blocks);
+        int cnt = 0;
+        for (int b0 = 0; b0 < pp.max_blocks; b0 += nt) {   // the same trip count on every thread
+          const int b = b0 + tid;
+          const int keep = (b < nb && !((pp.gmask[(size_t)gi * pp.max_blocks + b] >> r) & 1u)) ? 1 : 0;
+          int tot;
+          const int pos = block_exclusive_scan(keep, s_wsum, tot);
+          if (keep) pp.plist[(size_t)a * pp.max_blocks + cnt + pos] = b;
+          cnt += tot;
+        }
+        const int ni = (cnt + pp.ib - 1) / pp.ib;
+        if (tid == 0) pp.pcnt[a] = cnt;
+        for (int c = tid; c < pp.n_chunks; c += nt) pp.pne[(size_t)a * pp.n_chunks + c] = (uint8_t)(c < ni);
+      }
+    } else
     for (int i = tid; i < nm * pp.n_chunks; i += nt) {
       const int r = i / pp.n_chunks, c = i - r * pp.n_chunks, a = a0 + r;
       const int nb = plan_seq_blocks(pp.seq_len, a, pp.max_blocks);
@@ -528,8 +567,10 @@ __global__ void __launch_bounds__(256) tm_plan_items(PlanParams pp) {
       const int j = i - n_sh;
       const int c = j / pp.n_seq, a = j - c * pp.n_seq;
       keep = pp.pne[(size_t)a * pp.n_chunks + c];
+      // z: the end block, or (compact items) the length of the member's list
       if (keep)
-        item = make_int4(a, c, min((c + 1) * pp.ib, plan_seq_blocks(pp.seq_len, a, pp.max_blocks)), 1 << (a % pp.R));
+        item = make_int4(a, c, pp.compact ? pp.pcnt[a] : min((c + 1) * pp.ib, plan_seq_blocks(pp.seq_len, a, pp.max_blocks)),
+                         1 << (a % pp.R));
     }
     int cnt, cnt_w = 0, pos_w = 0;
     const int pos = block_exclusive_scan(keep, warp_sums, cnt);
@@ -573,7 +614,9 @@ struct TmParams {
   const int4* items;
   const uint32_t* gmask;
   const int32_t* gphys;
+  const int32_t* plist;   // compact items: each member's unshared logical blocks
   uint32_t* status;
+  int compact;            // private items over plist (rotation calls on the wide tile)
   int max_blocks, n_seq, hkv, g, hq, ib, n_chunks, ibs, n_chunks_s, R, SG, capacity, diff_capacity;
   int mwpr;           // merge warps per output row
   int stall_first;    // test-only (KVS_TEST_STALL_ONE_STAGE): leave one stage unarmed
@@ -641,7 +684,7 @@ attn_tm_kernel(const __grid_constant__ TmParams p, const __grid_constant__ CUten
   // the plan must have been built for this call's shapes
   const bool plan_ok = p.hdr[1] == kPlanMagic && p.hdr[2] == p.n_seq && p.hdr[3] == p.max_blocks &&
                        p.hdr[4] == p.R && p.hdr[5] == p.ib && p.hdr[6] == p.hkv && p.hdr[7] == p.SG &&
-                       p.hdr[9] == p.ibs;
+                       p.hdr[9] == p.ibs && p.hdr[11] == p.compact;
   if (!plan_ok && threadIdx.x == 0 && blockIdx.x == 0) set_err(p.status, KVS_DEVERR_PLAN);
   const int n_claims = plan_ok ? p.hdr[0] * p.hkv : 0;
   const int R = p.R;
@@ -654,17 +697,26 @@ attn_tm_kernel(const __grid_constant__ TmParams p, const __grid_constant__ CUten
   const int T = gridDim.x * kTmWarps;
   int n_id = blockIdx.x * kTmWarps + warp;   // next claim
   int4 n_it = make_int4(0, 0, 0, 0), nn_it = n_it;
-  int n_tab = -1, n_aux = 0, n_dif = -1, n_len = 0, n_dlt = 0;
+  int n_tab = -1, n_aux = 0, n_dif = -1, n_len = 0, n_dlt = 0, n_lb = 0;
   auto load_item = [&](int id) {
     return id < n_claims ? __ldg(p.items + id / p.hkv) : make_int4(0, 0, 0, 0);
   };
   // issue the loads for claim id (item entry it); nothing here consumes them
   auto prepare = [&](int id, const int4& it) {
-    n_tab = -1; n_aux = 0; n_dif = -1; n_len = 0; n_dlt = 0;
+    n_tab = -1; n_aux = 0; n_dif = -1; n_len = 0; n_dlt = 0; n_lb = 0;
     if (id >= n_claims) return;
     const int kind = it.x >> 30, idx = it.x & ((1 << 30) - 1);
-    const int b = it.y * p.ib + lane;
-    const bool in = b < it.z;
+    // lane j holds the item's block j: logical block chunk * ib + j, or
+    // (compact items, private) position chunk + j * n of the member's list
+    // of unshared blocks, n = its item count
+    int b = it.y * p.ib + lane;
+    bool in = b < it.z;
+    if (p.compact && !kind) {
+      const int ni = (it.z + p.ib - 1) / p.ib, li = it.y + lane * ni;
+      in = lane < p.ib && li < it.z;
+      b = in ? __ldg(p.plist + (size_t)idx * p.max_blocks + li) : 0;
+    }
+    n_lb = b;
     if (kind) {
       if (in) {
         n_tab = __ldg(p.gphys + (size_t)idx * p.max_blocks + b);
@@ -674,7 +726,8 @@ attn_tm_kernel(const __grid_constant__ TmParams p, const __grid_constant__ CUten
     } else {
       if (in) {
         n_tab = __ldg(p.block_table + (size_t)idx * p.max_blocks + b);
-        if (p.SG > 1) n_aux = (int)__ldg(p.gmask + (size_t)(idx / p.SG) * p.max_blocks + b);   // raw member bits
+        // raw member bits (a compact list holds unshared blocks only)
+        if (p.SG > 1 && !p.compact) n_aux = (int)__ldg(p.gmask + (size_t)(idx / p.SG) * p.max_blocks + b);
         if (DIFF) n_dif = __ldg(p.diff_table + (size_t)idx * p.max_blocks + b);
         if (ROPE) n_dlt = __ldg(p.bdelta + (size_t)idx * p.max_blocks + b);
       }
@@ -698,7 +751,8 @@ attn_tm_kernel(const __grid_constant__ TmParams p, const __grid_constant__ CUten
 
   int ord = -1;   // ordinal of the current claim
   int p_kind = 0, p_h = 0, p_b = 0, p_b0 = 0, p_bend = 0, p_mask = 0, p_slot = 0;
-  int tab_ent = -1, dif_ent = -1, aux_ent = 0, dlt_ent = 0;
+  int tab_ent = -1, dif_ent = -1, aux_ent = 0, dlt_ent = 0, lb_ent = 0;
+  bool p_compact = false;   // the current item's blocks come from lb_ent
   bool p_done = false;
   auto claim = [&]() {
     if (n_id >= n_claims) {
@@ -711,12 +765,19 @@ attn_tm_kernel(const __grid_constant__ TmParams p, const __grid_constant__ CUten
     p_h = n_id - (n_id / p.hkv) * p.hkv;
     p_b0 = p_b = it.y * p.ib;
     p_bend = it.z;
+    p_compact = p.compact && !p_kind;
+    if (p_compact) {   // the item's block count: list positions it.y + j * n below it.z
+      const int ni = (it.z + p.ib - 1) / p.ib;
+      p_b0 = p_b = 0;
+      p_bend = (it.z - it.y + ni - 1) / ni;
+    }
     p_mask = it.w;
     p_slot = p_kind ? 0 : (it.x & ((1 << 30) - 1)) % p.SG;
     tab_ent = n_tab;
     aux_ent = n_aux;
     dif_ent = n_dif;
     dlt_ent = n_dlt;
+    lb_ent = n_lb;
     TmRec& rec = recs[warp][ord & (kTmRec - 1)];
     if (lane == 0) {
       rec.id = n_id;
@@ -751,6 +812,7 @@ attn_tm_kernel(const __grid_constant__ TmParams p, const __grid_constant__ CUten
       if (p_done) break;
       const int j = p_b - p_b0;
       b = p_b++;
+      if (p_compact) b = __shfl_sync(0xffffffffu, lb_ent, j);
       const int ent = __shfl_sync(0xffffffffu, tab_ent, j);
       const int aux = __shfl_sync(0xffffffffu, aux_ent, j);
       if (p_kind == 0) {
@@ -1084,7 +1146,7 @@ __global__ void __launch_bounds__(kMergeWarps * 32, 2) tm_merge_kernel(const __g
   // go out together with the first (m, l) loads)
   const bool plan_ok = p.hdr[1] == kPlanMagic && p.hdr[2] == p.n_seq && p.hdr[3] == p.max_blocks &&
                        p.hdr[4] == p.R && p.hdr[5] == p.ib && p.hdr[6] == p.hkv && p.hdr[7] == p.SG &&
-                       p.hdr[9] == p.ibs;
+                       p.hdr[9] == p.ibs && p.hdr[11] == p.compact;
 
   // lane k owns slot w0 + k of each 32-slot window of this warp's range; the
   // first window keeps its (m, l) in registers between the passes.  The plan
@@ -1265,6 +1327,8 @@ struct TmPtrs {
   uint8_t* pne;
   uint32_t* spm;
   int32_t* bdelta;
+  int32_t* plist;
+  int32_t* pcnt;
   float *p1, *p1_ml, *p2, *p2_ml;
 };
 
@@ -1284,6 +1348,8 @@ static TmPtrs tm_ptrs(const TmLayout& L, const kvs_pool* pool, int n_seq, int g,
   t.wmem = reinterpret_cast<int2*>(w + L.off_wmem);
   t.wclaims = reinterpret_cast<int4*>(w + L.off_wclaims);
   t.bdelta = reinterpret_cast<int32_t*>(w + L.off_bdelta);
+  t.plist = reinterpret_cast<int32_t*>(w + L.off_plist);
+  t.pcnt = reinterpret_cast<int32_t*>(w + L.off_pcnt);
   t.p1 = reinterpret_cast<float*>(w + L.off_p1);
   t.p1_ml = t.p1 + split_vals;
   t.p2 = reinterpret_cast<float*>(w + L.off_p2);
@@ -1335,6 +1401,9 @@ kvs_status decode_plan_token_major(kvs_pool* pool, int n_q_heads, const int32_t*
   pp.capacity = pool->desc.capacity_blocks;
   pp.hkv = pool->desc.num_kv_heads;
   pp.wide_ctas = pool->num_sms;   // the wide tile's grid is at most one CTA per SM
+  pp.plist = t.plist;
+  pp.pcnt = t.pcnt;
+  pp.compact = L.compact ? 1 : 0;
   // item counters start at zero (several CTAs add to them)
   if (cudaMemsetAsync(t.hdr, 0, 64, stream) != cudaSuccess) return fail(KVS_ERR_CUDA, "decode_plan: memset failed");
   const int g1 = std::max(1, std::min(L.n_groups, pool->num_sms * 4));
@@ -1373,6 +1442,8 @@ kvs_status decode_attn_token_major(kvs_pool* pool, int layer, const void* q, int
   prm.items = t.items;
   prm.gmask = t.gmask;
   prm.gphys = t.gphys;
+  prm.plist = t.plist;
+  prm.compact = L.compact ? 1 : 0;
   prm.status = pool->status;
   prm.max_blocks = max_blocks;
   prm.n_seq = n_seq;
