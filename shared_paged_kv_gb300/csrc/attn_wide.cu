@@ -42,6 +42,10 @@ constexpr int kWdTile = 2 * kWdHalf;     // a 128 x 128 bf16 tile
 template <int ST, bool RUNS>
 constexpr int wd_smem() { return 1024 + kWdTile * ((RUNS ? 2 : 1) + 2 * ST); }
 constexpr uint32_t kWdCols = 512;        // S/P buffers at 0 and 128, O at 256
+// rotation calls: per row warp, (cos, sin) of a run's shift for each member
+// slot of its 32 rows (at most 8 for G >= 4), 64 frequencies per slot; the
+// row stride is padded by 16 bytes so that slots fall in different banks
+constexpr int kWdTblSlots = 8, kWdTblStride = 66;
 
 __device__ __forceinline__ bool wd_wait(uint64_t* bar, uint32_t parity, uint32_t* status) {
   const bool ok = mbar_wait_bounded(bar, parity, status);
@@ -141,6 +145,7 @@ attn_wide_kernel(const __grid_constant__ WideParams p, const __grid_constant__ C
   __shared__ uint32_t s_tmem;
   __shared__ volatile int s_abort;
   __shared__ float rsc[RUNS ? 4 * 64 : 1];   // RoPE frequency pieces (rotation calls)
+  __shared__ __align__(16) float2 tbl[RUNS ? 4 * kWdTblSlots * kWdTblStride : 2];
   constexpr int QT = RUNS ? 2 : 1;           // query tiles: Q (or Q hi, Q lo)
   // the token-major kernel queued behind this one (programmatic dependent
   // launch) computes other splits: let it start on the SMs left free
@@ -327,6 +332,9 @@ attn_wide_kernel(const __grid_constant__ WideParams p, const __grid_constant__ C
     float e_m = 0.f, e_l = 0.f;
     float m = -INFINITY, l = 0.f;
     bool first = true, row_ok = false;
+    // rotation calls: this row's query (the claim's KV head), loaded once per
+    // claim and rotated from registers for each of its runs
+    uint4 qreg[RUNS ? 16 : 1];
     // The finished chunk's splits of this warp's 32 rows.  Each 32-column
     // slice of O goes from tensor memory through shared memory (128-byte
     // rows, XOR-swizzled) so that stores cover whole row segments.
@@ -365,26 +373,43 @@ attn_wide_kernel(const __grid_constant__ WideParams p, const __grid_constant__ C
       const int a = gw * p.W + slot;
       row_ok = slot < p.W && a < p.n_seq;
       const uint4* src = reinterpret_cast<const uint4*>(p.q + ((size_t)(row_ok ? a : 0) * p.hq + h * p.g + hh) * 128);
-      if (RUNS) {
+      if constexpr (RUNS) {
         // this member's query rotated back by its shift on this run,
         // q' = R(-delta) q (rotate-half pairs i, i + 64), as bf16 hi (first
-        // tile) + lo (second tile); rows of non-members are zero
+        // tile) + lo (second tile); rows of non-members are zero.  The
+        // angles are computed once per member slot of the warp's rows.
         const bool mem = row_ok && ((((uint32_t)it.w) >> slot) & 1u);
-        const int dl = mem ? __ldg(p.wmem + (size_t)item * 32 + slot).y : 0;
+        const int s_lo = (warp * 32) / p.g;
+        const int n_s = min((warp * 32 + 31) / p.g - s_lo + 1, kWdTblSlots);
+        int dl_own = 0;
+        if (lane < n_s) {
+          const int sl = s_lo + lane;
+          const bool mm = sl < p.W && gw * p.W + sl < p.n_seq && ((((uint32_t)it.w) >> sl) & 1u);
+          dl_own = mm ? __ldg(p.wmem + (size_t)item * 32 + sl).y : 0;
+        }
+        float2* tb = tbl + warp * (kWdTblSlots * kWdTblStride);
+        __syncwarp();   // the previous run's table has been read
+        for (int t = 0; t < 2 * n_s; ++t) {   // slot t / 2, frequencies 32 (t & 1) + lane
+          const int k = t >> 1, i = 32 * (t & 1) + lane;
+          const int dl = __shfl_sync(0xffffffffu, dl_own, k);
+          float cs, sn;
+          rope_cos_sin(rsc, i, dl, cs, sn);
+          tb[k * kWdTblStride + i] = make_float2(cs, sn);
+        }
+        __syncwarp();
+        const float2* mine = tb + min(max(slot - s_lo, 0), kWdTblSlots - 1) * kWdTblStride;
         const uint4 z = make_uint4(0u, 0u, 0u, 0u);
-#pragma unroll 1
+#pragma unroll
         for (int c = 0; c < 8; ++c) {   // dims 8c..8c+7 and their partners 64 + 8c..
-          const uint4 xv = mem ? __ldg(src + c) : z, yv = mem ? __ldg(src + 8 + c) : z;
+          const uint4 xv = mem ? qreg[c] : z, yv = mem ? qreg[8 + c] : z;
           const uint32_t xs[4] = {xv.x, xv.y, xv.z, xv.w}, ys[4] = {yv.x, yv.y, yv.z, yv.w};
           uint32_t xh[4], xl[4], yh[4], yl[4];
 #pragma unroll
           for (int u = 0; u < 4; ++u) {
             const float x0 = bf16_lo(xs[u]), x1 = bf16_hi(xs[u]), y0 = bf16_lo(ys[u]), y1 = bf16_hi(ys[u]);
-            float c0, s0, c1, s1;
-            rope_cos_sin(rsc, 8 * c + 2 * u, dl, c0, s0);
-            rope_cos_sin(rsc, 8 * c + 2 * u + 1, dl, c1, s1);
-            split_bf16(x0 * c0 + y0 * s0, x1 * c1 + y1 * s1, xh[u], xl[u]);
-            split_bf16(y0 * c0 - x0 * s0, y1 * c1 - x1 * s1, yh[u], yl[u]);
+            const float4 cs = *reinterpret_cast<const float4*>(mine + 8 * c + 2 * u);   // (c0, s0, c1, s1)
+            split_bf16(x0 * cs.x + y0 * cs.y, x1 * cs.z + y1 * cs.w, xh[u], xl[u]);
+            split_bf16(y0 * cs.x - x0 * cs.y, y1 * cs.z - x1 * cs.w, yh[u], yl[u]);
           }
           const uint32_t off = r * 128 + ((c ^ (r & 7)) << 4);
           *reinterpret_cast<uint4*>(sQ + off) = make_uint4(xh[0], xh[1], xh[2], xh[3]);
@@ -423,7 +448,13 @@ attn_wide_kernel(const __grid_constant__ WideParams p, const __grid_constant__ C
         }
         const int a = gw * p.W + slot;
         row_ok = slot < p.W && a < p.n_seq;
-        if (!RUNS) load_q(gw, h, cur.it, 0);
+        if constexpr (RUNS) {
+          const uint4* src = reinterpret_cast<const uint4*>(p.q + ((size_t)(row_ok ? a : 0) * p.hq + h * p.g + hh) * 128);
+#pragma unroll
+          for (int c = 0; c < 16; ++c) qreg[c] = row_ok ? __ldg(src + c) : make_uint4(0u, 0u, 0u, 0u);
+        } else {
+          load_q(gw, h, cur.it, 0);
+        }
         m = -INFINITY;
         l = 0.f;
         first = true;
