@@ -130,11 +130,11 @@ __device__ __forceinline__ uint32_t wd_loaded(const int2& rec) {
   return __ballot_sync(0xffffffffu, rec.x != 0) & 0xffu;
 }
 
-// Rotation calls use kv_full / kv_empty [0] for the single K buffer and [1]
-// for the single V buffer, and two query buffers (q_full[0..1]); otherwise
-// they are the ST K/V stages and the one query tile (q_full[0]).
+// kv_full / kv_empty: the ST K/V stages (rotation calls: the two K buffers,
+// with v_full / v_empty for the two V buffers, so that a K buffer is refilled
+// as soon as S has read it).
 struct WdBars {
-  uint64_t kv_full[2], kv_empty[2], s_full[2], p_full[2], pv_done[2], q_full[2], o_free, fin;
+  uint64_t kv_full[2], kv_empty[2], v_full[2], v_empty[2], s_full[2], p_full[2], pv_done[2], q_full, o_free, fin;
 };
 
 }  // namespace
@@ -155,13 +155,10 @@ attn_wide_kernel(const __grid_constant__ WideParams p, const __grid_constant__ C
   asm volatile("griddepcontrol.launch_dependents;");
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   uint8_t* base = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-  // Q: [2][128][64] (rotation calls: Q hi, Q lo of buffer 0, then buffer 1,
-  // then one K and one V tile)
-  uint8_t* sQ = base;
-  auto sQb = [&](int b) { return base + kWdTile * QT * b; };
-  auto sK = [&](int s) { return RUNS ? base + 4 * kWdTile : base + kWdTile * (QT + 2 * s); };
-  auto sV = [&](int s) { return RUNS ? base + 5 * kWdTile : base + kWdTile * (QT + 1 + 2 * s); };
-  static_assert(!RUNS || ST == 2, "rotation calls lay out two query buffers in the space of the second stage");
+  uint8_t* sQ = base;                                   // [2][128][64] (rotation calls: then Q lo)
+  auto sK = [&](int s) { return base + kWdTile * (QT + 2 * s); };
+  auto sV = [&](int s) { return base + kWdTile * (QT + 1 + 2 * s); };
+  static_assert(!RUNS || ST == 2, "rotation calls use two K and two V buffers");
 
   // the plan header, the first item and its first record are independent
   // loads: issue them together (the grid never exceeds the item capacity)
@@ -181,9 +178,10 @@ attn_wide_kernel(const __grid_constant__ WideParams p, const __grid_constant__ C
       mbar_init(&bars.s_full[s], 1);
       mbar_init(&bars.p_full[s], 128);
       mbar_init(&bars.pv_done[s], 1);
+      mbar_init(&bars.v_full[s], 1);
+      mbar_init(&bars.v_empty[s], 1);
     }
-    mbar_init(&bars.q_full[0], 128);
-    mbar_init(&bars.q_full[1], 128);
+    mbar_init(&bars.q_full, 128);
     mbar_init(&bars.o_free, 128);
     mbar_init(&bars.fin, 1);
     s_abort = 0;
@@ -207,12 +205,12 @@ attn_wide_kernel(const __grid_constant__ WideParams p, const __grid_constant__ C
     // lane k < 8 copies block k of the sub-tile: both 64-column halves of K
     // and of V into the [half][token][64] stage
     int n = 0;
-    int armed[2] = {-1, -1};   // parity of the last arming of kv_full[s]
+    int armed[2] = {-1, -1}, armed_v[2] = {-1, -1};   // parity of the last arming of kv_full / v_full [s]
     bool quit = false;
     // lanes k < 8 (bit k of lm) copy block k's two halves of K or V
-    auto copy = [&](const CUtensorMap* map, uint8_t* dst, uint64_t* bar, const int2& rec, int h, uint32_t lm) {
+    auto copy = [&](const CUtensorMap* map, uint8_t* dst, uint64_t* bar, int h, uint32_t lm) {
       if ((lm >> lane) & 1u) {
-        int ph = rec.y;
+        int ph = cur.rec.y;
         if (ph < 0 || ph >= p.capacity) {   // the plan shares valid blocks only
           set_err(p.status, KVS_DEVERR_BLOCK_ID);
           ph = 0;
@@ -223,73 +221,47 @@ attn_wide_kernel(const __grid_constant__ WideParams p, const __grid_constant__ C
       }
       __syncwarp();
     };
-    // rotation calls: V lags K by one position (the V buffer is free once
-    // P V of the position before has completed, which comes after S of the
-    // next one)
-    int2 v_rec = make_int2(0, -1);
-    int v_h = 0;
-    uint32_t v_lm = 0;
-    bool v_pend = false;
-    auto issue_v = [&](int m) {   // V of position m
-      if (m >= 1 && !wd_wait(&bars.kv_empty[1], (m - 1) & 1, p.status)) return false;
-      if (lane == 0) {
-        mbar_arrive_expect_tx(&bars.kv_full[1], (uint32_t)__popc(v_lm) * 2u * 2048u);
-        armed[1] = m & 1;
-      }
-      __syncwarp();
-      copy(&tv, sV(0), &bars.kv_full[1], v_rec, v_h, v_lm);
-      return true;
-    };
     for (; cur.cl < n_claims; wd_advance<RUNS>(p, cur, n_claims, lane)) {
       if (stop()) { quit = true; break; }
       const uint32_t lm = wd_loaded(cur.rec);
       if (!lm) continue;
+      const int s = n % ST, h = cur.cl % p.hkv;
+      // rotation calls: K buffer s is free once S of position n - 2 has
+      // completed, V buffer s once P V of n - 2 has; otherwise the stage is
+      // free once P V of n - ST has completed
+      if (n >= ST && !wd_wait(&bars.kv_empty[s], ((n - ST) / ST) & 1, p.status)) {
+        s_abort = 1;
+        quit = true;
+        break;
+      }
+      if (lane == 0) {
+        mbar_arrive_expect_tx(&bars.kv_full[s], (uint32_t)__popc(lm) * (RUNS ? 2u : 4u) * 2048u);
+        armed[s] = (n / ST) & 1;
+      }
+      __syncwarp();
+      copy(&tk, sK(s), &bars.kv_full[s], h, lm);
       if constexpr (RUNS) {
-        // K of position n: the K buffer is free once S of n - 1 has completed
-        if (n >= 1 && !wd_wait(&bars.kv_empty[0], (n - 1) & 1, p.status)) {
+        if (n >= ST && !wd_wait(&bars.v_empty[s], ((n - ST) / ST) & 1, p.status)) {
           s_abort = 1;
           quit = true;
           break;
         }
         if (lane == 0) {
-          mbar_arrive_expect_tx(&bars.kv_full[0], (uint32_t)__popc(lm) * 2u * 2048u);
-          armed[0] = n & 1;
+          mbar_arrive_expect_tx(&bars.v_full[s], (uint32_t)__popc(lm) * 2u * 2048u);
+          armed_v[s] = (n / ST) & 1;
         }
         __syncwarp();
-        copy(&tk, sK(0), &bars.kv_full[0], cur.rec, cur.cl % p.hkv, lm);
-        if (v_pend && !issue_v(n - 1)) {
-          s_abort = 1;
-          quit = true;
-          break;
-        }
-        v_rec = cur.rec;
-        v_h = cur.cl % p.hkv;
-        v_lm = lm;
-        v_pend = true;
+        copy(&tv, sV(s), &bars.v_full[s], h, lm);
       } else {
-        const int s = n % ST;
-        if (n >= ST && !wd_wait(&bars.kv_empty[s], ((n - ST) / ST) & 1, p.status)) {
-          s_abort = 1;
-          quit = true;
-          break;
-        }
-        if (lane == 0) {
-          mbar_arrive_expect_tx(&bars.kv_full[s], (uint32_t)__popc(lm) * 4u * 2048u);
-          armed[s] = (n / ST) & 1;
-        }
-        __syncwarp();
-        copy(&tk, sK(s), &bars.kv_full[s], cur.rec, cur.cl % p.hkv, lm);
-        copy(&tv, sV(s), &bars.kv_full[s], cur.rec, cur.cl % p.hkv, lm);
+        copy(&tv, sV(s), &bars.kv_full[s], h, lm);
       }
       ++n;
     }
-    if (RUNS && !quit && v_pend && !issue_v(n - 1)) {
-      s_abort = 1;
-      quit = true;
-    }
     if (quit) {   // copies still in flight land before the shared memory goes away
-      for (int s = 0; s < 2; ++s)
+      for (int s = 0; s < 2; ++s) {
         if (armed[s] >= 0) mbar_drain(&bars.kv_full[s], (uint32_t)armed[s]);
+        if (armed_v[s] >= 0) mbar_drain(&bars.v_full[s], (uint32_t)armed_v[s]);
+      }
     }
   } else if (warp == 4) {
     // ----------------------------------------------------------- MMA issue
@@ -304,7 +276,7 @@ attn_wide_kernel(const __grid_constant__ WideParams p, const __grid_constant__ C
     auto issue_pv = [&](int m, uint32_t lmm) {
       if (first_pv && k >= 1 && !wd_wait(&bars.o_free, (k - 1) & 1, p.status)) return false;
       if (!wd_wait(&bars.p_full[m & 1], (m >> 1) & 1, p.status)) return false;
-      if (RUNS && !wd_wait(&bars.kv_full[1], m & 1, p.status)) return false;   // V of position m
+      if (RUNS && !wd_wait(&bars.v_full[m % ST], (m / ST) & 1, p.status)) return false;   // V of position m
       tc_fence_after();
       if (lane == 0) {
         const uint32_t tP = tmem + 128u * (m & 1);
@@ -319,7 +291,7 @@ attn_wide_kernel(const __grid_constant__ WideParams p, const __grid_constant__ C
           acc = true;
         }
         umma_commit(&bars.pv_done[m & 1]);
-        umma_commit(&bars.kv_empty[RUNS ? 1 : m % ST]);
+        umma_commit(RUNS ? &bars.v_empty[m % ST] : &bars.kv_empty[m % ST]);
       }
       __syncwarp();
       first_pv = false;
@@ -329,30 +301,29 @@ attn_wide_kernel(const __grid_constant__ WideParams p, const __grid_constant__ C
       if (stop()) { ok = false; break; }
       if (cur.j == 0) {   // a new claim: its query tile must be in place
         ++k;
-        if (!RUNS && !wd_wait(&bars.q_full[0], (qn++) & 1, p.status)) { ok = false; break; }
+        if (!RUNS && !wd_wait(&bars.q_full, (qn++) & 1, p.status)) { ok = false; break; }
         first_pv = true;
         pend = -1;
       }
       const uint32_t lm = wd_loaded(cur.rec);
       if (lm) {
-        // rotation calls: every run has its own (rotated) query, in buffer n & 1
-        if (RUNS && !wd_wait(&bars.q_full[n & 1], (n >> 1) & 1, p.status)) { ok = false; break; }
-        const int s = n & 1, ks = RUNS ? 0 : n % ST;   // TMEM buffer, shared-memory stage
-        if (!wd_wait(&bars.kv_full[ks], RUNS ? (n & 1) : ((n / ST) & 1), p.status)) { ok = false; break; }
+        // rotation calls: every run has its own (rotated) query tile
+        if (RUNS && !wd_wait(&bars.q_full, (qn++) & 1, p.status)) { ok = false; break; }
+        const int s = n & 1, ks = n % ST;   // TMEM buffer, shared-memory stage
+        if (!wd_wait(&bars.kv_full[ks], (n / ST) & 1, p.status)) { ok = false; break; }
         if (n >= 2 && !wd_wait(&bars.pv_done[s], ((n - 2) >> 1) & 1, p.status)) { ok = false; break; }
         tc_fence_after();
         if (lane == 0) {
 #pragma unroll
           for (int kk = 0; kk < 8 * QT; ++kk) {   // rotation calls: Q hi, then Q lo
-            const uint64_t a = umma_desc_sw128(
-                smem_u32(sQb(RUNS ? (n & 1) : 0)) + (kk >> 3) * kWdTile + ((kk >> 2) & 1) * kWdHalf + (kk & 3) * 32, 16,
-                1024);
+            const uint64_t a =
+                umma_desc_sw128(smem_u32(sQ) + (kk >> 3) * kWdTile + ((kk >> 2) & 1) * kWdHalf + (kk & 3) * 32, 16, 1024);
             const uint64_t b =
                 umma_desc_sw128(smem_u32(sK(ks)) + ((kk >> 2) & 1) * kWdHalf + (kk & 3) * 32, 16, 1024);
             umma_ss(tmem + 128u * s, a, b, idS, kk > 0 ? 1u : 0u);
           }
           umma_commit(&bars.s_full[s]);
-          if (RUNS) umma_commit(&bars.kv_empty[0]);   // the K buffer (and query buffer n & 1) may be refilled
+          if (RUNS) umma_commit(&bars.kv_empty[ks]);   // K buffer ks may be refilled
         }
         __syncwarp();
         if (pend >= 0 && !issue_pv(pend, pend_lm)) { ok = false; break; }
@@ -424,10 +395,10 @@ attn_wide_kernel(const __grid_constant__ WideParams p, const __grid_constant__ C
         __stcg(reinterpret_cast<float2*>(p.p2_ml + it * 2), make_float2(e_m, e_l));
       }
     };
-    // The query rows of a claim (a rotation call: of one run item, into query
-    // buffer buf) into the Q tile ([half][row][64], 128-byte swizzle); the S
-    // MMAs that read the previous contents have completed.
-    auto load_q = [&](int gw, int h, const int4& it, int item, int buf) {
+    // The query rows of a claim (a rotation call: of one run item) into the
+    // Q tile ([half][row][64], 128-byte swizzle); the S MMAs that read the
+    // previous contents have completed.
+    auto load_q = [&](int gw, int h, const int4& it, int item) {
       const int a = gw * p.W + slot;
       row_ok = slot < p.W && a < p.n_seq;
       const uint4* src = reinterpret_cast<const uint4*>(p.q + ((size_t)(row_ok ? a : 0) * p.hq + h * p.g + hh) * 128);
@@ -470,7 +441,7 @@ attn_wide_kernel(const __grid_constant__ WideParams p, const __grid_constant__ C
             split_bf16(y0 * cs.x - x0 * cs.y, y1 * cs.z - x1 * cs.w, yh[u], yl[u]);
           }
           const uint32_t off = r * 128 + ((c ^ (r & 7)) << 4);
-          uint8_t* qd = sQb(buf);
+          uint8_t* qd = sQ;
           *reinterpret_cast<uint4*>(qd + off) = make_uint4(xh[0], xh[1], xh[2], xh[3]);
           *reinterpret_cast<uint4*>(qd + kWdHalf + off) = make_uint4(yh[0], yh[1], yh[2], yh[3]);
           *reinterpret_cast<uint4*>(qd + kWdTile + off) = make_uint4(xl[0], xl[1], xl[2], xl[3]);
@@ -488,7 +459,7 @@ attn_wide_kernel(const __grid_constant__ WideParams p, const __grid_constant__ C
         }
       }
       fence_proxy_async_smem();
-      mbar_arrive(&bars.q_full[RUNS ? buf : 0]);
+      mbar_arrive(&bars.q_full);
     };
     for (; cur.cl < n_claims; wd_advance<RUNS>(p, cur, n_claims, lane)) {
       if (stop()) { ok = false; break; }
@@ -512,7 +483,7 @@ attn_wide_kernel(const __grid_constant__ WideParams p, const __grid_constant__ C
 #pragma unroll
           for (int c = 0; c < 16; ++c) qreg[c] = row_ok ? __ldg(src + c) : make_uint4(0u, 0u, 0u, 0u);
         } else {
-          load_q(gw, h, cur.it, 0, 0);
+          load_q(gw, h, cur.it, 0);
         }
         m = -INFINITY;
         l = 0.f;
@@ -520,12 +491,9 @@ attn_wide_kernel(const __grid_constant__ WideParams p, const __grid_constant__ C
       }
       const uint32_t lm = wd_loaded(cur.rec);
       if (lm) {
-        if (RUNS) {
-          // the claim's first run is rotated here; every later one while the
-          // tensor cores compute S of the run before it
-          if (cur.j == 0) load_q(gw, h, cur.it, cur.cr.y, n & 1);
-          if (cur.n_cl == cur.cl) load_q(gw, h, cur.n_it, cur.cr.y + cur.j + 1, (n + 1) & 1);
-        }
+        // rotation calls: the claim's first run is rotated here, every later
+        // one once S of the run before it has read the query tile (below)
+        if (RUNS && cur.j == 0) load_q(gw, h, cur.it, cur.cr.y);
         const int s = n & 1;
         uint32_t rl = 0;   // blocks this row takes
 #pragma unroll
@@ -535,6 +503,8 @@ attn_wide_kernel(const __grid_constant__ WideParams p, const __grid_constant__ C
         }
         if (!wd_wait(&bars.s_full[s], (n >> 1) & 1, p.status)) { ok = false; break; }
         tc_fence_after();
+        // the next run's query, so that its S runs under this run's softmax
+        if (RUNS && cur.n_cl == cur.cl) load_q(gw, h, cur.n_it, cur.cr.y + cur.j + 1);
         const uint32_t tS = tmem + lane_off + 128u * s;
         // two passes over the S row in tensor memory (32 columns at a time):
         // its maximum, then P; only one slice is held in registers
