@@ -1463,7 +1463,13 @@ kvs_status decode_attn_token_major(kvs_pool* pool, int layer, const void* q, int
   // fewer than half exist), so that the merge grid stays within one wave
   prm.mwpr = 1;
   const int n_slots = L.n_chunks + (L.SG > 1 ? L.n_chunks_s : 0);
-  while (prm.mwpr < kMergeWarps && prm.mwpr * 2 * kMergeBatch < n_slots) prm.mwpr <<= 1;
+  if (L.compact) {
+    // compact items fill only the first slots of a row (as many as its list
+    // needs items): the fewest warps whose ranges fit one 32-slot window
+    while (prm.mwpr < kMergeWarps && (n_slots + prm.mwpr - 1) / prm.mwpr > 32) prm.mwpr <<= 1;
+  } else {
+    while (prm.mwpr < kMergeWarps && prm.mwpr * 2 * kMergeBatch < n_slots) prm.mwpr <<= 1;
+  }
   if (rope) rope_split_host(theta, d.head_dim, prm.rs.c);
   prm.stall_first = (pool->test_flags & KVS_TEST_STALL_ONE_STAGE) ? 1 : 0;
   pool->test_flags &= ~KVS_TEST_STALL_ONE_STAGE;   // one launch only
