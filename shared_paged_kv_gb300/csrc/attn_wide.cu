@@ -33,7 +33,14 @@ namespace kvs {
 
 namespace {
 
-constexpr int kWdThreads = 192;          // 4 row warps, MMA warp, TMA warp
+// Row warps: four (one per 32-lane quadrant of tensor memory), or eight for
+// rotation calls, where warps w and w + 4 share a quadrant and split its 128
+// columns (their rows' softmax, the query rotation and the epilogue); then
+// the MMA warp and the TMA warp.
+template <bool RUNS>
+__host__ __device__ constexpr int wd_row_warps() { return RUNS ? 8 : 4; }
+template <bool RUNS>
+__host__ __device__ constexpr int wd_threads() { return 32 * (wd_row_warps<RUNS>() + 2); }
 constexpr int kWdSubBlocks = 8;          // blocks per sub-tile (128 tokens)
 constexpr int kWdHalf = 128 * 128;       // one [128][64] bf16 half of a 128-row tile, bytes
 constexpr int kWdTile = 2 * kWdHalf;     // a 128 x 128 bf16 tile
@@ -43,9 +50,10 @@ template <int ST, bool RUNS>
 constexpr int wd_smem() { return 1024 + kWdTile * ((RUNS ? 2 : 1) + 2 * ST); }
 constexpr uint32_t kWdCols = 512;        // S/P buffers at 0 and 128, O at 256
 // rotation calls: per row warp, (cos, sin) of a run's shift for each member
-// slot of its 32 rows (at most 8 for G >= 4), 64 frequencies per slot; the
-// row stride is padded by 16 bytes so that slots fall in different banks
-constexpr int kWdTblSlots = 8, kWdTblStride = 66;
+// slot of its 32 rows (at most 8 for G >= 4), for its 32 of the 64
+// frequencies; the row stride is padded by 16 bytes so that slots fall in
+// different banks
+constexpr int kWdTblSlots = 8, kWdTblStride = 34;
 
 __device__ __forceinline__ bool wd_wait(uint64_t* bar, uint32_t parity, uint32_t* status) {
   const bool ok = mbar_wait_bounded(bar, parity, status);
@@ -133,14 +141,17 @@ __device__ __forceinline__ uint32_t wd_loaded(const int2& rec) {
 // kv_full / kv_empty: the ST K/V stages (rotation calls: the two K buffers,
 // with v_full / v_empty for the two V buffers, so that a K buffer is refilled
 // as soon as S has read it).
+// pair[i] (rotation calls): the two row warps of quadrant i exchange their
+// halves' row maxima (every run) and row sums (every split).
 struct WdBars {
   uint64_t kv_full[2], kv_empty[2], v_full[2], v_empty[2], s_full[2], p_full[2], pv_done[2], q_full, o_free, fin;
+  uint64_t pair[4];
 };
 
 }  // namespace
 
 template <int ST, bool RUNS>
-__global__ void __launch_bounds__(kWdThreads, 1)
+__global__ void __launch_bounds__(wd_threads<RUNS>(), 1)
 attn_wide_kernel(const __grid_constant__ WideParams p, const __grid_constant__ CUtensorMap tk,
                  const __grid_constant__ CUtensorMap tv) {
   extern __shared__ uint8_t smem_raw[];
@@ -148,8 +159,12 @@ attn_wide_kernel(const __grid_constant__ WideParams p, const __grid_constant__ C
   __shared__ uint32_t s_tmem;
   __shared__ volatile int s_abort;
   __shared__ float rsc[RUNS ? 4 * 64 : 1];   // RoPE frequency pieces (rotation calls)
-  __shared__ __align__(16) float2 tbl[RUNS ? 4 * kWdTblSlots * kWdTblStride : 2];
+  __shared__ __align__(16) float2 tbl[RUNS ? 8 * kWdTblSlots * kWdTblStride : 2];
+  __shared__ float xch[RUNS ? 2 * 2 * 128 : 1];   // [run parity][column half][row] row maxima
+  __shared__ float xl[RUNS ? 2 * 128 : 1];        // [column half][row] row sums of a split
   constexpr int QT = RUNS ? 2 : 1;           // query tiles: Q (or Q hi, Q lo)
+  constexpr int RW = wd_row_warps<RUNS>();   // row warps
+  constexpr int NQ = 16 / RW;                // 32-column slices per row warp
   // the token-major kernel queued behind this one (programmatic dependent
   // launch) computes other splits: let it start on the SMs left free
   asm volatile("griddepcontrol.launch_dependents;");
@@ -176,13 +191,14 @@ attn_wide_kernel(const __grid_constant__ WideParams p, const __grid_constant__ C
       mbar_init(&bars.kv_full[s], 1);
       mbar_init(&bars.kv_empty[s], 1);
       mbar_init(&bars.s_full[s], 1);
-      mbar_init(&bars.p_full[s], 128);
+      mbar_init(&bars.p_full[s], 32 * RW);
       mbar_init(&bars.pv_done[s], 1);
       mbar_init(&bars.v_full[s], 1);
       mbar_init(&bars.v_empty[s], 1);
     }
-    mbar_init(&bars.q_full, 128);
-    mbar_init(&bars.o_free, 128);
+    mbar_init(&bars.q_full, 32 * RW);
+    mbar_init(&bars.o_free, 32 * RW);
+    for (int i = 0; i < 4; ++i) mbar_init(&bars.pair[i], 64);
     mbar_init(&bars.fin, 1);
     s_abort = 0;
     fence_barrier_init();
@@ -200,7 +216,7 @@ attn_wide_kernel(const __grid_constant__ WideParams p, const __grid_constant__ C
   // warp-uniform view of the abort flag
   auto stop = [&]() { return __any_sync(0xffffffffu, s_abort != 0); };
 
-  if (warp == 5) {
+  if (warp == RW + 1) {
     // ------------------------------------------------------ TMA producer
     // lane k < 8 copies block k of the sub-tile: both 64-column halves of K
     // and of V into the [half][token][64] stage
@@ -263,7 +279,7 @@ attn_wide_kernel(const __grid_constant__ WideParams p, const __grid_constant__ C
         if (armed_v[s] >= 0) mbar_drain(&bars.v_full[s], (uint32_t)armed_v[s]);
       }
     }
-  } else if (warp == 4) {
+  } else if (warp == RW) {
     // ----------------------------------------------------------- MMA issue
     constexpr uint32_t idS = umma_idesc_bf16(128, 128, false, false);
     constexpr uint32_t idO = umma_idesc_bf16(128, 128, false, true);
@@ -348,12 +364,20 @@ attn_wide_kernel(const __grid_constant__ WideParams p, const __grid_constant__ C
     mbar_wait_bounded(&bars.fin, 0, p.status);
   } else {
     // ------------------------------------------------------------ row warps
-    const int r = threadIdx.x;   // query row = TMEM lane
-    const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+    const int qd = warp & 3, ch = warp >> 2;   // TMEM lane quadrant, column half (rotation calls)
+    const int r = qd * 32 + lane;              // query row = TMEM lane
+    const uint32_t lane_off = (uint32_t)(qd * 32) << 16;
     const uint32_t tO = tmem + lane_off + 256;
     const int slot = r / p.g, hh = r - slot * p.g;
     const float sl2 = p.scale_log2;
-    uint8_t* stg = sQ + warp * 4096;   // this warp's query rows of half 0, reused to stage O
+    // 4 KB of the Q (hi) tile per row warp, reused to stage O
+    uint8_t* stg = sQ + warp * 4096;
+    int pu = 0;   // uses of this quadrant's pair barrier
+    // rotation calls: the two warps of the quadrant exchange a value per row
+    auto pair_sync = [&]() {
+      mbar_arrive(&bars.pair[qd]);
+      return wd_wait(&bars.pair[qd], (pu++) & 1, p.status);
+    };
     int n = 0, k = -1;
     bool ok = true, pend_epi = false;
     int e_gw = 0, e_h = 0, e_c = 0, e_last = 0;
@@ -361,15 +385,23 @@ attn_wide_kernel(const __grid_constant__ WideParams p, const __grid_constant__ C
     float e_m = 0.f, e_l = 0.f;
     float m = -INFINITY, l = 0.f;
     bool first = true, row_ok = false;
-    // rotation calls: this row's query (the claim's KV head), loaded once per
-    // claim and rotated from registers for each of its runs
-    uint4 qreg[RUNS ? 16 : 1];
+    // rotation calls: this row's query (the claim's KV head; the warp's
+    // half of the dims and their rotation partners), loaded once per claim
+    // and rotated from registers for each of its runs
+    uint4 qreg[RUNS ? 8 : 1];
     // The finished chunk's splits of this warp's 32 rows.  Each 32-column
     // slice of O goes from tensor memory through shared memory (128-byte
     // rows, XOR-swizzled) so that stores cover whole row segments.
     auto epilogue = [&]() {
+      float l_tot = e_l;
+      if (RUNS) {   // the row sum over both column halves
+        xl[ch * 128 + r] = e_l;
+        if (!pair_sync()) return false;
+        l_tot = xl[r] + xl[128 + r];
+      }
 #pragma unroll 1
-      for (int q = 0; q < 4; ++q) {
+      for (int qq = 0; qq < NQ; ++qq) {
+        const int q = ch * NQ + qq;
         uint32_t v[32];
         tmem_ld32(tO + 32 * q, v);
 #pragma unroll
@@ -380,7 +412,7 @@ attn_wide_kernel(const __grid_constant__ WideParams p, const __grid_constant__ C
 #pragma unroll
         for (int t = 0; t < 8; ++t) {
           const int jr = 4 * t + (lane >> 3), e = lane & 7;
-          const int r2 = warp * 32 + jr, sl = r2 / p.g, h2 = r2 - sl * p.g, a2 = e_gw * p.W + sl;
+          const int r2 = qd * 32 + jr, sl = r2 / p.g, h2 = r2 - sl * p.g, a2 = e_gw * p.W + sl;
           if (sl < p.W && a2 < p.n_seq && ((e_spm >> sl) & 1u)) {
             const size_t it2 = (((size_t)a2 * p.hkv + e_h) * p.n_chunks + e_c) * p.g + h2;
             __stcg(reinterpret_cast<uint4*>(p.p2 + it2 * 128 + 32 * q + 4 * e),
@@ -390,10 +422,11 @@ attn_wide_kernel(const __grid_constant__ WideParams p, const __grid_constant__ C
         __syncwarp();
       }
       const int a = e_gw * p.W + slot;
-      if (slot < p.W && a < p.n_seq && ((e_spm >> slot) & 1u)) {
+      if (ch == 0 && slot < p.W && a < p.n_seq && ((e_spm >> slot) & 1u)) {
         const size_t it = (((size_t)a * p.hkv + e_h) * p.n_chunks + e_c) * p.g + hh;
-        __stcg(reinterpret_cast<float2*>(p.p2_ml + it * 2), make_float2(e_m, e_l));
+        __stcg(reinterpret_cast<float2*>(p.p2_ml + it * 2), make_float2(e_m, l_tot));
       }
+      return true;
     };
     // The query rows of a claim (a rotation call: of one run item) into the
     // Q tile ([half][row][64], 128-byte swizzle); the S MMAs that read the
@@ -408,44 +441,44 @@ attn_wide_kernel(const __grid_constant__ WideParams p, const __grid_constant__ C
         // tile) + lo (second tile); rows of non-members are zero.  The
         // angles are computed once per member slot of the warp's rows.
         const bool mem = row_ok && ((((uint32_t)it.w) >> slot) & 1u);
-        const int s_lo = (warp * 32) / p.g;
-        const int n_s = min((warp * 32 + 31) / p.g - s_lo + 1, kWdTblSlots);
+        const int s_lo = (qd * 32) / p.g;
+        const int n_s = min((qd * 32 + 31) / p.g - s_lo + 1, kWdTblSlots);
         int dl_own = 0;
         if (lane < n_s) {
           const int sl = s_lo + lane;
           const bool mm = sl < p.W && gw * p.W + sl < p.n_seq && ((((uint32_t)it.w) >> sl) & 1u);
           dl_own = mm ? __ldg(p.wmem + (size_t)item * 32 + sl).y : 0;
         }
+        // this warp's frequencies 32 ch + lane, one table row per slot
         float2* tb = tbl + warp * (kWdTblSlots * kWdTblStride);
         __syncwarp();   // the previous run's table has been read
-        for (int t = 0; t < 2 * n_s; ++t) {   // slot t / 2, frequencies 32 (t & 1) + lane
-          const int k = t >> 1, i = 32 * (t & 1) + lane;
+        for (int k = 0; k < n_s; ++k) {
           const int dl = __shfl_sync(0xffffffffu, dl_own, k);
           float cs, sn;
-          rope_cos_sin(rsc, i, dl, cs, sn);
-          tb[k * kWdTblStride + i] = make_float2(cs, sn);
+          rope_cos_sin(rsc, 32 * ch + lane, dl, cs, sn);
+          tb[k * kWdTblStride + lane] = make_float2(cs, sn);
         }
         __syncwarp();
         const float2* mine = tb + min(max(slot - s_lo, 0), kWdTblSlots - 1) * kWdTblStride;
         const uint4 z = make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll
-        for (int c = 0; c < 8; ++c) {   // dims 8c..8c+7 and their partners 64 + 8c..
-          const uint4 xv = mem ? qreg[c] : z, yv = mem ? qreg[8 + c] : z;
+        for (int cc = 0; cc < 4; ++cc) {   // dims 8c..8c+7 (c = 4 ch + cc) and their partners 64 + 8c..
+          const int c = 4 * ch + cc;
+          const uint4 xv = mem ? qreg[cc] : z, yv = mem ? qreg[4 + cc] : z;
           const uint32_t xs[4] = {xv.x, xv.y, xv.z, xv.w}, ys[4] = {yv.x, yv.y, yv.z, yv.w};
-          uint32_t xh[4], xl[4], yh[4], yl[4];
+          uint32_t xh[4], xlo[4], yh[4], ylo[4];
 #pragma unroll
           for (int u = 0; u < 4; ++u) {
             const float x0 = bf16_lo(xs[u]), x1 = bf16_hi(xs[u]), y0 = bf16_lo(ys[u]), y1 = bf16_hi(ys[u]);
-            const float4 cs = *reinterpret_cast<const float4*>(mine + 8 * c + 2 * u);   // (c0, s0, c1, s1)
-            split_bf16(x0 * cs.x + y0 * cs.y, x1 * cs.z + y1 * cs.w, xh[u], xl[u]);
-            split_bf16(y0 * cs.x - x0 * cs.y, y1 * cs.z - x1 * cs.w, yh[u], yl[u]);
+            const float4 cs = *reinterpret_cast<const float4*>(mine + 8 * cc + 2 * u);   // (c0, s0, c1, s1)
+            split_bf16(x0 * cs.x + y0 * cs.y, x1 * cs.z + y1 * cs.w, xh[u], xlo[u]);
+            split_bf16(y0 * cs.x - x0 * cs.y, y1 * cs.z - x1 * cs.w, yh[u], ylo[u]);
           }
           const uint32_t off = r * 128 + ((c ^ (r & 7)) << 4);
-          uint8_t* qd = sQ;
-          *reinterpret_cast<uint4*>(qd + off) = make_uint4(xh[0], xh[1], xh[2], xh[3]);
-          *reinterpret_cast<uint4*>(qd + kWdHalf + off) = make_uint4(yh[0], yh[1], yh[2], yh[3]);
-          *reinterpret_cast<uint4*>(qd + kWdTile + off) = make_uint4(xl[0], xl[1], xl[2], xl[3]);
-          *reinterpret_cast<uint4*>(qd + kWdTile + kWdHalf + off) = make_uint4(yl[0], yl[1], yl[2], yl[3]);
+          *reinterpret_cast<uint4*>(sQ + off) = make_uint4(xh[0], xh[1], xh[2], xh[3]);
+          *reinterpret_cast<uint4*>(sQ + kWdHalf + off) = make_uint4(yh[0], yh[1], yh[2], yh[3]);
+          *reinterpret_cast<uint4*>(sQ + kWdTile + off) = make_uint4(xlo[0], xlo[1], xlo[2], xlo[3]);
+          *reinterpret_cast<uint4*>(sQ + kWdTile + kWdHalf + off) = make_uint4(ylo[0], ylo[1], ylo[2], ylo[3]);
         }
       } else {
 #pragma unroll
@@ -470,7 +503,7 @@ attn_wide_kernel(const __grid_constant__ WideParams p, const __grid_constant__ C
           if (pend_epi) {
             if (!wd_wait(&bars.pv_done[e_last & 1], (e_last >> 1) & 1, p.status)) { ok = false; break; }
             tc_fence_after();
-            epilogue();
+            if (!epilogue()) { ok = false; break; }
             pend_epi = false;
           }
           tc_fence_before();
@@ -481,7 +514,10 @@ attn_wide_kernel(const __grid_constant__ WideParams p, const __grid_constant__ C
         if constexpr (RUNS) {
           const uint4* src = reinterpret_cast<const uint4*>(p.q + ((size_t)(row_ok ? a : 0) * p.hq + h * p.g + hh) * 128);
 #pragma unroll
-          for (int c = 0; c < 16; ++c) qreg[c] = row_ok ? __ldg(src + c) : make_uint4(0u, 0u, 0u, 0u);
+          for (int cc = 0; cc < 4; ++cc) {
+            qreg[cc] = row_ok ? __ldg(src + 4 * ch + cc) : make_uint4(0u, 0u, 0u, 0u);
+            qreg[4 + cc] = row_ok ? __ldg(src + 8 + 4 * ch + cc) : make_uint4(0u, 0u, 0u, 0u);
+          }
         } else {
           load_q(gw, h, cur.it, 0);
         }
@@ -508,15 +544,24 @@ attn_wide_kernel(const __grid_constant__ WideParams p, const __grid_constant__ C
         const uint32_t tS = tmem + lane_off + 128u * s;
         // two passes over the S row in tensor memory (32 columns at a time):
         // its maximum, then P; only one slice is held in registers
+        // (rotation calls: over this warp's column half, then combined with
+        // the other half's through the quadrant's pair barrier)
         float mx = -INFINITY;
 #pragma unroll 1
-        for (int q = 0; q < 4; ++q) {
+        for (int qq = 0; qq < NQ; ++qq) {
+          const int q = ch * NQ + qq;
           uint32_t v[32];
           tmem_ld32(tS + 32 * q, v);
           const uint32_t lq = (rl >> (2 * q)) & 3u;
 #pragma unroll
           for (int t = 0; t < 32; ++t)
-            if ((lq >> (t >> 4)) & 1u) mx = fmaxf(mx, __uint_as_float(v[t]) * sl2);
+            if ((lq >> (t >> 4)) & 1u) mx = fmaxf(mx, __uint_as_float(v[t]));
+        }
+        mx = mx == -INFINITY ? mx : mx * sl2;
+        if (RUNS) {
+          xch[((n & 1) * 2 + ch) * 128 + r] = mx;
+          if (!pair_sync()) { ok = false; break; }
+          mx = fmaxf(mx, xch[((n & 1) * 2 + (ch ^ 1)) * 128 + r]);
         }
         const float mn = fmaxf(m, mx);
         // nothing live yet: reference point 0, so that 2^(-inf - 0) = 0
@@ -524,7 +569,8 @@ attn_wide_kernel(const __grid_constant__ WideParams p, const __grid_constant__ C
         const float alpha = fast_exp2(m - ref);
         float sum = 0.f;
 #pragma unroll 1
-        for (int q = 0; q < 4; ++q) {
+        for (int qq = 0; qq < NQ; ++qq) {
+          const int q = ch * NQ + qq;
           uint32_t v[32], hi[16], lo[16];
           tmem_ld32(tS + 32 * q, v);
           const uint32_t lq = (rl >> (2 * q)) & 3u;
@@ -548,7 +594,8 @@ attn_wide_kernel(const __grid_constant__ WideParams p, const __grid_constant__ C
           tc_fence_after();
           const float f = need ? alpha : 1.f;
 #pragma unroll 1
-          for (int q = 0; q < 4; ++q) {
+          for (int qq = 0; qq < NQ; ++qq) {
+            const int q = ch * NQ + qq;
             uint32_t v[32];
             tmem_ld32(tO + 32 * q, v);
 #pragma unroll
@@ -578,7 +625,7 @@ attn_wide_kernel(const __grid_constant__ WideParams p, const __grid_constant__ C
     if (ok && pend_epi) {
       if (wd_wait(&bars.pv_done[e_last & 1], (e_last >> 1) & 1, p.status)) {
         tc_fence_after();
-        epilogue();
+        if (!epilogue()) ok = false;
       } else {
         ok = false;
       }
@@ -598,7 +645,7 @@ template <int ST, bool RUNS>
 static kvs_status launch_wide(const WideParams& p, const kvs_pool* pool, int layer, int grid, cudaStream_t stream) {
   if (!smem_limit_once<attn_wide_kernel<ST, RUNS>>(wd_smem<ST, RUNS>(), pool->device))
     return fail(KVS_ERR_CUDA, "decode_attn: cannot raise the shared-memory limit (wide tile)");
-  attn_wide_kernel<ST, RUNS><<<grid, kWdThreads, wd_smem<ST, RUNS>(), stream>>>(p, pool->tk1[layer], pool->tv1[layer]);
+  attn_wide_kernel<ST, RUNS><<<grid, wd_threads<RUNS>(), wd_smem<ST, RUNS>(), stream>>>(p, pool->tk1[layer], pool->tv1[layer]);
   count_launch();
   return check_launch("decode_attn_wide");
 }
