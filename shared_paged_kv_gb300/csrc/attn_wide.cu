@@ -548,13 +548,13 @@ attn_wide_kernel(const __grid_constant__ WideParams p, const __grid_constant__ C
         // the other half's through the quadrant's pair barrier)
         float mx = -INFINITY;
 #pragma unroll 1
-        for (int qq = 0; qq < NQ; ++qq) {
+        for (int qq = 0; qq < NQ; qq += 2) {   // two slices under one wait
           const int q = ch * NQ + qq;
-          uint32_t v[32];
-          tmem_ld32(tS + 32 * q, v);
-          const uint32_t lq = (rl >> (2 * q)) & 3u;
+          uint32_t v[64];
+          tmem_ld64(tS + 32 * q, v);
+          const uint32_t lq = (rl >> (2 * q)) & 15u;
 #pragma unroll
-          for (int t = 0; t < 32; ++t)
+          for (int t = 0; t < 64; ++t)
             if ((lq >> (t >> 4)) & 1u) mx = fmaxf(mx, __uint_as_float(v[t]));
         }
         mx = mx == -INFINITY ? mx : mx * sl2;
@@ -563,7 +563,11 @@ attn_wide_kernel(const __grid_constant__ WideParams p, const __grid_constant__ C
           if (!pair_sync()) { ok = false; break; }
           mx = fmaxf(mx, xch[((n & 1) * 2 + (ch ^ 1)) * 128 + r]);
         }
-        const float mn = fmaxf(m, mx);
+        // The reference point moves only on a row's first live values or when
+        // the new maximum exceeds it by more than 8 (so P < 2^8 and O is
+        // rescaled rarely); m, l and O stay relative to the same reference,
+        // so the split is exact either way.
+        const float mn = (m == -INFINITY || mx > m + 8.f) ? fmaxf(m, mx) : m;
         // nothing live yet: reference point 0, so that 2^(-inf - 0) = 0
         const float ref = mn == -INFINITY ? 0.f : mn;
         const float alpha = fast_exp2(m - ref);
