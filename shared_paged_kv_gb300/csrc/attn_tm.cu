@@ -792,7 +792,9 @@ attn_tm_kernel(const __grid_constant__ TmParams p, const __grid_constant__ CUten
     prepare(n_id, n_it);
     nn_it = load_item(n_id + T);
   };
-  int pend_drow = -1;   // a diff tile pair still to issue for the last block
+  // A block that carries a mirror diff takes two positions: {K, DK}, then
+  // {V, DV}, so that the first is free as soon as S has been computed.
+  int pend_drow = -1, pend_row = 0;   // the {V, DV} position still to issue for the last block
   bool stall_pending = blockIdx.x == 0 && warp == 0;
   auto issue = [&](int s) {   // whole warp; lane 0 issues
     uint64_t* bar = &bars[warp][s];
@@ -800,7 +802,7 @@ attn_tm_kernel(const __grid_constant__ TmParams p, const __grid_constant__ CUten
     if (DIFF && pend_drow >= 0) {
       if (lane == 0) {
         mbar_arrive_expect_tx(bar, 2 * TILE);
-        tma_load_kv_tile<D>(st, &tdk, pend_drow, bar);
+        tma_load_kv_tile<D>(st, &tv, pend_row, bar);
         tma_load_kv_tile<D>(st + TILE, &tdv, pend_drow, bar);
       }
       pend_drow = -1;
@@ -836,7 +838,10 @@ attn_tm_kernel(const __grid_constant__ TmParams p, const __grid_constant__ CUten
     }
     const bool valid = phys >= 0 && phys < p.capacity;
     const bool dval = DIFF && valid && did >= 0 && did < p.diff_capacity;
-    if (dval) pend_drow = (did * p.hkv + p_h) * B;
+    if (dval) {
+      pend_drow = (did * p.hkv + p_h) * B;
+      pend_row = (phys * p.hkv + p_h) * B;
+    }
     if (lane != 0) return;
     if (p.stall_first && stall_pending) {
       // test-only: this stage is never armed, so its wait runs out
@@ -855,7 +860,8 @@ attn_tm_kernel(const __grid_constant__ TmParams p, const __grid_constant__ CUten
     mbar_arrive_expect_tx(bar, 2 * TILE);
     const int row = (phys * p.hkv + p_h) * B;
     tma_load_kv_tile<D>(st, &tk, row, bar);
-    tma_load_kv_tile<D>(st + TILE, &tv, row, bar);
+    if (dval) tma_load_kv_tile<D>(st + TILE, &tdk, pend_drow, bar);
+    else tma_load_kv_tile<D>(st + TILE, &tv, row, bar);
   };
   for (int s = 0; s < S; ++s) issue(s);
 
@@ -1018,8 +1024,9 @@ attn_tm_kernel(const __grid_constant__ TmParams p, const __grid_constant__ CUten
           cur_delta = nd;
         }
       }
-      const uint32_t tkb = wbase_u32 + s * STAGE, tvb = tkb + TILE;
-      const uint32_t dkb = wbase_u32 + s2 * STAGE, dvb = dkb + TILE;   // diff tiles (if any)
+      // {K, V}, or with a diff {K, DK} in stage s and {V, DV} in stage s2
+      const uint32_t tkb = wbase_u32 + s * STAGE, dkb = tkb + TILE;
+      const uint32_t tvb = has_diff ? wbase_u32 + s2 * STAGE : tkb + TILE, dvb = tvb + TILE;
       // S^T = K q^T : 16 tokens x 8 query columns, two accumulation chains
       float sc[4] = {0.f, 0.f, 0.f, 0.f}, sd[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
@@ -1037,6 +1044,11 @@ attn_tm_kernel(const __grid_constant__ TmParams p, const __grid_constant__ CUten
       }
 #pragma unroll
       for (int e = 0; e < 4; ++e) sc[e] += sd[e];
+      if (has_diff) {   // K and DK have been read: stage s takes the next position now
+        __syncwarp();
+        if (lane == 0) fence_proxy_async_smem();
+        issue(s);
+      }
       // sc: (t=g, col 2c), (g, 2c+1), (g+8, 2c), (g+8, 2c+1); a column is live
       // if its member takes this block (slot 31 never does: emask < 2^8) and
       // the token is inside its context
@@ -1095,7 +1107,7 @@ attn_tm_kernel(const __grid_constant__ TmParams p, const __grid_constant__ CUten
     }
     __syncwarp();
     if (lane == 0) fence_proxy_async_smem();
-    issue(s);
+    if (!(loaded && has_diff)) issue(s);   // (a loaded diff block released s after S)
     if (has_diff) issue(s2);
     i += has_diff ? 2 : 1;
   }
