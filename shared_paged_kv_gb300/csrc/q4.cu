@@ -15,7 +15,10 @@
 // The head-dim order inside each 16-wide k-step is permuted identically for q
 // and the codes (a dot product does not depend on the order), which lets a
 // thread fetch its codes with one 8-byte shared load per row and group.  The
-// P tile is transposed into the PV B operand with movmatrix.  K/V code tiles
+// P tile is transposed into the PV B operand with movmatrix.  For P V the
+// codes enter as fp16 subnormals: a low nibble masked in place is exactly
+// c * 2^-24 and a high nibble c * 2^-20 (one LOP3 each, no offset), and the
+// accumulators are scaled back by 2^24 / 2^20 once.  K/V code tiles
 // arrive by 2-D TMA (64-byte swizzle); scale/bias rows by 1-D bulk copies; a
 // 2-stage ring shared by the CTA's 4 warps (each warp takes 64 of the 256
 // tokens of every block) with full/empty mbarriers.
@@ -121,12 +124,10 @@ __device__ __forceinline__ uint32_t movmatrix_t(uint32_t x) {
 __device__ __forceinline__ uint32_t nib_lo1024(uint32_t w) { return (w & 0x000F000Fu) | 0x64006400u; }
 __device__ __forceinline__ uint32_t nib_hi1024(uint32_t w) { return (w & 0x00F000F0u) | 0x64006400u; }
 
-// two nibbles (bits [0,4) and [16,20) after the shift) -> fp16x2 exact codes
-__device__ __forceinline__ uint32_t nib2h(uint32_t w) {
-  const uint32_t m = (w & 0x000F000Fu) | 0x64006400u;
-  const __half2 r = __hsub2(*reinterpret_cast<const __half2*>(&m), __half2(__ushort_as_half(0x6400), __ushort_as_half(0x6400)));
-  return *reinterpret_cast<const uint32_t*>(&r);
-}
+// fp16x2 subnormals: bits [0,4) and [16,20) of w as c * 2^-24, bits [4,8)
+// and [20,24) as c * 2^-20 (exact)
+__device__ __forceinline__ uint32_t nib_lo_sub(uint32_t w) { return w & 0x000F000Fu; }
+__device__ __forceinline__ uint32_t nib_hi_sub(uint32_t w) { return w & 0x00F000F0u; }
 
 __global__ void __launch_bounds__(128, 2)
 q4_attn_kernel(const __grid_constant__ Q4Params p, const __grid_constant__ CUtensorMap tk,
@@ -344,7 +345,9 @@ q4_attn_kernel(const __grid_constant__ Q4Params p, const __grid_constant__ CUten
         corr[0][1] += pv[1] * v00.y + pv[3] * v10.y;
         corr[1][0] += pv[0] * v01.y + pv[2] * v11.y;
         corr[1][1] += pv[1] * v01.y + pv[3] * v11.y;
-        // A operand: V codes, m = head dim (permuted), k = token
+        // A operand: V codes, m = head dim (row g: the even dim 8g + 2lm of
+        // the group's 64, as c * 2^-24; row g + 8: the odd one, as c * 2^-20),
+        // k = token
         const int tb = tw + 16 * mt;
         const int tr[4] = {tb + 2 * c, tb + 2 * c + 1, tb + 2 * c + 8, tb + 2 * c + 9};
 #pragma unroll
@@ -357,8 +360,8 @@ q4_attn_kernel(const __grid_constant__ Q4Params p, const __grid_constant__ CUten
             const uint32_t sel = (uint32_t)lm | ((uint32_t)(4 + lm) << 8);
             const uint32_t x01 = __byte_perm(wv[0], wv[1], sel);
             const uint32_t x89 = __byte_perm(wv[2], wv[3], sel);
-            mma_f16(acc[grp * 4 + lm], nib2h(x01), nib2h(x01 >> 4), nib2h(x89), nib2h(x89 >> 4), bb[grp][0],
-                    bb[grp][1]);
+            mma_f16(acc[grp * 4 + lm], nib_lo_sub(x01), nib_hi_sub(x01), nib_lo_sub(x89), nib_hi_sub(x89),
+                    bb[grp][0], bb[grp][1]);
           }
         }
       }
@@ -401,7 +404,8 @@ q4_attn_kernel(const __grid_constant__ Q4Params p, const __grid_constant__ CUten
       for (int lm = 0; lm < 4; ++lm) {
         const int d0 = grp * 64 + 8 * g + 2 * lm;
         __stcg(reinterpret_cast<float2*>(pr + r * kQ4D + d0),
-               make_float2(acc[grp * 4 + lm][cc] + corr[grp][cc], acc[grp * 4 + lm][2 + cc] + corr[grp][cc]));
+               make_float2(fmaf(acc[grp * 4 + lm][cc], 16777216.f, corr[grp][cc]),
+                           fmaf(acc[grp * 4 + lm][2 + cc], 1048576.f, corr[grp][cc])));
       }
     }
     if (g == 0) __stcg(reinterpret_cast<float2*>(p.part_ml + (sidx * G_ + r) * 2), make_float2(m[cc], l[cc]));
