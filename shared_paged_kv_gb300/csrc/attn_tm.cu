@@ -87,7 +87,7 @@ struct TmLayout {
   bool compact;      // private items over each member's list of unshared blocks
   size_t max_items, max_witems;
   int max_sub;   // 8-block sub-tiles per wide item
-  size_t off_hdr, off_items, off_witems, off_wsub, off_wmem, off_wclaims, off_gmask, off_gphys, off_bdelta, off_pne, off_spm,
+  size_t off_hdr, off_items, off_witems, off_wsub, off_wmem, off_wclaims, off_gmask, off_gphys, off_bdelta, off_bwin, off_pne, off_spm,
       off_plist, off_pcnt, off_p1, off_p2, total;
 };
 
@@ -162,6 +162,7 @@ static TmLayout tm_layout(const kvs_pool* pool, int n_seq, int max_blocks, int g
   L.off_gmask = o; o = align256(o + grp * max_blocks * sizeof(uint32_t));
   L.off_gphys = o; o = align256(o + grp * max_blocks * sizeof(int32_t));
   L.off_bdelta = o; o = align256(o + (rope ? (size_t)n_seq * max_blocks * sizeof(int32_t) : 0));
+  L.off_bwin = o; o = align256(o + (rope ? (size_t)n_seq * max_blocks * sizeof(int32_t) : 0));
   L.off_pne = o; o = align256(o + (size_t)n_seq * L.n_chunks);
   L.off_spm = o; o = align256(o + grp * L.n_chunks_s * sizeof(uint32_t));
   L.off_plist = o; o = align256(o + (L.compact ? (size_t)n_seq * max_blocks * sizeof(int32_t) : 0));
@@ -203,6 +204,7 @@ struct PlanParams {
   const int32_t* rope_off;   // rotation calls: segment CSR
   const int4* rope_segs;
   int32_t* bdelta;   // [n_seq][max_blocks] RoPE shift of each logical block (rotation calls)
+  int32_t* bwin;     // [n_seq][max_blocks] the last entry covering each block (from the sequence's first), or -1
   uint32_t* status;
   float* p1_ml;      // (m, l) of the private splits [n_seq][hkv][n_chunks][g]
   float* p2_ml;      // (m, l) of the shared splits [n_seq][hkv][n_chunks_s][g] (SG > 1)
@@ -254,48 +256,47 @@ __device__ void plan_runs(const PlanParams& pp, int gi, int a0, int nm, unsigned
   for (int c = tid; c < pp.n_chunks_s; c += nt) pp.spm[(size_t)gi * pp.n_chunks_s + c] = 0u;
   __syncthreads();
   // candidates {first physical block, member, first logical block; shift;
-  // blocks with a mirror diff}
-  for (int r = 0; r < nm; ++r) {
-    const int a = a0 + r;
+  // blocks with a mirror diff}.  The group's entries are contiguous in the
+  // CSR: threads take them in turn and find their member.
+  const int eg0 = pp.rope_off[a0], eg1 = pp.rope_off[a0 + nm];
+  for (int e = eg0 + tid; e < eg1; e += nt) {
+    int r = 0;
+    while (r + 1 < nm && pp.rope_off[a0 + r + 1] <= e) ++r;
+    const int a = a0 + r, e0 = pp.rope_off[a];
     const int L = min(max(pp.seq_len[a], 0), pp.max_blocks * 16);
-    const int e0 = pp.rope_off[a], e1 = pp.rope_off[a + 1];
-    for (int e = e0 + tid; e < e1; e += nt) {
-      const int4 sg = __ldg(pp.rope_segs + e);
-      if (sg.z <= -(1 << 18) || sg.z >= (1 << 18) || sg.x < 0) continue;
-      for (int b = sg.x; b + 8 <= sg.x + sg.y && b + 8 <= pp.max_blocks && (b + 8) * 16 <= L; b += 8) {
-        const int* row = pp.block_table + (size_t)a * pp.max_blocks;
-        const int ph0 = row[b];
-        bool ok = ph0 >= 0 && ph0 <= pp.capacity - 8;
-        // this entry must be the last one covering each of the 8 blocks, so
-        // that a logical block belongs to one run at most
-        for (int e2 = e + 1; e2 < e1 && ok; ++e2) {
-          const int4 s2 = __ldg(pp.rope_segs + e2);
-          ok = s2.y <= 0 || s2.x >= b + 8 || s2.x + s2.y <= b;
-        }
-        uint32_t ex = 0;
-        for (int k = 0; k < 8 && ok; ++k) {
-          ok = row[b + k] == ph0 + k && pp.bdelta[(size_t)a * pp.max_blocks + b + k] == sg.z;
-          if (ok && pp.diff_table && pp.diff_table[(size_t)a * pp.max_blocks + b + k] >= 0) ex |= 1u << k;
-        }
-        if (!ok || ex == 0xffu) continue;
-        const int idx = atomicAdd(s_n, 1);
-        if (idx < kRunCap) {
-          s_key[idx] = ((unsigned long long)(unsigned)ph0 << 32) | ((unsigned long long)r << 20) | (unsigned)b;
-          s_dl[idx] = sg.z;
-          s_ex[idx] = (uint8_t)ex;
-        }
+    const int4 sg = __ldg(pp.rope_segs + e);
+    if (sg.z <= -(1 << 18) || sg.z >= (1 << 18) || sg.x < 0) continue;
+    const int* row = pp.block_table + (size_t)a * pp.max_blocks;
+    const size_t rb = (size_t)a * pp.max_blocks;
+    for (int b = sg.x; b + 8 <= sg.x + sg.y && b + 8 <= pp.max_blocks && (b + 8) * 16 <= L; b += 8) {
+      // the 8 blocks hold consecutive physical blocks, this entry is the
+      // last one covering each of them (so that a logical block belongs to
+      // one run at most), and their shift is the entry's; all loads at once
+      int ph[8], wn[8], dl[8], df[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        ph[k] = row[b + k];
+        wn[k] = pp.bwin[rb + b + k];
+        dl[k] = pp.bdelta[rb + b + k];
+        df[k] = pp.diff_table ? pp.diff_table[rb + b + k] : -1;
       }
+      bool ok = ph[0] >= 0 && ph[0] <= pp.capacity - 8;
+      uint32_t ex = 0;
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        ok = ok && ph[k] == ph[0] + k && wn[k] == e - e0 && dl[k] == sg.z;
+        ex |= (df[k] >= 0 ? 1u : 0u) << k;
+      }
+      if (!ok || ex == 0xffu) continue;
+      const int idx = atomicAdd(s_n, 1);
+      if (idx < kRunCap) s_key[idx] = ((unsigned long long)(unsigned)ph[0] << 32) | ((unsigned long long)r << 20) | (unsigned)b;
     }
   }
   __syncthreads();
   const int n = min(*s_n, kRunCap);
   int P = 1;
   while (P < n) P <<= 1;
-  for (int i = n + tid; i < P; i += nt) {
-    s_key[i] = ~0ull;
-    s_dl[i] = 0;
-    s_ex[i] = 0;
-  }
+  for (int i = n + tid; i < P; i += nt) s_key[i] = ~0ull;
   __syncthreads();
   // bitonic sort by (physical block, member, logical block): deterministic
   for (int k = 2; k <= P; k <<= 1)
@@ -308,17 +309,23 @@ __device__ void plan_runs(const PlanParams& pp, int gi, int a0, int nm, unsigned
           if ((x > y) == up) {
             s_key[i] = y;
             s_key[ixj] = x;
-            const int t = s_dl[i];
-            s_dl[i] = s_dl[ixj];
-            s_dl[ixj] = t;
-            const uint8_t u = s_ex[i];
-            s_ex[i] = s_ex[ixj];
-            s_ex[ixj] = u;
           }
         }
       }
       __syncthreads();
     }
+  // the shift and the diff blocks of each sorted candidate (the run check
+  // found the shift of all 8 blocks equal to the entry's)
+  for (int i = tid; i < n; i += nt) {
+    const int r = (int)((s_key[i] >> 20) & 31u), b = (int)(s_key[i] & 0xFFFFFu);
+    const size_t rb = (size_t)(a0 + r) * pp.max_blocks + b;
+    uint32_t ex = 0;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) ex |= ((pp.diff_table && pp.diff_table[rb + k] >= 0) ? 1u : 0u) << k;
+    s_dl[i] = pp.bdelta[rb];
+    s_ex[i] = (uint8_t)ex;
+  }
+  __syncthreads();
   // one item per physical run held by two or more members (a member's first
   // run with that block, by logical position).  Each thread takes a
   // contiguous range of the sorted candidates, so the group's items get
@@ -405,12 +412,42 @@ __device__ void plan_runs(const PlanParams& pp, int gi, int a0, int nm, unsigned
   }
 }
 
-__global__ void __launch_bounds__(256) tm_plan_groups(PlanParams pp) {
+// Plan, part 0 (rotation calls): the shift of every logical block, one CTA
+// per sequence.  The last entry covering a block wins (entries in order), so
+// every entry marks its blocks with an atomic maximum of its index; a block
+// no entry covers keeps shift 0.  bwin keeps the winning index for the run
+// search (a run must lie in the last entry covering each of its blocks).
+__global__ void __launch_bounds__(256) tm_plan_shifts(PlanParams pp) {
+  const int tid = threadIdx.x, nt = blockDim.x;
+  for (int a = blockIdx.x; a < pp.n_seq; a += gridDim.x) {
+    int32_t* win = pp.bwin + (size_t)a * pp.max_blocks;
+    for (int b = tid; b < pp.max_blocks; b += nt) win[b] = -1;
+    __syncthreads();
+    const int e0 = pp.rope_off[a], e1 = pp.rope_off[a + 1];
+    for (int e = e0 + tid; e < e1; e += nt) {
+      const int4 sg = __ldg(pp.rope_segs + e);
+      const int lo = max(sg.x, 0), hi = (int)min((long long)sg.x + sg.y, (long long)pp.max_blocks);
+      for (int b = lo; b < hi; ++b) atomicMax(win + b, e - e0);
+    }
+    __syncthreads();
+    for (int b = tid; b < pp.max_blocks; b += nt) {
+      const int w = win[b];
+      int dl = w >= 0 ? __ldg(pp.rope_segs + e0 + w).z : 0;
+      if (dl <= -(1 << 18) || dl >= (1 << 18)) {
+        set_err(pp.status, KVS_DEVERR_ROPE_RANGE);
+        dl = 0;
+      }
+      pp.bdelta[(size_t)a * pp.max_blocks + b] = dl;
+    }
+    __syncthreads();
+  }
+}
+
+__global__ void __launch_bounds__(512) tm_plan_groups(PlanParams pp) {
   __shared__ unsigned long long s_key[kRunCap];
   __shared__ int s_dl[kRunCap];
   __shared__ uint8_t s_ex[kRunCap];
   __shared__ int s_n;
-  __shared__ int s_wsum[32];
   const int tid = threadIdx.x, nt = blockDim.x;
   if (blockIdx.x == 0 && tid == 0) {
     pp.hdr[0] = 0;   // item counts, accumulated by tm_plan_items (and, for runs, here)
@@ -428,25 +465,7 @@ __global__ void __launch_bounds__(256) tm_plan_groups(PlanParams pp) {
   const int SG = pp.SG;
   for (int gi = blockIdx.x; gi < pp.n_groups; gi += gridDim.x) {
     const int a0 = gi * SG, nm = min(SG, pp.n_seq - a0);
-    // 0. rotation calls: the shift of every member's logical blocks (the last
-    // entry covering the block; 0 outside every entry)
-    if (pp.rope_off) {
-      for (int i = tid; i < nm * pp.max_blocks; i += nt) {
-        const int r = i / pp.max_blocks, b = i - r * pp.max_blocks, a = a0 + r;
-        const int e0 = pp.rope_off[a], e1 = pp.rope_off[a + 1];
-        int dl = 0;
-        for (int e = e0; e < e1; ++e) {
-          const int4 sg = __ldg(pp.rope_segs + e);
-          if (b >= sg.x && b - sg.x < sg.y) dl = sg.z;
-        }
-        if (dl <= -(1 << 18) || dl >= (1 << 18)) {
-          set_err(pp.status, KVS_DEVERR_ROPE_RANGE);
-          dl = 0;
-        }
-        pp.bdelta[(size_t)a * pp.max_blocks + b] = dl;
-      }
-      __syncthreads();
-    }
+    // (rotation calls: bdelta and bwin come from tm_plan_shifts)
     // 1. sharing
     if (SG > 1 && pp.runs) {
       plan_runs(pp, gi, a0, nm, s_key, s_dl, s_ex, &s_n);
@@ -483,21 +502,22 @@ __global__ void __launch_bounds__(256) tm_plan_groups(PlanParams pp) {
     }
     // 2. chunk occupancy (compact items: the list of unshared blocks first)
     if (pp.compact) {
-      for (int r = 0; r < nm; ++r) {
+      // one warp per member: its unshared blocks in order, by ballots
+      const int wid = tid >> 5, ln = tid & 31, nw = nt >> 5;
+      for (int r = wid; r < nm; r += nw) {
         const int a = a0 + r;
         const int nb = plan_seq_blocks(pp.seq_len, a, pp.max_blocks);
         int cnt = 0;
-        for (int b0 = 0; b0 < pp.max_blocks; b0 += nt) {   // the same trip count on every thread
-          const int b = b0 + tid;
-          const int keep = (b < nb && !((pp.gmask[(size_t)gi * pp.max_blocks + b] >> r) & 1u)) ? 1 : 0;
-          int tot;
-          const int pos = block_exclusive_scan(keep, s_wsum, tot);
-          if (keep) pp.plist[(size_t)a * pp.max_blocks + cnt + pos] = b;
-          cnt += tot;
+        for (int b0 = 0; b0 < nb; b0 += 32) {
+          const int b = b0 + ln;
+          const bool keep = b < nb && !((pp.gmask[(size_t)gi * pp.max_blocks + b] >> r) & 1u);
+          const unsigned bal = __ballot_sync(0xffffffffu, keep);
+          if (keep) pp.plist[(size_t)a * pp.max_blocks + cnt + __popc(bal & ((1u << ln) - 1u))] = b;
+          cnt += __popc(bal);
         }
         const int ni = (cnt + pp.ib - 1) / pp.ib;
-        if (tid == 0) pp.pcnt[a] = cnt;
-        for (int c = tid; c < pp.n_chunks; c += nt) pp.pne[(size_t)a * pp.n_chunks + c] = (uint8_t)(c < ni);
+        if (ln == 0) pp.pcnt[a] = cnt;
+        for (int c = ln; c < pp.n_chunks; c += 32) pp.pne[(size_t)a * pp.n_chunks + c] = (uint8_t)(c < ni);
       }
     } else
     for (int i = tid; i < nm * pp.n_chunks; i += nt) {
@@ -517,22 +537,22 @@ __global__ void __launch_bounds__(256) tm_plan_groups(PlanParams pp) {
       }
     }
     __syncthreads();
-    // 3. splits that no item writes
-    const int per_seq = pp.hkv * pp.n_chunks * pp.G;
-    for (int i = tid; i < nm * per_seq; i += nt) {
-      const int r = i / per_seq, rem = i - r * per_seq;
-      const int c = (rem / pp.G) % pp.n_chunks;
-      const int a = a0 + r;
-      const size_t e = (size_t)a * per_seq + rem;   // [a][h][c][hh]
-      if (!pp.pne[(size_t)a * pp.n_chunks + c]) reinterpret_cast<float2*>(pp.p1_ml)[e] = none;
+    // 3. splits that no item writes ([a][h][c][hh]): one (member, chunk)
+    // per thread, its flag read once
+    for (int i = tid; i < nm * pp.n_chunks; i += nt) {
+      const int r = i / pp.n_chunks, c = i - r * pp.n_chunks, a = a0 + r;
+      if (pp.pne[(size_t)a * pp.n_chunks + c]) continue;
+      float2* ml = reinterpret_cast<float2*>(pp.p1_ml) + (size_t)a * pp.hkv * pp.n_chunks * pp.G;
+      for (int h = 0; h < pp.hkv; ++h)
+        for (int hh = 0; hh < pp.G; ++hh) ml[((size_t)h * pp.n_chunks + c) * pp.G + hh] = none;
     }
     if (SG > 1) {
-      const int per_seq_s = pp.hkv * pp.n_chunks_s * pp.G;
-      for (int i = tid; i < nm * per_seq_s; i += nt) {
-        const int r = i / per_seq_s, rem = i - r * per_seq_s;
-        const int c = (rem / pp.G) % pp.n_chunks_s;
-        if (!((pp.spm[(size_t)gi * pp.n_chunks_s + c] >> r) & 1u))
-          reinterpret_cast<float2*>(pp.p2_ml)[(size_t)(a0 + r) * per_seq_s + rem] = none;
+      for (int i = tid; i < nm * pp.n_chunks_s; i += nt) {
+        const int r = i / pp.n_chunks_s, c = i - r * pp.n_chunks_s, a = a0 + r;
+        if ((pp.spm[(size_t)gi * pp.n_chunks_s + c] >> r) & 1u) continue;
+        float2* ml = reinterpret_cast<float2*>(pp.p2_ml) + (size_t)a * pp.hkv * pp.n_chunks_s * pp.G;
+        for (int h = 0; h < pp.hkv; ++h)
+          for (int hh = 0; hh < pp.G; ++hh) ml[((size_t)h * pp.n_chunks_s + c) * pp.G + hh] = none;
       }
     }
     __syncthreads();
@@ -1339,6 +1359,7 @@ struct TmPtrs {
   uint8_t* pne;
   uint32_t* spm;
   int32_t* bdelta;
+  int32_t* bwin;
   int32_t* plist;
   int32_t* pcnt;
   float *p1, *p1_ml, *p2, *p2_ml;
@@ -1360,6 +1381,7 @@ static TmPtrs tm_ptrs(const TmLayout& L, const kvs_pool* pool, int n_seq, int g,
   t.wmem = reinterpret_cast<int2*>(w + L.off_wmem);
   t.wclaims = reinterpret_cast<int4*>(w + L.off_wclaims);
   t.bdelta = reinterpret_cast<int32_t*>(w + L.off_bdelta);
+  t.bwin = reinterpret_cast<int32_t*>(w + L.off_bwin);
   t.plist = reinterpret_cast<int32_t*>(w + L.off_plist);
   t.pcnt = reinterpret_cast<int32_t*>(w + L.off_pcnt);
   t.p1 = reinterpret_cast<float*>(w + L.off_p1);
@@ -1389,6 +1411,7 @@ kvs_status decode_plan_token_major(kvs_pool* pool, int n_q_heads, const int32_t*
   pp.rope_off = rope_off;
   pp.rope_segs = reinterpret_cast<const int4*>(rope_segs);
   pp.bdelta = t.bdelta;
+  pp.bwin = t.bwin;
   pp.status = pool->status;
   pp.p1_ml = t.p1_ml;
   pp.p2_ml = t.p2_ml;
@@ -1418,8 +1441,14 @@ kvs_status decode_plan_token_major(kvs_pool* pool, int n_q_heads, const int32_t*
   pp.compact = L.compact ? 1 : 0;
   // item counters start at zero (several CTAs add to them)
   if (cudaMemsetAsync(t.hdr, 0, 64, stream) != cudaSuccess) return fail(KVS_ERR_CUDA, "decode_plan: memset failed");
+  if (rope) {
+    tm_plan_shifts<<<std::max(1, std::min(n_seq, pool->num_sms * 8)), 256, 0, stream>>>(pp);
+    count_launch();
+    const kvs_status st0 = check_launch("decode_plan");
+    if (st0 != KVS_OK) return st0;
+  }
   const int g1 = std::max(1, std::min(L.n_groups, pool->num_sms * 4));
-  tm_plan_groups<<<g1, 256, 0, stream>>>(pp);
+  tm_plan_groups<<<g1, 512, 0, stream>>>(pp);
   count_launch();
   kvs_status st = check_launch("decode_plan");
   if (st != KVS_OK) return st;
