@@ -12,10 +12,12 @@
 // sequence-major order; refcount = references.
 //
 // How (GB300, all on device, no host round trip):
-//  1. prep: one warp per sequence computes CalcHash of each full block and a
-//     segment-local chain key with a warp-wide segmented scan of the affine
-//     map h -> h*M + fp (restarted at segment starts), finalised with
-//     SplitMix64's mixer and folded with the segment-local index.
+//  1. hash: one thread per block slot computes CalcHash of each full block;
+//     prep: one warp per sequence finds the segment start of each block
+//     (accepted starts by a warp max-scan, then a running maximum over the
+//     blocks) and the segment-local chain key with a warp-wide segmented
+//     scan of the affine map h -> h*M + fp (restarted at segment starts),
+//     finalised with SplitMix64's mixer and folded with the local index.
 //  2. insert: every shareable block inserts its key into an open-addressing
 //     table; atomicMin keeps the lowest (sequence, block) slot per key.
 //  3. resolve: each block takes the table's owner as its representative and
@@ -23,7 +25,9 @@
 //     predecessor blocks resolve to the same representative (induction over
 //     the segment).  A failure (a key collision) raises a flag.
 //  4. fallback (only when flagged): exact brute-force representative search.
-//  5. scan: one CTA numbers first occurrences in slot order (deterministic).
+//  5. count, tiles, number: first occurrences counted per 1024-slot tile,
+//     the counts turned into prefix sums by one CTA, then numbered in slot
+//     order (deterministic).
 //  6. table: block_table and refcounts.
 #include <climits>
 
@@ -56,6 +60,7 @@ struct DedupParams {
   int32_t* segstart;  // per slot
   int32_t* pid;       // per slot physical id of first occurrences
   uint32_t* flags;    // [0] collision
+  int32_t* tile_cnt;  // first occurrences per numbering tile
   int n_seq, max_blocks, B, capacity, weak;
   uint32_t tmask;
 };
@@ -80,7 +85,30 @@ __device__ __forceinline__ void seq_geom(const DedupParams& p, int s, int64_t& o
   full = static_cast<int>(fu);
 }
 
-// 1. one warp per sequence
+// 1a. CalcHash of every full block, one thread per slot
+__global__ void dedup_hash(DedupParams p) {
+  const int slot = blockIdx.x * blockDim.x + threadIdx.x;
+  if (slot >= p.n_seq * p.max_blocks) return;
+  const int s = slot / p.max_blocks, b = slot - s * p.max_blocks;
+  int64_t off;
+  int nblk, full;
+  seq_geom(p, s, off, nblk, full);
+  uint64_t fp = 0;
+  if (b < full) {
+    const uint32_t* t = p.tokens + off + (int64_t)b * p.B;
+    uint64_t h = kFnvOffset;
+    for (int i = 0; i < p.B; ++i) {
+      h ^= (uint64_t)__ldg(t + i);
+      h *= kFnvPrime;
+    }
+    h ^= (uint64_t)(p.tier ? p.tier[s] : 0u);
+    h *= kFnvPrime;
+    fp = h;
+  }
+  p.fp_out[slot] = fp;
+}
+
+// 1b. one warp per sequence: segment starts and chain keys
 __global__ void dedup_prep(DedupParams p) {
   const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
@@ -95,48 +123,50 @@ __global__ void dedup_prep(DedupParams p) {
   }
   const uint32_t tier = p.tier ? p.tier[s] : 0u;
   const size_t row = (size_t)s * p.max_blocks;
-  // segment start of every block
   for (int b = lane; b < p.max_blocks; b += 32) p.segstart[row + b] = 0;
   __syncwarp();
   if (p.seg_off) {
+    // An entry starts a segment iff it lies inside the sequence and beyond
+    // every earlier in-range entry (unsorted and out-of-range starts are
+    // ignored); each accepted start marks its own block.
     const int64_t e0 = p.seg_off[s], e1 = p.seg_off[s + 1];
-    int prev = 0;
-    for (int64_t e = e0; e < e1; ++e) {
-      const int st = p.seg_blocks[e];
-      if (st <= prev || st >= nblk) continue;   // ignore unsorted / out-of-range starts
-      int nxt = nblk;
-      for (int64_t e2 = e + 1; e2 < e1; ++e2) {
-        const int v = p.seg_blocks[e2];
-        if (v > st) { nxt = min(nxt, v); break; }
+    int carry = 0;
+    for (int64_t base = e0; base < e1; base += 32) {
+      const int64_t e = base + lane;
+      const int st = e < e1 ? p.seg_blocks[e] : 0;
+      const int v = (e < e1 && st < nblk) ? st : 0;
+      int incl = v;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl = max(incl, y);
       }
-      for (int b = st + lane; b < nxt; b += 32) p.segstart[row + b] = st;
-      prev = st;
-      __syncwarp();
+      int excl = __shfl_up_sync(0xffffffffu, incl, 1);
+      excl = max(carry, lane ? excl : 0);
+      if (e < e1 && st < nblk && st > excl) p.segstart[row + st] = st;
+      carry = max(carry, __shfl_sync(0xffffffffu, incl, 31));
     }
+    __syncwarp();
   }
-  __syncwarp();
+  // the segment start of every block is the running maximum of the marks
+  int scarry = 0;
   uint64_t carryA = 1, carryC = 0;
+  uint64_t fp_next = lane < p.max_blocks ? p.fp_out[row + lane] : 0;
   for (int base = 0; base < p.max_blocks; base += 32) {
     const int b = base + lane;
-    uint64_t fp = 0;
-    bool shareable = false;
-    int st = 0;
-    if (b < nblk) {
-      st = p.segstart[row + b];
-      if (b < full) {
-        const uint32_t* t = p.tokens + off + (int64_t)b * p.B;
-        uint64_t h = kFnvOffset;
-        for (int i = 0; i < p.B; ++i) {
-          h ^= (uint64_t)t[i];
-          h *= kFnvPrime;
-        }
-        h ^= (uint64_t)tier;
-        h *= kFnvPrime;
-        fp = h;
-        shareable = tier != kPrivateTier;
-      }
+    const uint64_t fp = fp_next;
+    fp_next = b + 32 < p.max_blocks ? p.fp_out[row + b + 32] : 0;   // the next chunk's, ahead of use
+    int st = (b < nblk) ? p.segstart[row + b] : 0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, st, o);
+      if (lane >= o) st = max(st, y);
     }
-    if (b < p.max_blocks) p.fp_out[row + b] = fp;
+    st = max(st, scarry);
+    scarry = __shfl_sync(0xffffffffu, st, 31);
+    if (b >= nblk) st = 0;
+    if (b < p.max_blocks) p.segstart[row + b] = st;
+    const bool shareable = b < full && tier != kPrivateTier;
     // segmented scan of x -> A x + C
     uint64_t A = (b < nblk && b != st) ? kChainMul : (b < nblk ? 0ull : 1ull);
     uint64_t Cc = (b < nblk) ? (b == st ? fp + kChainMul : fp) : 0ull;
@@ -265,49 +295,57 @@ __global__ void dedup_fallback(DedupParams p) {
   p.rep[slot] = slot;
 }
 
-// 5. one CTA: number the first occurrences in slot order
-__global__ void __launch_bounds__(1024) dedup_scan(DedupParams p) {
-  __shared__ int warp_sums[32];
-  __shared__ int carry;
-  const int n = p.n_seq * p.max_blocks;
-  if (threadIdx.x == 0) carry = 0;
-  __syncthreads();
+// 5a. first occurrences (slots that are their own representative) per tile
+// of 1024 slots
+constexpr int kNumTile = 1024;
+
+__device__ __forceinline__ int block_sum_1024(int f, int* warp_sums) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  for (int base = 0; base < n; base += blockDim.x) {
-    const int slot = base + threadIdx.x;
-    int f = 0;
-    if (slot < n) {
-      const int r = p.rep[slot];
-      f = (r == slot) ? 1 : 0;
-    }
-    int x = f;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int y = __shfl_up_sync(0xffffffffu, x, o);
-      if (lane >= o) x += y;
-    }
-    if (lane == 31) warp_sums[warp] = x;
-    __syncthreads();
-    if (warp == 0) {
-      int w = warp_sums[lane];
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int y = __shfl_up_sync(0xffffffffu, w, o);
-        if (lane >= o) w += y;
-      }
-      warp_sums[lane] = w;
-    }
-    __syncthreads();
-    const int incl = x + (warp ? warp_sums[warp - 1] : 0) + carry;
-    if (slot < n && f) p.pid[slot] = incl - 1;
-    __syncthreads();
-    if (threadIdx.x == blockDim.x - 1) carry = incl;
-    __syncthreads();
+  int x = __reduce_add_sync(0xffffffffu, f);
+  if (lane == 0) warp_sums[warp] = x;
+  __syncthreads();
+  int t = 0;
+  for (int w = 0; w < (int)(blockDim.x >> 5); ++w) t += warp_sums[w];
+  return t;
+}
+
+__global__ void __launch_bounds__(kNumTile) dedup_count(DedupParams p) {
+  __shared__ int warp_sums[32];
+  const int n = p.n_seq * p.max_blocks;
+  const int slot = blockIdx.x * kNumTile + threadIdx.x;
+  const int f = (slot < n && p.rep[slot] == slot) ? 1 : 0;
+  const int t = block_sum_1024(f, warp_sums);
+  if (threadIdx.x == 0) p.tile_cnt[blockIdx.x] = t;
+}
+
+// 5b. one CTA: the tiles' counts become their exclusive prefix sums (slot
+// order), and the total is the number of physical blocks
+__global__ void __launch_bounds__(kNumTile) dedup_tiles(DedupParams p, int n_tiles) {
+  __shared__ int warp_sums[32];
+  int carry = 0;
+  for (int base = 0; base < n_tiles; base += kNumTile) {
+    const int t = base + threadIdx.x;
+    const int c = t < n_tiles ? p.tile_cnt[t] : 0;
+    int total;
+    const int pos = block_exclusive_scan(c, warp_sums, total);
+    if (t < n_tiles) p.tile_cnt[t] = carry + pos;
+    carry += total;
   }
   if (threadIdx.x == 0) {
     *p.n_phys = carry;
     if (carry > p.capacity) set_err(p.status, KVS_DEVERR_CAPACITY);
   }
+}
+
+// 5c. number the first occurrences in slot order from the tile's offset
+__global__ void __launch_bounds__(kNumTile) dedup_number(DedupParams p) {
+  __shared__ int warp_sums[32];
+  const int n = p.n_seq * p.max_blocks;
+  const int slot = blockIdx.x * kNumTile + threadIdx.x;
+  const int f = (slot < n && p.rep[slot] == slot) ? 1 : 0;
+  int total;
+  const int pos = block_exclusive_scan(f, warp_sums, total);
+  if (f) p.pid[slot] = p.tile_cnt[blockIdx.x] + pos;
 }
 
 // 6. block table + refcounts
@@ -364,6 +402,8 @@ extern "C" kvs_status kvs_fingerprint_dedup(kvs_pool* pool, const uint32_t* toke
   p.segstart = reinterpret_cast<int32_t*>(take(slots * 4));
   p.pid = reinterpret_cast<int32_t*>(take(slots * 4));
   p.flags = reinterpret_cast<uint32_t*>(take(16));
+  const int n_tiles = static_cast<int>((slots + kNumTile - 1) / kNumTile);
+  p.tile_cnt = reinterpret_cast<int32_t*>(take((size_t)n_tiles * 4));
   p.tokens = tokens_dev;
   p.seq_off = seq_off_dev;
   p.tier = tier_dev;
@@ -392,12 +432,15 @@ extern "C" kvs_status kvs_fingerprint_dedup(kvs_pool* pool, const uint32_t* toke
   }
   const int n = static_cast<int>(slots);
   const int tb = 256;
+  dedup_hash<<<(n + tb - 1) / tb, tb, 0, stream>>>(p);
   dedup_prep<<<(n_seq * 32 + tb - 1) / tb, tb, 0, stream>>>(p);
   dedup_insert<<<(n + tb - 1) / tb, tb, 0, stream>>>(p);
   dedup_resolve<<<(n + tb - 1) / tb, tb, 0, stream>>>(p);
   dedup_fallback<<<(n + tb - 1) / tb, tb, 0, stream>>>(p);
-  dedup_scan<<<1, 1024, 0, stream>>>(p);
+  dedup_count<<<n_tiles, kNumTile, 0, stream>>>(p);
+  dedup_tiles<<<1, kNumTile, 0, stream>>>(p, n_tiles);
+  dedup_number<<<n_tiles, kNumTile, 0, stream>>>(p);
   dedup_table<<<(n + tb - 1) / tb, tb, 0, stream>>>(p);
-  count_launch(6);
+  count_launch(9);
   return check_launch("fingerprint_dedup");
 }
