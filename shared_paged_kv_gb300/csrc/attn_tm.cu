@@ -1056,10 +1056,10 @@ attn_tm_kernel(const __grid_constant__ TmParams p, const __grid_constant__ CUten
         ldsm_x4(tkb + koff[kk], a[0], a[1], a[2], a[3]);
         mma_bf16(acc_s, a, qb[kk][0], qb[kk][1]);
         if (ROPE && q_has_lo) mma_bf16(acc_s, a, qlo[ROPE ? kk : 0][0], qlo[ROPE ? kk : 0][1]);
-        if (has_diff) {
+        if (has_diff) {   // the diff tile against the query's hi part only (its lo part
+                          // adds about 2^-9 of a correction term that is itself small)
           ldsm_x4(dkb + koff[kk], a[0], a[1], a[2], a[3]);
           mma_bf16(acc_s, a, qb[kk][0], qb[kk][1]);
-          if (ROPE && q_has_lo) mma_bf16(acc_s, a, qlo[ROPE ? kk : 0][0], qlo[ROPE ? kk : 0][1]);
         }
       }
 #pragma unroll
@@ -1118,10 +1118,9 @@ attn_tm_kernel(const __grid_constant__ TmParams p, const __grid_constant__ CUten
         ldsm_x4_t(tvb + voff[mt], a[0], a[1], a[2], a[3]);
         mma_bf16(acc[mt], a, bh0, bh1);
         mma_bf16(acc[mt], a, bl0, bl1);
-        if (has_diff) {
+        if (has_diff) {   // likewise P's hi part only against the diff tile
           ldsm_x4_t(dvb + voff[mt], a[0], a[1], a[2], a[3]);
           mma_bf16(acc[mt], a, bh0, bh1);
-          mma_bf16(acc[mt], a, bl0, bl1);
         }
       }
     }
