@@ -639,6 +639,11 @@ struct TmParams {
   int compact;            // private items over plist (rotation calls on the wide tile)
   int max_blocks, n_seq, hkv, g, hq, ib, n_chunks, ibs, n_chunks_s, R, SG, capacity, diff_capacity;
   int mwpr;           // merge warps per output row
+  // Every launch is a programmatic dependent of the kernel before it on the
+  // stream.  The first kernel of a call (first_wait) waits for that kernel
+  // to complete before it reads anything; behind the wide tile the kernel
+  // runs beside it and waits only before it completes.
+  int first_wait;
   int stall_first;    // test-only (KVS_TEST_STALL_ONE_STAGE): leave one stage unarmed
   float scale_log2;
   RopeSplit rs;
@@ -695,6 +700,7 @@ attn_tm_kernel(const __grid_constant__ TmParams p, const __grid_constant__ CUten
     for (int s = 0; s < S; ++s) mbar_init(&bars[warp][s], 1);
     fence_barrier_init();
   }
+  if (p.first_wait) asm volatile("griddepcontrol.wait;" ::: "memory");
   if (ROPE) {
     for (int i = threadIdx.x; i < 4 * 64; i += blockDim.x) rsc[i] = p.rs.c[i >> 6][i & 63];
     __syncthreads();
@@ -1307,7 +1313,7 @@ static kvs_status launch_merge(const TmParams& prm, cudaStream_t st) {
 
 template <int D, bool DIFF, bool ROPE>
 static kvs_status launch_tm(TmParams& prm, const kvs_pool* pool, int layer, int max_claims, bool after_wide,
-                            cudaStream_t st) {
+                            bool pdl, cudaStream_t st) {
   auto kern = attn_tm_kernel<D, DIFF, ROPE>;
   constexpr int smem = tm_smem_bytes<D>();
   // occupancy depends only on the kernel and the device type (one type of
@@ -1336,7 +1342,8 @@ static kvs_status launch_tm(TmParams& prm, const kvs_pool* pool, int layer, int 
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = after_wide ? 1 : 0;   // behind the wide tile: start on the SMs it leaves free
+  cfg.numAttrs = pdl ? 1 : 0;   // behind the wide tile: start on the SMs it leaves free
+  prm.first_wait = after_wide ? 0 : 1;
   if (cudaLaunchKernelEx(&cfg, kern, (const TmParams)prm, pool->tk[layer], pool->tv[layer], dk, dv) != cudaSuccess)
     return fail(KVS_ERR_CUDA, "decode_attn: launch failed");
   count_launch();
@@ -1514,7 +1521,7 @@ kvs_status decode_attn_token_major(kvs_pool* pool, int layer, const void* q, int
   prm.stall_first = (pool->test_flags & KVS_TEST_STALL_ONE_STAGE) ? 1 : 0;
   pool->test_flags &= ~KVS_TEST_STALL_ONE_STAGE;   // one launch only
   const int max_claims = (int)std::min<size_t>(L.max_items * d.num_kv_heads, 0x7fffffff);
-  bool wide_launched = false;
+  bool wide_launched = false, runs_launched = false;
   if (L.wide) {
     // the shared chunks of every sharing group, on the tensor cores; they
     // write the shared splits, disjoint from what the token-major kernel writes
@@ -1551,17 +1558,21 @@ kvs_status decode_attn_token_major(kvs_pool* pool, int layer, const void* q, int
     // rotation calls leave the token-major kernel the heavier part (private
     // blocks and mirror diffs); it runs after the tile at full occupancy
     wide_launched = wide_claims > 0 && !L.runs;
+    runs_launched = wide_claims > 0 && L.runs;
   }
+  // a programmatic dependent launch, except behind a rotation-call tile
+  // (which fills its SMs: the early CTAs would only wait)
+  const bool pdl = !runs_launched;
   if (d.head_dim == 128) {
-    if (dif) return rope ? launch_tm<128, true, true>(prm, pool, layer, max_claims, wide_launched, stream)
-                         : launch_tm<128, true, false>(prm, pool, layer, max_claims, wide_launched, stream);
-    return rope ? launch_tm<128, false, true>(prm, pool, layer, max_claims, wide_launched, stream)
-                : launch_tm<128, false, false>(prm, pool, layer, max_claims, wide_launched, stream);
+    if (dif) return rope ? launch_tm<128, true, true>(prm, pool, layer, max_claims, wide_launched, pdl, stream)
+                         : launch_tm<128, true, false>(prm, pool, layer, max_claims, wide_launched, pdl, stream);
+    return rope ? launch_tm<128, false, true>(prm, pool, layer, max_claims, wide_launched, pdl, stream)
+                : launch_tm<128, false, false>(prm, pool, layer, max_claims, wide_launched, pdl, stream);
   }
-  if (dif) return rope ? launch_tm<64, true, true>(prm, pool, layer, max_claims, wide_launched, stream)
-                       : launch_tm<64, true, false>(prm, pool, layer, max_claims, wide_launched, stream);
-  return rope ? launch_tm<64, false, true>(prm, pool, layer, max_claims, wide_launched, stream)
-              : launch_tm<64, false, false>(prm, pool, layer, max_claims, wide_launched, stream);
+  if (dif) return rope ? launch_tm<64, true, true>(prm, pool, layer, max_claims, wide_launched, pdl, stream)
+                       : launch_tm<64, true, false>(prm, pool, layer, max_claims, wide_launched, pdl, stream);
+  return rope ? launch_tm<64, false, true>(prm, pool, layer, max_claims, wide_launched, pdl, stream)
+              : launch_tm<64, false, false>(prm, pool, layer, max_claims, wide_launched, pdl, stream);
 }
 
 }  // namespace kvs

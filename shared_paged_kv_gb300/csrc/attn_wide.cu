@@ -165,8 +165,12 @@ attn_wide_kernel(const __grid_constant__ WideParams p, const __grid_constant__ C
   constexpr int QT = RUNS ? 2 : 1;           // query tiles: Q (or Q hi, Q lo)
   constexpr int RW = wd_row_warps<RUNS>();   // row warps
   constexpr int NQ = 16 / RW;                // 32-column slices per row warp
-  // the token-major kernel queued behind this one (programmatic dependent
-  // launch) computes other splits: let it start on the SMs left free
+  // launched as a programmatic dependent of the kernel before it (the
+  // previous layer's merge, which reads the same split slots): nothing is
+  // read before that kernel has completed.  Then the token-major kernel
+  // queued behind this one (it computes other splits) may start on the SMs
+  // left free.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   asm volatile("griddepcontrol.launch_dependents;");
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   uint8_t* base = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
@@ -649,7 +653,20 @@ template <int ST, bool RUNS>
 static kvs_status launch_wide(const WideParams& p, const kvs_pool* pool, int layer, int grid, cudaStream_t stream) {
   if (!smem_limit_once<attn_wide_kernel<ST, RUNS>>(wd_smem<ST, RUNS>(), pool->device))
     return fail(KVS_ERR_CUDA, "decode_attn: cannot raise the shared-memory limit (wide tile)");
-  attn_wide_kernel<ST, RUNS><<<grid, wd_threads<RUNS>(), wd_smem<ST, RUNS>(), stream>>>(p, pool->tk1[layer], pool->tv1[layer]);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(wd_threads<RUNS>());
+  cfg.dynamicSmemBytes = wd_smem<ST, RUNS>();
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  // a rotation-call tile fills its SM's shared memory: launched early it
+  // would hold SMs that the previous layer's merge still needs
+  cfg.numAttrs = RUNS ? 0 : 1;
+  if (cudaLaunchKernelEx(&cfg, attn_wide_kernel<ST, RUNS>, p, pool->tk1[layer], pool->tv1[layer]) != cudaSuccess)
+    return fail(KVS_ERR_CUDA, "decode_attn: wide tile launch failed");
   count_launch();
   return check_launch("decode_attn_wide");
 }
