@@ -95,6 +95,15 @@ constexpr int kMaxRanges = 256;    // wide-tile claims (split slots) per group, 
 
 static size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
+#ifndef KVS_RUNS_WIDE_PCT
+#define KVS_RUNS_WIDE_PCT 50
+#endif
+// Rotation calls: the wide tile (latency-bound on its row warps, light on
+// DRAM) takes this share of the SMs, and the token-major kernel
+// (bandwidth-bound) starts at once on the others and takes all SMs once the
+// tile is done.
+int runs_wide_ctas(const kvs_pool* pool) { return std::max(1, pool->num_sms * KVS_RUNS_WIDE_PCT / 100); }
+
 // Work-item size (blocks): about KVS_TM_ITEMS_PER_WARP items per resident
 // warp, at least max_blocks / (KVS_TM_MAX_SPLITS * split_mult) (bounding the
 // splits of one sequence per kind), at most 32 (one block-table entry per lane).  The work
@@ -140,7 +149,7 @@ static TmLayout tm_layout(const kvs_pool* pool, int n_seq, int max_blocks, int g
   if (L.runs) {
     // the shared splits of a rotation call are one per claim range, and a
     // group cuts its runs into at most its share of the wide grid's CTAs
-    const int share = std::max(1, pool->num_sms / std::max(1, pool->desc.num_kv_heads * L.n_groups));
+    const int share = std::max(1, runs_wide_ctas(pool) / std::max(1, pool->desc.num_kv_heads * L.n_groups));
     L.n_chunks_s = std::min(std::min(L.n_chunks_s, kMaxRanges), share);
   }
   // Rotation calls: a member's unshared blocks are its private history plus
@@ -639,6 +648,12 @@ struct TmParams {
   int compact;            // private items over plist (rotation calls on the wide tile)
   int max_blocks, n_seq, hkv, g, hq, ib, n_chunks, ibs, n_chunks_s, R, SG, capacity, diff_capacity;
   int mwpr;           // merge warps per output row
+  // Rotation calls: the token-major grid starts beside the wide tile on the
+  // SMs it leaves free and its other CTAs start as the tile finishes, so
+  // claims are taken in turn from a per-pool counter (dyn), one claim ahead;
+  // the merge kernel queued behind resets it once this grid has completed.
+  int dyn;
+  unsigned int* claim_ctr;
   // Every launch is a programmatic dependent of the kernel before it on the
   // stream.  The first kernel of a call (first_wait) waits for that kernel
   // to complete before it reads anything; behind the wide tile the kernel
@@ -721,7 +736,12 @@ attn_tm_kernel(const __grid_constant__ TmParams p, const __grid_constant__ CUten
   // entries of the next claim are loaded one claim early, so they have
   // arrived by the time they are used.
   const int T = gridDim.x * kTmWarps;
-  int n_id = blockIdx.x * kTmWarps + warp;   // next claim
+  auto take = [&]() {   // dynamic claims: the next claim id
+    int id = 0;
+    if (lane == 0) id = (int)atomicAdd(p.claim_ctr, 1u);
+    return __shfl_sync(0xffffffffu, id, 0);
+  };
+  int n_id = p.dyn ? take() : blockIdx.x * kTmWarps + warp;   // next claim
   int4 n_it = make_int4(0, 0, 0, 0), nn_it = n_it;
   int n_tab = -1, n_aux = 0, n_dif = -1, n_len = 0, n_dlt = 0, n_lb = 0;
   auto load_item = [&](int id) {
@@ -772,7 +792,7 @@ attn_tm_kernel(const __grid_constant__ TmParams p, const __grid_constant__ CUten
     }
   };
   n_it = load_item(n_id);
-  nn_it = load_item(n_id + T);
+  if (!p.dyn) nn_it = load_item(n_id + T);
   prepare(n_id, n_it);
 
   int ord = -1;   // ordinal of the current claim
@@ -813,10 +833,16 @@ attn_tm_kernel(const __grid_constant__ TmParams p, const __grid_constant__ CUten
     }
     if (lane < kTmMaxGroup) rec.len[lane] = n_len;
     // advance: the next claim's entries, then the entry of the one after
-    n_id += T;
-    n_it = nn_it;
-    prepare(n_id, n_it);
-    nn_it = load_item(n_id + T);
+    if (p.dyn) {
+      n_id = take();
+      n_it = load_item(n_id);
+      prepare(n_id, n_it);
+    } else {
+      n_id += T;
+      n_it = nn_it;
+      prepare(n_id, n_it);
+      nn_it = load_item(n_id + T);
+    }
   };
   // A block that carries a mirror diff takes two positions: {K, DK}, then
   // {V, DV}, so that the first is free as soon as S has been computed.
@@ -1162,6 +1188,8 @@ constexpr int kMergeBatch = 12;
 template <int D>
 __global__ void __launch_bounds__(kMergeWarps * 32, 2) tm_merge_kernel(const __grid_constant__ TmParams p) {
   asm volatile("griddepcontrol.wait;" ::: "memory");
+  // the token-major grid has completed: its claim counter starts the next call at zero
+  if (p.dyn && blockIdx.x == 0 && threadIdx.x == 0) *p.claim_ctr = 0u;
   constexpr int CPL = D / 32;   // columns per lane
   __shared__ float sM[kMergeWarps], sL[kMergeWarps];
   __shared__ __align__(16) float sv[kMergeWarps][D];
@@ -1441,7 +1469,7 @@ kvs_status decode_plan_token_major(kvs_pool* pool, int n_q_heads, const int32_t*
   pp.n_groups = L.n_groups;
   pp.capacity = pool->desc.capacity_blocks;
   pp.hkv = pool->desc.num_kv_heads;
-  pp.wide_ctas = pool->num_sms;   // the wide tile's grid is at most one CTA per SM
+  pp.wide_ctas = L.runs ? runs_wide_ctas(pool) : pool->num_sms;   // the wide tile's grid
   pp.plist = t.plist;
   pp.pcnt = t.pcnt;
   pp.compact = L.compact ? 1 : 0;
@@ -1518,6 +1546,7 @@ kvs_status decode_attn_token_major(kvs_pool* pool, int layer, const void* q, int
     while (prm.mwpr < kMergeWarps && prm.mwpr * 2 * kMergeBatch < n_slots) prm.mwpr <<= 1;
   }
   if (rope) rope_split_host(theta, d.head_dim, prm.rs.c);
+  prm.claim_ctr = reinterpret_cast<unsigned int*>(pool->status) + 1;
   prm.stall_first = (pool->test_flags & KVS_TEST_STALL_ONE_STAGE) ? 1 : 0;
   pool->test_flags &= ~KVS_TEST_STALL_ONE_STAGE;   // one launch only
   const int max_claims = (int)std::min<size_t>(L.max_items * d.num_kv_heads, 0x7fffffff);
@@ -1557,12 +1586,13 @@ kvs_status decode_attn_token_major(kvs_pool* pool, int layer, const void* q, int
     if (ws_ != KVS_OK) return ws_;
     // rotation calls leave the token-major kernel the heavier part (private
     // blocks and mirror diffs); it runs after the tile at full occupancy
-    wide_launched = wide_claims > 0 && !L.runs;
+    // behind the tile (shared chunks: beside it on every SM; rotation calls:
+    // on the SMs it leaves free), the merge waiting on both grids
+    wide_launched = wide_claims > 0;
     runs_launched = wide_claims > 0 && L.runs;
   }
-  // a programmatic dependent launch, except behind a rotation-call tile
-  // (which fills its SMs: the early CTAs would only wait)
-  const bool pdl = !runs_launched;
+  const bool pdl = true;
+  prm.dyn = runs_launched ? 1 : 0;
   if (d.head_dim == 128) {
     if (dif) return rope ? launch_tm<128, true, true>(prm, pool, layer, max_claims, wide_launched, pdl, stream)
                          : launch_tm<128, true, false>(prm, pool, layer, max_claims, wide_launched, pdl, stream);

@@ -677,7 +677,8 @@ kvs_status launch_wide_tile(const WideParams& p, const kvs_pool* pool, int layer
   // one CTA per SM (its 512 TMEM columns), claims taken round-robin; CTAs
   // beyond the plan's item count return at once.  Items of one sub-tile need
   // no second stage, which leaves room on the SM for a token-major CTA.
-  const int grid = std::max(1, std::min(pool->num_sms, max_claims));
+  // (rotation calls: on part of the SMs, the token-major kernel on the rest)
+  const int grid = std::max(1, std::min(p.runs ? runs_wide_ctas(pool) : pool->num_sms, max_claims));
   // the MMA thread issues S of the next sub-tile before P V of the current
   // one, so claims of several sub-tiles (and rotation ranges) need two stages
   if (p.runs) return launch_wide<2, true>(p, pool, layer, grid, stream);

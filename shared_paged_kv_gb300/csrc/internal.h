@@ -17,7 +17,7 @@ struct kvs_pool {
   std::vector<void*> k, v, ksb, vsb, dk, dv;    // per-layer device slabs (not owned)
   std::vector<CUtensorMap> tk, tv, tdk, tdv;    // TMA maps per layer
   std::vector<CUtensorMap> tk1, tv1;           // bf16 head_dim 128: one 64-column half of a block per copy
-  uint32_t* status = nullptr;                   // device status word (owned)
+  uint32_t* status = nullptr;                   // device status word [0] and token-major claim counter [1] (owned)
   int32_t* tickets = nullptr;                   // split-K arrival counters (owned)
   size_t n_tickets = 0;
   // every per-layer slab that holds block contents (K, V and, for Q4, the
@@ -97,6 +97,8 @@ struct WideParams {
   float scale_log2;
   float rs[4][64];          // RoPE frequency pieces (rotation calls), as RopeSplit::c
 };
+// CTAs of the wide tile's grid for rotation calls (attn_tm.cu)
+int runs_wide_ctas(const kvs_pool* pool);
 kvs_status launch_wide_tile(const WideParams& p, const kvs_pool* pool, int layer, int max_claims,
                             cudaStream_t stream);
 
