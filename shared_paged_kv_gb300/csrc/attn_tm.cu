@@ -855,7 +855,7 @@ attn_tm_kernel(const __grid_constant__ TmParams p, const __grid_constant__ CUten
       if (lane == 0) {
         mbar_arrive_expect_tx(bar, 2 * TILE);
         tma_load_kv_tile<D>(st, &tv, pend_row, bar);
-        tma_load_kv_tile<D>(st + TILE, &tdv, pend_drow, bar);
+        tma_load_kv_tile_hint<D>(st + TILE, &tdv, pend_drow, bar, l2_policy_evict_first());
       }
       pend_drow = -1;
       return;
@@ -911,9 +911,17 @@ attn_tm_kernel(const __grid_constant__ TmParams p, const __grid_constant__ CUten
     st_rec[warp][s] = make_int4(ord, dval ? (b | (1 << 30)) : b, mask, dlt);
     mbar_arrive_expect_tx(bar, 2 * TILE);
     const int row = (phys * p.hkv + p_h) * B;
-    tma_load_kv_tile<D>(st, &tk, row, bar);
-    if (dval) tma_load_kv_tile<D>(st + TILE, &tdk, pend_drow, bar);
-    else tma_load_kv_tile<D>(st + TILE, &tv, row, bar);
+    // K and V of a block are read once per call here, and so are the diff
+    // tiles: evict-first, so that the master blocks under mirror diffs (read
+    // by several agents, with the default policy) stay in L2
+    const uint64_t pol = l2_policy_evict_first();
+    if (dval) {
+      tma_load_kv_tile<D>(st, &tk, row, bar);
+      tma_load_kv_tile_hint<D>(st + TILE, &tdk, pend_drow, bar, pol);
+    } else {
+      tma_load_kv_tile_hint<D>(st, &tk, row, bar, pol);
+      tma_load_kv_tile_hint<D>(st + TILE, &tv, row, bar, pol);
+    }
   };
   for (int s = 0; s < S; ++s) issue(s);
 

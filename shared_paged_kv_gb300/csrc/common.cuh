@@ -90,6 +90,23 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, i
       : "memory");
 }
 
+// The same copy with an L2 cache policy (createpolicy), e.g. evict-first for
+// data that is read once, so that it does not push out data read again.
+__device__ __forceinline__ void tma_load_3d_hint(void* dst, const CUtensorMap* map, int c0, int c1, int c2,
+                                                 uint64_t* bar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(bar)), "l"(policy)
+      : "memory");
+}
+
+__device__ __forceinline__ uint64_t l2_policy_evict_first() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+
 __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int c0, int c1, uint64_t* bar) {
   asm volatile(
       "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
@@ -121,6 +138,12 @@ __device__ __forceinline__ uint32_t swz64(uint32_t o) { return o ^ (((o >> 7) & 
 template <int D>
 __device__ __forceinline__ void tma_load_kv_tile(void* dst, const CUtensorMap* map, int row, uint64_t* bar) {
   tma_load_3d(dst, map, 0, row, 0, bar);   // all D/64 halves of the tile in one copy
+}
+
+template <int D>
+__device__ __forceinline__ void tma_load_kv_tile_hint(void* dst, const CUtensorMap* map, int row, uint64_t* bar,
+                                                      uint64_t policy) {
+  tma_load_3d_hint(dst, map, 0, row, 0, bar, policy);
 }
 
 template <int D>
