@@ -157,6 +157,18 @@ static TmLayout tm_layout(const kvs_pool* pool, int n_seq, int max_blocks, int g
   // are taken over the list of those blocks (positions k, k + n, k + 2n, ...
   // for item k of n), so that the diff blocks spread over all its items.
   L.compact = L.runs;
+#ifndef KVS_COMPACT_IB
+#define KVS_COMPACT_IB 24
+#endif
+  // Compact items take a fixed size: their lists hold unshared blocks only,
+  // so the split bound above does not apply.  On the all-gather round (about
+  // three claims per warp) items of 8 / 12 / 16 / 24 / 32 blocks measured
+  // 266 / 254 / 242 / 239 / 240 us per layer: below 24 the per-item costs
+  // (query load, split, merge slot) win, above it the last claims' tail.
+  if (L.compact) {
+    L.ib = KVS_COMPACT_IB;
+    L.n_chunks = (max_blocks + L.ib - 1) / L.ib;
+  }
   L.max_items = (L.wide ? 0 : grp * L.n_chunks_s) + (size_t)n_seq * L.n_chunks;
   L.max_sub = (L.ibs + 7) / 8;
   const size_t per_split = (size_t)n_seq * pool->desc.num_kv_heads * g * (pool->desc.head_dim + 2) * sizeof(float);
