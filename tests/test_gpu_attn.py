@@ -113,6 +113,26 @@ def test_overlapping_rope_segments_last_entry_wins():
     run_case(dataclasses.replace(w, rope_off=ro2, rope_segs=rs2))
 
 
+
+def test_rotation_calls_repeat_on_one_pool():
+    """Rotation calls on the wide tile: the token-major kernel takes its
+    claims from a per-pool counter that the merge resets, so consecutive
+    calls on one pool (two query sets, the first repeated) each match the
+    oracle, and the repeated call is bit-identical."""
+    w = W.make_allgather(seed=21, n_seq=6, n_segs=6, priv_blocks_lo=3, priv_blocks_hi=9, hq=10, hkv=2, n_layers=1)
+    ref = OF.dedup(w.tokens, w.seq_off, w.tier, w.block_tokens, w.max_blocks, w.seg_start_off, w.seg_start_blocks)
+    pool = H.bf16_pool(w)
+    rng = np.random.default_rng(5)
+    q1 = w.q_layer(0)
+    q2 = W.f32_to_bf16_bits(rng.standard_normal(q1.shape).astype(np.float32))
+    outs = []
+    for q_bits in (q1, q2, q1):
+        got = H.attn(pool, 0, q_bits, w, ref["block_table"])
+        H.assert_close_attn(got, oracle_out(w, pool, ref["block_table"], q_bits))
+        outs.append(got)
+    assert np.array_equal(outs[0], outs[2])
+    assert K.kvs_pool_check(pool) == 0
+
 def test_allgather_d64_rotation():
     w = W.make_allgather(seed=9, n_seq=3, n_segs=5, priv_blocks_lo=2, priv_blocks_hi=5, hq=4, hkv=2, d=64,
                          n_layers=1, theta=1e4)
