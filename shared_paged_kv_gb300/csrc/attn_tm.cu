@@ -1352,8 +1352,12 @@ static kvs_status launch_merge(const TmParams& prm, cudaStream_t st) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (cudaLaunchKernelEx(&cfg, tm_merge_kernel<D>, prm) != cudaSuccess)
+  if (cudaLaunchKernelEx(&cfg, tm_merge_kernel<D>, prm) != cudaSuccess) {
+    // the merge would have reset the token-major claim counter: do it here so
+    // that the pool's next call starts from zero
+    if (prm.dyn) cudaMemsetAsync(prm.claim_ctr, 0, sizeof(unsigned int), st);
     return fail(KVS_ERR_CUDA, "decode_attn: merge launch failed");
+  }
   count_launch();
   return check_launch("decode_attn_merge");
 }
