@@ -1203,6 +1203,9 @@ attn_tm_kernel(const __grid_constant__ TmParams p, const __grid_constant__ CUten
 // combine through shared memory.  The partition and the order are fixed, so
 // the result does not depend on which warp computed which split.
 constexpr int kMergeWarps = 8;
+#ifndef KVS_MERGE_SLOTS_PER_WARP
+#define KVS_MERGE_SLOTS_PER_WARP 64
+#endif
 constexpr int kMergeBatch = 12;
 
 template <int D>
@@ -1564,8 +1567,10 @@ kvs_status decode_attn_token_major(kvs_pool* pool, int layer, const void* q, int
   const int n_slots = L.n_chunks + (L.SG > 1 ? L.n_chunks_s : 0);
   if (L.compact) {
     // compact items fill only the first slots of a row (as many as its list
-    // needs items): the fewest warps whose ranges fit one 32-slot window
-    while (prm.mwpr < kMergeWarps && (n_slots + prm.mwpr - 1) / prm.mwpr > 32) prm.mwpr <<= 1;
+    // needs items): one warp per row while its range spans at most two
+    // 32-slot windows (rows of such calls are many; 32 measured 0.5 % slower
+    // on the all-gather round)
+    while (prm.mwpr < kMergeWarps && (n_slots + prm.mwpr - 1) / prm.mwpr > KVS_MERGE_SLOTS_PER_WARP) prm.mwpr <<= 1;
   } else {
     while (prm.mwpr < kMergeWarps && prm.mwpr * 2 * kMergeBatch < n_slots) prm.mwpr <<= 1;
   }
