@@ -133,6 +133,22 @@ def test_rotation_calls_repeat_on_one_pool():
     assert np.array_equal(outs[0], outs[2])
     assert K.kvs_pool_check(pool) == 0
 
+
+def test_rotation_calls_with_more_claims_than_tile_ctas():
+    """260 agents at 40 query / 8 KV heads: 11 sharing groups x 8 KV heads
+    give more wide-tile claims than the tile's CTAs (half of the SMs), so
+    CTAs take several claims in turn, each with its own query tile, splits
+    and tensor-memory epilogue; sampled agents match the oracle."""
+    w = W.make_allgather(seed=31, n_seq=260, n_segs=3, priv_blocks_lo=1, priv_blocks_hi=3, hq=40, hkv=8, n_layers=1)
+    ref = OF.dedup(w.tokens, w.seq_off, w.tier, w.block_tokens, w.max_blocks, w.seg_start_off, w.seg_start_blocks)
+    pool = H.bf16_pool(w)
+    q_bits = w.q_layer(0)
+    got = H.attn(pool, 0, q_bits, w, ref["block_table"])
+    agents = [0, 1, 24, 25, 130, 258, 259]
+    exp = oracle_out(w, pool, ref["block_table"], q_bits, agents=agents)
+    H.assert_close_attn(got[agents], exp[agents])
+    assert K.kvs_pool_check(pool) == 0
+
 def test_allgather_d64_rotation():
     w = W.make_allgather(seed=9, n_seq=3, n_segs=5, priv_blocks_lo=2, priv_blocks_hi=5, hq=4, hkv=2, d=64,
                          n_layers=1, theta=1e4)
