@@ -5,38 +5,44 @@
 //
 // Rotate-half pairing (i, i + d/2), frequency theta^(-2i/d), angles by the
 // Cody-Waite reduced evaluation of common.cuh.  One CTA = one job x 64
-// tokens, eight warps.  A warp step covers TPW tokens of one KV head: lane
-// (token tl, vector v) holds head dims [8v, 8v+8) and [d/2 + 8v, d/2 + 8v+8)
-// of its token as two 16-byte vectors, so the 8 cos/sin pairs a lane needs
-// depend on v only and stay in registers for the whole job; each token's
-// low and high halves are 128-byte (d = 128) coalesced runs.  Rotation in
-// fp32, rounding to bf16 (RNE).
+// tokens, four warps.  Lane (token tl, vector v) of a warp step holds head
+// dims [8v, 8v+8) and [d/2 + 8v, d/2 + 8v+8) of one token as two 16-byte
+// vectors, so the 8 cos/sin pairs it needs depend on v only and stay in
+// registers for the whole job; each token's low and high halves are 128-byte
+// (d = 128) coalesced runs.  A lane walks all KV heads of its token: the
+// block-table lookups and the index arithmetic are done once per token, and
+// the heads are loaded in batches before any of them is stored (the stores
+// go to the same slab, so the compiler could not move later loads above
+// them).  Rotation in fp32, rounding to bf16 (RNE).
 #include "common.cuh"
 #include "internal.h"
 
 namespace kvs {
 
 struct RopeParams {
-  uint16_t* slab;             // this layer's K slab, bf16 [cap][hkv][B][D]
+  uint16_t* slab;             // this layer's K slab, bf16 [cap][hkv][16][D]
   const int4* jobs;           // pairs of int4: (src_row, src_tok0, dst_row, dst_tok0), (n_tok, src_pos, dst_pos, -)
   const int32_t* src_table;
   const int32_t* dst_table;
   uint32_t* status;
-  int n_jobs, max_blocks, hkv, B, capacity, tok_per_cta;
+  int n_jobs, max_blocks, hkv, capacity, tok_per_cta;
   RopeSplit rs;
 };
 
-constexpr int kRopeWarps = 8;
+constexpr int kRopeWarps = 4;
 constexpr int kRopeTokPerCta = 64;
+constexpr int kRopeB = 16;          // tokens per block of a bf16 pool
+constexpr int kRopeHeadBatch = 4;   // KV heads loaded before any is stored
 
 template <int D>
 __global__ void __launch_bounds__(kRopeWarps * 32) rope_rerotate_kernel(const __grid_constant__ RopeParams p) {
   constexpr int VEC = 8;                 // bf16 per 16-byte vector
   constexpr int NV = D / 2 / VEC;        // vectors per half row
   constexpr int TPW = 32 / NV;           // tokens per warp step
+  constexpr int B = kRopeB, HB = kRopeHeadBatch;
   __shared__ float rsc[4 * 64];          // RoPE frequency pieces (lanes index them differently)
   const int job = blockIdx.x;
-  const int4 j0 = p.jobs[2 * job], j1 = p.jobs[2 * job + 1];
+  const int4 j0 = __ldg(p.jobs + 2 * job), j1 = __ldg(p.jobs + 2 * job + 1);
   const int n_tok = j1.x;
   const int t0 = blockIdx.y * p.tok_per_cta;
   if (t0 >= n_tok) return;
@@ -53,40 +59,50 @@ __global__ void __launch_bounds__(kRopeWarps * 32) rope_rerotate_kernel(const __
 #pragma unroll
   for (int e = 0; e < VEC; ++e) rope_cos_sin(rsc, v * VEC + e, delta, cs[e], sn[e]);
   const int t1 = min(n_tok, t0 + p.tok_per_cta);
-  const int steps = (t1 - t0 + TPW - 1) / TPW;
-  const long long lim = (long long)p.max_blocks * p.B;
-  for (int u = warp; u < steps * p.hkv; u += kRopeWarps) {
-    const int st = u / p.hkv, h = u - st * p.hkv;
-    const int t = t0 + st * TPW + tl;
-    if (t >= t1) continue;
+  const long long lim = (long long)p.max_blocks * B;
+  const size_t hstride = (size_t)B * D;   // elements between the KV heads of one token
+  for (int t = t0 + warp * TPW + tl; t < t1; t += kRopeWarps * TPW) {
     const int ts = j0.y + t, td = j0.w + t;
     if (ts < 0 || td < 0 || ts >= lim || td >= lim) {
       set_err(p.status, KVS_DEVERR_JOB);
       continue;
     }
-    const int bs = ts / p.B, bd = td / p.B;
+    const int bs = ts / B, bd = td / B;
     const int ps = __ldg(p.src_table + (size_t)j0.x * p.max_blocks + bs);
     const int pd = __ldg(p.dst_table + (size_t)j0.z * p.max_blocks + bd);
     if (ps < 0 || ps >= p.capacity || pd < 0 || pd >= p.capacity) {
       set_err(p.status, KVS_DEVERR_BLOCK_ID);
       continue;
     }
-    const size_t rs = (((size_t)ps * p.hkv + h) * p.B + (ts - bs * p.B)) * D + v * VEC;
-    const size_t rd = (((size_t)pd * p.hkv + h) * p.B + (td - bd * p.B)) * D + v * VEC;
-    const uint4 lo = __ldg(reinterpret_cast<const uint4*>(p.slab + rs));
-    const uint4 hi = __ldg(reinterpret_cast<const uint4*>(p.slab + rs + D / 2));
-    const uint32_t lw[4] = {lo.x, lo.y, lo.z, lo.w};
-    const uint32_t hw[4] = {hi.x, hi.y, hi.z, hi.w};
-    uint32_t ol[4], oh[4];
+    const uint16_t* src = p.slab + ((size_t)ps * p.hkv * B + (ts - bs * B)) * D + v * VEC;
+    uint16_t* dst = p.slab + ((size_t)pd * p.hkv * B + (td - bd * B)) * D + v * VEC;
+    for (int h0 = 0; h0 < p.hkv; h0 += HB) {
+      uint4 lo[HB], hi[HB];
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const float a0 = bf16_lo(lw[e]), a1 = bf16_hi(lw[e]);
-      const float b0 = bf16_lo(hw[e]), b1 = bf16_hi(hw[e]);
-      ol[e] = pack_bf16(a0 * cs[2 * e] - b0 * sn[2 * e], a1 * cs[2 * e + 1] - b1 * sn[2 * e + 1]);
-      oh[e] = pack_bf16(b0 * cs[2 * e] + a0 * sn[2 * e], b1 * cs[2 * e + 1] + a1 * sn[2 * e + 1]);
+      for (int k = 0; k < HB; ++k) {
+        if (h0 + k < p.hkv) {
+          lo[k] = __ldg(reinterpret_cast<const uint4*>(src + (h0 + k) * hstride));
+          hi[k] = __ldg(reinterpret_cast<const uint4*>(src + (h0 + k) * hstride + D / 2));
+        }
+      }
+#pragma unroll
+      for (int k = 0; k < HB; ++k) {
+        if (h0 + k >= p.hkv) break;
+        const uint32_t lw[4] = {lo[k].x, lo[k].y, lo[k].z, lo[k].w};
+        const uint32_t hw[4] = {hi[k].x, hi[k].y, hi[k].z, hi[k].w};
+        uint32_t ol[4], oh[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float a0 = bf16_lo(lw[e]), a1 = bf16_hi(lw[e]);
+          const float b0 = bf16_lo(hw[e]), b1 = bf16_hi(hw[e]);
+          ol[e] = pack_bf16(a0 * cs[2 * e] - b0 * sn[2 * e], a1 * cs[2 * e + 1] - b1 * sn[2 * e + 1]);
+          oh[e] = pack_bf16(b0 * cs[2 * e] + a0 * sn[2 * e], b1 * cs[2 * e + 1] + a1 * sn[2 * e + 1]);
+        }
+        uint16_t* o = dst + (h0 + k) * hstride;
+        *reinterpret_cast<uint4*>(o) = make_uint4(ol[0], ol[1], ol[2], ol[3]);
+        *reinterpret_cast<uint4*>(o + D / 2) = make_uint4(oh[0], oh[1], oh[2], oh[3]);
+      }
     }
-    *reinterpret_cast<uint4*>(p.slab + rd) = make_uint4(ol[0], ol[1], ol[2], ol[3]);
-    *reinterpret_cast<uint4*>(p.slab + rd + D / 2) = make_uint4(oh[0], oh[1], oh[2], oh[3]);
   }
 }
 
@@ -99,7 +115,8 @@ extern "C" kvs_status kvs_rope_rerotate(kvs_pool* pool, int32_t layer, const kvs
                                         const int32_t* dst_table_dev, int32_t max_blocks, cudaStream_t stream) {
   if (!pool) return fail(KVS_ERR_INVALID_ARG, "rope_rerotate: null pool");
   const kvs_pool_desc& d = pool->desc;
-  if (d.dtype != KVS_DTYPE_BF16) return fail(KVS_ERR_INVALID_ARG, "rope_rerotate: bf16 pools only");
+  if (d.dtype != KVS_DTYPE_BF16 || d.block_tokens != kRopeB)
+    return fail(KVS_ERR_INVALID_ARG, "rope_rerotate: bf16 pools (16-token blocks) only");
   if (layer < 0 || layer >= d.num_layers) return fail(KVS_ERR_INVALID_ARG, "rope_rerotate: layer out of range");
   if (n_jobs < 0 || max_job_tokens < 0 || max_blocks < 1) return fail(KVS_ERR_INVALID_ARG, "rope_rerotate: bad sizes");
   if (!(theta > 0.f)) return fail(KVS_ERR_INVALID_ARG, "rope_rerotate: theta must be positive");
@@ -115,7 +132,6 @@ extern "C" kvs_status kvs_rope_rerotate(kvs_pool* pool, int32_t layer, const kvs
   p.n_jobs = n_jobs;
   p.max_blocks = max_blocks;
   p.hkv = d.num_kv_heads;
-  p.B = d.block_tokens;
   p.capacity = d.capacity_blocks;
   p.tok_per_cta = kRopeTokPerCta;
   rope_split_host(theta, d.head_dim, p.rs.c);

@@ -31,10 +31,12 @@ def rope_tolerance(e):
 
 
 # ---------------------------------------------------------------- RoPE ----
-def rope_case(w, check_rows=None, device_values=False):
+def rope_case(w, check_rows=None, device_values=False, edit_jobs=None):
     ref = OF.dedup(w.tokens, w.seq_off, w.tier, w.block_tokens, w.max_blocks, w.seg_start_off, w.seg_start_blocks)
     n_phys = ref["n_phys"]
     jobs, dst_table, n_dst = W.rope_jobs_for(w, first_free_block=n_phys)
+    if edit_jobs is not None:
+        jobs = edit_jobs(jobs)
     cap = n_phys + n_dst
     if device_values:
         # full size: K drawn by torch's seeded generator on the device
@@ -49,6 +51,7 @@ def rope_case(w, check_rows=None, device_values=False):
         kdev = pool.dev["k"][0]
     before = kdev[:n_phys].clone()
     sel = jobs if check_rows is None else jobs[check_rows]
+    sel = sel[sel[:, 4] > 0]
     K.kvs_rope_rerotate(pool, 0, H.i32(jobs), len(jobs), int(jobs[:, 4].max()), w.theta,
                         H.i32(ref["block_table"]), H.i32(dst_table), w.max_blocks)
     torch.cuda.synchronize()
@@ -83,6 +86,57 @@ def test_rope_small():
 def test_rope_small_d64_theta1e4():
     rope_case(W.make_allgather(seed=3, n_seq=3, n_segs=5, priv_blocks_lo=2, priv_blocks_hi=6, hq=4, hkv=2, d=64,
                                n_layers=1, theta=1e4))
+
+
+def test_rope_ragged_jobs():
+    """Jobs that start and end inside blocks, with lengths that are not a
+    multiple of the tokens a warp step covers, an empty job, and five KV
+    heads (a head batch that does not divide them)."""
+    def ragged(jobs):
+        out = jobs.copy()
+        for i in range(len(out)):
+            o = (7 * i) % 13
+            n = int(out[i, 4]) - o - (i % 5)
+            out[i, 1] += o; out[i, 3] += o; out[i, 5] += o; out[i, 6] += o
+            out[i, 4] = max(n, 0) if i != 3 else 0
+        return out
+    n = rope_case(W.make_allgather(seed=4, n_seq=4, n_segs=6, priv_blocks_lo=2, priv_blocks_hi=6, hq=10, hkv=5,
+                                   n_layers=1), edit_jobs=ragged)
+    assert n > 0
+
+
+def test_rope_bad_jobs_are_flagged():
+    """A token range past the block table, an unmapped destination block and
+    a shift of 2^18 each set their device error flag; nothing faults and the
+    pool's blocks are not written."""
+    w = W.make_allgather(n_seq=2, n_segs=2, priv_blocks_lo=2, priv_blocks_hi=3, hq=8, hkv=2, n_layers=1)
+    ref = OF.dedup(w.tokens, w.seq_off, w.tier, w.block_tokens, w.max_blocks, w.seg_start_off, w.seg_start_blocks)
+    n_phys = ref["n_phys"]
+    jobs, dst_table, n_dst = W.rope_jobs_for(w, first_free_block=n_phys)
+    pool = H.bf16_pool(w, capacity=n_phys + n_dst, with_diff=False)
+    kdev = pool.dev["k"][0]
+    lim = w.max_blocks * w.block_tokens
+    cases = [
+        (dict(col=3, val=lim - 8), K.KVS_DEVERR_JOB),            # runs past the table
+        (dict(col=2, val=1, unmap=True), K.KVS_DEVERR_BLOCK_ID),  # destination row without blocks
+        (dict(col=6, val=None), K.KVS_DEVERR_ROPE_RANGE),         # shift 2^18
+    ]
+    for edit, flag in cases:
+        j = jobs[:1].copy()
+        dt = dst_table.copy()
+        if edit["col"] == 6:
+            j[0, 6] = j[0, 5] + (1 << 18)
+        else:
+            j[0, edit["col"]] = edit["val"]
+        if edit.get("unmap"):
+            dt[1, :] = -1
+        before = kdev.clone()
+        K.kvs_rope_rerotate(pool, 0, H.i32(j), 1, int(j[0, 4]), w.theta, H.i32(ref["block_table"]), H.i32(dt),
+                            w.max_blocks)
+        torch.cuda.synchronize()
+        assert K.kvs_pool_check(pool) & flag
+        if flag != K.KVS_DEVERR_JOB:
+            assert torch.equal(kdev, before)
 
 
 def test_rope_full_size_sampled_jobs():
