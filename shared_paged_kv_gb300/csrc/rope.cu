@@ -13,7 +13,9 @@
 // block-table lookups and the index arithmetic are done once per token, and
 // the heads are loaded in batches before any of them is stored (the stores
 // go to the same slab, so the compiler could not move later loads above
-// them).  Rotation in fp32, rounding to bf16 (RNE).
+// them).  The rotated rows are written with streaming stores: a layer's
+// destinations are far larger than L2.  Rotation in fp32, rounding to bf16
+// (RNE).
 #include "common.cuh"
 #include "internal.h"
 
@@ -30,12 +32,26 @@ struct RopeParams {
 };
 
 constexpr int kRopeWarps = 4;
-constexpr int kRopeTokPerCta = 64;
+#ifndef KVS_ROPE_TOK_PER_CTA
+#define KVS_ROPE_TOK_PER_CTA 64
+#endif
+constexpr int kRopeTokPerCta = KVS_ROPE_TOK_PER_CTA;
 constexpr int kRopeB = 16;          // tokens per block of a bf16 pool
-constexpr int kRopeHeadBatch = 4;   // KV heads loaded before any is stored
+// Measured on the all-gather layer (524,288 rows, 8 KV heads): batches of
+// 4 / 8 heads took 176 / 171 us with plain stores; streaming (evict-first)
+// stores took the 8-head batch to 160 us.  64 tokens per CTA beat 32 and
+// 128; capping registers for more CTAs per SM (spills, or 2-head batches)
+// was slower.
+#ifndef KVS_ROPE_HEAD_BATCH
+#define KVS_ROPE_HEAD_BATCH 8
+#endif
+#ifndef KVS_ROPE_MIN_CTAS
+#define KVS_ROPE_MIN_CTAS 1
+#endif
+constexpr int kRopeHeadBatch = KVS_ROPE_HEAD_BATCH;   // KV heads loaded before any is stored
 
 template <int D>
-__global__ void __launch_bounds__(kRopeWarps * 32) rope_rerotate_kernel(const __grid_constant__ RopeParams p) {
+__global__ void __launch_bounds__(kRopeWarps * 32, KVS_ROPE_MIN_CTAS) rope_rerotate_kernel(const __grid_constant__ RopeParams p) {
   constexpr int VEC = 8;                 // bf16 per 16-byte vector
   constexpr int NV = D / 2 / VEC;        // vectors per half row
   constexpr int TPW = 32 / NV;           // tokens per warp step
@@ -99,8 +115,8 @@ __global__ void __launch_bounds__(kRopeWarps * 32) rope_rerotate_kernel(const __
           oh[e] = pack_bf16(b0 * cs[2 * e] + a0 * sn[2 * e], b1 * cs[2 * e + 1] + a1 * sn[2 * e + 1]);
         }
         uint16_t* o = dst + (h0 + k) * hstride;
-        *reinterpret_cast<uint4*>(o) = make_uint4(ol[0], ol[1], ol[2], ol[3]);
-        *reinterpret_cast<uint4*>(o + D / 2) = make_uint4(oh[0], oh[1], oh[2], oh[3]);
+        __stcs(reinterpret_cast<uint4*>(o), make_uint4(ol[0], ol[1], ol[2], ol[3]));
+        __stcs(reinterpret_cast<uint4*>(o + D / 2), make_uint4(oh[0], oh[1], oh[2], oh[3]));
       }
     }
   }
