@@ -1050,12 +1050,7 @@ attn_tm_kernel(const __grid_constant__ TmParams p, const __grid_constant__ CUten
     const bool has_diff = DIFF && (bword >> 30) != 0;
     const int b = bword & ((1 << 29) - 1);
     const bool loaded = ((bword >> 29) & 1) == 0;
-    const int s2 = (i + 1) % S;
-    if (has_diff && !mbar_wait_bounded(&bars[warp][s2], ((i + 1) / S) & 1, p.status)) {
-      timed_out = true;
-      ++i;   // the stage at i was consumed; drain from the one that timed out
-      break;
-    }
+    const int s2 = (i + 1) % S;   // a diff block's {V, DV} stage, waited for before P V
     if (item != cur) {
       if (cur >= 0) flush();
       cur = item;
@@ -1158,6 +1153,13 @@ attn_tm_kernel(const __grid_constant__ TmParams p, const __grid_constant__ CUten
           acc[mt][0] *= al0; acc[mt][1] *= al1;
           acc[mt][2] *= al0; acc[mt][3] *= al1;
         }
+      }
+      // a diff block's {V, DV} tiles (the stage after S's) are needed from here
+      // on: S and the softmax above overlapped their copy
+      if (has_diff && !mbar_wait_bounded(&bars[warp][s2], ((i + 1) / S) & 1, p.status)) {
+        timed_out = true;
+        ++i;   // stage s was re-armed for position i + 2 above: drain from there
+        break;
       }
       // P^T as the B operand (k = token, n = query column), bf16 hi + lo
       uint32_t h0, l0_, h1, l1_;
