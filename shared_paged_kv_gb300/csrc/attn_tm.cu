@@ -1040,13 +1040,13 @@ attn_tm_kernel(const __grid_constant__ TmParams p, const __grid_constant__ CUten
   bool timed_out = false;
   for (;;) {
     const int s = i % S;
-    if (!mbar_wait_bounded(&bars[warp][s], (i / S) & 1, p.status)) {
-      timed_out = true;
-      break;
-    }
+    // The stage's record was written by lane 0 when it armed the stage: the
+    // item switch (the previous item's split stores, the next query loads)
+    // and the query rotation below run while the stage's copies are in flight.
+    __syncwarp();
     const int4 srec = st_rec[warp][s];
     const int item = srec.x, bword = srec.y, emask = srec.z;
-    if (item < 0) break;
+    if (item < 0) break;   // armed without copies: the claims are exhausted
     const bool has_diff = DIFF && (bword >> 30) != 0;
     const int b = bword & ((1 << 29) - 1);
     const bool loaded = ((bword >> 29) & 1) == 0;
@@ -1083,14 +1083,18 @@ attn_tm_kernel(const __grid_constant__ TmParams p, const __grid_constant__ CUten
       load_q();
       cur_delta = 0;
     }
-    if (loaded) {
-      if (ROPE) {
-        const int nd = srec.w;   // the plan checked |nd| < 2^18
-        if (nd != cur_delta) {
-          if (nd == 0) load_q(); else rotate_q(nd);
-          cur_delta = nd;
-        }
+    if (ROPE && loaded) {
+      const int nd = srec.w;   // the plan checked |nd| < 2^18
+      if (nd != cur_delta) {
+        if (nd == 0) load_q(); else rotate_q(nd);
+        cur_delta = nd;
       }
+    }
+    if (!mbar_wait_bounded(&bars[warp][s], (i / S) & 1, p.status)) {
+      timed_out = true;
+      break;
+    }
+    if (loaded) {
       // {K, V}, or with a diff {K, DK} in stage s and {V, DV} in stage s2
       const uint32_t tkb = wbase_u32 + s * STAGE, dkb = tkb + TILE;
       const uint32_t tvb = has_diff ? wbase_u32 + s2 * STAGE : tkb + TILE, dvb = tvb + TILE;
