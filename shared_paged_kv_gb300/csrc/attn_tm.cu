@@ -1203,19 +1203,30 @@ attn_tm_kernel(const __grid_constant__ TmParams p, const __grid_constant__ CUten
 // Split merge: p.mwpr warps (1, 2, 4 or 8) per (sequence, query head) row,
 // eight warps per CTA.  A row's splits sit in "slots": the private split of
 // each chunk, then (with sharing groups) the shared split of each chunk.
-// Each warp takes a fixed range of about kMergeBatch slots: one pass loads
-// their (m, l) (one slot per lane), a second loads every existing split of
-// the range at once (each lane a D/32 slice), and the warps' partial states
-// combine through shared memory.  The partition and the order are fixed, so
+// Each warp takes a fixed range of slots: one pass loads their (m, l) (one
+// slot per lane), a second loads the existing splits of the range
+// kMergeBatch at a time (each lane a D/32 slice), and the warps' partial
+// states combine through shared memory.  The partition and the order are fixed, so
 // the result does not depend on which warp computed which split.
 constexpr int kMergeWarps = 8;
 #ifndef KVS_MERGE_SLOTS_PER_WARP
 #define KVS_MERGE_SLOTS_PER_WARP 64
 #endif
-constexpr int kMergeBatch = 12;
+// Four CTAs per SM (64 registers; batches of 8 split loads per lane, the
+// most that fits without spills) keep the all-gather round's 320 merge CTAs
+// in one wave: per layer 230.9 us with two CTAs per SM and batches of 12,
+// 228.0 us with three, 228.6 us with four; the GQA fan-out took 21.2, 21.4
+// and 20.7 us.
+#ifndef KVS_MERGE_BATCH
+#define KVS_MERGE_BATCH 8
+#endif
+#ifndef KVS_MERGE_MIN_CTAS
+#define KVS_MERGE_MIN_CTAS 4
+#endif
+constexpr int kMergeBatch = KVS_MERGE_BATCH;
 
 template <int D>
-__global__ void __launch_bounds__(kMergeWarps * 32, 2) tm_merge_kernel(const __grid_constant__ TmParams p) {
+__global__ void __launch_bounds__(kMergeWarps * 32, KVS_MERGE_MIN_CTAS) tm_merge_kernel(const __grid_constant__ TmParams p) {
   asm volatile("griddepcontrol.wait;" ::: "memory");
   // the token-major grid has completed: its claim counter starts the next call at zero
   if (p.dyn && blockIdx.x == 0 && threadIdx.x == 0) *p.claim_ctr = 0u;
