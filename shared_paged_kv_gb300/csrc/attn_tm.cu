@@ -444,6 +444,7 @@ __device__ void plan_runs(const PlanParams& pp, int gi, int a0, int nm, unsigned
 // no entry covers keeps shift 0.  bwin keeps the winning index for the run
 // search (a run must lie in the last entry covering each of its blocks).
 __global__ void __launch_bounds__(256) tm_plan_shifts(PlanParams pp) {
+  pdl_enter();
   const int tid = threadIdx.x, nt = blockDim.x;
   for (int a = blockIdx.x; a < pp.n_seq; a += gridDim.x) {
     int32_t* win = pp.bwin + (size_t)a * pp.max_blocks;
@@ -470,6 +471,7 @@ __global__ void __launch_bounds__(256) tm_plan_shifts(PlanParams pp) {
 }
 
 __global__ void __launch_bounds__(512) tm_plan_groups(PlanParams pp) {
+  pdl_enter();
   __shared__ unsigned long long s_key[kRunCap];
   __shared__ int s_dl[kRunCap];
   __shared__ uint8_t s_ex[kRunCap];
@@ -591,6 +593,7 @@ __global__ void __launch_bounds__(512) tm_plan_groups(PlanParams pp) {
 // chunk-major up to the interleaving of CTAs; results do not depend on the
 // order (every split has a fixed slot and a fixed merge order).
 __global__ void __launch_bounds__(256) tm_plan_items(PlanParams pp) {
+  pdl_enter();
   __shared__ int warp_sums[32];
   __shared__ int s_base, s_wbase;
   const int n_sh = (pp.SG > 1 && !pp.runs) ? pp.n_groups * pp.n_chunks_s : 0, n_pr = pp.n_seq * pp.n_chunks;
@@ -1525,19 +1528,23 @@ kvs_status decode_plan_token_major(kvs_pool* pool, int n_q_heads, const int32_t*
   // item counters start at zero (several CTAs add to them)
   if (cudaMemsetAsync(t.hdr, 0, 64, stream) != cudaSuccess) return fail(KVS_ERR_CUDA, "decode_plan: memset failed");
   if (rope) {
-    tm_plan_shifts<<<std::max(1, std::min(n_seq, pool->num_sms * 8)), 256, 0, stream>>>(pp);
+    if (launch_pdl(tm_plan_shifts, dim3(std::max(1, std::min(n_seq, pool->num_sms * 8))), dim3(256), stream, pp) !=
+        cudaSuccess)
+      return fail(KVS_ERR_CUDA, "decode_plan: launch failed");
     count_launch();
     const kvs_status st0 = check_launch("decode_plan");
     if (st0 != KVS_OK) return st0;
   }
   const int g1 = std::max(1, std::min(L.n_groups, pool->num_sms * 4));
-  tm_plan_groups<<<g1, 512, 0, stream>>>(pp);
+  if (launch_pdl(tm_plan_groups, dim3(g1), dim3(512), stream, pp) != cudaSuccess)
+    return fail(KVS_ERR_CUDA, "decode_plan: launch failed");
   count_launch();
   kvs_status st = check_launch("decode_plan");
   if (st != KVS_OK) return st;
   const long long slots = (long long)(L.max_items + L.max_witems);
   const int g2 = (int)std::max<long long>(1, std::min<long long>((slots + 255) / 256, pool->num_sms * 8));
-  tm_plan_items<<<g2, 256, 0, stream>>>(pp);
+  if (launch_pdl(tm_plan_items, dim3(g2), dim3(256), stream, pp) != cudaSuccess)
+    return fail(KVS_ERR_CUDA, "decode_plan: launch failed");
   count_launch();
   return check_launch("decode_plan");
 }

@@ -217,6 +217,31 @@ __device__ __forceinline__ void split_bf16(float x, float y, uint32_t& hi, uint3
 // in float32 and their fractional parts are exact; delta*c3 < 1 carries only
 // float32 rounding.  The reduced angle lies in [-pi, pi], where the hardware
 // __sincosf is accurate to about 4e-7 absolute.
+// Kernels of a chain on one stream (the dedup steps, the plan steps) are
+// programmatic dependent launches: each is scheduled while the one before it
+// runs, and its first statement (pdl_enter) waits for that kernel to complete
+// with its writes visible, then lets the next kernel of the chain be
+// scheduled.  A kernel launched without the attribute passes the wait at once.
+__device__ __forceinline__ void pdl_enter() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;");
+}
+
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, cudaStream_t st, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, args...);
+}
+
 struct RopeSplit {
   float c[4][64];   // [piece][frequency index], up to head_dim 128
 };

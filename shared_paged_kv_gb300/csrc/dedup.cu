@@ -87,6 +87,7 @@ __device__ __forceinline__ void seq_geom(const DedupParams& p, int s, int64_t& o
 
 // 1a. CalcHash of every full block, one thread per slot
 __global__ void dedup_hash(DedupParams p) {
+  pdl_enter();
   const int slot = blockIdx.x * blockDim.x + threadIdx.x;
   if (slot >= p.n_seq * p.max_blocks) return;
   const int s = slot / p.max_blocks, b = slot - s * p.max_blocks;
@@ -110,6 +111,7 @@ __global__ void dedup_hash(DedupParams p) {
 
 // 1b. one warp per sequence: segment starts and chain keys
 __global__ void dedup_prep(DedupParams p) {
+  pdl_enter();
   const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   if (warp >= p.n_seq) return;
@@ -202,6 +204,7 @@ __device__ __forceinline__ uint32_t table_slot(uint64_t k, uint32_t mask) {
 
 // 2. insert every shareable slot
 __global__ void dedup_insert(DedupParams p) {
+  pdl_enter();
   const int slot = blockIdx.x * blockDim.x + threadIdx.x;
   if (slot >= p.n_seq * p.max_blocks) return;
   const uint64_t k = p.key[slot];
@@ -238,6 +241,7 @@ __device__ __forceinline__ bool same_block_tokens(const DedupParams& p, int s1, 
 
 // 3. resolve and verify representatives
 __global__ void dedup_resolve(DedupParams p) {
+  pdl_enter();
   const int slot = blockIdx.x * blockDim.x + threadIdx.x;
   if (slot >= p.n_seq * p.max_blocks) return;
   const uint64_t k = p.key[slot];
@@ -265,6 +269,7 @@ __global__ void dedup_resolve(DedupParams p) {
 
 // 4. exact brute force, only after a collision was detected
 __global__ void dedup_fallback(DedupParams p) {
+  pdl_enter();
   if (*(volatile uint32_t*)p.flags == 0u) return;
   const int slot = blockIdx.x * blockDim.x + threadIdx.x;
   if (slot >= p.n_seq * p.max_blocks) return;
@@ -310,6 +315,7 @@ __device__ __forceinline__ int block_sum_1024(int f, int* warp_sums) {
 }
 
 __global__ void __launch_bounds__(kNumTile) dedup_count(DedupParams p) {
+  pdl_enter();
   __shared__ int warp_sums[32];
   const int n = p.n_seq * p.max_blocks;
   const int slot = blockIdx.x * kNumTile + threadIdx.x;
@@ -321,6 +327,7 @@ __global__ void __launch_bounds__(kNumTile) dedup_count(DedupParams p) {
 // 5b. one CTA: the tiles' counts become their exclusive prefix sums (slot
 // order), and the total is the number of physical blocks
 __global__ void __launch_bounds__(kNumTile) dedup_tiles(DedupParams p, int n_tiles) {
+  pdl_enter();
   __shared__ int warp_sums[32];
   int carry = 0;
   for (int base = 0; base < n_tiles; base += kNumTile) {
@@ -339,6 +346,7 @@ __global__ void __launch_bounds__(kNumTile) dedup_tiles(DedupParams p, int n_til
 
 // 5c. number the first occurrences in slot order from the tile's offset
 __global__ void __launch_bounds__(kNumTile) dedup_number(DedupParams p) {
+  pdl_enter();
   __shared__ int warp_sums[32];
   const int n = p.n_seq * p.max_blocks;
   const int slot = blockIdx.x * kNumTile + threadIdx.x;
@@ -350,6 +358,7 @@ __global__ void __launch_bounds__(kNumTile) dedup_number(DedupParams p) {
 
 // 6. block table + refcounts
 __global__ void dedup_table(DedupParams p) {
+  pdl_enter();
   const int slot = blockIdx.x * blockDim.x + threadIdx.x;
   if (slot >= p.n_seq * p.max_blocks) return;
   const int r = p.rep[slot];
@@ -432,15 +441,17 @@ extern "C" kvs_status kvs_fingerprint_dedup(kvs_pool* pool, const uint32_t* toke
   }
   const int n = static_cast<int>(slots);
   const int tb = 256;
-  dedup_hash<<<(n + tb - 1) / tb, tb, 0, stream>>>(p);
-  dedup_prep<<<(n_seq * 32 + tb - 1) / tb, tb, 0, stream>>>(p);
-  dedup_insert<<<(n + tb - 1) / tb, tb, 0, stream>>>(p);
-  dedup_resolve<<<(n + tb - 1) / tb, tb, 0, stream>>>(p);
-  dedup_fallback<<<(n + tb - 1) / tb, tb, 0, stream>>>(p);
-  dedup_count<<<n_tiles, kNumTile, 0, stream>>>(p);
-  dedup_tiles<<<1, kNumTile, 0, stream>>>(p, n_tiles);
-  dedup_number<<<n_tiles, kNumTile, 0, stream>>>(p);
-  dedup_table<<<(n + tb - 1) / tb, tb, 0, stream>>>(p);
+  const dim3 gs((n + tb - 1) / tb);
+  cudaError_t e = launch_pdl(dedup_hash, gs, dim3(tb), stream, p);
+  if (e == cudaSuccess) e = launch_pdl(dedup_prep, dim3((n_seq * 32 + tb - 1) / tb), dim3(tb), stream, p);
+  if (e == cudaSuccess) e = launch_pdl(dedup_insert, gs, dim3(tb), stream, p);
+  if (e == cudaSuccess) e = launch_pdl(dedup_resolve, gs, dim3(tb), stream, p);
+  if (e == cudaSuccess) e = launch_pdl(dedup_fallback, gs, dim3(tb), stream, p);
+  if (e == cudaSuccess) e = launch_pdl(dedup_count, dim3(n_tiles), dim3(kNumTile), stream, p);
+  if (e == cudaSuccess) e = launch_pdl(dedup_tiles, dim3(1), dim3(kNumTile), stream, p, n_tiles);
+  if (e == cudaSuccess) e = launch_pdl(dedup_number, dim3(n_tiles), dim3(kNumTile), stream, p);
+  if (e == cudaSuccess) e = launch_pdl(dedup_table, gs, dim3(tb), stream, p);
+  if (e != cudaSuccess) return fail(KVS_ERR_CUDA, "fingerprint_dedup: launch failed");
   count_launch(9);
   return check_launch("fingerprint_dedup");
 }
