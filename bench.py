@@ -1,22 +1,27 @@
 """Benchmark of the shared paged KV decode step on GB300.
 
-Workload (the configuration the headline metric is quoted on): 8 agents x
+Headline workload (the configuration the metric is quoted on): 8 agents x
 16384-token contexts, 32 query heads = 32 KV heads, head_dim 128, 16-token
 blocks, 60 % common prefix stored once (614 shared + 8 x 410 private blocks
 per layer), 32 layers, bf16 values ~N(0,1), one decode query per agent.
 
 One step = the whole hot path on that batch: GPU block fingerprints + dedup
-of the 8 token sequences (block tables, refcounts), then decode attention on
-all 32 layers through the deduplicated pool.  value = decode tokens/s =
-agents / step time.  KV of one step is 32.7 GB, far above L2, so no flush is
-needed between steps.
+of the 8 token sequences (block tables, refcounts), one work plan, then
+decode attention on all 32 layers through the deduplicated pool.  value =
+decode tokens/s = agents / step time, timed with two CUDA events around the
+K steps (no events inside them).  KV of one step is 32.7 GB, far above L2, so
+no flush is needed between steps.  The per-layer attention time of the
+roofline comes from a separate breakdown pass of the same steps with events
+around every layer.
 
-Also reported: KV GB/s (unique bytes / step time), the attention kernel's
-roofline (algorithmic bytes per launch / average CUDA-event launch time vs
-the measured HBM peak), RoPE-reuse throughput (one layer of the all-gather
-round: 64 agents x 64 shared 128-token segments re-rotated into private
-blocks), the end-to-end rate through the public API with pinned host buffers,
-and the CPU oracle timed on a bounded sample of the same workload.
+Also reported on the same line: KV GB/s, the attention kernel's roofline
+(algorithmic bytes per launch / average launch time vs the measured HBM
+peak), the end-to-end rate through the public API with pinned host buffers,
+the CPU oracle on every host core over a bounded sample of the workload, and
+one key per other synthetic workload (tiny, tiny x 4096, GQA fan-out,
+all-gather round, Q4, selection, mirror build, RoPE re-rotation), each with
+eager and CUDA-graph-replayed times, algorithmic bytes per launch and the
+fraction of the measured HBM peak.
 
 Multi-GPU: the path partitions by agent with no exchange, so N ranks each run
 the full workload on their own agents (weak scaling, no collective).
@@ -41,6 +46,7 @@ METRIC = "decode-attn tokens/s & KV GB/s vs GB300 HBM roofline; RoPE-reuse token
 UNIT = "tokens/s"
 WORKLOAD = ("mha7b: 8 agents x 16384-token context, 60% shared prefix (614 shared + 8x410 private "
             "16-token blocks), 32 q heads = 32 kv heads, head_dim 128, bf16, 32 layers, 1 decode token per agent")
+EXTRA_CONFIGS = ["tiny", "gqa_fanout", "allgather", "q4", "select", "mirror"]
 
 
 def parse():
@@ -52,9 +58,14 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-rope", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
-    ap.add_argument("--layers", type=int, default=32)
-    ap.add_argument("--workload", default="mha7b", choices=["mha7b", "tiny", "gqa_fanout", "allgather", "q4", "select", "mirror", "cow", "evict", "io"],
-                    help="mha7b is the headline workload; the others print a per-workload record for profiling")
+    ap.add_argument("--no-extra", action="store_true", help="headline workload only")
+    ap.add_argument("--extra-steps", type=int, default=10, help="timed steps of each extra workload")
+    ap.add_argument("--layers", type=int, default=None, help="layers (default: the workload's own)")
+    ap.add_argument("--workload", default="mha7b",
+                    choices=["mha7b"] + EXTRA_CONFIGS + ["cow", "evict", "io"],
+                    help="mha7b is the headline workload; the others print one record")
+    ap.add_argument("--cpu-oracle", nargs=3, type=int, metavar=("LAYERS", "REPS", "PAIRS"),
+                    help=argparse.SUPPRESS)
     return ap.parse_args()
 
 
@@ -167,75 +178,127 @@ class ClockSampler:
 
 
 # ----------------------------------------------------------- CPU oracle -----
-CPU_PAIRS = [(a, h) for a in range(8) for h in (0, 9, 22, 31)]
+# The oracle as it stands, on the host cores: the dedup of all 8 sequences
+# (a sequential scan, one core) plus (agent, head) attention pairs of one
+# layer (dense materialisation + fp64 attention) spread over a spawn pool of
+# every usable core, then scaled to a full step of 8 agents x 32 heads x the
+# step's layers.  The same sample serves the cpu_baseline key and the
+# reference arm.
+_ORACLE = {}
 
 
-def cpu_sample_text(n_pairs):
-    return (f"oracle dedup of all 8 sequences + {n_pairs} (agent, head) pairs of one mha7b layer through the fp64 "
-            "oracle (dense materialise + attention), scaled to a full step of 8 agents x 32 heads x 32 layers")
-
-
-def cpu_oracle_step_seconds(layers: int, reps: int = 1, n_pairs: int = len(CPU_PAIRS)):
-    """Time the oracle as it stands on a bounded sample of the workload, reps
-    times; returns the extrapolated seconds of one full step for each rep.
-    Runs in a fresh interpreter with BLAS pinned to one thread, so it uses one
-    host core."""
-    code = f"""
-import sys, time, json
-sys.path.insert(0, {ROOT!r})
-import numpy as np
-from shared_paged_kv_gb300 import workloads as W
-from oracle import attention as OA, fingerprint as OF
-w = W.make_mha7b(n_layers=1)
-pairs = {CPU_PAIRS[:n_pairs]!r}
-rng = np.random.default_rng(0)
-out = []
-for rep in range({reps}):
-    t0 = time.perf_counter()
+def _oracle_init(seed):
+    """Worker start: the dedup result and one set of K/V values of one head
+    (the oracle's cost does not depend on the values)."""
+    from shared_paged_kv_gb300 import workloads as W
+    from oracle import fingerprint as OF
+    w = W.make_mha7b(n_layers=1)
     ref = OF.dedup(w.tokens, w.seq_off, w.tier, w.block_tokens, w.max_blocks)
-    t_dedup = time.perf_counter() - t0
+    rng = np.random.default_rng(seed)
     cap = ref["n_phys"]
-    t_attn = 0.0
-    for a, h in pairs:
-        k = rng.standard_normal((cap, 1, 16, 128)).astype(np.float32)
-        v = rng.standard_normal((cap, 1, 16, 128)).astype(np.float32)
-        q = rng.standard_normal((1, 1, 128)).astype(np.float32)
-        t0 = time.perf_counter()
-        OA.decode_attention(q, k, v, ref["block_table"][a:a+1], w.seq_len[a:a+1], 16, w.scale)
-        t_attn += time.perf_counter() - t0
-    out.append(t_dedup + t_attn / len(pairs) * 8 * 32 * {layers})
-print(json.dumps(out))
-"""
+    _ORACLE.update(w=w, table=ref["block_table"],
+                   k=rng.standard_normal((cap, 1, 16, 128)).astype(np.float32),
+                   v=rng.standard_normal((cap, 1, 16, 128)).astype(np.float32),
+                   q=rng.standard_normal((1, 1, 128)).astype(np.float32))
+
+
+def _oracle_warm(_):
+    time.sleep(0.05)
+    return len(_ORACLE)
+
+
+def _oracle_pair(a):
+    from oracle import attention as OA
+    o = _ORACLE
+    w = o["w"]
+    OA.decode_attention(o["q"], o["k"], o["v"], o["table"][a:a + 1], w.seq_len[a:a + 1], 16, w.scale)
+    return a
+
+
+def host_cores() -> int:
+    if hasattr(os, "sched_getaffinity"):
+        return len(os.sched_getaffinity(0))
+    return os.cpu_count() or 1
+
+
+def cpu_oracle_run(layers: int, reps: int, n_pairs: int) -> dict:
+    """Runs in its own interpreter (bench.py --cpu-oracle): returns the cores
+    used and, per rep, the extrapolated seconds of one full step."""
+    import multiprocessing as mp
+    from shared_paged_kv_gb300 import workloads as W
+    from oracle import fingerprint as OF
+    cores = host_cores()
+    w = W.make_mha7b(n_layers=1)
+    agents = [p % 8 for p in range(n_pairs)]
+    total_pairs = 8 * 32 * layers
+    steps, dedup_s, pairs_s = [], [], []
+    with mp.get_context("spawn").Pool(cores, initializer=_oracle_init, initargs=(0,)) as pool:
+        pool.map(_oracle_warm, range(4 * cores), chunksize=1)
+        for _ in range(reps):
+            t0 = time.perf_counter()
+            OF.dedup(w.tokens, w.seq_off, w.tier, w.block_tokens, w.max_blocks)
+            t1 = time.perf_counter()
+            pool.map(_oracle_pair, agents, chunksize=1)
+            t2 = time.perf_counter()
+            dedup_s.append(t1 - t0)
+            pairs_s.append(t2 - t1)
+            steps.append((t1 - t0) + (t2 - t1) * total_pairs / n_pairs)
+    return {"cores": cores, "steps": steps, "dedup_s": dedup_s, "pairs_wall_s": pairs_s, "n_pairs": n_pairs,
+            "scale": total_pairs / n_pairs}
+
+
+def cpu_oracle(layers: int, reps: int) -> dict:
+    """The oracle timing in a fresh interpreter (BLAS pinned to one thread per
+    worker process); 4 pairs per core per rep."""
+    n_pairs = 4 * host_cores()
     env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1")
-    r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, env=env, timeout=1800)
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--cpu-oracle", str(layers), str(reps),
+                        str(n_pairs)], capture_output=True, text=True, env=env, timeout=1800)
     if r.returncode != 0:
         raise RuntimeError(r.stderr[-2000:])
     return json.loads(r.stdout.strip().splitlines()[-1])
 
 
+def cpu_sample_text(res: dict, layers: int) -> str:
+    return (f"per step: oracle dedup of all 8 sequences (one core, {statistics.median(res['dedup_s']):.3f} s) + "
+            f"{res['n_pairs']} (agent, head) pairs of one mha7b layer through the fp64 oracle (dense materialise "
+            f"+ attention) on a spawn pool of {res['cores']} processes "
+            f"({statistics.median(res['pairs_wall_s']):.3f} s wall), the pairs' time scaled by "
+            f"{res['scale']:.0f} to a full step of 8 agents x 32 heads x {layers} layers")
+
+
 # ------------------------------------------------------------------ main ----
 def main():
     args = parse()
+    if args.cpu_oracle:
+        layers, reps, n_pairs = args.cpu_oracle
+        print(json.dumps(cpu_oracle_run(layers, reps, n_pairs)))
+        return 0
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
 
     if args.impl == "reference":
-        # the CPU oracle as it stands; rank 0 only
+        # the CPU oracle as it stands, on the host cores; rank 0 only
         if rank != 0:
             return 0
-        n_pairs = 2
-        per_rep = cpu_oracle_step_seconds(args.layers, reps=args.warmup + args.steps, n_pairs=n_pairs)
-        timed = per_rep[args.warmup:]
+        L = args.layers or 32
+        res = cpu_oracle(L, args.warmup + args.steps)
+        timed = res["steps"][args.warmup:]
         step_s = sum(timed) / len(timed)
         val = 8.0 / step_s
         line = {"impl": "reference", "metric": METRIC, "value": val, "unit": UNIT, "n_gpus": args.gpus,
                 "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_s * 1e3,
                 "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-                "data": "synthetic", "config": {"workload": WORKLOAD},
-                "cpu_baseline": {"kind": "oracle", "value": val, "unit": UNIT, "cores": 1,
-                                 "sample": cpu_sample_text(n_pairs) + " (per step)"},
-                "e2e": {"value": val, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+                "data": "synthetic", "config": {"workload": WORKLOAD, "agents": 8, "context": 16384, "layers": L},
+                "cpu_baseline": {"kind": "oracle", "value": val, "unit": UNIT, "cores": res["cores"],
+                                 "sample": cpu_sample_text(res, L)},
+                "e2e": {"value": val, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+                "ms_per_step_from": "extrapolated: the measured sample of each step (sample_ms_per_step) with its "
+                                    "attention pairs scaled by sample_scale to a full step",
+                "sample_ms_per_step": 1e3 * (sum(res["dedup_s"][args.warmup:]) +
+                                             sum(res["pairs_wall_s"][args.warmup:])) / args.steps,
+                "sample_scale": res["scale"]}
         print(json.dumps(line))
         return 0
 
@@ -247,7 +310,11 @@ def main():
     from shared_paged_kv_gb300 import workloads as W
 
     if args.workload != "mha7b":
-        return bench_workload(args, torch, K, W)
+        dev = torch.device("cuda", 0)
+        torch.cuda.set_device(dev)
+        rec = run_extra(args.workload, torch, K, W, dev, args.steps, args.warmup, args.layers)
+        print(json.dumps(rec))
+        return 0
 
     if world > 1:
         dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
@@ -256,7 +323,7 @@ def main():
     stream = torch.cuda.current_stream()
 
     # ---- workload, resident in HBM
-    L = args.layers
+    L = args.layers or 32
     w = W.make_mha7b(n_layers=L)
     B, D, H, N = w.block_tokens, w.head_dim, w.n_kv_heads, w.n_seq
     cap = 614 + N * 410                       # physical blocks the dedup produces
@@ -278,22 +345,19 @@ def main():
                        dtype=torch.uint8, device=dev)
     out = torch.zeros((L, N, w.n_q_heads, D), dtype=torch.float32, device=dev)
 
-    ev_a = [[torch.cuda.Event(enable_timing=True) for _ in range(L)] for _ in range(args.steps)]
-    ev_b = [[torch.cuda.Event(enable_timing=True) for _ in range(L)] for _ in range(args.steps)]
-
-    def step(i=None):
+    def step(ev=None):
         # block tables change per step: fingerprint + dedup, then one work
         # plan for all layers, then attention on every layer
         K.kvs_fingerprint_dedup(pool, tokens, seq_off, N, None, None, None, fp, table, w.max_blocks, refc,
                                 nphys, ws_d)
         K.kvs_decode_plan(pool, w.n_q_heads, table, w.max_blocks, seq_len, N, None, None, None, ws_a)
         for l in range(L):
-            if i is not None:
-                ev_a[i][l].record(stream)
+            if ev is not None:
+                ev[l][0].record(stream)
             K.kvs_decode_attn_planned(pool, l, q[l], w.n_q_heads, table, w.max_blocks, seq_len, N, None, None,
                                       None, w.theta, w.scale, out[l], ws_a)
-            if i is not None:
-                ev_b[i][l].record(stream)
+            if ev is not None:
+                ev[l][1].record(stream)
 
     for _ in range(args.warmup):
         step()
@@ -303,6 +367,7 @@ def main():
         raise RuntimeError(f"device status flags {flags:#x}")
     assert int(nphys.item()) == cap, (int(nphys.item()), cap)
 
+    # ---- timed region: K steps between two events, nothing else recorded
     launches0 = K.kvs_launch_count()
     if world > 1:
         dist.barrier()
@@ -311,8 +376,8 @@ def main():
     t1 = torch.cuda.Event(enable_timing=True)
     with ClockSampler(local_rank) as clk:
         t0.record(stream)
-        for i in range(args.steps):
-            step(i)
+        for _ in range(args.steps):
+            step()
         t1.record(stream)
         torch.cuda.synchronize()
     if world > 1:
@@ -320,7 +385,16 @@ def main():
     launches = K.kvs_launch_count() - launches0
     ms = max_over_ranks(t0.elapsed_time(t1), world, dev)
     ms_step = ms / args.steps
-    attn_ms = [ev_a[i][l].elapsed_time(ev_b[i][l]) for i in range(args.steps) for l in range(L)]
+    value = job_tokens_per_s(N, world, ms_step)
+
+    # ---- breakdown pass (outside the timed region): the same steps with an
+    # event pair around every layer's attention call
+    ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(L)]
+          for _ in range(args.steps)]
+    for i in range(args.steps):
+        step([e for e in ev[i]])
+    torch.cuda.synchronize()
+    attn_ms = [a.elapsed_time(b) for row in ev for a, b in row]
     attn_avg_ms = sum(attn_ms) / len(attn_ms)
 
     # ---- algorithmic bytes of one attention launch (unique bytes leaving HBM)
@@ -329,7 +403,6 @@ def main():
     peak, peak_kind = read_peaks()
     achieved = attn_bytes / (attn_avg_ms * 1e-3) / 1e9
     step_bytes = L * attn_bytes + w.tokens.nbytes + N * w.max_blocks * (8 + 4)
-    value = job_tokens_per_s(N, world, ms_step)
 
     # ---- end to end through the public API with pinned host buffers
     e2e = None
@@ -364,19 +437,12 @@ def main():
         e2e = {"value": job_tokens_per_s(N, world, e2e_s * 1e3), "unit": UNIT,
                "h2d_bytes_per_step": int(h_tok.numel() * 4 + h_off.numel() * 8 + h_q.numel() * 2),
                "d2h_bytes_per_step": int(h_out.numel() * 4)}
+        del h_tok, h_off, h_q, h_out, d_tok, d_off, d_q
+    flags |= K.kvs_pool_check(pool)
+    del k_slabs, v_slabs, pool, q, out, ws_a, ws_d
+    torch.cuda.empty_cache()
 
-    # ---- RoPE re-rotation on one layer of the all-gather round
-    rope = None
-    if not args.no_rope:
-        rope = bench_rope(torch, K, W, dev, stream, args, peak)
-
-    # ---- CPU oracle
-    cpu = None
-    if not args.no_cpu_baseline and rank == 0:
-        step_s = cpu_oracle_step_seconds(L)[0]
-        cpu = {"value": N / step_s, "unit": UNIT, "cores": 1, "kind": "oracle",
-               "sample": cpu_sample_text(len(CPU_PAIRS))}
-
+    line = None
     if rank == 0:
         line = {
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
@@ -389,51 +455,60 @@ def main():
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "traffic": profiled_traffic(source_hash(ATTN_SOURCES)),
                          "kernel": ATTN_KERNEL, "peak_kind": peak_kind,
-                         "bytes_per_launch": attn_bytes, "avg_launch_ms": attn_avg_ms},
-            "cpu_baseline": cpu,
+                         "bytes_per_launch": attn_bytes, "avg_launch_ms": attn_avg_ms,
+                         "avg_launch_from": "breakdown pass after the timed region: the same steps with events "
+                                            "around every layer's attention call"},
             "e2e": e2e,
             "gpu_launches": launches,
             "clocks": clk.summary(),
-            "rope_reuse": rope,
+            "status_flags": flags,
         }
+
+    # ---- RoPE re-rotation on one layer of the all-gather round
+    if not args.no_rope and line is not None:
+        line["rope_reuse"] = bench_rope(torch, K, W, dev, stream, args, peak)
+
+    # ---- every other workload, one key each (one GPU only)
+    if not args.no_extra and world == 1:
+        for name in EXTRA_CONFIGS:
+            try:
+                line[name] = run_extra(name, torch, K, W, dev, args.extra_steps, min(args.warmup, 3), None)
+            except Exception as ex:  # keep the headline line; record what failed
+                line[name] = {"error": f"{type(ex).__name__}: {ex}"[:500]}
+            torch.cuda.empty_cache()
+
+    # ---- CPU oracle (rank 0, after all GPU work)
+    if not args.no_cpu_baseline and rank == 0:
+        res = cpu_oracle(L, 3)
+        step_s = statistics.median(res["steps"])
+        line["cpu_baseline"] = {"value": N / step_s, "unit": UNIT, "cores": res["cores"], "kind": "oracle",
+                                "sample": cpu_sample_text(res, L)}
+
+    if rank == 0:
         print(json.dumps(line))
     if world > 1:
         dist.destroy_process_group()
     return 0
 
 
-def bench_select(args, torch, K, dev, stream):
-    """Critical-position selection of the all-gather round at one check layer:
-    64 agents x 8192 shared positions x 8 KV heads x 128 dims, top 15 %."""
-    n, rows, E = 64, 8192, 1024
-    gen = torch.Generator(device=dev).manual_seed(11)
-    kc = torch.randn((n * rows, E), generator=gen, device=dev)
-    sig = 0.05 + 0.45 * torch.rand((n * rows, 1), generator=gen, device=dev)
-    kn = (kc + torch.randn((n * rows, E), generator=gen, device=dev) * sig).to(torch.bfloat16).view(torch.int16)
-    kc = kc.to(torch.bfloat16).view(torch.int16)
-    off = torch.arange(n + 1, dtype=torch.int64, device=dev) * rows
-    ws = torch.zeros(4 * n * rows, dtype=torch.uint8, device=dev)
-    idx = torch.zeros(n * rows, dtype=torch.int32, device=dev)
-    idx_off = torch.zeros(n + 1, dtype=torch.int64, device=dev)
-
-    def run():
-        K.kvs_select_critical(kc, kn, off, n, rows, E, 0.15, idx, idx_off, ws)
-
-    for _ in range(args.warmup):
-        run()
-    torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(args.steps):
-        run()
-    e1.record(stream)
-    torch.cuda.synchronize()
-    ms = e0.elapsed_time(e1) / args.steps
-    byts = 2 * n * rows * E * 2
-    peak, _ = read_peaks()
-    print(json.dumps({"workload": "select", "ms_per_call": ms, "rows_per_s": n * rows / (ms * 1e-3),
-                      "gbs": byts / (ms * 1e-3) / 1e9, "frac_of_measured_peak": byts / (ms * 1e-3) / 1e9 / peak}))
-    return 0
+# --------------------------------------------------------- other workloads --
+# name -> (dominant kernels, committed ncu summary, workload description)
+CONFIG_INFO = {
+    "tiny": ("attn_tm_kernel<64,1,0> + tm_merge_kernel<64> (latency-bound)", None,
+             "tiny: 4 agents, 1 layer, 8 q / 2 kv heads, d 64, 256-token shared prefix + 64-128 private, "
+             "2 mirror-diff blocks per agent"),
+    "gqa_fanout": ("attn_wide_kernel<1,0> beside attn_tm_kernel<128,0,0>, then tm_merge_kernel<128>",
+                   "profiles/launches_gqa_step.md",
+                   "gqa_fanout: 32 sequences, 4096-token shared system prefix + 512-2048 private, 16 q / 2 kv heads, "
+                   "d 128, 28 layers"),
+    "allgather": ("attn_tm_kernel<128,1,1> beside attn_wide_kernel<2,1>, then tm_merge_kernel<128>",
+                  "profiles/launches_allgather_step.md",
+                  "allgather: 64 agents, private 1k-6k + 64 shared 128-token segments per agent with RoPE shifts "
+                  "(theta 1e6), 31 mirror-diff blocks per agent, 40 q / 8 kv heads, d 128, 48 layers"),
+    "q4": ("q4_attn_kernel", "profiles/q4_attn_q4.md",
+           "q4: 12 agents x 8192 tokens, 32 q / 8 kv heads, d 128, Q4G64 codes with fp16 scale+bias, "
+           "256-token blocks, 32 layers"),
+}
 
 
 def graph_replay_ms(torch, fn, reps, flush):
@@ -461,6 +536,57 @@ def graph_replay_ms(torch, fn, reps, flush):
         b.record(st)
     torch.cuda.synchronize()
     return sum(a.elapsed_time(b) for a, b in ev) / reps
+
+
+def run_extra(name, torch, K, W, dev, steps, warmup, layers):
+    stream = torch.cuda.current_stream()
+    if name == "select":
+        return bench_select(torch, K, dev, stream, steps, warmup)
+    if name == "mirror":
+        return bench_mirror(torch, K, W, dev, steps)
+    if name == "cow":
+        return bench_cow(torch, K, W, dev, stream, steps, warmup)
+    if name == "evict":
+        return bench_evict(torch, K, dev, steps)
+    if name == "io":
+        return bench_io(torch, K, W, dev, steps)
+    return workload_record(name, torch, K, W, dev, stream, steps, warmup, layers)
+
+
+def bench_select(torch, K, dev, stream, steps, warmup):
+    """Critical-position selection of the all-gather round at one check layer:
+    64 agents x 8192 shared positions x 8 KV heads x 128 dims, top 15 %."""
+    n, rows, E = 64, 8192, 1024
+    gen = torch.Generator(device=dev).manual_seed(11)
+    kc = torch.randn((n * rows, E), generator=gen, device=dev)
+    sig = 0.05 + 0.45 * torch.rand((n * rows, 1), generator=gen, device=dev)
+    kn = (kc + torch.randn((n * rows, E), generator=gen, device=dev) * sig).to(torch.bfloat16).view(torch.int16)
+    kc = kc.to(torch.bfloat16).view(torch.int16)
+    off = torch.arange(n + 1, dtype=torch.int64, device=dev) * rows
+    ws = torch.zeros(4 * n * rows, dtype=torch.uint8, device=dev)
+    idx = torch.zeros(n * rows, dtype=torch.int32, device=dev)
+    idx_off = torch.zeros(n + 1, dtype=torch.int64, device=dev)
+
+    def run():
+        K.kvs_select_critical(kc, kn, off, n, rows, E, 0.15, idx, idx_off, ws)
+
+    for _ in range(warmup):
+        run()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        run()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / steps
+    byts = 2 * n * rows * E * 2
+    peak, kind = read_peaks()
+    return {"workload": "select: 64 agents x 8192 positions x (8 kv heads x 128), top 15 % by ||K_cached - K_new||",
+            "kernel": "sel_scores + sel_topk", "profile": "profiles/sel_scores_select.md",
+            "ms_per_call": ms, "rows_per_s": n * rows / (ms * 1e-3), "bytes_per_call": byts,
+            "gbs": byts / (ms * 1e-3) / 1e9, "frac": byts / (ms * 1e-3) / 1e9 / peak, "peak": peak,
+            "peak_kind": kind, "l2": "inputs (2.1 GB) larger than L2", "timing": "eager, back to back"}
 
 
 def bench_tiny_replicated(torch, K, W, dev, reps, flush, n_inst=4096):
@@ -509,11 +635,145 @@ def bench_tiny_replicated(torch, K, W, dev, reps, flush, n_inst=4096):
     byts = (cap + ndr) * H * B * D * 2 * 2 + NS * w.n_q_heads * D * (2 + 4) + NS * w.max_blocks * 4 * 2
     peak, _ = read_peaks()
     return {"instances": n_inst, "sequences": NS, "ms_plan_plus_attn": ms, "tokens_per_s": NS / (ms * 1e-3),
-            "bytes": byts, "gbs": byts / (ms * 1e-3) / 1e9, "frac_of_measured_peak": byts / (ms * 1e-3) / 1e9 / peak,
-            "status_flags": flags}
+            "bytes": byts, "gbs": byts / (ms * 1e-3) / 1e9, "frac": byts / (ms * 1e-3) / 1e9 / peak,
+            "timing": "CUDA graph of plan + attention, L2 flushed before every replay", "status_flags": flags}
 
 
-def bench_mirror(args, torch, K, W, dev, stream):
+def workload_record(name, torch, K, W, dev, stream, steps, warmup, layers):
+    """GPU dedup + plan + decode attention on every layer (Q4: attention only),
+    eager through the public API and replayed from CUDA graphs."""
+    mk = {"tiny": W.make_tiny, "gqa_fanout": W.make_gqa_fanout, "allgather": W.make_allgather, "q4": W.make_q4}
+    w = mk[name]()
+    L = layers or w.n_layers
+    N, H, D, B = w.n_seq, w.n_kv_heads, w.head_dim, w.block_tokens
+    q4 = name == "q4"
+    tokens = torch.from_numpy(w.tokens.view(np.int32)).to(dev)
+    seq_off = torch.from_numpy(w.seq_off).to(dev)
+    seq_len = torch.from_numpy(w.seq_len).to(dev)
+    tier = torch.from_numpy(w.tier.view(np.int32)).to(dev) if (w.tier != 0).any() else None
+    so = sb = None
+    if w.seg_start_off is not None:
+        so = torch.from_numpy(w.seg_start_off).to(dev)
+        sb = torch.from_numpy(w.seg_start_blocks).to(dev)
+    fp = torch.zeros((N, w.max_blocks), dtype=torch.int64, device=dev)
+    table = torch.zeros((N, w.max_blocks), dtype=torch.int32, device=dev)
+    # dedup once on a pool whose capacity is the upper bound, to size the slabs
+    dummy = torch.zeros(16, dtype=torch.int16, device=dev)
+    if q4:
+        d8 = torch.zeros(16, dtype=torch.uint8, device=dev)
+        dh = torch.zeros(16, dtype=torch.float16, device=dev)
+        probe = K.kvs_pool_create(1, H, D, B, K.KVS_DTYPE_Q4G64, w.capacity_blocks, N, [d8], [d8], [dh], [dh])
+    else:
+        probe = K.kvs_pool_create(1, H, D, B, K.KVS_DTYPE_BF16, w.capacity_blocks, N, [dummy], [dummy])
+    refc = torch.zeros(w.capacity_blocks, dtype=torch.int32, device=dev)
+    nphys = torch.zeros(1, dtype=torch.int32, device=dev)
+    ws_d = torch.zeros(K.kvs_workspace_size(probe, K.KVS_OP_DEDUP, N, w.max_blocks), dtype=torch.uint8, device=dev)
+    K.kvs_fingerprint_dedup(probe, tokens, seq_off, N, tier, so, sb, fp, table, w.max_blocks, refc, nphys, ws_d)
+    cap = int(nphys.item())
+    gen = torch.Generator(device=dev).manual_seed(7)
+    nd = 0
+    if q4:
+        ks = [torch.empty(cap * H * B * D // 2, dtype=torch.uint8, device=dev) for _ in range(L)]
+        vs = [torch.empty_like(ks[0]) for _ in range(L)]
+        ksb = [torch.empty(cap * H * B * 4, dtype=torch.float16, device=dev) for _ in range(L)]
+        vsb = [torch.empty_like(ksb[0]) for _ in range(L)]
+        pool = K.kvs_pool_create(L, H, D, B, K.KVS_DTYPE_Q4G64, cap, N, ks, vs, ksb, vsb)
+        ids = torch.arange(cap, dtype=torch.int32, device=dev)
+        for l in range(L):
+            src_k = torch.randn((cap, H, B, D), generator=gen, device=dev, dtype=torch.bfloat16)
+            src_v = torch.randn((cap, H, B, D), generator=gen, device=dev, dtype=torch.bfloat16)
+            K.kvs_quantize_q4(pool, l, src_k.view(torch.int16), src_v.view(torch.int16), ids, cap)
+            del src_k, src_v
+        per_launch = cap * H * B * 144
+    else:
+        ks = [torch.randn((cap, H, B, D), generator=gen, device=dev, dtype=torch.bfloat16).view(torch.int16)
+              for _ in range(L)]
+        vs = [torch.randn((cap, H, B, D), generator=gen, device=dev, dtype=torch.bfloat16).view(torch.int16)
+              for _ in range(L)]
+        nd = w.diff_capacity_blocks
+        dks = [(0.1 * torch.randn((nd, H, B, D), generator=gen, device=dev)).to(torch.bfloat16).view(torch.int16)
+               for _ in range(L)] if nd else None
+        dvs = [(0.1 * torch.randn((nd, H, B, D), generator=gen, device=dev)).to(torch.bfloat16).view(torch.int16)
+               for _ in range(L)] if nd else None
+        pool = K.kvs_pool_create(L, H, D, B, K.KVS_DTYPE_BF16, cap, N, ks, vs, dk_layers=dks, dv_layers=dvs,
+                                 diff_capacity_blocks=nd)
+        per_launch = (cap + nd) * H * B * D * 2 * 2
+    per_launch += N * w.n_q_heads * D * (2 + 4) + N * w.max_blocks * 4 * (2 if w.diff_table is not None else 1)
+    refc = torch.zeros(cap, dtype=torch.int32, device=dev)
+    q = torch.randn((L, N, w.n_q_heads, D), generator=gen, device=dev, dtype=torch.bfloat16)
+    out = torch.zeros((L, N, w.n_q_heads, D), dtype=torch.float32, device=dev)
+    dt = torch.from_numpy(w.diff_table).to(dev) if w.diff_table is not None else None
+    ro = torch.from_numpy(w.rope_off).to(dev) if w.rope_off is not None else None
+    rs = torch.from_numpy(w.rope_segs).to(dev) if w.rope_segs is not None else None
+    op = K.KVS_OP_DECODE_ATTN_Q4 if q4 else K.KVS_OP_DECODE_ATTN
+    ws_a = torch.zeros(K.kvs_workspace_size(pool, op, N, w.max_blocks, w.n_q_heads), dtype=torch.uint8, device=dev)
+
+    def attn(l):
+        if q4:
+            K.kvs_decode_attn_q4(pool, l, q[l], w.n_q_heads, table, w.max_blocks, seq_len, N, w.scale, out[l], ws_a)
+        else:
+            K.kvs_decode_attn_planned(pool, l, q[l], w.n_q_heads, table, w.max_blocks, seq_len, N, dt, ro, rs,
+                                      w.theta, w.scale, out[l], ws_a)
+
+    def step(ev=None):
+        if not q4:
+            K.kvs_fingerprint_dedup(pool, tokens, seq_off, N, tier, so, sb, fp, table, w.max_blocks, refc, nphys, ws_d)
+            K.kvs_decode_plan(pool, w.n_q_heads, table, w.max_blocks, seq_len, N, dt, ro, rs, ws_a)
+        for l in range(L):
+            if ev is not None:
+                ev[l][0].record(stream)
+            attn(l)
+            if ev is not None:
+                ev[l][1].record(stream)
+
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+    flags = K.kvs_pool_check(pool)
+    # eager, whole steps between two events
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for _ in range(steps):
+        step()
+    t1.record(stream)
+    torch.cuda.synchronize()
+    ms_step = t0.elapsed_time(t1) / steps
+    # eager breakdown: events around every layer's attention call
+    ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(L)]
+          for _ in range(steps)]
+    for i in range(steps):
+        step(ev[i])
+    torch.cuda.synchronize()
+    attn_ms = sum(a.elapsed_time(b) for row in ev for a, b in row) / (steps * L)
+    peak, kind = read_peaks()
+    # the same work replayed from CUDA graphs (host launch cost removed): the
+    # whole step, and the attention launches alone
+    flush = torch.zeros(64 << 20, dtype=torch.float32, device=dev)
+    g_step = graph_replay_ms(torch, step, steps, flush)
+    g_attn = graph_replay_ms(torch, lambda: [attn(l) for l in range(L)], steps, flush) / L
+    kern, prof, desc = CONFIG_INFO[name]
+
+    def gbs(ms):
+        return per_launch / (ms * 1e-3) / 1e9
+
+    rec = {"workload": desc, "kernel": kern, "profile": prof, "layers": L, "n_phys": cap, "diff_blocks": nd,
+           "attn_bytes_per_launch": per_launch, "peak": peak, "peak_kind": kind,
+           "eager": {"tokens_per_s": N / (ms_step * 1e-3), "ms_per_step": ms_step, "attn_ms_per_layer": attn_ms,
+                     "attn_gbs": gbs(attn_ms), "frac": gbs(attn_ms) / peak,
+                     "timing": "public API calls from Python; step = dedup + plan + every layer" +
+                               (" (Q4: attention only)" if q4 else "") +
+                               "; per-layer time from a second pass with events around each call"},
+           "graph": {"tokens_per_s": N / (g_step * 1e-3), "ms_per_step": g_step, "attn_ms_per_layer": g_attn,
+                     "attn_gbs": gbs(g_attn), "frac": gbs(g_attn) / peak,
+                     "timing": "CUDA graph replays, L2 flushed before every replay"},
+           "status_flags": flags | K.kvs_pool_check(pool)}
+    if name == "tiny":
+        rec["eager"]["l2"] = "the 0.43 MB working set stays in L2 between eager steps"
+        rec["tiny_x4096"] = bench_tiny_replicated(torch, K, W, dev, steps, flush)
+    return rec
+
+
+def bench_mirror(torch, K, W, dev, steps):
     """Mirror construction of the all-gather round at one layer: 64 agents,
     each refreshing every row of 31 blocks among its 512 shared-segment
     blocks (the round's mirror structure), K rotated back by the segment
@@ -565,19 +825,19 @@ def bench_mirror(args, torch, K, W, dev, stream):
                            diff_table, n_diff, ws)
 
     flush = torch.zeros(64 << 20, dtype=torch.float32, device=dev)
-    ms = graph_replay_ms(torch, run, args.steps, flush)
+    ms = graph_replay_ms(torch, run, steps, flush)
     flags = K.kvs_pool_check(pool)
     tile = 16 * D * 2
     byts = (cap_d * H * tile * 2) * 3 + n_rows * 4 + N * w.max_blocks * 4 * 2
     peak, _ = read_peaks()
-    print(json.dumps({"workload": "mirror", "ms_per_call": ms, "dirty_blocks": cap_d, "rows": n_rows,
-                      "bytes": byts, "gbs": byts / (ms * 1e-3) / 1e9,
-                      "frac_of_measured_peak": byts / (ms * 1e-3) / 1e9 / peak,
-                      "l2": "flushed before every replay", "status_flags": flags}))
-    return 0
+    return {"workload": "mirror: all-gather round, 64 agents x 31 refreshed blocks among 512 shared-segment blocks, "
+                        "8 kv heads x 128, K rotated back by the segment shift",
+            "kernel": "mir_write + 3 index kernels", "ms_per_call": ms, "dirty_blocks": cap_d, "rows": n_rows,
+            "bytes": byts, "gbs": byts / (ms * 1e-3) / 1e9, "frac": byts / (ms * 1e-3) / 1e9 / peak,
+            "timing": "CUDA graph replays, L2 flushed before every replay", "status_flags": flags}
 
 
-def bench_cow(args, torch, K, W, dev, stream):
+def bench_cow(torch, K, W, dev, stream, steps, warmup):
     """Copy-on-write burst on the 7B multi-head tables (32 layers x 32 KV
     heads): agent 0 writes into all 614 shared blocks, so each is copied (K
     and V of every layer, 8 MiB per block); then all 8 sequences are
@@ -612,7 +872,7 @@ def bench_cow(args, torch, K, W, dev, stream):
         table.copy_(table0); ref.copy_(ref0); free.copy_(free0); nfree.copy_(nfree0); sl.copy_(sl0)
 
     times_w, times_r = [], []
-    for it in range(args.warmup + args.steps):
+    for it in range(warmup + steps):
         restore()
         torch.cuda.synchronize()
         e0, e1, e2 = (torch.cuda.Event(enable_timing=True) for _ in range(3))
@@ -622,7 +882,7 @@ def bench_cow(args, torch, K, W, dev, stream):
         K.kvs_seq_release(pool, table, w.max_blocks, sl, N, rel, N, ref, free, nfree, ws)
         e2.record(stream)
         torch.cuda.synchronize()
-        if it >= args.warmup:
+        if it >= warmup:
             times_w.append(e0.elapsed_time(e1))
             times_r.append(e1.elapsed_time(e2))
     flags = K.kvs_pool_check(pool)
@@ -631,15 +891,14 @@ def bench_cow(args, torch, K, W, dev, stream):
     ms_r = sum(times_r) / len(times_r)
     byts = 614 * L * 2 * (H * 16 * D * 2) * 2   # every copied byte read once and written once
     peak, _ = read_peaks()
-    print(json.dumps({"workload": "cow", "copies": 614, "bytes_per_copy": L * 2 * H * 16 * D * 2,
+    return ({"workload": "cow", "copies": 614, "bytes_per_copy": L * 2 * H * 16 * D * 2,
                       "write_batch_ms": ms_w, "gbs": byts / (ms_w * 1e-3) / 1e9,
                       "frac_of_measured_peak": byts / (ms_w * 1e-3) / 1e9 / peak,
                       "release_ms": ms_r, "released_blocks": cap - 614, "all_blocks_free_after": ok,
-                      "status_flags": flags}))
-    return 0
+                      "status_flags": flags})
 
 
-def bench_evict(args, torch, K, W, dev, stream):
+def bench_evict(torch, K, dev, steps):
     """Block-granular eviction scoring: 64 agents x 16,384 tokens (1,024
     blocks each), five regions with the MemDecay post's suggested initial
     scores, each agent evicting a quarter of its blocks."""
@@ -669,16 +928,15 @@ def bench_evict(args, torch, K, W, dev, stream):
         K.kvs_evict_score(pool, reg_t, cr_t, ac_t, sl, n, mb, init, decay, T + 10, k, scores, victims, voff)
 
     flush = torch.zeros(64 << 20, dtype=torch.float32, device=dev)
-    ms = graph_replay_ms(torch, run, args.steps, flush)
+    ms = graph_replay_ms(torch, run, steps, flush)
     byts = n * T * 9 + n * mb * 4 + n * mb // 4 * 4
-    print(json.dumps({"workload": "evict", "ms_per_call": ms, "blocks_scored": n * mb, "victims": n * mb // 4,
+    return ({"workload": "evict", "ms_per_call": ms, "blocks_scored": n * mb, "victims": n * mb // 4,
                       "blocks_per_s": n * mb / (ms * 1e-3), "bytes": byts, "gbs": byts / (ms * 1e-3) / 1e9,
                       "note": "9.4 MB per call: latency-bound", "l2": "flushed before every replay",
-                      "status_flags": K.kvs_pool_check(pool)}))
-    return 0
+                      "status_flags": K.kvs_pool_check(pool)})
 
 
-def bench_io(args, torch, K, W, dev, stream):
+def bench_io(torch, K, W, dev, steps):
     """Export and import of the Q4 configuration's whole pool: 12 agents x 32
     blocks of 256 tokens, 32 layers x 8 KV heads (codes and scale/bias), the
     device side of saving and reloading a persistent Q4 cache."""
@@ -699,153 +957,14 @@ def bench_io(args, torch, K, W, dev, stream):
     src = torch.arange(cap, dtype=torch.int32, device=dev)
     dst = src + cap
     flush = torch.zeros(64 << 20, dtype=torch.float32, device=dev)
-    ms_e = graph_replay_ms(torch, lambda: K.kvs_pool_export(pool, src, cap, packed), args.steps, flush)
-    ms_i = graph_replay_ms(torch, lambda: K.kvs_pool_import(pool, dst, cap, packed), args.steps, flush)
+    ms_e = graph_replay_ms(torch, lambda: K.kvs_pool_export(pool, src, cap, packed), steps, flush)
+    ms_i = graph_replay_ms(torch, lambda: K.kvs_pool_import(pool, dst, cap, packed), steps, flush)
     byts = 2 * cap * rec
     peak, _ = read_peaks()
-    print(json.dumps({"workload": "io", "blocks": cap, "record_bytes": rec, "export_ms": ms_e, "import_ms": ms_i,
+    return ({"workload": "io", "blocks": cap, "record_bytes": rec, "export_ms": ms_e, "import_ms": ms_i,
                       "export_gbs": byts / (ms_e * 1e-3) / 1e9, "import_gbs": byts / (ms_i * 1e-3) / 1e9,
                       "frac_of_measured_peak": [byts / (ms_e * 1e-3) / 1e9 / peak, byts / (ms_i * 1e-3) / 1e9 / peak],
-                      "status_flags": K.kvs_pool_check(pool)}))
-    return 0
-
-
-def bench_workload(args, torch, K, W):
-    """One-GPU record for a non-headline workload: GPU dedup + decode attention
-    on every layer (Q4: attention only), timed with CUDA events."""
-    dev = torch.device("cuda", 0)
-    torch.cuda.set_device(dev)
-    stream = torch.cuda.current_stream()
-    if args.workload == "select":
-        return bench_select(args, torch, K, dev, stream)
-    if args.workload == "mirror":
-        return bench_mirror(args, torch, K, W, dev, stream)
-    if args.workload == "cow":
-        return bench_cow(args, torch, K, W, dev, stream)
-    if args.workload == "evict":
-        return bench_evict(args, torch, K, W, dev, stream)
-    if args.workload == "io":
-        return bench_io(args, torch, K, W, dev, stream)
-    mk = {"tiny": W.make_tiny, "gqa_fanout": W.make_gqa_fanout, "allgather": W.make_allgather, "q4": W.make_q4}
-    w = mk[args.workload]()
-    L = min(w.n_layers, args.layers)
-    N, H, D, B = w.n_seq, w.n_kv_heads, w.head_dim, w.block_tokens
-    q4 = args.workload == "q4"
-    tokens = torch.from_numpy(w.tokens.view(np.int32)).to(dev)
-    seq_off = torch.from_numpy(w.seq_off).to(dev)
-    seq_len = torch.from_numpy(w.seq_len).to(dev)
-    tier = torch.from_numpy(w.tier.view(np.int32)).to(dev) if (w.tier != 0).any() else None
-    so = sb = None
-    if w.seg_start_off is not None:
-        so = torch.from_numpy(w.seg_start_off).to(dev)
-        sb = torch.from_numpy(w.seg_start_blocks).to(dev)
-    fp = torch.zeros((N, w.max_blocks), dtype=torch.int64, device=dev)
-    table = torch.zeros((N, w.max_blocks), dtype=torch.int32, device=dev)
-    # dedup once on a pool whose capacity is the upper bound, to size the slabs
-    dummy = torch.zeros(16, dtype=torch.int16, device=dev)
-    if q4:
-        d8 = torch.zeros(16, dtype=torch.uint8, device=dev)
-        dh = torch.zeros(16, dtype=torch.float16, device=dev)
-        probe = K.kvs_pool_create(1, H, D, B, K.KVS_DTYPE_Q4G64, w.capacity_blocks, N, [d8], [d8], [dh], [dh])
-    else:
-        probe = K.kvs_pool_create(1, H, D, B, K.KVS_DTYPE_BF16, w.capacity_blocks, N, [dummy], [dummy])
-    refc = torch.zeros(w.capacity_blocks, dtype=torch.int32, device=dev)
-    nphys = torch.zeros(1, dtype=torch.int32, device=dev)
-    ws_d = torch.zeros(K.kvs_workspace_size(probe, K.KVS_OP_DEDUP, N, w.max_blocks), dtype=torch.uint8, device=dev)
-    K.kvs_fingerprint_dedup(probe, tokens, seq_off, N, tier, so, sb, fp, table, w.max_blocks, refc, nphys, ws_d)
-    cap = int(nphys.item())
-    gen = torch.Generator(device=dev).manual_seed(7)
-    if q4:
-        ks = [torch.empty(cap * H * B * D // 2, dtype=torch.uint8, device=dev) for _ in range(L)]
-        vs = [torch.empty_like(ks[0]) for _ in range(L)]
-        ksb = [torch.empty(cap * H * B * 4, dtype=torch.float16, device=dev) for _ in range(L)]
-        vsb = [torch.empty_like(ksb[0]) for _ in range(L)]
-        pool = K.kvs_pool_create(L, H, D, B, K.KVS_DTYPE_Q4G64, cap, N, ks, vs, ksb, vsb)
-        ids = torch.arange(cap, dtype=torch.int32, device=dev)
-        for l in range(L):
-            src_k = torch.randn((cap, H, B, D), generator=gen, device=dev, dtype=torch.bfloat16)
-            src_v = torch.randn((cap, H, B, D), generator=gen, device=dev, dtype=torch.bfloat16)
-            K.kvs_quantize_q4(pool, l, src_k.view(torch.int16), src_v.view(torch.int16), ids, cap)
-            del src_k, src_v
-        per_launch = cap * H * B * 144
-    else:
-        ks = [torch.randn((cap, H, B, D), generator=gen, device=dev, dtype=torch.bfloat16).view(torch.int16) for _ in range(L)]
-        vs = [torch.randn((cap, H, B, D), generator=gen, device=dev, dtype=torch.bfloat16).view(torch.int16) for _ in range(L)]
-        nd = w.diff_capacity_blocks
-        dks = [(0.1 * torch.randn((nd, H, B, D), generator=gen, device=dev)).to(torch.bfloat16).view(torch.int16)
-               for _ in range(L)] if nd else None
-        dvs = [(0.1 * torch.randn((nd, H, B, D), generator=gen, device=dev)).to(torch.bfloat16).view(torch.int16)
-               for _ in range(L)] if nd else None
-        pool = K.kvs_pool_create(L, H, D, B, K.KVS_DTYPE_BF16, cap, N, ks, vs, dk_layers=dks, dv_layers=dvs,
-                                 diff_capacity_blocks=nd)
-        per_launch = (cap + nd) * H * B * D * 2 * 2
-    per_launch += N * w.n_q_heads * D * (2 + 4) + N * w.max_blocks * 4 * (2 if w.diff_table is not None else 1)
-    refc = torch.zeros(cap, dtype=torch.int32, device=dev)
-    q = torch.randn((L, N, w.n_q_heads, D), generator=gen, device=dev, dtype=torch.bfloat16)
-    out = torch.zeros((L, N, w.n_q_heads, D), dtype=torch.float32, device=dev)
-    dt = torch.from_numpy(w.diff_table).to(dev) if w.diff_table is not None else None
-    ro = torch.from_numpy(w.rope_off).to(dev) if w.rope_off is not None else None
-    rs = torch.from_numpy(w.rope_segs).to(dev) if w.rope_segs is not None else None
-    op = K.KVS_OP_DECODE_ATTN_Q4 if q4 else K.KVS_OP_DECODE_ATTN
-    ws_a = torch.zeros(K.kvs_workspace_size(pool, op, N, w.max_blocks, w.n_q_heads), dtype=torch.uint8, device=dev)
-    ev_a = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps * L)]
-    ev_b = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps * L)]
-
-    def step(i=None):
-        if not q4:
-            K.kvs_fingerprint_dedup(pool, tokens, seq_off, N, tier, so, sb, fp, table, w.max_blocks, refc, nphys, ws_d)
-            K.kvs_decode_plan(pool, w.n_q_heads, table, w.max_blocks, seq_len, N, dt, ro, rs, ws_a)
-        for l in range(L):
-            if i is not None:
-                ev_a[i * L + l].record(stream)
-            if q4:
-                K.kvs_decode_attn_q4(pool, l, q[l], w.n_q_heads, table, w.max_blocks, seq_len, N, w.scale, out[l], ws_a)
-            else:
-                K.kvs_decode_attn_planned(pool, l, q[l], w.n_q_heads, table, w.max_blocks, seq_len, N, dt, ro, rs,
-                                          w.theta, w.scale, out[l], ws_a)
-            if i is not None:
-                ev_b[i * L + l].record(stream)
-
-    for _ in range(args.warmup):
-        step()
-    torch.cuda.synchronize()
-    flags = K.kvs_pool_check(pool)
-    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    t0.record(stream)
-    for i in range(args.steps):
-        step(i)
-    t1.record(stream)
-    torch.cuda.synchronize()
-    ms_step = t0.elapsed_time(t1) / args.steps
-    attn_ms = sum(a.elapsed_time(b) for a, b in zip(ev_a, ev_b)) / len(ev_a)
-    peak, kind = read_peaks()
-    # the same work replayed from CUDA graphs, so host launch cost is not
-    # counted: the whole step, and the attention launches alone
-    flush = torch.zeros(64 << 20, dtype=torch.float32, device=dev)
-    g_step = graph_replay_ms(torch, step, args.steps, flush)
-
-    def attn_only():
-        for l in range(L):
-            if q4:
-                K.kvs_decode_attn_q4(pool, l, q[l], w.n_q_heads, table, w.max_blocks, seq_len, N, w.scale, out[l], ws_a)
-            else:
-                K.kvs_decode_attn_planned(pool, l, q[l], w.n_q_heads, table, w.max_blocks, seq_len, N, dt, ro, rs,
-                                          w.theta, w.scale, out[l], ws_a)
-
-    g_attn = graph_replay_ms(torch, attn_only, args.steps, flush) / L
-    rec = {"workload": args.workload, "tokens_per_s": N / (ms_step * 1e-3), "ms_per_step": ms_step,
-           "layers": L, "attn_avg_ms": attn_ms, "attn_bytes_per_launch": per_launch,
-           "attn_gbs": per_launch / (attn_ms * 1e-3) / 1e9,
-           "attn_frac_of_measured_peak": per_launch / (attn_ms * 1e-3) / 1e9 / peak,
-           "graph": {"ms_per_step": g_step, "tokens_per_s": N / (g_step * 1e-3), "attn_ms_per_layer": g_attn,
-                     "attn_gbs": per_launch / (g_attn * 1e-3) / 1e9,
-                     "attn_frac_of_measured_peak": per_launch / (g_attn * 1e-3) / 1e9 / peak,
-                     "l2": "flushed before every replay"},
-           "n_phys": cap, "status_flags": flags | K.kvs_pool_check(pool)}
-    if args.workload == "tiny":
-        rec["replicated"] = bench_tiny_replicated(torch, K, W, dev, args.steps, flush)
-    print(json.dumps(rec))
-    return 0
+                      "status_flags": K.kvs_pool_check(pool)})
 
 
 def bench_rope(torch, K, W, dev, stream, args, peak):
@@ -891,12 +1010,12 @@ def bench_rope(torch, K, W, dev, stream, args, peak):
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
-    for _ in range(args.steps):
+    for _ in range(min(args.steps, 20)):
         run()
     e1.record(stream)
     torch.cuda.synchronize()
     flags = K.kvs_pool_check(pool)
-    t = e0.elapsed_time(e1) / args.steps * 1e-3
+    t = e0.elapsed_time(e1) / min(args.steps, 20) * 1e-3
     row_bytes = w.n_kv_heads * w.head_dim * 2
     algo = n_master * w.n_kv_heads * B * w.head_dim * 2 + n_rows * row_bytes + jobs.nbytes
     del k, pool

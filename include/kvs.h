@@ -125,6 +125,19 @@ kvs_status kvs_pool_destroy(kvs_pool* pool);
  * refcount_dev  int32 [pool capacity]: references per physical block
  *               (entries >= n_phys are zeroed).
  * n_phys_dev    int32 [1]: physical blocks used.
+ * owner_seq_dev int32 [pool capacity] or NULL: the sequence of each physical
+ *               block's first occurrence (the sequence that owns it, [INMS]
+ *               §2.2); -1 for ids >= n_phys.
+ * ref_off_dev / ref_seq_dev   int64 [capacity + 1] / int32 [n_seq *
+ *               max_blocks], both NULL or both set: the references of every
+ *               physical block as a CSR (the shared-reference lists that
+ *               [INMS] §3.3 hooks walk and that the shared attention tiles
+ *               group by): ref_off is the exclusive prefix sum of refcount
+ *               (ref_off[capacity] = total references) and ref_seq[ref_off[id]
+ *               .. ref_off[id + 1]) lists the sequence of every slot mapped to
+ *               id, in ascending (sequence, block) order; a block is shared
+ *               when it has more than one entry.  Costs one extra single-CTA
+ *               kernel.
  * Rule: full blocks of equal tier (not PRIVATE), at the same index inside
  * their segment, with identical token runs from the segment start through the
  * block, share one physical block; tail and PRIVATE blocks get fresh ones; ids
@@ -143,6 +156,7 @@ kvs_status kvs_fingerprint_dedup(kvs_pool* pool,
                                  const int64_t* seg_off_dev, const int32_t* seg_blocks_dev,
                                  uint64_t* fp_out_dev, int32_t* block_table_dev,
                                  int32_t max_blocks, int32_t* refcount_dev, int32_t* n_phys_dev,
+                                 int32_t* owner_seq_dev, int64_t* ref_off_dev, int32_t* ref_seq_dev,
                                  uint32_t flags, void* ws, size_t ws_bytes, cudaStream_t stream);
 
 /* ---------------------------------------------------------------------------
@@ -176,7 +190,14 @@ kvs_status kvs_rope_rerotate(kvs_pool* pool, int32_t layer, const kvs_rope_job* 
  * their positions, relative to the agent's first row, ascending, to
  * idx_out_dev[idx_off[a] ...]; idx_off_dev (int64 [n_agents+1]) is the
  * exclusive prefix sum of k_a.  row_elems must be a multiple of 8.
- * max_rows_per_agent bounds n_a (<= 65536).  ws: kvs_workspace_size(SELECT). */
+ * max_rows_per_agent bounds n_a (<= 65536).  ws: kvs_workspace_size(SELECT).
+ * row_off must be non-decreasing with every value in [0, n_agents *
+ * max_rows_per_agent]; k_cached/k_new hold rows [row_off[0],
+ * row_off[n_agents]).  Because row_off is device memory this is not checked
+ * before launch: an agent whose range ends before it starts, or leaves
+ * [max(row_off[0], 0), min(row_off[n_agents], n_agents * max_rows_per_agent)),
+ * is treated as empty (k_a = 0, nothing written for it), and rows past
+ * n_agents * max_rows_per_agent are ignored. */
 kvs_status kvs_select_critical(const void* k_cached_dev, const void* k_new_dev,
                                const int64_t* row_off_dev, int32_t n_agents,
                                int32_t max_rows_per_agent, int32_t row_elems, float ratio,
@@ -196,11 +217,14 @@ kvs_status kvs_select_critical(const void* k_cached_dev, const void* k_new_dev,
  * KVS_ERR_CAPACITY is returned before anything is enqueued.  The caller still
  * passes all inputs and outputs (same meaning as kvs_select_critical).
  * Allocates nothing: no cudaMalloc, cudaFree or allocating library call.
- * The first call made with a given device current looks up the array's
- * device address (cudaGetSymbolAddress, which can load the library's device
- * code); make that first call before any stream capture.
+ * Every call looks up the array's device address in the current context
+ * (cudaGetSymbolAddress: no allocation, and correct after a device reset).
+ * The first call made with a given device current can load the library's
+ * device code as part of that lookup; make that first call before any stream
+ * capture.
  * All calls on a device share the one array and it keeps the previous call's
- * contents; every value a call reads is written earlier in the same call.
+ * contents; every value a call reads is written earlier in the same call
+ * (row_off rules as for kvs_select_critical).
  * Calls whose work can overlap on the GPU (different streams, or threads
  * without ordering) race on the array and give undefined results. */
 kvs_status kvs_select_critical_noalloc(const void* k_cached_dev, const void* k_new_dev,

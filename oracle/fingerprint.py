@@ -108,6 +108,29 @@ def dedup(tokens, seq_off, tier, block_tokens: int, max_blocks: int,
                 n_phys=len(refcount), owner=np.array(owner, dtype=np.int32))
 
 
+def references(block_table, n_phys: int):
+    """The references of every physical block as a CSR.
+
+    INMS walkthrough §2.2: a physical block's reference count is the number of
+    sequence blocks that point at it, and the block is shared while that
+    count exceeds one; §3.3: the engine's hooks walk these references.
+    Returns (off [n_phys + 1] int64, seq [total] int32): seq[off[p]:off[p+1]]
+    are the sequences s of the slots (s, b) whose table entry is p, in
+    ascending (s, b) order (a sequence appears once per slot)."""
+    table = np.asarray(block_table)
+    lists = [[] for _ in range(n_phys)]
+    for s in range(table.shape[0]):
+        for b in range(table.shape[1]):
+            p = int(table[s, b])
+            if p >= 0:
+                lists[p].append(s)
+    off, seq = [0], []
+    for p in range(n_phys):
+        seq.extend(lists[p])
+        off.append(len(seq))
+    return np.array(off, dtype=np.int64), np.array(seq, dtype=np.int32)
+
+
 def find_match_length(input_ids, checkpoint_len: int, pool_hashes, tag: int = 0) -> int:
     """Longest matched prefix (in tokens) against a set of stored block
     hashes, scanning checkpoints from 0 and stopping at the first miss —

@@ -29,6 +29,7 @@
 //     the counts turned into prefix sums by one CTA, then numbered in slot
 //     order (deterministic).
 //  6. table: block_table and refcounts.
+//  7. (optional) owner of each id, and the references of each id as a CSR.
 #include <climits>
 
 #include "common.cuh"
@@ -51,6 +52,9 @@ struct DedupParams {
   int32_t* block_table;
   int32_t* refcount;
   int32_t* n_phys;
+  int32_t* owner;     // optional [capacity]: sequence of each id's first occurrence
+  int64_t* ref_off;   // optional [capacity + 1]: CSR offsets of the references per id
+  int32_t* ref_seq;   // optional [n_seq * max_blocks]: referencing sequence per reference
   uint32_t* status;
   // workspace
   unsigned long long* tkeys;
@@ -61,6 +65,7 @@ struct DedupParams {
   int32_t* pid;       // per slot physical id of first occurrences
   uint32_t* flags;    // [0] collision
   int32_t* tile_cnt;  // first occurrences per numbering tile
+  int32_t* ref_cnt;   // [kRefChunks][capacity] per-chunk reference counts, then starts
   int n_seq, max_blocks, B, capacity, weak;
   uint32_t tmask;
 };
@@ -353,7 +358,11 @@ __global__ void __launch_bounds__(kNumTile) dedup_number(DedupParams p) {
   const int f = (slot < n && p.rep[slot] == slot) ? 1 : 0;
   int total;
   const int pos = block_exclusive_scan(f, warp_sums, total);
-  if (f) p.pid[slot] = p.tile_cnt[blockIdx.x] + pos;
+  if (f) {
+    const int id = p.tile_cnt[blockIdx.x] + pos;
+    p.pid[slot] = id;
+    if (p.owner && id < p.capacity) p.owner[id] = slot / p.max_blocks;
+  }
 }
 
 // 6. block table + refcounts
@@ -371,6 +380,68 @@ __global__ void dedup_table(DedupParams p) {
   if (id < p.capacity) atomicAdd(p.refcount + id, 1);
 }
 
+// 7. (optional) the references of every physical block: ref_off = exclusive
+// prefix sum of the refcounts, and ref_seq[ref_off[id] ..] the sequences of
+// the slots that map to id, in ascending slot (sequence, block) order.  One
+// CTA of kRefChunks warps: warp k owns a contiguous range of slots and counts
+// its references per id; the counts become each warp's first position per id
+// (ids in parallel, chunks in order); then every warp walks its range in
+// order, ranking equal ids among the 32 lanes of a step by __match_any_sync,
+// so the order is deterministic and needs no sort.
+constexpr int kRefChunks = 32;
+
+__global__ void __launch_bounds__(kRefChunks * 32) dedup_refs(DedupParams p) {
+  pdl_enter();
+  __shared__ int warp_sums[32];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int n = p.n_seq * p.max_blocks;
+  const int cap = p.capacity;
+  const int per = (n + kRefChunks - 1) / kRefChunks;
+  const int lo = min(n, warp * per), hi = min(n, lo + per);
+  int32_t* cnt = p.ref_cnt + (size_t)warp * cap;
+  for (int i = threadIdx.x; i < kRefChunks * cap; i += blockDim.x) p.ref_cnt[i] = 0;
+  __syncthreads();
+  for (int sl = lo + lane; sl < hi; sl += 32) {
+    const int id = p.block_table[sl];
+    if (id >= 0 && id < cap) atomicAdd(cnt + id, 1);
+  }
+  __syncthreads();
+  int carry = 0;
+  for (int base = 0; base < cap; base += blockDim.x) {
+    const int id = base + threadIdx.x;
+    const int c = id < cap ? p.refcount[id] : 0;
+    int total;
+    const int pos = block_exclusive_scan(c, warp_sums, total);
+    if (id < cap) {
+      int run = carry + pos;
+      p.ref_off[id] = run;
+      for (int k = 0; k < kRefChunks; ++k) {
+        int32_t* e = p.ref_cnt + (size_t)k * cap + id;
+        const int ck = *e;
+        *e = run;
+        run += ck;
+      }
+    }
+    carry += total;
+  }
+  if (threadIdx.x == 0) p.ref_off[cap] = carry;
+  __syncthreads();
+  const unsigned lt = (1u << lane) - 1u;
+  for (int base = lo; base < hi; base += 32) {
+    const int sl = base + lane;
+    const int id = sl < hi ? p.block_table[sl] : -1;
+    const bool ok = id >= 0 && id < cap;
+    const unsigned m = __match_any_sync(0xffffffffu, ok ? id : -1);
+    const int leader = __ffs(m) - 1;
+    const int first = (ok && lane == leader) ? cnt[id] : 0;
+    const int at = __shfl_sync(0xffffffffu, first, leader) + __popc(m & lt);
+    if (ok) {
+      p.ref_seq[at] = sl / p.max_blocks;
+      if (lane == leader) cnt[id] = first + __popc(m);
+    }
+  }
+}
+
 }  // namespace kvs
 
 using namespace kvs;
@@ -379,7 +450,8 @@ extern "C" kvs_status kvs_fingerprint_dedup(kvs_pool* pool, const uint32_t* toke
                                             int32_t n_seq, const uint32_t* tier_dev, const int64_t* seg_off_dev,
                                             const int32_t* seg_blocks_dev, uint64_t* fp_out_dev,
                                             int32_t* block_table_dev, int32_t max_blocks, int32_t* refcount_dev,
-                                            int32_t* n_phys_dev, uint32_t flags, void* ws, size_t ws_bytes,
+                                            int32_t* n_phys_dev, int32_t* owner_seq_dev, int64_t* ref_off_dev,
+                                            int32_t* ref_seq_dev, uint32_t flags, void* ws, size_t ws_bytes,
                                             cudaStream_t stream) {
   if (!pool) return fail(KVS_ERR_INVALID_ARG, "fingerprint_dedup: null pool");
   if (n_seq < 0 || max_blocks < 1) return fail(KVS_ERR_INVALID_ARG, "fingerprint_dedup: bad sizes");
@@ -388,6 +460,8 @@ extern "C" kvs_status kvs_fingerprint_dedup(kvs_pool* pool, const uint32_t* toke
   if (n_seq > 0 && !tokens_dev) return fail(KVS_ERR_INVALID_ARG, "fingerprint_dedup: null tokens");
   if ((seg_off_dev == nullptr) != (seg_blocks_dev == nullptr))
     return fail(KVS_ERR_INVALID_ARG, "fingerprint_dedup: seg_off and seg_blocks go together");
+  if ((ref_off_dev == nullptr) != (ref_seq_dev == nullptr))
+    return fail(KVS_ERR_INVALID_ARG, "fingerprint_dedup: ref_off and ref_seq go together");
   if (!aligned16(ws)) return fail(KVS_ERR_INVALID_ARG, "fingerprint_dedup: ws must be 16-byte aligned");
   if ((long long)n_seq * max_blocks > 0x3fffffffll) return fail(KVS_ERR_CAPACITY, "fingerprint_dedup: too many slots");
   size_t need = 0;
@@ -413,6 +487,7 @@ extern "C" kvs_status kvs_fingerprint_dedup(kvs_pool* pool, const uint32_t* toke
   p.flags = reinterpret_cast<uint32_t*>(take(16));
   const int n_tiles = static_cast<int>((slots + kNumTile - 1) / kNumTile);
   p.tile_cnt = reinterpret_cast<int32_t*>(take((size_t)n_tiles * 4));
+  p.ref_cnt = reinterpret_cast<int32_t*>(take((size_t)kRefChunks * pool->desc.capacity_blocks * 4));
   p.tokens = tokens_dev;
   p.seq_off = seq_off_dev;
   p.tier = tier_dev;
@@ -422,6 +497,9 @@ extern "C" kvs_status kvs_fingerprint_dedup(kvs_pool* pool, const uint32_t* toke
   p.block_table = block_table_dev;
   p.refcount = refcount_dev;
   p.n_phys = n_phys_dev;
+  p.owner = owner_seq_dev;
+  p.ref_off = ref_off_dev;
+  p.ref_seq = ref_seq_dev;
   p.status = pool->status;
   p.n_seq = n_seq;
   p.max_blocks = max_blocks;
@@ -433,10 +511,15 @@ extern "C" kvs_status kvs_fingerprint_dedup(kvs_pool* pool, const uint32_t* toke
   if (cudaMemsetAsync(p.tkeys, 0, T * 8, stream) != cudaSuccess ||
       cudaMemsetAsync(p.tmin, 0x7f, T * 4, stream) != cudaSuccess ||
       cudaMemsetAsync(p.flags, 0, 16, stream) != cudaSuccess ||
-      cudaMemsetAsync(refcount_dev, 0, (size_t)pool->desc.capacity_blocks * 4, stream) != cudaSuccess)
+      cudaMemsetAsync(refcount_dev, 0, (size_t)pool->desc.capacity_blocks * 4, stream) != cudaSuccess ||
+      (owner_seq_dev &&
+       cudaMemsetAsync(owner_seq_dev, 0xff, (size_t)pool->desc.capacity_blocks * 4, stream) != cudaSuccess))
     return fail(KVS_ERR_CUDA, "fingerprint_dedup: memset failed");
   if (n_seq == 0) {
-    if (cudaMemsetAsync(n_phys_dev, 0, 4, stream) != cudaSuccess) return fail(KVS_ERR_CUDA, "fingerprint_dedup: memset failed");
+    if (cudaMemsetAsync(n_phys_dev, 0, 4, stream) != cudaSuccess ||
+        (ref_off_dev &&
+         cudaMemsetAsync(ref_off_dev, 0, ((size_t)pool->desc.capacity_blocks + 1) * 8, stream) != cudaSuccess))
+      return fail(KVS_ERR_CUDA, "fingerprint_dedup: memset failed");
     return KVS_OK;
   }
   const int n = static_cast<int>(slots);
@@ -451,7 +534,8 @@ extern "C" kvs_status kvs_fingerprint_dedup(kvs_pool* pool, const uint32_t* toke
   if (e == cudaSuccess) e = launch_pdl(dedup_tiles, dim3(1), dim3(kNumTile), stream, p, n_tiles);
   if (e == cudaSuccess) e = launch_pdl(dedup_number, dim3(n_tiles), dim3(kNumTile), stream, p);
   if (e == cudaSuccess) e = launch_pdl(dedup_table, gs, dim3(tb), stream, p);
+  if (e == cudaSuccess && ref_off_dev) e = launch_pdl(dedup_refs, dim3(1), dim3(kRefChunks * 32), stream, p);
   if (e != cudaSuccess) return fail(KVS_ERR_CUDA, "fingerprint_dedup: launch failed");
-  count_launch(9);
+  count_launch(ref_off_dev ? 10 : 9);
   return check_launch("fingerprint_dedup");
 }

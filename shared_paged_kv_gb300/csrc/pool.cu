@@ -293,7 +293,8 @@ kvs_status kvs_workspace_size(const kvs_pool* p, int32_t op, int32_t n_seq, int3
       const size_t slots = static_cast<size_t>(n_seq) * max_blocks;
       size_t t = 1024;
       while (t < 2 * slots) t <<= 1;
-      b = t * 16 + slots * (8 + 4 + 4 + 4 + 4) + 64 * 1024 + 256;
+      // + per-chunk reference counts of the optional CSR (32 x capacity)
+      b = t * 16 + slots * (8 + 4 + 4 + 4 + 4) + 64 * 1024 + 256 + 32ull * p->desc.capacity_blocks * 4 + 256;
       break;
     }
     case KVS_OP_DECODE_ATTN:

@@ -7,18 +7,17 @@
 // m16n8k16 with tokens (QK^T) or head dims (PV) as the 16-row M dimension and
 // the <= 8 query heads of a KV head as the 8-column N dimension, so a GQA
 // group of 4 fills half of every MMA instead of a quarter.  Codes are turned
-// into fp16 in registers with the 1024-offset trick ((nibble | 0x6400) is the
-// fp16 value 1024 + nibble; subtracting 1024 is exact), and the affine
-// dequantisation is applied around the MMAs:
+// into fp16 in registers as exact subnormals (a nibble masked in place is
+// c * 2^-24 in the low position, c * 2^-20 in the high one; one LOP3 per
+// pair), and the affine dequantisation is applied around the MMAs:
 //   q.k_hat   = sum_groups  s_g * (q_g . c_g) + b_g * sum(q_g)
 //   p.v_hat   = sum_t (p_t s_g[t]) c_t + sum_t p_t b_g[t]
 // The head-dim order inside each 16-wide k-step is permuted identically for q
 // and the codes (a dot product does not depend on the order), which lets a
 // thread fetch its codes with one 8-byte shared load per row and group.  The
-// P tile is transposed into the PV B operand with movmatrix.  For P V the
-// codes enter as fp16 subnormals: a low nibble masked in place is exactly
-// c * 2^-24 and a high nibble c * 2^-20 (one LOP3 each, no offset), and the
-// accumulators are scaled back by 2^24 / 2^20 once.  K/V code tiles
+// P tile is transposed into the PV B operand with movmatrix.  The powers of
+// two of the subnormal codes are folded into the score scale (QK^T) and into
+// the final accumulator scaling (PV, 2^24 / 2^20 once).  K/V code tiles
 // arrive by 2-D TMA (64-byte swizzle); scale/bias rows by 1-D bulk copies; a
 // 2-stage ring shared by the CTA's 4 warps (each warp takes 64 of the 256
 // tokens of every block) with full/empty mbarriers.
@@ -119,11 +118,6 @@ __device__ __forceinline__ uint32_t movmatrix_t(uint32_t x) {
   return y;
 }
 
-// fp16x2 (1024 + nibble) from bits [0,4) and [16,20) of w, and
-// (1024 + 16 * nibble) from bits [4,8) and [20,24): one LOP3 each, exact
-__device__ __forceinline__ uint32_t nib_lo1024(uint32_t w) { return (w & 0x000F000Fu) | 0x64006400u; }
-__device__ __forceinline__ uint32_t nib_hi1024(uint32_t w) { return (w & 0x00F000F0u) | 0x64006400u; }
-
 // fp16x2 subnormals: bits [0,4) and [16,20) of w as c * 2^-24, bits [4,8)
 // and [20,24) as c * 2^-20 (exact)
 __device__ __forceinline__ uint32_t nib_lo_sub(uint32_t w) { return w & 0x000F000Fu; }
@@ -192,48 +186,71 @@ q4_attn_kernel(const __grid_constant__ Q4Params p, const __grid_constant__ CUten
 
   // ---- query as the B operand (k = head dim, n = query head), fp16.  Each
   // 32-bit code word w (elements 8w..8w+7 of this thread's 16 head dims of a
-  // group) feeds two MMAs: "lo" takes the low nibbles (elements 0,4 and 2,6,
-  // as 1024 + c) and "hi" the high nibbles (elements 1,5 and 3,7, as
-  // 1024 + 16c); the query is laid out in the same k order.  Per group and
-  // column: qs = sum of q, off = 1024 * sum(q over lo dims) + 64 * sum(q
-  // over hi dims), from the same fp16 values the MMAs use, so that
-  //   q . c = acc_lo + acc_hi / 16 - off   (exactly, up to fp32 accumulation).
+  // group) feeds two MMAs: "lo" takes the low nibbles (elements 0,4 and 2,6)
+  // and "hi" the high nibbles (elements 1,5 and 3,7); the query is laid out
+  // in the same k order.  The codes enter as exact fp16 subnormals (a low
+  // nibble masked in place is c * 2^-24, a high nibble c * 2^-20), so
+  //   (q . c) * 2^-24 = acc_lo + acc_hi / 16   (no offset, no cancellation).
+  // Each query row is first scaled by a power of two 2^-e that puts its
+  // largest |q| in [2^14, 2^15): every finite bf16 query then converts to
+  // fp16 without overflow or loss of its leading bits, and 2^e is folded
+  // back into the row's score scale (exact).
   const int G_ = p.g;
   const uint16_t* qbase = p.q + ((size_t)a * p.hq + h * G_) * kQ4D;
   uint32_t qlo[2][2][2], qhi[2][2][2];   // [group][word][k half]
-  float qs[2][2], qoff[2][2];            // [group][column 2c / 2c+1]
+  float qs[2][2];                        // [group][column 2c / 2c+1]: 2^-24 * sum of the group's q
+  float colscale[2];                     // [column]: scale * log2(e) * 2^24 * 2^e(row)
   {
     const bool ok = g < G_;
-    auto qv = [&](int d) { return ok ? __uint_as_float((uint32_t)qbase[g * kQ4D + d] << 16) : 0.f; };
+    float qf[2][2][8];
+    float qmax = 0.f;
+#pragma unroll
+    for (int grp = 0; grp < 2; ++grp)
+#pragma unroll
+      for (int w = 0; w < 2; ++w)
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const int d = grp * 64 + 16 * c + 8 * w + j;
+          qf[grp][w][j] = ok ? __uint_as_float((uint32_t)qbase[g * kQ4D + d] << 16) : 0.f;
+          qmax = fmaxf(qmax, fabsf(qf[grp][w][j]));
+        }
+    qmax = fmaxf(qmax, __shfl_xor_sync(0xffffffffu, qmax, 1));
+    qmax = fmaxf(qmax, __shfl_xor_sync(0xffffffffu, qmax, 2));
+    // qmax = f * 2^x with f in [0.5, 1) and x = biased exponent - 126 (normal
+    // qmax); e = x - 15; zero, subnormal and non-finite rows keep e = 0 or
+    // the clamp, so both 2^-e and 2^e stay normal floats
+    const int bexp = (int)((__float_as_uint(qmax) >> 23) & 255u);
+    int e = (bexp > 0 && bexp < 255) ? bexp - 126 - 15 : 0;
+    e = min(max(e, -100), 113);
+    const float down = __uint_as_float((uint32_t)(127 - e) << 23);   // 2^-e
+    const float up = __uint_as_float((uint32_t)(127 + e) << 23);     // 2^e
 #pragma unroll
     for (int grp = 0; grp < 2; ++grp) {
-      float slo = 0.f, shi = 0.f;
+      float sum = 0.f;
 #pragma unroll
       for (int w = 0; w < 2; ++w) {
-        const int base = grp * 64 + 16 * c + 8 * w;
-        qlo[grp][w][0] = pack_f16(qv(base + 0), qv(base + 4));
-        qlo[grp][w][1] = pack_f16(qv(base + 2), qv(base + 6));
-        qhi[grp][w][0] = pack_f16(qv(base + 1), qv(base + 5));
-        qhi[grp][w][1] = pack_f16(qv(base + 3), qv(base + 7));
+        const float* v = qf[grp][w];
+        qlo[grp][w][0] = pack_f16(v[0] * down, v[4] * down);
+        qlo[grp][w][1] = pack_f16(v[2] * down, v[6] * down);
+        qhi[grp][w][0] = pack_f16(v[1] * down, v[5] * down);
+        qhi[grp][w][1] = pack_f16(v[3] * down, v[7] * down);
 #pragma unroll
         for (int k = 0; k < 2; ++k) {
           const float2 l2 = __half22float2(*reinterpret_cast<const __half2*>(&qlo[grp][w][k]));
           const float2 h2 = __half22float2(*reinterpret_cast<const __half2*>(&qhi[grp][w][k]));
-          slo += l2.x + l2.y;
-          shi += h2.x + h2.y;
+          sum += (l2.x + l2.y) + (h2.x + h2.y);
         }
       }
       // sums over the 4 lanes of row g, then fetched for columns 2c and 2c+1
-      slo += __shfl_xor_sync(0xffffffffu, slo, 1);
-      slo += __shfl_xor_sync(0xffffffffu, slo, 2);
-      shi += __shfl_xor_sync(0xffffffffu, shi, 1);
-      shi += __shfl_xor_sync(0xffffffffu, shi, 2);
-      const float sum = slo + shi, off = 1024.f * slo + 64.f * shi;
+      sum += __shfl_xor_sync(0xffffffffu, sum, 1);
+      sum += __shfl_xor_sync(0xffffffffu, sum, 2);
+      sum *= 5.9604644775390625e-8f;   // 2^-24
       qs[grp][0] = __shfl_sync(0xffffffffu, sum, (2 * c) * 4);
       qs[grp][1] = __shfl_sync(0xffffffffu, sum, (2 * c + 1) * 4);
-      qoff[grp][0] = __shfl_sync(0xffffffffu, off, (2 * c) * 4);
-      qoff[grp][1] = __shfl_sync(0xffffffffu, off, (2 * c + 1) * 4);
     }
+    const float rs = p.scale_log2 * 16777216.f;   // 2^24
+    colscale[0] = rs * __shfl_sync(0xffffffffu, up, (2 * c) * 4);
+    colscale[1] = rs * __shfl_sync(0xffffffffu, up, (2 * c + 1) * 4);
   }
 
   float m[2] = {-INFINITY, -INFINITY}, l[2] = {0.f, 0.f};
@@ -262,7 +279,7 @@ q4_attn_kernel(const __grid_constant__ Q4Params p, const __grid_constant__ CUten
 #pragma unroll
       for (int mt = 0; mt < 4; ++mt) {
         const int t0 = tw + 16 * mt + g, t1 = t0 + 8;
-        float cg[2][4];   // q . c per group, rows (t0, t1) x columns (2c, 2c+1)
+        float cg[2][4];   // 2^-24 q . c per group, rows (t0, t1) x columns (2c, 2c+1)
 #pragma unroll
         for (int grp = 0; grp < 2; ++grp) {
           float al_[4] = {0.f, 0.f, 0.f, 0.f}, ah_[4] = {0.f, 0.f, 0.f, 0.f};
@@ -272,11 +289,11 @@ q4_attn_kernel(const __grid_constant__ Q4Params p, const __grid_constant__ CUten
           for (int w = 0; w < 2; ++w) {
             const uint32_t r0 = w ? w0.y : w0.x, r1 = w ? w1.y : w1.x;
             const uint32_t s0 = r0 >> 8, s1 = r1 >> 8;
-            mma_f16(al_, nib_lo1024(r0), nib_lo1024(r1), nib_lo1024(s0), nib_lo1024(s1), qlo[grp][w][0], qlo[grp][w][1]);
-            mma_f16(ah_, nib_hi1024(r0), nib_hi1024(r1), nib_hi1024(s0), nib_hi1024(s1), qhi[grp][w][0], qhi[grp][w][1]);
+            mma_f16(al_, nib_lo_sub(r0), nib_lo_sub(r1), nib_lo_sub(s0), nib_lo_sub(s1), qlo[grp][w][0], qlo[grp][w][1]);
+            mma_f16(ah_, nib_hi_sub(r0), nib_hi_sub(r1), nib_hi_sub(s0), nib_hi_sub(s1), qhi[grp][w][0], qhi[grp][w][1]);
           }
 #pragma unroll
-          for (int e = 0; e < 4; ++e) cg[grp][e] = fmaf(ah_[e], 0.0625f, al_[e]) - qoff[grp][e & 1];
+          for (int e = 0; e < 4; ++e) cg[grp][e] = fmaf(ah_[e], 0.0625f, al_[e]);
         }
         const uint2 sb0 = *reinterpret_cast<const uint2*>(ksb + t0 * 8);
         const uint2 sb1 = *reinterpret_cast<const uint2*>(ksb + t1 * 8);
@@ -291,7 +308,7 @@ q4_attn_kernel(const __grid_constant__ Q4Params p, const __grid_constant__ CUten
           const float2 s1 = (e < 2) ? g01 : g11;
           float x = s0.x * cg[0][e] + s0.y * qs[0][cc] + s1.x * cg[1][e] + s1.y * qs[1][cc];
           const int tok = (e < 2) ? t0 : t1;
-          sc[mt][e] = tok < nv ? x * p.scale_log2 : -INFINITY;
+          sc[mt][e] = tok < nv ? x * colscale[cc] : -INFINITY;
         }
       }
       // online softmax over this warp's 64 tokens, per query column

@@ -8,7 +8,6 @@
 // score by a 4 x 8-bit radix select on the float bits (scores are >= 0, so
 // the bit pattern orders them), then emits, in ascending position order, every
 // position above the threshold and the lowest-positioned ones equal to it.
-#include <mutex>
 #include <string>
 
 #include "common.cuh"
@@ -16,12 +15,20 @@
 
 namespace kvs {
 
-// Rows beyond the score buffer (cap_rows) are never read or written.
-__device__ __forceinline__ int agent_rows(const int64_t* row_off, int a, long long cap_rows) {
-  long long r0 = row_off[a], r1 = row_off[a + 1];
-  if (r0 < 0) r0 = 0;
-  if (r1 > cap_rows) r1 = cap_rows;
-  return r1 > r0 ? static_cast<int>(r1 - r0) : 0;
+// The rows sel_scores writes: [row_off[0], row_off[n_agents]) clipped to the
+// score buffer [0, cap_rows).
+__device__ __forceinline__ long long rows_lo(const int64_t* row_off) { return row_off[0] > 0 ? row_off[0] : 0; }
+__device__ __forceinline__ long long rows_hi(const int64_t* row_off, int n_agents, long long cap_rows) {
+  return row_off[n_agents] < cap_rows ? row_off[n_agents] : cap_rows;
+}
+
+// Rows of agent a, or 0 when its range is malformed: a range that ends
+// before it starts or leaves the scored rows [lo, hi) selects nothing, so
+// every score the selection reads was written by sel_scores in the same call.
+__device__ __forceinline__ int agent_rows(const int64_t* row_off, int a, long long lo, long long hi) {
+  const long long r0 = row_off[a], r1 = row_off[a + 1];
+  if (r0 < lo || r1 < r0 || r1 > hi) return 0;
+  return static_cast<int>(r1 - r0);
 }
 
 __global__ void sel_scores(const uint16_t* __restrict__ kc, const uint16_t* __restrict__ kn,
@@ -29,7 +36,7 @@ __global__ void sel_scores(const uint16_t* __restrict__ kc, const uint16_t* __re
                            long long cap_rows, float* __restrict__ scores) {
   const long long row = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
-  if (row >= row_off[n_agents] || row >= cap_rows) return;
+  if (row < rows_lo(row_off) || row >= rows_hi(row_off, n_agents, cap_rows)) return;
   const uint4* a = reinterpret_cast<const uint4*>(kc + row * row_elems);
   const uint4* b = reinterpret_cast<const uint4*>(kn + row * row_elems);
   float acc = 0.f;
@@ -64,13 +71,14 @@ __global__ void __launch_bounds__(1024) sel_topk(const float* __restrict__ score
   __shared__ unsigned s_prefix;
   __shared__ int s_remaining;
   const int a = blockIdx.x;
-  const int64_t r0 = row_off[a];
-  const int n = agent_rows(row_off, a, cap_rows);
+  const long long lo = rows_lo(row_off), hi = rows_hi(row_off, n_agents, cap_rows);
+  const int n = agent_rows(row_off, a, lo, hi);
+  const int64_t r0 = n > 0 ? row_off[a] : 0;   // rows [r0, r0 + n) lie in [lo, hi) when n > 0
   const int k = count_for(ratio, n);
   // exclusive prefix of k over agents
   if (threadIdx.x == 0) {
     int64_t o = 0;
-    for (int b = 0; b < a; ++b) o += count_for(ratio, agent_rows(row_off, b, cap_rows));
+    for (int b = 0; b < a; ++b) o += count_for(ratio, agent_rows(row_off, b, lo, hi));
     idx_off[a] = o;
     if (a == n_agents - 1) idx_off[n_agents] = o + k;
     s_prefix = 0u;
@@ -158,16 +166,16 @@ extern "C" kvs_status kvs_select_critical(const void* k_cached_dev, const void* 
 // ---------------------------------------------------------------------------
 // kvs_select_critical_noalloc: the same selection for callers that cannot
 // allocate device memory on the call path.  Its only scratch (one fp32 score
-// per position row) lives in this file-scope device array, reserved once per
-// device when the library's device code is loaded and held until the process
-// exits.  Host code never uses the array's name as a pointer: the device
-// address is fetched with cudaGetSymbolAddress once per device (on the first
-// call made with that device current) and cached.
+// per position row) lives in this file-scope device array, reserved on every
+// device where the library's device code is loaded and held until the
+// process exits.  Host code never uses the array's name as a pointer: every
+// call asks the runtime for the array's device address in the current context
+// (cudaGetSymbolAddress, a lookup that allocates nothing).  The address is not
+// cached, because a device reset or a new primary context reloads the device
+// code at another address.
 namespace kvs {
 constexpr long long kSelNoallocMaxRows = 1ll << 20;   // 4 MiB of scores
 static __device__ __align__(256) float g_sel_scores[kSelNoallocMaxRows];
-static float* g_sel_scores_dev[64] = {};
-static std::mutex g_sel_scores_mu;
 }  // namespace kvs
 
 extern "C" kvs_status kvs_select_critical_noalloc(const void* k_cached_dev, const void* k_new_dev,
@@ -187,24 +195,16 @@ extern "C" kvs_status kvs_select_critical_noalloc(const void* k_cached_dev, cons
   if (!aligned16(k_cached_dev) || !aligned16(k_new_dev))
     return fail(KVS_ERR_INVALID_ARG, "select_critical_noalloc: K buffers must be 16-byte aligned");
   if (!(ratio >= 0.f)) return fail(KVS_ERR_INVALID_ARG, "select_critical_noalloc: ratio must be >= 0");
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64)
-    return fail(KVS_ERR_CUDA, "select_critical_noalloc: cannot identify the current device");
-  float* scores = nullptr;
-  {
-    std::lock_guard<std::mutex> lock(g_sel_scores_mu);
-    if (!g_sel_scores_dev[dev]) {
-      void* ptr = nullptr;
-      const cudaError_t e = cudaGetSymbolAddress(&ptr, g_sel_scores);
-      if (e != cudaSuccess || !ptr)
-        return fail(KVS_ERR_CUDA, std::string("select_critical_noalloc: cudaGetSymbolAddress failed: ") +
-                                      cudaGetErrorString(e));
-      g_sel_scores_dev[dev] = static_cast<float*>(ptr);
-    }
-    scores = g_sel_scores_dev[dev];
-  }
-  // Every score the selection reads is written by sel_scores in this call, so
-  // nothing in the array has to start at zero.
+  void* ptr = nullptr;
+  const cudaError_t e = cudaGetSymbolAddress(&ptr, g_sel_scores);
+  if (e != cudaSuccess || !ptr)
+    return fail(KVS_ERR_CUDA, std::string("select_critical_noalloc: cudaGetSymbolAddress failed: ") +
+                                  cudaGetErrorString(e));
+  float* scores = static_cast<float*>(ptr);
+  // Every score the selection reads is written by sel_scores in this call
+  // (rows [row_off[0], row_off[n_agents]) below the capacity; an agent whose
+  // range is malformed or leaves those rows reads nothing), so nothing in the
+  // array has to start at zero.
   const long long threads = rows * 32;
   const int tb = 256;
   if (rows > 0) {

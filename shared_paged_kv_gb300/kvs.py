@@ -86,7 +86,7 @@ def load(path: str = LIB_PATH):
     sigs = {
         "kvs_pool_create": [ctypes.POINTER(PoolDesc), P, P, P, P, P, P, ctypes.POINTER(P)],
         "kvs_pool_destroy": [P],
-        "kvs_fingerprint_dedup": [P, P, P, I32, P, P, P, P, P, I32, P, P, U32, P, SZ, P],
+        "kvs_fingerprint_dedup": [P, P, P, I32, P, P, P, P, P, I32, P, P, P, P, P, U32, P, SZ, P],
         "kvs_rope_rerotate": [P, I32, P, I32, I32, F32, P, P, I32, P],
         "kvs_select_critical": [P, P, P, I32, I32, I32, F32, P, P, P, SZ, P],
         "kvs_select_critical_noalloc": [P, P, P, I32, I32, I32, F32, P, P, P],
@@ -188,11 +188,14 @@ def kvs_workspace_size(pool: Pool, op: int, n_seq: int, max_blocks: int, n_q_hea
 
 
 def kvs_fingerprint_dedup(pool: Pool, tokens, seq_off, n_seq, tier, seg_off, seg_blocks, fp_out,
-                          block_table, max_blocks, refcount, n_phys, ws, flags=0, stream=None):
+                          block_table, max_blocks, refcount, n_phys, ws, flags=0, stream=None,
+                          owner_seq=None, ref_off=None, ref_seq=None):
+    """Fingerprints, block table, refcounts and n_phys; optionally the owner
+    sequence of every physical block and the CSR of its references."""
     _check(load().kvs_fingerprint_dedup(
         pool.handle, _ptr(tokens), _ptr(seq_off), n_seq, _ptr(tier), _ptr(seg_off), _ptr(seg_blocks),
-        _ptr(fp_out), _ptr(block_table), max_blocks, _ptr(refcount), _ptr(n_phys), flags,
-        _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)))
+        _ptr(fp_out), _ptr(block_table), max_blocks, _ptr(refcount), _ptr(n_phys), _ptr(owner_seq),
+        _ptr(ref_off), _ptr(ref_seq), flags, _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)))
 
 
 def kvs_rope_rerotate(pool: Pool, layer, jobs, n_jobs, max_job_tokens, theta, src_table, dst_table,

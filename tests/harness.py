@@ -5,6 +5,7 @@ import torch
 
 from shared_paged_kv_gb300 import kvs as K
 from shared_paged_kv_gb300 import workloads as W
+from oracle import select as OS
 
 DEV = torch.device("cuda:0")
 
@@ -48,13 +49,19 @@ def gpu_dedup(pool, w: W.Workload, flags: int = 0, segments: bool = True, tier=N
     cap = pool.desc.capacity_blocks
     refc = torch.zeros(cap, dtype=torch.int32, device=DEV)
     nphys = torch.zeros(1, dtype=torch.int32, device=DEV)
+    owner = torch.full((cap,), -7, dtype=torch.int32, device=DEV)
+    ref_off = torch.full((cap + 1,), -7, dtype=torch.int64, device=DEV)
+    ref_seq = torch.full((max(w.n_seq * w.max_blocks, 1),), -7, dtype=torch.int32, device=DEV)
     ws = workspace(K.kvs_workspace_size(pool, K.KVS_OP_DEDUP, w.n_seq, w.max_blocks))
     K.kvs_fingerprint_dedup(pool, tokens, seq_off, w.n_seq, tier_t, seg_off, seg_blocks, fp, table,
-                            w.max_blocks, refc, nphys, ws, flags=flags)
+                            w.max_blocks, refc, nphys, ws, flags=flags, owner_seq=owner, ref_off=ref_off,
+                            ref_seq=ref_seq)
     torch.cuda.synchronize()
     n = int(nphys.item())
     return dict(fp=fp.cpu().numpy().view(np.uint64), block_table=table.cpu().numpy(),
-                refcount=refc.cpu().numpy()[:n], refcount_full=refc.cpu().numpy(), n_phys=n)
+                refcount=refc.cpu().numpy()[:n], refcount_full=refc.cpu().numpy(), n_phys=n,
+                owner=owner.cpu().numpy(), ref_off=ref_off.cpu().numpy(), ref_seq=ref_seq.cpu().numpy(),
+                refc_dev=refc, nphys_dev=nphys)
 
 
 def bf16_pool(w: W.Workload, n_layers: int = 1, capacity=None, with_diff: bool = None, layers_np=None):
@@ -109,3 +116,23 @@ def assert_close_attn(got, exp, atol=ATOL, rtol=RTOL_L2):
     rel = np.linalg.norm(got - exp) / max(np.linalg.norm(exp), 1e-30)
     assert err <= atol and rel <= rtol, f"max|d|={err:.3e} relL2={rel:.3e}"
     return err, rel
+
+
+def check_selection(kc_bits, kn_bits, off, ratio, gi, go):
+    """A GPU selection (positions gi, offsets go) against the oracle: offsets
+    equal, positions ascending, and the position sets equal except for ties
+    within 1e-5 of the k-th score (relative to that score once it exceeds 1:
+    the GPU sums row_elems squared differences in float32, whose rounding
+    error is relative to the sum)."""
+    f32 = W.bf16_bits_to_f32
+    ridx, roff, sc = OS.select_critical(f32(kc_bits), f32(kn_bits), off, ratio)
+    np.testing.assert_array_equal(go, roff)
+    for a in range(len(off) - 1):
+        g = set(gi[go[a]:go[a + 1]].tolist())
+        r = set(ridx[roff[a]:roff[a + 1]].tolist())
+        assert list(gi[go[a]:go[a + 1]]) == sorted(g)
+        if g != r:
+            s = sc[off[a]:off[a + 1]]
+            kth = np.sort(s)[::-1][len(r) - 1]
+            for t in g ^ r:
+                assert abs(s[t] - kth) <= 1e-5 * max(1.0, kth), (a, t, s[t], kth)

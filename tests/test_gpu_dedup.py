@@ -1,5 +1,6 @@
 """GPU fingerprint + dedup vs the oracle: bit-exact fingerprints, block
-tables, refcounts and physical-block counts."""
+tables, refcounts, physical-block counts, owner sequences and the reference
+lists of every physical block; pool statistics on the 7B workload."""
 import numpy as np
 import pytest
 
@@ -8,7 +9,7 @@ pytestmark = pytest.mark.gpu
 
 from shared_paged_kv_gb300 import kvs as K
 from shared_paged_kv_gb300 import workloads as W
-from oracle import fingerprint as OF
+from oracle import accounting as OA, fingerprint as OF
 import harness as H
 
 
@@ -26,7 +27,15 @@ def check(w, flags=0, segments=True, tier=None, capacity=None):
     np.testing.assert_array_equal(got["refcount"], ref["refcount"])
     np.testing.assert_array_equal(got["fp"], ref["fp"])
     assert (got["refcount_full"][ref["n_phys"]:] == 0).all()
+    n = ref["n_phys"]
+    np.testing.assert_array_equal(got["owner"][:n], ref["owner"])
+    assert (got["owner"][n:] == -1).all()
+    r_off, r_seq = OF.references(ref["block_table"], n)
+    np.testing.assert_array_equal(got["ref_off"][:n + 1], r_off)
+    assert (got["ref_off"][n + 1:] == r_off[-1]).all()
+    np.testing.assert_array_equal(got["ref_seq"][:r_off[-1]], r_seq)
     assert K.kvs_pool_check(pool) == 0
+    got["pool"] = pool
     return got, ref
 
 
@@ -99,3 +108,11 @@ def test_full_size(name):
     got, ref = check(w, capacity=w.capacity_blocks)
     if name == "mha7b":
         assert ref["n_phys"] == 614 + 8 * 410
+        # pool statistics: INMS walkthrough §1.2 independent (n*L) against
+        # shared ((1-p)*n + p)*L footprint, at block granularity (L = 1024
+        # blocks, p = 614/1024); this pool holds one layer of 32 KV heads x 128
+        st = K.kvs_pool_stats(got["pool"], got["refc_dev"], got["nphys_dev"])
+        per_block = 2 * w.n_kv_heads * 16 * w.head_dim * 2
+        assert st["unique_blocks"] == 3894 and st["shared_blocks"] == 614 and st["total_refs"] == 8 * 1024
+        assert st["pool_bytes"] == round(OA.shared_bytes(8, 1024, per_block, 614 / 1024))
+        assert st["dense_bytes"] == OA.independent_bytes(8, 1024, per_block)

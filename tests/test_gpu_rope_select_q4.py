@@ -159,19 +159,7 @@ def select_case(kc_bits, kn_bits, off, ratio, max_rows):
     return idx.cpu().numpy(), idx_off.cpu().numpy()
 
 
-def check_selection(kc_bits, kn_bits, off, ratio, gi, go):
-    ridx, roff, sc = OS.select_critical(f32(kc_bits), f32(kn_bits), off, ratio)
-    np.testing.assert_array_equal(go, roff)
-    for a in range(len(off) - 1):
-        g = set(gi[go[a]:go[a + 1]].tolist())
-        r = set(ridx[roff[a]:roff[a + 1]].tolist())
-        assert list(gi[go[a]:go[a + 1]]) == sorted(g)
-        if g != r:
-            # only ties within 1e-5 of the k-th score may differ
-            s = sc[off[a]:off[a + 1]]
-            kth = np.sort(s)[::-1][len(r) - 1]
-            for t in g ^ r:
-                assert abs(s[t] - kth) <= 1e-5 * max(1.0, kth), (a, t, s[t], kth)
+check_selection = H.check_selection
 
 
 def test_select_small():
@@ -229,10 +217,11 @@ def q4_pool(w, cap, n_layers=1):
     return pool
 
 
-def q4_case(w, sample_agents=None):
+def q4_case(w, sample_agents=None, q_pow2=0):
     """Source bf16 K/V per physical block -> GPU quantiser; the oracle
     quantises the same source values itself and must match bit for bit; then
-    Q4 attention vs the oracle on its dequantised values."""
+    Q4 attention vs the oracle on its dequantised values.  q_pow2 multiplies
+    the query by 2^q_pow2 (exact in bf16) and the score scale by 2^-q_pow2."""
     ref = OF.dedup(w.tokens, w.seq_off, w.tier, w.block_tokens, w.max_blocks)
     cap = ref["n_phys"]
     g = torch.Generator(device=H.DEV).manual_seed(77)
@@ -243,11 +232,15 @@ def q4_case(w, sample_agents=None):
     K.kvs_quantize_q4(pool, 0, ksrc.view(torch.int16), vsrc.view(torch.int16),
                       H.i32(np.arange(cap)), cap)
     q_bits = w.q_layer(0)
+    scale = w.scale
+    if q_pow2:
+        q_bits = W.f32_to_bf16_bits(f32(q_bits) * np.float32(2.0 ** q_pow2))
+        scale = w.scale * 2.0 ** -q_pow2
     n = w.n_seq
     out = torch.full((n, w.n_q_heads, 128), float("nan"), dtype=torch.float32, device=H.DEV)
     ws = H.workspace(K.kvs_workspace_size(pool, K.KVS_OP_DECODE_ATTN_Q4, n, w.max_blocks, w.n_q_heads))
     K.kvs_decode_attn_q4(pool, 0, H.bits_to_dev(q_bits), w.n_q_heads, H.i32(ref["block_table"]), w.max_blocks,
-                         H.i32(w.seq_len), n, w.scale, out, ws)
+                         H.i32(w.seq_len), n, scale, out, ws)
     torch.cuda.synchronize()
     assert K.kvs_pool_check(pool) == 0
     got = out.cpu().numpy().astype(np.float64)
@@ -271,7 +264,7 @@ def q4_case(w, sample_agents=None):
         np.testing.assert_array_equal(vsbh[b].view(np.uint16), sb_v.view(np.uint16))
         kd[b] = OQ.dequantize(c_k, sb_k)
         vd[b] = OQ.dequantize(c_v, sb_v)
-    exp = OA.decode_attention(f32(q_bits), kd, vd, ref["block_table"], w.seq_len, w.block_tokens, w.scale,
+    exp = OA.decode_attention(f32(q_bits), kd, vd, ref["block_table"], w.seq_len, w.block_tokens, scale,
                               agents=agents)
     sel = list(agents)
     H.assert_close_attn(got[sel], exp[sel])
@@ -289,6 +282,16 @@ def test_q4_small_ragged():
 
 def test_q4_group8():
     q4_case(W.make_q4(n_seq=2, ctx=600, hq=16, hkv=2))
+
+
+def test_q4_query_outside_fp16_range():
+    # the Q4 kernel multiplies in fp16: a bf16 query above 65504, or one deep
+    # in fp16's subnormal range, must still give the oracle's attention
+    w = W.make_q4(n_seq=2, ctx=600, hq=8, hkv=2)
+    q_big = W.f32_to_bf16_bits(f32(w.q_layer(0)) * np.float32(2.0 ** 15))
+    assert np.abs(f32(q_big)).max() > 65504.0
+    q4_case(w, q_pow2=15)
+    q4_case(w, q_pow2=-22)
 
 
 def test_q4_full_size_sampled():

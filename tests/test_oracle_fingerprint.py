@@ -135,6 +135,15 @@ def test_dedup_matches_bruteforce(seed, segments):
     np.testing.assert_array_equal(r["refcount"], ref2)
     assert r["n_phys"] == len(ref2)
     assert r["refcount"].sum() == (r["block_table"] >= 0).sum()
+    # owner = sequence of each id's first slot in scan order; reference CSR =
+    # the slots holding each id, read off the flattened (sequence-major) table
+    flat = t2.ravel()
+    ref_off, ref_seq = F.references(r["block_table"], r["n_phys"])
+    for p in range(r["n_phys"]):
+        where = np.flatnonzero(flat == p)
+        assert r["owner"][p] == where[0] // mb
+        np.testing.assert_array_equal(ref_seq[ref_off[p]:ref_off[p + 1]], where // mb)
+    np.testing.assert_array_equal(np.diff(ref_off), ref2)
     # fingerprints of full blocks are CalcHash of the block's tokens and tier
     for s in range(len(off) - 1):
         L = int(off[s + 1] - off[s])
@@ -180,3 +189,15 @@ def test_divergence_ends_sharing():
     r = F.dedup(np.concatenate([a, b]), off, None, B, 3)
     t = r["block_table"]
     assert t[0, 0] == t[1, 0] and t[0, 2] != t[1, 2]
+
+
+def test_references_hand_example():
+    # three sequences: a 1-block common prefix, a second block shared by the
+    # first two, then private blocks; worked out by hand
+    table = np.array([[0, 1, 2], [0, 1, 3], [0, 4, -1]], np.int32)
+    off, seq = F.references(table, 5)
+    assert off.tolist() == [0, 3, 5, 6, 7, 8]
+    assert seq.tolist() == [0, 1, 2, 0, 1, 0, 1, 2]
+    # a sequence that holds one block twice (a repeated segment) lists it twice
+    off, seq = F.references(np.array([[0, 1, 0], [1, -1, -1]], np.int32), 2)
+    assert off.tolist() == [0, 2, 4] and seq.tolist() == [0, 0, 0, 1]
