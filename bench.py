@@ -46,7 +46,7 @@ METRIC = "decode-attn tokens/s & KV GB/s vs GB300 HBM roofline; RoPE-reuse token
 UNIT = "tokens/s"
 WORKLOAD = ("mha7b: 8 agents x 16384-token context, 60% shared prefix (614 shared + 8x410 private "
             "16-token blocks), 32 q heads = 32 kv heads, head_dim 128, bf16, 32 layers, 1 decode token per agent")
-EXTRA_CONFIGS = ["tiny", "gqa_fanout", "allgather", "q4", "select", "mirror"]
+EXTRA_CONFIGS = ["tiny", "gqa_fanout", "allgather", "q4", "q4_mirror", "select", "mirror"]
 
 
 def parse():
@@ -505,9 +505,12 @@ CONFIG_INFO = {
                   "profiles/launches_allgather_step.md",
                   "allgather: 64 agents, private 1k-6k + 64 shared 128-token segments per agent with RoPE shifts "
                   "(theta 1e6), 31 mirror-diff blocks per agent, 40 q / 8 kv heads, d 128, 48 layers"),
-    "q4": ("q4_attn_kernel", "profiles/q4_attn_q4.md",
+    "q4": ("q4_attn_kernel<0>", "profiles/q4_attn_q4.md",
            "q4: 12 agents x 8192 tokens, 32 q / 8 kv heads, d 128, Q4G64 codes with fp16 scale+bias, "
            "256-token blocks, 32 layers"),
+    "q4_mirror": ("q4_attn_kernel<1>", None,
+                  "q4_mirror: the q4 workload with bf16 mirror diffs ~N(0,0.1) on 31 of each agent's 512 "
+                  "16-token sub-blocks (6 %), restored inside the Q4 read"),
 }
 
 
@@ -642,11 +645,12 @@ def bench_tiny_replicated(torch, K, W, dev, reps, flush, n_inst=4096):
 def workload_record(name, torch, K, W, dev, stream, steps, warmup, layers):
     """GPU dedup + plan + decode attention on every layer (Q4: attention only),
     eager through the public API and replayed from CUDA graphs."""
-    mk = {"tiny": W.make_tiny, "gqa_fanout": W.make_gqa_fanout, "allgather": W.make_allgather, "q4": W.make_q4}
+    mk = {"tiny": W.make_tiny, "gqa_fanout": W.make_gqa_fanout, "allgather": W.make_allgather, "q4": W.make_q4,
+          "q4_mirror": W.make_q4_mirror}
     w = mk[name]()
     L = layers or w.n_layers
     N, H, D, B = w.n_seq, w.n_kv_heads, w.head_dim, w.block_tokens
-    q4 = name == "q4"
+    q4 = name in ("q4", "q4_mirror")
     tokens = torch.from_numpy(w.tokens.view(np.int32)).to(dev)
     seq_off = torch.from_numpy(w.seq_off).to(dev)
     seq_len = torch.from_numpy(w.seq_len).to(dev)
@@ -677,14 +681,20 @@ def workload_record(name, torch, K, W, dev, stream, steps, warmup, layers):
         vs = [torch.empty_like(ks[0]) for _ in range(L)]
         ksb = [torch.empty(cap * H * B * 4, dtype=torch.float16, device=dev) for _ in range(L)]
         vsb = [torch.empty_like(ksb[0]) for _ in range(L)]
-        pool = K.kvs_pool_create(L, H, D, B, K.KVS_DTYPE_Q4G64, cap, N, ks, vs, ksb, vsb)
+        nd = w.diff_capacity_blocks
+        dks = [(0.1 * torch.randn((nd, H, 16, D), generator=gen, device=dev)).to(torch.bfloat16).view(torch.int16)
+               for _ in range(L)] if nd else None
+        dvs = [(0.1 * torch.randn((nd, H, 16, D), generator=gen, device=dev)).to(torch.bfloat16).view(torch.int16)
+               for _ in range(L)] if nd else None
+        pool = K.kvs_pool_create(L, H, D, B, K.KVS_DTYPE_Q4G64, cap, N, ks, vs, ksb, vsb, dk_layers=dks,
+                                 dv_layers=dvs, diff_capacity_blocks=nd)
         ids = torch.arange(cap, dtype=torch.int32, device=dev)
         for l in range(L):
             src_k = torch.randn((cap, H, B, D), generator=gen, device=dev, dtype=torch.bfloat16)
             src_v = torch.randn((cap, H, B, D), generator=gen, device=dev, dtype=torch.bfloat16)
             K.kvs_quantize_q4(pool, l, src_k.view(torch.int16), src_v.view(torch.int16), ids, cap)
             del src_k, src_v
-        per_launch = cap * H * B * 144
+        per_launch = cap * H * B * 144 + nd * H * 16 * D * 2 * 2
     else:
         ks = [torch.randn((cap, H, B, D), generator=gen, device=dev, dtype=torch.bfloat16).view(torch.int16)
               for _ in range(L)]
@@ -698,7 +708,9 @@ def workload_record(name, torch, K, W, dev, stream, steps, warmup, layers):
         pool = K.kvs_pool_create(L, H, D, B, K.KVS_DTYPE_BF16, cap, N, ks, vs, dk_layers=dks, dv_layers=dvs,
                                  diff_capacity_blocks=nd)
         per_launch = (cap + nd) * H * B * D * 2 * 2
-    per_launch += N * w.n_q_heads * D * (2 + 4) + N * w.max_blocks * 4 * (2 if w.diff_table is not None else 1)
+    per_launch += N * w.n_q_heads * D * (2 + 4) + N * w.max_blocks * 4
+    if w.diff_table is not None:
+        per_launch += w.diff_table.nbytes
     refc = torch.zeros(cap, dtype=torch.int32, device=dev)
     q = torch.randn((L, N, w.n_q_heads, D), generator=gen, device=dev, dtype=torch.bfloat16)
     out = torch.zeros((L, N, w.n_q_heads, D), dtype=torch.float32, device=dev)
@@ -710,7 +722,8 @@ def workload_record(name, torch, K, W, dev, stream, steps, warmup, layers):
 
     def attn(l):
         if q4:
-            K.kvs_decode_attn_q4(pool, l, q[l], w.n_q_heads, table, w.max_blocks, seq_len, N, w.scale, out[l], ws_a)
+            K.kvs_decode_attn_q4(pool, l, q[l], w.n_q_heads, table, w.max_blocks, seq_len, N, w.scale, out[l], ws_a,
+                                 diff_table=dt)
         else:
             K.kvs_decode_attn_planned(pool, l, q[l], w.n_q_heads, table, w.max_blocks, seq_len, N, dt, ro, rs,
                                       w.theta, w.scale, out[l], ws_a)

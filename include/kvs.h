@@ -78,9 +78,11 @@ typedef enum { KVS_DTYPE_BF16 = 0, KVS_DTYPE_Q4G64 = 1 } kvs_dtype;
  *           [capacity_blocks][num_kv_heads][block_tokens][head_dim/64][2] fp16
  *           (index 0 = scale, 1 = bias; value = scale * code + bias) — [Q4]
  *           §2.1 (ratio 0.281 fixes group 64 with fp16 scale and bias).
- *   Mirror diffs (BF16 only): dk/dv slabs [diff_capacity_blocks][num_kv_heads]
- *           [block_tokens][head_dim] bf16 holding K and V differences added to
- *           a master block — [TD] section 3.
+ *   Mirror diffs: dk/dv slabs [diff_capacity_blocks][num_kv_heads]
+ *           [diff_tokens][head_dim] bf16 holding K and V differences added to
+ *           a master block — [TD] section 3; diff_tokens = block_tokens for
+ *           BF16 pools and 16 (one sub-block of a 256-token block) for Q4G64
+ *           pools.
  * Supported by this build: head_dim 64 or 128; BF16 block_tokens 16;
  * Q4G64 block_tokens 256 with head_dim 128. */
 typedef struct {
@@ -293,11 +295,27 @@ kvs_status kvs_decode_attn_planned(kvs_pool* pool, int32_t layer, const void* q_
                                    void* ws, size_t ws_bytes, cudaStream_t stream);
 
 /* Decode attention reading a Q4G64 pool directly, dequantising in registers
- * ([Q4] §2.2).  Same meaning as kvs_decode_attn without diffs or rotation. */
+ * ([Q4] §2.2), with optional mirror diffs over the Q4 master ([TD] section 3,
+ * Fig. 8: a mirror is the master plus block-sparse K/V differences, restored
+ * inside the read):
+ *   out[a][h] = sum_t softmax_t(scale * <q[a][h], K^_a[t] + DK>) (V^_a[t] + DV)
+ * with K^, V^ the dequantised codes (scale * code + bias) and DK, DV the
+ * agent's diff rows for token t (zero where it has none).  Q4 pools keep
+ * their diffs per 16-token sub-block of a 256-token block (the bf16 pool's
+ * block size, so a refreshed position dirties 16 rows, not 256):
+ * diff_table_dev  int32 [n_seq][max_blocks * 16] (16-byte aligned): entry
+ *               [a][t / 16] is the diff sub-block holding token t's K and V
+ *               differences at row t % 16 of the pool's dk / dv slabs
+ *               (bf16 [diff_capacity_blocks][num_kv_heads][16][head_dim]), or
+ *               -1; NULL for no diffs.  Ids >= diff_capacity_blocks set
+ *               KVS_DEVERR_DIFF_ID and are ignored.
+ * Every finite bf16 query is accepted (each query row is scaled by a power of
+ * two before the fp16 tensor-core products and the factor is folded back
+ * into its scores).  Other arguments as kvs_decode_attn; no rotation. */
 kvs_status kvs_decode_attn_q4(kvs_pool* pool, int32_t layer, const void* q_dev, int32_t n_q_heads,
                               const int32_t* block_table_dev, int32_t max_blocks,
                               const int32_t* seq_len_dev, int32_t n_seq,
-                              float scale, float* out_dev,
+                              const int32_t* diff_table_dev, float scale, float* out_dev,
                               void* ws, size_t ws_bytes, cudaStream_t stream);
 
 /* Quantise bf16 K/V blocks into a Q4G64 pool ([Q4] §2.1).  k_src/v_src are

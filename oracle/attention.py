@@ -41,9 +41,13 @@ def segment_delta_per_block(max_blocks: int, rope_off, rope_segs, a: int) -> np.
 
 def materialise(a: int, seq_len: int, k_pool, v_pool, block_table, block_tokens: int,
                 diff_table=None, dk_pool=None, dv_pool=None,
-                rope_off=None, rope_segs=None, theta: float = 1e4):
-    """Dense fp64 K, V of agent a: [L][Hkv][d]."""
+                rope_off=None, rope_segs=None, theta: float = 1e4, diff_block_tokens=None):
+    """Dense fp64 K, V of agent a: [L][Hkv][d].  Mirror diffs are kept per
+    diff block of diff_block_tokens tokens (default: the pool's block size):
+    diff_table[a, t // diff_block_tokens] names the diff block holding token
+    t's differences at row t % diff_block_tokens."""
     B = block_tokens
+    DB = B if diff_block_tokens is None else diff_block_tokens
     hkv, d = k_pool.shape[1], k_pool.shape[3]
     K = np.zeros((seq_len, hkv, d), dtype=np.float64)
     V = np.zeros((seq_len, hkv, d), dtype=np.float64)
@@ -53,10 +57,11 @@ def materialise(a: int, seq_len: int, k_pool, v_pool, block_table, block_tokens:
         p = int(block_table[a, b])
         k = np.array(k_pool[p, :, o, :], dtype=np.float64)
         v = np.array(v_pool[p, :, o, :], dtype=np.float64)
-        if diff_table is not None and diff_table[a, b] >= 0:
-            q = int(diff_table[a, b])
-            k = k + dk_pool[q, :, o, :]
-            v = v + dv_pool[q, :, o, :]
+        db, do = divmod(t, DB)
+        if diff_table is not None and diff_table[a, db] >= 0:
+            q = int(diff_table[a, db])
+            k = k + dk_pool[q, :, do, :]
+            v = v + dv_pool[q, :, do, :]
         if deltas[b] != 0:
             k = _rope.rotate(k, int(deltas[b]), theta)
         K[t] = k
@@ -77,7 +82,8 @@ def attend(q, K, V, scale: float) -> np.ndarray:
 
 def decode_attention(q, k_pool, v_pool, block_table, seq_len, block_tokens: int, scale: float,
                      diff_table=None, dk_pool=None, dv_pool=None,
-                     rope_off=None, rope_segs=None, theta: float = 1e4, agents=None, heads=None):
+                     rope_off=None, rope_segs=None, theta: float = 1e4, agents=None, heads=None,
+                     diff_block_tokens=None):
     """out [N][Hq][d] fp64 (rows not in ``agents``/``heads`` stay zero)."""
     q = np.asarray(q, dtype=np.float64)
     n, hq, d = q.shape
@@ -87,7 +93,7 @@ def decode_attention(q, k_pool, v_pool, block_table, seq_len, block_tokens: int,
     agents = range(n) if agents is None else agents
     for a in agents:
         K, V = materialise(a, int(seq_len[a]), k_pool, v_pool, block_table, block_tokens,
-                           diff_table, dk_pool, dv_pool, rope_off, rope_segs, theta)
+                           diff_table, dk_pool, dv_pool, rope_off, rope_segs, theta, diff_block_tokens)
         for h in (range(hq) if heads is None else heads):
             out[a, h] = attend(q[a, h], K[:, h // g, :], V[:, h // g, :], scale)
     return out

@@ -152,10 +152,11 @@ kvs_status kvs_pool_create(const kvs_pool_desc* d, void* const* k_layers, void* 
     return fail(KVS_ERR_INVALID_ARG, "pool_create: Q4G64 needs scale/bias slabs");
   if (!q4 && (k_sb_layers || v_sb_layers))
     return fail(KVS_ERR_INVALID_ARG, "pool_create: scale/bias slabs are for Q4G64 pools only");
-  if (d->diff_capacity_blocks > 0 && (!dk_layers || !dv_layers || q4))
-    return fail(KVS_ERR_INVALID_ARG, "pool_create: diff slabs missing (or given for a Q4 pool)");
+  if (d->diff_capacity_blocks > 0 && (!dk_layers || !dv_layers))
+    return fail(KVS_ERR_INVALID_ARG, "pool_create: diff slabs missing");
   const long long rows = static_cast<long long>(d->capacity_blocks) * d->num_kv_heads * d->block_tokens;
-  const long long drows = static_cast<long long>(d->diff_capacity_blocks) * d->num_kv_heads * d->block_tokens;
+  // Q4 pools keep mirror diffs per 16-token sub-block of their 256-token blocks
+  const long long drows = static_cast<long long>(d->diff_capacity_blocks) * d->num_kv_heads * (q4 ? 16 : d->block_tokens);
   if (rows > 0x7FFFFFFFll || drows > 0x7FFFFFFFll)
     return fail(KVS_ERR_CAPACITY, "pool_create: capacity * kv_heads * block_tokens must fit in int32");
 

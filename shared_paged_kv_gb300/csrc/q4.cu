@@ -102,9 +102,17 @@ struct Q4Params {
   float* part_ml;
   int32_t* tickets;
   uint32_t* status;
+  // mirror diffs per 16-token sub-block (nullptr: none): diff_table [n_seq]
+  // [max_blocks * 16] ids into dk / dv bf16 [diff_capacity][hkv][16][128]
+  const int32_t* diff_table;
+  const uint16_t* dk;
+  const uint16_t* dv;
+  int diff_capacity;
   int max_blocks, n_seq, hkv, g, hq, bpc, n_chunks, capacity;
   float scale_log2;
 };
+
+constexpr int kQ4Sub = 16;   // tokens per mirror-diff sub-block (one warp m-tile)
 
 constexpr int kQ4B = 256, kQ4D = 128, kQ4Stages = 2;
 constexpr int kQ4Codes = kQ4B * kQ4D / 2;       // 16 KB per K or V tile
@@ -123,6 +131,94 @@ __device__ __forceinline__ uint32_t movmatrix_t(uint32_t x) {
 __device__ __forceinline__ uint32_t nib_lo_sub(uint32_t w) { return w & 0x000F000Fu; }
 __device__ __forceinline__ uint32_t nib_hi_sub(uint32_t w) { return w & 0x00F000F0u; }
 
+// The 4 diff entries of warp w's sub-blocks of block b (-1 where none; an
+// id beyond the diff capacity is reported and ignored).
+template <bool DIFF>
+__device__ __forceinline__ int4 q4_diff_entries(const Q4Params& p, int a, int b, int warp) {
+  if (!DIFF) return make_int4(-1, -1, -1, -1);
+  int4 e = __ldg(reinterpret_cast<const int4*>(p.diff_table + ((size_t)a * p.max_blocks + b) * (kQ4B / kQ4Sub) + warp * 4));
+  int* v = reinterpret_cast<int*>(&e);
+#pragma unroll
+  for (int k = 0; k < 4; ++k)
+    if (v[k] >= p.diff_capacity) {
+      set_err(p.status, KVS_DEVERR_DIFF_ID);
+      v[k] = -1;
+    }
+  return e;
+}
+
+__device__ __forceinline__ int int4_at(const int4& v, int k) {
+  return k == 0 ? v.x : (k == 1 ? v.y : (k == 2 ? v.z : v.w));
+}
+
+// L2 prefetch of the diff rows (DK and DV, 4 KB each) of the dirty
+// sub-blocks in e, one lane per sub-block, so that the direct loads below
+// find them in L2.
+__device__ __forceinline__ void q4_prefetch_diffs(const Q4Params& p, const int4& e, int h, int lane) {
+  if (lane >= 4) return;
+  const int did = int4_at(e, lane);
+  if (did < 0) return;
+  const size_t off = ((size_t)did * p.hkv + h) * kQ4Sub * kQ4D;
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p.dk + off), "r"(kQ4Sub * kQ4D * 2) : "memory");
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p.dv + off), "r"(kQ4Sub * kQ4D * 2) : "memory");
+}
+
+// q . DK for the 16 tokens of one dirty sub-block (rows g and g + 8, the
+// m-tile's score rows) and query columns (2c, 2c + 1), in bf16 MMAs from the
+// exact bf16 query.  Each 32-dim slice of the head dims feeds two k-steps;
+// the dims are permuted identically for DK and q (thread c takes dims
+// 8c .. 8c + 7 of the slice), so one 16-byte load serves both k-steps.
+__device__ __forceinline__ void q4_diff_scores(const Q4Params& p, int did, int h, int g, int c, int G_,
+                                               const uint16_t* qbase, float* dks) {
+  const uint4* r0 = reinterpret_cast<const uint4*>(p.dk + (((size_t)did * p.hkv + h) * kQ4Sub + g) * kQ4D);
+  const uint4* r1 = r0 + 8 * kQ4D / 8;
+  const uint4* qr = reinterpret_cast<const uint4*>(qbase + (size_t)g * kQ4D);
+#pragma unroll
+  for (int j = 0; j < kQ4D / 32; ++j) {
+    const uint4 x0 = __ldg(r0 + 4 * j + c), x1 = __ldg(r1 + 4 * j + c);
+    const uint4 qq = g < G_ ? __ldg(qr + 4 * j + c) : make_uint4(0u, 0u, 0u, 0u);
+    const uint32_t a0[4] = {x0.x, x1.x, x0.y, x1.y};
+    const uint32_t a1[4] = {x0.z, x1.z, x0.w, x1.w};
+    mma_bf16(dks, a0, qq.x, qq.y);
+    mma_bf16(dks, a1, qq.z, qq.w);
+  }
+}
+
+// P . DV of one dirty sub-block into the O^T accumulators: A = DV^T with the
+// accumulators' row order (row g: head dim 8g + 2lm of the group, row g + 8:
+// the next one; tokens 2c, 2c+1, 2c+8, 2c+9 as k), B = P^T (bf16) through
+// movmatrix.  The accumulator rows carry 2^-24 (even dims) and 2^-20 (odd
+// dims) from the subnormal V codes, so the products are scaled to match.
+__device__ __forceinline__ void q4_diff_values(const Q4Params& p, int did, int h, int g, int c, const float* pv,
+                                               float (*acc)[4]) {
+  const uint32_t pb0 = movmatrix_t(pack_bf16(pv[0], pv[1]));
+  const uint32_t pb1 = movmatrix_t(pack_bf16(pv[2], pv[3]));
+  const uint16_t* vb = p.dv + ((size_t)did * p.hkv + h) * kQ4Sub * kQ4D;
+#pragma unroll
+  for (int grp = 0; grp < 2; ++grp) {
+    const int col = grp * 64 + 8 * g;
+    const uint4 w0 = __ldg(reinterpret_cast<const uint4*>(vb + (2 * c) * kQ4D + col));
+    const uint4 w1 = __ldg(reinterpret_cast<const uint4*>(vb + (2 * c + 1) * kQ4D + col));
+    const uint4 w8 = __ldg(reinterpret_cast<const uint4*>(vb + (2 * c + 8) * kQ4D + col));
+    const uint4 w9 = __ldg(reinterpret_cast<const uint4*>(vb + (2 * c + 9) * kQ4D + col));
+    const uint32_t e0[4] = {w0.x, w0.y, w0.z, w0.w}, e1[4] = {w1.x, w1.y, w1.z, w1.w};
+    const uint32_t e8[4] = {w8.x, w8.y, w8.z, w8.w}, e9[4] = {w9.x, w9.y, w9.z, w9.w};
+#pragma unroll
+    for (int lm = 0; lm < 4; ++lm) {
+      const uint32_t a[4] = {__byte_perm(e0[lm], e1[lm], 0x5410), __byte_perm(e0[lm], e1[lm], 0x7632),
+                             __byte_perm(e8[lm], e9[lm], 0x5410), __byte_perm(e8[lm], e9[lm], 0x7632)};
+      float t[4] = {0.f, 0.f, 0.f, 0.f};
+      mma_bf16(t, a, pb0, pb1);
+      float* ac = acc[grp * 4 + lm];
+      ac[0] = fmaf(t[0], 5.9604644775390625e-8f, ac[0]);   // 2^-24
+      ac[1] = fmaf(t[1], 5.9604644775390625e-8f, ac[1]);
+      ac[2] = fmaf(t[2], 9.5367431640625e-7f, ac[2]);      // 2^-20
+      ac[3] = fmaf(t[3], 9.5367431640625e-7f, ac[3]);
+    }
+  }
+}
+
+template <bool DIFF>
 __global__ void __launch_bounds__(128, 2)
 q4_attn_kernel(const __grid_constant__ Q4Params p, const __grid_constant__ CUtensorMap tk,
                const __grid_constant__ CUtensorMap tv) {
@@ -259,9 +355,21 @@ q4_attn_kernel(const __grid_constant__ Q4Params p, const __grid_constant__ CUten
 #pragma unroll
   for (int i = 0; i < 8; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
 
+  // mirror diffs: this warp's sub-block entries of the current block and of
+  // the next two; the rows of block i + 2's dirty sub-blocks are prefetched
+  // into L2 at the end of block i
+  int4 d_cur = make_int4(-1, -1, -1, -1), d_n1 = d_cur, d_n2 = d_cur;
+  if (DIFF) {
+    if (n_mine > 0) d_cur = q4_diff_entries<DIFF>(p, a, b0, warp);
+    if (n_mine > 1) d_n1 = q4_diff_entries<DIFF>(p, a, b0 + 1, warp);
+    q4_prefetch_diffs(p, d_cur, h, lane);
+    q4_prefetch_diffs(p, d_n1, h, lane);
+  }
+
   bool timed_out = false;
   for (int i = 0; i < n_mine; ++i) {
     const int s = i % kQ4Stages;
+    if (DIFF) d_n2 = i + 2 < n_mine ? q4_diff_entries<DIFF>(p, a, b0 + i + 2, warp) : make_int4(-1, -1, -1, -1);
     if (!mbar_wait_bounded(&full[s], (i / kQ4Stages) & 1, p.status)) {
       timed_out = true;
       break;
@@ -295,6 +403,8 @@ q4_attn_kernel(const __grid_constant__ Q4Params p, const __grid_constant__ CUten
 #pragma unroll
           for (int e = 0; e < 4; ++e) cg[grp][e] = fmaf(ah_[e], 0.0625f, al_[e]);
         }
+        float dks[4] = {0.f, 0.f, 0.f, 0.f};   // q . DK of a dirty sub-block (true units)
+        if (DIFF && int4_at(d_cur, mt) >= 0) q4_diff_scores(p, int4_at(d_cur, mt), h, g, c, G_, qbase, dks);
         const uint2 sb0 = *reinterpret_cast<const uint2*>(ksb + t0 * 8);
         const uint2 sb1 = *reinterpret_cast<const uint2*>(ksb + t1 * 8);
         const float2 g00 = __half22float2(*reinterpret_cast<const __half2*>(&sb0.x));   // (s, b) group 0, t0
@@ -308,7 +418,7 @@ q4_attn_kernel(const __grid_constant__ Q4Params p, const __grid_constant__ CUten
           const float2 s1 = (e < 2) ? g01 : g11;
           float x = s0.x * cg[0][e] + s0.y * qs[0][cc] + s1.x * cg[1][e] + s1.y * qs[1][cc];
           const int tok = (e < 2) ? t0 : t1;
-          sc[mt][e] = tok < nv ? x * colscale[cc] : -INFINITY;
+          sc[mt][e] = tok < nv ? fmaf(dks[e], p.scale_log2, x * colscale[cc]) : -INFINITY;
         }
       }
       // online softmax over this warp's 64 tokens, per query column
@@ -381,7 +491,13 @@ q4_attn_kernel(const __grid_constant__ Q4Params p, const __grid_constant__ CUten
                     bb[grp][0], bb[grp][1]);
           }
         }
+        if (DIFF && int4_at(d_cur, mt) >= 0) q4_diff_values(p, int4_at(d_cur, mt), h, g, c, pv, acc);
       }
+    }
+    if (DIFF) {
+      q4_prefetch_diffs(p, d_n2, h, lane);
+      d_cur = d_n1;
+      d_n1 = d_n2;
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[s]);
@@ -474,8 +590,8 @@ extern "C" kvs_status kvs_quantize_q4(kvs_pool* pool, int32_t layer, const void*
 
 extern "C" kvs_status kvs_decode_attn_q4(kvs_pool* pool, int32_t layer, const void* q_dev, int32_t n_q_heads,
                                          const int32_t* block_table_dev, int32_t max_blocks, const int32_t* seq_len_dev,
-                                         int32_t n_seq, float scale, float* out_dev, void* ws, size_t ws_bytes,
-                                         cudaStream_t stream) {
+                                         int32_t n_seq, const int32_t* diff_table_dev, float scale, float* out_dev,
+                                         void* ws, size_t ws_bytes, cudaStream_t stream) {
   if (!pool) return fail(KVS_ERR_INVALID_ARG, "decode_attn_q4: null pool");
   const kvs_pool_desc& d = pool->desc;
   if (d.dtype != KVS_DTYPE_Q4G64) return fail(KVS_ERR_INVALID_ARG, "decode_attn_q4: pool is not Q4G64");
@@ -486,6 +602,8 @@ extern "C" kvs_status kvs_decode_attn_q4(kvs_pool* pool, int32_t layer, const vo
     return fail(KVS_ERR_INVALID_ARG, "decode_attn_q4: null pointer");
   if (!aligned16(q_dev) || !aligned16(out_dev) || !aligned16(ws))
     return fail(KVS_ERR_INVALID_ARG, "decode_attn_q4: q, out and ws must be 16-byte aligned");
+  if (diff_table_dev && (d.diff_capacity_blocks < 1 || !aligned16(diff_table_dev)))
+    return fail(KVS_ERR_INVALID_ARG, "decode_attn_q4: a diff table needs a pool with diff slabs and 16-byte alignment");
   if (max_blocks < 1) return fail(KVS_ERR_INVALID_ARG, "decode_attn_q4: max_blocks must be >= 1");
   if (n_q_heads < 1 || n_q_heads % d.num_kv_heads) return fail(KVS_ERR_INVALID_ARG, "decode_attn_q4: n_q_heads must be a multiple of num_kv_heads");
   const int g = n_q_heads / d.num_kv_heads;
@@ -508,6 +626,12 @@ extern "C" kvs_status kvs_decode_attn_q4(kvs_pool* pool, int32_t layer, const vo
   prm.part_ml = prm.part + splits * g * kQ4D;
   prm.tickets = pool->tickets;
   prm.status = pool->status;
+  prm.diff_table = diff_table_dev;
+  if (diff_table_dev) {
+    prm.dk = static_cast<const uint16_t*>(pool->dk[layer]);
+    prm.dv = static_cast<const uint16_t*>(pool->dv[layer]);
+    prm.diff_capacity = d.diff_capacity_blocks;
+  }
   prm.max_blocks = max_blocks;
   prm.n_seq = n_seq;
   prm.hkv = d.num_kv_heads;
@@ -517,9 +641,15 @@ extern "C" kvs_status kvs_decode_attn_q4(kvs_pool* pool, int32_t layer, const vo
   prm.n_chunks = plan.n_chunks;
   prm.capacity = d.capacity_blocks;
   prm.scale_log2 = scale * 1.4426950408889634f;
-  if (!smem_limit_once<q4_attn_kernel>(kQ4Smem, pool->device))
-    return fail(KVS_ERR_CUDA, "decode_attn_q4: cannot raise the shared-memory limit");
-  q4_attn_kernel<<<(int)grid, 128, kQ4Smem, stream>>>(prm, pool->tk[layer], pool->tv[layer]);
+  if (diff_table_dev) {
+    if (!smem_limit_once<q4_attn_kernel<true>>(kQ4Smem, pool->device))
+      return fail(KVS_ERR_CUDA, "decode_attn_q4: cannot raise the shared-memory limit");
+    q4_attn_kernel<true><<<(int)grid, 128, kQ4Smem, stream>>>(prm, pool->tk[layer], pool->tv[layer]);
+  } else {
+    if (!smem_limit_once<q4_attn_kernel<false>>(kQ4Smem, pool->device))
+      return fail(KVS_ERR_CUDA, "decode_attn_q4: cannot raise the shared-memory limit");
+    q4_attn_kernel<false><<<(int)grid, 128, kQ4Smem, stream>>>(prm, pool->tk[layer], pool->tv[layer]);
+  }
   count_launch();
   return check_launch("decode_attn_q4");
 }

@@ -102,7 +102,7 @@ def load(path: str = LIB_PATH):
         "kvs_decode_attn": [P, I32, P, I32, P, I32, P, I32, P, P, P, F32, F32, P, P, SZ, P],
         "kvs_decode_attn_planned": [P, I32, P, I32, P, I32, P, I32, P, P, P, F32, F32, P, P, SZ, P],
         "kvs_decode_plan": [P, I32, P, I32, P, I32, P, P, P, P, SZ, P],
-        "kvs_decode_attn_q4": [P, I32, P, I32, P, I32, P, I32, F32, P, P, SZ, P],
+        "kvs_decode_attn_q4": [P, I32, P, I32, P, I32, P, I32, P, F32, P, P, SZ, P],
         "kvs_quantize_q4": [P, I32, P, P, P, I32, P],
         "kvs_workspace_size": [P, I32, I32, I32, I32, ctypes.POINTER(SZ)],
         "kvs_pool_check": [P, P, ctypes.POINTER(U32)],
@@ -312,9 +312,11 @@ def kvs_decode_attn_planned(pool: Pool, layer, q, n_q_heads, block_table, max_bl
 
 
 def kvs_decode_attn_q4(pool: Pool, layer, q, n_q_heads, block_table, max_blocks, seq_len, n_seq,
-                       scale, out, ws, stream=None):
+                       scale, out, ws, stream=None, diff_table=None):
+    """Q4 decode attention; diff_table (int32 [n_seq][max_blocks * 16]) adds
+    the pool's per-16-token mirror diffs."""
     _check(load().kvs_decode_attn_q4(pool.handle, layer, _ptr(q), n_q_heads, _ptr(block_table), max_blocks,
-                                     _ptr(seq_len), n_seq, scale, _ptr(out), _ptr(ws),
+                                     _ptr(seq_len), n_seq, _ptr(diff_table), scale, _ptr(out), _ptr(ws),
                                      ws.numel() * ws.element_size(), _stream(stream)))
 
 

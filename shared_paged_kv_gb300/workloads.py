@@ -76,9 +76,12 @@ class Workload:
     rope_off: Optional[np.ndarray] = None          # int32 [n_seq + 1]
     rope_segs: Optional[np.ndarray] = None         # int32 [n_segs, 4]
     # mirror diffs: diff_table[a, b] = diff block id or -1
-    diff_table: Optional[np.ndarray] = None        # int32 [n_seq, max_blocks]
+    diff_table: Optional[np.ndarray] = None        # int32 [n_seq, max_blocks * block_tokens / diff_block_tokens]
     diff_capacity_blocks: int = 0
     seed: int = 0
+    # tokens per mirror-diff block (0: the pool's block size; Q4 pools keep
+    # their diffs per 16-token sub-block of a 256-token block)
+    diff_block_tokens: int = 0
 
     @property
     def seq_len(self) -> np.ndarray:
@@ -105,7 +108,8 @@ class Workload:
 
     def diff_layer(self, layer: int, sigma: float = 0.1):
         """bf16 bits of the mirror-diff K and V slabs: [diff_cap][Hkv][B][d]."""
-        shape = (max(self.diff_capacity_blocks, 0), self.n_kv_heads, self.block_tokens, self.head_dim)
+        shape = (max(self.diff_capacity_blocks, 0), self.n_kv_heads, self.diff_block_tokens or self.block_tokens,
+                 self.head_dim)
         dk = self._rng(layer, 3).standard_normal(shape, dtype=np.float32) * np.float32(sigma)
         dv = self._rng(layer, 4).standard_normal(shape, dtype=np.float32) * np.float32(sigma)
         return f32_to_bf16_bits(dk), f32_to_bf16_bits(dv)
@@ -234,16 +238,38 @@ def make_allgather(seed: int = 4, n_seq: int = 64, n_segs: int = 64, seg_tokens:
 
 
 def make_q4(seed: int = 5, n_seq: int = 12, ctx: int = 8192, n_layers: int = 32,
-            hq: int = 32, hkv: int = 8, d: int = 128, block: int = 256) -> Workload:
-    """12 agents x 8192 tokens, no sharing, 256-token blocks (Q4 pool)."""
+            hq: int = 32, hkv: int = 8, d: int = 128, block: int = 256, diff_frac: float = 0.0,
+            diff_block: int = 16) -> Workload:
+    """12 agents x 8192 tokens, no sharing, 256-token blocks (Q4 pool).  With
+    diff_frac > 0, each agent gets round(diff_frac * its diff_block-token
+    sub-blocks) mirror-diff sub-blocks, chosen uniformly (the all-gather
+    round's 31 of 512 at 6 %), with diffs ~N(0, 0.1)."""
     rng = np.random.default_rng(seed)
     seqs = [rng.integers(0, 32000, size=ctx, dtype=np.uint32) for _ in range(n_seq)]
     off, toks = _csr(seqs)
     lens = np.diff(off)
     max_blocks = int(-(-lens.max() // block))
     cap = int(sum(-(-int(l) // block) for l in lens))
-    return Workload("q4", n_seq, hq, hkv, d, block, n_layers, 1e4, toks.astype(np.uint32), off,
-                    np.full(n_seq, PRIVATE_TIER, np.uint32), max_blocks, cap, seed=seed)
+    diff_table, nd = None, 0
+    if diff_frac > 0:
+        per = block // diff_block
+        diff_table = np.full((n_seq, max_blocks * per), -1, dtype=np.int32)
+        for a in range(n_seq):
+            n_sub = -(-int(lens[a]) // diff_block)
+            for sb in np.sort(rng.choice(n_sub, size=int(round(diff_frac * n_sub)), replace=False)):
+                diff_table[a, sb] = nd
+                nd += 1
+    return Workload("q4_mirror" if diff_frac > 0 else "q4", n_seq, hq, hkv, d, block, n_layers, 1e4,
+                    toks.astype(np.uint32), off, np.full(n_seq, PRIVATE_TIER, np.uint32), max_blocks, cap,
+                    diff_table=diff_table, diff_capacity_blocks=nd, seed=seed,
+                    diff_block_tokens=diff_block if diff_frac > 0 else 0)
+
+
+def make_q4_mirror(**kw) -> Workload:
+    """The Q4 configuration with mirror diffs on 6 % of every agent's 16-token
+    sub-blocks (31 of 512)."""
+    kw.setdefault("diff_frac", 0.06)
+    return make_q4(**kw)
 
 
 def selection_inputs(seed: int, n_agents: int, rows_per_agent, row_elems: int,

@@ -211,9 +211,19 @@ def q4_pool(w, cap, n_layers=1):
     vs = [torch.zeros_like(ks[0]) for _ in range(n_layers)]
     ksb = [torch.zeros(cap * w.n_kv_heads * w.block_tokens * 4, dtype=torch.float16, device=H.DEV) for _ in range(n_layers)]
     vsb = [torch.zeros_like(ksb[0]) for _ in range(n_layers)]
+    nd = w.diff_capacity_blocks
+    dks = dvs = None
+    if nd:
+        # mirror diffs per 16-token sub-block, from the workload's seeded values
+        dks, dvs = [], []
+        for l in range(n_layers):
+            db, dvb = w.diff_layer(l)
+            dks.append(H.bits_to_dev(db))
+            dvs.append(H.bits_to_dev(dvb))
     pool = K.kvs_pool_create(n_layers, w.n_kv_heads, 128, w.block_tokens, K.KVS_DTYPE_Q4G64, cap, w.n_seq,
-                             ks, vs, ksb, vsb)
+                             ks, vs, ksb, vsb, dk_layers=dks, dv_layers=dvs, diff_capacity_blocks=nd)
     pool.q4 = (ks, vs, ksb, vsb)
+    pool.diffs = (dks, dvs)
     return pool
 
 
@@ -239,8 +249,9 @@ def q4_case(w, sample_agents=None, q_pow2=0):
     n = w.n_seq
     out = torch.full((n, w.n_q_heads, 128), float("nan"), dtype=torch.float32, device=H.DEV)
     ws = H.workspace(K.kvs_workspace_size(pool, K.KVS_OP_DECODE_ATTN_Q4, n, w.max_blocks, w.n_q_heads))
+    dt = H.i32(w.diff_table) if w.diff_table is not None else None
     K.kvs_decode_attn_q4(pool, 0, H.bits_to_dev(q_bits), w.n_q_heads, H.i32(ref["block_table"]), w.max_blocks,
-                         H.i32(w.seq_len), n, scale, out, ws)
+                         H.i32(w.seq_len), n, scale, out, ws, diff_table=dt)
     torch.cuda.synchronize()
     assert K.kvs_pool_check(pool) == 0
     got = out.cpu().numpy().astype(np.float64)
@@ -264,8 +275,12 @@ def q4_case(w, sample_agents=None, q_pow2=0):
         np.testing.assert_array_equal(vsbh[b].view(np.uint16), sb_v.view(np.uint16))
         kd[b] = OQ.dequantize(c_k, sb_k)
         vd[b] = OQ.dequantize(c_v, sb_v)
+    dk_h = dv_h = None
+    if w.diff_table is not None:
+        dk_h, dv_h = (f32(x.cpu().numpy().view(np.uint16)) for x in (pool.diffs[0][0], pool.diffs[1][0]))
     exp = OA.decode_attention(f32(q_bits), kd, vd, ref["block_table"], w.seq_len, w.block_tokens, scale,
-                              agents=agents)
+                              agents=agents, diff_table=w.diff_table, dk_pool=dk_h, dv_pool=dv_h,
+                              diff_block_tokens=w.diff_block_tokens or None)
     sel = list(agents)
     H.assert_close_attn(got[sel], exp[sel])
 
@@ -294,5 +309,26 @@ def test_q4_query_outside_fp16_range():
     q4_case(w, q_pow2=-22)
 
 
-def test_q4_full_size_sampled():
-    q4_case(W.make_q4(n_layers=1), sample_agents=[0, 5, 11])
+def test_q4_full_size_every_pair():
+    q4_case(W.make_q4(n_layers=1))       # 12 agents x 32 heads
+
+
+def test_q4_mirror_small_ragged():
+    # mirror diffs on 16-token sub-blocks of Q4 masters, ragged lengths (the
+    # last block partial, a dirty sub-block past the end of a sequence's
+    # tokens) and a query group of 4
+    w = W.make_q4_mirror(n_seq=3, ctx=700, hq=8, hkv=2, diff_frac=0.2)
+    lens = np.array([700, 256, 513], np.int64)
+    toks = np.concatenate([w.tokens[:700], w.tokens[700:956], w.tokens[1400:1913]])
+    import dataclasses
+    w2 = dataclasses.replace(w, tokens=toks, seq_off=np.concatenate([[0], np.cumsum(lens)]).astype(np.int64))
+    q4_case(w2)
+
+
+def test_q4_mirror_group8():
+    q4_case(W.make_q4_mirror(n_seq=2, ctx=600, hq=16, hkv=2, diff_frac=0.3))
+
+
+def test_q4_mirror_full_size_every_pair():
+    # the Q4 configuration with 31 dirty 16-token sub-blocks of 512 per agent
+    q4_case(W.make_q4_mirror(n_layers=1))

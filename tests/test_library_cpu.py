@@ -55,7 +55,7 @@ def test_host_argument_errors(lib):
     assert lib.kvs_pool_destroy(None) == K.KVS_ERR_INVALID_ARG
     # every compute entry point rejects a null pool on the host
     assert lib.kvs_decode_attn(None, 0, None, 8, None, 1, None, 1, None, None, None, 1.0, 1.0, None, None, 0, None) == K.KVS_ERR_INVALID_ARG
-    assert lib.kvs_decode_attn_q4(None, 0, None, 8, None, 1, None, 1, 1.0, None, None, 0, None) == K.KVS_ERR_INVALID_ARG
+    assert lib.kvs_decode_attn_q4(None, 0, None, 8, None, 1, None, 1, None, 1.0, None, None, 0, None) == K.KVS_ERR_INVALID_ARG
     assert lib.kvs_fingerprint_dedup(None, None, None, 1, None, None, None, None, None, 1, None, None, None, None, None,
                                      0, None, 0, None) == K.KVS_ERR_INVALID_ARG
     assert lib.kvs_rope_rerotate(None, 0, None, 1, 16, 1e4, None, None, 1, None) == K.KVS_ERR_INVALID_ARG

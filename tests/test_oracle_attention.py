@@ -97,6 +97,36 @@ def test_mirror_overlay_equals_dense_mirror():
     np.testing.assert_allclose(o1, o2, atol=1e-13)
 
 
+def test_sub_block_diffs_equal_dense_mirror():
+    # Q4 pools keep mirror diffs per 16-token sub-block of their 256-token
+    # blocks: a diff block smaller than the pool block.  Pool blocks of 8
+    # tokens, diff blocks of 2: the overlay must equal a dense mirror built by
+    # copying the master and adding each diff row by hand.
+    rng = np.random.default_rng(9)
+    B, DB, d = 8, 2, 8
+    k, v = pool(rng, 3, 2, B, d)
+    dk, dv = 0.1 * rng.standard_normal((3, 2, DB, d)), 0.1 * rng.standard_normal((3, 2, DB, d))
+    bt = np.array([[0, 1, 2], [0, 1, -1]], np.int32)
+    dt = np.full((2, 3 * B // DB), -1, np.int32)
+    dt[0, 1], dt[0, 10], dt[1, 7] = 0, 2, 1      # tokens 2-3 and 20-21 of agent 0, 14-15 of agent 1
+    q = rng.standard_normal((2, 4, d))
+    o1 = AT.decode_attention(q, k, v, bt, [23, 16], B, 0.3, diff_table=dt, dk_pool=dk, dv_pool=dv,
+                             diff_block_tokens=DB)
+    k2 = np.concatenate([k, k[0:2], k[2:3]])      # agent 0's mirror blocks 3, 4; agent 1's block 5
+    v2 = np.concatenate([v, v[0:2], v[2:3]])
+    for (blk, row, src) in [(3, 2, 0), (3, 3, 0), (5, 4, 2), (5, 5, 2)]:
+        r = row - 2 if src == 0 else row - 4
+        k2[blk, :, row] += dk[src, :, r]
+        v2[blk, :, row] += dv[src, :, r]
+    k3 = np.concatenate([k2, k[0:2]])              # agent 1's mirror of blocks 0 and 1 -> 6, 7
+    v3 = np.concatenate([v2, v[0:2]])
+    k3[7, :, 6:8] += dk[1]
+    v3[7, :, 6:8] += dv[1]
+    bt2 = np.array([[3, 4, 5], [6, 7, -1]], np.int32)
+    o2 = AT.decode_attention(q, k3, v3, bt2, [23, 16], B, 0.3)
+    np.testing.assert_allclose(o1, o2, atol=1e-13)
+
+
 def test_segment_rotation_collective_equals_per_agent():
     # Collective path: one shared master segment rotated per agent inside the
     # read.  Per-agent path: each agent's materialised copy rotated from the
