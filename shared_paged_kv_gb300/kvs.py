@@ -126,17 +126,26 @@ def _check(st: int):
 
 
 def _ptr(t: Optional[torch.Tensor]):
+    # a plain int: ctypes passes it as the void* argument without a wrapper
     if t is None:
         return None
     if not t.is_contiguous():
         raise ValueError("tensors passed to libkvs must be contiguous")
-    return ctypes.c_void_p(t.data_ptr())
+    return t.data_ptr()
+
+
+_raw_stream = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+_cur_dev = getattr(torch._C, "_cuda_getDevice", None)
 
 
 def _stream(stream=None):
-    if stream is None:
-        stream = torch.cuda.current_stream()
-    return ctypes.c_void_p(stream.cuda_stream)
+    """The cudaStream_t of `stream`, or of torch's current stream on the
+    current device (read without building a Stream object)."""
+    if stream is not None:
+        return stream.cuda_stream
+    if _raw_stream is not None and _cur_dev is not None:
+        return _raw_stream(_cur_dev())
+    return torch.cuda.current_stream().cuda_stream
 
 
 def _ptr_array(ts: Optional[Sequence[torch.Tensor]]):
