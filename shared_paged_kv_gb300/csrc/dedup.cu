@@ -30,6 +30,7 @@
 //     order (deterministic).
 //  6. table: block_table and refcounts.
 //  7. (optional) owner of each id, and the references of each id as a CSR.
+#include <algorithm>
 #include <climits>
 
 #include "common.cuh"
@@ -396,27 +397,30 @@ __global__ void __launch_bounds__(kRefChunks * 32) dedup_refs(DedupParams p) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int n = p.n_seq * p.max_blocks;
   const int cap = p.capacity;
+  // every id in use is below min(capacity, slots): a physical block has at
+  // least one slot, so the per-chunk counts need only that many columns
+  const int ids = min(cap, n);
   const int per = (n + kRefChunks - 1) / kRefChunks;
   const int lo = min(n, warp * per), hi = min(n, lo + per);
-  int32_t* cnt = p.ref_cnt + (size_t)warp * cap;
-  for (int i = threadIdx.x; i < kRefChunks * cap; i += blockDim.x) p.ref_cnt[i] = 0;
+  int32_t* cnt = p.ref_cnt + (size_t)warp * ids;
+  for (int i = threadIdx.x; i < kRefChunks * ids; i += blockDim.x) p.ref_cnt[i] = 0;
   __syncthreads();
   for (int sl = lo + lane; sl < hi; sl += 32) {
     const int id = p.block_table[sl];
-    if (id >= 0 && id < cap) atomicAdd(cnt + id, 1);
+    if (id >= 0 && id < ids) atomicAdd(cnt + id, 1);
   }
   __syncthreads();
   int carry = 0;
-  for (int base = 0; base < cap; base += blockDim.x) {
+  for (int base = 0; base < ids; base += blockDim.x) {
     const int id = base + threadIdx.x;
-    const int c = id < cap ? p.refcount[id] : 0;
+    const int c = id < ids ? p.refcount[id] : 0;
     int total;
     const int pos = block_exclusive_scan(c, warp_sums, total);
-    if (id < cap) {
+    if (id < ids) {
       int run = carry + pos;
       p.ref_off[id] = run;
       for (int k = 0; k < kRefChunks; ++k) {
-        int32_t* e = p.ref_cnt + (size_t)k * cap + id;
+        int32_t* e = p.ref_cnt + (size_t)k * ids + id;
         const int ck = *e;
         *e = run;
         run += ck;
@@ -424,13 +428,13 @@ __global__ void __launch_bounds__(kRefChunks * 32) dedup_refs(DedupParams p) {
     }
     carry += total;
   }
-  if (threadIdx.x == 0) p.ref_off[cap] = carry;
+  for (int id = ids + threadIdx.x; id <= cap; id += blockDim.x) p.ref_off[id] = carry;   // unused ids, and the end
   __syncthreads();
   const unsigned lt = (1u << lane) - 1u;
   for (int base = lo; base < hi; base += 32) {
     const int sl = base + lane;
     const int id = sl < hi ? p.block_table[sl] : -1;
-    const bool ok = id >= 0 && id < cap;
+    const bool ok = id >= 0 && id < ids;
     const unsigned m = __match_any_sync(0xffffffffu, ok ? id : -1);
     const int leader = __ffs(m) - 1;
     const int first = (ok && lane == leader) ? cnt[id] : 0;
@@ -487,7 +491,7 @@ extern "C" kvs_status kvs_fingerprint_dedup(kvs_pool* pool, const uint32_t* toke
   p.flags = reinterpret_cast<uint32_t*>(take(16));
   const int n_tiles = static_cast<int>((slots + kNumTile - 1) / kNumTile);
   p.tile_cnt = reinterpret_cast<int32_t*>(take((size_t)n_tiles * 4));
-  p.ref_cnt = reinterpret_cast<int32_t*>(take((size_t)kRefChunks * pool->desc.capacity_blocks * 4));
+  p.ref_cnt = reinterpret_cast<int32_t*>(take((size_t)kRefChunks * std::min<size_t>(pool->desc.capacity_blocks, slots) * 4));
   p.tokens = tokens_dev;
   p.seq_off = seq_off_dev;
   p.tier = tier_dev;

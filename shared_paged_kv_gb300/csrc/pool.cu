@@ -1,5 +1,6 @@
 // libkvs host side: pool lifetime, TMA tensor maps, workspace sizing, status
 // and statistics.  No kernels of the hot path live here.
+#include <algorithm>
 #include <atomic>
 #include <cmath>
 #include <cstring>
@@ -294,8 +295,9 @@ kvs_status kvs_workspace_size(const kvs_pool* p, int32_t op, int32_t n_seq, int3
       const size_t slots = static_cast<size_t>(n_seq) * max_blocks;
       size_t t = 1024;
       while (t < 2 * slots) t <<= 1;
-      // + per-chunk reference counts of the optional CSR (32 x capacity)
-      b = t * 16 + slots * (8 + 4 + 4 + 4 + 4) + 64 * 1024 + 256 + 32ull * p->desc.capacity_blocks * 4 + 256;
+      // + per-chunk reference counts of the optional CSR (32 x min(capacity, slots))
+      b = t * 16 + slots * (8 + 4 + 4 + 4 + 4) + 64 * 1024 + 256 +
+          32ull * std::min<size_t>(p->desc.capacity_blocks, slots) * 4 + 256;
       break;
     }
     case KVS_OP_DECODE_ATTN:

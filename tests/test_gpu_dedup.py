@@ -85,6 +85,14 @@ def test_empty_and_short_sequences():
     assert (got["block_table"][0] == -1).all() and (got["block_table"][4] == -1).all()
 
 
+def test_pool_filled_exactly():
+    # a pool whose capacity is exactly the number of physical blocks: no error
+    w = W.make_gqa_fanout(n_seq=5, prefix_tokens=96, priv_lo=10, priv_hi=70, hq=4, hkv=2, d=64)
+    n = OF.dedup(w.tokens, w.seq_off, w.tier, w.block_tokens, w.max_blocks)["n_phys"]
+    got, ref = check(w, capacity=n)
+    assert got["n_phys"] == n and (got["owner"] >= 0).all()
+
+
 def test_too_long_sequence_is_flagged():
     w = W.make_gqa_fanout(n_seq=3, prefix_tokens=64, priv_lo=10, priv_hi=20, hq=4, hkv=2, d=64)
     w.max_blocks -= 1      # the longest sequence no longer fits its table row

@@ -169,6 +169,21 @@ def test_select_small():
     check_selection(kc, kn, off, 0.15, gi, go)
 
 
+def test_select_max_rows_and_malformed_offsets():
+    # one agent at the 65,536-row limit
+    kc, kn, off = W.selection_inputs(3, 1, [65536], 64)
+    gi, go = select_case(kc, kn, off, 0.01, 65536)
+    check_selection(kc, kn, off, 0.01, gi, go)
+    # offsets that decrease (that agent selects nothing) and overlap (an agent
+    # whose rows start inside its predecessor's): the oracle's slices of the
+    # same offsets define both
+    kc, kn, _ = W.selection_inputs(4, 3, [100, 50, 150], 64)
+    off2 = np.array([0, 100, 50, 200], np.int64)
+    gi, go = select_case(kc, kn, off2, 0.2, 150)
+    assert go[2] == go[1]
+    check_selection(kc, kn, off2, 0.2, gi, go)
+
+
 def test_select_ties_and_ratio_edges():
     rows = [10, 10]
     kc = np.zeros((20, 16), np.uint16)
@@ -227,7 +242,7 @@ def q4_pool(w, cap, n_layers=1):
     return pool
 
 
-def q4_case(w, sample_agents=None, q_pow2=0):
+def q4_case(w, sample_agents=None, q_pow2=0, gpu_diff_table=None, expect_flags=0):
     """Source bf16 K/V per physical block -> GPU quantiser; the oracle
     quantises the same source values itself and must match bit for bit; then
     Q4 attention vs the oracle on its dequantised values.  q_pow2 multiplies
@@ -249,11 +264,12 @@ def q4_case(w, sample_agents=None, q_pow2=0):
     n = w.n_seq
     out = torch.full((n, w.n_q_heads, 128), float("nan"), dtype=torch.float32, device=H.DEV)
     ws = H.workspace(K.kvs_workspace_size(pool, K.KVS_OP_DECODE_ATTN_Q4, n, w.max_blocks, w.n_q_heads))
-    dt = H.i32(w.diff_table) if w.diff_table is not None else None
+    gdt = w.diff_table if gpu_diff_table is None else gpu_diff_table
+    dt = H.i32(gdt) if gdt is not None else None
     K.kvs_decode_attn_q4(pool, 0, H.bits_to_dev(q_bits), w.n_q_heads, H.i32(ref["block_table"]), w.max_blocks,
                          H.i32(w.seq_len), n, scale, out, ws, diff_table=dt)
     torch.cuda.synchronize()
-    assert K.kvs_pool_check(pool) == 0
+    assert K.kvs_pool_check(pool) == expect_flags
     got = out.cpu().numpy().astype(np.float64)
     ks, vs, ksb, vsb = pool.q4
     agents = range(n) if sample_agents is None else sample_agents
@@ -327,6 +343,29 @@ def test_q4_mirror_small_ragged():
 
 def test_q4_mirror_group8():
     q4_case(W.make_q4_mirror(n_seq=2, ctx=600, hq=16, hkv=2, diff_frac=0.3))
+
+
+def test_q4_edge_lengths_with_and_without_diffs():
+    # empty context (zeros), one token, exactly one block, a partial second block
+    import dataclasses
+    for frac in (0.0, 0.25):
+        w = W.make_q4(n_seq=4, ctx=300, hq=8, hkv=2, diff_frac=frac)
+        lens = np.array([0, 1, 256, 300], np.int64)
+        toks = np.concatenate([w.tokens[300:301], w.tokens[600:856], w.tokens[900:1200]])
+        q4_case(dataclasses.replace(w, tokens=toks, seq_off=np.concatenate([[0], np.cumsum(lens)]).astype(np.int64)))
+
+
+def test_q4_bad_diff_id_is_flagged_and_ignored():
+    # an id beyond the diff capacity sets KVS_DEVERR_DIFF_ID and that
+    # sub-block is read as the master alone (the oracle with the entry at -1)
+    w = W.make_q4_mirror(n_seq=2, ctx=512, hq=8, hkv=2, diff_frac=0.1)
+    a, sb = np.argwhere(w.diff_table >= 0)[0]
+    bad = w.diff_table.copy()
+    bad[a, sb] = w.diff_capacity_blocks + 5
+    import dataclasses
+    ok = w.diff_table.copy()
+    ok[a, sb] = -1
+    q4_case(dataclasses.replace(w, diff_table=ok), gpu_diff_table=bad, expect_flags=K.KVS_DEVERR_DIFF_ID)
 
 
 def test_q4_mirror_full_size_every_pair():
