@@ -66,7 +66,7 @@ struct DedupParams {
   int32_t* pid;       // per slot physical id of first occurrences
   uint32_t* flags;    // [0] collision
   int32_t* tile_cnt;  // first occurrences per numbering tile
-  int32_t* ref_cnt;   // [kRefChunks][capacity] per-chunk reference counts, then starts
+  int32_t* ref_cnt;   // [kRefChunks][min(capacity, slots)] per-chunk reference counts, then starts
   int n_seq, max_blocks, B, capacity, weak;
   uint32_t tmask;
 };
@@ -403,7 +403,7 @@ __global__ void __launch_bounds__(kRefChunks * 32) dedup_refs(DedupParams p) {
   const int per = (n + kRefChunks - 1) / kRefChunks;
   const int lo = min(n, warp * per), hi = min(n, lo + per);
   int32_t* cnt = p.ref_cnt + (size_t)warp * ids;
-  for (int i = threadIdx.x; i < kRefChunks * ids; i += blockDim.x) p.ref_cnt[i] = 0;
+  for (long long i = threadIdx.x; i < (long long)kRefChunks * ids; i += blockDim.x) p.ref_cnt[i] = 0;
   __syncthreads();
   for (int sl = lo + lane; sl < hi; sl += 32) {
     const int id = p.block_table[sl];
