@@ -64,6 +64,9 @@ def parse():
     ap.add_argument("--workload", default="mha7b",
                     choices=["mha7b"] + EXTRA_CONFIGS + ["cow", "evict", "io"],
                     help="mha7b is the headline workload; the others print one record")
+    ap.add_argument("--trace", action="store_true",
+                    help="with --workload: add the kernels' start/end times of one CUDA-graph replay "
+                         "(torch.profiler CUDA activity trace) to the record")
     ap.add_argument("--cpu-oracle", nargs=3, type=int, metavar=("LAYERS", "REPS", "PAIRS"),
                     help=argparse.SUPPRESS)
     return ap.parse_args()
@@ -309,10 +312,10 @@ def main():
     from shared_paged_kv_gb300 import kvs as K
     from shared_paged_kv_gb300 import workloads as W
 
-    if args.workload != "mha7b":
+    if args.workload != "mha7b" or args.trace:
         dev = torch.device("cuda", 0)
         torch.cuda.set_device(dev)
-        rec = run_extra(args.workload, torch, K, W, dev, args.steps, args.warmup, args.layers)
+        rec = run_extra(args.workload, torch, K, W, dev, args.steps, args.warmup, args.layers, trace=args.trace)
         print(json.dumps(rec))
         return 0
 
@@ -494,6 +497,7 @@ def main():
 # --------------------------------------------------------- other workloads --
 # name -> (dominant kernels, committed ncu summary, workload description)
 CONFIG_INFO = {
+    "mha7b": ("attn_tm_kernel<128,0,0>, then tm_merge_kernel<128>", "profiles/attn_bf16_mha7b.md", WORKLOAD),
     "tiny": ("attn_tm_kernel<64,1,0> + tm_merge_kernel<64> (latency-bound)", None,
              "tiny: 4 agents, 1 layer, 8 q / 2 kv heads, d 64, 256-token shared prefix + 64-128 private, "
              "2 mirror-diff blocks per agent"),
@@ -541,7 +545,45 @@ def graph_replay_ms(torch, fn, reps, flush):
     return sum(a.elapsed_time(b) for a, b in ev) / reps
 
 
-def run_extra(name, torch, K, W, dev, steps, warmup, layers):
+def graph_timeline(torch, fn, tag):
+    """Kernel start/end times (microseconds from the first kernel) of one
+    replay of fn captured in a CUDA graph, from torch.profiler's CUDA
+    activity trace: the real overlap of the kernels, which a serialising
+    profiler does not show."""
+    import tempfile
+    from torch.profiler import ProfilerActivity, profile
+    g = torch.cuda.CUDAGraph()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        fn()
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    with torch.cuda.graph(g):
+        fn()
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize()
+    # the first profiling session of a process records no kernel activity
+    # here: run one to set the tracer up, then the one that is kept
+    for _ in range(2):
+        with profile(activities=[ProfilerActivity.CUDA]) as prof:
+            g.replay()
+            torch.cuda.synchronize()
+    path = os.path.join(tempfile.gettempdir(), f"kvs_trace_{tag}_{os.getpid()}.json")
+    prof.export_chrome_trace(path)
+    with open(path) as f:
+        ev = json.load(f)["traceEvents"]
+    os.remove(path)
+    ks = sorted((e for e in ev if e.get("cat") == "kernel" and "dur" in e), key=lambda e: e["ts"])
+    if not ks:
+        return []
+    t0 = ks[0]["ts"]
+    return [[e["name"].split("(")[0].replace("void ", "").replace("kvs::", ""), round(e["ts"] - t0, 2),
+             round(e["ts"] + e["dur"] - t0, 2)] for e in ks]
+
+
+def run_extra(name, torch, K, W, dev, steps, warmup, layers, trace=False):
     stream = torch.cuda.current_stream()
     if name == "select":
         return bench_select(torch, K, dev, stream, steps, warmup)
@@ -553,7 +595,7 @@ def run_extra(name, torch, K, W, dev, steps, warmup, layers):
         return bench_evict(torch, K, dev, steps)
     if name == "io":
         return bench_io(torch, K, W, dev, steps)
-    return workload_record(name, torch, K, W, dev, stream, steps, warmup, layers)
+    return workload_record(name, torch, K, W, dev, stream, steps, warmup, layers, trace)
 
 
 def bench_select(torch, K, dev, stream, steps, warmup):
@@ -642,11 +684,11 @@ def bench_tiny_replicated(torch, K, W, dev, reps, flush, n_inst=4096):
             "timing": "CUDA graph of plan + attention, L2 flushed before every replay", "status_flags": flags}
 
 
-def workload_record(name, torch, K, W, dev, stream, steps, warmup, layers):
+def workload_record(name, torch, K, W, dev, stream, steps, warmup, layers, trace=False):
     """GPU dedup + plan + decode attention on every layer (Q4: attention only),
     eager through the public API and replayed from CUDA graphs."""
     mk = {"tiny": W.make_tiny, "gqa_fanout": W.make_gqa_fanout, "allgather": W.make_allgather, "q4": W.make_q4,
-          "q4_mirror": W.make_q4_mirror}
+          "q4_mirror": W.make_q4_mirror, "mha7b": W.make_mha7b}
     w = mk[name]()
     L = layers or w.n_layers
     N, H, D, B = w.n_seq, w.n_kv_heads, w.head_dim, w.block_tokens
@@ -780,6 +822,10 @@ def workload_record(name, torch, K, W, dev, stream, steps, warmup, layers):
                      "attn_gbs": gbs(g_attn), "frac": gbs(g_attn) / peak,
                      "timing": "CUDA graph replays, L2 flushed before every replay"},
            "status_flags": flags | K.kvs_pool_check(pool)}
+    if trace:
+        rec["timeline"] = {"what": "kernel [name, start_us, end_us] of one CUDA-graph replay of every layer's "
+                                   "attention call (torch.profiler CUDA activity trace)",
+                           "kernels": graph_timeline(torch, lambda: [attn(l) for l in range(L)], name)}
     if name == "tiny":
         rec["eager"]["l2"] = "the 0.43 MB working set stays in L2 between eager steps"
         rec["tiny_x4096"] = bench_tiny_replicated(torch, K, W, dev, steps, flush)
