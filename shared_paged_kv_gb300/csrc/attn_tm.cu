@@ -668,6 +668,13 @@ struct TmParams {
   int compact;            // private items over plist (rotation calls on the wide tile)
   int max_blocks, n_seq, hkv, g, hq, ib, n_chunks, ibs, n_chunks_s, R, SG, capacity, diff_capacity;
   int mwpr;           // merge warps per output row
+  // the merge prefetches every split slot's data into L2 before its wait:
+  // worth it when its CTAs become resident long before the attention grid
+  // completes (no wide tile beside it: on the 7B layer 161.8-162.1 us against
+  // 164.9-165.1 us per layer), not behind the wide tile, where they start
+  // about 1 us before the end and the lines of slots without a split would
+  // only compete with the reads (GQA fan-out 21.2 against 20.7 us)
+  int merge_prefetch;
   // Rotation calls: the token-major grid starts beside the wide tile on the
   // SMs it leaves free and its other CTAs start as the tile finishes, so
   // claims are taken in turn from a per-pool counter (dyn), one claim ahead;
@@ -693,6 +700,13 @@ struct TmRec {
   int len[kTmMaxGroup];    // context lengths: of each member (shared), of the sequence in len[0] (private)
   int pad[4];
 };
+
+// the plan was built for this call's shapes (every compare evaluated, no
+// short circuit)
+__device__ __forceinline__ bool tm_plan_ok(const PlanHdr& h, const TmParams& p) {
+  return (h.v[1] == kPlanMagic) & (h.v[2] == p.n_seq) & (h.v[3] == p.max_blocks) & (h.v[4] == p.R) &
+         (h.v[5] == p.ib) & (h.v[6] == p.hkv) & (h.v[7] == p.SG) & (h.v[9] == p.ibs) & (h.v[11] == p.compact);
+}
 
 __device__ __forceinline__ uint32_t movm_t(uint32_t x) {
   uint32_t y;
@@ -728,6 +742,14 @@ attn_tm_kernel(const __grid_constant__ TmParams p, const __grid_constant__ CUten
   // a merge kernel queued behind this one (programmatic dependent launch) may
   // be scheduled now; it waits for this grid to complete before reading
   asm volatile("griddepcontrol.launch_dependents;");
+  if (threadIdx.x == 0) {
+    prefetch_tmap(&tk);
+    prefetch_tmap(&tv);
+    if (DIFF) {
+      prefetch_tmap(&tdk);
+      prefetch_tmap(&tdv);
+    }
+  }
   uint8_t* base = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   uint8_t* wbase = base + warp * S * STAGE;
   const uint32_t wbase_u32 = smem_u32(wbase);
@@ -743,11 +765,10 @@ attn_tm_kernel(const __grid_constant__ TmParams p, const __grid_constant__ CUten
   __syncwarp();
 
   // the plan must have been built for this call's shapes
-  const bool plan_ok = p.hdr[1] == kPlanMagic && p.hdr[2] == p.n_seq && p.hdr[3] == p.max_blocks &&
-                       p.hdr[4] == p.R && p.hdr[5] == p.ib && p.hdr[6] == p.hkv && p.hdr[7] == p.SG &&
-                       p.hdr[9] == p.ibs && p.hdr[11] == p.compact;
+  const PlanHdr ph = load_plan_hdr(p.hdr);
+  const bool plan_ok = tm_plan_ok(ph, p);
   if (!plan_ok && threadIdx.x == 0 && blockIdx.x == 0) set_err(p.status, KVS_DEVERR_PLAN);
-  const int n_claims = plan_ok ? p.hdr[0] * p.hkv : 0;
+  const int n_claims = plan_ok ? ph.v[0] * p.hkv : 0;
   const int R = p.R;
 
   // ------------------------------------------ producer state (warp-uniform)
@@ -1208,14 +1229,6 @@ attn_tm_kernel(const __grid_constant__ TmParams p, const __grid_constant__ CUten
   asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
-// Split merge: p.mwpr warps (1, 2, 4 or 8) per (sequence, query head) row,
-// eight warps per CTA.  A row's splits sit in "slots": the private split of
-// each chunk, then (with sharing groups) the shared split of each chunk.
-// Each warp takes a fixed range of slots: one pass loads their (m, l) (one
-// slot per lane), a second loads the existing splits of the range
-// kMergeBatch at a time (each lane a D/32 slice), and the warps' partial
-// states combine through shared memory.  The partition and the order are fixed, so
-// the result does not depend on which warp computed which split.
 constexpr int kMergeWarps = 8;
 #ifndef KVS_MERGE_SLOTS_PER_WARP
 #define KVS_MERGE_SLOTS_PER_WARP 64
@@ -1233,14 +1246,23 @@ constexpr int kMergeWarps = 8;
 #endif
 constexpr int kMergeBatch = KVS_MERGE_BATCH;
 
+// Split merge, interleaved form.  The row's splits are dealt out round
+// robin: warp wq of the row takes slots wq, wq + wpr, wq + 2 wpr, ...
+// Existing splits sit in runs of consecutive slots (a sequence's chunks with
+// unshared work, the chunks of its shared prefix), so every warp gets about
+// the same number of them and loads them in one batch.  Each warp reads the
+// (m, l) of every slot of the row to find the row's maximum M itself (all
+// those 8-byte loads in flight together, with the (m, l) of its own slots),
+// so the warps' parts are relative to the same M and combine by plain sums
+// in a fixed order.
+constexpr int kMergeWin = 4;   // 32-slot windows whose loads are issued together
+
 template <int D>
-__global__ void __launch_bounds__(kMergeWarps * 32, KVS_MERGE_MIN_CTAS) tm_merge_kernel(const __grid_constant__ TmParams p) {
-  asm volatile("griddepcontrol.wait;" ::: "memory");
-  // the token-major grid has completed: its claim counter starts the next call at zero
-  if (p.dyn && blockIdx.x == 0 && threadIdx.x == 0) *p.claim_ctr = 0u;
+__global__ void __launch_bounds__(kMergeWarps * 32, KVS_MERGE_MIN_CTAS)
+tm_merge_kernel(const __grid_constant__ TmParams p) {
   constexpr int CPL = D / 32;   // columns per lane
-  __shared__ float sM[kMergeWarps], sL[kMergeWarps];
   __shared__ __align__(16) float sv[kMergeWarps][D];
+  __shared__ float sL[kMergeWarps];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int wpr = p.mwpr;
   const int rl = warp / wpr, wq = warp - rl * wpr;
@@ -1248,67 +1270,75 @@ __global__ void __launch_bounds__(kMergeWarps * 32, KVS_MERGE_MIN_CTAS) tm_merge
   const bool in_range = row < p.n_seq * p.hq;
   const int a = in_range ? row / p.hq : 0, qh = row - a * p.hq, h = qh / p.g, hh = qh - h * p.g;
   const size_t sbase = ((size_t)a * p.hkv + h) * p.n_chunks, sbase_s = ((size_t)a * p.hkv + h) * p.n_chunks_s;
-  const int n_slots = p.n_chunks + (p.SG > 1 ? p.n_chunks_s : 0);
-  const int spw = (n_slots + wpr - 1) / wpr;
-  const int sbeg = wq * spw, send = in_range ? min(n_slots, sbeg + spw) : sbeg;
+  const int n_slots = in_range ? p.n_chunks + (p.SG > 1 ? p.n_chunks_s : 0) : 0;
   auto slot_off = [&](int sl) {   // split index of a slot
     return sl < p.n_chunks ? (sbase + sl) * p.g + hh : (sbase_s + (sl - p.n_chunks)) * p.g + hh;
   };
-  // the attention kernel has flagged a plan built for other shapes and
-  // computed nothing; leave the output untouched as well (the header loads
-  // go out together with the first (m, l) loads)
-  const bool plan_ok = p.hdr[1] == kPlanMagic && p.hdr[2] == p.n_seq && p.hdr[3] == p.max_blocks &&
-                       p.hdr[4] == p.R && p.hdr[5] == p.ib && p.hdr[6] == p.hkv && p.hdr[7] == p.SG &&
-                       p.hdr[9] == p.ibs && p.hdr[11] == p.compact;
-
-  // lane k owns slot w0 + k of each 32-slot window of this warp's range; the
-  // first window keeps its (m, l) in registers between the passes.  The plan
-  // set the (m, l) of splits that no item writes to (-inf, 0), so a split
-  // exists exactly when its l is positive.
-  auto own = [&](int w0, float2& ml) {
-    const int sl = w0 + lane;
-    ml = make_float2(0.f, 0.f);
-    if (sl < send) {
-      const float* base = sl >= p.n_chunks ? p.p2_ml : p.p1_ml;
-      ml = __ldcg(reinterpret_cast<const float2*>(base + slot_off(sl) * 2));
+  // Before the wait: this CTA is often resident well before the attention
+  // grid completes, and what it reads below has usually left L2 (the (m, l)
+  // of splits that no item writes were set by the plan once per step; early
+  // splits were written long ago).  It fetches its row's lines into L2: every
+  // slot's (m, l) line and, when the launch asks for it (p.merge_prefetch),
+  // every slot's data.  A prefetch returns nothing to this program, and L2
+  // is where every write lands, so everything is read after the wait and is
+  // correct.
+  for (int sl = wq + lane * wpr; sl < n_slots; sl += 32 * wpr) {
+    asm volatile("prefetch.global.L2 [%0];" ::"l"((sl >= p.n_chunks ? p.p2_ml : p.p1_ml) + slot_off(sl) * 2));
+    if (p.merge_prefetch) {
+      const char* src = reinterpret_cast<const char*>((sl >= p.n_chunks ? p.p2 : p.p1) + slot_off(sl) * D);
+#pragma unroll
+      for (int j = 0; j < D * 4; j += 128) asm volatile("prefetch.global.L2 [%0];" ::"l"(src + j));
     }
+  }
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  // the token-major grid has completed: its claim counter starts the next call at zero
+  if (p.dyn && blockIdx.x == 0 && threadIdx.x == 0) *p.claim_ctr = 0u;
+  // a plan built for other shapes: the attention kernel computed nothing and
+  // flagged it; the output is left untouched as well
+  const bool plan_ok = tm_plan_ok(load_plan_hdr(p.hdr), p);
+  // The plan set the (m, l) of splits that no item writes to (-inf, 0), so a
+  // split exists exactly when its l is positive.
+  auto load_ml = [&](int sl) {
+    if (sl >= n_slots) return make_float2(-INFINITY, 0.f);
+    const float* base = sl >= p.n_chunks ? p.p2_ml : p.p1_ml;
+    return __ldcg(reinterpret_cast<const float2*>(base + slot_off(sl) * 2));
   };
-  float2 ml0 = make_float2(0.f, 0.f);
+
+  // 1. M of the row; the (m, l) of this lane's own slots in the first two
+  // passes come along
+  const float2 own0 = load_ml(lane * wpr + wq), own1 = load_ml(32 * wpr + lane * wpr + wq);
   float M = -INFINITY;
-  for (int w0 = sbeg; w0 < send; w0 += 32) {
-    float2 ml;
-    own(w0, ml);
-    if (ml.y > 0.f) M = fmaxf(M, ml.x);
-    if (w0 == sbeg) ml0 = ml;
+  for (int w0 = 0; w0 < n_slots; w0 += 32 * kMergeWin) {
+    float2 ml[kMergeWin];
+#pragma unroll
+    for (int k = 0; k < kMergeWin; ++k) ml[k] = load_ml(w0 + k * 32 + lane);
+#pragma unroll
+    for (int k = 0; k < kMergeWin; ++k)
+      if (ml[k].y > 0.f) M = fmaxf(M, ml[k].x);
   }
 #pragma unroll
   for (int off = 16; off; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
-  float Ls = 0.f, v[CPL];
+
+  // 2. this warp's slots, 32 per pass (lane k: slot base + k * wpr + wq)
+  float v[CPL], Lw = 0.f;
 #pragma unroll
   for (int j = 0; j < CPL; ++j) v[j] = 0.f;
-  for (int w0 = sbeg; w0 < send; w0 += 32) {
-    float2 ml;
-    if (w0 == sbeg) ml = ml0; else own(w0, ml);
+  for (int base = 0; base < n_slots; base += 32 * wpr) {
+    const int sl = base + lane * wpr + wq;
+    const float2 ml = base == 0 ? own0 : base == 32 * wpr ? own1 : load_ml(sl);
     const bool ex = ml.y > 0.f;
     const float wk = ex ? fast_exp2(ml.x - M) : 0.f;
-    Ls += wk * ml.y;
+    Lw += wk * ml.y;
     unsigned mk = __ballot_sync(0xffffffffu, ex);
-    while (mk) {   // warp-uniform
-      int idx[kMergeBatch];
-#pragma unroll
-      for (int u = 0; u < kMergeBatch; ++u) {
-        idx[u] = -1;
-        if (mk) {
-          idx[u] = __ffs(mk) - 1;
-          mk &= mk - 1;
-        }
-      }
+    while (mk) {   // warp-uniform: up to kMergeBatch splits, their loads all in flight
       float x[kMergeBatch][CPL];
+      unsigned mq = mk;
 #pragma unroll
       for (int u = 0; u < kMergeBatch; ++u) {
-        if (idx[u] < 0) continue;
-        const int sl = w0 + idx[u];
-        const float* src = (sl >= p.n_chunks ? p.p2 : p.p1) + slot_off(sl) * D + lane * CPL;
+        if (!mq) continue;
+        const int s2 = base + (__ffs(mq) - 1) * wpr + wq;
+        mq &= mq - 1;
+        const float* src = (s2 >= p.n_chunks ? p.p2 : p.p1) + slot_off(s2) * D + lane * CPL;
         if (CPL == 4) {
           const float4 t = __ldcg(reinterpret_cast<const float4*>(src));
           x[u][0] = t.x; x[u][1 % CPL] = t.y; x[u][2 % CPL] = t.z; x[u][3 % CPL] = t.w;
@@ -1319,50 +1349,38 @@ __global__ void __launch_bounds__(kMergeWarps * 32, KVS_MERGE_MIN_CTAS) tm_merge
       }
 #pragma unroll
       for (int u = 0; u < kMergeBatch; ++u) {
-        if (idx[u] < 0) continue;
-        const float wgt = __shfl_sync(0xffffffffu, wk, idx[u]);
+        if (!mk) continue;
+        const float wgt = __shfl_sync(0xffffffffu, wk, __ffs(mk) - 1);
+        mk &= mk - 1;
 #pragma unroll
         for (int j = 0; j < CPL; ++j) v[j] += wgt * x[u][j];
       }
     }
   }
 #pragma unroll
-  for (int off = 16; off; off >>= 1) Ls += __shfl_xor_sync(0xffffffffu, Ls, off);
-  float* o = p.out + (size_t)row * D + lane * CPL;
-  float Mt = M, Lt = Ls, r[CPL];
-#pragma unroll
-  for (int j = 0; j < CPL; ++j) r[j] = v[j];
+  for (int off = 16; off; off >>= 1) Lw += __shfl_xor_sync(0xffffffffu, Lw, off);
+
+  // 3. the row's warps add their parts in order; its first warp stores
   if (wpr > 1) {
-    if (lane == 0) {
-      sM[warp] = M;
-      sL[warp] = Ls;
-    }
 #pragma unroll
     for (int j = 0; j < CPL; ++j) sv[warp][lane * CPL + j] = v[j];
+    if (lane == 0) sL[warp] = Lw;
     __syncthreads();
     if (wq != 0) return;
-    const int w0 = rl * wpr;
-    Mt = -INFINITY;
-    for (int w = 0; w < wpr; ++w)
-      if (sL[w0 + w] > 0.f) Mt = fmaxf(Mt, sM[w0 + w]);
-    Lt = 0.f;
+    for (int w = 1; w < wpr; ++w) {
 #pragma unroll
-    for (int j = 0; j < CPL; ++j) r[j] = 0.f;
-    for (int w = 0; w < wpr; ++w) {
-      const float lw = sL[w0 + w];
-      const float wt = lw > 0.f ? fast_exp2(sM[w0 + w] - Mt) : 0.f;
-      Lt += wt * lw;
-#pragma unroll
-      for (int j = 0; j < CPL; ++j) r[j] += wt * sv[w0 + w][lane * CPL + j];
+      for (int j = 0; j < CPL; ++j) v[j] += sv[warp + w][lane * CPL + j];
+      Lw += sL[warp + w];
     }
   }
   if (!in_range || !plan_ok) return;
   // an empty context (no splits at all) gives a zero output
-  const float inv = Lt > 0.f ? 1.f / Lt : 0.f;
+  const float inv = Lw > 0.f ? 1.f / Lw : 0.f;
+  float* o = p.out + (size_t)row * D + lane * CPL;
   if (CPL == 4) {
-    *reinterpret_cast<float4*>(o) = make_float4(r[0] * inv, r[1 % CPL] * inv, r[2 % CPL] * inv, r[3 % CPL] * inv);
+    *reinterpret_cast<float4*>(o) = make_float4(v[0] * inv, v[1 % CPL] * inv, v[2 % CPL] * inv, v[3 % CPL] * inv);
   } else {
-    *reinterpret_cast<float2*>(o) = make_float2(r[0] * inv, r[1 % CPL] * inv);
+    *reinterpret_cast<float2*>(o) = make_float2(v[0] * inv, v[1 % CPL] * inv);
   }
 }
 
@@ -1593,6 +1611,7 @@ kvs_status decode_attn_token_major(kvs_pool* pool, int layer, const void* q, int
   // about two batches of split slots per merge warp (of which typically
   // fewer than half exist), so that the merge grid stays within one wave
   prm.mwpr = 1;
+  prm.merge_prefetch = L.wide ? 0 : 1;
   const int n_slots = L.n_chunks + (L.SG > 1 ? L.n_chunks_s : 0);
   if (L.compact) {
     // compact items fill only the first slots of a row (as many as its list

@@ -170,6 +170,10 @@ attn_wide_kernel(const __grid_constant__ WideParams p, const __grid_constant__ C
   // read before that kernel has completed.  Then the token-major kernel
   // queued behind this one (it computes other splits) may start on the SMs
   // left free.
+  if (threadIdx.x == 0) {
+    prefetch_tmap(&tk);
+    prefetch_tmap(&tv);
+  }
   asm volatile("griddepcontrol.wait;" ::: "memory");
   asm volatile("griddepcontrol.launch_dependents;");
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -183,10 +187,12 @@ attn_wide_kernel(const __grid_constant__ WideParams p, const __grid_constant__ C
   // loads: issue them together (the grid never exceeds the item capacity)
   WdCursor cur;
   wd_start<RUNS>(p, cur, lane);
-  const bool plan_ok = p.hdr[1] == p.magic && p.hdr[2] == p.n_seq && p.hdr[3] == p.max_blocks &&
-                       p.hdr[4] == p.R && p.hdr[5] == p.ibp && p.hdr[6] == p.hkv && p.hdr[7] == p.W &&
-                       p.hdr[9] == p.ib;
-  const int n_claims = plan_ok ? min(p.hdr[RUNS ? 10 : 8], p.max_witems) * p.hkv : 0;
+  // every compare evaluated (no short circuit): the header's loads are all
+  // in flight together
+  const PlanHdr ph = load_plan_hdr(p.hdr);
+  const bool plan_ok = (ph.v[1] == p.magic) & (ph.v[2] == p.n_seq) & (ph.v[3] == p.max_blocks) & (ph.v[4] == p.R) &
+                       (ph.v[5] == p.ibp) & (ph.v[6] == p.hkv) & (ph.v[7] == p.W) & (ph.v[9] == p.ib);
+  const int n_claims = plan_ok ? min(ph.v[RUNS ? 10 : 8], p.max_witems) * p.hkv : 0;
   if ((int)blockIdx.x >= n_claims) return;   // uniform over the CTA: nothing allocated yet
   wd_prefetch<RUNS>(p, cur, n_claims, lane);
 

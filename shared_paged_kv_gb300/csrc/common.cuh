@@ -81,6 +81,14 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
 }
 
 // ------------------------------------------------------------------- TMA ---
+// Fetch a tensor map (a __grid_constant__ kernel parameter) into the
+// descriptor cache, so that the first copy through it does not wait for it.
+// It reads only the kernel's own parameters, so it may run before
+// griddepcontrol.wait.
+__device__ __forceinline__ void prefetch_tmap(const CUtensorMap* map) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
 __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, int c0, int c1, int c2,
                                             uint64_t* bar) {
   asm volatile(

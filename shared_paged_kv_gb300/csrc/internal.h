@@ -97,6 +97,21 @@ struct WideParams {
   float scale_log2;
   float rs[4][64];          // RoPE frequency pieces (rotation calls), as RopeSplit::c
 };
+// The plan header (the first 12 of its 16 ints), read with three 16-byte
+// loads that are all in flight at once.  A check written as a chain of
+// short-circuit compares on the header would make each load wait for the
+// compare before it.  The loads are plain (L1-cached) loads: every warp of
+// every CTA reads the same line, and loads that bypass L1 would queue all of
+// those requests at one L2 slice.
+struct PlanHdr {
+  int v[12];
+};
+__device__ __forceinline__ PlanHdr load_plan_hdr(const int* hdr) {
+  const int4* h4 = reinterpret_cast<const int4*>(hdr);
+  const int4 a = h4[0], b = h4[1], c = h4[2];
+  return PlanHdr{{a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w, c.x, c.y, c.z, c.w}};
+}
+
 // CTAs of the wide tile's grid for rotation calls (attn_tm.cu)
 int runs_wide_ctas(const kvs_pool* pool);
 kvs_status launch_wide_tile(const WideParams& p, const kvs_pool* pool, int layer, int max_claims,

@@ -233,6 +233,16 @@ q4_attn_kernel(const __grid_constant__ Q4Params p, const __grid_constant__ CUten
   bid /= p.n_seq;
   const int h = bid % p.hkv;
   const int chunk = bid / p.hkv;
+  if (threadIdx.x == 0) {
+    prefetch_tmap(&tk);
+    prefetch_tmap(&tv);
+  }
+  // launched as a programmatic dependent of the kernel before it on the
+  // stream: nothing is read before that kernel has completed; the kernel
+  // queued behind this one may then be scheduled as this grid drains (it
+  // waits the same way before it reads anything)
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;");
 
   int L = p.seq_len[a];
   if (L < 0 || L > p.max_blocks * kQ4B) {
@@ -641,15 +651,22 @@ extern "C" kvs_status kvs_decode_attn_q4(kvs_pool* pool, int32_t layer, const vo
   prm.n_chunks = plan.n_chunks;
   prm.capacity = d.capacity_blocks;
   prm.scale_log2 = scale * 1.4426950408889634f;
-  if (diff_table_dev) {
-    if (!smem_limit_once<q4_attn_kernel<true>>(kQ4Smem, pool->device))
-      return fail(KVS_ERR_CUDA, "decode_attn_q4: cannot raise the shared-memory limit");
-    q4_attn_kernel<true><<<(int)grid, 128, kQ4Smem, stream>>>(prm, pool->tk[layer], pool->tv[layer]);
-  } else {
-    if (!smem_limit_once<q4_attn_kernel<false>>(kQ4Smem, pool->device))
-      return fail(KVS_ERR_CUDA, "decode_attn_q4: cannot raise the shared-memory limit");
-    q4_attn_kernel<false><<<(int)grid, 128, kQ4Smem, stream>>>(prm, pool->tk[layer], pool->tv[layer]);
-  }
+  auto kern = diff_table_dev ? q4_attn_kernel<true> : q4_attn_kernel<false>;
+  if (!(diff_table_dev ? smem_limit_once<q4_attn_kernel<true>>(kQ4Smem, pool->device)
+                       : smem_limit_once<q4_attn_kernel<false>>(kQ4Smem, pool->device)))
+    return fail(KVS_ERR_CUDA, "decode_attn_q4: cannot raise the shared-memory limit");
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid);
+  cfg.blockDim = dim3(128);
+  cfg.dynamicSmemBytes = kQ4Smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, kern, prm, pool->tk[layer], pool->tv[layer]) != cudaSuccess)
+    return fail(KVS_ERR_CUDA, "decode_attn_q4: launch failed");
   count_launch();
   return check_launch("decode_attn_q4");
 }

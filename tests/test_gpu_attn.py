@@ -155,6 +155,38 @@ def test_allgather_d64_rotation():
     run_case(w)
 
 
+@pytest.mark.parametrize("kind", ["gqa_wide", "allgather_rotation"])
+def test_collective_call_equals_per_agent_calls(kind):
+    # the collective call (shared blocks computed once for the group, on the
+    # wide tile) against one call per agent on the same pool, where nothing is
+    # shared: every agent's output agrees, and both match the oracle
+    import dataclasses
+    if kind == "gqa_wide":
+        w = W.make_gqa_fanout(n_seq=6, prefix_tokens=300, priv_lo=20, priv_hi=200, hq=16, hkv=2, d=128)
+    else:
+        w = W.make_allgather(n_seq=4, n_segs=5, priv_blocks_lo=2, priv_blocks_hi=6, hq=10, hkv=2, n_layers=1)
+    segs = w.seg_start_off is not None
+    ref = OF.dedup(w.tokens, w.seq_off, w.tier, w.block_tokens, w.max_blocks,
+                   w.seg_start_off if segs else None, w.seg_start_blocks if segs else None)
+    pool = H.bf16_pool(w)
+    q_bits = w.q_layer(0)
+    together = H.attn(pool, 0, q_bits, w, ref["block_table"])
+    exp = oracle_out(w, pool, ref["block_table"], q_bits)
+    H.assert_close_attn(together, exp)
+    for a in range(w.n_seq):
+        ro = rs = None
+        if w.rope_off is not None:
+            rs = w.rope_segs[w.rope_off[a]:w.rope_off[a + 1]]
+            ro = np.array([0, len(rs)], np.int32)
+        w1 = dataclasses.replace(w, n_seq=1, seq_off=np.array([0, w.seq_len[a]], np.int64),
+                                 diff_table=None if w.diff_table is None else w.diff_table[a:a + 1],
+                                 rope_off=ro, rope_segs=rs)
+        alone = H.attn(pool, 0, q_bits[a:a + 1], w1, ref["block_table"][a:a + 1])
+        H.assert_close_attn(alone[0], exp[a])
+        H.assert_close_attn(alone[0], together[a])
+    assert K.kvs_pool_check(pool) == 0
+
+
 def test_edge_lengths():
     # empty context -> zeros; a single token -> that token's V; exact block
     # multiples and one-past.

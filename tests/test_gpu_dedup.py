@@ -56,6 +56,26 @@ def test_segments_allgather_small():
     check(w, segments=False)   # prefix hashing of the same tokens shares nothing
 
 
+def test_reference_lists_take_both_buffers():
+    # ref_off without ref_seq (or the reverse) is an argument error
+    w = W.make_tiny()
+    pool = H.bf16_pool(w, with_diff=False)
+    cap = pool.desc.capacity_blocks
+    tokens = torch.from_numpy(w.tokens.view(np.int32)).to(H.DEV)
+    fp = torch.zeros(w.n_seq, w.max_blocks, dtype=torch.int64, device=H.DEV)
+    table = torch.zeros(w.n_seq, w.max_blocks, dtype=torch.int32, device=H.DEV)
+    refc = torch.zeros(cap, dtype=torch.int32, device=H.DEV)
+    nphys = torch.zeros(1, dtype=torch.int32, device=H.DEV)
+    ws = H.workspace(K.kvs_workspace_size(pool, K.KVS_OP_DEDUP, w.n_seq, w.max_blocks))
+    ref_off = torch.zeros(cap + 1, dtype=torch.int64, device=H.DEV)
+    ref_seq = torch.zeros(w.n_seq * w.max_blocks, dtype=torch.int32, device=H.DEV)
+    for kw in (dict(ref_off=ref_off), dict(ref_seq=ref_seq)):
+        with pytest.raises(K.KvsError) as e:
+            K.kvs_fingerprint_dedup(pool, tokens, H.i64(w.seq_off), w.n_seq, None, None, None, fp, table,
+                                    w.max_blocks, refc, nphys, ws, **kw)
+        assert e.value.status == K.KVS_ERR_INVALID_ARG
+
+
 def test_tiers_and_private():
     w = W.make_gqa_fanout(n_seq=6, prefix_tokens=96, priv_lo=0, priv_hi=40, hq=4, hkv=2, d=64)
     tier = np.array([0, 1, 0, W.PRIVATE_TIER, 1, 0], dtype=np.uint32)

@@ -242,11 +242,12 @@ def q4_pool(w, cap, n_layers=1):
     return pool
 
 
-def q4_case(w, sample_agents=None, q_pow2=0, gpu_diff_table=None, expect_flags=0):
+def q4_case(w, sample_agents=None, q_pow2=0, gpu_diff_table=None, expect_flags=0, repeat=False):
     """Source bf16 K/V per physical block -> GPU quantiser; the oracle
     quantises the same source values itself and must match bit for bit; then
     Q4 attention vs the oracle on its dequantised values.  q_pow2 multiplies
-    the query by 2^q_pow2 (exact in bf16) and the score scale by 2^-q_pow2."""
+    the query by 2^q_pow2 (exact in bf16) and the score scale by 2^-q_pow2.
+    repeat: a second call on the same inputs must give the same bits."""
     ref = OF.dedup(w.tokens, w.seq_off, w.tier, w.block_tokens, w.max_blocks)
     cap = ref["n_phys"]
     g = torch.Generator(device=H.DEV).manual_seed(77)
@@ -271,6 +272,12 @@ def q4_case(w, sample_agents=None, q_pow2=0, gpu_diff_table=None, expect_flags=0
     torch.cuda.synchronize()
     assert K.kvs_pool_check(pool) == expect_flags
     got = out.cpu().numpy().astype(np.float64)
+    if repeat:
+        out2 = torch.full_like(out, float("nan"))
+        K.kvs_decode_attn_q4(pool, 0, H.bits_to_dev(q_bits), w.n_q_heads, H.i32(ref["block_table"]), w.max_blocks,
+                             H.i32(w.seq_len), n, scale, out2, ws, diff_table=dt)
+        torch.cuda.synchronize()
+        assert torch.equal(out.view(torch.int32), out2.view(torch.int32))
     ks, vs, ksb, vsb = pool.q4
     agents = range(n) if sample_agents is None else sample_agents
     blocks = sorted({int(b) for a in agents for b in ref["block_table"][a] if b >= 0})
@@ -325,6 +332,22 @@ def test_q4_query_outside_fp16_range():
     q4_case(w, q_pow2=-22)
 
 
+def test_q4_diff_table_needs_diff_slabs():
+    # a diff table on a Q4 pool created without mirror-diff slabs is an
+    # argument error, raised before any launch
+    w = W.make_q4(n_seq=2, ctx=300, hq=8, hkv=2)
+    pool = q4_pool(w, 8)
+    n = w.n_seq
+    out = torch.zeros((n, w.n_q_heads, 128), dtype=torch.float32, device=H.DEV)
+    ws = H.workspace(K.kvs_workspace_size(pool, K.KVS_OP_DECODE_ATTN_Q4, n, w.max_blocks, w.n_q_heads))
+    dt = H.i32(np.full((n, w.max_blocks * 16), -1, np.int32))
+    with pytest.raises(K.KvsError) as e:
+        K.kvs_decode_attn_q4(pool, 0, H.bits_to_dev(w.q_layer(0)), w.n_q_heads,
+                             H.i32(np.zeros((n, w.max_blocks), np.int32)), w.max_blocks, H.i32(w.seq_len), n,
+                             w.scale, out, ws, diff_table=dt)
+    assert e.value.status == K.KVS_ERR_INVALID_ARG
+
+
 def test_q4_full_size_every_pair():
     q4_case(W.make_q4(n_layers=1))       # 12 agents x 32 heads
 
@@ -338,7 +361,7 @@ def test_q4_mirror_small_ragged():
     toks = np.concatenate([w.tokens[:700], w.tokens[700:956], w.tokens[1400:1913]])
     import dataclasses
     w2 = dataclasses.replace(w, tokens=toks, seq_off=np.concatenate([[0], np.cumsum(lens)]).astype(np.int64))
-    q4_case(w2)
+    q4_case(w2, repeat=True)
 
 
 def test_q4_mirror_group8():
