@@ -232,8 +232,8 @@ struct PlanParams {
   int32_t* bdelta;   // [n_seq][max_blocks] RoPE shift of each logical block (rotation calls)
   int32_t* bwin;     // [n_seq][max_blocks] the last entry covering each block (from the sequence's first), or -1
   uint32_t* status;
-  float* p1_ml;      // (m, l) of the private splits [n_seq][hkv][n_chunks][g]
-  float* p2_ml;      // (m, l) of the shared splits [n_seq][hkv][n_chunks_s][g] (SG > 1)
+  float* p1_ml;      // (m, l) of the private splits [n_seq][hkv][g][n_chunks]
+  float* p2_ml;      // (m, l) of the shared splits [n_seq][hkv][g][n_chunks_s] (SG > 1)
   int n_seq, max_blocks, R, SG, G, ib, n_chunks, ibs, n_chunks_s, n_groups, capacity, hkv, wide, max_sub, runs;
   int max_witems;
   int wide_ctas;     // CTAs of the wide tile's grid (rotation calls size their claims to it)
@@ -565,14 +565,14 @@ __global__ void __launch_bounds__(512) tm_plan_groups(PlanParams pp) {
       }
     }
     __syncthreads();
-    // 3. splits that no item writes ([a][h][c][hh]): one (member, chunk)
-    // per thread, its flag read once
+    // 3. splits that no item writes (their (m, l) at [a][h][hh][c]): one
+    // (member, chunk) per thread, its flag read once
     for (int i = tid; i < nm * pp.n_chunks; i += nt) {
       const int r = i / pp.n_chunks, c = i - r * pp.n_chunks, a = a0 + r;
       if (pp.pne[(size_t)a * pp.n_chunks + c]) continue;
       float2* ml = reinterpret_cast<float2*>(pp.p1_ml) + (size_t)a * pp.hkv * pp.n_chunks * pp.G;
       for (int h = 0; h < pp.hkv; ++h)
-        for (int hh = 0; hh < pp.G; ++hh) ml[((size_t)h * pp.n_chunks + c) * pp.G + hh] = none;
+        for (int hh = 0; hh < pp.G; ++hh) ml[((size_t)h * pp.G + hh) * pp.n_chunks + c] = none;
     }
     if (SG > 1) {
       for (int i = tid; i < nm * pp.n_chunks_s; i += nt) {
@@ -580,7 +580,7 @@ __global__ void __launch_bounds__(512) tm_plan_groups(PlanParams pp) {
         if ((pp.spm[(size_t)gi * pp.n_chunks_s + c] >> r) & 1u) continue;
         float2* ml = reinterpret_cast<float2*>(pp.p2_ml) + (size_t)a * pp.hkv * pp.n_chunks_s * pp.G;
         for (int h = 0; h < pp.hkv; ++h)
-          for (int hh = 0; hh < pp.G; ++hh) ml[((size_t)h * pp.n_chunks_s + c) * pp.G + hh] = none;
+          for (int hh = 0; hh < pp.G; ++hh) ml[((size_t)h * pp.G + hh) * pp.n_chunks_s + c] = none;
       }
     }
     __syncthreads();
@@ -656,7 +656,7 @@ struct TmParams {
   const int32_t* bdelta;   // RoPE shift per logical block (rotation calls)
   float* out;
   float* p1;          // private splits [n_seq][hkv][n_chunks][g][D]
-  float* p1_ml;       // [n_seq][hkv][n_chunks][g][2]
+  float* p1_ml;       // [n_seq][hkv][g][n_chunks][2]: a row's (m, l) are contiguous
   float* p2;          // shared splits, same shape
   float* p2_ml;
   const int* hdr;
@@ -1053,14 +1053,16 @@ attn_tm_kernel(const __grid_constant__ TmParams p, const __grid_constant__ CUten
       if (slot != 31) {
         const int a = ckind ? cidx * R + slot : cidx;
         const int hh = j - slot * p.g;
-        const size_t it = (((size_t)a * p.hkv + ch_) * (ckind ? p.n_chunks_s : p.n_chunks) + cchunk) * p.g + hh;
+        const int nch = ckind ? p.n_chunks_s : p.n_chunks;
+        const size_t it = (((size_t)a * p.hkv + ch_) * nch + cchunk) * p.g + hh;
         float* pr = dst + it * D;
 #pragma unroll
         for (int mt = 0; mt < D / 16; ++mt) {
           __stcg(pr + mt * 16 + g, acc[mt][cc]);
           __stcg(pr + mt * 16 + g + 8, acc[mt][2 + cc]);
         }
-        if (g == 0) __stcg(reinterpret_cast<float2*>(dml + it * 2), make_float2(m[cc], lt[cc]));
+        const size_t im = (((size_t)a * p.hkv + ch_) * p.g + hh) * nch + cchunk;
+        if (g == 0) __stcg(reinterpret_cast<float2*>(dml + im * 2), make_float2(m[cc], lt[cc]));
       }
     }
   };
@@ -1274,6 +1276,12 @@ tm_merge_kernel(const __grid_constant__ TmParams p) {
   auto slot_off = [&](int sl) {   // split index of a slot
     return sl < p.n_chunks ? (sbase + sl) * p.g + hh : (sbase_s + (sl - p.n_chunks)) * p.g + hh;
   };
+  // (m, l) index of a slot: a row's (m, l) are contiguous, so a warp reading
+  // 32 consecutive slots touches two or three cache lines
+  const size_t mrow = ((size_t)a * p.hkv + h) * p.g + hh;
+  auto ml_off = [&](int sl) {
+    return sl < p.n_chunks ? mrow * p.n_chunks + sl : mrow * p.n_chunks_s + (sl - p.n_chunks);
+  };
   // Before the wait: this CTA is often resident well before the attention
   // grid completes, and what it reads below has usually left L2 (the (m, l)
   // of splits that no item writes were set by the plan once per step; early
@@ -1283,7 +1291,7 @@ tm_merge_kernel(const __grid_constant__ TmParams p) {
   // is where every write lands, so everything is read after the wait and is
   // correct.
   for (int sl = wq + lane * wpr; sl < n_slots; sl += 32 * wpr) {
-    asm volatile("prefetch.global.L2 [%0];" ::"l"((sl >= p.n_chunks ? p.p2_ml : p.p1_ml) + slot_off(sl) * 2));
+    asm volatile("prefetch.global.L2 [%0];" ::"l"((sl >= p.n_chunks ? p.p2_ml : p.p1_ml) + ml_off(sl) * 2));
     if (p.merge_prefetch) {
       const char* src = reinterpret_cast<const char*>((sl >= p.n_chunks ? p.p2 : p.p1) + slot_off(sl) * D);
 #pragma unroll
@@ -1301,11 +1309,12 @@ tm_merge_kernel(const __grid_constant__ TmParams p) {
   auto load_ml = [&](int sl) {
     if (sl >= n_slots) return make_float2(-INFINITY, 0.f);
     const float* base = sl >= p.n_chunks ? p.p2_ml : p.p1_ml;
-    return __ldcg(reinterpret_cast<const float2*>(base + slot_off(sl) * 2));
+    return __ldcg(reinterpret_cast<const float2*>(base + ml_off(sl) * 2));
   };
 
-  // 1. M of the row; the (m, l) of this lane's own slots in the first two
-  // passes come along
+  // 1. M of the row: lane k reads slots k, k + 32, ... (consecutive (m, l),
+  // two or three lines per load); the (m, l) of this lane's own slots in the
+  // first two passes of step 2 come along
   const float2 own0 = load_ml(lane * wpr + wq), own1 = load_ml(32 * wpr + lane * wpr + wq);
   float M = -INFINITY;
   for (int w0 = 0; w0 < n_slots; w0 += 32 * kMergeWin) {

@@ -433,8 +433,8 @@ attn_wide_kernel(const __grid_constant__ WideParams p, const __grid_constant__ C
       }
       const int a = e_gw * p.W + slot;
       if (ch == 0 && slot < p.W && a < p.n_seq && ((e_spm >> slot) & 1u)) {
-        const size_t it = (((size_t)a * p.hkv + e_h) * p.n_chunks + e_c) * p.g + hh;
-        __stcg(reinterpret_cast<float2*>(p.p2_ml + it * 2), make_float2(e_m, l_tot));
+        const size_t im = (((size_t)a * p.hkv + e_h) * p.g + hh) * p.n_chunks + e_c;
+        __stcg(reinterpret_cast<float2*>(p.p2_ml + im * 2), make_float2(e_m, l_tot));
       }
       return true;
     };

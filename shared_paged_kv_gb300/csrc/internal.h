@@ -87,7 +87,7 @@ struct WideParams {
   const int2* wmem;        // rotation calls: [item][32] {split slot, RoPE shift} per member
   const int4* wclaims;     // rotation calls: claims {group, first item, items | slot << 16, members}
   float* p2;                // [n_seq][hkv][n_chunks][g][128]
-  float* p2_ml;             // [n_seq][hkv][n_chunks][g][2]
+  float* p2_ml;             // [n_seq][hkv][g][n_chunks][2]
   uint32_t* status;
   int n_seq, max_blocks, hkv, g, hq, W, ib, n_chunks, R, capacity, max_sub;   // ib, n_chunks: shared chunks
   int ibp;                  // private chunk blocks (plan header check)
