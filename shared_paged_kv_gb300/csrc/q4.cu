@@ -226,6 +226,8 @@ q4_attn_kernel(const __grid_constant__ Q4Params p, const __grid_constant__ CUten
   __shared__ uint64_t full[kQ4Stages], empty[kQ4Stages];
   __shared__ int s_last;
   __shared__ float sM[16], sL[16];
+  __shared__ __align__(16) float s_acc[kAttnWarps][8][kQ4D];   // the warps' states at the end
+  __shared__ float2 s_wml[kAttnWarps][8];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, c = lane & 3;
   int bid = blockIdx.x;
@@ -535,8 +537,9 @@ q4_attn_kernel(const __grid_constant__ Q4Params p, const __grid_constant__ CUten
       corr[1][cc] += __shfl_xor_sync(0xffffffffu, corr[1][cc], o);
     }
   }
-  const size_t sidx = (((size_t)a * p.hkv + h) * p.n_chunks + chunk) * kAttnWarps + warp;
-  float* pr = p.part + sidx * G_ * kQ4D;
+  // The four warps' states (64 tokens of every block each) combine in
+  // shared memory into one split per CTA, so the merge behind the last CTA
+  // of the (sequence, KV head) reads one split per chunk.
 #pragma unroll
   for (int cc = 0; cc < 2; ++cc) {
     const int r = 2 * c + cc;
@@ -546,16 +549,42 @@ q4_attn_kernel(const __grid_constant__ Q4Params p, const __grid_constant__ CUten
 #pragma unroll
       for (int lm = 0; lm < 4; ++lm) {
         const int d0 = grp * 64 + 8 * g + 2 * lm;
-        __stcg(reinterpret_cast<float2*>(pr + r * kQ4D + d0),
-               make_float2(fmaf(acc[grp * 4 + lm][cc], 16777216.f, corr[grp][cc]),
-                           fmaf(acc[grp * 4 + lm][2 + cc], 1048576.f, corr[grp][cc])));
+        *reinterpret_cast<float2*>(&s_acc[warp][r][d0]) =
+            make_float2(fmaf(acc[grp * 4 + lm][cc], 16777216.f, corr[grp][cc]),
+                        fmaf(acc[grp * 4 + lm][2 + cc], 1048576.f, corr[grp][cc]));
       }
     }
-    if (g == 0) __stcg(reinterpret_cast<float2*>(p.part_ml + (sidx * G_ + r) * 2), make_float2(m[cc], l[cc]));
+    if (g == 0) s_wml[warp][r] = make_float2(m[cc], l[cc]);
+  }
+  __syncthreads();
+  const size_t sidx = ((size_t)a * p.hkv + h) * p.n_chunks + chunk;
+  {
+    const int r = threadIdx.x >> 4, c0 = (threadIdx.x & 15) * 8;   // 8 rows x 16 threads of 8 columns
+    if (r < G_) {
+      float M = -INFINITY;
+#pragma unroll
+      for (int w = 0; w < kAttnWarps; ++w)
+        if (s_wml[w][r].y > 0.f) M = fmaxf(M, s_wml[w][r].x);
+      float Lc = 0.f, o[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int w = 0; w < kAttnWarps; ++w) {
+        const float2 ml = s_wml[w][r];
+        const float wt = ml.y > 0.f ? fast_exp2(ml.x - M) : 0.f;
+        Lc += wt * ml.y;
+        const float4 x0 = *reinterpret_cast<const float4*>(&s_acc[w][r][c0]);
+        const float4 x1 = *reinterpret_cast<const float4*>(&s_acc[w][r][c0 + 4]);
+        o[0] += wt * x0.x; o[1] += wt * x0.y; o[2] += wt * x0.z; o[3] += wt * x0.w;
+        o[4] += wt * x1.x; o[5] += wt * x1.y; o[6] += wt * x1.z; o[7] += wt * x1.w;
+      }
+      float* pr = p.part + (sidx * G_ + r) * kQ4D + c0;
+      __stcg(reinterpret_cast<float4*>(pr), make_float4(o[0], o[1], o[2], o[3]));
+      __stcg(reinterpret_cast<float4*>(pr + 4), make_float4(o[4], o[5], o[6], o[7]));
+      if ((threadIdx.x & 15) == 0) __stcg(reinterpret_cast<float2*>(p.part_ml + (sidx * G_ + r) * 2), make_float2(M, Lc));
+    }
   }
   if (!arrive_last(p.tickets + a * p.hkv + h, nch, &s_last)) return;
-  const size_t s0 = ((size_t)a * p.hkv + h) * p.n_chunks * kAttnWarps;
-  merge_splits<kQ4D>(p.part, p.part_ml, s0, nch * kAttnWarps, G_, p.out + ((size_t)a * p.hq + h * G_) * kQ4D, sM, sL);
+  const size_t s0 = ((size_t)a * p.hkv + h) * p.n_chunks;
+  merge_splits<kQ4D>(p.part, p.part_ml, s0, nch, G_, p.out + ((size_t)a * p.hq + h * G_) * kQ4D, sM, sL);
 }
 
 AttnPlan q4_plan(const kvs_pool* pool, int n_seq, int max_blocks) {
