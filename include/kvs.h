@@ -255,7 +255,13 @@ kvs_status kvs_select_critical_noalloc(const void* k_cached_dev, const void* k_n
  *               (seq_len 0) yields zeros.
  * ws            kvs_workspace_size(KVS_OP_DECODE_ATTN) bytes of device memory.
  * Requires n_q_heads % num_kv_heads == 0 and a group of at most 16 query
- * heads per KV head; BF16 pools. */
+ * heads per KV head; BF16 pools.
+ * Two implementations, chosen from the call's shape on the host: groups of
+ * 9-16 heads, and small calls (n_seq * num_kv_heads * max_blocks <= 2048)
+ * with groups <= 8, run one kernel per layer with no plan; larger calls with
+ * groups <= 8 run the planned token-major path (blocks that a group of
+ * sequences shares are computed once for the group).  The results agree to
+ * rounding. */
 typedef struct { int32_t first_block, n_blocks, delta, reserved; } kvs_seg_rope;
 kvs_status kvs_decode_attn(kvs_pool* pool, int32_t layer, const void* q_dev, int32_t n_q_heads,
                            const int32_t* block_table_dev, int32_t max_blocks,
@@ -280,7 +286,8 @@ kvs_status kvs_decode_attn(kvs_pool* pool, int32_t layer, const void* q_dev, int
  * on the device (KVS_DEVERR_PLAN, no output written), a change of table or
  * segment contents without a new plan is not.
  * kvs_decode_attn is kvs_decode_plan followed by kvs_decode_attn_planned.
- * Groups of more than 8 query heads need no plan (the calls accept them). */
+ * Groups of more than 8 query heads, and small calls, need no plan (the calls
+ * accept them and kvs_decode_plan writes nothing). */
 kvs_status kvs_decode_plan(kvs_pool* pool, int32_t n_q_heads, const int32_t* block_table_dev,
                            int32_t max_blocks, const int32_t* seq_len_dev, int32_t n_seq,
                            const int32_t* diff_table_dev, const int32_t* rope_off_dev,
@@ -449,6 +456,13 @@ kvs_status kvs_pool_import(kvs_pool* pool, const int32_t* blocks_dev, int32_t n_
  * consumed by that launch.  It exists to test the timeout path without a
  * device fault; nothing else sets it. */
 #define KVS_TEST_STALL_ONE_STAGE 0x1u
+/* KVS_TEST_TOKEN_MAJOR: while set, every kvs_decode_attn / kvs_decode_plan /
+ * kvs_decode_attn_planned call with a query group <= 8 takes the planned
+ * token-major path, also below the small-call bound (see kvs_decode_attn),
+ * so that tests can run that path on small inputs.  It stays set until
+ * kvs_pool_set_test_flags clears it.  Results agree between the two paths to
+ * rounding. */
+#define KVS_TEST_TOKEN_MAJOR 0x2u
 kvs_status kvs_pool_set_test_flags(kvs_pool* pool, uint32_t flags);
 
 /* Workspace bytes for an operation with the given call shape. */

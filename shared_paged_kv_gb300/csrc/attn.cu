@@ -79,10 +79,24 @@ attn_bf16_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ C
   __shared__ int s_last;
   __shared__ float sM[16], sL[16];
   __shared__ float rsc[ROPE ? 4 * 64 : 1];   // RoPE frequency pieces (rotation calls)
+  __shared__ float2 s_wml[kAttnWarps][16];    // the warps' (m, l) at the end
+  if (threadIdx.x == 0) {
+    prefetch_tmap(&tk);
+    prefetch_tmap(&tv);
+    if (DIFF) {
+      prefetch_tmap(&tdk);
+      prefetch_tmap(&tdv);
+    }
+  }
   if (ROPE) {
     for (int i = threadIdx.x; i < 4 * 64; i += blockDim.x) rsc[i] = p.rs.c[i >> 6][i & 63];
     __syncthreads();
   }
+  // launched as a programmatic dependent of the kernel before it on the
+  // stream: nothing is read before that kernel has completed; the kernel
+  // queued behind this one may be scheduled as this grid drains
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;");
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, c = lane & 3;
@@ -389,24 +403,59 @@ attn_bf16_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ C
   l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
   l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
 
-  // ---- write this warp's split
-  const size_t sidx = (((size_t)a * p.hkv + h) * p.n_chunks + chunk) * kAttnWarps + warp;
-  float* pr = p.part + sidx * p.g * D;
+  // ---- the four warps' states combine into one split per CTA.  The stage
+  // buffers are free once every warp is past its last block (a warp that
+  // timed out has drained its copies, each wait bounded), so they hold the
+  // warps' accumulators: [warp][row][D] fp32.
+  __syncthreads();
+  float* s_acc = reinterpret_cast<float*>(base);
+  static_assert(kAttnWarps * 16 * D * 4 <= kAttnWarps * S * STAGE, "combine buffer fits the stages");
   if (r0ok) {
 #pragma unroll
     for (int n = 0; n < D / 8; ++n)
-      __stcg(reinterpret_cast<float2*>(pr + g * D + n * 8 + 2 * c), make_float2(acc[n][0], acc[n][1]));
-    if (c == 0) __stcg(reinterpret_cast<float2*>(p.part_ml + (sidx * p.g + g) * 2), make_float2(m0, l0));
+      *reinterpret_cast<float2*>(s_acc + ((size_t)warp * 16 + g) * D + n * 8 + 2 * c) = make_float2(acc[n][0], acc[n][1]);
+    if (c == 0) s_wml[warp][g] = make_float2(m0, l0);
   }
   if (r1ok) {
 #pragma unroll
     for (int n = 0; n < D / 8; ++n)
-      __stcg(reinterpret_cast<float2*>(pr + (g + 8) * D + n * 8 + 2 * c), make_float2(acc[n][2], acc[n][3]));
-    if (c == 0) __stcg(reinterpret_cast<float2*>(p.part_ml + (sidx * p.g + g + 8) * 2), make_float2(m1, l1));
+      *reinterpret_cast<float2*>(s_acc + ((size_t)warp * 16 + g + 8) * D + n * 8 + 2 * c) = make_float2(acc[n][2], acc[n][3]);
+    if (c == 0) s_wml[warp][g + 8] = make_float2(m1, l1);
+  }
+  __syncthreads();
+  const size_t sidx = ((size_t)a * p.hkv + h) * p.n_chunks + chunk;
+  {
+    constexpr int CPT = D / 8;   // columns per thread: 16 rows x 8 threads
+    const int r = threadIdx.x >> 3, c0 = (threadIdx.x & 7) * CPT;
+    if (r < p.g) {
+      float M = -INFINITY;
+#pragma unroll
+      for (int w = 0; w < kAttnWarps; ++w)
+        if (s_wml[w][r].y > 0.f) M = fmaxf(M, s_wml[w][r].x);
+      float Lc = 0.f, o[CPT];
+#pragma unroll
+      for (int j = 0; j < CPT; ++j) o[j] = 0.f;
+#pragma unroll
+      for (int w = 0; w < kAttnWarps; ++w) {
+        const float2 ml = s_wml[w][r];
+        const float wt = ml.y > 0.f ? fast_exp2(ml.x - M) : 0.f;
+        Lc += wt * ml.y;
+        const float* src = s_acc + ((size_t)w * 16 + r) * D + c0;
+#pragma unroll
+        for (int j = 0; j < CPT; j += 4) {
+          const float4 x = *reinterpret_cast<const float4*>(src + j);
+          o[j] += wt * x.x; o[j + 1] += wt * x.y; o[j + 2] += wt * x.z; o[j + 3] += wt * x.w;
+        }
+      }
+      float* pr = p.part + (sidx * p.g + r) * D + c0;
+#pragma unroll
+      for (int j = 0; j < CPT; j += 4) __stcg(reinterpret_cast<float4*>(pr + j), make_float4(o[j], o[j + 1], o[j + 2], o[j + 3]));
+      if ((threadIdx.x & 7) == 0) __stcg(reinterpret_cast<float2*>(p.part_ml + (sidx * p.g + r) * 2), make_float2(M, Lc));
+    }
   }
   if (!arrive_last(p.tickets + a * p.hkv + h, nch, &s_last)) return;
-  const size_t s0 = ((size_t)a * p.hkv + h) * p.n_chunks * kAttnWarps;
-  merge_splits<D>(p.part, p.part_ml, s0, nch * kAttnWarps, p.g, p.out + ((size_t)a * p.hq + h * p.g) * D, sM, sL);
+  const size_t s0 = ((size_t)a * p.hkv + h) * p.n_chunks;
+  merge_splits<D>(p.part, p.part_ml, s0, nch, p.g, p.out + ((size_t)a * p.hq + h * p.g) * D, sM, sL);
 }
 
 template <int D, bool DIFF, bool ROPE>
@@ -417,7 +466,18 @@ static kvs_status launch_attn(const AttnParams& prm, const kvs_pool* pool, int l
     return fail(KVS_ERR_CUDA, "decode_attn: cannot raise the shared-memory limit");
   const CUtensorMap& dk = DIFF ? pool->tdk[layer] : pool->tk[layer];
   const CUtensorMap& dv = DIFF ? pool->tdv[layer] : pool->tv[layer];
-  kern<<<grid, 128, smem, st>>>(prm, pool->tk[layer], pool->tv[layer], dk, dv);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(128);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, kern, prm, pool->tk[layer], pool->tv[layer], dk, dv) != cudaSuccess)
+    return fail(KVS_ERR_CUDA, "decode_attn: launch failed");
   count_launch();
   return check_launch("decode_attn");
 }
@@ -425,6 +485,12 @@ static kvs_status launch_attn(const AttnParams& prm, const kvs_pool* pool, int l
 }  // namespace kvs
 
 using namespace kvs;
+
+// Small calls with a query group <= 8 run on the 16-row kernel alone, unless
+// a test asks for the planned path.
+static bool use_small_path(const kvs_pool* pool, int n_seq, int max_blocks, int g) {
+  return small_call(n_seq, pool->desc.num_kv_heads, max_blocks, g) && !(pool->test_flags & KVS_TEST_TOKEN_MAJOR);
+}
 
 // Host checks shared by the decode-attention entry points.
 static kvs_status attn_check(kvs_pool* pool, int32_t layer, const void* q_dev, int32_t n_q_heads,
@@ -462,7 +528,10 @@ extern "C" kvs_status kvs_decode_plan(kvs_pool* pool, int32_t n_q_heads, const i
   kvs_status st = attn_check(pool, 0, nullptr, n_q_heads, block_table_dev, max_blocks, seq_len_dev, n_seq,
                              diff_table_dev, rope_off_dev, rope_segs_dev, 1.f, nullptr, ws, ws_bytes, false);
   if (st != KVS_OK || n_seq == 0) return st;
-  if (n_q_heads / pool->desc.num_kv_heads > kTmMaxGroup) return KVS_OK;   // the 16-row kernel needs no plan
+  // the 16-row kernel (groups of 9-16, and small calls) needs no plan
+  if (n_q_heads / pool->desc.num_kv_heads > kTmMaxGroup ||
+      use_small_path(pool, n_seq, max_blocks, n_q_heads / pool->desc.num_kv_heads))
+    return KVS_OK;
   return decode_plan_token_major(pool, n_q_heads, block_table_dev, max_blocks, seq_len_dev, n_seq, diff_table_dev,
                                  rope_off_dev, rope_segs_dev, ws, stream);
 }
@@ -474,7 +543,7 @@ static kvs_status attn_launch(kvs_pool* pool, int32_t layer, const void* q_dev, 
                               cudaStream_t stream) {
   const kvs_pool_desc& d = pool->desc;
   const int g = n_q_heads / d.num_kv_heads;
-  if (g <= kTmMaxGroup)
+  if (g <= kTmMaxGroup && !use_small_path(pool, n_seq, max_blocks, g))
     return decode_attn_token_major(pool, layer, q_dev, n_q_heads, block_table_dev, max_blocks, seq_len_dev, n_seq,
                                    diff_table_dev, rope_off_dev, rope_segs_dev, theta, scale, out_dev, ws, stream);
   const AttnPlan plan = attn_plan(pool, n_seq, max_blocks);

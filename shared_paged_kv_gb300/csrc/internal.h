@@ -75,6 +75,16 @@ kvs_status decode_plan_token_major(kvs_pool* pool, int n_q_heads, const int32_t*
                                    const int32_t* seq_len, int n_seq, const int32_t* diff, const int32_t* rope_off,
                                    const kvs_seg_rope* rope_segs, void* ws, cudaStream_t stream);
 constexpr int kTmMaxGroup = 8;
+// Small calls: up to this many (sequence, KV head, logical block) triples a
+// call with a query group <= 8 runs on the 16-row kernel alone (attn.cu: one
+// launch, no plan, no separate merge), whose fixed cost is lower than the
+// planned token-major path's three launches.  The 4-agent, 24-block layer
+// (192 triples) took 12.9 us per layer there against 17.0 us planned; 16,384
+// sequences of that shape (786,432 triples) took 2.31 ms against 0.70 ms.
+constexpr long long kSmallCallWork = 2048;
+inline bool small_call(int n_seq, int num_kv_heads, int max_blocks, int g) {
+  return g <= kTmMaxGroup && (long long)n_seq * num_kv_heads * max_blocks <= kSmallCallWork;
+}
 
 // Wide shared tile (attn_wide.cu): tcgen05 attention of a sharing group's
 // W * G query rows over the blocks the group shares.  Writes the shared splits

@@ -304,13 +304,15 @@ kvs_status kvs_workspace_size(const kvs_pool* p, int32_t op, int32_t n_seq, int3
     case KVS_OP_DECODE_ATTN_Q4: {
       if (n_q_heads < 1 || n_q_heads % p->desc.num_kv_heads) return fail(KVS_ERR_INVALID_ARG, "workspace_size: n_q_heads");
       const int g = n_q_heads / p->desc.num_kv_heads;
-      if (op == KVS_OP_DECODE_ATTN && g <= kTmMaxGroup) {
-        b = tm_workspace_bytes(p, n_seq, max_blocks, g);
-        break;
-      }
       const AttnPlan plan = op == KVS_OP_DECODE_ATTN ? attn_plan(p, n_seq, max_blocks) : q4_plan(p, n_seq, max_blocks);
       const size_t splits = static_cast<size_t>(n_seq) * p->desc.num_kv_heads * plan.n_chunks * kAttnWarps;
       b = splits * g * (p->desc.head_dim + 2) * sizeof(float) + 256;
+      // query groups <= 8: the planned token-major path, and for small calls
+      // also the 16-row kernel (either may run: see KVS_TEST_TOKEN_MAJOR)
+      if (op == KVS_OP_DECODE_ATTN && g <= kTmMaxGroup) {
+        const size_t tm = tm_workspace_bytes(p, n_seq, max_blocks, g);
+        b = small_call(n_seq, p->desc.num_kv_heads, max_blocks, g) ? std::max(b, tm) : tm;
+      }
       break;
     }
     case KVS_OP_SELECT: {

@@ -36,6 +36,7 @@ KVS_DEVERR_JOB = 0x40
 KVS_DEVERR_PLAN = 0x80
 KVS_DEVERR_REFCOUNT = 0x100
 KVS_TEST_STALL_ONE_STAGE = 0x1
+KVS_TEST_TOKEN_MAJOR = 0x2
 
 KVS_DTYPE_BF16 = 0
 KVS_DTYPE_Q4G64 = 1

@@ -64,8 +64,13 @@ def gpu_dedup(pool, w: W.Workload, flags: int = 0, segments: bool = True, tier=N
                 refc_dev=refc, nphys_dev=nphys)
 
 
-def bf16_pool(w: W.Workload, n_layers: int = 1, capacity=None, with_diff: bool = None, layers_np=None):
-    """Pool of n_layers bf16 slabs filled from the workload's seeded values."""
+def bf16_pool(w: W.Workload, n_layers: int = 1, capacity=None, with_diff: bool = None, layers_np=None,
+              path: str = "token_major"):
+    """Pool of n_layers bf16 slabs filled from the workload's seeded values.
+    path "token_major" makes every attention call on it take the planned
+    token-major path (KVS_TEST_TOKEN_MAJOR), also for small calls, which the
+    library would otherwise run on the single-kernel path; "auto" keeps the
+    library's own choice."""
     cap = capacity or w.capacity_blocks
     ks, vs, dks, dvs = [], [], [], []
     host = []
@@ -90,6 +95,8 @@ def bf16_pool(w: W.Workload, n_layers: int = 1, capacity=None, with_diff: bool =
                              diff_capacity_blocks=w.diff_capacity_blocks if use_diff else 0)
     pool.host = host
     pool.dev = dict(k=ks, v=vs, dk=dks, dv=dvs)
+    if path == "token_major":
+        K.kvs_pool_set_test_flags(pool, K.KVS_TEST_TOKEN_MAJOR)
     return pool
 
 

@@ -23,7 +23,7 @@ def test_wait_timeout_is_reported_and_the_context_survives():
     ref = OF.dedup(w.tokens, w.seq_off, w.tier, w.block_tokens, w.max_blocks)
     pool = H.bf16_pool(w)
     q_bits = w.q_layer(0)
-    K.kvs_pool_set_test_flags(pool, K.KVS_TEST_STALL_ONE_STAGE)
+    K.kvs_pool_set_test_flags(pool, K.KVS_TEST_STALL_ONE_STAGE | K.KVS_TEST_TOKEN_MAJOR)
     t0 = time.time()
     H.attn(pool, 0, q_bits, w, ref["block_table"])
     dt = time.time() - t0

@@ -32,6 +32,7 @@ def table_case(table, seq_len, hq, hkv, kf, vf, seed):
     q_bits = W.f32_to_bf16_bits(rng.standard_normal((n, hq, d)).astype(np.float32))
     pool = K.kvs_pool_create(1, hkv, d, 16, K.KVS_DTYPE_BF16, kb.shape[0], n, [H.bits_to_dev(kb)],
                              [H.bits_to_dev(vb)])
+    K.kvs_pool_set_test_flags(pool, K.KVS_TEST_TOKEN_MAJOR)   # the planned path, also for small calls
     w = SimpleNamespace(n_seq=n, n_q_heads=hq, head_dim=d, diff_table=None, rope_off=None, rope_segs=None,
                         max_blocks=max_blocks, theta=1e6, scale=1.0 / np.sqrt(d), seq_len=seq_len)
     got = H.attn(pool, 0, q_bits, w, table)
@@ -163,6 +164,7 @@ def rope_case(table, seq_len, rope_off, rope_segs, hq, hkv, kf, vf, seed, diff_t
         kw = dict(dk_layers=[H.bits_to_dev(dkb)], dv_layers=[H.bits_to_dev(dvb)], diff_capacity_blocks=dkb.shape[0])
     pool = K.kvs_pool_create(1, hkv, d, 16, K.KVS_DTYPE_BF16, kb.shape[0], n, [H.bits_to_dev(kb)],
                              [H.bits_to_dev(vb)], **kw)
+    K.kvs_pool_set_test_flags(pool, K.KVS_TEST_TOKEN_MAJOR)   # the planned path, also for small calls
     w = SimpleNamespace(n_seq=n, n_q_heads=hq, head_dim=d, diff_table=diff_table, rope_off=rope_off,
                         rope_segs=rope_segs, max_blocks=max_blocks, theta=1e6, scale=1.0 / np.sqrt(d),
                         seq_len=seq_len)
