@@ -498,7 +498,7 @@ def main():
 # name -> (dominant kernels, committed ncu summary, workload description)
 CONFIG_INFO = {
     "mha7b": ("attn_tm_kernel<128,0,0>, then tm_merge_kernel<128>", "profiles/attn_bf16_mha7b.md", WORKLOAD),
-    "tiny": ("attn_tm_kernel<64,1,0> + tm_merge_kernel<64> (latency-bound)", None,
+    "tiny": ("attn_bf16_kernel<64,1,0> (small-call path: one launch, latency-bound)", "profiles/attn_bf16_tiny.md",
              "tiny: 4 agents, 1 layer, 8 q / 2 kv heads, d 64, 256-token shared prefix + 64-128 private, "
              "2 mirror-diff blocks per agent"),
     "gqa_fanout": ("attn_wide_kernel<1,0> beside attn_tm_kernel<128,0,0>, then tm_merge_kernel<128>",
@@ -512,7 +512,7 @@ CONFIG_INFO = {
     "q4": ("q4_attn_kernel<0>", "profiles/q4_attn_q4.md",
            "q4: 12 agents x 8192 tokens, 32 q / 8 kv heads, d 128, Q4G64 codes with fp16 scale+bias, "
            "256-token blocks, 32 layers"),
-    "q4_mirror": ("q4_attn_kernel<1>", None,
+    "q4_mirror": ("q4_attn_kernel<1>", "profiles/q4_attn_q4_mirror.md",
                   "q4_mirror: the q4 workload with bf16 mirror diffs ~N(0,0.1) on 31 of each agent's 512 "
                   "16-token sub-blocks (6 %), restored inside the Q4 read"),
 }
