@@ -187,6 +187,50 @@ def test_collective_call_equals_per_agent_calls(kind):
     assert K.kvs_pool_check(pool) == 0
 
 
+@pytest.mark.parametrize("kind", ["tiny", "allgather_rotation"])
+def test_fused_diff_overlay_equals_materialised_mirror(kind):
+    # the same attention with every mirror-diff block materialised as a plain
+    # block of its own (master + diff rounded to bf16, the agent's table
+    # pointing at it, no diff table): the fused overlay agrees with it, and
+    # each agrees with the oracle on its own values
+    import dataclasses
+    if kind == "tiny":
+        w = W.make_tiny()
+    else:
+        w = W.make_allgather(n_seq=4, n_segs=6, priv_blocks_lo=3, priv_blocks_hi=9, hq=10, hkv=2, n_layers=1)
+    segs = w.seg_start_off is not None
+    ref = OF.dedup(w.tokens, w.seq_off, w.tier, w.block_tokens, w.max_blocks,
+                   w.seg_start_off if segs else None, w.seg_start_blocks if segs else None)
+    table = ref["block_table"]
+    pool = H.bf16_pool(w)
+    q_bits = w.q_layer(0)
+    fused = H.attn(pool, 0, q_bits, w, table)
+    H.assert_close_attn(fused, oracle_out(w, pool, table, q_bits))
+    hst = pool.host[0]
+    kb, vb, dkb, dvb = hst["k"], hst["v"], hst["dk"], hst["dv"]
+    new_k, new_v = [kb], [vb]
+    table_m = table.copy()
+    nxt = kb.shape[0]
+    for a in range(w.n_seq):
+        for b in range(w.max_blocks):
+            d = int(w.diff_table[a, b])
+            if d < 0 or table[a, b] < 0:
+                continue
+            p = int(table[a, b])
+            new_k.append(W.f32_to_bf16_bits(f32(kb[p]) + f32(dkb[d]))[None])
+            new_v.append(W.f32_to_bf16_bits(f32(vb[p]) + f32(dvb[d]))[None])
+            table_m[a, b] = nxt
+            nxt += 1
+    assert nxt > kb.shape[0], "the workload carries mirror diffs"
+    km, vm = np.concatenate(new_k), np.concatenate(new_v)
+    wm = dataclasses.replace(w, diff_table=None, diff_capacity_blocks=0, capacity_blocks=km.shape[0])
+    pool_m = H.bf16_pool(wm, layers_np=[(km, vm)], with_diff=False)
+    mat = H.attn(pool_m, 0, q_bits, wm, table_m)
+    H.assert_close_attn(mat, oracle_out(wm, pool_m, table_m, q_bits))
+    H.assert_close_attn(fused, mat)
+    assert K.kvs_pool_check(pool) == 0 and K.kvs_pool_check(pool_m) == 0
+
+
 def test_edge_lengths():
     # empty context -> zeros; a single token -> that token's V; exact block
     # multiples and one-past.

@@ -76,6 +76,19 @@ def test_reference_lists_take_both_buffers():
         assert e.value.status == K.KVS_ERR_INVALID_ARG
 
 
+def test_rerun_is_bit_identical():
+    # the dedup has a fixed result for given inputs (no order from atomics
+    # reaches the outputs): a second call on the same inputs gives the same bits
+    w = W.make_allgather(n_seq=6, n_segs=9, priv_blocks_lo=1, priv_blocks_hi=7, hq=4, hkv=2, d=64, n_layers=1)
+    pool = H.bf16_pool(w, with_diff=False)
+    tier = np.array([0, 1, 0, W.PRIVATE_TIER, 1, 0], dtype=np.uint32)
+    first = H.gpu_dedup(pool, w, tier=tier)
+    second = H.gpu_dedup(pool, w, tier=tier)
+    for k in ("fp", "block_table", "refcount_full", "owner", "ref_off", "ref_seq"):
+        np.testing.assert_array_equal(first[k], second[k], err_msg=k)
+    assert first["n_phys"] == second["n_phys"]
+
+
 def test_tiers_and_private():
     w = W.make_gqa_fanout(n_seq=6, prefix_tokens=96, priv_lo=0, priv_hi=40, hq=4, hkv=2, d=64)
     tier = np.array([0, 1, 0, W.PRIVATE_TIER, 1, 0], dtype=np.uint32)
