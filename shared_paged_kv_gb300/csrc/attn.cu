@@ -427,6 +427,37 @@ attn_bf16_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ C
   {
     constexpr int CPT = D / 8;   // columns per thread: 16 rows x 8 threads
     const int r = threadIdx.x >> 3, c0 = (threadIdx.x & 7) * CPT;
+    if (nch == 1) {
+      // the whole context in this CTA: its combined state is the output (an
+      // empty context gives zeros)
+      if (r < p.g) {
+        float M = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < kAttnWarps; ++w)
+          if (s_wml[w][r].y > 0.f) M = fmaxf(M, s_wml[w][r].x);
+        float Lc = 0.f, o[CPT];
+#pragma unroll
+        for (int j = 0; j < CPT; ++j) o[j] = 0.f;
+#pragma unroll
+        for (int w = 0; w < kAttnWarps; ++w) {
+          const float2 ml = s_wml[w][r];
+          const float wt = ml.y > 0.f ? fast_exp2(ml.x - M) : 0.f;
+          Lc += wt * ml.y;
+          const float* src = s_acc + ((size_t)w * 16 + r) * D + c0;
+#pragma unroll
+          for (int j = 0; j < CPT; j += 4) {
+            const float4 x = *reinterpret_cast<const float4*>(src + j);
+            o[j] += wt * x.x; o[j + 1] += wt * x.y; o[j + 2] += wt * x.z; o[j + 3] += wt * x.w;
+          }
+        }
+        const float inv = Lc > 0.f ? 1.f / Lc : 0.f;
+        float* dst = p.out + ((size_t)a * p.hq + h * p.g + r) * D + c0;
+#pragma unroll
+        for (int j = 0; j < CPT; j += 4)
+          *reinterpret_cast<float4*>(dst + j) = make_float4(o[j] * inv, o[j + 1] * inv, o[j + 2] * inv, o[j + 3] * inv);
+      }
+      return;
+    }
     if (r < p.g) {
       float M = -INFINITY;
 #pragma unroll
@@ -546,7 +577,14 @@ static kvs_status attn_launch(kvs_pool* pool, int32_t layer, const void* q_dev, 
   if (g <= kTmMaxGroup && !use_small_path(pool, n_seq, max_blocks, g))
     return decode_attn_token_major(pool, layer, q_dev, n_q_heads, block_table_dev, max_blocks, seq_len_dev, n_seq,
                                    diff_table_dev, rope_off_dev, rope_segs_dev, theta, scale, out_dev, ws, stream);
-  const AttnPlan plan = attn_plan(pool, n_seq, max_blocks);
+  AttnPlan plan = attn_plan(pool, n_seq, max_blocks);
+  if (g <= kTmMaxGroup && max_blocks <= kSmallOneChunk) {
+    // a small call with short contexts: one CTA per (sequence, KV head)
+    // writes its output directly, with no split and no merge (the 4-agent,
+    // 24-block layer: 11.7-12.1 us against 12.9 us in three chunks)
+    plan.bpc = (max_blocks + kAttnWarps - 1) / kAttnWarps * kAttnWarps;
+    plan.n_chunks = 1;
+  }
   const long long grid = (long long)n_seq * d.num_kv_heads * plan.n_chunks;
   if (grid > 0x7fffffffll) return fail(KVS_ERR_CAPACITY, "decode_attn: grid too large");
   AttnParams prm{};

@@ -82,6 +82,9 @@ constexpr int kTmMaxGroup = 8;
 // (192 triples) took 12.9 us per layer there against 17.0 us planned; 16,384
 // sequences of that shape (786,432 triples) took 2.31 ms against 0.70 ms.
 constexpr long long kSmallCallWork = 2048;
+// small calls whose block tables are at most this long run one chunk per
+// (sequence, KV head): at most 8 blocks per warp, no split merge
+constexpr int kSmallOneChunk = 32;
 inline bool small_call(int n_seq, int num_kv_heads, int max_blocks, int g) {
   return g <= kTmMaxGroup && (long long)n_seq * num_kv_heads * max_blocks <= kSmallCallWork;
 }
