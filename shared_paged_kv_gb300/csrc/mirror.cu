@@ -6,20 +6,23 @@
 // master's frame).
 //
 // Steps, all on the device:
-//  1. mir_agent   one CTA per agent: validate the refreshed positions, flag
-//                 the logical blocks holding one and record, per (block,
-//                 row), which refreshed row it is; then count the agent's
-//                 dirty blocks;
+//  1. mir_agent   one CTA per agent: clear the agent's dirty flags, validate
+//                 the refreshed positions and flag the logical blocks holding
+//                 one; then count the agent's dirty blocks;
 //  2. mir_scan    exclusive scan of the per-agent counts (one CTA): diff ids
 //                 are consecutive in agent order, then block order;
-//  3. mir_apply   one CTA per agent: diff table, the list of dirty slots and,
-//                 for rotation calls, each dirty block's shift (the last
-//                 covering segment entry);
+//  3. mir_apply   one CTA per agent: diff table, the list of dirty slots,
+//                 each dirty block's refreshed rows (the first one's index
+//                 and a 16-bit mask: positions are sorted, so the k-th set
+//                 bit is refreshed row first + k) and, for rotation calls,
+//                 its shift (the last covering segment entry);
 //  4. mir_write   one warp per (dirty block, kv head): 16 rows, a refreshed
 //                 row becoming bf16(R(-delta) k_new - K_master) and
 //                 bf16(v_new - V_master), every other row zero.  Lane (row,
 //                 v) holds head dims [8v, 8v+8) and [d/2+8v, d/2+8v+8), so the
 //                 rotate-half partners sit in the same lane.
+// The four kernels are programmatic dependent launches: each waits for the
+// one before it at its first statement and lets the next be scheduled.
 #include "common.cuh"
 #include "internal.h"
 
@@ -30,7 +33,7 @@ constexpr int kMirB = 16;         // block tokens this path supports
 static size_t mir_align(size_t x) { return (x + 255) & ~size_t(255); }
 
 struct MirLayout {
-  size_t off_flags, off_rowmap, off_counts, off_list, off_delta, total;
+  size_t off_flags, off_rows, off_counts, off_list, off_delta, total;
 };
 
 static MirLayout mir_layout(int n_seq, int max_blocks) {
@@ -38,7 +41,7 @@ static MirLayout mir_layout(int n_seq, int max_blocks) {
   MirLayout L{};
   size_t o = 0;
   L.off_flags = o; o = mir_align(o + slots);
-  L.off_rowmap = o; o = mir_align(o + slots * kMirB * sizeof(int32_t));
+  L.off_rows = o; o = mir_align(o + slots * sizeof(int2));
   L.off_counts = o; o = mir_align(o + (size_t)(n_seq + 1) * sizeof(int32_t));
   L.off_list = o; o = mir_align(o + slots * sizeof(int32_t));
   L.off_delta = o; o = mir_align(o + slots * sizeof(int32_t));
@@ -64,7 +67,7 @@ struct MirParams {
   int32_t* diff_table;
   int32_t* n_diff;
   uint8_t* flags;     // [n_seq][max_blocks] 1 = dirty
-  int32_t* rowmap;    // [n_seq][max_blocks][16] refreshed row of each token, -1 if none
+  int2* rows;         // [n_diff] {first refreshed row, mask of refreshed tokens} per diff id
   int32_t* counts;    // [n_seq + 1] dirty blocks per agent, then their exclusive scan
   int32_t* list;      // [n_diff] dirty slot (a * max_blocks + b) of each diff id
   int32_t* dlt;       // [n_diff] RoPE shift of each dirty block (rotation calls)
@@ -75,6 +78,7 @@ struct MirParams {
 
 // 1. positions -> dirty flags and row map; dirty blocks per agent
 __global__ void __launch_bounds__(256) mir_agent(const __grid_constant__ MirParams p) {
+  pdl_enter();
   __shared__ int warp_sums[32];
   for (int a = blockIdx.x; a < p.n_seq; a += gridDim.x) {
     const long long r0 = p.idx_off[a], r1 = p.idx_off[a + 1];
@@ -84,6 +88,8 @@ __global__ void __launch_bounds__(256) mir_agent(const __grid_constant__ MirPara
       L = L < 0 ? 0 : p.max_blocks * kMirB;
     }
     uint8_t* fl = p.flags + (size_t)a * p.max_blocks;
+    for (int b = threadIdx.x; b < p.max_blocks; b += blockDim.x) fl[b] = 0;
+    __syncthreads();
     if (r0 < 0 || r1 < r0) {
       if (threadIdx.x == 0) set_err(p.status, KVS_DEVERR_JOB);
     } else {
@@ -94,7 +100,6 @@ __global__ void __launch_bounds__(256) mir_agent(const __grid_constant__ MirPara
           continue;
         }
         fl[t / kMirB] = 1;   // equal-value writes
-        p.rowmap[((size_t)a * p.max_blocks + t / kMirB) * kMirB + t % kMirB] = (int)r;
       }
     }
     __syncthreads();
@@ -108,6 +113,7 @@ __global__ void __launch_bounds__(256) mir_agent(const __grid_constant__ MirPara
 
 // 2. exclusive scan of the per-agent counts (one CTA); the total is n_diff
 __global__ void __launch_bounds__(1024) mir_scan(const __grid_constant__ MirParams p) {
+  pdl_enter();
   __shared__ int warp_sums[32];
   int carry = 0;
   for (int base = 0; base < p.n_seq; base += blockDim.x) {
@@ -129,6 +135,7 @@ __global__ void __launch_bounds__(1024) mir_scan(const __grid_constant__ MirPara
 constexpr int kMirSegChunk = 256;   // segment entries staged in shared memory at a time
 
 __global__ void __launch_bounds__(256) mir_apply(const __grid_constant__ MirParams p) {
+  pdl_enter();
   __shared__ int warp_sums[32];
   __shared__ int4 segs[kMirSegChunk];
   for (int a = blockIdx.x; a < p.n_seq; a += gridDim.x) {
@@ -146,10 +153,30 @@ __global__ void __launch_bounds__(256) mir_apply(const __grid_constant__ MirPara
         p.diff_table[slot] = f ? id : -1;
         if (f && id < p.diff_capacity) {
           p.list[id] = (int)slot;
+          p.rows[id] = make_int2(-1, 0);
           if (!p.rope_off) p.dlt[id] = 0;
         }
       }
       carry += total;
+    }
+    // each dirty block's refreshed rows: the thread holding the first valid
+    // position of a block records it, every valid position sets its bit (the
+    // validity test is mir_agent's, so an invalid position counts nowhere)
+    __syncthreads();   // the diff table entries above are read by other threads
+    {
+      const long long r0 = p.idx_off[a], r1 = p.idx_off[a + 1];
+      int L = p.seq_len[a];
+      L = L < 0 ? 0 : min(L, p.max_blocks * kMirB);
+      if (r0 >= 0 && r1 >= r0) {
+        for (long long r = r0 + threadIdx.x; r < r1; r += blockDim.x) {
+          const int t = p.idx[r];
+          if (t < 0 || t >= L || (r > r0 && p.idx[r - 1] >= t)) continue;
+          const int id = p.diff_table[(size_t)a * p.max_blocks + t / kMirB];
+          if (id < 0 || id >= p.diff_capacity) continue;
+          if (r == r0 || p.idx[r - 1] / kMirB != t / kMirB) p.rows[id].x = (int)r;
+          atomicOr(reinterpret_cast<unsigned int*>(&p.rows[id].y), 1u << (t % kMirB));
+        }
+      }
     }
     if (!p.rope_off) continue;
     // shifts of this agent's dirty blocks: the last covering entry, the
@@ -185,6 +212,7 @@ __global__ void __launch_bounds__(256) mir_apply(const __grid_constant__ MirPara
 // 4. diff tiles of every dirty (block, kv head)
 template <int D>
 __global__ void __launch_bounds__(256) mir_write(const __grid_constant__ MirParams p) {
+  pdl_enter();
   constexpr int VEC = 8;              // bf16 per 16-byte vector
   constexpr int NV = D / 2 / VEC;     // lanes per row
   constexpr int RPS = 32 / NV;        // rows per warp step
@@ -204,8 +232,17 @@ __global__ void __launch_bounds__(256) mir_write(const __grid_constant__ MirPara
     const int phys = p.table[slot];
     const bool valid = phys >= 0 && phys < p.capacity;
     if (!valid && lane == 0 && h == 0) set_err(p.status, KVS_DEVERR_BLOCK_ID);
-    // lane j < 16: the refreshed row of token j of the block (or -1)
-    const int myrow = lane < kMirB ? p.rowmap[(size_t)slot * kMirB + lane] : -1;
+    // lane j < 16: the refreshed row of token j of the block (or -1): the
+    // k-th refreshed token of the block is row first + k (positions are
+    // sorted); a row outside the agent's list (only after invalid input,
+    // which mir_agent flags) is treated as not refreshed
+    const int2 ri = p.rows[id];
+    const int a = slot / p.max_blocks;
+    const long long ra = p.idx_off[a], rb = p.idx_off[a + 1];
+    long long rr = -1;
+    if (lane < kMirB && ri.x >= 0 && ((ri.y >> lane) & 1))
+      rr = (long long)ri.x + __popc((unsigned)ri.y & ((1u << lane) - 1u));
+    const int myrow = (rr >= ra && rr < rb && rr >= 0) ? (int)rr : -1;
     float cs[VEC], sn[VEC];
     const int delta = p.rope_off ? p.dlt[id] : 0;
 #pragma unroll
@@ -312,7 +349,7 @@ extern "C" kvs_status kvs_mirror_build(kvs_pool* pool, int32_t layer, const int3
   p.diff_table = diff_table_dev;
   p.n_diff = n_diff_dev;
   p.flags = w + L.off_flags;
-  p.rowmap = reinterpret_cast<int32_t*>(w + L.off_rowmap);
+  p.rows = reinterpret_cast<int2*>(w + L.off_rows);
   p.counts = reinterpret_cast<int32_t*>(w + L.off_counts);
   p.list = reinterpret_cast<int32_t*>(w + L.off_list);
   p.dlt = reinterpret_cast<int32_t*>(w + L.off_delta);
@@ -323,21 +360,17 @@ extern "C" kvs_status kvs_mirror_build(kvs_pool* pool, int32_t layer, const int3
   p.capacity = d.capacity_blocks;
   p.diff_capacity = d.diff_capacity_blocks;
   if (rope_off_dev) rope_split_host(theta, d.head_dim, p.rs.c);
-  const size_t slots = (size_t)n_seq * max_blocks;
-  if (cudaMemsetAsync(p.flags, 0, slots, stream) != cudaSuccess ||
-      cudaMemsetAsync(p.rowmap, 0xff, slots * kMirB * sizeof(int32_t), stream) != cudaSuccess)
-    return fail(KVS_ERR_CUDA, "mirror_build: memset failed");
   const int sms = pool->num_sms;
   const int agent_grid = std::min(n_seq, sms * 8);
-  mir_agent<<<agent_grid, 256, 0, stream>>>(p);
-  mir_scan<<<1, 1024, 0, stream>>>(p);
-  mir_apply<<<agent_grid, 256, 0, stream>>>(p);
+  cudaError_t e = launch_pdl(mir_agent, dim3(agent_grid), dim3(256), stream, p);
+  if (e == cudaSuccess) e = launch_pdl(mir_scan, dim3(1), dim3(1024), stream, p);
+  if (e == cudaSuccess) e = launch_pdl(mir_apply, dim3(agent_grid), dim3(256), stream, p);
   // the dirty count is only known on the device: a persistent grid of warps
   // walks the (dirty block, kv head) units
-  if (d.head_dim == 128)
-    mir_write<128><<<sms * 8, 256, 0, stream>>>(p);
-  else
-    mir_write<64><<<sms * 8, 256, 0, stream>>>(p);
+  if (e == cudaSuccess)
+    e = d.head_dim == 128 ? launch_pdl(mir_write<128>, dim3(sms * 8), dim3(256), stream, p)
+                          : launch_pdl(mir_write<64>, dim3(sms * 8), dim3(256), stream, p);
+  if (e != cudaSuccess) return fail(KVS_ERR_CUDA, "mirror_build: launch failed");
   count_launch(4);
   return check_launch("mirror_build");
 }
