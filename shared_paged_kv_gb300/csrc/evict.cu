@@ -18,6 +18,7 @@
 namespace kvs {
 
 constexpr int kEvMaxRegions = 16;
+constexpr int kEvUnroll = 4;   // blocks per half-warp whose loads are in flight together
 
 struct EvictParams {
   const uint8_t* region;
@@ -53,6 +54,7 @@ __global__ void __launch_bounds__(1024) evict_kernel(const __grid_constant__ Evi
   __shared__ unsigned s_prefix;
   __shared__ int s_remaining;
   __shared__ long long s_out0;
+  __shared__ long long s_part[32];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   for (int a = blockIdx.x; a < p.n_seq; a += gridDim.x) {
     int L = p.seq_len[a];
@@ -62,43 +64,59 @@ __global__ void __launch_bounds__(1024) evict_kernel(const __grid_constant__ Evi
     }
     const int nb = (L + p.B - 1) / p.B;
     float* srow = p.scores + (size_t)a * p.max_blocks;
-    // ---- 1. block scores: a half-warp per block (B <= 16), one lane per token
+    // ---- 1. block scores: a half-warp per block (B <= 16), one lane per token;
+    // the loads of kEvUnroll blocks per half-warp go out before any is used
     const int half = lane >> 4, hl = lane & 15;
-    for (int b0 = warp * 2; b0 < p.max_blocks; b0 += 64) {
-      const int b = b0 + half;
-      float s = 0.f;
-      int cnt = 0;
-      if (b < nb && hl < p.B) {
-        const int t = b * p.B + hl;
-        if (t < L) {
-          const size_t o = (size_t)a * p.max_blocks * p.B + t;
-          int r = p.region[o];
-          if (r >= p.n_regions) {
-            set_err(p.status, KVS_DEVERR_JOB);
-            r = -1;
-          }
-          if (r >= 0) {
-            const float age = (float)(p.step - (long long)p.created[o]);
-            s = p.init[r] * expf(-p.decay[r] * age);
-            const int acc = p.access[o];
-            if (acc > 0) s *= 1.f + 0.1f * log1pf((float)acc);
-          }
-          cnt = 1;
-        }
+    for (int b0 = warp * 2; b0 < p.max_blocks; b0 += 64 * kEvUnroll) {
+      int rg[kEvUnroll], cr[kEvUnroll], ac[kEvUnroll];
+      bool on[kEvUnroll];
+#pragma unroll
+      for (int j = 0; j < kEvUnroll; ++j) {
+        const int b = b0 + 64 * j + half, t = b * p.B + hl;
+        on[j] = b < nb && hl < p.B && t < L;
+        const size_t o = (size_t)a * p.max_blocks * p.B + t;
+        rg[j] = on[j] ? (int)p.region[o] : -1;
+        cr[j] = on[j] ? p.created[o] : 0;
+        ac[j] = on[j] ? p.access[o] : 0;
       }
 #pragma unroll
-      for (int off = 8; off; off >>= 1) {
-        s += __shfl_xor_sync(0xffffffffu, s, off);
-        cnt += __shfl_xor_sync(0xffffffffu, cnt, off);
+      for (int j = 0; j < kEvUnroll; ++j) {
+        const int b = b0 + 64 * j + half;
+        float s = 0.f;
+        int r = rg[j];
+        if (r >= p.n_regions) {
+          set_err(p.status, KVS_DEVERR_JOB);
+          r = -1;
+        }
+        if (r >= 0) {
+          const float age = (float)(p.step - (long long)cr[j]);
+          s = p.init[r] * expf(-p.decay[r] * age);
+          if (ac[j] > 0) s *= 1.f + 0.1f * log1pf((float)ac[j]);
+        }
+        int cnt = on[j] ? 1 : 0;
+#pragma unroll
+        for (int off = 8; off; off >>= 1) {
+          s += __shfl_xor_sync(0xffffffffu, s, off);
+          cnt += __shfl_xor_sync(0xffffffffu, cnt, off);
+        }
+        if (hl == 0 && b < p.max_blocks) srow[b] = b < nb ? s / (float)cnt : INFINITY;
       }
-      if (hl == 0 && b < p.max_blocks) srow[b] = b < nb ? s / (float)cnt : INFINITY;
+    }
+    // ---- 2. the k-th lowest bit pattern.  The output offset of this
+    // sequence's victims is the sum of the counts of the sequences before it,
+    // summed by all threads.
+    const int k = ev_k(p, a);
+    {
+      long long part = 0;
+      for (int c = threadIdx.x; c < a; c += blockDim.x) part += ev_k(p, c);
+#pragma unroll
+      for (int off = 16; off; off >>= 1) part += __shfl_xor_sync(0xffffffffu, part, off);
+      if (lane == 0) s_part[warp] = part;
     }
     __syncthreads();
-    // ---- 2. the k-th lowest bit pattern
-    const int k = ev_k(p, a);
     if (threadIdx.x == 0) {
       long long o = 0;
-      for (int c = 0; c < a; ++c) o += ev_k(p, c);
+      for (int w = 0; w < (int)(blockDim.x >> 5); ++w) o += s_part[w];
       s_out0 = o;
       p.victims_off[a] = o;
       if (a == p.n_seq - 1) p.victims_off[p.n_seq] = o + k;
@@ -119,15 +137,40 @@ __global__ void __launch_bounds__(1024) evict_kernel(const __grid_constant__ Evi
           if ((v & mask) == pre) atomicAdd(&hist[(v >> shift) & 255u], 1u);
         }
         __syncthreads();
-        if (threadIdx.x == 0) {
-          int rem = s_remaining;
-          int digit = 0;
-          for (; digit < 255; ++digit) {
-            if ((int)hist[digit] >= rem) break;
-            rem -= hist[digit];
+        if (warp == 0) {
+          // the digit: the first bin whose running count reaches the
+          // remaining rank (bin 255 if none does); lane l scans bins 8l..8l+7
+          // after a prefix sum of the lanes' totals
+          unsigned c8[8], lsum = 0u;
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            c8[j] = hist[lane * 8 + j];
+            lsum += c8[j];
           }
-          s_prefix = pre | ((unsigned)digit << shift);
-          s_remaining = rem;
+          unsigned incl = lsum;
+#pragma unroll
+          for (int off = 1; off < 32; off <<= 1) {
+            const unsigned y = __shfl_up_sync(0xffffffffu, incl, off);
+            if (lane >= off) incl += y;
+          }
+          const unsigned excl = incl - lsum;
+          const unsigned rem0 = (unsigned)s_remaining;
+          const bool mine = excl < rem0 && rem0 <= incl;
+          const unsigned who = __ballot_sync(0xffffffffu, mine);
+          if (mine) {
+            unsigned r = rem0 - excl;
+            int digit = lane * 8 + 7;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              if (c8[j] >= r) { digit = lane * 8 + j; break; }
+              r -= c8[j];
+            }
+            s_prefix = pre | ((unsigned)digit << shift);
+            s_remaining = (int)r;
+          } else if (who == 0u && lane == 31) {
+            s_prefix = pre | (255u << shift);
+            s_remaining = (int)(rem0 - (incl - c8[7]));
+          }
         }
         __syncthreads();
         mask |= 255u << shift;
