@@ -131,9 +131,12 @@ __global__ void dedup_prep(DedupParams p) {
   }
   const uint32_t tier = p.tier ? p.tier[s] : 0u;
   const size_t row = (size_t)s * p.max_blocks;
-  for (int b = lane; b < p.max_blocks; b += 32) p.segstart[row + b] = 0;
-  __syncwarp();
-  if (p.seg_off) {
+  // without a segment list every block's segment starts at block 0: the marks
+  // are all zero and need neither clearing nor reading back below
+  const bool segs = p.seg_off != nullptr;
+  if (segs) {
+    for (int b = lane; b < p.max_blocks; b += 32) p.segstart[row + b] = 0;
+    __syncwarp();
     // An entry starts a segment iff it lies inside the sequence and beyond
     // every earlier in-range entry (unsorted and out-of-range starts are
     // ignored); each accepted start marks its own block.
@@ -156,15 +159,23 @@ __global__ void dedup_prep(DedupParams p) {
     }
     __syncwarp();
   }
-  // the segment start of every block is the running maximum of the marks
+  // the segment start of every block is the running maximum of the marks;
+  // the fingerprints and marks of the next two chunks are loaded ahead of use
+  // (the chunk written back is always behind the ones read ahead)
   int scarry = 0;
   uint64_t carryA = 1, carryC = 0;
-  uint64_t fp_next = lane < p.max_blocks ? p.fp_out[row + lane] : 0;
+  uint64_t fp_n1 = lane < p.max_blocks ? p.fp_out[row + lane] : 0;
+  uint64_t fp_n2 = lane + 32 < p.max_blocks ? p.fp_out[row + lane + 32] : 0;
+  int st_n1 = (segs && lane < nblk) ? p.segstart[row + lane] : 0;
+  int st_n2 = (segs && lane + 32 < nblk) ? p.segstart[row + lane + 32] : 0;
   for (int base = 0; base < p.max_blocks; base += 32) {
     const int b = base + lane;
-    const uint64_t fp = fp_next;
-    fp_next = b + 32 < p.max_blocks ? p.fp_out[row + b + 32] : 0;   // the next chunk's, ahead of use
-    int st = (b < nblk) ? p.segstart[row + b] : 0;
+    const uint64_t fp = fp_n1;
+    fp_n1 = fp_n2;
+    fp_n2 = b + 64 < p.max_blocks ? p.fp_out[row + b + 64] : 0;
+    int st = (b < nblk) ? st_n1 : 0;
+    st_n1 = st_n2;
+    st_n2 = (segs && b + 64 < nblk) ? p.segstart[row + b + 64] : 0;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
       const int y = __shfl_up_sync(0xffffffffu, st, o);
