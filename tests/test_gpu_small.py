@@ -79,6 +79,14 @@ def test_rotation_and_diffs_group5():
     both_paths(w)
 
 
+def test_one_chunk_rotation_and_diffs():
+    # block tables of at most 32 blocks: one CTA per (sequence, KV head)
+    # writes the output directly; here with rotated segments and mirror diffs
+    w = W.make_allgather(n_seq=3, n_segs=2, priv_blocks_lo=1, priv_blocks_hi=4, hq=10, hkv=2, n_layers=1)
+    assert w.max_blocks <= 32 and (w.diff_table >= 0).any() and w.rope_off is not None
+    both_paths(w)
+
+
 def test_edge_lengths_small_path():
     # empty context -> zeros; a single token; a block multiple and one past
     w = W.make_gqa_fanout(n_seq=5, prefix_tokens=64, priv_lo=40, priv_hi=90, hq=8, hkv=2, d=128)
