@@ -425,8 +425,9 @@ attn_wide_kernel(const __grid_constant__ WideParams p, const __grid_constant__ C
           const int r2 = qd * 32 + jr, sl = r2 / p.g, h2 = r2 - sl * p.g, a2 = e_gw * p.W + sl;
           if (sl < p.W && a2 < p.n_seq && ((e_spm >> sl) & 1u)) {
             const size_t it2 = (((size_t)a2 * p.hkv + e_h) * p.n_chunks + e_c) * p.g + h2;
-            __stcg(reinterpret_cast<uint4*>(p.p2 + it2 * 128 + 32 * q + 4 * e),
-                   *reinterpret_cast<const uint4*>(stg + jr * 128 + ((e ^ (jr & 7)) << 4)));
+            // evict-last, as the token-major kernel's splits: the merge reads it back
+            st_hint_v4u32(p.p2 + it2 * 128 + 32 * q + 4 * e,
+                          *reinterpret_cast<const uint4*>(stg + jr * 128 + ((e ^ (jr & 7)) << 4)), l2_policy_evict_last());
           }
         }
         __syncwarp();
