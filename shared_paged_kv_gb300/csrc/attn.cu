@@ -385,11 +385,10 @@ attn_bf16_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ C
         }
       }
     }
+    // the copy overwrites tiles this warp has only read, and those reads have
+    // completed (their registers fed the MMAs above): no proxy fence needed
     __syncwarp();
-    if (lane == 0 && i + S < n_mine) {
-      fence_proxy_async_smem();
-      issue(i + S, s);
-    }
+    if (lane == 0 && i + S < n_mine) issue(i + S, s);
   }
   if (timed_out) {
     // drain the copies this warp still has in flight (each wait bounded)

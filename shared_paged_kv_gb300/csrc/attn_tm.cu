@@ -1157,7 +1157,6 @@ attn_tm_kernel(const __grid_constant__ TmParams p, const __grid_constant__ CUten
       for (int e = 0; e < 4; ++e) sc[e] += sd[e];
       if (has_diff) {   // K and DK have been read: stage s takes the next position now
         __syncwarp();
-        if (lane == 0) fence_proxy_async_smem();
         issue(s);
       }
       // sc: (t=g, col 2c), (g, 2c+1), (g+8, 2c), (g+8, 2c+1); a column is live
@@ -1222,8 +1221,10 @@ attn_tm_kernel(const __grid_constant__ TmParams p, const __grid_constant__ CUten
         }
       }
     }
+    // The copies issued next overwrite tiles that this warp has only read, and
+    // every such read (an ldmatrix whose registers the MMAs above consumed) has
+    // completed, so no proxy fence is needed before the async-proxy writes.
     __syncwarp();
-    if (lane == 0) fence_proxy_async_smem();
     if (!(loaded && has_diff)) issue(s);   // (a loaded diff block released s after S)
     if (has_diff) issue(s2);
     i += has_diff ? 2 : 1;

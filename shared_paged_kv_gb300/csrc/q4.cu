@@ -517,7 +517,9 @@ q4_attn_kernel(const __grid_constant__ Q4Params p, const __grid_constant__ CUten
       if (!mbar_wait_bounded(&empty[s], (i / kQ4Stages) & 1, p.status)) {
         timed_out = true;
       } else {
-        fence_proxy_async_smem();
+        // every warp has arrived after its last read of the stage (plain
+        // reads that have completed): the copy may overwrite it with no
+        // proxy fence
         issue(i + kQ4Stages, s);
       }
     }
