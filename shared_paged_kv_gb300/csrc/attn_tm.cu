@@ -734,11 +734,6 @@ attn_tm_kernel(const __grid_constant__ TmParams p, const __grid_constant__ CUten
   static_assert(kTmRec > S + 1, "claim records must outnumber the items a ring can hold");
   extern __shared__ uint8_t smem_raw[];
   __shared__ uint64_t bars[kTmWarps][S];
-  // per stage {claim ordinal (-1: no more work), block index (bit 30: the
-  // next position holds the block's diff tiles; bit 29: the block id was out
-  // of range and nothing was loaded), group members whose columns take this
-  // block, RoPE shift of the block (rotation calls)}
-  __shared__ int4 st_rec[kTmWarps][S];
   __shared__ TmRec recs[kTmWarps][kTmRec];
   __shared__ float rsc[ROPE ? 4 * 64 : 1];   // RoPE frequency pieces (rotation calls)
 
@@ -890,6 +885,20 @@ attn_tm_kernel(const __grid_constant__ TmParams p, const __grid_constant__ CUten
       nn_it = load_item(n_id + T);
     }
   };
+  // Per stage, the record of what it holds: {claim ordinal (-1: no more
+  // work), block index (bit 30: the next position holds the block's diff
+  // tiles; bit 29: the block id was out of range and nothing was loaded),
+  // group members whose columns take this block, RoPE shift of the block
+  // (rotation calls)}.  Every field is warp-uniform, so each lane keeps its
+  // own copy in registers (selected by stage, never indexed dynamically).
+  int4 st_rec[S];
+#pragma unroll
+  for (int j = 0; j < S; ++j) st_rec[j] = make_int4(-1, 0, 0, 0);
+  auto set_rec = [&](int s, const int4& v) {
+#pragma unroll
+    for (int j = 0; j < S; ++j)
+      if (j == s) st_rec[j] = v;
+  };
   // A block that carries a mirror diff takes two positions: {K, DK}, then
   // {V, DV}, so that the first is free as soon as S has been computed.
   int pend_drow = -1, pend_row = 0;   // the {V, DV} position still to issue for the last block
@@ -928,10 +937,8 @@ attn_tm_kernel(const __grid_constant__ TmParams p, const __grid_constant__ CUten
       break;
     }
     if (p_done) {
-      if (lane == 0) {
-        st_rec[warp][s] = make_int4(-1, 0, 0, 0);
-        mbar_arrive(bar);
-      }
+      set_rec(s, make_int4(-1, 0, 0, 0));
+      if (lane == 0) mbar_arrive(bar);
       return;
     }
     const bool valid = phys >= 0 && phys < p.capacity;
@@ -940,21 +947,19 @@ attn_tm_kernel(const __grid_constant__ TmParams p, const __grid_constant__ CUten
       pend_drow = (did * p.hkv + p_h) * B;
       pend_row = (phys * p.hkv + p_h) * B;
     }
-    if (lane != 0) return;
-    if (p.stall_first && stall_pending) {
-      // test-only: this stage is never armed, so its wait runs out
-      stall_pending = false;
-      st_rec[warp][s] = make_int4(ord, b | (1 << 29), mask, dlt);
-      return;
-    }
+    // test-only: the first stage of warp 0 of CTA 0 is never armed, so its
+    // wait runs out
+    const bool stall = p.stall_first && stall_pending;
+    stall_pending = false;
+    // nothing loaded (stall, or a block id out of range): the consumer skips it
+    set_rec(s, make_int4(ord, (stall || !valid) ? (b | (1 << 29)) : dval ? (b | (1 << 30)) : b, mask, dlt));
+    if (lane != 0 || stall) return;
     if (!valid) {
       set_err(p.status, KVS_DEVERR_BLOCK_ID);
-      st_rec[warp][s] = make_int4(ord, b | (1 << 29), mask, dlt);   // nothing loaded: skip this block
       mbar_arrive(bar);
       return;
     }
     if (DIFF && did >= p.diff_capacity) set_err(p.status, KVS_DEVERR_DIFF_ID);
-    st_rec[warp][s] = make_int4(ord, dval ? (b | (1 << 30)) : b, mask, dlt);
     mbar_arrive_expect_tx(bar, 2 * TILE);
     const int row = (phys * p.hkv + p_h) * B;
     // K and V of a block are read once per call here, and so are the diff
@@ -1080,11 +1085,14 @@ attn_tm_kernel(const __grid_constant__ TmParams p, const __grid_constant__ CUten
   bool timed_out = false;
   for (;;) {
     const int s = i % S;
-    // The stage's record was written by lane 0 when it armed the stage: the
-    // item switch (the previous item's split stores, the next query loads)
-    // and the query rotation below run while the stage's copies are in flight.
+    // The stage's record was set when the stage was armed: the item switch
+    // (the previous item's split stores, the next query loads) and the query
+    // rotation below run while the stage's copies are in flight.
     __syncwarp();
-    const int4 srec = st_rec[warp][s];
+    int4 srec = st_rec[0];
+#pragma unroll
+    for (int j = 1; j < S; ++j)
+      if (j == s) srec = st_rec[j];
     const int item = srec.x, bword = srec.y, emask = srec.z;
     if (item < 0) break;   // armed without copies: the claims are exhausted
     const bool has_diff = DIFF && (bword >> 30) != 0;
