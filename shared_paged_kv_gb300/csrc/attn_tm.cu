@@ -43,6 +43,8 @@
 namespace kvs {
 
 constexpr int kTmWarps = 4;
+// Lazy-rescale threshold of the online softmax, in log2 units of P.
+constexpr float kTmLazyLog2 = 8.f;
 constexpr int kTmMaxIb = 32;
 constexpr int kTmRec = 8;   // claim records per warp (more than stages + 1)
 constexpr int kPlanMagic = 0x6b76730a;
@@ -1178,33 +1180,43 @@ attn_tm_kernel(const __grid_constant__ TmParams p, const __grid_constant__ CUten
         sc[2] = g + 8 < lim0 ? sc[2] * p.scale_log2 : -INFINITY;
         sc[3] = g + 8 < lim1 ? sc[3] * p.scale_log2 : -INFINITY;
       }
-      float mx0 = fmaxf(sc[0], sc[2]), mx1 = fmaxf(sc[1], sc[3]);
+      // Lazy rescale: a column keeps its reference point m while none of its
+      // scores exceeds m by more than kTmLazyLog2, so most blocks need no
+      // reduction of the column maxima over the tile.  P then stays below
+      // 2^kTmLazyLog2, which the bf16 hi + lo split and the fp32 sums carry at
+      // full relative precision, and (m, l, acc) keep one reference point
+      // for the merge.
+      const float t0 = fmaxf(sc[0], sc[2]), t1 = fmaxf(sc[1], sc[3]);
+      if (__any_sync(0xffffffffu, t0 > m[0] + kTmLazyLog2 || t1 > m[1] + kTmLazyLog2)) {
+        float mx0 = t0, mx1 = t1;
 #pragma unroll
-      for (int o = 4; o < 32; o <<= 1) {
-        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
-        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
-      }
-      const float mn0 = fmaxf(m[0], mx0), mn1 = fmaxf(m[1], mx1);
-      // a column with nothing live yet keeps (m, l, acc) = (-inf, 0, 0): its
-      // reference point is taken as 0 so that exp2(-inf - 0) = 0
-      const float r0 = mn0 == -INFINITY ? 0.f : mn0, r1 = mn1 == -INFINITY ? 0.f : mn1;
-      const float al0 = fast_exp2(m[0] - r0), al1 = fast_exp2(m[1] - r1);
-      m[0] = mn0;
-      m[1] = mn1;
-      sc[0] = fast_exp2(sc[0] - r0);
-      sc[1] = fast_exp2(sc[1] - r1);
-      sc[2] = fast_exp2(sc[2] - r0);
-      sc[3] = fast_exp2(sc[3] - r1);
-      l[0] = l[0] * al0 + sc[0] + sc[2];
-      l[1] = l[1] * al1 + sc[1] + sc[3];
-      // rescale the accumulators only when some column's maximum moved
-      if (__any_sync(0xffffffffu, al0 != 1.f || al1 != 1.f)) {
+        for (int o = 4; o < 32; o <<= 1) {
+          mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
+          mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
+        }
+        const float mn0 = fmaxf(m[0], mx0), mn1 = fmaxf(m[1], mx1);
+        // (a column whose state is still empty has l = 0 and acc = 0)
+        const float al0 = m[0] == -INFINITY ? 0.f : fast_exp2(m[0] - mn0);
+        const float al1 = m[1] == -INFINITY ? 0.f : fast_exp2(m[1] - mn1);
+        m[0] = mn0;
+        m[1] = mn1;
+        l[0] *= al0;
+        l[1] *= al1;
 #pragma unroll
         for (int mt = 0; mt < D / 16; ++mt) {
           acc[mt][0] *= al0; acc[mt][1] *= al1;
           acc[mt][2] *= al0; acc[mt][3] *= al1;
         }
       }
+      // a column with nothing live yet keeps (m, l, acc) = (-inf, 0, 0): its
+      // reference point is taken as 0 so that exp2(-inf - 0) = 0
+      const float r0 = m[0] == -INFINITY ? 0.f : m[0], r1 = m[1] == -INFINITY ? 0.f : m[1];
+      sc[0] = fast_exp2(sc[0] - r0);
+      sc[1] = fast_exp2(sc[1] - r1);
+      sc[2] = fast_exp2(sc[2] - r0);
+      sc[3] = fast_exp2(sc[3] - r1);
+      l[0] += sc[0] + sc[2];
+      l[1] += sc[1] + sc[3];
       // a diff block's {V, DV} tiles (the stage after S's) are needed from here
       // on: S and the softmax above overlapped their copy
       if (has_diff && !mbar_wait_bounded(&bars[warp][s2], ((i + 1) / S) & 1, p.status)) {
