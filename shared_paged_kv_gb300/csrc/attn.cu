@@ -332,31 +332,43 @@ attn_bf16_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ C
         mx0 = fmaxf(mx0, fmaxf(sc[n][0], sc[n][1]));
         mx1 = fmaxf(mx1, fmaxf(sc[n][2], sc[n][3]));
       }
-      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
-      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
-      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
-      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
-      const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
-      const float al0 = fast_exp2(m0 - mn0), al1 = fast_exp2(m1 - mn1);
+      // Lazy rescale: a row keeps its reference point while none of its
+      // scores exceeds it by more than 2^8 in P (the bf16 hi + lo split and
+      // the fp32 sums carry such P at full relative precision); only then are
+      // the row maxima reduced and l and the accumulators rescaled.
+      if (__any_sync(0xffffffffu, mx0 > m0 + 8.f || mx1 > m1 + 8.f)) {
+        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
+        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
+        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
+        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
+        const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+        // (a row whose state is still empty has l = 0 and acc = 0)
+        const float al0 = m0 == -INFINITY ? 0.f : fast_exp2(m0 - mn0);
+        const float al1 = m1 == -INFINITY ? 0.f : fast_exp2(m1 - mn1);
+        m0 = mn0;
+        m1 = mn1;
+        l0 *= al0;
+        l1 *= al1;
+#pragma unroll
+        for (int n = 0; n < D / 8; ++n) {
+          acc[n][0] *= al0; acc[n][1] *= al0;
+          acc[n][2] *= al1; acc[n][3] *= al1;
+        }
+      }
+      // nothing live yet: reference point 0, so that 2^(-inf - 0) = 0
+      const float r0 = m0 == -INFINITY ? 0.f : m0, r1 = m1 == -INFINITY ? 0.f : m1;
       float ps0 = 0.f, ps1 = 0.f;
 #pragma unroll
       for (int n = 0; n < 2; ++n) {
-        sc[n][0] = fast_exp2(sc[n][0] - mn0);
-        sc[n][1] = fast_exp2(sc[n][1] - mn0);
-        sc[n][2] = fast_exp2(sc[n][2] - mn1);
-        sc[n][3] = fast_exp2(sc[n][3] - mn1);
+        sc[n][0] = fast_exp2(sc[n][0] - r0);
+        sc[n][1] = fast_exp2(sc[n][1] - r0);
+        sc[n][2] = fast_exp2(sc[n][2] - r1);
+        sc[n][3] = fast_exp2(sc[n][3] - r1);
         ps0 += sc[n][0] + sc[n][1];
         ps1 += sc[n][2] + sc[n][3];
       }
-      l0 = l0 * al0 + ps0;
-      l1 = l1 * al1 + ps1;
-      m0 = mn0;
-      m1 = mn1;
-#pragma unroll
-      for (int n = 0; n < D / 8; ++n) {
-        acc[n][0] *= al0; acc[n][1] *= al0;
-        acc[n][2] *= al1; acc[n][3] *= al1;
-      }
+      l0 += ps0;
+      l1 += ps1;
       // P = P_hi + P_lo, both bf16, so the probabilities enter the PV MMA to
       // ~16 significant bits (V is exact bf16)
       uint32_t pa[4], pl[4];
