@@ -1282,19 +1282,17 @@ constexpr int kMergeBatch = KVS_MERGE_BATCH;
 // robin: warp wq of the row takes slots wq, wq + wpr, wq + 2 wpr, ...
 // Existing splits sit in runs of consecutive slots (a sequence's chunks with
 // unshared work, the chunks of its shared prefix), so every warp gets about
-// the same number of them and loads them in one batch.  Each warp reads the
-// (m, l) of every slot of the row to find the row's maximum M itself (all
-// those 8-byte loads in flight together, with the (m, l) of its own slots),
-// so the warps' parts are relative to the same M and combine by plain sums
-// in a fixed order.
-constexpr int kMergeWin = 4;   // 32-slot windows whose loads are issued together
+// the same number of them and loads them in one batch.  Each warp reads only
+// its own slots' (m, l) and sums its splits relative to its own maximum; the
+// row's warps then rescale their parts to the row's maximum and add them in
+// a fixed order, so results are deterministic.
 
 template <int D>
 __global__ void __launch_bounds__(kMergeWarps * 32, KVS_MERGE_MIN_CTAS)
 tm_merge_kernel(const __grid_constant__ TmParams p) {
   constexpr int CPL = D / 32;   // columns per lane
   __shared__ __align__(16) float sv[kMergeWarps][D];
-  __shared__ float sL[kMergeWarps];
+  __shared__ float sL[kMergeWarps], sM[kMergeWarps];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int wpr = p.mwpr;
   const int rl = warp / wpr, wq = warp - rl * wpr;
@@ -1345,23 +1343,21 @@ tm_merge_kernel(const __grid_constant__ TmParams p) {
     return __ldcg(reinterpret_cast<const float2*>(base + ml_off(sl) * 2));
   };
 
-  // 1. M of the row: lane k reads slots k, k + 32, ... (consecutive (m, l),
-  // two or three lines per load); the (m, l) of this lane's own slots in the
-  // first two passes of step 2 come along
+  // 1. This warp's slots (lane k of pass j: slot 32 * wpr * j + k * wpr + wq)
+  // and the warp's own maximum Mw over the splits among them.  The (m, l) of
+  // the first two passes are loaded together and kept for step 2.
   const float2 own0 = load_ml(lane * wpr + wq), own1 = load_ml(32 * wpr + lane * wpr + wq);
-  float M = -INFINITY;
-  for (int w0 = 0; w0 < n_slots; w0 += 32 * kMergeWin) {
-    float2 ml[kMergeWin];
-#pragma unroll
-    for (int k = 0; k < kMergeWin; ++k) ml[k] = load_ml(w0 + k * 32 + lane);
-#pragma unroll
-    for (int k = 0; k < kMergeWin; ++k)
-      if (ml[k].y > 0.f) M = fmaxf(M, ml[k].x);
+  float Mw = -INFINITY;
+  if (own0.y > 0.f) Mw = own0.x;
+  if (own1.y > 0.f) Mw = fmaxf(Mw, own1.x);
+  for (int base = 64 * wpr; base < n_slots; base += 32 * wpr) {   // rows of more than 64 * wpr slots
+    const float2 ml = load_ml(base + lane * wpr + wq);
+    if (ml.y > 0.f) Mw = fmaxf(Mw, ml.x);
   }
 #pragma unroll
-  for (int off = 16; off; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+  for (int off = 16; off; off >>= 1) Mw = fmaxf(Mw, __shfl_xor_sync(0xffffffffu, Mw, off));
 
-  // 2. this warp's slots, 32 per pass (lane k: slot base + k * wpr + wq)
+  // 2. the warp's splits, weighted relative to Mw
   float v[CPL], Lw = 0.f;
 #pragma unroll
   for (int j = 0; j < CPL; ++j) v[j] = 0.f;
@@ -1369,7 +1365,7 @@ tm_merge_kernel(const __grid_constant__ TmParams p) {
     const int sl = base + lane * wpr + wq;
     const float2 ml = base == 0 ? own0 : base == 32 * wpr ? own1 : load_ml(sl);
     const bool ex = ml.y > 0.f;
-    const float wk = ex ? fast_exp2(ml.x - M) : 0.f;
+    const float wk = ex ? fast_exp2(ml.x - Mw) : 0.f;
     Lw += wk * ml.y;
     unsigned mk = __ballot_sync(0xffffffffu, ex);
     while (mk) {   // warp-uniform: up to kMergeBatch splits, their loads all in flight
@@ -1402,17 +1398,30 @@ tm_merge_kernel(const __grid_constant__ TmParams p) {
 #pragma unroll
   for (int off = 16; off; off >>= 1) Lw += __shfl_xor_sync(0xffffffffu, Lw, off);
 
-  // 3. the row's warps add their parts in order; its first warp stores
+  // 3. the row's warps add their parts in order, each rescaled from its own
+  // maximum to the row's (a warp without splits adds nothing); the first
+  // warp stores
   if (wpr > 1) {
 #pragma unroll
     for (int j = 0; j < CPL; ++j) sv[warp][lane * CPL + j] = v[j];
-    if (lane == 0) sL[warp] = Lw;
+    if (lane == 0) {
+      sL[warp] = Lw;
+      sM[warp] = Mw;
+    }
     __syncthreads();
     if (wq != 0) return;
-    for (int w = 1; w < wpr; ++w) {
+    float M = Mw;
+    for (int w = 1; w < wpr; ++w) M = fmaxf(M, sM[warp + w]);
+    const float f0 = Mw == -INFINITY ? 0.f : fast_exp2(Mw - M);
 #pragma unroll
-      for (int j = 0; j < CPL; ++j) v[j] += sv[warp + w][lane * CPL + j];
-      Lw += sL[warp + w];
+    for (int j = 0; j < CPL; ++j) v[j] *= f0;
+    Lw *= f0;
+    for (int w = 1; w < wpr; ++w) {
+      const float mw = sM[warp + w];
+      const float f = mw == -INFINITY ? 0.f : fast_exp2(mw - M);
+#pragma unroll
+      for (int j = 0; j < CPL; ++j) v[j] += f * sv[warp + w][lane * CPL + j];
+      Lw += f * sL[warp + w];
     }
   }
   if (!in_range || !plan_ok) return;
