@@ -498,7 +498,8 @@ def main():
 # name -> (dominant kernels, committed ncu summary, workload description)
 CONFIG_INFO = {
     "mha7b": ("attn_tm_kernel<128,0,0>, then tm_merge_kernel<128>", "profiles/attn_bf16_mha7b.md", WORKLOAD),
-    "tiny": ("attn_bf16_kernel<64,1,0> (small-call path: one launch, latency-bound)", "profiles/attn_bf16_tiny.md",
+    "tiny": ("attn_bf16_kernel<64,1,0,8> (small-call path: one launch of 8-warp CTAs, latency-bound)",
+             "profiles/attn_bf16_tiny.md",
              "tiny: 4 agents, 1 layer, 8 q / 2 kv heads, d 64, 256-token shared prefix + 64-128 private, "
              "2 mirror-diff blocks per agent"),
     "gqa_fanout": ("attn_wide_kernel<1,0> beside attn_tm_kernel<128,0,0>, then tm_merge_kernel<128>",

@@ -58,14 +58,22 @@ __host__ __device__ constexpr int attn_stages() {
   return (D == 128) ? 3 : (DIFF ? 3 : 4);
 }
 
-template <int D, bool DIFF>
+template <int D, bool DIFF, int W = kAttnWarps>
 __host__ __device__ constexpr int attn_smem_bytes() {
-  return 1024 + kAttnWarps * attn_stages<D, DIFF>() * (DIFF ? 4 : 2) * AttnCfg<D>::TILE;
+  return 1024 + W * attn_stages<D, DIFF>() * (DIFF ? 4 : 2) * AttnCfg<D>::TILE;
+}
+
+// Warps per CTA: four, or eight for calls that take a whole (sequence, KV
+// head) in one CTA (twice the warps on its blocks, half the chain per warp)
+// where eight warps' rings fit in shared memory.
+template <int D, bool DIFF>
+__host__ __device__ constexpr bool attn_wide_cta_ok() {
+  return attn_smem_bytes<D, DIFF, 8>() <= 227 * 1024;
 }
 
 
-template <int D, bool DIFF, bool ROPE>
-__global__ void __launch_bounds__(128, 2)
+template <int D, bool DIFF, bool ROPE, int W>
+__global__ void __launch_bounds__(32 * W, W == 4 ? 2 : 1)
 attn_bf16_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ CUtensorMap tk,
                  const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdk,
                  const __grid_constant__ CUtensorMap tdv) {
@@ -75,11 +83,11 @@ attn_bf16_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ C
   constexpr int NT = DIFF ? 4 : 2;
   constexpr int STAGE = NT * TILE;
   extern __shared__ uint8_t smem_raw[];
-  __shared__ uint64_t bars[kAttnWarps][S];
+  __shared__ uint64_t bars[W][S];
   __shared__ int s_last;
   __shared__ float sM[16], sL[16];
   __shared__ float rsc[ROPE ? 4 * 64 : 1];   // RoPE frequency pieces (rotation calls)
-  __shared__ float2 s_wml[kAttnWarps][16];    // the warps' (m, l) at the end
+  __shared__ float2 s_wml[W][16];    // the warps' (m, l) at the end
   if (threadIdx.x == 0) {
     prefetch_tmap(&tk);
     prefetch_tmap(&tv);
@@ -126,7 +134,7 @@ attn_bf16_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ C
   const uint32_t wbase_u32 = smem_u32(wbase);
 
   // ---- this warp's contiguous block range
-  const int quarter = p.bpc / kAttnWarps;
+  const int quarter = p.bpc / W;
   const int b_first = chunk * p.bpc + warp * quarter;
   int n_mine = min(quarter, nblk - b_first);
   if (n_mine < 0) n_mine = 0;
@@ -414,13 +422,13 @@ attn_bf16_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ C
   l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
   l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
 
-  // ---- the four warps' states combine into one split per CTA.  The stage
+  // ---- the W warps' states combine into one split per CTA.  The stage
   // buffers are free once every warp is past its last block (a warp that
   // timed out has drained its copies, each wait bounded), so they hold the
   // warps' accumulators: [warp][row][D] fp32.
   __syncthreads();
   float* s_acc = reinterpret_cast<float*>(base);
-  static_assert(kAttnWarps * 16 * D * 4 <= kAttnWarps * S * STAGE, "combine buffer fits the stages");
+  static_assert(W * 16 * D * 4 <= W * S * STAGE, "combine buffer fits the stages");
   if (r0ok) {
 #pragma unroll
     for (int n = 0; n < D / 8; ++n)
@@ -436,7 +444,7 @@ attn_bf16_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ C
   __syncthreads();
   const size_t sidx = ((size_t)a * p.hkv + h) * p.n_chunks + chunk;
   {
-    constexpr int CPT = D / 8;   // columns per thread: 16 rows x 8 threads
+    constexpr int CPT = D / 8;   // columns per thread: 16 rows x 8 threads (g <= 16 rows used)
     const int r = threadIdx.x >> 3, c0 = (threadIdx.x & 7) * CPT;
     if (nch == 1) {
       // the whole context in this CTA: its combined state is the output (an
@@ -444,13 +452,13 @@ attn_bf16_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ C
       if (r < p.g) {
         float M = -INFINITY;
 #pragma unroll
-        for (int w = 0; w < kAttnWarps; ++w)
+        for (int w = 0; w < W; ++w)
           if (s_wml[w][r].y > 0.f) M = fmaxf(M, s_wml[w][r].x);
         float Lc = 0.f, o[CPT];
 #pragma unroll
         for (int j = 0; j < CPT; ++j) o[j] = 0.f;
 #pragma unroll
-        for (int w = 0; w < kAttnWarps; ++w) {
+        for (int w = 0; w < W; ++w) {
           const float2 ml = s_wml[w][r];
           const float wt = ml.y > 0.f ? fast_exp2(ml.x - M) : 0.f;
           Lc += wt * ml.y;
@@ -472,13 +480,13 @@ attn_bf16_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ C
     if (r < p.g) {
       float M = -INFINITY;
 #pragma unroll
-      for (int w = 0; w < kAttnWarps; ++w)
+      for (int w = 0; w < W; ++w)
         if (s_wml[w][r].y > 0.f) M = fmaxf(M, s_wml[w][r].x);
       float Lc = 0.f, o[CPT];
 #pragma unroll
       for (int j = 0; j < CPT; ++j) o[j] = 0.f;
 #pragma unroll
-      for (int w = 0; w < kAttnWarps; ++w) {
+      for (int w = 0; w < W; ++w) {
         const float2 ml = s_wml[w][r];
         const float wt = ml.y > 0.f ? fast_exp2(ml.x - M) : 0.f;
         Lc += wt * ml.y;
@@ -500,17 +508,17 @@ attn_bf16_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ C
   merge_splits<D>(p.part, p.part_ml, s0, nch, p.g, p.out + ((size_t)a * p.hq + h * p.g) * D, sM, sL);
 }
 
-template <int D, bool DIFF, bool ROPE>
-static kvs_status launch_attn(const AttnParams& prm, const kvs_pool* pool, int layer, int grid, cudaStream_t st) {
-  auto kern = attn_bf16_kernel<D, DIFF, ROPE>;
-  constexpr int smem = attn_smem_bytes<D, DIFF>();
-  if (!smem_limit_once<attn_bf16_kernel<D, DIFF, ROPE>>(smem, pool->device))
+template <int D, bool DIFF, bool ROPE, int W>
+static kvs_status launch_attn_w(const AttnParams& prm, const kvs_pool* pool, int layer, int grid, cudaStream_t st) {
+  auto kern = attn_bf16_kernel<D, DIFF, ROPE, W>;
+  constexpr int smem = attn_smem_bytes<D, DIFF, W>();
+  if (!smem_limit_once<attn_bf16_kernel<D, DIFF, ROPE, W>>(smem, pool->device))
     return fail(KVS_ERR_CUDA, "decode_attn: cannot raise the shared-memory limit");
   const CUtensorMap& dk = DIFF ? pool->tdk[layer] : pool->tk[layer];
   const CUtensorMap& dv = DIFF ? pool->tdv[layer] : pool->tv[layer];
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(128);
+  cfg.blockDim = dim3(32 * W);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
   cudaLaunchAttribute attr[1];
@@ -522,6 +530,15 @@ static kvs_status launch_attn(const AttnParams& prm, const kvs_pool* pool, int l
     return fail(KVS_ERR_CUDA, "decode_attn: launch failed");
   count_launch();
   return check_launch("decode_attn");
+}
+
+template <int D, bool DIFF, bool ROPE>
+static kvs_status launch_attn(const AttnParams& prm, const kvs_pool* pool, int layer, int grid, bool wide_cta,
+                              cudaStream_t st) {
+  if constexpr (attn_wide_cta_ok<D, DIFF>()) {
+    if (wide_cta) return launch_attn_w<D, DIFF, ROPE, 8>(prm, pool, layer, grid, st);
+  }
+  return launch_attn_w<D, DIFF, ROPE, kAttnWarps>(prm, pool, layer, grid, st);
 }
 
 }  // namespace kvs
@@ -589,11 +606,16 @@ static kvs_status attn_launch(kvs_pool* pool, int32_t layer, const void* q_dev, 
     return decode_attn_token_major(pool, layer, q_dev, n_q_heads, block_table_dev, max_blocks, seq_len_dev, n_seq,
                                    diff_table_dev, rope_off_dev, rope_segs_dev, theta, scale, out_dev, ws, stream);
   AttnPlan plan = attn_plan(pool, n_seq, max_blocks);
+  const bool diff = diff_table_dev != nullptr;
+  bool wide_cta = false;
   if (g <= kTmMaxGroup && max_blocks <= kSmallOneChunk) {
     // a small call with short contexts: one CTA per (sequence, KV head)
     // writes its output directly, with no split and no merge (the 4-agent,
-    // 24-block layer: 11.7-12.1 us against 12.9 us in three chunks)
-    plan.bpc = (max_blocks + kAttnWarps - 1) / kAttnWarps * kAttnWarps;
+    // 24-block layer: 11.7-12.1 us against 12.9 us in three chunks), on
+    // eight warps where their rings fit (all but head_dim 128 with diffs)
+    wide_cta = !(d.head_dim == 128 && diff);
+    const int w = wide_cta ? 8 : kAttnWarps;
+    plan.bpc = (max_blocks + w - 1) / w * w;
     plan.n_chunks = 1;
   }
   const long long grid = (long long)n_seq * d.num_kv_heads * plan.n_chunks;
@@ -623,18 +645,17 @@ static kvs_status attn_launch(kvs_pool* pool, int32_t layer, const void* q_dev, 
   prm.scale_log2 = scale * 1.4426950408889634f;
   const bool rope = rope_off_dev != nullptr;
   if (rope) rope_split_host(theta, d.head_dim, prm.rs.c);
-  const bool diff = diff_table_dev != nullptr;
   const int gr = static_cast<int>(grid);
   if (d.head_dim == 128) {
-    if (diff) return rope ? launch_attn<128, true, true>(prm, pool, layer, gr, stream)
-                          : launch_attn<128, true, false>(prm, pool, layer, gr, stream);
-    return rope ? launch_attn<128, false, true>(prm, pool, layer, gr, stream)
-                : launch_attn<128, false, false>(prm, pool, layer, gr, stream);
+    if (diff) return rope ? launch_attn<128, true, true>(prm, pool, layer, gr, wide_cta, stream)
+                          : launch_attn<128, true, false>(prm, pool, layer, gr, wide_cta, stream);
+    return rope ? launch_attn<128, false, true>(prm, pool, layer, gr, wide_cta, stream)
+                : launch_attn<128, false, false>(prm, pool, layer, gr, wide_cta, stream);
   }
-  if (diff) return rope ? launch_attn<64, true, true>(prm, pool, layer, gr, stream)
-                        : launch_attn<64, true, false>(prm, pool, layer, gr, stream);
-  return rope ? launch_attn<64, false, true>(prm, pool, layer, gr, stream)
-              : launch_attn<64, false, false>(prm, pool, layer, gr, stream);
+  if (diff) return rope ? launch_attn<64, true, true>(prm, pool, layer, gr, wide_cta, stream)
+                        : launch_attn<64, true, false>(prm, pool, layer, gr, wide_cta, stream);
+  return rope ? launch_attn<64, false, true>(prm, pool, layer, gr, wide_cta, stream)
+              : launch_attn<64, false, false>(prm, pool, layer, gr, wide_cta, stream);
 }
 
 extern "C" kvs_status kvs_decode_attn_planned(kvs_pool* pool, int32_t layer, const void* q_dev, int32_t n_q_heads,
