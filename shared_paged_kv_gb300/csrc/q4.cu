@@ -361,6 +361,11 @@ q4_attn_kernel(const __grid_constant__ Q4Params p, const __grid_constant__ CUten
     colscale[1] = rs * __shfl_sync(0xffffffffu, up, (2 * c + 1) * 4);
   }
 
+  // the same per-column constants as packed pairs (columns 2c, 2c+1)
+  const float2 qs2[2] = {make_float2(qs[0][0], qs[0][1]), make_float2(qs[1][0], qs[1][1])};
+  const float2 cs2 = make_float2(colscale[0], colscale[1]);
+  const float2 sl2 = make_float2(p.scale_log2, p.scale_log2);
+
   float m[2] = {-INFINITY, -INFINITY}, l[2] = {0.f, 0.f};
   float acc[8][4];
   float corr[2][2] = {{0.f, 0.f}, {0.f, 0.f}};
@@ -399,7 +404,8 @@ q4_attn_kernel(const __grid_constant__ Q4Params p, const __grid_constant__ CUten
 #pragma unroll
       for (int mt = 0; mt < 4; ++mt) {
         const int t0 = tw + 16 * mt + g, t1 = t0 + 8;
-        float cg[2][4];   // 2^-24 q . c per group, rows (t0, t1) x columns (2c, 2c+1)
+        // 2^-24 q . c per group: [group][row t0 / t1], columns (2c, 2c+1) as a pair
+        float2 cg[2][2];
 #pragma unroll
         for (int grp = 0; grp < 2; ++grp) {
           float al_[4] = {0.f, 0.f, 0.f, 0.f}, ah_[4] = {0.f, 0.f, 0.f, 0.f};
@@ -412,8 +418,9 @@ q4_attn_kernel(const __grid_constant__ Q4Params p, const __grid_constant__ CUten
             mma_f16(al_, nib_lo_sub(r0), nib_lo_sub(r1), nib_lo_sub(s0), nib_lo_sub(s1), qlo[grp][w][0], qlo[grp][w][1]);
             mma_f16(ah_, nib_hi_sub(r0), nib_hi_sub(r1), nib_hi_sub(s0), nib_hi_sub(s1), qhi[grp][w][0], qhi[grp][w][1]);
           }
-#pragma unroll
-          for (int e = 0; e < 4; ++e) cg[grp][e] = fmaf(ah_[e], 0.0625f, al_[e]);
+          const float2 s16 = make_float2(0.0625f, 0.0625f);
+          cg[grp][0] = __ffma2_rn(make_float2(ah_[0], ah_[1]), s16, make_float2(al_[0], al_[1]));
+          cg[grp][1] = __ffma2_rn(make_float2(ah_[2], ah_[3]), s16, make_float2(al_[2], al_[3]));
         }
         float dks[4] = {0.f, 0.f, 0.f, 0.f};   // q . DK of a dirty sub-block (true units)
         if (DIFF && int4_at(d_cur, mt) >= 0) q4_diff_scores(p, int4_at(d_cur, mt), h, g, c, G_, qbase, dks);
@@ -423,14 +430,20 @@ q4_attn_kernel(const __grid_constant__ Q4Params p, const __grid_constant__ CUten
         const float2 g01 = __half22float2(*reinterpret_cast<const __half2*>(&sb0.y));   // group 1, t0
         const float2 g10 = __half22float2(*reinterpret_cast<const __half2*>(&sb1.x));
         const float2 g11 = __half22float2(*reinterpret_cast<const __half2*>(&sb1.y));
+        // per row (t0, t1), both columns at once (packed fp32 pairs):
+        // x = s0 cg0 + b0 qs0 + s1 cg1 + b1 qs1, score = dks scale + x colscale
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int cc = e & 1;
-          const float2 s0 = (e < 2) ? g00 : g10;
-          const float2 s1 = (e < 2) ? g01 : g11;
-          float x = s0.x * cg[0][e] + s0.y * qs[0][cc] + s1.x * cg[1][e] + s1.y * qs[1][cc];
-          const int tok = (e < 2) ? t0 : t1;
-          sc[mt][e] = tok < nv ? fmaf(dks[e], p.scale_log2, x * colscale[cc]) : -INFINITY;
+        for (int hr = 0; hr < 2; ++hr) {
+          const float2 s0 = hr ? g10 : g00;
+          const float2 s1 = hr ? g11 : g01;
+          float2 x = __fmul2_rn(make_float2(s0.x, s0.x), cg[0][hr]);
+          x = __ffma2_rn(make_float2(s0.y, s0.y), qs2[0], x);
+          x = __ffma2_rn(make_float2(s1.x, s1.x), cg[1][hr], x);
+          x = __ffma2_rn(make_float2(s1.y, s1.y), qs2[1], x);
+          const float2 y = __ffma2_rn(make_float2(dks[2 * hr], dks[2 * hr + 1]), sl2, __fmul2_rn(x, cs2));
+          const bool live = (hr ? t1 : t0) < nv;
+          sc[mt][2 * hr] = live ? y.x : -INFINITY;
+          sc[mt][2 * hr + 1] = live ? y.y : -INFINITY;
         }
       }
       // online softmax over this warp's 64 tokens, per query column
@@ -451,14 +464,23 @@ q4_attn_kernel(const __grid_constant__ Q4Params p, const __grid_constant__ CUten
         const float mn = fmaxf(m[cc], mx[cc]);
         al[cc] = fast_exp2(m[cc] - mn);
         m[cc] = mn;
-        l[cc] *= al[cc];
-        corr[0][cc] *= al[cc];
-        corr[1][cc] *= al[cc];
       }
+      // rescale the state only when some column's maximum moved
+      if (__any_sync(0xffffffffu, al[0] != 1.f || al[1] != 1.f)) {
+        const float2 al2 = make_float2(al[0], al[1]);
+        float2 t = __fmul2_rn(make_float2(l[0], l[1]), al2);
+        l[0] = t.x; l[1] = t.y;
+        t = __fmul2_rn(make_float2(corr[0][0], corr[0][1]), al2);
+        corr[0][0] = t.x; corr[0][1] = t.y;
+        t = __fmul2_rn(make_float2(corr[1][0], corr[1][1]), al2);
+        corr[1][0] = t.x; corr[1][1] = t.y;
 #pragma unroll
-      for (int i2 = 0; i2 < 8; ++i2) {
-        acc[i2][0] *= al[0]; acc[i2][1] *= al[1];
-        acc[i2][2] *= al[0]; acc[i2][3] *= al[1];
+        for (int i2 = 0; i2 < 8; ++i2) {
+          const float2 a01 = __fmul2_rn(make_float2(acc[i2][0], acc[i2][1]), al2);
+          const float2 a23 = __fmul2_rn(make_float2(acc[i2][2], acc[i2][3]), al2);
+          acc[i2][0] = a01.x; acc[i2][1] = a01.y;
+          acc[i2][2] = a23.x; acc[i2][3] = a23.y;
+        }
       }
 #pragma unroll
       for (int mt = 0; mt < 4; ++mt) {
@@ -476,14 +498,22 @@ q4_attn_kernel(const __grid_constant__ Q4Params p, const __grid_constant__ CUten
         const float2 v11 = __half22float2(*reinterpret_cast<const __half2*>(&sb1.y));
         // B operands (k = token, n = query head) per group, via transposition
         uint32_t bb[2][2];
-        bb[0][0] = movmatrix_t(pack_f16(pv[0] * v00.x, pv[1] * v00.x));
-        bb[0][1] = movmatrix_t(pack_f16(pv[2] * v10.x, pv[3] * v10.x));
-        bb[1][0] = movmatrix_t(pack_f16(pv[0] * v01.x, pv[1] * v01.x));
-        bb[1][1] = movmatrix_t(pack_f16(pv[2] * v11.x, pv[3] * v11.x));
-        corr[0][0] += pv[0] * v00.y + pv[2] * v10.y;
-        corr[0][1] += pv[1] * v00.y + pv[3] * v10.y;
-        corr[1][0] += pv[0] * v01.y + pv[2] * v11.y;
-        corr[1][1] += pv[1] * v01.y + pv[3] * v11.y;
+        // (P of rows t0 and t1, both columns as packed pairs)
+        const float2 p0 = make_float2(pv[0], pv[1]), p1 = make_float2(pv[2], pv[3]);
+        float2 t = __fmul2_rn(p0, make_float2(v00.x, v00.x));
+        bb[0][0] = movmatrix_t(pack_f16(t.x, t.y));
+        t = __fmul2_rn(p1, make_float2(v10.x, v10.x));
+        bb[0][1] = movmatrix_t(pack_f16(t.x, t.y));
+        t = __fmul2_rn(p0, make_float2(v01.x, v01.x));
+        bb[1][0] = movmatrix_t(pack_f16(t.x, t.y));
+        t = __fmul2_rn(p1, make_float2(v11.x, v11.x));
+        bb[1][1] = movmatrix_t(pack_f16(t.x, t.y));
+        t = __ffma2_rn(p1, make_float2(v10.y, v10.y), __fmul2_rn(p0, make_float2(v00.y, v00.y)));
+        t = __fadd2_rn(make_float2(corr[0][0], corr[0][1]), t);
+        corr[0][0] = t.x; corr[0][1] = t.y;
+        t = __ffma2_rn(p1, make_float2(v11.y, v11.y), __fmul2_rn(p0, make_float2(v01.y, v01.y)));
+        t = __fadd2_rn(make_float2(corr[1][0], corr[1][1]), t);
+        corr[1][0] = t.x; corr[1][1] = t.y;
         // A operand: V codes, m = head dim (row g: the even dim 8g + 2lm of
         // the group's 64, as c * 2^-24; row g + 8: the odd one, as c * 2^-20),
         // k = token
