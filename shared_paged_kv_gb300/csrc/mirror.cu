@@ -9,19 +9,19 @@
 //  1. mir_agent   one CTA per agent: clear the agent's dirty flags, validate
 //                 the refreshed positions and flag the logical blocks holding
 //                 one; then count the agent's dirty blocks;
-//  2. mir_scan    exclusive scan of the per-agent counts (one CTA): diff ids
-//                 are consecutive in agent order, then block order;
-//  3. mir_apply   one CTA per agent: diff table, the list of dirty slots,
+//  2. mir_apply   one CTA per agent: its first diff id (the dirty blocks of
+//                 the agents before it: diff ids are consecutive in agent
+//                 order, then block order), the diff table, the list of dirty slots,
 //                 each dirty block's refreshed rows (the first one's index
 //                 and a 16-bit mask: positions are sorted, so the k-th set
 //                 bit is refreshed row first + k) and, for rotation calls,
 //                 its shift (the last covering segment entry);
-//  4. mir_write   one warp per (dirty block, kv head): 16 rows, a refreshed
+//  3. mir_write   one warp per (dirty block, kv head): 16 rows, a refreshed
 //                 row becoming bf16(R(-delta) k_new - K_master) and
 //                 bf16(v_new - V_master), every other row zero.  Lane (row,
 //                 v) holds head dims [8v, 8v+8) and [d/2+8v, d/2+8v+8), so the
 //                 rotate-half partners sit in the same lane.
-// The four kernels are programmatic dependent launches: each waits for the
+// The three kernels are programmatic dependent launches: each waits for the
 // one before it at its first statement and lets the next be scheduled.
 #include "common.cuh"
 #include "internal.h"
@@ -68,7 +68,7 @@ struct MirParams {
   int32_t* n_diff;
   uint8_t* flags;     // [n_seq][max_blocks] 1 = dirty
   int2* rows;         // [n_diff] {first refreshed row, mask of refreshed tokens} per diff id
-  int32_t* counts;    // [n_seq + 1] dirty blocks per agent, then their exclusive scan
+  int32_t* counts;    // [n_seq] dirty blocks per agent
   int32_t* list;      // [n_diff] dirty slot (a * max_blocks + b) of each diff id
   int32_t* dlt;       // [n_diff] RoPE shift of each dirty block (rotation calls)
   uint32_t* status;
@@ -111,36 +111,39 @@ __global__ void __launch_bounds__(256) mir_agent(const __grid_constant__ MirPara
   }
 }
 
-// 2. exclusive scan of the per-agent counts (one CTA); the total is n_diff
-__global__ void __launch_bounds__(1024) mir_scan(const __grid_constant__ MirParams p) {
-  pdl_enter();
-  __shared__ int warp_sums[32];
-  int carry = 0;
-  for (int base = 0; base < p.n_seq; base += blockDim.x) {
-    const int i = base + threadIdx.x;
-    const int x = i < p.n_seq ? p.counts[i] : 0;
-    int total;
-    const int ex = block_exclusive_scan(x, warp_sums, total);
-    if (i < p.n_seq) p.counts[i] = carry + ex;
-    carry += total;
-  }
-  if (threadIdx.x == 0) {
-    p.counts[p.n_seq] = carry;
-    *p.n_diff = carry;
-    if (carry > p.diff_capacity) set_err(p.status, KVS_DEVERR_DIFF_ID);
-  }
-}
-
-// 3. diff table, dirty list and shifts, one CTA per agent
+// 2. diff table, dirty list and shifts, one CTA per agent
 constexpr int kMirSegChunk = 256;   // segment entries staged in shared memory at a time
 
 __global__ void __launch_bounds__(256) mir_apply(const __grid_constant__ MirParams p) {
   pdl_enter();
   __shared__ int warp_sums[32];
   __shared__ int4 segs[kMirSegChunk];
+  // the total number of dirty blocks (CTA 0)
+  if (blockIdx.x == 0) {
+    int x = 0;
+    for (int i = threadIdx.x; i < p.n_seq; i += blockDim.x) x += p.counts[i];
+    int total;
+    block_exclusive_scan(x, warp_sums, total);
+    if (threadIdx.x == 0) {
+      *p.n_diff = total;
+      if (total > p.diff_capacity) set_err(p.status, KVS_DEVERR_DIFF_ID);
+    }
+  }
+  // first diff id of agent a: the dirty blocks of agents 0 .. a-1, summed
+  // from the last agent this CTA handled
+  int pre = 0, pre_a = 0;
   for (int a = blockIdx.x; a < p.n_seq; a += gridDim.x) {
+    {
+      int x = 0;
+      for (int i = pre_a + threadIdx.x; i < a; i += blockDim.x) x += p.counts[i];
+      int total;
+      __syncthreads();   // warp_sums is reused
+      block_exclusive_scan(x, warp_sums, total);
+      pre += total;
+      pre_a = a;
+    }
     const uint8_t* fl = p.flags + (size_t)a * p.max_blocks;
-    const int first = p.counts[a];
+    const int first = pre;
     int carry = first;
     for (int base = 0; base < p.max_blocks; base += blockDim.x) {
       const int b = base + threadIdx.x;
@@ -363,7 +366,6 @@ extern "C" kvs_status kvs_mirror_build(kvs_pool* pool, int32_t layer, const int3
   const int sms = pool->num_sms;
   const int agent_grid = std::min(n_seq, sms * 8);
   cudaError_t e = launch_pdl(mir_agent, dim3(agent_grid), dim3(256), stream, p);
-  if (e == cudaSuccess) e = launch_pdl(mir_scan, dim3(1), dim3(1024), stream, p);
   if (e == cudaSuccess) e = launch_pdl(mir_apply, dim3(agent_grid), dim3(256), stream, p);
   // the dirty count is only known on the device: a persistent grid of warps
   // walks the (dirty block, kv head) units
@@ -371,6 +373,6 @@ extern "C" kvs_status kvs_mirror_build(kvs_pool* pool, int32_t layer, const int3
     e = d.head_dim == 128 ? launch_pdl(mir_write<128>, dim3(sms * 8), dim3(256), stream, p)
                           : launch_pdl(mir_write<64>, dim3(sms * 8), dim3(256), stream, p);
   if (e != cudaSuccess) return fail(KVS_ERR_CUDA, "mirror_build: launch failed");
-  count_launch(4);
+  count_launch(3);
   return check_launch("mirror_build");
 }
