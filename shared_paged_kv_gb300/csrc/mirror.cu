@@ -29,6 +29,7 @@
 namespace kvs {
 
 constexpr int kMirB = 16;         // block tokens this path supports
+constexpr int kMirUnroll = 4;     // refreshed positions a thread takes at once
 
 static size_t mir_align(size_t x) { return (x + 255) & ~size_t(255); }
 
@@ -93,13 +94,24 @@ __global__ void __launch_bounds__(256) mir_agent(const __grid_constant__ MirPara
     if (r0 < 0 || r1 < r0) {
       if (threadIdx.x == 0) set_err(p.status, KVS_DEVERR_JOB);
     } else {
-      for (long long r = r0 + threadIdx.x; r < r1; r += blockDim.x) {
-        const int t = p.idx[r];
-        if (t < 0 || t >= L || (r > r0 && p.idx[r - 1] >= t)) {
-          set_err(p.status, KVS_DEVERR_JOB);
-          continue;
+      // kMirUnroll positions per thread at a time, their loads in flight together
+      for (long long base = r0 + threadIdx.x; base < r1; base += (long long)kMirUnroll * blockDim.x) {
+        int t[kMirUnroll], tp[kMirUnroll];
+#pragma unroll
+        for (int k = 0; k < kMirUnroll; ++k) {
+          const long long r = base + (long long)k * blockDim.x;
+          t[k] = r < r1 ? p.idx[r] : 0;
+          tp[k] = (r < r1 && r > r0) ? p.idx[r - 1] : -1;
         }
-        fl[t / kMirB] = 1;   // equal-value writes
+#pragma unroll
+        for (int k = 0; k < kMirUnroll; ++k) {
+          if (base + (long long)k * blockDim.x >= r1) continue;
+          if (t[k] < 0 || t[k] >= L || tp[k] >= t[k]) {
+            set_err(p.status, KVS_DEVERR_JOB);
+            continue;
+          }
+          fl[t[k] / kMirB] = 1;   // equal-value writes
+        }
       }
     }
     __syncthreads();
@@ -171,13 +183,28 @@ __global__ void __launch_bounds__(256) mir_apply(const __grid_constant__ MirPara
       int L = p.seq_len[a];
       L = L < 0 ? 0 : min(L, p.max_blocks * kMirB);
       if (r0 >= 0 && r1 >= r0) {
-        for (long long r = r0 + threadIdx.x; r < r1; r += blockDim.x) {
-          const int t = p.idx[r];
-          if (t < 0 || t >= L || (r > r0 && p.idx[r - 1] >= t)) continue;
-          const int id = p.diff_table[(size_t)a * p.max_blocks + t / kMirB];
-          if (id < 0 || id >= p.diff_capacity) continue;
-          if (r == r0 || p.idx[r - 1] / kMirB != t / kMirB) p.rows[id].x = (int)r;
-          atomicOr(reinterpret_cast<unsigned int*>(&p.rows[id].y), 1u << (t % kMirB));
+        // kMirUnroll positions per thread at a time: their position loads,
+        // then their diff-table loads, each group in flight together
+        for (long long base = r0 + threadIdx.x; base < r1; base += (long long)kMirUnroll * blockDim.x) {
+          int t[kMirUnroll], tp[kMirUnroll], id[kMirUnroll];
+#pragma unroll
+          for (int k = 0; k < kMirUnroll; ++k) {
+            const long long r = base + (long long)k * blockDim.x;
+            t[k] = r < r1 ? p.idx[r] : -1;
+            tp[k] = (r < r1 && r > r0) ? p.idx[r - 1] : -1;
+          }
+#pragma unroll
+          for (int k = 0; k < kMirUnroll; ++k) {
+            const bool ok = t[k] >= 0 && t[k] < L && tp[k] < t[k];
+            id[k] = ok ? p.diff_table[(size_t)a * p.max_blocks + t[k] / kMirB] : -1;
+          }
+#pragma unroll
+          for (int k = 0; k < kMirUnroll; ++k) {
+            if (id[k] < 0 || id[k] >= p.diff_capacity) continue;
+            const long long r = base + (long long)k * blockDim.x;
+            if (r == r0 || tp[k] / kMirB != t[k] / kMirB) p.rows[id[k]].x = (int)r;
+            atomicOr(reinterpret_cast<unsigned int*>(&p.rows[id[k]].y), 1u << (t[k] % kMirB));
+          }
         }
       }
     }
