@@ -892,7 +892,7 @@ def bench_mirror(torch, K, W, dev, steps):
     peak, _ = read_peaks()
     return {"workload": "mirror: all-gather round, 64 agents x 31 refreshed blocks among 512 shared-segment blocks, "
                         "8 kv heads x 128, K rotated back by the segment shift",
-            "kernel": "mir_write + 3 index kernels", "ms_per_call": ms, "dirty_blocks": cap_d, "rows": n_rows,
+            "kernel": "mir_write + 2 index kernels (mir_agent, mir_apply)", "ms_per_call": ms, "dirty_blocks": cap_d, "rows": n_rows,
             "bytes": byts, "gbs": byts / (ms * 1e-3) / 1e9, "frac": byts / (ms * 1e-3) / 1e9 / peak,
             "timing": "CUDA graph replays, L2 flushed before every replay", "status_flags": flags}
 
