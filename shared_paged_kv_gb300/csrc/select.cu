@@ -75,14 +75,24 @@ __global__ void __launch_bounds__(1024) sel_topk(const float* __restrict__ score
   const int n = agent_rows(row_off, a, lo, hi);
   const int64_t r0 = n > 0 ? row_off[a] : 0;   // rows [r0, r0 + n) lie in [lo, hi) when n > 0
   const int k = count_for(ratio, n);
-  // exclusive prefix of k over agents
-  if (threadIdx.x == 0) {
-    int64_t o = 0;
-    for (int b = 0; b < a; ++b) o += count_for(ratio, agent_rows(row_off, b, lo, hi));
-    idx_off[a] = o;
-    if (a == n_agents - 1) idx_off[n_agents] = o + k;
-    s_prefix = 0u;
-    s_remaining = k;
+  // exclusive prefix of k over agents: the earlier agents' counts, summed
+  // over the CTA
+  {
+    long long part = 0;
+    for (int b = threadIdx.x; b < a; b += blockDim.x) part += count_for(ratio, agent_rows(row_off, b, lo, hi));
+    __shared__ long long s_part[32];
+#pragma unroll
+    for (int off = 16; off; off >>= 1) part += __shfl_xor_sync(0xffffffffu, part, off);
+    if ((threadIdx.x & 31) == 0) s_part[threadIdx.x >> 5] = part;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      int64_t o = 0;
+      for (int w = 0; w < (int)(blockDim.x >> 5); ++w) o += s_part[w];
+      idx_off[a] = o;
+      if (a == n_agents - 1) idx_off[n_agents] = o + k;
+      s_prefix = 0u;
+      s_remaining = k;
+    }
   }
   __syncthreads();
   const int64_t out0 = idx_off[a];
@@ -99,15 +109,41 @@ __global__ void __launch_bounds__(1024) sel_topk(const float* __restrict__ score
       if ((v & mask) == pre) atomicAdd(&hist[(v >> shift) & 255u], 1u);
     }
     __syncthreads();
-    if (threadIdx.x == 0) {
-      int rem = s_remaining;
-      int digit = 255;
-      for (; digit > 0; --digit) {
-        if ((int)hist[digit] >= rem) break;
-        rem -= hist[digit];
+    if (threadIdx.x < 32) {
+      // the digit: from the top, the first bin whose running count reaches
+      // the remaining rank (bin 0 if none does before it); lane l scans bins
+      // 255 - 8l .. 248 - 8l after a prefix sum of the lanes' totals
+      const int lane = threadIdx.x;
+      unsigned c8[8], lsum = 0u;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        c8[j] = hist[255 - (lane * 8 + j)];
+        lsum += c8[j];
       }
-      s_prefix = pre | ((unsigned)digit << shift);
-      s_remaining = rem;
+      unsigned incl = lsum;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const unsigned y = __shfl_up_sync(0xffffffffu, incl, off);
+        if (lane >= off) incl += y;
+      }
+      const unsigned excl = incl - lsum;
+      const unsigned rem0 = (unsigned)s_remaining;
+      const bool mine = excl < rem0 && rem0 <= incl;
+      const unsigned who = __ballot_sync(0xffffffffu, mine);
+      if (mine) {
+        unsigned r = rem0 - excl;
+        int digit = 255 - (lane * 8 + 7);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          if (c8[j] >= r) { digit = 255 - (lane * 8 + j); break; }
+          r -= c8[j];
+        }
+        s_prefix = pre | ((unsigned)digit << shift);
+        s_remaining = (int)r;
+      } else if (who == 0u && lane == 31) {
+        s_prefix = pre;   // digit 0
+        s_remaining = (int)(rem0 - (incl - c8[7]));
+      }
     }
     __syncthreads();
     mask |= 255u << shift;
