@@ -63,6 +63,8 @@ __device__ __forceinline__ int count_for(float ratio, int n) {
   return static_cast<int>(k);
 }
 
+constexpr int kSelUnroll = 8;   // scores a thread loads at once in a radix pass
+
 __global__ void __launch_bounds__(1024) sel_topk(const float* __restrict__ scores, const int64_t* __restrict__ row_off,
                                                  int n_agents, float ratio, long long cap_rows,
                                                  int32_t* __restrict__ idx_out, int64_t* __restrict__ idx_off) {
@@ -104,9 +106,17 @@ __global__ void __launch_bounds__(1024) sel_topk(const float* __restrict__ score
     for (int i = threadIdx.x; i < 256; i += blockDim.x) hist[i] = 0u;
     __syncthreads();
     const unsigned pre = s_prefix;
-    for (int i = threadIdx.x; i < n; i += blockDim.x) {
-      const unsigned v = sb[i];
-      if ((v & mask) == pre) atomicAdd(&hist[(v >> shift) & 255u], 1u);
+    // kSelUnroll scores per thread at a time, their loads in flight together
+    for (int i0 = threadIdx.x; i0 < n; i0 += kSelUnroll * blockDim.x) {
+      unsigned v[kSelUnroll];
+#pragma unroll
+      for (int u = 0; u < kSelUnroll; ++u) {
+        const int i = i0 + u * blockDim.x;
+        v[u] = i < n ? sb[i] : 0u;
+      }
+#pragma unroll
+      for (int u = 0; u < kSelUnroll; ++u)
+        if (i0 + u * (int)blockDim.x < n && (v[u] & mask) == pre) atomicAdd(&hist[(v[u] >> shift) & 255u], 1u);
     }
     __syncthreads();
     if (threadIdx.x < 32) {
@@ -150,11 +160,13 @@ __global__ void __launch_bounds__(1024) sel_topk(const float* __restrict__ score
   }
   const unsigned thr = s_prefix;
   const int need_eq = s_remaining;    // how many positions equal to thr to keep
-  // ordered emission
+  // ordered emission (the next chunk's score is loaded before this one's scans)
   int base_out = 0, eq_seen = 0;
+  unsigned v_next = (int)threadIdx.x < n ? sb[threadIdx.x] : 0u;
   for (int c0 = 0; c0 < n; c0 += blockDim.x) {
     const int i = c0 + threadIdx.x;
-    const unsigned v = i < n ? sb[i] : 0u;
+    const unsigned v = v_next;
+    v_next = i + (int)blockDim.x < n ? sb[i + blockDim.x] : 0u;
     const int is_eq = (i < n && v == thr) ? 1 : 0;
     int eq_total;
     const int eq_rank = block_exclusive_scan(is_eq, warp_sums, eq_total) + eq_seen;
