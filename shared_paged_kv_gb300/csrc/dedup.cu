@@ -116,18 +116,27 @@ __global__ void dedup_hash(DedupParams p) {
 }
 
 // 1b. one warp per sequence: segment starts and chain keys
-__global__ void dedup_prep(DedupParams p) {
+// One CTA per sequence; its warps take contiguous 32-block-aligned ranges of
+// the block row.  Both scans over the row (the running maximum of the
+// segment marks, and the chain x -> A x + C) are associative: pass 1 finds
+// each range's aggregate (its largest mark and its composed map; whether a
+// block starts a segment is its own mark's business), pass 2 runs every
+// range again from the composition of the ranges before it.
+constexpr int kPrepMaxWarps = 8;
+constexpr int kPrepRange = 128;   // blocks per warp aimed at
+
+__global__ void __launch_bounds__(kPrepMaxWarps * 32) dedup_prep(DedupParams p) {
   pdl_enter();
-  const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-  const int lane = threadIdx.x & 31;
-  if (warp >= p.n_seq) return;
-  const int s = warp;
+  __shared__ uint64_t s_aggA[kPrepMaxWarps], s_aggC[kPrepMaxWarps];
+  __shared__ int s_aggM[kPrepMaxWarps];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
+  const int s = blockIdx.x;
   int64_t off;
   int nblk, full;
   seq_geom(p, s, off, nblk, full);
-  {
+  if (threadIdx.x == 0) {
     const int64_t len = p.seq_off[s + 1] - off;
-    if (lane == 0 && (len < 0 || (len + p.B - 1) / p.B > p.max_blocks)) set_err(p.status, KVS_DEVERR_SEQ_LEN);
+    if (len < 0 || (len + p.B - 1) / p.B > p.max_blocks) set_err(p.status, KVS_DEVERR_SEQ_LEN);
   }
   const uint32_t tier = p.tier ? p.tier[s] : 0u;
   const size_t row = (size_t)s * p.max_blocks;
@@ -135,47 +144,99 @@ __global__ void dedup_prep(DedupParams p) {
   // are all zero and need neither clearing nor reading back below
   const bool segs = p.seg_off != nullptr;
   if (segs) {
-    for (int b = lane; b < p.max_blocks; b += 32) p.segstart[row + b] = 0;
-    __syncwarp();
+    for (int b = threadIdx.x; b < p.max_blocks; b += blockDim.x) p.segstart[row + b] = 0;
+    __syncthreads();
     // An entry starts a segment iff it lies inside the sequence and beyond
     // every earlier in-range entry (unsorted and out-of-range starts are
     // ignored); each accepted start marks its own block.
-    const int64_t e0 = p.seg_off[s], e1 = p.seg_off[s + 1];
-    int carry = 0;
-    for (int64_t base = e0; base < e1; base += 32) {
-      const int64_t e = base + lane;
-      const int st = e < e1 ? p.seg_blocks[e] : 0;
-      const int v = (e < e1 && st < nblk) ? st : 0;
-      int incl = v;
+    if (warp == 0) {
+      const int64_t e0 = p.seg_off[s], e1 = p.seg_off[s + 1];
+      int carry = 0;
+      for (int64_t base = e0; base < e1; base += 32) {
+        const int64_t e = base + lane;
+        const int st = e < e1 ? p.seg_blocks[e] : 0;
+        const int v = (e < e1 && st < nblk) ? st : 0;
+        int incl = v;
 #pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int y = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl = max(incl, y);
+        for (int o = 1; o < 32; o <<= 1) {
+          const int y = __shfl_up_sync(0xffffffffu, incl, o);
+          if (lane >= o) incl = max(incl, y);
+        }
+        int excl = __shfl_up_sync(0xffffffffu, incl, 1);
+        excl = max(carry, lane ? excl : 0);
+        if (e < e1 && st < nblk && st > excl) p.segstart[row + st] = st;
+        carry = max(carry, __shfl_sync(0xffffffffu, incl, 31));
       }
-      int excl = __shfl_up_sync(0xffffffffu, incl, 1);
-      excl = max(carry, lane ? excl : 0);
-      if (e < e1 && st < nblk && st > excl) p.segstart[row + st] = st;
-      carry = max(carry, __shfl_sync(0xffffffffu, incl, 31));
     }
-    __syncwarp();
+    __syncthreads();
   }
-  // the segment start of every block is the running maximum of the marks;
-  // the fingerprints and marks of the next two chunks are loaded ahead of use
-  // (the chunk written back is always behind the ones read ahead)
+  // this warp's range [b0, b1)
+  const int per = ((p.max_blocks + nw - 1) / nw + 31) / 32 * 32;
+  const int b0 = warp * per, b1 = min(p.max_blocks, b0 + per);
+
+  // ---- pass 1 (several warps only): each range's largest mark and composed map
   int scarry = 0;
   uint64_t carryA = 1, carryC = 0;
-  uint64_t fp_n1 = lane < p.max_blocks ? p.fp_out[row + lane] : 0;
-  uint64_t fp_n2 = lane + 32 < p.max_blocks ? p.fp_out[row + lane + 32] : 0;
-  int st_n1 = (segs && lane < nblk) ? p.segstart[row + lane] : 0;
-  int st_n2 = (segs && lane + 32 < nblk) ? p.segstart[row + lane + 32] : 0;
-  for (int base = 0; base < p.max_blocks; base += 32) {
+  if (nw > 1) {
+    uint64_t aggA = 1, aggC = 0;
+    int aggM = 0;
+    for (int base = b0; base < b1; base += 32) {
+      const int b = base + lane;
+      const bool in = b < b1;
+      const uint64_t fp = in ? p.fp_out[row + b] : 0;
+      const int mk = (segs && in && b < nblk) ? p.segstart[row + b] : 0;
+      // a block starts a segment iff it is block 0 or carries its own mark
+      const bool start = b == 0 || mk == b;
+      uint64_t A = !in ? 1ull : (b < nblk && !start) ? kChainMul : (b < nblk ? 0ull : 1ull);
+      uint64_t Cc = !in ? 0ull : (b < nblk) ? (start ? fp + kChainMul : fp) : 0ull;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const uint64_t A2 = __shfl_up_sync(0xffffffffu, A, o);
+        const uint64_t C2 = __shfl_up_sync(0xffffffffu, Cc, o);
+        if (lane >= o) {
+          Cc = A * C2 + Cc;
+          A = A * A2;
+        }
+      }
+      const uint64_t cA = __shfl_sync(0xffffffffu, A, 31), cC = __shfl_sync(0xffffffffu, Cc, 31);
+      aggC = cA * aggC + cC;
+      aggA = cA * aggA;
+      int m = mk;
+#pragma unroll
+      for (int o = 16; o; o >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, o));
+      aggM = max(aggM, m);
+    }
+    if (lane == 0) {
+      s_aggA[warp] = aggA;
+      s_aggC[warp] = aggC;
+      s_aggM[warp] = aggM;
+    }
+    __syncthreads();
+    // the composition of the ranges before this one, in order
+    for (int w = 0; w < warp; ++w) {
+      carryC = s_aggA[w] * carryC + s_aggC[w];
+      carryA = s_aggA[w] * carryA;
+      scarry = max(scarry, s_aggM[w]);
+    }
+  }
+
+  // ---- pass 2: the segment start of every block is the running maximum of
+  // the marks; the fingerprints and marks of the next two chunks of this
+  // range are loaded ahead of use (the chunk written back is always behind
+  // the ones read ahead, and no range reads another's marks)
+  const int nb1 = min(nblk, b1);
+  uint64_t fp_n1 = b0 + lane < b1 ? p.fp_out[row + b0 + lane] : 0;
+  uint64_t fp_n2 = b0 + lane + 32 < b1 ? p.fp_out[row + b0 + lane + 32] : 0;
+  int st_n1 = (segs && b0 + lane < nb1) ? p.segstart[row + b0 + lane] : 0;
+  int st_n2 = (segs && b0 + lane + 32 < nb1) ? p.segstart[row + b0 + lane + 32] : 0;
+  for (int base = b0; base < b1; base += 32) {
     const int b = base + lane;
     const uint64_t fp = fp_n1;
     fp_n1 = fp_n2;
-    fp_n2 = b + 64 < p.max_blocks ? p.fp_out[row + b + 64] : 0;
+    fp_n2 = b + 64 < b1 ? p.fp_out[row + b + 64] : 0;
     int st = (b < nblk) ? st_n1 : 0;
     st_n1 = st_n2;
-    st_n2 = (segs && b + 64 < nblk) ? p.segstart[row + b + 64] : 0;
+    st_n2 = (segs && b + 64 < nb1) ? p.segstart[row + b + 64] : 0;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
       const int y = __shfl_up_sync(0xffffffffu, st, o);
@@ -184,7 +245,7 @@ __global__ void dedup_prep(DedupParams p) {
     st = max(st, scarry);
     scarry = __shfl_sync(0xffffffffu, st, 31);
     if (b >= nblk) st = 0;
-    if (b < p.max_blocks) p.segstart[row + b] = st;
+    if (b < b1) p.segstart[row + b] = st;
     const bool shareable = b < full && tier != kPrivateTier;
     // segmented scan of x -> A x + C
     uint64_t A = (b < nblk && b != st) ? kChainMul : (b < nblk ? 0ull : 1ull);
@@ -202,7 +263,7 @@ __global__ void dedup_prep(DedupParams p) {
     const uint64_t gA = A * carryA;
     carryA = __shfl_sync(0xffffffffu, gA, 31);
     carryC = __shfl_sync(0xffffffffu, gC, 31);
-    if (b < p.max_blocks) {
+    if (b < b1) {
       uint64_t k = 0;
       if (shareable) {
         k = splitmix_mix(gC ^ ((uint64_t)(b - st) * 0xD6E8FEB86659FD93ull) ^ ((uint64_t)tier << 32));
@@ -541,7 +602,9 @@ extern "C" kvs_status kvs_fingerprint_dedup(kvs_pool* pool, const uint32_t* toke
   const int tb = 256;
   const dim3 gs((n + tb - 1) / tb);
   cudaError_t e = launch_pdl(dedup_hash, gs, dim3(tb), stream, p);
-  if (e == cudaSuccess) e = launch_pdl(dedup_prep, dim3((n_seq * 32 + tb - 1) / tb), dim3(tb), stream, p);
+  // dedup_prep: one CTA per sequence, about kPrepRange blocks per warp
+  const int prep_warps = std::max(1, std::min(kPrepMaxWarps, (max_blocks + kPrepRange - 1) / kPrepRange));
+  if (e == cudaSuccess) e = launch_pdl(dedup_prep, dim3(n_seq), dim3(32 * prep_warps), stream, p);
   if (e == cudaSuccess) e = launch_pdl(dedup_insert, gs, dim3(tb), stream, p);
   if (e == cudaSuccess) e = launch_pdl(dedup_resolve, gs, dim3(tb), stream, p);
   if (e == cudaSuccess) e = launch_pdl(dedup_fallback, gs, dim3(tb), stream, p);
